@@ -1,0 +1,90 @@
+"""Engine-level pins of the CPU oracle (paper: "Polestar: Drift-Aware Cache
+Calibration and Token Commitment for Efficient Inference of Diffusion LLMs")."""
+import numpy as np
+import pytest
+
+from drift_aware_kv_gb300 import synth
+from oracle import polestar_oracle as O
+
+
+def _run(cfg, exact_cache=False, steps=None):
+    W = O.weights_to_numpy(synth.make_weights(cfg))
+    orc = O.PolestarOracle(cfg, W, exact_cache=exact_cache)
+    tr = synth.Trajectory(cfg)
+    out = []
+    while True:
+        st = tr.next_step()
+        if st is None or (steps is not None and len(out) >= steps):
+            break
+        x0 = st["x0"].to(synth.torch_dtype(cfg)).double().numpy()
+        rec = orc.calibrate_step(x0, st["n_unmasked"], st["block_index"], st["block_entry"])
+        com = orc.commit(st["logits"].numpy(), st["masked"].numpy())
+        out.append((st, rec, com))
+    return orc, out
+
+
+def test_sparse_refresh_with_all_clusters_equals_block_entry_forward():
+    """Closed-form special case of §4.1: when the refresh fires, every cluster is
+    selected (k = K) and the cached hidden states are exact, the sparse layer-wise
+    update of the window equals a forward of window + active block over the cached
+    context, i.e. the block-entry forward at an odd block (Algorithm 1 line 5)."""
+    cfg = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(n_layers=3, topk=8, tau_upd=0)
+    W = O.weights_to_numpy(synth.make_weights(cfg))
+    tr = synth.Trajectory(cfg)
+    s0 = tr.next_step()
+    # move to block 1 (odd) directly: fresh state for both engines
+    x0 = s0["x0"].double().numpy()
+    a = O.PolestarOracle(cfg, W, exact_cache=True)
+    b = O.PolestarOracle(cfg, W, exact_cache=True)
+    a.calibrate_step(x0, [0], 0, True)  # full forward fills every position
+    a.calibrate_step(x0, [0], 1, True)
+    b.calibrate_step(x0, [0], 0, True)
+    x1 = x0.copy()
+    g = np.random.default_rng(0)
+    win = a.window(1)
+    x1[0, win] += 0.3 * g.standard_normal((len(win), cfg.d_model))
+    x1[0, 96:100] = g.standard_normal((4, cfg.d_model))
+    rec = a.calibrate_step(x1, [5], 1, False)[0]
+    assert rec["fire"] and all(len(t) == 8 for t in rec["topk"])
+    b.calibrate_step(x1, [0], 1, True)
+    pos = sorted(set(win) | set(range(96, 128)))
+    for l in range(cfg.n_layers):
+        assert np.allclose(a.seqs[0].kv[l][pos], b.seqs[0].kv[l][pos], rtol=1e-10, atol=1e-12)
+        assert np.allclose(a.exact_H[0][l], b.exact_H[0][l], rtol=1e-10, atol=1e-12)
+
+
+def test_tiny_trajectory_invariants():
+    """Whole-trajectory sanity on the fp32 single-layer workload: drift is
+    non-negative, selected rows are exactly the members of the top-k clusters,
+    committed rows were masked, and tau_d = alpha (tau_s - c)^2."""
+    cfg = synth.WORKLOADS["tiny_l1_d256_fp32"]
+    orc, out = _run(cfg)
+    assert len(out) == 16
+    fired = 0
+    for st, recs, coms in out:
+        for si in range(cfg.batch):
+            rec, com = recs[si], coms[si]
+            if not st["block_entry"]:
+                assert np.all(rec["delta"] >= -1e-15)
+                if rec["fire"]:
+                    fired += 1
+                    for D, ids, sel in zip(rec["D"], rec["topk"], rec["sel"]):
+                        assert np.all(D >= -1e-15)
+                        assert len(set(ids)) == cfg.topk
+                assert np.allclose(com["tau_d"][:32], 10 * (0.9 - com["conf"][:32]) ** 2)
+            start = cfg.prompt_len + st["block_index"] * cfg.block
+            m = st["masked"][si].numpy()
+            for j in np.nonzero(com["commit"])[0]:
+                assert m[start + j]
+    assert fired >= 2
+
+
+@pytest.mark.parametrize("name", ["mini_l2_d512_bf16", "mini_gqa_l2_d448_bf16"])
+def test_mini_bf16_runs(name):
+    cfg = synth.WORKLOADS[name].replace(n_steps=6)
+    orc, out = _run(cfg)
+    assert len(out) == 6
+    for st, recs, coms in out:
+        for rec in recs:
+            if "act_out" in rec:
+                assert np.all(np.isfinite(rec["act_out"]))
