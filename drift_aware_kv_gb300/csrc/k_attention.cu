@@ -1,0 +1,188 @@
+// Row attention over the whole cached sequence, with the KL drift epilogue.
+//
+// Every query row (active block, window rows, centroid proxies) attends
+// bidirectionally to all N cached keys of its sequence (Eq. 3; proxies use
+// "cached KV and recomputed KV tensors for the active block", §4.1).  For
+// tracked rows the kernel also measures the drift of Eq. 4,
+// KL(softmax(s) || softmax(s')), against the scores s' the same row produced at
+// the previous measurement, and replaces s' by the new scores:
+//   - proxy rows at every layer (per-cluster drift D, §4.1 "Measuring Drift");
+//   - active rows at the last layer (token drift delta_j, §4.2 / Algorithm 1
+//     line 28).
+//
+// KL is evaluated in the cancellation-free form
+//   KL = sum_j p_j d_j - log1p( sum_j q~_j expm1(d_j) / sum_j q~_j ),
+// d_j = s_j - s'_j, q~_j = exp(s'_j - lse'), which equals sum_j p_j log(p_j/q_j)
+// exactly (lse - lse' = log sum_j q_j e^{d_j}) but keeps fp32 accuracy when the
+// two distributions are close.
+//
+// Work split: one CTA = 8 query rows (one per warp) x one query head; K/V tiles
+// of 64 keys are staged in shared memory as fp32 (odd row pitch: conflict-free
+// for both the per-key dot products and the per-dimension P.V sums).
+#include "kernels.h"
+
+namespace polestar {
+
+constexpr int ATT_ROWS = 8;   // rows per CTA (one warp each)
+constexpr int ATT_TK = 64;    // keys per tile
+
+template <typename T, int DH>
+__global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
+  extern __shared__ float smem[];
+  constexpr int PITCH = DH + 1;
+  float* Ks = smem;                       // [TK][PITCH]
+  float* Vs = Ks + ATT_TK * PITCH;        // [TK][PITCH]
+  float* Qs = Vs + ATT_TK * PITCH;        // [ROWS][DH]
+  float* Ps = Qs + ATT_ROWS * DH;         // [ROWS][TK]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int r0 = blockIdx.x * ATT_ROWS;
+  const int r = r0 + warp;
+  const int grp = p.H / p.Hkv;
+  const int kvh = h / grp;
+
+  // the CTA's sequence: rows of one CTA never mix sequences (host layout rule)
+  const int4 m0 = p.rows[r0];
+  const int seq = m0.x;
+  const T* kvbase = (const T*)p.kv_layer + (size_t)seq * p.kv_seq_stride;
+
+  int4 m = make_int4(0, 0, ROW_NONE, 0);
+  if (r < p.R) m = p.rows[r];
+  const bool live = (m.z != ROW_NONE) && (m.z != ROW_OTHER || p.other_live);
+  const bool need_out = live && m.z != ROW_PROXY;
+
+  // tracking: where the previous scores of this (row, head) live
+  float* prev = nullptr;
+  float* prev_lse = nullptr;
+  if (live && m.z == ROW_PROXY && p.proxy_prev) {
+    const size_t idx = ((size_t)seq * p.K + m.w) * p.H + h;
+    prev = p.proxy_prev + idx * p.N;
+    prev_lse = p.proxy_prev_lse + idx;
+  } else if (live && m.z == ROW_ACTIVE && p.active_prev) {
+    const size_t idx = ((size_t)seq * p.B + m.w) * p.H + h;
+    prev = p.active_prev + idx * p.N;
+    prev_lse = p.active_prev_lse + idx;
+  }
+  const bool do_kl = prev && p.measure;
+  const float shift_prev = do_kl ? *prev_lse : 0.f;
+
+  // stage this warp's query (fp32)
+  if (live) {
+    const T* q = (const T*)p.q + (size_t)r * p.ldq + h * DH;
+    for (int i = lane; i < DH; i += 32) Qs[warp * DH + i] = to_f<T>(q[i]);
+  }
+
+  constexpr int NV = DH / 32;
+  float acc[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+  float mrun = -INFINITY, l_part = 0.f, a_part = 0.f, sq_part = 0.f, e_part = 0.f;
+
+  for (int j0 = 0; j0 < p.N; j0 += ATT_TK) {
+    __syncthreads();
+    // cooperative K/V tile load -> fp32 shared memory
+    for (int idx = threadIdx.x; idx < ATT_TK * DH; idx += blockDim.x) {
+      const int kk = idx / DH, dd = idx % DH;
+      const int j = j0 + kk;
+      float kv = 0.f, vv = 0.f;
+      if (j < p.N) {
+        const T* rowp = kvbase + (size_t)j * 2 * p.kvdim + kvh * DH + dd;
+        kv = to_f<T>(rowp[0]);
+        vv = to_f<T>(rowp[p.kvdim]);
+      }
+      Ks[kk * PITCH + dd] = kv;
+      Vs[kk * PITCH + dd] = vv;
+    }
+    __syncthreads();
+    if (!live) continue;
+    // scores of keys j0+lane and j0+lane+32
+    float s[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int kk = lane + 32 * t;
+      const float* kr = Ks + kk * PITCH;
+      const float* qr = Qs + warp * DH;
+      float dot = 0.f;
+#pragma unroll 16
+      for (int i = 0; i < DH; ++i) dot = fmaf(qr[i], kr[i], dot);
+      s[t] = (j0 + kk < p.N) ? dot * p.scale : -INFINITY;
+    }
+    const float tmax = warp_max(fmaxf(s[0], s[1]));
+    const float mnew = fmaxf(mrun, tmax);
+    const float corr = expf(mrun - mnew);  // 0 on the first tile (mrun = -inf)
+    l_part *= corr;
+    a_part *= corr;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) acc[i] *= corr;
+    mrun = mnew;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int kk = lane + 32 * t;
+      const int j = j0 + kk;
+      const float pj = (j < p.N) ? expf(s[t] - mnew) : 0.f;
+      Ps[warp * ATT_TK + kk] = pj;
+      l_part += pj;
+      if (prev && j < p.N) {
+        if (do_kl) {
+          const float sp = prev[j];
+          const float dj = s[t] - sp;
+          const float qt = expf(sp - shift_prev);
+          a_part += pj * dj;
+          sq_part += qt;
+          e_part += qt * expm1f(dj);
+        }
+        if (p.store) prev[j] = s[t];
+      }
+    }
+    __syncwarp();
+    if (need_out) {
+      for (int kk = 0; kk < ATT_TK; ++kk) {
+        const float pk = Ps[warp * ATT_TK + kk];
+        const float* vr = Vs + kk * PITCH;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc[i] = fmaf(pk, vr[lane + 32 * i], acc[i]);
+      }
+    }
+    __syncwarp();
+  }
+  if (!live) return;
+  const float l_tot = warp_sum(l_part);
+  if (need_out) {
+    T* o = (T*)p.out + (size_t)r * p.ldo + h * DH;
+    const float inv = 1.f / l_tot;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) o[lane + 32 * i] = from_f<T>(acc[i] * inv);
+  }
+  if (prev) {
+    const float a_tot = warp_sum(a_part);
+    const float sq_tot = warp_sum(sq_part);
+    const float e_tot = warp_sum(e_part);
+    if (lane == 0) {
+      if (do_kl) p.kl_out[(size_t)r * p.H + h] = a_tot / l_tot - log1pf(e_tot / sq_tot);
+      if (p.store) *prev_lse = mrun + logf(l_tot);
+    }
+  }
+}
+
+template <typename T>
+void launch_row_attention(const AttnArgs& a, cudaStream_t st) {
+  const dim3 grid((a.R + ATT_ROWS - 1) / ATT_ROWS, a.H);
+  if (a.dh == 128) {
+    const size_t sm = (2 * ATT_TK * 129 + ATT_ROWS * 128 + ATT_ROWS * ATT_TK) * sizeof(float);
+    static bool cfg = false;
+    if (!cfg) {
+      cudaFuncSetAttribute(row_attention_kernel<T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      cfg = true;
+    }
+    row_attention_kernel<T, 128><<<grid, 256, sm, st>>>(a);
+  } else {
+    const size_t sm = (2 * ATT_TK * 65 + ATT_ROWS * 64 + ATT_ROWS * ATT_TK) * sizeof(float);
+    row_attention_kernel<T, 64><<<grid, 256, sm, st>>>(a);
+  }
+}
+
+template void launch_row_attention<float>(const AttnArgs&, cudaStream_t);
+template void launch_row_attention<__nv_bfloat16>(const AttnArgs&, cudaStream_t);
+
+}  // namespace polestar

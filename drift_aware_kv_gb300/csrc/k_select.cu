@@ -1,0 +1,109 @@
+// Drift aggregation, top-k cluster selection and gathered-row compaction
+// (Polestar-Cache, §4.1 "Measuring Drift and Layer-wise KV Updates";
+// Algorithm 1 lines 20-22).
+//
+// One CTA serves the whole batch (at most a few thousand window rows): per
+// refreshing sequence it averages the per-head proxy KL into D_c, picks the k
+// largest (ties to the lower cluster id), marks the member rows S, and writes
+// the compact row list [active rows of every sequence, then S of each
+// refreshing sequence in window order] with its length on the device, so the
+// following projections run on exactly those rows without a host round trip.
+#include "kernels.h"
+
+namespace polestar {
+
+__global__ void select_kernel(SelectArgs a) {
+  __shared__ int s_topk[32][16];
+  __shared__ int s_count[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  // 1. per sequence: D_c, top-k (thread s)
+  for (int s = tid; s < a.batch; s += blockDim.x) {
+    const int pr = a.proxy_row[s];
+    float* D = a.drift + (size_t)s * a.K;
+    int* tk = a.topk_out + (size_t)s * a.topk;
+    if (pr < 0) {
+      for (int c = 0; c < a.K; ++c) D[c] = 0.f;
+      for (int i = 0; i < a.topk; ++i) tk[i] = -1;
+      continue;
+    }
+    float Dv[16];
+    for (int c = 0; c < a.K; ++c) {
+      float sum = 0.f;
+      for (int h = 0; h < a.H; ++h) sum += a.kl_rows[(size_t)(pr + c) * a.H + h];
+      Dv[c] = sum / (float)a.H;
+      D[c] = Dv[c];
+    }
+    unsigned taken = 0;
+    for (int i = 0; i < a.topk; ++i) {
+      int best = -1;
+      for (int c = 0; c < a.K; ++c) {
+        if (taken & (1u << c)) continue;
+        if (best < 0 || Dv[c] > Dv[best]) best = c;
+      }
+      taken |= 1u << best;
+      tk[i] = best;
+      if (s < 32) s_topk[s][i] = best;
+    }
+    if (s < 32) s_topk[s][15] = (int)taken;
+  }
+  __syncthreads();
+  // 2. selection masks and per-sequence counts (warp per sequence)
+  for (int s = warp; s < a.batch; s += nwarps) {
+    const bool fire = a.proxy_row[s] >= 0;
+    const unsigned taken = fire ? (unsigned)s_topk[s][15] : 0u;
+    int count = 0;
+    for (int j0 = 0; j0 < a.Wmax; j0 += 32) {
+      const int j = j0 + lane;
+      bool sel = false;
+      if (fire && j < a.nw) sel = (taken >> a.labels[(size_t)s * a.Wmax + j]) & 1u;
+      if (j < a.Wmax) {
+        a.selected[(size_t)s * a.Wmax + j] = sel;
+        a.sel_cur[(size_t)s * a.Wmax + j] = sel;
+      }
+      count += __popc(__ballot_sync(0xffffffffu, sel));
+    }
+    if (lane == 0) s_count[s] = count;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = a.n_active;
+    for (int s = 0; s < a.batch; ++s) {
+      const int c = s_count[s];
+      s_count[s] = acc;
+      acc += c;
+    }
+    *a.m_o = acc;
+  }
+  __syncthreads();
+  for (int i = tid; i < a.n_active; i += blockDim.x) a.o_src[i] = i;
+  // 3. compact row list
+  for (int s = warp; s < a.batch; s += nwarps) {
+    if (a.proxy_row[s] < 0) continue;
+    int base = s_count[s];
+    for (int j0 = 0; j0 < a.nw; j0 += 32) {
+      const int j = j0 + lane;
+      const bool sel = (j < a.nw) && a.sel_cur[(size_t)s * a.Wmax + j];
+      const unsigned bal = __ballot_sync(0xffffffffu, sel);
+      if (sel) a.o_src[base + __popc(bal & ((1u << lane) - 1u))] = a.win_row[s] + j;
+      base += __popc(bal);
+    }
+  }
+}
+
+void launch_select(const SelectArgs& a, cudaStream_t st) { select_kernel<<<1, 1024, 0, st>>>(a); }
+
+// delta_j = mean over heads of the last-layer active-row KL (Algorithm 1 line 28)
+__global__ void delta_kernel(const float* __restrict__ kl_rows, int batch, int B, int H,
+                             float* __restrict__ delta) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= batch * B) return;
+  float sum = 0.f;
+  for (int h = 0; h < H; ++h) sum += kl_rows[(size_t)i * H + h];
+  delta[i] = sum / (float)H;
+}
+
+void launch_delta_finalize(const float* kl_rows, int batch, int B, int H, float* delta, cudaStream_t st) {
+  delta_kernel<<<(batch * B + 127) / 128, 128, 0, st>>>(kl_rows, batch, B, H, delta);
+}
+
+}  // namespace polestar

@@ -1,0 +1,147 @@
+// Internal launch interface of the Polestar kernels (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace polestar {
+
+// ---- row kernels (k_rows.cu) ----
+template <typename T>
+void launch_gather_input(const void* x0, const int4* rows, int R, int N, int d, float* h, cudaStream_t st);
+template <typename T>
+void launch_gather_window(const void* x0, const int* win_pos, int nw, const int* fire_seqs, int n_fire, int N,
+                          int d, int Wmax, float* U, uint8_t* sel, cudaStream_t st);
+template <typename T>
+void launch_rmsnorm(const float* h, const int* src, const int* m_dev, const int4* rows, const float* z, int K,
+                    const void* gain, int R, int d, float eps, void* a, cudaStream_t st);
+template <typename T>
+void launch_rope_scatter(const float* qkv, int ldq, const int4* rows, const uint8_t* write_kv, int R, int H,
+                         int Hkv, int dh, const float2* tab, void* qout, void* kv_layer, size_t kv_seq_stride,
+                         int kvdim, cudaStream_t st);
+template <typename T>
+void launch_residual_rmsnorm(const float* h, const int* src, const int* m_dev, int R, const float* y, int ldy,
+                             const void* gain, int d, float eps, float* h1, void* a, cudaStream_t st);
+template <typename T>
+void launch_swiglu(const float* gu, int ldg, const int* m_dev, int R, int F, void* act, cudaStream_t st);
+void launch_residual_scatter(const float* h1, const float* y, int ldy, const int* src, const int* m_dev, int R,
+                             const int4* rows, int d, int Wmax, float* h, float* U, cudaStream_t st);
+template <typename T>
+void launch_gather_T(const void* src, const int* idx, const int* m_dev, int R, int w, void* dst,
+                     cudaStream_t st);
+void launch_capture_window(const float* h, const int4* rows, int R, int d, int Wmax, float* Hw_layer,
+                           size_t seq_stride, cudaStream_t st);
+
+// ---- attention + KL (k_attention.cu) ----
+struct AttnArgs {
+  const void* q;           // [R, ldq] storage type, rotary applied
+  int ldq;
+  const int4* rows;        // [R] {seq, pos, kind, aux}
+  int R;
+  const void* kv_layer;    // layer base of the K/V cache; seq stride below
+  size_t kv_seq_stride;    // elements between sequences
+  int kvdim;               // Hkv * dh
+  int N, H, Hkv, dh, K, B;
+  float scale;             // 1/sqrt(dh)
+  void* out;               // [R, ldo] storage type (not written for proxy rows)
+  int ldo;
+  int other_live;
+  // drift tracking (nullptr = off)
+  float* proxy_prev;       // [batch, K, H, N] scores of this layer's proxies
+  float* proxy_prev_lse;   // [batch, K, H]
+  float* active_prev;      // [batch, B, H, N] scores of the active rows (last layer)
+  float* active_prev_lse;  // [batch, B, H]
+  int measure;             // 1: write KL(new || prev) to kl_out[r, h]
+  int store;               // 1: replace prev by the new scores
+  float* kl_out;           // [R, H]
+};
+template <typename T>
+void launch_row_attention(const AttnArgs& a, cudaStream_t st);
+
+// ---- K-means + NVFP4 (k_cluster.cu) ----
+struct KmeansArgs {
+  const float* Hw;         // [L, batch, Wmax, d] block-entry layer inputs of window rows
+  int L, batch, Wmax, nw, d, K, iters;
+  uint64_t seed;
+  int block;
+  uint8_t* labels;         // [L, batch, Wmax]
+  float* z;                // [L, batch, K, d]
+  float* csum;             // [L, batch, K, d]
+  float* anchor;           // [L, batch, K, d]
+  uint8_t* codes;          // [L, batch, Wmax, d/2]
+  uint8_t* scales;         // [L, batch, Wmax, d/16]
+};
+void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st);
+
+// Within-block patch of layer l's window cache (Algorithm 1 lines 16-17):
+// decode every window row of each firing sequence, replace the rows of the
+// previous layer's selection by their update packet, re-encode those rows,
+// and write the patched hidden states into the step's row space.
+struct PatchArgs {
+  const int* fire_seqs;    // [n_fire]
+  int n_fire, nw, Wmax, d, K;
+  const uint8_t* labels;   // layer base [batch, Wmax]
+  const float* anchor;     // layer base [batch, K, d]
+  uint8_t* codes;          // layer base [batch, Wmax, d/2]
+  uint8_t* scales;         // layer base [batch, Wmax, d/16]
+  const float* U;          // [batch, Wmax, d]
+  const uint8_t* sel_prev; // [batch, Wmax]
+  const int* win_row;      // [batch] first row of the sequence's window rows in the step row space (-1: none)
+  float* h_rows;           // [R, d]
+  uint8_t* write_kv;       // [R]
+  float* dn;               // [batch, Wmax, d]: normalise(new) - normalise(old) for patched rows
+  float* csum;             // layer base [batch, K, d]
+  float* z;                // layer base [batch, K, d]
+};
+void launch_window_patch(const PatchArgs& a, cudaStream_t st);
+void launch_centroid_update(const PatchArgs& a, cudaStream_t st);
+
+// ---- selection (k_select.cu) ----
+struct SelectArgs {
+  int batch, Wmax, nw, K, topk, H, B;
+  const float* kl_rows;    // [R, H]
+  const int* proxy_row;    // [batch] first proxy row of the sequence (-1: not refreshing)
+  const int* win_row;      // [batch] first window row (-1)
+  const uint8_t* labels;   // layer base [batch, Wmax]
+  float* drift;            // layer base [batch, K]
+  int* topk_out;           // layer base [batch, topk]
+  uint8_t* selected;       // layer base [batch, Wmax]
+  uint8_t* sel_cur;        // [batch, Wmax]
+  int* o_src;              // [R] compact row list (active rows then selected window rows)
+  int* m_o;                // [1]
+  int n_active;            // batch * B
+};
+void launch_select(const SelectArgs& a, cudaStream_t st);
+void launch_delta_finalize(const float* kl_rows, int batch, int B, int H, float* delta, cudaStream_t st);
+
+// ---- commit (k_commit.cu) ----
+struct CommitArgs {
+  const float* logits;     // [batch, 2B, V]
+  int V, batch, B, N, start, hist, Wmax, nw, block_entry;
+  float tau_s, tau_suf, alpha;
+  const uint8_t* masked;   // [batch, N]
+  const float* delta;      // [batch, B]
+  float* theta;            // [batch, B, hist]
+  int* theta_n;            // [batch, B]
+  const uint8_t* fire;     // device [batch]
+  const uint8_t* sel_last; // [batch, Wmax] last-layer selection
+  const int* win_pos;      // [nw]
+  float* part;             // [batch*2B, splits, 2]
+  int splits;
+  uint8_t* commit;         // [batch, 2B]
+  float* conf;             // [batch, 2B]
+  float* conf_user;        // optional copy
+  float* drel;             // [batch, 2B]
+  float* taud;             // [batch, 2B]
+};
+void launch_commit(const CommitArgs& a, cudaStream_t st);
+
+// ---- GEMM: C[M, N] (fp32, ldc) = A[M, K] (T, lda) * W[N, K]^T (T, ldw) ----
+// m_dev (nullable): device row count; rows >= min(M, *m_dev) are not computed.
+template <typename T>
+void launch_gemm_simt(const void* A, int lda, const void* W, int ldw, float* C, int ldc, int M, const int* m_dev,
+                      int N, int K, cudaStream_t st);
+
+}  // namespace polestar

@@ -1,0 +1,894 @@
+// Host side of the Polestar C ABI: context, buffers, and the per-step layer loop.
+//
+// One polestar_calibrate_step runs Algorithm 1 of "Polestar: Drift-Aware Cache
+// Calibration and Token Commitment for Efficient Inference of Diffusion LLMs"
+// for every sequence of the batch:
+//   block entry (lines 4-12): forward over E_b (full sequence at even b, window +
+//     block at odd b) writing the K/V cache and capturing the window's layer
+//     inputs; spherical K-means + residual NVFP4 of every layer (one batched
+//     launch); proxy-attention baseline of every layer.
+//   within-block step (lines 15-26, §4.1 "Update Schedule"): the tau_upd trigger
+//     per sequence on the host; then for every layer l, on the device: patch the
+//     window with U(t, l) and re-project its K/V, incremental centroid update,
+//     one QKV projection for active rows + window rows + proxies, attention with
+//     the KL epilogue, top-k selection + row compaction, and the gathered O/FFN
+//     projections producing the next layer's active inputs and U(t, l+1).
+// polestar_commit runs the drift-aware commit gate of §4.2.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/polestar.h"
+#include "gemm_tc.h"
+#include "kernels.h"
+
+using namespace polestar;
+
+namespace {
+thread_local std::string g_init_error;
+
+size_t pad8(size_t x) { return (x + 7) & ~size_t(7); }
+
+struct MetaLayout {
+  size_t rows_off, prow_off, win_row_off, proxy_row_off, fire_seqs_off, win_pos_off, fire_off, total;
+};
+}  // namespace
+
+struct polestar_ctx {
+  polestar_config cfg{};
+  std::vector<polestar_layer_weights> W;
+  cudaStream_t sm = nullptr, ss = nullptr;
+  int N = 0, d = 0, H = 0, Hkv = 0, dh = 0, F = 0, L = 0, b = 0, B = 0, Wmax = 0, K = 0;
+  int qdim = 0, kvdim = 0, ldg = 0, entry_chunk = 1;
+  size_t esz = 4;
+  bool bf16 = false;
+  int Rmax = 0, rows_cap = 0;
+  std::string err;
+  uint64_t launches = 0;
+
+  // persistent state
+  void* kv = nullptr;            // [L, b, N, 2, kvdim]
+  float2* rope = nullptr;        // [N, dh/2]
+  uint8_t* labels = nullptr;     // [L, b, Wmax]
+  float *z = nullptr, *csum = nullptr, *anchor = nullptr;  // [L, b, K, d]
+  uint8_t *codes = nullptr, *scales = nullptr;             // device [L, b, Wmax, d/2], [.., d/16]
+  uint8_t *codes_host = nullptr, *scales_host = nullptr;   // pinned mirror (host_offload)
+  float *pprev = nullptr, *pprev_lse = nullptr;            // [L, b, K, H, N], [L, b, K, H]
+  float *aprev = nullptr, *aprev_lse = nullptr;            // [b, B, H, N], [b, B, H]
+  float* theta = nullptr;        // [b, B, hist]
+  int* theta_n = nullptr;        // [b, B]
+  float* Hw = nullptr;           // [L, b, Wmax, d]
+  // workspaces
+  float *h_rows = nullptr, *h1 = nullptr, *gout = nullptr, *kl_rows = nullptr;
+  void *a_in = nullptr, *q_rows = nullptr, *attn_out = nullptr;
+  uint8_t* write_kv = nullptr;
+  float *U = nullptr, *dn = nullptr;
+  uint8_t *sel_a = nullptr, *sel_b = nullptr, *sel_last = nullptr;
+  int *o_src = nullptr, *m_o = nullptr;
+  // outputs
+  float* drift = nullptr;        // [L, b, K]
+  int* topk_out = nullptr;       // [L, b, topk]
+  uint8_t* selected = nullptr;   // [L, b, Wmax]
+  float* delta = nullptr;        // [b, B]
+  float *conf = nullptr, *drel = nullptr, *taud = nullptr, *cpart = nullptr;
+  uint8_t* commit_dev = nullptr;
+  int csplits = 1;
+  // step metadata (pinned host + device mirror)
+  MetaLayout ml{};
+  uint8_t* meta_h = nullptr;
+  uint8_t* meta_d = nullptr;
+  cudaEvent_t meta_ev = nullptr, side_ev = nullptr, main_ev = nullptr;
+  // host bookkeeping
+  std::vector<int> cum;
+  std::vector<uint8_t> fire;
+  std::vector<int> win_pos;
+  int cur_block = -1, cur_entry = 0, stepped = 0, nw = 0, start = 0, end = 0;
+  // e2e staging
+  void* st_x0 = nullptr;
+  float* st_logits = nullptr;
+  size_t st_logits_cap = 0;
+  uint8_t *st_masked = nullptr, *st_commit = nullptr;
+
+  std::vector<void*> dev_allocs;
+  std::vector<void*> host_allocs;
+
+  TcGemmCache tc;
+};
+
+namespace {
+
+polestar_status fail(polestar_ctx* c, polestar_status st, const std::string& msg) {
+  if (c)
+    c->err = msg;
+  else
+    g_init_error = msg;
+  return st;
+}
+
+#define CUDA_OR_FAIL(ctx, call)                                                                   \
+  do {                                                                                            \
+    cudaError_t e_ = (call);                                                                      \
+    if (e_ != cudaSuccess)                                                                        \
+      return fail(ctx, e_ == cudaErrorMemoryAllocation ? POLESTAR_ERR_OOM : POLESTAR_ERR_CUDA,    \
+                  std::string(#call) + ": " + cudaGetErrorString(e_));                            \
+  } while (0)
+
+#define LAUNCHED(ctx)                                                                             \
+  do {                                                                                            \
+    ++(ctx)->launches;                                                                            \
+    cudaError_t e_ = cudaGetLastError();                                                          \
+    if (e_ != cudaSuccess) return fail(ctx, POLESTAR_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e_)); \
+  } while (0)
+
+template <typename P>
+polestar_status dalloc(polestar_ctx* c, P** p, size_t bytes) {
+  void* q = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, POLESTAR_ERR_OOM, "cudaMalloc(" + std::to_string(bytes) + "): " + cudaGetErrorString(e));
+  }
+  c->dev_allocs.push_back(q);
+  *p = (P*)q;
+  return POLESTAR_OK;
+}
+
+template <typename P>
+polestar_status halloc(polestar_ctx* c, P** p, size_t bytes) {
+  void* q = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaHostAlloc(&q, bytes, cudaHostAllocDefault);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, POLESTAR_ERR_OOM, "cudaHostAlloc(" + std::to_string(bytes) + "): " + cudaGetErrorString(e));
+  }
+  c->host_allocs.push_back(q);
+  *p = (P*)q;
+  return POLESTAR_OK;
+}
+
+#define TRY(x)                             \
+  do {                                     \
+    polestar_status s_ = (x);              \
+    if (s_ != POLESTAR_OK) return s_;      \
+  } while (0)
+
+void free_all(polestar_ctx* c) {
+  if (c->sm) cudaStreamSynchronize(c->sm);
+  if (c->ss && c->ss != c->sm) cudaStreamSynchronize(c->ss);
+  for (void* p : c->dev_allocs) cudaFree(p);
+  for (void* p : c->host_allocs) cudaFreeHost(p);
+  c->dev_allocs.clear();
+  c->host_allocs.clear();
+  if (c->meta_ev) cudaEventDestroy(c->meta_ev);
+  if (c->side_ev) cudaEventDestroy(c->side_ev);
+  if (c->main_ev) cudaEventDestroy(c->main_ev);
+  c->meta_ev = c->side_ev = c->main_ev = nullptr;
+  tc_gemm_cache_clear(&c->tc);
+}
+
+std::string validate(const polestar_config* c) {
+  if (c->n_layers < 1) return "n_layers must be >= 1";
+  if (c->dtype != POLESTAR_FP32 && c->dtype != POLESTAR_BF16) return "dtype must be 0 (fp32) or 1 (bf16)";
+  if (c->head_dim != 64 && c->head_dim != 128) return "head_dim must be 64 or 128";
+  if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+  if (c->d_model < 16 || c->d_model % 16) return "d_model must be a positive multiple of 16";
+  if (c->d_model > 4096) return "d_model above 4096 is not supported by the clustering kernel";
+  if (c->ffn_dim < 1) return "ffn_dim must be >= 1";
+  if (c->batch < 1 || c->batch > 32) return "batch must be in [1, 32]";
+  if (c->block < 8 || c->block % 8) return "block must be a positive multiple of 8";
+  if (c->gen_len < c->block || c->gen_len % c->block) return "gen_len must be a positive multiple of block";
+  if (c->prompt_len < 0) return "prompt_len must be >= 0";
+  if (c->prefix_win < 0 || c->suffix_win < 0 || c->prefix_win + c->suffix_win < 1) return "bad window sizes";
+  if (c->prefix_win + c->suffix_win > 128) return "window above 128 rows is not supported";
+  if (c->K < 1 || c->K > 8) return "K must be in [1, 8]";
+  if (c->topk < 1 || c->topk > c->K) return "topk must be in [1, K]";
+  if (c->tau_upd < 0 || c->hist < 0 || c->hist > 64 || c->kmeans_iters < 1) return "bad schedule parameters";
+  if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return "bad rms_eps / rope_base";
+  return "";
+}
+
+MetaLayout meta_layout(int rows_cap, int b, int K, int Wmax) {
+  MetaLayout m{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o = (o + bytes + 15) & ~size_t(15);
+    return r;
+  };
+  m.rows_off = take(sizeof(int4) * rows_cap);
+  m.prow_off = take(sizeof(int4) * pad8((size_t)b * K));
+  m.win_row_off = take(sizeof(int) * b);
+  m.proxy_row_off = take(sizeof(int) * b);
+  m.fire_seqs_off = take(sizeof(int) * b);
+  m.win_pos_off = take(sizeof(int) * Wmax);
+  m.fire_off = take(b);
+  m.total = o;
+  return m;
+}
+
+template <typename T>
+T* meta_h(polestar_ctx* c, size_t off) { return (T*)(c->meta_h + off); }
+template <typename T>
+T* meta_d(polestar_ctx* c, size_t off) { return (T*)(c->meta_d + off); }
+
+void compute_window(polestar_ctx* c, int blk) {
+  c->start = c->cfg.prompt_len + blk * c->B;
+  c->end = c->start + c->B;
+  c->win_pos.clear();
+  for (int p = c->start - c->cfg.prefix_win; p < c->start; ++p)
+    if (p >= 0) c->win_pos.push_back(p);
+  for (int p = c->end; p < c->end + c->cfg.suffix_win; ++p)
+    if (p < c->N) c->win_pos.push_back(p);
+  c->nw = (int)c->win_pos.size();
+}
+
+// ---- GEMM dispatch: tcgen05 tensor cores for bf16, CUDA cores for fp32 ----
+template <typename T>
+polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int ldw, float* C, int ldc, int M,
+                     const int* m_dev, int N, int K) {
+  if (M <= 0) return POLESTAR_OK;
+  if (sizeof(T) == 2 && tc_gemm_supported(K, lda, ldw)) {
+    cudaError_t e = tc_gemm_bf16(&c->tc, A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm);
+    ++c->launches;
+    if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 gemm: ") + cudaGetErrorString(e));
+    return POLESTAR_OK;
+  }
+  launch_gemm_simt<T>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm);
+  LAUNCHED(c);
+  return POLESTAR_OK;
+}
+
+// ------------------------------------------------------------------ block entry
+template <typename T>
+polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
+  const int L = c->L, b = c->b, N = c->N, d = c->d;
+  const bool full = (blk % 2 == 0);
+  // rows of one sequence (E_b), padded to 8
+  std::vector<int> E;
+  if (full) {
+    for (int p = 0; p < N; ++p) E.push_back(p);
+  } else {
+    std::vector<char> in(N, 0);
+    for (int p : c->win_pos) in[p] = 1;
+    for (int p = c->start; p < c->end; ++p) in[p] = 1;
+    for (int p = 0; p < N; ++p)
+      if (in[p]) E.push_back(p);
+  }
+  const int per_seq = (int)pad8(E.size());
+  const int chunk = std::max(1, std::min(b, c->Rmax / per_seq));
+  // host metadata: rows of all sequences, proxy rows, window positions
+  int4* rows_h = meta_h<int4>(c, c->ml.rows_off);
+  std::vector<int> widx_of(N, -1);
+  for (int i = 0; i < c->nw; ++i) widx_of[c->win_pos[i]] = i;
+  for (int s = 0; s < b; ++s) {
+    for (int i = 0; i < per_seq; ++i) {
+      int4 m = make_int4(s, 0, ROW_NONE, 0);
+      if (i < (int)E.size()) {
+        const int p = E[i];
+        m.y = p;
+        if (p >= c->start && p < c->end) {
+          m.z = ROW_ACTIVE;
+          m.w = p - c->start;
+        } else if (widx_of[p] >= 0) {
+          m.z = ROW_WINDOW;
+          m.w = widx_of[p];
+        } else {
+          m.z = ROW_OTHER;
+        }
+      }
+      rows_h[(size_t)s * per_seq + i] = m;
+    }
+  }
+  int4* prow_h = meta_h<int4>(c, c->ml.prow_off);
+  for (int s = 0; s < b; ++s)
+    for (int k = 0; k < c->K; ++k) prow_h[s * c->K + k] = make_int4(s, 0, ROW_PROXY, k);
+  for (size_t i = (size_t)b * c->K; i < pad8((size_t)b * c->K); ++i) prow_h[i] = make_int4(b - 1, 0, ROW_NONE, 0);
+  int* wp = meta_h<int>(c, c->ml.win_pos_off);
+  for (int i = 0; i < c->nw; ++i) wp[i] = c->win_pos[i];
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
+  CUDA_OR_FAIL(c, cudaEventRecord(c->meta_ev, c->sm));
+
+  const size_t kv_layer = (size_t)b * N * 2 * c->kvdim;
+  const size_t kv_seq = (size_t)N * 2 * c->kvdim;
+  T* kv = (T*)c->kv;
+  const float eps = c->cfg.rms_eps;
+  const int4* rows_all = meta_d<int4>(c, c->ml.rows_off);
+
+  for (int s0 = 0; s0 < b; s0 += chunk) {
+    const int ns = std::min(chunk, b - s0);
+    const int R = ns * per_seq;
+    const int4* rows = rows_all + (size_t)s0 * per_seq;
+    launch_gather_input<T>(x0, rows, R, N, d, c->h_rows, c->sm);
+    LAUNCHED(c);
+    for (int l = 0; l < L; ++l) {
+      const polestar_layer_weights& w = c->W[l];
+      launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
+                            (size_t)c->Wmax * d, c->sm);
+      LAUNCHED(c);
+      launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm);
+      LAUNCHED(c);
+      TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, R, nullptr, c->qdim, d));
+      TRY(gemm<T>(c, c->a_in, d, w.wk, d, c->gout + c->qdim, c->ldg, R, nullptr, c->kvdim, d));
+      TRY(gemm<T>(c, c->a_in, d, w.wv, d, c->gout + c->qdim + c->kvdim, c->ldg, R, nullptr, c->kvdim, d));
+      launch_rope_scatter<T>(c->gout, c->ldg, rows, nullptr, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
+                             kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm);
+      LAUNCHED(c);
+      AttnArgs aa{};
+      aa.q = c->q_rows;
+      aa.ldq = c->qdim;
+      aa.rows = rows;
+      aa.R = R;
+      aa.kv_layer = kv + (size_t)l * kv_layer;
+      aa.kv_seq_stride = kv_seq;
+      aa.kvdim = c->kvdim;
+      aa.N = N;
+      aa.H = c->H;
+      aa.Hkv = c->Hkv;
+      aa.dh = c->dh;
+      aa.K = c->K;
+      aa.B = c->B;
+      aa.scale = 1.f / sqrtf((float)c->dh);
+      aa.out = c->attn_out;
+      aa.ldo = c->qdim;
+      aa.other_live = 1;
+      if (l == L - 1) {
+        aa.active_prev = c->aprev;
+        aa.active_prev_lse = c->aprev_lse;
+        aa.store = 1;
+      }
+      launch_row_attention<T>(aa, c->sm);
+      LAUNCHED(c);
+      TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
+      launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
+                                 c->a_in, c->sm);
+      LAUNCHED(c);
+      TRY(gemm<T>(c, c->a_in, d, w.w_gate, d, c->gout, c->ldg, R, nullptr, c->F, d));
+      TRY(gemm<T>(c, c->a_in, d, w.w_up, d, c->gout + c->F, c->ldg, R, nullptr, c->F, d));
+      launch_swiglu<T>(c->gout, c->ldg, nullptr, R, c->F, c->a_in, c->sm);
+      LAUNCHED(c);
+      TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, R, nullptr, d, c->F));
+      launch_residual_scatter(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows, nullptr,
+                              c->sm);
+      LAUNCHED(c);
+    }
+  }
+  // spherical K-means + residual NVFP4 for every (layer, sequence)
+  KmeansArgs ka{};
+  ka.Hw = c->Hw;
+  ka.L = L;
+  ka.batch = b;
+  ka.Wmax = c->Wmax;
+  ka.nw = c->nw;
+  ka.d = d;
+  ka.K = c->K;
+  ka.iters = c->cfg.kmeans_iters;
+  ka.seed = c->cfg.seed;
+  ka.block = blk;
+  ka.labels = c->labels;
+  ka.z = c->z;
+  ka.csum = c->csum;
+  ka.anchor = c->anchor;
+  ka.codes = c->codes;
+  ka.scales = c->scales;
+  launch_kmeans_encode(ka, c->sm);
+  LAUNCHED(c);
+  // proxy-attention baseline P(t_b, l) of every layer
+  const int Rp = (int)pad8((size_t)b * c->K);
+  const int4* prow = meta_d<int4>(c, c->ml.prow_off);
+  for (int l = 0; l < L; ++l) {
+    const polestar_layer_weights& w = c->W[l];
+    launch_rmsnorm<T>(nullptr, nullptr, nullptr, prow, c->z + (size_t)l * b * c->K * d, c->K, w.attn_norm, Rp, d,
+                      eps, c->a_in, c->sm);
+    LAUNCHED(c);
+    TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, Rp, nullptr, c->qdim, d));
+    launch_rope_scatter<T>(c->gout, c->ldg, prow, nullptr, Rp, c->H, c->Hkv, c->dh, c->rope, c->q_rows, nullptr,
+                           0, c->kvdim, c->sm);
+    LAUNCHED(c);
+    AttnArgs aa{};
+    aa.q = c->q_rows;
+    aa.ldq = c->qdim;
+    aa.rows = prow;
+    aa.R = Rp;
+    aa.kv_layer = kv + (size_t)l * kv_layer;
+    aa.kv_seq_stride = kv_seq;
+    aa.kvdim = c->kvdim;
+    aa.N = N;
+    aa.H = c->H;
+    aa.Hkv = c->Hkv;
+    aa.dh = c->dh;
+    aa.K = c->K;
+    aa.B = c->B;
+    aa.scale = 1.f / sqrtf((float)c->dh);
+    aa.out = c->attn_out;
+    aa.ldo = c->qdim;
+    aa.proxy_prev = c->pprev + (size_t)l * b * c->K * c->H * N;
+    aa.proxy_prev_lse = c->pprev_lse + (size_t)l * b * c->K * c->H;
+    aa.store = 1;
+    launch_row_attention<T>(aa, c->sm);
+    LAUNCHED(c);
+  }
+  std::fill(c->cum.begin(), c->cum.end(), 0);
+  std::fill(c->fire.begin(), c->fire.end(), 0);
+  c->sel_last = nullptr;
+  return POLESTAR_OK;
+}
+
+// ------------------------------------------------------------- within-block step
+template <typename T>
+polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_unmasked) {
+  const int L = c->L, b = c->b, N = c->N, d = c->d, B = c->B;
+  // update schedule (§4.1): refresh when the tokens decoded since the last
+  // refresh exceed tau_upd
+  std::vector<int> fire_seqs;
+  for (int s = 0; s < b; ++s) {
+    c->cum[s] += n_unmasked ? n_unmasked[s] : 0;
+    c->fire[s] = c->cum[s] > c->cfg.tau_upd;
+    if (c->fire[s]) {
+      c->cum[s] = 0;
+      fire_seqs.push_back(s);
+    }
+  }
+  const int n_fire = (int)fire_seqs.size();
+  // row space: active rows of every sequence, then per refreshing sequence its
+  // window rows and its K proxy rows (padded to 8)
+  int4* rows_h = meta_h<int4>(c, c->ml.rows_off);
+  int* win_row = meta_h<int>(c, c->ml.win_row_off);
+  int* proxy_row = meta_h<int>(c, c->ml.proxy_row_off);
+  int* fseq = meta_h<int>(c, c->ml.fire_seqs_off);
+  int* wp = meta_h<int>(c, c->ml.win_pos_off);
+  uint8_t* fire_h = meta_h<uint8_t>(c, c->ml.fire_off);
+  int R = 0;
+  for (int s = 0; s < b; ++s)
+    for (int j = 0; j < B; ++j) rows_h[R++] = make_int4(s, c->start + j, ROW_ACTIVE, j);
+  for (int s = 0; s < b; ++s) {
+    win_row[s] = -1;
+    proxy_row[s] = -1;
+    fire_h[s] = c->fire[s];
+  }
+  for (int f = 0; f < n_fire; ++f) {
+    const int s = fire_seqs[f];
+    fseq[f] = s;
+    win_row[s] = R;
+    for (int j = 0; j < c->nw; ++j) rows_h[R++] = make_int4(s, c->win_pos[j], ROW_WINDOW, j);
+    proxy_row[s] = R;
+    for (int k = 0; k < c->K; ++k) rows_h[R++] = make_int4(s, 0, ROW_PROXY, k);
+    while (R % 8) rows_h[R++] = make_int4(s, 0, ROW_NONE, 0);
+  }
+  for (int i = 0; i < c->nw; ++i) wp[i] = c->win_pos[i];
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
+  CUDA_OR_FAIL(c, cudaEventRecord(c->meta_ev, c->sm));
+  const int4* rows = meta_d<int4>(c, c->ml.rows_off);
+  const int* fire_d = meta_d<int>(c, c->ml.fire_seqs_off);
+  const int* win_row_d = meta_d<int>(c, c->ml.win_row_off);
+  const int* proxy_row_d = meta_d<int>(c, c->ml.proxy_row_off);
+
+  const size_t kv_layer = (size_t)b * N * 2 * c->kvdim;
+  const size_t kv_seq = (size_t)N * 2 * c->kvdim;
+  T* kv = (T*)c->kv;
+  const float eps = c->cfg.rms_eps;
+  const int n_active = b * B;
+
+  launch_gather_input<T>(x0, rows, n_active, N, d, c->h_rows, c->sm);
+  LAUNCHED(c);
+  uint8_t* sel_prev = c->sel_a;
+  uint8_t* sel_cur = c->sel_b;
+  if (n_fire > 0) {
+    launch_gather_window<T>(x0, meta_d<int>(c, c->ml.win_pos_off), c->nw, fire_d, n_fire, N, d, c->Wmax, c->U,
+                            sel_prev, c->sm);
+    LAUNCHED(c);
+  }
+  for (int l = 0; l < L; ++l) {
+    const polestar_layer_weights& w = c->W[l];
+    float* zl = c->z + (size_t)l * b * c->K * d;
+    if (n_fire > 0) {
+      PatchArgs pa{};
+      pa.fire_seqs = fire_d;
+      pa.n_fire = n_fire;
+      pa.nw = c->nw;
+      pa.Wmax = c->Wmax;
+      pa.d = d;
+      pa.K = c->K;
+      pa.labels = c->labels + (size_t)l * b * c->Wmax;
+      pa.anchor = c->anchor + (size_t)l * b * c->K * d;
+      pa.codes = c->codes + (size_t)l * b * c->Wmax * (d / 2);
+      pa.scales = c->scales + (size_t)l * b * c->Wmax * (d / 16);
+      pa.U = c->U;
+      pa.sel_prev = sel_prev;
+      pa.win_row = win_row_d;
+      pa.h_rows = c->h_rows;
+      pa.write_kv = c->write_kv;
+      pa.dn = c->dn;
+      pa.csum = c->csum + (size_t)l * b * c->K * d;
+      pa.z = zl;
+      launch_window_patch(pa, c->sm);
+      LAUNCHED(c);
+      launch_centroid_update(pa, c->sm);
+      LAUNCHED(c);
+    }
+    launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, zl, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm);
+    LAUNCHED(c);
+    TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, R, nullptr, c->qdim, d));
+    TRY(gemm<T>(c, c->a_in, d, w.wk, d, c->gout + c->qdim, c->ldg, R, nullptr, c->kvdim, d));
+    TRY(gemm<T>(c, c->a_in, d, w.wv, d, c->gout + c->qdim + c->kvdim, c->ldg, R, nullptr, c->kvdim, d));
+    launch_rope_scatter<T>(c->gout, c->ldg, rows, c->write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
+                           kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm);
+    LAUNCHED(c);
+    AttnArgs aa{};
+    aa.q = c->q_rows;
+    aa.ldq = c->qdim;
+    aa.rows = rows;
+    aa.R = R;
+    aa.kv_layer = kv + (size_t)l * kv_layer;
+    aa.kv_seq_stride = kv_seq;
+    aa.kvdim = c->kvdim;
+    aa.N = N;
+    aa.H = c->H;
+    aa.Hkv = c->Hkv;
+    aa.dh = c->dh;
+    aa.K = c->K;
+    aa.B = B;
+    aa.scale = 1.f / sqrtf((float)c->dh);
+    aa.out = c->attn_out;
+    aa.ldo = c->qdim;
+    aa.other_live = 1;
+    aa.proxy_prev = c->pprev + (size_t)l * b * c->K * c->H * N;
+    aa.proxy_prev_lse = c->pprev_lse + (size_t)l * b * c->K * c->H;
+    if (l == L - 1) {
+      aa.active_prev = c->aprev;
+      aa.active_prev_lse = c->aprev_lse;
+    }
+    aa.measure = 1;
+    aa.store = 1;
+    aa.kl_out = c->kl_rows;
+    launch_row_attention<T>(aa, c->sm);
+    LAUNCHED(c);
+    SelectArgs sa{};
+    sa.batch = b;
+    sa.Wmax = c->Wmax;
+    sa.nw = c->nw;
+    sa.K = c->K;
+    sa.topk = c->cfg.topk;
+    sa.H = c->H;
+    sa.B = B;
+    sa.kl_rows = c->kl_rows;
+    sa.proxy_row = proxy_row_d;
+    sa.win_row = win_row_d;
+    sa.labels = c->labels + (size_t)l * b * c->Wmax;
+    sa.drift = c->drift + (size_t)l * b * c->K;
+    sa.topk_out = c->topk_out + (size_t)l * b * c->cfg.topk;
+    sa.selected = c->selected + (size_t)l * b * c->Wmax;
+    sa.sel_cur = sel_cur;
+    sa.o_src = c->o_src;
+    sa.m_o = c->m_o;
+    sa.n_active = n_active;
+    launch_select(sa, c->sm);
+    LAUNCHED(c);
+    if (l == L - 1) {
+      launch_delta_finalize(c->kl_rows, b, B, c->H, c->delta, c->sm);
+      LAUNCHED(c);
+    }
+    // gathered O/FFN over active rows + selected window rows
+    const int Rc = n_active + n_fire * c->nw;
+    launch_gather_T<T>(c->attn_out, c->o_src, c->m_o, Rc, c->qdim, c->a_in, c->sm);
+    LAUNCHED(c);
+    TRY(gemm<T>(c, c->a_in, c->qdim, w.wo, c->qdim, c->gout, c->ldg, Rc, c->m_o, d, c->qdim));
+    launch_residual_rmsnorm<T>(c->h_rows, c->o_src, c->m_o, Rc, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
+                               c->a_in, c->sm);
+    LAUNCHED(c);
+    TRY(gemm<T>(c, c->a_in, d, w.w_gate, d, c->gout, c->ldg, Rc, c->m_o, c->F, d));
+    TRY(gemm<T>(c, c->a_in, d, w.w_up, d, c->gout + c->F, c->ldg, Rc, c->m_o, c->F, d));
+    launch_swiglu<T>(c->gout, c->ldg, c->m_o, Rc, c->F, c->a_in, c->sm);
+    LAUNCHED(c);
+    TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, Rc, c->m_o, d, c->F));
+    launch_residual_scatter(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows, c->U,
+                            c->sm);
+    LAUNCHED(c);
+    std::swap(sel_prev, sel_cur);
+  }
+  c->sel_last = sel_prev;  // selection of the last layer
+  return POLESTAR_OK;
+}
+
+template <typename T>
+polestar_status step_impl(polestar_ctx* c, const void* x0, const int32_t* n_unmasked, int blk, int entry) {
+  if (entry) return block_entry<T>(c, x0, blk);
+  return within_step<T>(c, x0, n_unmasked);
+}
+
+}  // namespace
+
+// ============================================================================ ABI
+
+extern "C" polestar_status polestar_init(const polestar_config* cfg, const polestar_layer_weights* layers,
+                                         void* stream_main, void* stream_side, polestar_ctx** out) {
+  if (!out) return fail(nullptr, POLESTAR_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg || !layers) return fail(nullptr, POLESTAR_ERR_INVALID_ARG, "cfg or layers is NULL");
+  const std::string v = validate(cfg);
+  if (!v.empty()) return fail(nullptr, POLESTAR_ERR_INVALID_ARG, v);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const polestar_layer_weights& w = layers[l];
+    if (!w.wq || !w.wk || !w.wv || !w.wo || !w.w_gate || !w.w_up || !w.w_down || !w.attn_norm || !w.ffn_norm)
+      return fail(nullptr, POLESTAR_ERR_INVALID_ARG, "layer " + std::to_string(l) + " has a NULL weight pointer");
+  }
+  polestar_ctx* c = new (std::nothrow) polestar_ctx();
+  if (!c) return fail(nullptr, POLESTAR_ERR_OOM, "context allocation failed");
+  c->cfg = *cfg;
+  c->W.assign(layers, layers + cfg->n_layers);
+  c->sm = (cudaStream_t)stream_main;
+  c->ss = stream_side ? (cudaStream_t)stream_side : c->sm;
+  c->L = cfg->n_layers;
+  c->d = cfg->d_model;
+  c->H = cfg->n_heads;
+  c->Hkv = cfg->n_kv_heads;
+  c->dh = cfg->head_dim;
+  c->F = cfg->ffn_dim;
+  c->b = cfg->batch;
+  c->B = cfg->block;
+  c->N = cfg->prompt_len + cfg->gen_len;
+  c->Wmax = cfg->prefix_win + cfg->suffix_win;
+  c->K = cfg->K;
+  c->qdim = c->H * c->dh;
+  c->kvdim = c->Hkv * c->dh;
+  c->bf16 = cfg->dtype == POLESTAR_BF16;
+  c->esz = c->bf16 ? 2 : 4;
+  c->ldg = std::max(std::max(c->qdim + 2 * c->kvdim, 2 * c->F), c->d);
+  c->ldg = (c->ldg + 3) & ~3;
+  c->cum.assign(c->b, 0);
+  c->fire.assign(c->b, 0);
+
+  auto run = [&]() -> polestar_status {
+    const int L = c->L, b = c->b, N = c->N, d = c->d, Wmax = c->Wmax, K = c->K, H = c->H, B = c->B;
+    const int within_rows = b * B + b * (int)pad8(Wmax + K);
+    const int entry_rows = std::max((int)pad8(N), std::min(b * (int)pad8(N), 16384));
+    c->Rmax = std::max(within_rows, entry_rows);
+    c->rows_cap = std::max(within_rows, b * (int)pad8(N));
+    CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->meta_ev, cudaEventDisableTiming));
+    CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->side_ev, cudaEventDisableTiming));
+    CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->main_ev, cudaEventDisableTiming));
+    TRY(dalloc(c, &c->kv, (size_t)L * b * N * 2 * c->kvdim * c->esz));
+    CUDA_OR_FAIL(c, cudaMemsetAsync(c->kv, 0, (size_t)L * b * N * 2 * c->kvdim * c->esz, c->sm));
+    TRY(dalloc(c, &c->rope, sizeof(float2) * (size_t)N * (c->dh / 2)));
+    {
+      std::vector<float2> tab((size_t)N * (c->dh / 2));
+      for (int p = 0; p < N; ++p)
+        for (int i = 0; i < c->dh / 2; ++i) {
+          const double th = std::pow((double)cfg->rope_base, -2.0 * i / (double)c->dh);
+          tab[(size_t)p * (c->dh / 2) + i] = make_float2((float)std::cos(p * th), (float)std::sin(p * th));
+        }
+      CUDA_OR_FAIL(c, cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    }
+    TRY(dalloc(c, &c->labels, (size_t)L * b * Wmax));
+    CUDA_OR_FAIL(c, cudaMemset(c->labels, 0, (size_t)L * b * Wmax));
+    TRY(dalloc(c, &c->z, sizeof(float) * (size_t)L * b * K * d));
+    TRY(dalloc(c, &c->csum, sizeof(float) * (size_t)L * b * K * d));
+    TRY(dalloc(c, &c->anchor, sizeof(float) * (size_t)L * b * K * d));
+    TRY(dalloc(c, &c->codes, (size_t)L * b * Wmax * (d / 2)));
+    TRY(dalloc(c, &c->scales, (size_t)L * b * Wmax * (d / 16)));
+    TRY(dalloc(c, &c->pprev, sizeof(float) * (size_t)L * b * K * H * N));
+    TRY(dalloc(c, &c->pprev_lse, sizeof(float) * (size_t)L * b * K * H));
+    TRY(dalloc(c, &c->aprev, sizeof(float) * (size_t)b * B * H * N));
+    TRY(dalloc(c, &c->aprev_lse, sizeof(float) * (size_t)b * B * H));
+    TRY(dalloc(c, &c->theta, sizeof(float) * (size_t)b * B * std::max(1, cfg->hist)));
+    TRY(dalloc(c, &c->theta_n, sizeof(int) * (size_t)b * B));
+    CUDA_OR_FAIL(c, cudaMemset(c->theta_n, 0, sizeof(int) * (size_t)b * B));
+    TRY(dalloc(c, &c->Hw, sizeof(float) * (size_t)L * b * Wmax * d));
+    const int R = c->Rmax;
+    TRY(dalloc(c, &c->h_rows, sizeof(float) * (size_t)R * d));
+    TRY(dalloc(c, &c->h1, sizeof(float) * (size_t)R * d));
+    TRY(dalloc(c, &c->gout, sizeof(float) * (size_t)R * c->ldg));
+    TRY(dalloc(c, &c->kl_rows, sizeof(float) * (size_t)R * H));
+    TRY(dalloc(c, &c->a_in, c->esz * (size_t)R * std::max(std::max(d, c->F), c->qdim)));
+    TRY(dalloc(c, &c->q_rows, c->esz * (size_t)R * c->qdim));
+    TRY(dalloc(c, &c->attn_out, c->esz * (size_t)R * c->qdim));
+    TRY(dalloc(c, &c->write_kv, (size_t)R));
+    TRY(dalloc(c, &c->U, sizeof(float) * (size_t)b * Wmax * d));
+    TRY(dalloc(c, &c->dn, sizeof(float) * (size_t)b * Wmax * d));
+    TRY(dalloc(c, &c->sel_a, (size_t)b * Wmax));
+    TRY(dalloc(c, &c->sel_b, (size_t)b * Wmax));
+    CUDA_OR_FAIL(c, cudaMemset(c->sel_a, 0, (size_t)b * Wmax));
+    CUDA_OR_FAIL(c, cudaMemset(c->sel_b, 0, (size_t)b * Wmax));
+    TRY(dalloc(c, &c->o_src, sizeof(int) * (size_t)R));
+    TRY(dalloc(c, &c->m_o, sizeof(int)));
+    TRY(dalloc(c, &c->drift, sizeof(float) * (size_t)L * b * K));
+    TRY(dalloc(c, &c->topk_out, sizeof(int) * (size_t)L * b * cfg->topk));
+    TRY(dalloc(c, &c->selected, (size_t)L * b * Wmax));
+    TRY(dalloc(c, &c->delta, sizeof(float) * (size_t)b * B));
+    CUDA_OR_FAIL(c, cudaMemset(c->drift, 0, sizeof(float) * (size_t)L * b * K));
+    CUDA_OR_FAIL(c, cudaMemset(c->topk_out, 0xFF, sizeof(int) * (size_t)L * b * cfg->topk));
+    CUDA_OR_FAIL(c, cudaMemset(c->selected, 0, (size_t)L * b * Wmax));
+    CUDA_OR_FAIL(c, cudaMemset(c->delta, 0, sizeof(float) * (size_t)b * B));
+    TRY(dalloc(c, &c->conf, sizeof(float) * (size_t)b * 2 * B));
+    TRY(dalloc(c, &c->drel, sizeof(float) * (size_t)b * 2 * B));
+    TRY(dalloc(c, &c->taud, sizeof(float) * (size_t)b * 2 * B));
+    TRY(dalloc(c, &c->commit_dev, (size_t)b * 2 * B));
+    c->csplits = std::max(1, std::min(32, (2 * 152 + b * 2 * B - 1) / (b * 2 * B)));
+    TRY(dalloc(c, &c->cpart, sizeof(float) * 2 * (size_t)b * 2 * B * c->csplits));
+    c->ml = meta_layout(c->rows_cap, b, K, Wmax);
+    TRY(halloc(c, &c->meta_h, c->ml.total));
+    TRY(dalloc(c, &c->meta_d, c->ml.total));
+    if (cfg->host_offload) {
+      TRY(halloc(c, &c->codes_host, (size_t)L * b * Wmax * (d / 2)));
+      TRY(halloc(c, &c->scales_host, (size_t)L * b * Wmax * (d / 16)));
+    }
+    CUDA_OR_FAIL(c, cudaDeviceSynchronize());
+    return POLESTAR_OK;
+  };
+  const polestar_status st = run();
+  if (st != POLESTAR_OK) {
+    g_init_error = c->err;
+    free_all(c);
+    delete c;
+    return st;
+  }
+  *out = c;
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_calibrate_step(polestar_ctx* c, const void* x0, const int32_t* n_unmasked,
+                                                   int32_t block_index, int32_t block_entry,
+                                                   polestar_step_out* out) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!x0) return fail(c, POLESTAR_ERR_INVALID_ARG, "x0 is NULL");
+  const int n_blocks = c->cfg.gen_len / c->B;
+  if (block_index < 0 || block_index >= n_blocks)
+    return fail(c, POLESTAR_ERR_INVALID_ARG, "block_index out of range");
+  if (!block_entry && c->cur_block != block_index)
+    return fail(c, POLESTAR_ERR_STATE, "within-block step without the block's entry step");
+  if (!block_entry && !n_unmasked) return fail(c, POLESTAR_ERR_INVALID_ARG, "n_unmasked is NULL");
+  if (!block_entry)
+    for (int s = 0; s < c->b; ++s)
+      if (n_unmasked[s] < 0) return fail(c, POLESTAR_ERR_INVALID_ARG, "negative n_unmasked");
+  // the host metadata buffer may still be in flight from the previous step
+  CUDA_OR_FAIL(c, cudaEventSynchronize(c->meta_ev));
+  compute_window(c, block_index);
+  polestar_status st = c->bf16 ? step_impl<__nv_bfloat16>(c, x0, n_unmasked, block_index, block_entry)
+                               : step_impl<float>(c, x0, n_unmasked, block_index, block_entry);
+  if (st != POLESTAR_OK) {
+    c->stepped = 0;
+    return st;
+  }
+  c->cur_block = block_index;
+  c->cur_entry = block_entry ? 1 : 0;
+  c->stepped = 1;
+  if (out) {
+    out->drift = c->drift;
+    out->topk = c->topk_out;
+    out->selected = c->selected;
+    out->labels = c->labels;
+    out->delta = c->delta;
+    out->fire = c->fire.data();
+    out->win_len = c->nw;
+    out->win_max = c->Wmax;
+  }
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_commit(polestar_ctx* c, const float* logits, int32_t vocab,
+                                           const uint8_t* masked, uint8_t* commit_mask, float* conf) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!logits || !masked || !commit_mask) return fail(c, POLESTAR_ERR_INVALID_ARG, "NULL buffer");
+  if (vocab < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "vocab must be >= 1");
+  if (!c->stepped) return fail(c, POLESTAR_ERR_STATE, "polestar_commit before polestar_calibrate_step");
+  CommitArgs a{};
+  a.logits = logits;
+  a.V = vocab;
+  a.batch = c->b;
+  a.B = c->B;
+  a.N = c->N;
+  a.start = c->start;
+  a.hist = c->cfg.hist;
+  a.Wmax = c->Wmax;
+  a.nw = c->nw;
+  a.block_entry = c->cur_entry;
+  a.tau_s = c->cfg.tau_s;
+  a.tau_suf = c->cfg.tau_suf;
+  a.alpha = c->cfg.alpha;
+  a.masked = masked;
+  a.delta = c->delta;
+  a.theta = c->theta;
+  a.theta_n = c->theta_n;
+  a.fire = meta_d<uint8_t>(c, c->ml.fire_off);
+  a.sel_last = c->sel_last ? c->sel_last : c->sel_a;
+  a.win_pos = meta_d<int>(c, c->ml.win_pos_off);
+  a.part = c->cpart;
+  a.splits = c->csplits;
+  a.commit = commit_mask;
+  a.conf = c->conf;
+  a.conf_user = conf;
+  a.drel = c->drel;
+  a.taud = c->taud;
+  launch_commit(a, c->sm);
+  c->launches += 2;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("commit launch: ") + cudaGetErrorString(e));
+  c->stepped = 0;
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_step_host(polestar_ctx* c, const void* x0_host, const int32_t* n_unmasked,
+                                              int32_t block_index, int32_t block_entry, const float* logits_host,
+                                              int32_t vocab, const uint8_t* masked_host,
+                                              uint8_t* commit_mask_host) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!x0_host || !logits_host || !masked_host || !commit_mask_host)
+    return fail(c, POLESTAR_ERR_INVALID_ARG, "NULL host buffer");
+  if (vocab < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "vocab must be >= 1");
+  const size_t x0_bytes = (size_t)c->b * c->N * c->d * c->esz;
+  const size_t lg_bytes = (size_t)c->b * 2 * c->B * vocab * sizeof(float);
+  if (!c->st_x0) {
+    TRY(dalloc(c, &c->st_x0, x0_bytes));
+    TRY(dalloc(c, &c->st_masked, (size_t)c->b * c->N));
+    TRY(dalloc(c, &c->st_commit, (size_t)c->b * 2 * c->B));
+  }
+  if (lg_bytes > c->st_logits_cap) {
+    TRY(dalloc(c, &c->st_logits, lg_bytes));
+    c->st_logits_cap = lg_bytes;
+  }
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_x0, x0_host, x0_bytes, cudaMemcpyHostToDevice, c->sm));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_logits, logits_host, lg_bytes, cudaMemcpyHostToDevice, c->sm));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_masked, masked_host, (size_t)c->b * c->N, cudaMemcpyHostToDevice, c->sm));
+  TRY(polestar_calibrate_step(c, c->st_x0, n_unmasked, block_index, block_entry, nullptr));
+  TRY(polestar_commit(c, c->st_logits, vocab, c->st_masked, c->st_commit, nullptr));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(commit_mask_host, c->st_commit, (size_t)c->b * 2 * c->B, cudaMemcpyDeviceToHost,
+                                  c->sm));
+  CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  return POLESTAR_OK;
+}
+
+extern "C" void polestar_release(polestar_ctx* c) {
+  if (!c) return;
+  free_all(c);
+  delete c;
+}
+
+extern "C" const char* polestar_last_error(const polestar_ctx* c) {
+  return c ? c->err.c_str() : g_init_error.c_str();
+}
+
+extern "C" uint64_t polestar_launch_count(const polestar_ctx* c) { return c ? c->launches : 0; }
+
+extern "C" polestar_status polestar_debug_read(polestar_ctx* c, int32_t which, int32_t layer, void* host_dst,
+                                               size_t bytes) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!host_dst) return fail(c, POLESTAR_ERR_INVALID_ARG, "host_dst is NULL");
+  const size_t L = c->L, b = c->b, N = c->N, d = c->d, Wmax = c->Wmax, K = c->K, H = c->H, B = c->B;
+  const void* base = nullptr;
+  size_t per = 0;
+  bool layered = true;
+  switch (which) {
+    case POLESTAR_BUF_KV: base = c->kv; per = b * N * 2 * c->kvdim * c->esz; break;
+    case POLESTAR_BUF_CENTROID: base = c->z; per = b * K * d * 4; break;
+    case POLESTAR_BUF_CSUM: base = c->csum; per = b * K * d * 4; break;
+    case POLESTAR_BUF_ANCHOR: base = c->anchor; per = b * K * d * 4; break;
+    case POLESTAR_BUF_LABELS: base = c->labels; per = b * Wmax; break;
+    case POLESTAR_BUF_CODES: base = c->codes; per = b * Wmax * (d / 2); break;
+    case POLESTAR_BUF_SCALES: base = c->scales; per = b * Wmax * (d / 16); break;
+    case POLESTAR_BUF_ACT_OUT: base = c->h_rows; per = b * B * d * 4; layered = false; break;
+    case POLESTAR_BUF_UPDATE: base = c->U; per = b * Wmax * d * 4; layered = false; break;
+    case POLESTAR_BUF_CONF: base = c->conf; per = b * 2 * B * 4; layered = false; break;
+    case POLESTAR_BUF_DREL: base = c->drel; per = b * 2 * B * 4; layered = false; break;
+    case POLESTAR_BUF_TAUD: base = c->taud; per = b * 2 * B * 4; layered = false; break;
+    case POLESTAR_BUF_PROXY: base = c->pprev; per = b * K * H * N * 4; break;
+    case POLESTAR_BUF_WINDOW_H: base = c->Hw; per = b * Wmax * d * 4; break;
+    case POLESTAR_BUF_DRIFT: base = c->drift; per = b * K * 4; break;
+    case POLESTAR_BUF_TOPK: base = c->topk_out; per = b * c->cfg.topk * 4; break;
+    case POLESTAR_BUF_SELECTED: base = c->selected; per = b * Wmax; break;
+    case POLESTAR_BUF_DELTA: base = c->delta; per = b * B * 4; layered = false; break;
+    default: return fail(c, POLESTAR_ERR_INVALID_ARG, "unknown buffer id");
+  }
+  if (layered && (layer < 0 || (size_t)layer >= L)) return fail(c, POLESTAR_ERR_INVALID_ARG, "layer out of range");
+  if (bytes > per) return fail(c, POLESTAR_ERR_INVALID_ARG, "bytes exceeds the buffer size");
+  const char* src = (const char*)base + (layered ? (size_t)layer * per : 0);
+  CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  CUDA_OR_FAIL(c, cudaMemcpy(host_dst, src, bytes, cudaMemcpyDeviceToHost));
+  return POLESTAR_OK;
+}

@@ -1,0 +1,172 @@
+"""ctypes binding of the Polestar C ABI (``include/polestar.h``).
+
+Argument marshalling only: every step of the calibration + commit path runs in
+the CUDA library.  The functions keep the C names; ``Polestar`` is a small
+convenience wrapper that owns a context for torch-allocated weights/streams.
+If the library is missing the binding raises -- there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, List, Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libpolestar.so")
+
+OK, ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_STATE, ERR_TIMEOUT, ERR_UNSUPPORTED = range(7)
+FP32, BF16 = 0, 1
+(BUF_KV, BUF_CENTROID, BUF_CSUM, BUF_ANCHOR, BUF_LABELS, BUF_CODES, BUF_SCALES, BUF_ACT_OUT,
+ BUF_UPDATE, BUF_CONF, BUF_DREL, BUF_TAUD, BUF_PROXY, BUF_WINDOW_H, BUF_DRIFT, BUF_TOPK,
+ BUF_SELECTED, BUF_DELTA) = range(18)
+
+EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
+            "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read")
+
+
+class polestar_config(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_heads", C.c_int32),
+                ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn_dim", C.c_int32),
+                ("rope_base", C.c_float), ("rms_eps", C.c_float), ("dtype", C.c_int32),
+                ("batch", C.c_int32), ("prompt_len", C.c_int32), ("gen_len", C.c_int32),
+                ("block", C.c_int32), ("prefix_win", C.c_int32), ("suffix_win", C.c_int32),
+                ("K", C.c_int32), ("topk", C.c_int32), ("tau_upd", C.c_int32), ("hist", C.c_int32),
+                ("kmeans_iters", C.c_int32), ("tau_s", C.c_float), ("tau_suf", C.c_float),
+                ("alpha", C.c_float), ("seed", C.c_uint64), ("host_offload", C.c_int32)]
+
+
+class polestar_layer_weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down",
+                                          "attn_norm", "ffn_norm")]
+
+
+class polestar_step_out(C.Structure):
+    _fields_ = [("drift", C.c_void_p), ("topk", C.c_void_p), ("selected", C.c_void_p),
+                ("labels", C.c_void_p), ("delta", C.c_void_p), ("fire", C.POINTER(C.c_uint8)),
+                ("win_len", C.c_int32), ("win_max", C.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    """Load libpolestar.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run drift_aware_kv_gb300.build.build() first")
+    lib = C.CDLL(path)
+    P = C.c_void_p
+    lib.polestar_init.argtypes = [C.POINTER(polestar_config), C.POINTER(polestar_layer_weights), P, P,
+                                  C.POINTER(P)]
+    lib.polestar_calibrate_step.argtypes = [P, P, C.POINTER(C.c_int32), C.c_int32, C.c_int32,
+                                            C.POINTER(polestar_step_out)]
+    lib.polestar_commit.argtypes = [P, P, C.c_int32, P, P, P]
+    lib.polestar_step_host.argtypes = [P, P, C.POINTER(C.c_int32), C.c_int32, C.c_int32, P, C.c_int32, P, P]
+    lib.polestar_release.argtypes = [P]
+    lib.polestar_release.restype = None
+    lib.polestar_last_error.argtypes = [P]
+    lib.polestar_last_error.restype = C.c_char_p
+    lib.polestar_launch_count.argtypes = [P]
+    lib.polestar_launch_count.restype = C.c_uint64
+    lib.polestar_debug_read.argtypes = [P, C.c_int32, C.c_int32, P, C.c_size_t]
+    for f in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
+              "polestar_debug_read"):
+        getattr(lib, f).restype = C.c_int
+    _lib = lib
+    return lib
+
+
+class PolestarError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"polestar status {status}: {msg}")
+        self.status = status
+
+
+def _check(st: int, ctx=None):
+    if st != OK:
+        msg = load().polestar_last_error(ctx).decode()
+        raise PolestarError(st, msg)
+
+
+def make_config(w, host_offload: bool = False) -> polestar_config:
+    """polestar_config from a workload description (attributes as in synth.Workload)."""
+    return polestar_config(
+        n_layers=w.n_layers, d_model=w.d_model, n_heads=w.n_heads, n_kv_heads=w.n_kv_heads,
+        head_dim=w.head_dim, ffn_dim=w.ffn_dim, rope_base=w.rope_base, rms_eps=w.rms_eps,
+        dtype=BF16 if w.dtype == "bf16" else FP32, batch=w.batch, prompt_len=w.prompt_len,
+        gen_len=w.gen_len, block=w.block, prefix_win=w.prefix_win, suffix_win=w.suffix_win, K=w.K,
+        topk=w.topk, tau_upd=w.tau_upd, hist=w.hist, kmeans_iters=w.kmeans_iters, tau_s=w.tau_s,
+        tau_suf=w.tau_suf, alpha=w.alpha, seed=w.seed, host_offload=int(host_offload))
+
+
+class Polestar:
+    """Owns one library context.  Weights are torch CUDA tensors (kept alive here)."""
+
+    def __init__(self, workload, layer_weights: List[Dict], stream=None, side_stream=None,
+                 host_offload: bool = False):
+        import torch
+        self.lib = load()
+        self.w = workload
+        self.weights = layer_weights
+        self.cfg = make_config(workload, host_offload)
+        arr = (polestar_layer_weights * workload.n_layers)()
+        for i, lw in enumerate(layer_weights):
+            for name in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "attn_norm", "ffn_norm"):
+                t = lw[name]
+                assert t.is_cuda and t.is_contiguous()
+                setattr(arr[i], name, t.data_ptr())
+        self._arr = arr
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self.side = side_stream if side_stream is not None else self.stream
+        ctx = C.c_void_p()
+        st = self.lib.polestar_init(C.byref(self.cfg), arr, C.c_void_p(self.stream.cuda_stream),
+                                    C.c_void_p(self.side.cuda_stream), C.byref(ctx))
+        if st != OK:
+            raise PolestarError(st, self.lib.polestar_last_error(None).decode())
+        self.ctx = ctx
+        self.last_out = polestar_step_out()
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            self.lib.polestar_release(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def calibrate_step(self, x0, n_unmasked: Sequence[int], block_index: int, block_entry: bool):
+        arr = (C.c_int32 * self.w.batch)(*[int(v) for v in n_unmasked])
+        _check(self.lib.polestar_calibrate_step(self.ctx, C.c_void_p(x0.data_ptr()), arr, int(block_index),
+                                                int(bool(block_entry)), C.byref(self.last_out)), self.ctx)
+        return self.last_out
+
+    def commit(self, logits, masked_u8, commit_mask_u8, conf=None):
+        _check(self.lib.polestar_commit(self.ctx, C.c_void_p(logits.data_ptr()), int(logits.shape[-1]),
+                                        C.c_void_p(masked_u8.data_ptr()),
+                                        C.c_void_p(commit_mask_u8.data_ptr()),
+                                        C.c_void_p(conf.data_ptr()) if conf is not None else None),
+               self.ctx)
+
+    def step_host(self, x0_host, n_unmasked, block_index, block_entry, logits_host, masked_host,
+                  commit_host):
+        arr = (C.c_int32 * self.w.batch)(*[int(v) for v in n_unmasked])
+        _check(self.lib.polestar_step_host(self.ctx, C.c_void_p(x0_host.data_ptr()), arr, int(block_index),
+                                           int(bool(block_entry)), C.c_void_p(logits_host.data_ptr()),
+                                           int(logits_host.shape[-1]), C.c_void_p(masked_host.data_ptr()),
+                                           C.c_void_p(commit_host.data_ptr())), self.ctx)
+
+    def launch_count(self) -> int:
+        return int(self.lib.polestar_launch_count(self.ctx))
+
+    def read(self, which: int, layer: int, shape, dtype):
+        """Copy an internal buffer to a new CPU torch tensor of the given shape/dtype."""
+        import torch
+        out = torch.empty(shape, dtype=dtype)
+        _check(self.lib.polestar_debug_read(self.ctx, which, layer, C.c_void_p(out.data_ptr()),
+                                            out.numel() * out.element_size()), self.ctx)
+        return out

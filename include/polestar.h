@@ -1,0 +1,188 @@
+/*
+ * polestar.h -- C ABI of the GB300 (sm_103a) Polestar calibration + commit path.
+ *
+ * The operations follow "Polestar: Drift-Aware Cache Calibration and Token
+ * Commitment for Efficient Inference of Diffusion LLMs" (arXiv 2607.14107):
+ *   - Polestar-Cache, §4.1 (block entry, spherical K-means, residual NVFP4 of
+ *     App. C.3, proxy attention + KL drift of Eq. 4, top-k clusters, sparse
+ *     layer-wise update packets, update schedule) and Algorithm 1 lines 4-26;
+ *   - Polestar-Commit, §4.2 (drift history, dynamic threshold, current- and
+ *     suffix-block commit) and Algorithm 1 lines 11-12, 27-39;
+ *   - the system design of §4.3 (pinned-host NVFP4 store, side-stream prefetch).
+ *
+ * Conventions (all entry points):
+ *   - No call throws; every failure is a polestar_status, with a message kept
+ *     for polestar_last_error().  Argument errors are detected on the host
+ *     before any launch and leave the context unchanged.
+ *   - All device work is issued asynchronously on the context's main stream
+ *     (given at init).  Device outputs are valid once that stream is
+ *     synchronised.  The side stream carries host<->device traffic of the
+ *     NVFP4 store only.
+ *   - "device" pointers are CUDA device (or managed) memory of the current
+ *     device; "host" pointers are ordinary host memory.  Caller-provided
+ *     buffers stay owned by the caller; the context never frees them.
+ *   - Layouts are dense, row-major, innermost index last.
+ *   - A context is not thread-safe; use one context per host thread.
+ */
+#ifndef POLESTAR_H
+#define POLESTAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct polestar_ctx polestar_ctx; /* opaque; owned by the library */
+
+typedef enum {
+  POLESTAR_OK = 0,
+  POLESTAR_ERR_INVALID_ARG = 1, /* bad pointer, size or configuration          */
+  POLESTAR_ERR_CUDA = 2,        /* a CUDA runtime/driver call failed            */
+  POLESTAR_ERR_OOM = 3,         /* device or pinned-host allocation failed      */
+  POLESTAR_ERR_STATE = 4,       /* call out of order (e.g. commit before step)  */
+  POLESTAR_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up           */
+  POLESTAR_ERR_UNSUPPORTED = 6  /* shape outside what the kernels implement     */
+} polestar_status;
+
+typedef enum { POLESTAR_FP32 = 0, POLESTAR_BF16 = 1 } polestar_dtype;
+
+/* Model shape and Polestar hyper-parameters (Table 5 defaults in brackets). */
+typedef struct {
+  int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim;
+  float rope_base; /* rotary base theta                                        */
+  float rms_eps;   /* RMSNorm epsilon                                          */
+  int32_t dtype;   /* polestar_dtype: storage of weights, x0, K/V cache         */
+  int32_t batch;   /* independent sequences decoded in lockstep blocks          */
+  int32_t prompt_len, gen_len;        /* N = prompt_len + gen_len positions     */
+  int32_t block;                      /* B [32]                                 */
+  int32_t prefix_win, suffix_win;     /* |Omega^p| [2B], |Omega^s| [B]          */
+  int32_t K;                          /* centroids [8]                          */
+  int32_t topk;                       /* refreshed clusters k [4]               */
+  int32_t tau_upd;                    /* refresh trigger [3]                    */
+  int32_t hist;                       /* drift history h [5]                    */
+  int32_t kmeans_iters;               /* Lloyd iterations [10]                  */
+  float tau_s;                        /* static confidence threshold [0.9]      */
+  float tau_suf;                      /* suffix commit confidence [0.9]         */
+  float alpha;                        /* drift-gate coefficient [10]            */
+  uint64_t seed;                      /* K-means initialisation seed            */
+  int32_t host_offload; /* 1: NVFP4 window store in pinned host memory (§4.3) */
+} polestar_config;
+
+/* Borrowed device pointers of one decoder layer, in the config dtype.
+ * Matrices are row-major [out, in] (y = x W^T): wq [H*dh, d], wk/wv [Hkv*dh, d],
+ * wo [d, H*dh], w_gate/w_up [F, d], w_down [d, F]; norms are gains [d]. */
+typedef struct {
+  const void *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down, *attn_norm, *ffn_norm;
+} polestar_layer_weights;
+
+/* Per-step results.  Device pointers are owned by the context and stay valid
+ * until the next polestar_calibrate_step or polestar_release. */
+typedef struct {
+  const float *drift;      /* device [n_layers, batch, K]: per-cluster KL drift D
+                              (Eq. 4 on proxy attention, mean over query heads);
+                              0 for sequences that did not refresh this step     */
+  const int32_t *topk;     /* device [n_layers, batch, topk]: selected clusters,
+                              descending drift, ties to the lower id; -1 when the
+                              sequence did not refresh                           */
+  const uint8_t *selected; /* device [n_layers, batch, win_max]: 1 = window row in
+                              a selected cluster (its update packet was computed) */
+  const uint8_t *labels;   /* device [n_layers, batch, win_max]: cluster ids       */
+  const float *delta;      /* device [batch, block]: last-layer drift delta_j      */
+  const uint8_t *fire;     /* host [batch]: 1 = the sparse refresh ran             */
+  int32_t win_len;         /* |Omega_b| of the current block (<= win_max)          */
+  int32_t win_max;         /* prefix_win + suffix_win                              */
+} polestar_step_out;
+
+/* Create a context: validates cfg, allocates the K/V cache [L, batch, N, 2,
+ * Hkv*dh], the window state (centroids, anchors, labels, NVFP4 codes -- in
+ * pinned host memory when host_offload = 1), the proxy-attention history and
+ * the step workspaces.  `layers` is a host array of n_layers entries whose
+ * device pointers must stay valid for the life of the context.  stream_main
+ * and stream_side are cudaStream_t values (NULL = legacy default stream; the
+ * side stream may equal the main stream).  On success *out receives the
+ * context; on failure *out is NULL and nothing stays allocated. */
+polestar_status polestar_init(const polestar_config *cfg, const polestar_layer_weights *layers,
+                              void *stream_main, void *stream_side, polestar_ctx **out);
+
+/* One denoising step of Polestar-Cache over every layer (Algorithm 1).
+ *   x0          device [batch, N, d] (config dtype): layer-0 hidden states of
+ *               the current step (embeddings of the partially unmasked sequence)
+ *   n_unmasked  host [batch]: tokens unmasked since the previous step (drives the
+ *               tau_upd trigger of §4.1 "Update Schedule"); ignored at block entry
+ *   block_index active block b, 0 <= b < gen_len / block
+ *   block_entry 1 at the first step of block b: forward over the full sequence
+ *               (even b) or window + block (odd b), K-means, NVFP4, proxy
+ *               attention baseline; 0 for a within-block step
+ *   out         may be NULL. */
+polestar_status polestar_calibrate_step(polestar_ctx *ctx, const void *x0, const int32_t *n_unmasked,
+                                        int32_t block_index, int32_t block_entry,
+                                        polestar_step_out *out);
+
+/* Polestar-Commit for the step just calibrated (§4.2).
+ *   logits      device [batch, 2*block, vocab] fp32: rows 0..B-1 are the active
+ *               block, rows B..2B-1 the suffix block (rows past the sequence end
+ *               are ignored)
+ *   masked      device [batch, N] uint8: 1 = position still [MASK]
+ *   commit_mask device [batch, 2*block] uint8, written: 1 = commit the token
+ *   conf        device [batch, 2*block] fp32 or NULL: max-softmax confidence c_j
+ * Requires a preceding polestar_calibrate_step on this context. */
+polestar_status polestar_commit(polestar_ctx *ctx, const float *logits, int32_t vocab,
+                                const uint8_t *masked, uint8_t *commit_mask, float *conf);
+
+/* End-to-end step on HOST buffers: copies x0 (host [batch, N, d], config dtype),
+ * logits (host [batch, 2B, vocab] fp32) and masked (host [batch, N] uint8) to the
+ * device on the main stream, runs polestar_calibrate_step + polestar_commit,
+ * copies the commit mask back to commit_mask_host ([batch, 2B] uint8) and
+ * synchronises the main stream.  Host buffers should be pinned for full
+ * bandwidth.  Staging buffers are allocated on first use. */
+polestar_status polestar_step_host(polestar_ctx *ctx, const void *x0_host, const int32_t *n_unmasked,
+                                   int32_t block_index, int32_t block_entry,
+                                   const float *logits_host, int32_t vocab,
+                                   const uint8_t *masked_host, uint8_t *commit_mask_host);
+
+/* Free everything the context owns.  NULL is accepted; the context pointer is
+ * invalid afterwards.  Synchronises the context's streams first. */
+void polestar_release(polestar_ctx *ctx);
+
+/* Message of the last failure on this context ("" if none).  With ctx == NULL,
+ * the message of the last failed polestar_init on this thread. */
+const char *polestar_last_error(const polestar_ctx *ctx);
+
+/* Number of kernel launches issued on this context since init (diagnostics). */
+uint64_t polestar_launch_count(const polestar_ctx *ctx);
+
+/* ---- inspection (used by parity tests; synchronises the main stream) ---- */
+typedef enum {
+  POLESTAR_BUF_KV = 0,        /* layer l: [batch, N, 2, Hkv*dh] config dtype        */
+  POLESTAR_BUF_CENTROID = 1,  /* layer l: [batch, K, d] fp32 unit proxies z_c       */
+  POLESTAR_BUF_CSUM = 2,      /* layer l: [batch, K, d] fp32 member sums s_c        */
+  POLESTAR_BUF_ANCHOR = 3,    /* layer l: [batch, K, d] fp32 residual anchors A_c   */
+  POLESTAR_BUF_LABELS = 4,    /* layer l: [batch, win_max] uint8                    */
+  POLESTAR_BUF_CODES = 5,     /* layer l: [batch, win_max, d/2] uint8 E2M1 pairs,
+                                 element 2i in the low nibble                       */
+  POLESTAR_BUF_SCALES = 6,    /* layer l: [batch, win_max, d/16] uint8 E4M3         */
+  POLESTAR_BUF_ACT_OUT = 7,   /* [batch, block, d] fp32 last-layer output, active rows */
+  POLESTAR_BUF_UPDATE = 8,    /* [batch, win_max, d] fp32 last update packet U(t,L)  */
+  POLESTAR_BUF_CONF = 9,      /* [batch, 2B] fp32 confidence c                       */
+  POLESTAR_BUF_DREL = 10,     /* [batch, 2B] fp32 Delta_j (drift minus history mean) */
+  POLESTAR_BUF_TAUD = 11,     /* [batch, 2B] fp32 dynamic threshold tau_d            */
+  POLESTAR_BUF_PROXY = 12,    /* layer l: [batch, K, H, N] fp32 last proxy scores    */
+  POLESTAR_BUF_WINDOW_H = 13, /* layer l: [batch, win_max, d] fp32 block-entry inputs */
+  POLESTAR_BUF_DRIFT = 14,    /* layer l: [batch, K] fp32 (same data as step_out.drift) */
+  POLESTAR_BUF_TOPK = 15,     /* layer l: [batch, topk] int32                       */
+  POLESTAR_BUF_SELECTED = 16, /* layer l: [batch, win_max] uint8                    */
+  POLESTAR_BUF_DELTA = 17     /* [batch, block] fp32 token drift delta_j            */
+} polestar_buffer;
+
+/* Copy `bytes` bytes of an internal buffer (layer `layer` where the buffer is
+ * per layer) to host memory.  Fails with INVALID_ARG if bytes exceeds the
+ * buffer size or the layer is out of range. */
+polestar_status polestar_debug_read(polestar_ctx *ctx, int32_t which, int32_t layer, void *host_dst,
+                                    size_t bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* POLESTAR_H */

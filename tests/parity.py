@@ -1,0 +1,242 @@
+"""Lockstep parity harness: runs the CUDA library (through the C ABI) and the CPU
+oracle on the same seeded trajectory and compares every step.
+
+Exactness bar: cluster ids, top-k sets, selected rows, NVFP4 codes/scales and
+commit masks are compared exactly; a mismatch is accepted only when the
+oracle's decision margin is below NEAR_TIE (a near tie), and is then counted.
+After a near-tie divergence the two trajectories legitimately differ, so the
+comparison stops at that step.  Floating-point outputs use the tolerances
+below (KL drift 1e-5 abs + 1e-3 rel; K/V, hidden states and update packets by
+relative L2 error)."""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+from drift_aware_kv_gb300 import polestar as P
+from drift_aware_kv_gb300 import synth
+from oracle import polestar_oracle as O
+
+NEAR_TIE = 1e-4
+KL_ABS, KL_REL = 1e-5, 1e-3
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / max(den, 1e-30))
+
+
+def unpack_codes(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+@dataclasses.dataclass
+class Report:
+    steps: int = 0
+    near_ties: int = 0
+    diverged_at: int = -1
+    max_kv_err: float = 0.0
+    max_act_err: float = 0.0
+    max_u_err: float = 0.0
+    max_kl_err: float = 0.0
+    code_mismatch: int = 0
+    max_dec_err: float = 0.0
+    fires: int = 0
+    commits: int = 0
+    notes: list = dataclasses.field(default_factory=list)
+
+
+class Lockstep:
+    def __init__(self, w: synth.Workload, kv_tol: float, act_tol: float):
+        self.w = w
+        self.kv_tol, self.act_tol = kv_tol, act_tol
+        # block-entry centroids/anchors: fp32 path ~1e-6; bf16 path inherits the
+        # bf16 rounding of the A operands of the preceding layers
+        self.state_tol = 1e-5 if w.dtype == "fp32" else 1e-3
+        W_cpu = synth.make_weights(w, "cpu")
+        self.orc = O.PolestarOracle(w, O.weights_to_numpy(W_cpu))
+        self.Wg = [{k: v.cuda() for k, v in lw.items()} for lw in W_cpu]
+        self.lib = P.Polestar(w, self.Wg)
+        self.tr = synth.Trajectory(w)
+        self.rep = Report()
+        self.N = w.seq_len
+        self.Wmax = w.prefix_win + w.suffix_win
+
+    def read_layer(self, which, layer, shape, dtype):
+        return self.lib.read(which, layer, shape, dtype)
+
+    def run(self, max_steps=None):
+        w, rep = self.w, self.rep
+        dt = synth.torch_dtype(w)
+        while True:
+            st = self.tr.next_step()
+            if st is None or (max_steps is not None and rep.steps >= max_steps):
+                break
+            x0 = st["x0"].to(dt)
+            recs = self.orc.calibrate_step(x0.double().numpy(), st["n_unmasked"], st["block_index"],
+                                           st["block_entry"])
+            xg = x0.cuda()
+            out = self.lib.calibrate_step(xg, st["n_unmasked"], st["block_index"], st["block_entry"])
+            torch.cuda.synchronize()
+            ok = self._compare_step(st, recs, out)
+            coms = self.orc.commit(st["logits"].numpy(), st["masked"].numpy())
+            lg = st["logits"].cuda()
+            mk = st["masked"].to(torch.uint8).cuda()
+            cm = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device="cuda")
+            self.lib.commit(lg, mk, cm)
+            torch.cuda.synchronize()
+            ok = ok and self._compare_commit(st, coms, cm.cpu().numpy())
+            rep.steps += 1
+            if not ok:
+                rep.diverged_at = st["t"]
+                break
+        return rep
+
+    # ------------------------------------------------------------------
+    def _decision(self, name, equal, margin):
+        """Exact decision check; returns False (stop) on an accepted near tie."""
+        if equal:
+            return True
+        if margin < NEAR_TIE:
+            self.rep.near_ties += 1
+            self.rep.notes.append(f"near tie in {name} (margin {margin:.2e})")
+            return False
+        raise AssertionError(f"{name}: mismatch with oracle margin {margin:.3e}")
+
+    def _compare_step(self, st, recs, out):
+        w, rep = self.w, self.rep
+        L, b, K, d = w.n_layers, w.batch, w.K, w.d_model
+        nw = out.win_len
+        if st["block_entry"]:
+            for l in range(L):
+                lab = self.read_layer(P.BUF_LABELS, l, (b, self.Wmax), torch.uint8).numpy()
+                for s in range(b):
+                    o = self.orc.seqs[s]
+                    if not self._decision(f"kmeans labels (l={l}, s={s})",
+                                          np.array_equal(lab[s, :nw], o.labels[l]),
+                                          recs[s]["kmeans_margin"][l]):
+                        return False
+                codes = unpack_codes(self.read_layer(P.BUF_CODES, l, (b, self.Wmax, d // 2),
+                                                     torch.uint8).numpy())
+                scales = self.read_layer(P.BUF_SCALES, l, (b, self.Wmax, d // 16), torch.uint8).numpy()
+                anchor = self.read_layer(P.BUF_ANCHOR, l, (b, K, d), torch.float32).numpy()
+                z = self.read_layer(P.BUF_CENTROID, l, (b, K, d), torch.float32).numpy()
+                for s in range(b):
+                    o = self.orc.seqs[s]
+                    ea, ez = rel_l2(anchor[s], o.A[l]), rel_l2(z[s], o.z[l])
+                    assert ea < self.state_tol, f"anchors rel err {ea} (layer {l}, seq {s})"
+                    assert ez < self.state_tol, f"centroids rel err {ez} (layer {l}, seq {s})"
+                    self._check_codes(codes[s, :nw], scales[s, :nw], o, l)
+        else:
+            fire = [bool(out.fire[s]) for s in range(b)]
+            assert fire == [bool(r["fire"]) for r in recs], "trigger"
+            rep.fires += sum(fire)
+            drift = np.stack([self.read_layer(P.BUF_DRIFT, l, (b, K), torch.float32).numpy()
+                              for l in range(L)])
+            topk = np.stack([self.read_layer(P.BUF_TOPK, l, (b, w.topk), torch.int32).numpy()
+                             for l in range(L)])
+            sel = np.stack([self.read_layer(P.BUF_SELECTED, l, (b, self.Wmax), torch.uint8).numpy()
+                            for l in range(L)])
+            for s in range(b):
+                if not fire[s]:
+                    continue
+                for l in range(L):
+                    D_o = recs[s]["D"][l]
+                    err = np.abs(drift[l, s] - D_o)
+                    rep.max_kl_err = max(rep.max_kl_err, float(np.max(err / (KL_ABS + KL_REL * np.abs(D_o)))))
+                    assert np.all(err <= KL_ABS + KL_REL * np.abs(D_o)), f"drift D (l={l}, s={s})"
+                    if not self._decision(f"top-k (l={l}, s={s})",
+                                          list(topk[l, s]) == list(recs[s]["topk"][l]),
+                                          recs[s]["topk_margin"][l]):
+                        return False
+                    assert np.array_equal(sel[l, s, :nw].astype(bool), recs[s]["sel"][l]), "selection"
+            delta = self.read_layer(P.BUF_DELTA, 0, (b, w.block), torch.float32).numpy()
+            for s in range(b):
+                d_o = recs[s]["delta"]
+                assert np.all(np.abs(delta[s] - d_o) <= KL_ABS + KL_REL * np.abs(d_o)), "token drift delta"
+            act = self.read_layer(P.BUF_ACT_OUT, 0, (b, w.block, d), torch.float32).numpy()
+            for s in range(b):
+                e = rel_l2(act[s], recs[s]["act_out"])
+                rep.max_act_err = max(rep.max_act_err, e)
+                assert e < self.act_tol, f"active-row output rel err {e}"
+            if any(fire):
+                U = self.read_layer(P.BUF_UPDATE, 0, (b, self.Wmax, d), torch.float32).numpy()
+                for s in range(b):
+                    if not fire[s]:
+                        continue
+                    selm = recs[s]["sel"][-1]
+                    e = rel_l2(U[s, :nw][selm], recs[s]["U_last"][selm])
+                    rep.max_u_err = max(rep.max_u_err, e)
+                    assert e < self.act_tol, f"update packet rel err {e}"
+                    for l in range(L):
+                        self._check_codes(None, None, self.orc.seqs[s], l, s=s, nw=nw)
+        # K/V cache of every layer
+        dt = synth.torch_dtype(w)
+        for l in range(L):
+            kv = self.read_layer(P.BUF_KV, l, (b, self.N, 2, w.n_kv_heads, w.head_dim), dt).double().numpy()
+            for s in range(b):
+                e = rel_l2(kv[s], self.orc.seqs[s].kv[l])
+                rep.max_kv_err = max(rep.max_kv_err, e)
+                assert e < self.kv_tol, f"K/V cache rel err {e} (layer {l}, seq {s})"
+        return True
+
+    def _check_codes(self, codes, scales, o, l, s=None, nw=None):
+        """NVFP4 store of layer l.  Where the encoder's inputs are exact on both
+        sides (fp32 workloads; layer 0, whose rows are the caller's x0) the codes
+        and scales must match bit for bit up to near ties.  Deeper layers of a
+        bf16 stack carry the upstream bf16 rounding differences into the residual
+        r = h - A, so there the decoded hidden states are compared instead."""
+        w = self.w
+        d = w.d_model
+        if codes is None:
+            codes = unpack_codes(self.read_layer(P.BUF_CODES, l, (w.batch, self.Wmax, d // 2),
+                                                 torch.uint8).numpy())[s, :nw]
+            scales = self.read_layer(P.BUF_SCALES, l, (w.batch, self.Wmax, d // 16), torch.uint8).numpy()[s, :nw]
+        oc, osb, om = o.codes[l], o.sbytes[l], o.code_margin[l]
+        exact = w.dtype == "fp32" or l == 0
+        if not exact:
+            lab = o.labels[l]
+            dec_g = O.nvfp4_decode(codes, scales) + o.A[l][lab]
+            dec_o = O.nvfp4_decode(oc, osb) + o.A[l][lab]
+            e = rel_l2(dec_g, dec_o)
+            self.rep.max_dec_err = max(self.rep.max_dec_err, e)
+            assert e < self.act_tol, f"decoded window states rel err {e} (layer {l})"
+            return
+        bad = codes != oc
+        sbad = np.repeat(scales != osb, 16, axis=1)
+        bad = bad | sbad
+        if np.any(bad):
+            worst = float(np.max(om[bad]))
+            self.rep.code_mismatch += int(bad.sum())
+            if worst >= NEAR_TIE:
+                raise AssertionError(f"NVFP4 codes differ with oracle margin {worst:.3e} "
+                                     f"({int(bad.sum())} elements, layer {l})")
+
+    def _compare_commit(self, st, coms, cm):
+        w = self.w
+        conf = self.read_layer(P.BUF_CONF, 0, (w.batch, 2 * w.block), torch.float32).numpy()
+        drel = self.read_layer(P.BUF_DREL, 0, (w.batch, 2 * w.block), torch.float32).numpy()
+        taud = self.read_layer(P.BUF_TAUD, 0, (w.batch, 2 * w.block), torch.float32).numpy()
+        for s in range(w.batch):
+            co = coms[s]
+            valid = np.arange(2 * w.block) + w.prompt_len + st["block_index"] * w.block < self.N
+            assert np.allclose(conf[s][valid], co["conf"][valid], rtol=1e-5, atol=1e-6), "confidence"
+            assert np.all(np.abs(drel[s] - co["delta_rel"]) <= KL_ABS + KL_REL * np.abs(co["delta_rel"])), "Delta"
+            assert np.allclose(taud[s], co["tau_d"], rtol=1e-4, atol=1e-6), "tau_d"
+            eq = np.array_equal(cm[s].astype(bool), co["commit"])
+            if not eq:
+                diff = cm[s].astype(bool) != co["commit"]
+                m = float(np.min(co["margin"][diff]))
+                if not self._decision(f"commit mask (s={s})", False, m):
+                    return False
+            self.rep.commits += int(co["commit"].sum())
+        return True

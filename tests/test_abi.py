@@ -1,0 +1,46 @@
+"""The C-ABI library builds, loads and exports every function include/polestar.h
+declares (no GPU needed: nothing here calls into the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "polestar.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(polestar_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_four_calls():
+    names = _declared()
+    for n in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_release"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    from drift_aware_kv_gb300.build import build
+    from drift_aware_kv_gb300 import polestar as P
+    lib = ctypes.CDLL(build())
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert set(P.EXPORTED) <= set(_declared())
+
+
+def test_init_rejects_bad_config_without_touching_the_device():
+    from drift_aware_kv_gb300 import polestar as P
+    from drift_aware_kv_gb300 import synth
+    lib = P.load()
+    cfg = P.make_config(synth.WORKLOADS["tiny_l1_d256_fp32"].replace(K=9))
+    arr = (P.polestar_layer_weights * 1)()
+    ctx = ctypes.c_void_p()
+    st = lib.polestar_init(ctypes.byref(cfg), arr, None, None, ctypes.byref(ctx))
+    assert st == P.ERR_INVALID_ARG and not ctx.value
+    assert b"K must be" in lib.polestar_last_error(None)
+    cfg = P.make_config(synth.WORKLOADS["tiny_l1_d256_fp32"])
+    st = lib.polestar_init(ctypes.byref(cfg), arr, None, None, ctypes.byref(ctx))
+    assert st == P.ERR_INVALID_ARG and b"NULL weight" in lib.polestar_last_error(None)
+    lib.polestar_release(None)
