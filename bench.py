@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Throughput of the Polestar calibration + commit path on GB300.
+
+One *step* is one denoising step of the seeded synthetic trajectory: a
+``polestar_calibrate_step`` over every layer of every sequence (block entry:
+full/partial forward, K-means, NVFP4, proxy baseline; within-block: patch,
+proxy KL, top-k, sparse update packets) followed by ``polestar_commit``.  The
+timed steps continue the trajectory after the warm-up, so they contain the
+trajectory's own mix of block entries and within-block steps.
+
+Metric: calibration steps/s (``value``); window tokens/s, per-class kernel
+time, the roofline of the dominant kernel and the CPU oracle's throughput are
+reported alongside.  Inputs (x0, logits, mask) of every step are resident in
+HBM before the timed region; the per-step working set (the 32-layer weights,
+14 GB) is far larger than L2, so no L2 flush is needed between steps.
+
+Multi-GPU (torchrun): every rank runs an independent replica on its own
+sequences (weak scaling, no collective on the data path); the JSON line
+reports the whole-job aggregate over max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "llada8b_p512_g256_b1"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["_source"] = "fallback"
+    return d
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """Max of a host scalar over ranks (identity for one rank)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_line(per_rank_units: float, ws: int, seconds_max: float) -> float:
+    """Whole-job throughput: units of every rank over the slowest rank's time."""
+    return per_rank_units * ws / seconds_max
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clk_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload
+def make_inputs(w, n_steps, device):
+    """Trajectory inputs of the first n_steps steps, moved to `device`."""
+    import torch
+    from drift_aware_kv_gb300 import synth
+    tr = synth.Trajectory(w)
+    dt = synth.torch_dtype(w)
+    steps = []
+    for _ in range(n_steps):
+        st = tr.next_step()
+        if st is None:
+            break
+        steps.append(dict(
+            x0=st["x0"].to(dt).to(device), logits=st["logits"].to(device),
+            masked=st["masked"].to(torch.uint8).to(device), n_unmasked=st["n_unmasked"],
+            block_index=st["block_index"], block_entry=st["block_entry"]))
+    return steps
+
+
+def run_device(args, w, peaks, ws, rank, local):
+    import torch
+    from drift_aware_kv_gb300 import polestar as P
+    from drift_aware_kv_gb300 import synth
+    from drift_aware_kv_gb300.build import build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or ws == 1:
+        build()
+    barrier(ws)
+    W = synth.make_weights(w, dev)
+    total = args.warmup + args.steps
+    steps = make_inputs(w.replace(seed=w.seed + rank), total, dev)
+    if len(steps) < total:
+        raise SystemExit(f"trajectory has only {len(steps)} steps < warmup + steps = {total}")
+    stream = torch.cuda.current_stream(dev)
+    ps = P.Polestar(w, W, stream=stream)
+    cm = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device=dev)
+
+    def do_step(st):
+        ps.calibrate_step(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"])
+        ps.commit(st["logits"], st["masked"], cm)
+
+    for st in steps[: args.warmup]:
+        do_step(st)
+    torch.cuda.synchronize(dev)
+
+    timed = steps[args.warmup:]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(timed) + 1)]
+    capacity = 32 * w.n_layers * len(timed) + 256
+    clk = ClockSampler(local)
+    launches0 = ps.launch_count()
+    ps.profile_begin(capacity)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    clk.start()
+    t0 = time.perf_counter()
+    ev[0].record(stream)
+    for i, st in enumerate(timed):
+        do_step(st)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    barrier(ws)
+    clocks = clk.stop()
+    stats = ps.profile_end()
+    launches = ps.launch_count() - launches0
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(timed))]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_s = max_over_ranks(total_ms / 1e3, ws, dev)
+    n_entry = sum(1 for st in timed if st["block_entry"])
+    n_within = len(timed) - n_entry
+    entry_ms = [m for m, st in zip(step_ms, timed) if st["block_entry"]]
+    within_ms = [m for m, st in zip(step_ms, timed) if not st["block_entry"]]
+    ps.close()
+    del ps
+
+    # ---- e2e: host buffers through polestar_step_host, copies in the timed region
+    e2e = None
+    if not args.no_e2e:
+        ps2 = P.Polestar(w, W, stream=stream)
+        host = []
+        for st in steps:
+            host.append(dict(x0=st["x0"].cpu().pin_memory(), logits=st["logits"].cpu().pin_memory(),
+                             masked=st["masked"].cpu().pin_memory(), n_unmasked=st["n_unmasked"],
+                             block_index=st["block_index"], block_entry=st["block_entry"]))
+        cmh = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8).pin_memory()
+        for st in host[: args.warmup]:
+            ps2.step_host(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"], st["logits"],
+                          st["masked"], cmh)
+        barrier(ws)
+        t0 = time.perf_counter()
+        for st in host[args.warmup:]:
+            ps2.step_host(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"], st["logits"],
+                          st["masked"], cmh)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
+        ps2.close()
+        h2d = host[0]["x0"].numel() * host[0]["x0"].element_size() + \
+            host[0]["logits"].numel() * 4 + host[0]["masked"].numel()
+        e2e = {"value": aggregate_line(len(timed), ws, e2e_s), "unit": "steps/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(cmh.numel())}
+
+    # ---- roofline of the dominant kernel class
+    dom = max(stats, key=lambda k: stats[k]["ms"])
+    s = stats[dom]
+    if dom in ("gemm_entry",) or (dom == "gemm_step" and w.batch >= 8):
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        achieved = s["flops"] / (s["ms"] / 1e3) / 1e12 if s["ms"] > 0 else 0.0
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "peak_source": peaks["_source"] + " sustained"}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = s["bytes"] / (s["ms"] / 1e3) / 1e9 if s["ms"] > 0 else 0.0
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None, "peak_source": peaks["_source"]}
+    roof["avg_launch_us"] = s["ms"] * 1e3 / max(1, s["launches"])
+    roof["launches"] = s["launches"]
+
+    nw_mean = statistics.mean(len(synth.window_positions(w, st["block_index"])) for st in timed)
+    value = aggregate_line(len(timed), ws, total_s)
+    out = {
+        "metric": "calibration steps/s", "value": value, "unit": "steps/s", "n_gpus": ws,
+        "steps": len(timed), "warmup": args.warmup, "ms_per_step": total_ms / len(timed),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded trajectory, random-init N(0,0.02) weights)",
+        "config": {"workload": w.name, "model": "LLaDA-8B-shaped" if "llada" in w.name else w.name,
+                   "layers": w.n_layers, "d_model": w.d_model, "batch": w.batch, "seq_len": w.seq_len,
+                   "block": w.block, "window": w.prefix_win + w.suffix_win, "K": w.K, "topk": w.topk,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "per-step working set (weights) >> L2; no flush needed",
+                   "timed_block_entries": n_entry, "timed_within_block_steps": n_within},
+        "window_tokens_per_s": value * w.batch * nw_mean,
+        "block_entry_ms": statistics.mean(entry_ms) if entry_ms else None,
+        "within_block_ms": statistics.mean(within_ms) if within_ms else None,
+        "within_block_steps_per_s": 1e3 / statistics.mean(within_ms) if within_ms else None,
+        "kernel_ms": {k: round(v["ms"], 3) for k, v in stats.items()},
+        "kernel_launches": {k: v["launches"] for k, v in stats.items()},
+        "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
+        "wall_s": wall,
+    }
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(w, n_layers_sample, n_steps, warmup=0):
+    """Time the unmodified CPU oracle on the workload truncated to the first
+    n_layers_sample layers; returns per-step seconds scaled to all layers."""
+    import numpy as np
+    from drift_aware_kv_gb300 import synth
+    from oracle import polestar_oracle as O
+    ws = w.replace(n_layers=n_layers_sample)
+    W = O.weights_to_numpy(synth.make_weights(ws, "cpu"))
+    orc = O.PolestarOracle(ws, W)
+    tr = synth.Trajectory(ws)
+    dt = synth.torch_dtype(ws)
+    scale = w.n_layers / n_layers_sample
+    times, kinds = [], []
+    for i in range(warmup + n_steps):
+        st = tr.next_step()
+        if st is None:
+            break
+        x0 = st["x0"].to(dt).double().numpy()
+        lg = st["logits"].numpy()
+        mk = st["masked"].numpy()
+        t0 = time.perf_counter()
+        orc.calibrate_step(x0, st["n_unmasked"], st["block_index"], st["block_entry"])
+        orc.commit(lg, mk)
+        dtm = time.perf_counter() - t0
+        if i >= warmup:
+            times.append(dtm * scale)
+            kinds.append(bool(st["block_entry"]))
+    return times, kinds
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] or [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, n_entry, n_within, budget_steps=3):
+    times, kinds = oracle_sample(w, min(2, w.n_layers), budget_steps)
+    te = [t for t, k in zip(times, kinds) if k]
+    tw = [t for t, k in zip(times, kinds) if not k]
+    te_m = statistics.mean(te) if te else None
+    tw_m = statistics.mean(tw) if tw else None
+    n = n_entry + n_within
+    est = ((n_entry * (te_m or 0)) + (n_within * (tw_m or te_m or 0))) / max(1, n)
+    return {"value": 1.0 / est if est > 0 else None, "unit": "steps/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": (f"first {len(times)} steps of the {w.name} trajectory on {min(2, w.n_layers)} of "
+                       f"{w.n_layers} layers (numpy float64), times x{w.n_layers / min(2, w.n_layers):g}, mixed {n_entry} entry : {n_within} "
+                       f"within-block like the timed GPU steps"),
+            "entry_s_per_step": te_m, "within_s_per_step": tw_m}
+
+
+def run_reference(args, w):
+    """Reference arm: the CPU oracle as it stands, on the same workload and metric."""
+    times, kinds = oracle_sample(w, min(2, w.n_layers), args.steps, warmup=args.warmup)
+    total = sum(times)
+    value = len(times) / total
+    cb = {"value": value, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
+          "sample": f"{len(times)} trajectory steps of {w.name} on {min(2, w.n_layers)} of "
+                    f"{w.n_layers} layers, times x{w.n_layers / min(2, w.n_layers):g}"}
+    return {"impl": "reference", "metric": "calibration steps/s", "value": value, "unit": "steps/s",
+            "n_gpus": 1, "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name}, "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=16)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="polestar", choices=["polestar", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    from drift_aware_kv_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+    init_dist(ws, "nccl")
+    peaks = load_peaks()
+    out = run_device(args, w, peaks, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(w, out["config"]["timed_block_entries"],
+                                               out["config"]["timed_within_block_steps"])
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,29 +1,50 @@
 // tcgen05 (5th-generation tensor core) GEMM for bf16 operands, fp32 output.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <vector>
+#include <unordered_map>
 
 namespace polestar {
 
-struct TcGemmCache {
-  struct Entry {
-    const void* ptr;
-    int rows, cols, ld, box_rows;
-    alignas(64) unsigned char map[128];
-  };
-  std::vector<Entry> maps;
+struct TcMapKey {
+  const void* ptr;
+  int rows, cols, ld, box_rows;
+  bool operator==(const TcMapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows;
+  }
+};
+struct TcMapKeyHash {
+  size_t operator()(const TcMapKey& k) const {
+    size_t h = (size_t)k.ptr;
+    h ^= (size_t)k.rows * 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+    h ^= (size_t)k.cols * 0xC2B2AE3D27D4EB4Full + (h << 6) + (h >> 2);
+    h ^= (size_t)k.ld * 0x165667B19E3779F9ull + (h << 6) + (h >> 2);
+    h ^= (size_t)k.box_rows + (h << 6) + (h >> 2);
+    return h;
+  }
 };
 
-// True when the tensor-core path handles this shape (K and leading dimensions
-// multiples of 64 elements / 16 bytes).
+// Per-context state of the tensor-core GEMM: encoded TMA descriptors (keyed by
+// buffer, shape and box), the device error word of the bounded waits, SM count.
+struct TcGemmCache {
+  std::unordered_map<TcMapKey, CUtensorMap, TcMapKeyHash> maps;
+  int* err = nullptr;
+  int num_sms = 0;
+};
+
+// True when the tensor-core path handles this shape: leading dimensions must
+// give 16-byte aligned rows (multiples of 8 bf16 elements).
 bool tc_gemm_supported(int K, int lda, int ldw);
 
 // C[M, N] (fp32, ldc) = A[M, K] (bf16, lda) * W[N, K]^T (bf16, ldw); rows at or
-// beyond min(M, *m_dev) are neither read meaningfully nor written.
+// beyond min(M, *m_dev) are not written (m_dev may be null).
 cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,
                          int M, const int* m_dev, int N, int K, cudaStream_t st);
+
+// Device word holding the code of the first timed-out wait (0 = none).
+int* tc_error_word(TcGemmCache* cache);
 
 void tc_gemm_cache_clear(TcGemmCache* cache);
 

@@ -79,22 +79,48 @@ __global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
   for (int i = 0; i < NV; ++i) acc[i] = 0.f;
   float mrun = -INFINITY, l_part = 0.f, a_part = 0.f, sq_part = 0.f, e_part = 0.f;
 
+  // K/V tiles are fetched with 16-byte loads, one tile ahead of the compute
+  constexpr int VEC = 16 / sizeof(T);                 // elements per 16-byte chunk
+  constexpr int CPR = DH / VEC;                        // chunks per key row
+  constexpr int PER_T = ATT_TK * CPR / 256;            // chunks per thread per matrix
+  uint4 kreg[PER_T], vreg[PER_T];
+  auto fetch = [&](int j0) {
+#pragma unroll
+    for (int i = 0; i < PER_T; ++i) {
+      const int chunk = threadIdx.x + i * 256;
+      const int kk = chunk / CPR, cv = chunk % CPR;
+      const int j = j0 + kk;
+      if (j < p.N) {
+        const T* rowp = kvbase + (size_t)j * 2 * p.kvdim + kvh * DH + cv * VEC;
+        kreg[i] = __ldg((const uint4*)rowp);
+        vreg[i] = __ldg((const uint4*)(rowp + p.kvdim));
+      } else {
+        kreg[i] = make_uint4(0, 0, 0, 0);
+        vreg[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int i = 0; i < PER_T; ++i) {
+      const int chunk = threadIdx.x + i * 256;
+      const int kk = chunk / CPR, cv = chunk % CPR;
+      const T* kv8 = (const T*)&kreg[i];
+      const T* vv8 = (const T*)&vreg[i];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        Ks[kk * PITCH + cv * VEC + e] = to_f<T>(kv8[e]);
+        Vs[kk * PITCH + cv * VEC + e] = to_f<T>(vv8[e]);
+      }
+    }
+  };
+
+  fetch(0);
   for (int j0 = 0; j0 < p.N; j0 += ATT_TK) {
     __syncthreads();
-    // cooperative K/V tile load -> fp32 shared memory
-    for (int idx = threadIdx.x; idx < ATT_TK * DH; idx += blockDim.x) {
-      const int kk = idx / DH, dd = idx % DH;
-      const int j = j0 + kk;
-      float kv = 0.f, vv = 0.f;
-      if (j < p.N) {
-        const T* rowp = kvbase + (size_t)j * 2 * p.kvdim + kvh * DH + dd;
-        kv = to_f<T>(rowp[0]);
-        vv = to_f<T>(rowp[p.kvdim]);
-      }
-      Ks[kk * PITCH + dd] = kv;
-      Vs[kk * PITCH + dd] = vv;
-    }
+    stash();
     __syncthreads();
+    if (j0 + ATT_TK < p.N) fetch(j0 + ATT_TK);
     if (!live) continue;
     // scores of keys j0+lane and j0+lane+32
     float s[2];
@@ -165,8 +191,278 @@ __global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 path on the tensor cores (mma.sync m16n8k16, fp32 accumulation).
+// One CTA = 4 warps x 16 query rows of one row segment (host work list: a
+// segment never mixes sequences) x one query head.  K/V tiles of 64 keys are
+// double-buffered in shared memory with cp.async; S = Q K^T and O += P V run on
+// the tensor cores with the online softmax and the KL epilogue in registers.
+// ---------------------------------------------------------------------------
+constexpr int AM_TK = 64;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *(const uint32_t*)&v;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
+  constexpr int KP = DH + 8;  // smem pitch (elements): 16-byte rows, conflict-free ldmatrix
+  extern __shared__ __align__(16) __nv_bfloat16 sm_kv[];
+  __nv_bfloat16* Ks = sm_kv;                   // [2][TK][KP]
+  __nv_bfloat16* Vs = Ks + 2 * AM_TK * KP;     // [2][TK][KP]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int4 wk = p.work[blockIdx.x];          // {row_start, row_count, seq, 0}
+  const int seq = wk.z;
+  const int kvh = h / (p.H / p.Hkv);
+  const __nv_bfloat16* kvbase = (const __nv_bfloat16*)p.kv_layer + (size_t)seq * p.kv_seq_stride + kvh * DH;
+
+  const int qr = lane >> 2, qc = lane & 3;     // fragment row / column group
+  const int rl0 = warp * 16 + qr, rl1 = rl0 + 8;
+  const int rows[2] = {wk.x + rl0, wk.x + rl1};
+  bool live[2], outp[2];
+  float* prev[2] = {nullptr, nullptr};
+  float* prev_lse[2] = {nullptr, nullptr};
+  float shift[2] = {0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int rl = i ? rl1 : rl0;
+    int4 m = make_int4(0, 0, ROW_NONE, 0);
+    if (rl < wk.y) m = p.rows[rows[i]];
+    live[i] = m.z != ROW_NONE;
+    outp[i] = live[i] && m.z != ROW_PROXY;
+    if (live[i] && m.z == ROW_PROXY && p.proxy_prev) {
+      const size_t idx = ((size_t)seq * p.K + m.w) * p.H + h;
+      prev[i] = p.proxy_prev + idx * p.N;
+      prev_lse[i] = p.proxy_prev_lse + idx;
+    } else if (live[i] && m.z == ROW_ACTIVE && p.active_prev) {
+      const size_t idx = ((size_t)seq * p.B + m.w) * p.H + h;
+      prev[i] = p.active_prev + idx * p.N;
+      prev_lse[i] = p.active_prev_lse + idx;
+    }
+    if (prev[i] && p.measure) shift[i] = *prev_lse[i];
+  }
+  const bool warp_live = __any_sync(0xffffffffu, live[0] || live[1]);
+
+  // Q fragments (A operand) straight from global memory
+  constexpr int KT = DH / 16;
+  uint32_t qa[KT][4];
+  {
+    const __nv_bfloat16* q0 = (const __nv_bfloat16*)p.q + (size_t)rows[0] * p.ldq + h * DH;
+    const __nv_bfloat16* q1 = (const __nv_bfloat16*)p.q + (size_t)rows[1] * p.ldq + h * DH;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      const int c = kt * 16 + qc * 2;
+      qa[kt][0] = live[0] ? *(const uint32_t*)(q0 + c) : 0u;
+      qa[kt][1] = live[1] ? *(const uint32_t*)(q1 + c) : 0u;
+      qa[kt][2] = live[0] ? *(const uint32_t*)(q0 + c + 8) : 0u;
+      qa[kt][3] = live[1] ? *(const uint32_t*)(q1 + c + 8) : 0u;
+    }
+  }
+
+  auto load_tile = [&](int buf, int j0) {
+    __nv_bfloat16* kd = Ks + buf * AM_TK * KP;
+    __nv_bfloat16* vd = Vs + buf * AM_TK * KP;
+    constexpr int CPR = DH / 8;  // 16-byte chunks per row
+    for (int ch = threadIdx.x; ch < AM_TK * CPR; ch += 128) {
+      const int kk = ch / CPR, cv = ch % CPR;
+      const int j = j0 + kk;
+      const bool v = j < p.N;
+      const __nv_bfloat16* src = kvbase + (size_t)(v ? j : 0) * 2 * p.kvdim + cv * 8;
+      cp_async16(kd + kk * KP + cv * 8, src, v);
+      cp_async16(vd + kk * KP + cv * 8, src + p.kvdim, v);
+    }
+    cp_async_commit();
+  };
+
+  constexpr int NT = DH / 8;  // output n-tiles
+  float acc[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  float mrun[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
+  float asum[2] = {0.f, 0.f}, sqs[2] = {0.f, 0.f}, esum[2] = {0.f, 0.f};
+
+  const int ntiles = (p.N + AM_TK - 1) / AM_TK;
+  load_tile(0, 0);
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    if (t + 1 < ntiles) {
+      load_tile(buf ^ 1, (t + 1) * AM_TK);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const __nv_bfloat16* kt_s = Ks + buf * AM_TK * KP;
+    const __nv_bfloat16* vt_s = Vs + buf * AM_TK * KP;
+    const int j0 = t * AM_TK;
+    if (warp_live) {
+      // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
+      float sc[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kt = 0; kt < KT; kt += 2) {
+          const int mi = lane >> 3, ri = lane & 7;
+          const __nv_bfloat16* ad = kt_s + (nt * 8 + ri) * KP + kt * 16 + (mi & 1) * 8 + (mi >> 1) * 16;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(b0, b1, b2, b3, ad);
+          mma16816(sc[nt], qa[kt], b0, b1);
+          mma16816(sc[nt], qa[kt + 1], b2, b3);
+        }
+      }
+      // scale, mask, online softmax
+      float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = j0 + nt * 8 + qc * 2 + (e & 1);
+          sc[nt][e] = (j < p.N) ? sc[nt][e] * p.scale : -INFINITY;
+          tmax[e >> 1] = fmaxf(tmax[e >> 1], sc[nt][e]);
+        }
+      }
+      float corr[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
+        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
+        const float mnew = fmaxf(mrun[i], tmax[i]);
+        corr[i] = expf(mrun[i] - mnew);
+        mrun[i] = mnew;
+        lsum[i] *= corr[i];
+        asum[i] *= corr[i];
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[nt][0] *= corr[0];
+        acc[nt][1] *= corr[0];
+        acc[nt][2] *= corr[1];
+        acc[nt][3] *= corr[1];
+      }
+      uint32_t pa[4][4];  // P as A fragments: 4 k-steps of 16 keys
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = e >> 1;
+          const int j = j0 + nt * 8 + qc * 2 + (e & 1);
+          pv[e] = (j < p.N) ? expf(sc[nt][e] - mrun[i]) : 0.f;
+          lsum[i] += pv[e];
+          if (prev[i] && j < p.N) {
+            if (p.measure) {
+              const float sp = prev[i][j];
+              const float dj = sc[nt][e] - sp;
+              const float qt = expf(sp - shift[i]);
+              asum[i] += pv[e] * dj;
+              sqs[i] += qt;
+              esum[i] += qt * expm1f(dj);
+            }
+            if (p.store) prev[i][j] = sc[nt][e];
+          }
+        }
+        const int kt = nt >> 1;
+        if ((nt & 1) == 0) {
+          pa[kt][0] = pack_bf16(pv[0], pv[1]);
+          pa[kt][1] = pack_bf16(pv[2], pv[3]);
+        } else {
+          pa[kt][2] = pack_bf16(pv[0], pv[1]);
+          pa[kt][3] = pack_bf16(pv[2], pv[3]);
+        }
+      }
+      // O += P V
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt += 2) {
+          const int mi = lane >> 3, ri = lane & 7;
+          const __nv_bfloat16* ad = vt_s + (kt * 16 + (mi & 1) * 8 + ri) * KP + (nt + (mi >> 1)) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(b0, b1, b2, b3, ad);
+          mma16816(acc[nt], pa[kt], b0, b1);
+          mma16816(acc[nt + 1], pa[kt], b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // finalize: row sums across the 4 threads sharing a row
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], o);
+      asum[i] += __shfl_xor_sync(0xffffffffu, asum[i], o);
+      sqs[i] += __shfl_xor_sync(0xffffffffu, sqs[i], o);
+      esum[i] += __shfl_xor_sync(0xffffffffu, esum[i], o);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (outp[i]) {
+      __nv_bfloat16* o = (__nv_bfloat16*)p.out + (size_t)rows[i] * p.ldo + h * DH;
+      const float inv = 1.f / lsum[i];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *(uint32_t*)(o + nt * 8 + qc * 2) = pack_bf16(acc[nt][2 * i] * inv, acc[nt][2 * i + 1] * inv);
+    }
+    if (prev[i] && qc == 0) {
+      if (p.measure) p.kl_out[(size_t)rows[i] * p.H + h] = asum[i] / lsum[i] - log1pf(esum[i] / sqs[i]);
+      if (p.store) *prev_lse[i] = mrun[i] + logf(lsum[i]);
+    }
+  }
+}
+
 template <typename T>
 void launch_row_attention(const AttnArgs& a, cudaStream_t st) {
+  if (sizeof(T) == 2 && a.work) {
+    const dim3 grid(a.n_work, a.H);
+    if (a.dh == 128) {
+      const size_t sm = 4 * AM_TK * (128 + 8) * sizeof(__nv_bfloat16);
+      static bool cfg = false;
+      if (!cfg) {
+        cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        cfg = true;
+      }
+      attn_mma_kernel<128><<<grid, 128, sm, st>>>(a);
+    } else {
+      const size_t sm = 4 * AM_TK * (64 + 8) * sizeof(__nv_bfloat16);
+      attn_mma_kernel<64><<<grid, 128, sm, st>>>(a);
+    }
+    return;
+  }
   const dim3 grid((a.R + ATT_ROWS - 1) / ATT_ROWS, a.H);
   if (a.dh == 128) {
     const size_t sm = (2 * ATT_TK * 129 + ATT_ROWS * 128 + ATT_ROWS * ATT_TK) * sizeof(float);

@@ -56,6 +56,10 @@ struct AttnArgs {
   int measure;             // 1: write KL(new || prev) to kl_out[r, h]
   int store;               // 1: replace prev by the new scores
   float* kl_out;           // [R, H]
+  // bf16 tensor-core path: CTA work list {row_start, row_count <= 64, seq, 0};
+  // a work item never spans two sequences (nullptr: CUDA-core path by rows)
+  const int4* work;
+  int n_work;
 };
 template <typename T>
 void launch_row_attention(const AttnArgs& a, cudaStream_t st);

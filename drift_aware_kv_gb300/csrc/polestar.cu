@@ -36,8 +36,16 @@ thread_local std::string g_init_error;
 size_t pad8(size_t x) { return (x + 7) & ~size_t(7); }
 
 struct MetaLayout {
-  size_t rows_off, prow_off, win_row_off, proxy_row_off, fire_seqs_off, win_pos_off, fire_off, total;
+  size_t rows_off, prow_off, win_row_off, proxy_row_off, fire_seqs_off, win_pos_off, fire_off, work_off, total;
+  int work_cap;
 };
+
+// Attention work items {row_start, row_count <= 64, seq, 0} covering the rows
+// [start, start + count) of one sequence.
+int push_work(int4* w, int n, int start, int count, int seq) {
+  for (int k = 0; k < count; k += 64) w[n++] = make_int4(start + k, std::min(64, count - k), seq, 0);
+  return n;
+}
 }  // namespace
 
 struct polestar_ctx {
@@ -99,6 +107,17 @@ struct polestar_ctx {
   std::vector<void*> host_allocs;
 
   TcGemmCache tc;
+
+  // live per-kernel timing
+  struct ProfRec {
+    int cls;
+    double bytes, flops;
+  };
+  bool prof_armed = false;
+  int prof_cap = 0, prof_used = 0, gemm_cls = POLESTAR_KC_GEMM_STEP;
+  std::vector<cudaEvent_t> prof_ev;
+  std::vector<ProfRec> prof_rec;
+  uint64_t prof_dropped[POLESTAR_KC_COUNT] = {};
 };
 
 namespace {
@@ -160,6 +179,41 @@ polestar_status halloc(polestar_ctx* c, P** p, size_t bytes) {
     if (s_ != POLESTAR_OK) return s_;      \
   } while (0)
 
+int prof_start(polestar_ctx* c, int cls) {
+  if (!c->prof_armed) return -1;
+  if (c->prof_used >= c->prof_cap) {
+    ++c->prof_dropped[cls];
+    return -1;
+  }
+  const int i = c->prof_used++;
+  cudaEventRecord(c->prof_ev[2 * i], c->sm);
+  c->prof_rec[i] = {cls, 0.0, 0.0};
+  return i;
+}
+
+void prof_stop(polestar_ctx* c, int i, double bytes, double flops) {
+  if (i < 0) return;
+  cudaEventRecord(c->prof_ev[2 * i + 1], c->sm);
+  c->prof_rec[i].bytes = bytes;
+  c->prof_rec[i].flops = flops;
+}
+
+void prof_release(polestar_ctx* c) {
+  for (cudaEvent_t e : c->prof_ev) cudaEventDestroy(e);
+  c->prof_ev.clear();
+  c->prof_rec.clear();
+  c->prof_armed = false;
+  c->prof_cap = c->prof_used = 0;
+}
+
+#define RUN(cls, bytes, flops, stmt)        \
+  do {                                      \
+    const int pi_ = prof_start(c, (cls));   \
+    stmt;                                   \
+    prof_stop(c, pi_, (bytes), (flops));    \
+    LAUNCHED(c);                            \
+  } while (0)
+
 void free_all(polestar_ctx* c) {
   if (c->sm) cudaStreamSynchronize(c->sm);
   if (c->ss && c->ss != c->sm) cudaStreamSynchronize(c->ss);
@@ -172,6 +226,7 @@ void free_all(polestar_ctx* c) {
   if (c->main_ev) cudaEventDestroy(c->main_ev);
   c->meta_ev = c->side_ev = c->main_ev = nullptr;
   tc_gemm_cache_clear(&c->tc);
+  prof_release(c);
 }
 
 std::string validate(const polestar_config* c) {
@@ -195,8 +250,9 @@ std::string validate(const polestar_config* c) {
   return "";
 }
 
-MetaLayout meta_layout(int rows_cap, int b, int K, int Wmax) {
+MetaLayout meta_layout(int rows_cap, int b, int K, int Wmax, int N) {
   MetaLayout m{};
+  m.work_cap = b * (N / 64 + 2) + b * ((Wmax + K + 7) / 64 + 2) + 2 * b + 64;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t r = o;
@@ -210,6 +266,7 @@ MetaLayout meta_layout(int rows_cap, int b, int K, int Wmax) {
   m.fire_seqs_off = take(sizeof(int) * b);
   m.win_pos_off = take(sizeof(int) * Wmax);
   m.fire_off = take(b);
+  m.work_off = take(sizeof(int4) * m.work_cap);
   m.total = o;
   return m;
 }
@@ -235,14 +292,17 @@ template <typename T>
 polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int ldw, float* C, int ldc, int M,
                      const int* m_dev, int N, int K) {
   if (M <= 0) return POLESTAR_OK;
+  const double bytes = ((double)N * K + (double)M * K) * sizeof(T) + (double)M * N * 4.0;
+  const double flops = 2.0 * M * N * K;
   if (sizeof(T) == 2 && tc_gemm_supported(K, lda, ldw)) {
+    const int pi = prof_start(c, c->gemm_cls);
     cudaError_t e = tc_gemm_bf16(&c->tc, A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm);
+    prof_stop(c, pi, bytes, flops);
     ++c->launches;
     if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 gemm: ") + cudaGetErrorString(e));
     return POLESTAR_OK;
   }
-  launch_gemm_simt<T>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm);
-  LAUNCHED(c);
+  RUN(c->gemm_cls, bytes, flops, (launch_gemm_simt<T>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm)));
   return POLESTAR_OK;
 }
 
@@ -262,6 +322,7 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
     for (int p = 0; p < N; ++p)
       if (in[p]) E.push_back(p);
   }
+  c->gemm_cls = POLESTAR_KC_GEMM_ENTRY;
   const int per_seq = (int)pad8(E.size());
   const int chunk = std::max(1, std::min(b, c->Rmax / per_seq));
   // host metadata: rows of all sequences, proxy rows, window positions
@@ -293,8 +354,23 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
   for (size_t i = (size_t)b * c->K; i < pad8((size_t)b * c->K); ++i) prow_h[i] = make_int4(b - 1, 0, ROW_NONE, 0);
   int* wp = meta_h<int>(c, c->ml.win_pos_off);
   for (int i = 0; i < c->nw; ++i) wp[i] = c->win_pos[i];
+  // attention work lists: per chunk (row offsets relative to the chunk), then proxies
+  int4* work_h = meta_h<int4>(c, c->ml.work_off);
+  int nwk = 0;
+  std::vector<int> chunk_work_off, chunk_work_n;
+  for (int s0 = 0; s0 < b; s0 += chunk) {
+    const int ns = std::min(chunk, b - s0);
+    chunk_work_off.push_back(nwk);
+    for (int i = 0; i < ns; ++i) nwk = push_work(work_h, nwk, i * per_seq, (int)E.size(), s0 + i);
+    chunk_work_n.push_back(nwk - chunk_work_off.back());
+  }
+  const int proxy_work_off = nwk;
+  for (int s = 0; s < b; ++s) nwk = push_work(work_h, nwk, s * c->K, c->K, s);
+  const int proxy_work_n = nwk - proxy_work_off;
+  if (nwk > c->ml.work_cap) return fail(c, POLESTAR_ERR_UNSUPPORTED, "attention work list overflow");
   CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
   CUDA_OR_FAIL(c, cudaEventRecord(c->meta_ev, c->sm));
+  const int4* work_d = meta_d<int4>(c, c->ml.work_off);
 
   const size_t kv_layer = (size_t)b * N * 2 * c->kvdim;
   const size_t kv_seq = (size_t)N * 2 * c->kvdim;
@@ -302,25 +378,21 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
   const float eps = c->cfg.rms_eps;
   const int4* rows_all = meta_d<int4>(c, c->ml.rows_off);
 
-  for (int s0 = 0; s0 < b; s0 += chunk) {
+  for (int s0 = 0, ci = 0; s0 < b; s0 += chunk, ++ci) {
     const int ns = std::min(chunk, b - s0);
     const int R = ns * per_seq;
     const int4* rows = rows_all + (size_t)s0 * per_seq;
-    launch_gather_input<T>(x0, rows, R, N, d, c->h_rows, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_input<T>(x0, rows, R, N, d, c->h_rows, c->sm)));
     for (int l = 0; l < L; ++l) {
       const polestar_layer_weights& w = c->W[l];
-      launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
-                            (size_t)c->Wmax * d, c->sm);
-      LAUNCHED(c);
-      launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm);
-      LAUNCHED(c);
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
+                            (size_t)c->Wmax * d, c->sm)));
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
       TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, R, nullptr, c->qdim, d));
       TRY(gemm<T>(c, c->a_in, d, w.wk, d, c->gout + c->qdim, c->ldg, R, nullptr, c->kvdim, d));
       TRY(gemm<T>(c, c->a_in, d, w.wv, d, c->gout + c->qdim + c->kvdim, c->ldg, R, nullptr, c->kvdim, d));
-      launch_rope_scatter<T>(c->gout, c->ldg, rows, nullptr, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
-                             kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm);
-      LAUNCHED(c);
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, rows, nullptr, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
+                             kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm)));
       AttnArgs aa{};
       aa.q = c->q_rows;
       aa.ldq = c->qdim;
@@ -339,25 +411,25 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       aa.out = c->attn_out;
       aa.ldo = c->qdim;
       aa.other_live = 1;
+      aa.work = work_d + chunk_work_off[ci];
+      aa.n_work = chunk_work_n[ci];
       if (l == L - 1) {
         aa.active_prev = c->aprev;
         aa.active_prev_lse = c->aprev_lse;
         aa.store = 1;
       }
-      launch_row_attention<T>(aa, c->sm);
-      LAUNCHED(c);
+      const double attn_bytes = (double)ns * N * 2 * c->kvdim * c->esz +
+                                (l == L - 1 ? (double)ns * c->B * c->H * N * 4.0 : 0.0);
+      RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
       TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
-      launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
-                                 c->a_in, c->sm);
-      LAUNCHED(c);
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
+                                 c->a_in, c->sm)));
       TRY(gemm<T>(c, c->a_in, d, w.w_gate, d, c->gout, c->ldg, R, nullptr, c->F, d));
       TRY(gemm<T>(c, c->a_in, d, w.w_up, d, c->gout + c->F, c->ldg, R, nullptr, c->F, d));
-      launch_swiglu<T>(c->gout, c->ldg, nullptr, R, c->F, c->a_in, c->sm);
-      LAUNCHED(c);
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, nullptr, R, c->F, c->a_in, c->sm)));
       TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, R, nullptr, d, c->F));
-      launch_residual_scatter(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows, nullptr,
-                              c->sm);
-      LAUNCHED(c);
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_scatter(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows, nullptr,
+                              c->sm)));
     }
   }
   // spherical K-means + residual NVFP4 for every (layer, sequence)
@@ -378,20 +450,17 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
   ka.anchor = c->anchor;
   ka.codes = c->codes;
   ka.scales = c->scales;
-  launch_kmeans_encode(ka, c->sm);
-  LAUNCHED(c);
+  RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_kmeans_encode(ka, c->sm)));
   // proxy-attention baseline P(t_b, l) of every layer
   const int Rp = (int)pad8((size_t)b * c->K);
   const int4* prow = meta_d<int4>(c, c->ml.prow_off);
   for (int l = 0; l < L; ++l) {
     const polestar_layer_weights& w = c->W[l];
-    launch_rmsnorm<T>(nullptr, nullptr, nullptr, prow, c->z + (size_t)l * b * c->K * d, c->K, w.attn_norm, Rp, d,
-                      eps, c->a_in, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(nullptr, nullptr, nullptr, prow, c->z + (size_t)l * b * c->K * d, c->K, w.attn_norm, Rp, d,
+                      eps, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, Rp, nullptr, c->qdim, d));
-    launch_rope_scatter<T>(c->gout, c->ldg, prow, nullptr, Rp, c->H, c->Hkv, c->dh, c->rope, c->q_rows, nullptr,
-                           0, c->kvdim, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, prow, nullptr, Rp, c->H, c->Hkv, c->dh, c->rope, c->q_rows, nullptr,
+                           0, c->kvdim, c->sm)));
     AttnArgs aa{};
     aa.q = c->q_rows;
     aa.ldq = c->qdim;
@@ -412,8 +481,10 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
     aa.proxy_prev = c->pprev + (size_t)l * b * c->K * c->H * N;
     aa.proxy_prev_lse = c->pprev_lse + (size_t)l * b * c->K * c->H;
     aa.store = 1;
-    launch_row_attention<T>(aa, c->sm);
-    LAUNCHED(c);
+    aa.work = work_d + proxy_work_off;
+    aa.n_work = proxy_work_n;
+    const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz + (double)b * c->K * c->H * N * 4.0;
+    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
   }
   std::fill(c->cum.begin(), c->cum.end(), 0);
   std::fill(c->fire.begin(), c->fire.end(), 0);
@@ -437,6 +508,7 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     }
   }
   const int n_fire = (int)fire_seqs.size();
+  c->gemm_cls = POLESTAR_KC_GEMM_STEP;
   // row space: active rows of every sequence, then per refreshing sequence its
   // window rows and its K proxy rows (padded to 8)
   int4* rows_h = meta_h<int4>(c, c->ml.rows_off);
@@ -463,6 +535,14 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     while (R % 8) rows_h[R++] = make_int4(s, 0, ROW_NONE, 0);
   }
   for (int i = 0; i < c->nw; ++i) wp[i] = c->win_pos[i];
+  int4* work_h = meta_h<int4>(c, c->ml.work_off);
+  int nwk = 0;
+  for (int s = 0; s < b; ++s) nwk = push_work(work_h, nwk, s * B, B, s);
+  for (int f = 0; f < n_fire; ++f) {
+    const int s = fire_seqs[f];
+    nwk = push_work(work_h, nwk, win_row[s], c->nw + c->K, s);
+  }
+  if (nwk > c->ml.work_cap) return fail(c, POLESTAR_ERR_UNSUPPORTED, "attention work list overflow");
   CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
   CUDA_OR_FAIL(c, cudaEventRecord(c->meta_ev, c->sm));
   const int4* rows = meta_d<int4>(c, c->ml.rows_off);
@@ -476,14 +556,12 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
   const float eps = c->cfg.rms_eps;
   const int n_active = b * B;
 
-  launch_gather_input<T>(x0, rows, n_active, N, d, c->h_rows, c->sm);
-  LAUNCHED(c);
+  RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_input<T>(x0, rows, n_active, N, d, c->h_rows, c->sm)));
   uint8_t* sel_prev = c->sel_a;
   uint8_t* sel_cur = c->sel_b;
   if (n_fire > 0) {
-    launch_gather_window<T>(x0, meta_d<int>(c, c->ml.win_pos_off), c->nw, fire_d, n_fire, N, d, c->Wmax, c->U,
-                            sel_prev, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_window<T>(x0, meta_d<int>(c, c->ml.win_pos_off), c->nw, fire_d, n_fire, N, d, c->Wmax, c->U,
+                            sel_prev, c->sm)));
   }
   for (int l = 0; l < L; ++l) {
     const polestar_layer_weights& w = c->W[l];
@@ -508,19 +586,15 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       pa.dn = c->dn;
       pa.csum = c->csum + (size_t)l * b * c->K * d;
       pa.z = zl;
-      launch_window_patch(pa, c->sm);
-      LAUNCHED(c);
-      launch_centroid_update(pa, c->sm);
-      LAUNCHED(c);
+      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_window_patch(pa, c->sm)));
+      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_centroid_update(pa, c->sm)));
     }
-    launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, zl, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, zl, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, R, nullptr, c->qdim, d));
     TRY(gemm<T>(c, c->a_in, d, w.wk, d, c->gout + c->qdim, c->ldg, R, nullptr, c->kvdim, d));
     TRY(gemm<T>(c, c->a_in, d, w.wv, d, c->gout + c->qdim + c->kvdim, c->ldg, R, nullptr, c->kvdim, d));
-    launch_rope_scatter<T>(c->gout, c->ldg, rows, c->write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
-                           kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, rows, c->write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
+                           kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm)));
     AttnArgs aa{};
     aa.q = c->q_rows;
     aa.ldq = c->qdim;
@@ -548,8 +622,12 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     aa.measure = 1;
     aa.store = 1;
     aa.kl_out = c->kl_rows;
-    launch_row_attention<T>(aa, c->sm);
-    LAUNCHED(c);
+    aa.work = meta_d<int4>(c, c->ml.work_off);
+    aa.n_work = nwk;
+    const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz +
+                              (double)n_fire * c->K * c->H * N * 8.0 +
+                              (l == L - 1 ? (double)b * B * c->H * N * 8.0 : 0.0);
+    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
     SelectArgs sa{};
     sa.batch = b;
     sa.Wmax = c->Wmax;
@@ -569,28 +647,23 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     sa.o_src = c->o_src;
     sa.m_o = c->m_o;
     sa.n_active = n_active;
-    launch_select(sa, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_SELECT, 0.0, 0.0, (launch_select(sa, c->sm)));
     if (l == L - 1) {
-      launch_delta_finalize(c->kl_rows, b, B, c->H, c->delta, c->sm);
-      LAUNCHED(c);
+      RUN(POLESTAR_KC_SELECT, 0.0, 0.0, (launch_delta_finalize(c->kl_rows, b, B, c->H, c->delta, c->sm)));
     }
     // gathered O/FFN over active rows + selected window rows
     const int Rc = n_active + n_fire * c->nw;
     launch_gather_T<T>(c->attn_out, c->o_src, c->m_o, Rc, c->qdim, c->a_in, c->sm);
     LAUNCHED(c);
     TRY(gemm<T>(c, c->a_in, c->qdim, w.wo, c->qdim, c->gout, c->ldg, Rc, c->m_o, d, c->qdim));
-    launch_residual_rmsnorm<T>(c->h_rows, c->o_src, c->m_o, Rc, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
-                               c->a_in, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, c->o_src, c->m_o, Rc, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
+                               c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, d, w.w_gate, d, c->gout, c->ldg, Rc, c->m_o, c->F, d));
     TRY(gemm<T>(c, c->a_in, d, w.w_up, d, c->gout + c->F, c->ldg, Rc, c->m_o, c->F, d));
-    launch_swiglu<T>(c->gout, c->ldg, c->m_o, Rc, c->F, c->a_in, c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, c->m_o, Rc, c->F, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, Rc, c->m_o, d, c->F));
-    launch_residual_scatter(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows, c->U,
-                            c->sm);
-    LAUNCHED(c);
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_scatter(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows, c->U,
+                            c->sm)));
     std::swap(sel_prev, sel_cur);
   }
   c->sel_last = sel_prev;  // selection of the last layer
@@ -712,7 +785,7 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
     TRY(dalloc(c, &c->commit_dev, (size_t)b * 2 * B));
     c->csplits = std::max(1, std::min(32, (2 * 152 + b * 2 * B - 1) / (b * 2 * B)));
     TRY(dalloc(c, &c->cpart, sizeof(float) * 2 * (size_t)b * 2 * B * c->csplits));
-    c->ml = meta_layout(c->rows_cap, b, K, Wmax);
+    c->ml = meta_layout(c->rows_cap, b, K, Wmax, N);
     TRY(halloc(c, &c->meta_h, c->ml.total));
     TRY(dalloc(c, &c->meta_d, c->ml.total));
     if (cfg->host_offload) {
@@ -806,7 +879,9 @@ extern "C" polestar_status polestar_commit(polestar_ctx* c, const float* logits,
   a.conf_user = conf;
   a.drel = c->drel;
   a.taud = c->taud;
+  const int pi = prof_start(c, POLESTAR_KC_COMMIT);
   launch_commit(a, c->sm);
+  prof_stop(c, pi, (double)c->b * 2 * c->B * vocab * 4.0, 0.0);
   c->launches += 2;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("commit launch: ") + cudaGetErrorString(e));
@@ -891,4 +966,65 @@ extern "C" polestar_status polestar_debug_read(polestar_ctx* c, int32_t which, i
   CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
   CUDA_OR_FAIL(c, cudaMemcpy(host_dst, src, bytes, cudaMemcpyDeviceToHost));
   return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_profile_begin(polestar_ctx* c, int32_t capacity) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (capacity < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "capacity must be >= 1");
+  CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  prof_release(c);
+  c->prof_ev.resize(2 * (size_t)capacity);
+  for (size_t i = 0; i < c->prof_ev.size(); ++i) {
+    cudaError_t e = cudaEventCreate(&c->prof_ev[i]);
+    if (e != cudaSuccess) {
+      c->prof_ev.resize(i);
+      prof_release(c);
+      return fail(c, POLESTAR_ERR_CUDA, std::string("cudaEventCreate: ") + cudaGetErrorString(e));
+    }
+  }
+  c->prof_rec.assign(capacity, {0, 0.0, 0.0});
+  c->prof_cap = capacity;
+  c->prof_used = 0;
+  for (auto& d : c->prof_dropped) d = 0;
+  c->prof_armed = true;
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_profile_end(polestar_ctx* c, polestar_kernel_stats* out, int32_t n_classes) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!c->prof_armed) return fail(c, POLESTAR_ERR_STATE, "profiling is not armed");
+  if (!out || n_classes < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "bad output array");
+  CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  for (int k = 0; k < n_classes; ++k) out[k] = polestar_kernel_stats{0, 0.0, 0.0, 0.0, 0};
+  for (int i = 0; i < c->prof_used; ++i) {
+    const auto& r = c->prof_rec[i];
+    if (r.cls >= n_classes) continue;
+    float ms = 0.f;
+    CUDA_OR_FAIL(c, cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]));
+    out[r.cls].launches += 1;
+    out[r.cls].ms += ms;
+    out[r.cls].bytes += r.bytes;
+    out[r.cls].flops += r.flops;
+  }
+  for (int k = 0; k < n_classes && k < POLESTAR_KC_COUNT; ++k) out[k].dropped = c->prof_dropped[k];
+  prof_release(c);
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const void* W, int32_t ldw, float* C,
+                                               int32_t ldc, int32_t M, const int32_t* m_dev, int32_t N, int32_t K,
+                                               int32_t dtype, int32_t path, void* stream) {
+  static TcGemmCache cache;
+  if (!A || !W || !C || M < 0 || N < 1 || K < 1) return POLESTAR_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (path == 1) {
+    if (dtype != POLESTAR_BF16 || !tc_gemm_supported(K, lda, ldw)) return POLESTAR_ERR_UNSUPPORTED;
+    return tc_gemm_bf16(&cache, A, lda, W, ldw, C, ldc, M, m_dev, N, K, st) == cudaSuccess ? POLESTAR_OK
+                                                                                           : POLESTAR_ERR_CUDA;
+  }
+  if (dtype == POLESTAR_BF16)
+    launch_gemm_simt<__nv_bfloat16>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, st);
+  else
+    launch_gemm_simt<float>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, st);
+  return cudaGetLastError() == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }

@@ -21,7 +21,9 @@ FP32, BF16 = 0, 1
  BUF_SELECTED, BUF_DELTA) = range(18)
 
 EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
-            "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read")
+            "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
+            "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm")
+KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows")
 
 
 class polestar_config(C.Structure):
@@ -44,6 +46,11 @@ class polestar_step_out(C.Structure):
     _fields_ = [("drift", C.c_void_p), ("topk", C.c_void_p), ("selected", C.c_void_p),
                 ("labels", C.c_void_p), ("delta", C.c_void_p), ("fire", C.POINTER(C.c_uint8)),
                 ("win_len", C.c_int32), ("win_max", C.c_int32)]
+
+
+class polestar_kernel_stats(C.Structure):
+    _fields_ = [("launches", C.c_uint64), ("ms", C.c_double), ("bytes", C.c_double),
+                ("flops", C.c_double), ("dropped", C.c_uint64)]
 
 
 _lib = None
@@ -71,8 +78,13 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_launch_count.argtypes = [P]
     lib.polestar_launch_count.restype = C.c_uint64
     lib.polestar_debug_read.argtypes = [P, C.c_int32, C.c_int32, P, C.c_size_t]
+    lib.polestar_debug_gemm.argtypes = [P, C.c_int32, P, C.c_int32, P, C.c_int32, C.c_int32, P, C.c_int32,
+                                        C.c_int32, C.c_int32, C.c_int32, P]
+    lib.polestar_debug_gemm.restype = C.c_int
+    lib.polestar_profile_begin.argtypes = [P, C.c_int32]
+    lib.polestar_profile_end.argtypes = [P, C.POINTER(polestar_kernel_stats), C.c_int32]
     for f in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
-              "polestar_debug_read"):
+              "polestar_debug_read", "polestar_profile_begin", "polestar_profile_end"):
         getattr(lib, f).restype = C.c_int
     _lib = lib
     return lib
@@ -170,3 +182,28 @@ class Polestar:
         _check(self.lib.polestar_debug_read(self.ctx, which, layer, C.c_void_p(out.data_ptr()),
                                             out.numel() * out.element_size()), self.ctx)
         return out
+
+    def profile_begin(self, capacity: int):
+        _check(self.lib.polestar_profile_begin(self.ctx, int(capacity)), self.ctx)
+
+    def profile_end(self) -> Dict[str, dict]:
+        arr = (polestar_kernel_stats * len(KERNEL_CLASSES))()
+        _check(self.lib.polestar_profile_end(self.ctx, arr, len(KERNEL_CLASSES)), self.ctx)
+        return {name: dict(launches=int(a.launches), ms=float(a.ms), bytes=float(a.bytes),
+                           flops=float(a.flops), dropped=int(a.dropped))
+                for name, a in zip(KERNEL_CLASSES, arr)}
+
+
+def debug_gemm(A, W, out, path: int, m_dev=None, stream=None):
+    """out = A @ W^T through the library's projection kernel (path 0 CUDA cores,
+    1 tcgen05).  torch CUDA tensors, row-major with unit inner stride."""
+    import torch
+    lib = load()
+    M, K = A.shape
+    N = W.shape[0]
+    st = stream if stream is not None else torch.cuda.current_stream()
+    dt = BF16 if A.dtype == torch.bfloat16 else FP32
+    _check(lib.polestar_debug_gemm(C.c_void_p(A.data_ptr()), A.stride(0), C.c_void_p(W.data_ptr()), W.stride(0),
+                                   C.c_void_p(out.data_ptr()), out.stride(0), M,
+                                   C.c_void_p(m_dev.data_ptr()) if m_dev is not None else None, N, K, dt,
+                                   path, C.c_void_p(st.cuda_stream)))

@@ -153,6 +153,47 @@ const char *polestar_last_error(const polestar_ctx *ctx);
 /* Number of kernel launches issued on this context since init (diagnostics). */
 uint64_t polestar_launch_count(const polestar_ctx *ctx);
 
+/* ---- live per-kernel timing (CUDA events on the launching stream) ----
+ * polestar_profile_begin arms up to `capacity` timed launches (event pairs are
+ * recorded around each kernel launch of the classes below until the capacity
+ * is used up); polestar_profile_end synchronises the main stream, fills
+ * out[0 .. n_classes-1] (indexed by polestar_kernel_class) and disarms.
+ * Bytes and flops are the algorithmic figures of each launch: for GEMMs the
+ * weight, A-operand and output bytes and 2*M*N*K, with M the launch's row
+ * bound. */
+typedef enum {
+  POLESTAR_KC_GEMM_STEP = 0,  /* projections of within-block steps           */
+  POLESTAR_KC_GEMM_ENTRY = 1, /* projections of block-entry forwards          */
+  POLESTAR_KC_ATTENTION = 2,  /* row attention + KL drift                     */
+  POLESTAR_KC_CLUSTER = 3,    /* K-means/NVFP4, window patch, centroid update */
+  POLESTAR_KC_SELECT = 4,     /* top-k + compaction, delta                    */
+  POLESTAR_KC_COMMIT = 5,     /* confidence + commit gate                     */
+  POLESTAR_KC_ROWS = 6,       /* norms, rotary/scatter, residuals, gathers    */
+  POLESTAR_KC_COUNT = 7
+} polestar_kernel_class;
+
+typedef struct {
+  uint64_t launches;   /* timed launches                     */
+  double ms;           /* summed event-measured duration     */
+  double bytes;        /* summed algorithmic bytes           */
+  double flops;        /* summed algorithmic flops           */
+  uint64_t dropped;    /* launches not timed (capacity full) */
+} polestar_kernel_stats;
+
+polestar_status polestar_profile_begin(polestar_ctx *ctx, int32_t capacity);
+polestar_status polestar_profile_end(polestar_ctx *ctx, polestar_kernel_stats *out, int32_t n_classes);
+
+/* ---- projection kernel on caller buffers (test hook) ----
+ * C[M, N] (fp32, row stride ldc) = A[M, K] (row stride lda) * W[N, K]^T (row
+ * stride ldw), A and W in `dtype`, all device pointers, on `stream`.
+ * path 0: CUDA-core kernel; path 1: tcgen05 tensor-core kernel (bf16 only).
+ * m_dev (device int, may be NULL) lowers the row count on the device: rows at
+ * or beyond min(M, *m_dev) are left untouched.  Asynchronous; returns
+ * UNSUPPORTED for a path/dtype/stride combination the kernels do not cover. */
+polestar_status polestar_debug_gemm(const void *A, int32_t lda, const void *W, int32_t ldw, float *C,
+                                    int32_t ldc, int32_t M, const int32_t *m_dev, int32_t N, int32_t K,
+                                    int32_t dtype, int32_t path, void *stream);
+
 /* ---- inspection (used by parity tests; synchronises the main stream) ---- */
 typedef enum {
   POLESTAR_BUF_KV = 0,        /* layer l: [batch, N, 2, Hkv*dh] config dtype        */

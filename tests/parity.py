@@ -4,10 +4,13 @@ oracle on the same seeded trajectory and compares every step.
 Exactness bar: cluster ids, top-k sets, selected rows, NVFP4 codes/scales and
 commit masks are compared exactly; a mismatch is accepted only when the
 oracle's decision margin is below NEAR_TIE (a near tie), and is then counted.
-After a near-tie divergence the two trajectories legitimately differ, so the
-comparison stops at that step.  Floating-point outputs use the tolerances
-below (KL drift 1e-5 abs + 1e-3 rel; K/V, hidden states and update packets by
-relative L2 error)."""
+After a near-tie divergence the two states legitimately differ.  Both engines
+keep running on the same inputs, and comparison resumes at the next block
+entry with an even block index: that entry recomputes every position's K/V,
+the window cache, centroids, proxy baselines and histories from x0 alone, so
+the states coincide again without taking anything from the GPU side.
+Floating-point outputs use the tolerances below (KL drift 1e-5 abs + 1e-3
+rel; K/V, hidden states and update packets by relative L2 error)."""
 from __future__ import annotations
 
 import dataclasses
@@ -42,6 +45,7 @@ def unpack_codes(packed):
 @dataclasses.dataclass
 class Report:
     steps: int = 0
+    compared: int = 0
     near_ties: int = 0
     diverged_at: int = -1
     max_kv_err: float = 0.0
@@ -68,6 +72,7 @@ class Lockstep:
         self.lib = P.Polestar(w, self.Wg)
         self.tr = synth.Trajectory(w)
         self.rep = Report()
+        self.diverged = False
         self.N = w.seq_len
         self.Wmax = w.prefix_win + w.suffix_win
 
@@ -82,23 +87,31 @@ class Lockstep:
             if st is None or (max_steps is not None and rep.steps >= max_steps):
                 break
             x0 = st["x0"].to(dt)
+            if self.diverged and st["block_entry"] and st["block_index"] % 2 == 0:
+                self.diverged = False  # full refresh: both states are functions of x0 again
             recs = self.orc.calibrate_step(x0.double().numpy(), st["n_unmasked"], st["block_index"],
                                            st["block_entry"])
             xg = x0.cuda()
             out = self.lib.calibrate_step(xg, st["n_unmasked"], st["block_index"], st["block_entry"])
             torch.cuda.synchronize()
-            ok = self._compare_step(st, recs, out)
+            ok = True
+            if not self.diverged:
+                ok = self._compare_step(st, recs, out)
             coms = self.orc.commit(st["logits"].numpy(), st["masked"].numpy())
             lg = st["logits"].cuda()
             mk = st["masked"].to(torch.uint8).cuda()
             cm = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device="cuda")
             self.lib.commit(lg, mk, cm)
             torch.cuda.synchronize()
-            ok = ok and self._compare_commit(st, coms, cm.cpu().numpy())
+            if not self.diverged:
+                ok = ok and self._compare_commit(st, coms, cm.cpu().numpy())
+                if ok:
+                    rep.compared += 1
             rep.steps += 1
             if not ok:
-                rep.diverged_at = st["t"]
-                break
+                if rep.diverged_at < 0:
+                    rep.diverged_at = st["t"]
+                self.diverged = True
         return rep
 
     # ------------------------------------------------------------------
@@ -154,8 +167,9 @@ class Lockstep:
                     err = np.abs(drift[l, s] - D_o)
                     rep.max_kl_err = max(rep.max_kl_err, float(np.max(err / (KL_ABS + KL_REL * np.abs(D_o)))))
                     assert np.all(err <= KL_ABS + KL_REL * np.abs(D_o)), f"drift D (l={l}, s={s})"
+                    # the selected set is the decision; the order inside it is not
                     if not self._decision(f"top-k (l={l}, s={s})",
-                                          list(topk[l, s]) == list(recs[s]["topk"][l]),
+                                          sorted(topk[l, s]) == sorted(recs[s]["topk"][l]),
                                           recs[s]["topk_margin"][l]):
                         return False
                     assert np.array_equal(sel[l, s, :nw].astype(bool), recs[s]["sel"][l]), "selection"

@@ -29,7 +29,7 @@ def _run(name, kv_tol, act_tol, **kw):
 def test_tiny_fp32_trajectory():
     """Single-layer fp32 workload, 16 steps: every decision exact, fp32 tolerances."""
     rep = _run("tiny_l1_d256_fp32", kv_tol=1e-5, act_tol=1e-5)
-    assert rep.steps >= 8 and rep.fires >= 2, rep
+    assert rep.compared >= 12 and rep.fires >= 2, rep
     assert rep.near_ties <= 1
 
 
@@ -37,6 +37,6 @@ def test_tiny_fp32_trajectory():
 def test_mini_bf16_trajectory(name):
     """Two-layer bf16 stacks (MHA and 7:1 GQA): decisions exact up to counted near
     ties; K/V, active outputs and update packets within 1e-2 relative L2."""
-    rep = _run(name, kv_tol=1e-2, act_tol=1e-2)
-    assert rep.steps >= 4, rep
-    assert rep.near_ties <= 1
+    rep = _run(name, kv_tol=1e-2, act_tol=1e-2, n_steps=26)
+    assert rep.compared >= 10 and rep.fires >= 3, rep
+    assert rep.near_ties <= 2
