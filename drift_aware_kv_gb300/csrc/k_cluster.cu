@@ -8,7 +8,7 @@
 //   window_patch_kernel   within-block: decode a window row, swap in its update
 //                         packet when the previous layer selected it, re-encode
 //                         it and record the change of its unit direction.
-//   centroid_update_kernel  s_c += sum of those changes (window order),
+//   centroid_sum/norm     s_c += sum of those changes (window order),
 //                         z_c = s_c / |s_c| (incremental centroid update).
 #include "kernels.h"
 
@@ -261,33 +261,50 @@ __global__ void window_patch_kernel(PatchArgs a) {
   if (threadIdx.x == 0) a.write_kv[row] = 1;
 }
 
-__global__ void centroid_update_kernel(PatchArgs a) {
-  __shared__ float red[32];
-  const int c = blockIdx.x, f = blockIdx.y;
-  const int s = a.fire_seqs[f];
-  const int d = a.d;
-  float* cs = a.csum + ((size_t)s * a.K + c) * d;
-  float* z = a.z + ((size_t)s * a.K + c) * d;
+// s_c += sum over the patched member rows (window order) of their direction
+// change; one thread per channel, all clusters of one sequence per CTA column.
+__global__ void centroid_sum_kernel(PatchArgs a) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  const int s = a.fire_seqs[blockIdx.y];
+  if (k >= a.d) return;
   const uint8_t* lab = a.labels + (size_t)s * a.Wmax;
   const uint8_t* sel = a.sel_prev + (size_t)s * a.Wmax;
-  float ss = 0.f;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) {
-    float acc = cs[k];
-    for (int j = 0; j < a.nw; ++j)
-      if (sel[j] && lab[j] == c) acc += a.dn[((size_t)s * a.Wmax + j) * d + k];
-    cs[k] = acc;
-    ss = fmaf(acc, acc, ss);
+  float acc[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+  for (int j = 0; j < a.nw; ++j) {
+    if (!sel[j]) continue;  // uniform across the CTA
+    const int c = lab[j];
+    const float v = a.dn[((size_t)s * a.Wmax + j) * a.d + k];
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+      if (cc == c) acc[cc] += v;
   }
+  float* cs = a.csum + (size_t)s * a.K * a.d;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    if (c < a.K) cs[(size_t)c * a.d + k] += acc[c];
+}
+
+// z_c = s_c / |s_c| for every cluster of a refreshing sequence
+__global__ void centroid_norm_kernel(PatchArgs a) {
+  __shared__ float red[32];
+  const int c = blockIdx.x, s = a.fire_seqs[blockIdx.y];
+  const float* cs = a.csum + ((size_t)s * a.K + c) * a.d;
+  float* z = a.z + ((size_t)s * a.K + c) * a.d;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < a.d; k += blockDim.x) ss = fmaf(cs[k], cs[k], ss);
   ss = block_sum(ss, red);
   const float nrm = sqrtf(ss);
-  for (int k = threadIdx.x; k < d; k += blockDim.x) z[k] = cs[k] / nrm;
+  for (int k = threadIdx.x; k < a.d; k += blockDim.x) z[k] = cs[k] / nrm;
 }
 
 void launch_window_patch(const PatchArgs& a, cudaStream_t st) {
   window_patch_kernel<<<dim3(a.nw, a.n_fire), 256, 0, st>>>(a);
 }
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st) {
-  centroid_update_kernel<<<dim3(a.K, a.n_fire), 256, 0, st>>>(a);
+  centroid_sum_kernel<<<dim3((a.d + 127) / 128, a.n_fire), 128, 0, st>>>(a);
+  centroid_norm_kernel<<<dim3(a.K, a.n_fire), 256, 0, st>>>(a);
 }
 
 }  // namespace polestar

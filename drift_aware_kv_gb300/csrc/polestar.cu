@@ -588,6 +588,7 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       pa.z = zl;
       RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_window_patch(pa, c->sm)));
       RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_centroid_update(pa, c->sm)));
+      ++c->launches;  // two kernels
     }
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, zl, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, R, nullptr, c->qdim, d));
@@ -1027,4 +1028,95 @@ extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const
   else
     launch_gemm_simt<float>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, st);
   return cudaGetLastError() == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
+extern "C" polestar_status polestar_debug_attention(const void* q, const void* kv, int32_t N, int32_t H,
+                                                    int32_t Hkv, int32_t head_dim, int32_t R,
+                                                    const uint8_t* tracked, float* prev, float* prev_lse,
+                                                    int32_t measure, int32_t store, void* out, float* kl,
+                                                    int32_t dtype, void* stream) {
+  if (!q || !kv || !out || R < 1 || N < 1 || H < 1 || Hkv < 1 || H % Hkv) return POLESTAR_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return POLESTAR_ERR_UNSUPPORTED;
+  bool any_tracked = false;
+  for (int r = 0; tracked && r < R; ++r) any_tracked |= tracked[r] != 0;
+  if (any_tracked && (!prev || !prev_lse || (measure && !kl))) return POLESTAR_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  std::vector<int4> rows(R), work;
+  for (int r = 0; r < R; ++r)
+    rows[r] = make_int4(0, 0, (tracked && tracked[r]) ? ROW_ACTIVE : ROW_OTHER, r);
+  for (int k = 0; k < R; k += 64) work.push_back(make_int4(k, std::min(64, R - k), 0, 0));
+  int4* d_rows = nullptr;
+  int4* d_work = nullptr;
+  if (cudaMalloc(&d_rows, sizeof(int4) * R) != cudaSuccess) return POLESTAR_ERR_OOM;
+  if (cudaMalloc(&d_work, sizeof(int4) * work.size()) != cudaSuccess) {
+    cudaFree(d_rows);
+    return POLESTAR_ERR_OOM;
+  }
+  cudaMemcpy(d_rows, rows.data(), sizeof(int4) * R, cudaMemcpyHostToDevice);
+  cudaMemcpy(d_work, work.data(), sizeof(int4) * work.size(), cudaMemcpyHostToDevice);
+  AttnArgs a{};
+  a.q = q;
+  a.ldq = H * head_dim;
+  a.rows = d_rows;
+  a.R = R;
+  a.kv_layer = kv;
+  a.kv_seq_stride = 0;
+  a.kvdim = Hkv * head_dim;
+  a.N = N;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.dh = head_dim;
+  a.K = 1;
+  a.B = R;
+  a.scale = 1.f / sqrtf((float)head_dim);
+  a.out = out;
+  a.ldo = H * head_dim;
+  a.other_live = 1;
+  a.active_prev = any_tracked ? prev : nullptr;
+  a.active_prev_lse = any_tracked ? prev_lse : nullptr;
+  a.measure = measure;
+  a.store = store;
+  a.kl_out = kl;
+  a.work = d_work;
+  a.n_work = (int)work.size();
+  if (dtype == POLESTAR_BF16)
+    launch_row_attention<__nv_bfloat16>(a, st);
+  else
+    launch_row_attention<float>(a, st);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(d_rows);
+  cudaFree(d_work);
+  return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
+extern "C" polestar_status polestar_debug_kmeans(const float* Hw, int32_t P, int32_t nw, int32_t d, int32_t K,
+                                                 int32_t iters, uint64_t seed, int32_t block, uint8_t* labels,
+                                                 float* z, float* csum, float* anchor, uint8_t* codes,
+                                                 uint8_t* scales, void* stream) {
+  if (!Hw || !labels || !z || !csum || !anchor || !codes || !scales || P < 1 || iters < 1)
+    return POLESTAR_ERR_INVALID_ARG;
+  if (nw < 1 || nw > 128 || K < 1 || K > 8 || K > nw || d < 16 || d % 16 || d > 4096) return POLESTAR_ERR_UNSUPPORTED;
+  KmeansArgs a{};
+  a.Hw = Hw;
+  a.L = P;
+  a.batch = 1;
+  a.Wmax = nw;
+  a.nw = nw;
+  a.d = d;
+  a.K = K;
+  a.iters = iters;
+  a.seed = seed;
+  a.block = block;
+  a.labels = labels;
+  a.z = z;
+  a.csum = csum;
+  a.anchor = anchor;
+  a.codes = codes;
+  a.scales = scales;
+  cudaStream_t st = (cudaStream_t)stream;
+  launch_kmeans_encode(a, st);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }

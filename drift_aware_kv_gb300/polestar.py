@@ -22,7 +22,8 @@ FP32, BF16 = 0, 1
 
 EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
             "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
-            "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm")
+            "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
+            "polestar_debug_attention", "polestar_debug_kmeans")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows")
 
 
@@ -81,6 +82,12 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_debug_gemm.argtypes = [P, C.c_int32, P, C.c_int32, P, C.c_int32, C.c_int32, P, C.c_int32,
                                         C.c_int32, C.c_int32, C.c_int32, P]
     lib.polestar_debug_gemm.restype = C.c_int
+    lib.polestar_debug_attention.argtypes = [P, P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, P, P,
+                                             P, C.c_int32, C.c_int32, P, P, C.c_int32, P]
+    lib.polestar_debug_attention.restype = C.c_int
+    lib.polestar_debug_kmeans.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_uint64,
+                                          C.c_int32, P, P, P, P, P, P, P]
+    lib.polestar_debug_kmeans.restype = C.c_int
     lib.polestar_profile_begin.argtypes = [P, C.c_int32]
     lib.polestar_profile_end.argtypes = [P, C.POINTER(polestar_kernel_stats), C.c_int32]
     for f in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
@@ -207,3 +214,41 @@ def debug_gemm(A, W, out, path: int, m_dev=None, stream=None):
                                    C.c_void_p(out.data_ptr()), out.stride(0), M,
                                    C.c_void_p(m_dev.data_ptr()) if m_dev is not None else None, N, K, dt,
                                    path, C.c_void_p(st.cuda_stream)))
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def debug_attention(q, kv, H, Hkv, tracked, prev, prev_lse, measure, store, out, kl, stream=None):
+    """Row attention + KL on caller tensors (one sequence); see polestar_debug_attention."""
+    import torch
+    lib = load()
+    R = q.shape[0]
+    N = kv.shape[0]
+    dh = q.shape[1] // H
+    st = stream if stream is not None else torch.cuda.current_stream()
+    tr = (C.c_uint8 * R)(*[int(bool(v)) for v in tracked])
+    dt = BF16 if q.dtype == torch.bfloat16 else FP32
+    _check(lib.polestar_debug_attention(_ptr(q), _ptr(kv), N, H, Hkv, dh, R, tr, _ptr(prev), _ptr(prev_lse),
+                                        int(measure), int(store), _ptr(out), _ptr(kl), dt,
+                                        C.c_void_p(st.cuda_stream)))
+
+
+def debug_kmeans(Hw, K, iters, seed, block, stream=None):
+    """Spherical K-means + residual NVFP4 of P problems Hw [P, nw, d] (fp32, CUDA).
+    Returns dict of CUDA tensors labels, z, csum, anchor, codes, scales."""
+    import torch
+    lib = load()
+    P_, nw, d = Hw.shape
+    dev = Hw.device
+    out = dict(labels=torch.empty(P_, nw, dtype=torch.uint8, device=dev),
+               z=torch.empty(P_, K, d, device=dev), csum=torch.empty(P_, K, d, device=dev),
+               anchor=torch.empty(P_, K, d, device=dev),
+               codes=torch.empty(P_, nw, d // 2, dtype=torch.uint8, device=dev),
+               scales=torch.empty(P_, nw, d // 16, dtype=torch.uint8, device=dev))
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.polestar_debug_kmeans(_ptr(Hw), P_, nw, d, K, iters, int(seed), int(block), _ptr(out["labels"]),
+                                     _ptr(out["z"]), _ptr(out["csum"]), _ptr(out["anchor"]),
+                                     _ptr(out["codes"]), _ptr(out["scales"]), C.c_void_p(st.cuda_stream)))
+    return out

@@ -194,6 +194,28 @@ polestar_status polestar_debug_gemm(const void *A, int32_t lda, const void *W, i
                                     int32_t ldc, int32_t M, const int32_t *m_dev, int32_t N, int32_t K,
                                     int32_t dtype, int32_t path, void *stream);
 
+/* ---- row attention + KL drift on caller buffers (test hook) ----
+ * One sequence: q [R, H*dh] (rotary applied), kv [N, 2, Hkv*dh] (K then V of
+ * every position), both in `dtype`; out [R, H*dh] in `dtype`.  Rows with
+ * tracked[r] != 0 (host array) also read prev [R, H, N] fp32 scores and
+ * prev_lse [R, H] (previous measurement), write kl [R, H] =
+ * KL(softmax(new) || softmax(prev)) when `measure`, and replace prev/prev_lse by
+ * the new scores when `store` (Eq. 4).  Synchronous; allocates and frees its
+ * own row tables. */
+polestar_status polestar_debug_attention(const void *q, const void *kv, int32_t N, int32_t H, int32_t Hkv,
+                                         int32_t head_dim, int32_t R, const uint8_t *tracked, float *prev,
+                                         float *prev_lse, int32_t measure, int32_t store, void *out, float *kl,
+                                         int32_t dtype, void *stream);
+
+/* ---- spherical K-means + residual NVFP4 on caller buffers (test hook) ----
+ * P independent problems of nw rows: Hw [P, nw, d] fp32 -> labels [P, nw]
+ * uint8, z / csum / anchor [P, K, d] fp32, codes [P, nw, d/2], scales
+ * [P, nw, d/16]; problem p is initialised from seed like layer p of sequence 0
+ * at block `block`.  Synchronous. */
+polestar_status polestar_debug_kmeans(const float *Hw, int32_t P, int32_t nw, int32_t d, int32_t K,
+                                      int32_t iters, uint64_t seed, int32_t block, uint8_t *labels, float *z,
+                                      float *csum, float *anchor, uint8_t *codes, uint8_t *scales, void *stream);
+
 /* ---- inspection (used by parity tests; synchronises the main stream) ---- */
 typedef enum {
   POLESTAR_BUF_KV = 0,        /* layer l: [batch, N, 2, Hkv*dh] config dtype        */

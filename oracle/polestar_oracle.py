@@ -561,6 +561,7 @@ class PolestarOracle:
             delta_rel = np.zeros(2 * B)
             tau_d = np.zeros(2 * B)
             margin = np.full(2 * B, math.inf)
+            margin_drift = np.full(2 * B, math.inf)
             pos = np.arange(start, start + 2 * B)
             valid = pos < self.N
             msk = np.zeros(2 * B, dtype=bool)
@@ -581,8 +582,8 @@ class PolestarOracle:
                         st.theta[j] = []
                 tau_d[cur] = drift_threshold(conf[cur], c.tau_s, c.alpha)
                 m[cur] = msk[cur] & ((conf[cur] >= c.tau_s) | (delta_rel[cur] >= tau_d[cur]))
-                margin[cur] = np.minimum(np.abs(conf[cur] - c.tau_s),
-                                         np.abs(delta_rel[cur] - tau_d[cur]))
+                margin[cur] = np.abs(conf[cur] - c.tau_s)
+                margin_drift[cur] = np.abs(delta_rel[cur] - tau_d[cur])
                 if st.fire and st.sel_last is not None:
                     win = self.window(b)
                     for wi, p in enumerate(win):
@@ -591,7 +592,7 @@ class PolestarOracle:
                             m[j] = msk[j] and conf[j] >= c.tau_suf
                             margin[j] = abs(conf[j] - c.tau_suf)
             out.append(dict(commit=m, conf=conf, delta_rel=delta_rel, tau_d=tau_d,
-                            margin=margin))
+                            margin=margin, margin_drift=margin_drift))
         return out
 
 

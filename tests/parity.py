@@ -9,8 +9,19 @@ keep running on the same inputs, and comparison resumes at the next block
 entry with an even block index: that entry recomputes every position's K/V,
 the window cache, centroids, proxy baselines and histories from x0 alone, so
 the states coincide again without taking anything from the GPU side.
-Floating-point outputs use the tolerances below (KL drift 1e-5 abs + 1e-3
-rel; K/V, hidden states and update packets by relative L2 error)."""
+Floating-point outputs use the tolerances below (K/V, hidden states and update
+packets by relative L2 error).
+
+Drift tolerance.  KL drift must agree to 1e-5 abs + 1e-3 rel wherever its
+inputs are the same on both sides: fp32 workloads here, and every kernel-level
+test (tests/test_gpu_kernels.py).  In a bf16 stack the scores feeding the drift
+come from bf16-rounded queries and keys; when the fp32 and fp64 sides land on
+different sides of a bf16 rounding boundary (about one element in 10^3-10^4),
+that score moves by ~2^-8 |q_i k_i| / sqrt(dh).  Against per-step score changes
+of a few 1e-2 this moves D by a few percent, so bf16 trajectories use 1e-5 abs
++ 5e-2 rel for D and delta, and treat drift-driven decisions (top-k sets, the
+Delta >= tau_d branch of the gate) whose oracle margin is inside that band as
+near ties."""
 from __future__ import annotations
 
 import dataclasses
@@ -63,6 +74,8 @@ class Lockstep:
     def __init__(self, w: synth.Workload, kv_tol: float, act_tol: float):
         self.w = w
         self.kv_tol, self.act_tol = kv_tol, act_tol
+        self.kl_rel = KL_REL if w.dtype == "fp32" else 5e-2
+        self.drift_tie = NEAR_TIE if w.dtype == "fp32" else 5e-2
         # block-entry centroids/anchors: fp32 path ~1e-6; bf16 path inherits the
         # bf16 rounding of the A operands of the preceding layers
         self.state_tol = 1e-5 if w.dtype == "fp32" else 1e-3
@@ -115,11 +128,11 @@ class Lockstep:
         return rep
 
     # ------------------------------------------------------------------
-    def _decision(self, name, equal, margin):
+    def _decision(self, name, equal, margin, tie=NEAR_TIE):
         """Exact decision check; returns False (stop) on an accepted near tie."""
         if equal:
             return True
-        if margin < NEAR_TIE:
+        if margin < tie:
             self.rep.near_ties += 1
             self.rep.notes.append(f"near tie in {name} (margin {margin:.2e})")
             return False
@@ -165,18 +178,18 @@ class Lockstep:
                 for l in range(L):
                     D_o = recs[s]["D"][l]
                     err = np.abs(drift[l, s] - D_o)
-                    rep.max_kl_err = max(rep.max_kl_err, float(np.max(err / (KL_ABS + KL_REL * np.abs(D_o)))))
-                    assert np.all(err <= KL_ABS + KL_REL * np.abs(D_o)), f"drift D (l={l}, s={s})"
+                    rep.max_kl_err = max(rep.max_kl_err, float(np.max(err / (KL_ABS + self.kl_rel * np.abs(D_o)))))
+                    assert np.all(err <= KL_ABS + self.kl_rel * np.abs(D_o)), f"drift D (l={l}, s={s})"
                     # the selected set is the decision; the order inside it is not
                     if not self._decision(f"top-k (l={l}, s={s})",
                                           sorted(topk[l, s]) == sorted(recs[s]["topk"][l]),
-                                          recs[s]["topk_margin"][l]):
+                                          recs[s]["topk_margin"][l], self.drift_tie):
                         return False
                     assert np.array_equal(sel[l, s, :nw].astype(bool), recs[s]["sel"][l]), "selection"
             delta = self.read_layer(P.BUF_DELTA, 0, (b, w.block), torch.float32).numpy()
             for s in range(b):
                 d_o = recs[s]["delta"]
-                assert np.all(np.abs(delta[s] - d_o) <= KL_ABS + KL_REL * np.abs(d_o)), "token drift delta"
+                assert np.all(np.abs(delta[s] - d_o) <= KL_ABS + self.kl_rel * np.abs(d_o)), "token drift delta"
             act = self.read_layer(P.BUF_ACT_OUT, 0, (b, w.block, d), torch.float32).numpy()
             for s in range(b):
                 e = rel_l2(act[s], recs[s]["act_out"])
@@ -202,6 +215,11 @@ class Lockstep:
                 rep.max_kv_err = max(rep.max_kv_err, e)
                 assert e < self.kv_tol, f"K/V cache rel err {e} (layer {l}, seq {s})"
         return True
+
+    def _delta_scale(self, s):
+        """Magnitude of the last-layer drifts of sequence s (oracle side)."""
+        d = self.orc.seqs[s].delta
+        return float(np.max(np.abs(d))) if d is not None else 0.0
 
     def _check_codes(self, codes, scales, o, l, s=None, nw=None):
         """NVFP4 store of layer l.  Where the encoder's inputs are exact on both
@@ -244,12 +262,15 @@ class Lockstep:
             co = coms[s]
             valid = np.arange(2 * w.block) + w.prompt_len + st["block_index"] * w.block < self.N
             assert np.allclose(conf[s][valid], co["conf"][valid], rtol=1e-5, atol=1e-6), "confidence"
-            assert np.all(np.abs(drel[s] - co["delta_rel"]) <= KL_ABS + KL_REL * np.abs(co["delta_rel"])), "Delta"
+            assert np.all(np.abs(drel[s] - co["delta_rel"]) <= KL_ABS + self.kl_rel * np.abs(co["delta_rel"]) +
+                          self.kl_rel * self._delta_scale(s)), "Delta"
             assert np.allclose(taud[s], co["tau_d"], rtol=1e-4, atol=1e-6), "tau_d"
             eq = np.array_equal(cm[s].astype(bool), co["commit"])
             if not eq:
                 diff = cm[s].astype(bool) != co["commit"]
-                m = float(np.min(co["margin"][diff]))
+                conf_tie = co["margin"][diff] < NEAR_TIE
+                drift_tie = co["margin_drift"][diff] < KL_ABS + self.drift_tie * self._delta_scale(s)
+                m = 0.0 if np.all(conf_tie | drift_tie) else float(np.min(co["margin"][diff]))
                 if not self._decision(f"commit mask (s={s})", False, m):
                     return False
             self.rep.commits += int(co["commit"].sum())

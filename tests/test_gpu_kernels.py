@@ -1,0 +1,142 @@
+"""Kernel-level parity through the C ABI's test hooks, on identical inputs for
+both sides, at the sizes of the benchmark workloads (LLaDA-8B: 32 heads x 128,
+N = 768 or 2048 keys, 96-row windows of d = 4096; Dream-7B: 28/4 GQA heads,
+d = 3584) plus ragged and small cases.
+
+Attention + KL follows Eq. 3 / Eq. 4 of "Polestar: Drift-Aware Cache
+Calibration and Token Commitment for Efficient Inference of Diffusion LLMs";
+K-means + NVFP4 follows §4.1 and App. C.3; confidence follows §2."""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from oracle import polestar_oracle as O  # noqa: E402
+
+NEAR_TIE = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from drift_aware_kv_gb300.build import build
+    build()
+
+
+def _oracle_attention(q, kv, H, Hkv):
+    """fp64 scores [R, H, N] and outputs [R, H*dh] from the same stored values."""
+    R, N = q.shape[0], kv.shape[0]
+    dh = q.shape[1] // H
+    qq = q.double().cpu().numpy().reshape(R, H, dh)
+    K = kv[:, 0].double().cpu().numpy().reshape(N, Hkv, dh)
+    V = kv[:, 1].double().cpu().numpy().reshape(N, Hkv, dh)
+    g = H // Hkv
+    K = np.repeat(K, g, axis=1)
+    V = np.repeat(V, g, axis=1)
+    s = np.einsum("rhd,nhd->rhn", qq, K) / math.sqrt(dh)
+    lse = O.logsumexp(s)
+    p = np.exp(s - lse[..., None])
+    out = np.einsum("rhn,nhd->rhd", p, V).reshape(R, H * dh)
+    return s, lse, out
+
+
+ATTN_CASES = [  # (R, N, H, Hkv, dh, dtype)
+    (136, 768, 32, 32, 128, torch.bfloat16),   # LLaDA-8B within-block rows
+    (40, 2048, 32, 32, 128, torch.bfloat16),   # long-context workload
+    (104, 768, 28, 4, 128, torch.bfloat16),    # Dream-7B GQA
+    (70, 100, 4, 4, 64, torch.bfloat16),       # ragged tile tail
+    (24, 192, 4, 4, 64, torch.float32),        # fp32 single-layer workload
+]
+
+
+@pytest.mark.parametrize("R,N,H,Hkv,dh,dt", ATTN_CASES)
+def test_attention_and_kl_match_definition(R, N, H, Hkv, dh, dt):
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator().manual_seed(R * 131 + N)
+    scale = 1.6 if dh == 128 else 0.4  # score spread of the LLaDA-shaped projections
+    q1 = (scale * torch.randn(R, H * dh, generator=g)).to(dt)
+    q2 = (q1.float() + 0.05 * scale * torch.randn(R, H * dh, generator=g)).to(dt)
+    kv = (scale * torch.randn(N, 2, Hkv * dh, generator=g)).to(dt)
+    tracked = [r % 3 == 0 for r in range(R)]
+    prev = torch.zeros(R, H, N, device="cuda")
+    plse = torch.zeros(R, H, device="cuda")
+    out = torch.empty(R, H * dh, dtype=dt, device="cuda")
+    kl = torch.full((R, H), float("nan"), device="cuda")
+    kvg = kv.cuda()
+    P.debug_attention(q1.cuda(), kvg, H, Hkv, tracked, prev, plse, 0, 1, out, kl)
+    s1, lse1, o1 = _oracle_attention(q1, kv, H, Hkv)
+    tr = np.array(tracked)
+    assert np.allclose(prev.cpu().numpy()[tr], s1[tr], atol=2e-5 * np.abs(s1).max())
+    P.debug_attention(q2.cuda(), kvg, H, Hkv, tracked, prev, plse, 1, 1, out, kl)
+    s2, lse2, o2 = _oracle_attention(q2, kv, H, Hkv)
+    # attention output (stored in the workload dtype)
+    got = out.double().cpu().numpy()
+    err = np.linalg.norm(got - o2, axis=1) / np.linalg.norm(o2, axis=1)
+    assert err.max() < (1e-5 if dt == torch.float32 else 8e-3), err.max()
+    # KL drift of the tracked rows: 1e-5 absolute + 1e-3 relative
+    kl_o = O.kl_div(s2, lse2, s1, lse1)[tr]
+    kl_g = kl.cpu().numpy()[tr]
+    assert np.all(np.abs(kl_g - kl_o) <= 1e-5 + 1e-3 * np.abs(kl_o)), np.max(np.abs(kl_g - kl_o))
+    assert np.all(np.isnan(kl.cpu().numpy()[~tr]))
+
+
+@pytest.mark.parametrize("P_,nw,d", [(32, 96, 4096), (4, 96, 3584), (3, 64, 256), (2, 70, 448)])
+def test_kmeans_nvfp4_match_oracle(P_, nw, d):
+    from drift_aware_kv_gb300 import polestar as P
+    g = np.random.default_rng(P_ * 7 + nw + d)
+    centers = g.standard_normal((P_, 8, d)) * 2.0
+    lab = g.integers(0, 8, (P_, nw))
+    Hw = O.to_f32(np.take_along_axis(centers, lab[..., None], 1) + g.standard_normal((P_, nw, d)))
+    res = P.debug_kmeans(torch.tensor(Hw, dtype=torch.float32).cuda(), 8, 10, 1234, 3)
+    torch.cuda.synchronize()
+    near = 0
+    for p in range(P_):
+        init = O.kmeans_init(1234, 0, 3, p, nw, 8)
+        labels, z, s, A, gap = O.spherical_kmeans(Hw[p], 8, 10, init)
+        lg = res["labels"][p].cpu().numpy()
+        if not np.array_equal(lg, labels):
+            assert gap < NEAR_TIE, f"labels differ with margin {gap}"
+            near += 1
+            continue
+        assert np.allclose(res["z"][p].cpu().numpy(), z, atol=1e-5)
+        assert np.allclose(res["csum"][p].cpu().numpy(), s, rtol=1e-5, atol=1e-4)
+        assert np.allclose(res["anchor"][p].cpu().numpy(), A, rtol=1e-5, atol=1e-5)
+        codes, sb, margin = O.nvfp4_encode(O.to_f32(O.to_f32(Hw[p]) - A[labels]))
+        cg = res["codes"][p].cpu().numpy()
+        cg = np.stack([cg & 0xF, cg >> 4], -1).reshape(nw, d)
+        sg = res["scales"][p].cpu().numpy()
+        bad = (cg != codes) | np.repeat(sg != sb, 16, axis=1)
+        assert np.all(margin[bad] < NEAR_TIE), margin[bad].max() if bad.any() else 0
+    assert near <= max(1, P_ // 8)
+
+
+@pytest.mark.parametrize("V", [126464, 152064, 1000])
+def test_confidence_and_entry_commit_full_vocab(V):
+    """Max-softmax confidence over the full vocabulary (§2) and the block-entry
+    commit (confidence only, Algorithm 1 line 12) through the public calls."""
+    from drift_aware_kv_gb300 import polestar as P
+    from drift_aware_kv_gb300 import synth
+    w = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(batch=2, vocab=V, embed_vocab=V)
+    tr = synth.Trajectory(w)
+    st = tr.next_step()
+    W = [{k: v.cuda() for k, v in lw.items()} for lw in synth.make_weights(w)]
+    ps = P.Polestar(w, W)
+    ps.calibrate_step(st["x0"].cuda(), st["n_unmasked"], 0, True)
+    cm = torch.zeros(2, 2 * w.block, dtype=torch.uint8, device="cuda")
+    conf = torch.zeros(2, 2 * w.block, device="cuda")
+    ps.commit(st["logits"].cuda(), st["masked"].to(torch.uint8).cuda(), cm, conf)
+    torch.cuda.synchronize()
+    for s in range(2):
+        c_o = O.confidence(st["logits"][s].numpy())
+        assert np.allclose(conf[s].cpu().numpy(), c_o, rtol=2e-6, atol=1e-7)
+        m = st["masked"][s].numpy()[w.prompt_len:w.prompt_len + w.block]
+        want = np.zeros(2 * w.block, dtype=bool)
+        want[:w.block] = m & (c_o[:w.block] >= w.tau_s)
+        got = cm[s].cpu().numpy().astype(bool)
+        diff = got != want
+        assert np.all(np.abs(c_o[diff] - w.tau_s) < NEAR_TIE)
+    ps.close()
