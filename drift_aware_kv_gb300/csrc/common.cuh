@@ -119,6 +119,19 @@ __device__ __forceinline__ uint8_t nvfp4_encode16(const float* r, uint8_t* out8)
   return sb;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel of the layer loop is launched with programmatic stream
+// serialisation: it lets its successor start launching right away and waits
+// for its predecessor's results before touching memory the predecessor writes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_launch_dependents();
+  pdl_wait();
+}
+
 // ---- row metadata -------------------------------------------------------------
 enum RowKind : int { ROW_NONE = 0, ROW_ACTIVE = 1, ROW_WINDOW = 2, ROW_PROXY = 3, ROW_OTHER = 4 };
 

@@ -23,6 +23,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "common.cuh"
 #include "gemm_tc.h"
 
 namespace polestar {
@@ -38,13 +39,17 @@ constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int RED_PITCH = BN + 4;                     // fp32 staging row pitch
 
 struct Params {
-  int M, N, K;
+  int M, K;
   const int* m_dev;
-  float* C;
   int ldc;
   int ktiles;
   int splits;
   int* err;
+  // up to three weight segments sharing A: tiles [seg_start[s], seg_start[s+1])
+  int nseg;
+  int seg_start[4];
+  int seg_N[3];
+  float* seg_C[3];
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -146,17 +151,21 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float ld_dsmem(const float* local_ptr, uint32_t rank) {
+__device__ __forceinline__ float4 ld_dsmem4(const float* local_ptr, uint32_t rank) {
   uint32_t a = smem_u32(local_ptr), ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
   return v;
 }
 
 template <int MT, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   constexpr int A_BYTES = BM * BK * 2;  // 16 KB per row sub-tile
@@ -169,11 +178,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN;
+  const int tile = blockIdx.x;
+  const int seg = (tile >= p.seg_start[1]) + (tile >= p.seg_start[2]);
+  const int n0 = (tile - p.seg_start[seg]) * BN;
+  const int segN = p.seg_N[seg];
+  float* const Cseg = p.seg_C[seg];
+  const CUtensorMap* tmB = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
   const int m0 = blockIdx.y * (MT * BM);
   const int split = blockIdx.z;
-  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
-  if (m0 >= M_eff) return;  // the whole cluster shares (x, y): all its CTAs leave together
 
   const int kt0 = (int)((long long)split * p.ktiles / p.splits);
   const int kt1 = (int)((long long)(split + 1) * p.ktiles / p.splits);
@@ -199,19 +211,39 @@ __global__ void __launch_bounds__(THREADS, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
+  // Weights never depend on earlier kernels: the first stages' W tiles are
+  // requested before waiting for the predecessor that produces A (and m_dev).
+  const int npre = nk < STAGES ? nk : STAGES;
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < npre; ++i) {
+      const uint32_t fb = smem_u32(&full[i]);
+      mbar_expect_tx(fb, STAGE_BYTES);
+      tma_load_2d(smem_u32(smem + i * STAGE_BYTES) + MT * A_BYTES, tmB, (kt0 + i) * BK, n0, fb);
+    }
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
+
   if (warp == 0) {
     // ---------------- TMA producer
     if (lane == 0) {
-      for (int i = 0; i < nk; ++i) {
+      for (int i = 0; i < npre; ++i) {
+        const uint32_t st = smem_u32(smem + i * STAGE_BYTES);
+        const int kx = (kt0 + i) * BK;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, smem_u32(&full[i]));
+      }
+      for (int i = npre; i < nk; ++i) {
         const int s = i % STAGES;
-        if (i >= STAGES && !mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) break;
+        if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) break;
         const uint32_t fb = smem_u32(&full[s]);
         mbar_expect_tx(fb, STAGE_BYTES);
         const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
         const int kx = (kt0 + i) * BK;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, fb);
-        tma_load_2d(st + MT * A_BYTES, &tmB, kx, n0, fb);
+        tma_load_2d(st + MT * A_BYTES, tmB, kx, n0, fb);
       }
     }
   } else if (warp == 1) {
@@ -256,14 +288,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           float v[32];
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + mt * BN + c, v);
           if (row < M_eff) {
-            float* dst = p.C + (size_t)row * p.ldc + n0 + c;
-            if (n0 + c + 32 <= p.N && ((p.ldc & 3) == 0)) {
+            float* dst = Cseg + (size_t)row * p.ldc + n0 + c;
+            if (n0 + c + 32 <= segN && ((p.ldc & 3) == 0) && ((((uintptr_t)Cseg) & 15) == 0)) {
 #pragma unroll
               for (int j = 0; j < 32; j += 4) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (n0 + c + j < p.N) dst[j] = v[j];
+                if (n0 + c + j < segN) dst[j] = v[j];
             }
           }
         }
@@ -273,7 +305,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // split-K: stage partials in shared memory, reduce across the cluster
     float* red = (float*)smem;  // [BM][RED_PITCH] fp32, pipeline buffers are idle now
     const uint32_t rank = cluster_rank();
-    const int rows_per = BM / p.splits;
 #pragma unroll 1
     for (int mt = 0; mt < MT; ++mt) {
       __syncthreads();
@@ -290,14 +321,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       cluster_sync();
-      // this CTA reduces rows [rank*rows_per, (rank+1)*rows_per) of the sub-tile
-      const int rbeg = (int)rank * rows_per;
-      for (int idx = threadIdx.x; idx < rows_per * BN; idx += THREADS) {
-        const int rr = rbeg + idx / BN, cc = idx % BN;
+      // this CTA reduces its share of the sub-tile's rows, splits in fixed order
+      const int rbeg = (int)rank * BM / p.splits, rend = ((int)rank + 1) * BM / p.splits;
+      for (int idx = threadIdx.x; idx < (rend - rbeg) * (BN / 4); idx += THREADS) {
+        const int rr = rbeg + idx / (BN / 4), cc = (idx % (BN / 4)) * 4;
         const int row = m0 + mt * BM + rr;
-        float acc = 0.f;
-        for (int s = 0; s < p.splits; ++s) acc += ld_dsmem(red + rr * RED_PITCH + cc, (uint32_t)s);
-        if (row < M_eff && n0 + cc < p.N) p.C[(size_t)row * p.ldc + n0 + cc] = acc;
+        if (row >= M_eff) continue;
+        float4 acc = ld_dsmem4(red + rr * RED_PITCH + cc, 0u);
+        for (int s = 1; s < p.splits; ++s) {
+          const float4 v = ld_dsmem4(red + rr * RED_PITCH + cc, (uint32_t)s);
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        float* dst = Cseg + (size_t)row * p.ldc + n0 + cc;
+        if (n0 + cc + 4 <= segN && ((p.ldc & 3) == 0) && ((((uintptr_t)Cseg) & 15) == 0)) {
+          *(float4*)dst = acc;
+        } else {
+          const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+          for (int j = 0; j < 4; ++j)
+            if (n0 + cc + j < segN) dst[j] = vv[j];
+        }
       }
       cluster_sync();
     }
@@ -350,7 +395,7 @@ const CUtensorMap* get_map(TcGemmCache* cache, const void* ptr, int rows, int co
 }
 
 template <int MT, int STAGES>
-cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const Params& p, dim3 grid, int splits,
+cudaError_t launch(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid, int splits,
                    cudaStream_t st) {
   auto kern = gemm_kernel<MT, STAGES>;
   static bool attr = false;
@@ -364,14 +409,16 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const Params& p, 
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 1;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = splits;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, *a, *b, p);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, *a, *b[0], *b[1], *b[2], p);
 }
 
 }  // namespace tc
@@ -388,44 +435,64 @@ bool tc_gemm_supported(int K, int lda, int ldw) {
   return K >= 16 && (lda % 8) == 0 && (ldw % 8) == 0;
 }
 
-cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,
-                         int M, const int* m_dev, int N, int K, cudaStream_t st) {
+cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int nseg, const void* const* W,
+                               const int* ldw, const int* N, float* const* C, int ldc, int M, const int* m_dev,
+                               int K, cudaStream_t st) {
   using namespace tc;
-  if (M <= 0 || N <= 0) return cudaSuccess;
-  if (((uintptr_t)A & 15) || ((uintptr_t)W & 15)) return cudaErrorInvalidValue;
+  if (M <= 0 || nseg < 1 || nseg > 3) return M <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+  if ((uintptr_t)A & 15) return cudaErrorInvalidValue;
   int* err = tc_error_word(cache);
   if (!err) return cudaErrorMemoryAllocation;
-  const int MT = M > BM ? 2 : 1;
-  const int mgroups = (M + MT * BM - 1) / (MT * BM);
-  const int ntiles = (N + BN - 1) / BN;
-  const int ktiles = (K + BK - 1) / BK;
   if (cache->num_sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&cache->num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (cache->num_sms <= 0) cache->num_sms = 148;
   }
-  // split K over a cluster while the doubled grid still fits in one wave and
-  // every split keeps at least 4 K-tiles (cluster size <= 8)
-  const int base = ntiles * mgroups;
-  int splits = 1;
-  while (splits < 8 && base * splits * 2 <= cache->num_sms && ktiles >= splits * 2 * 4) splits *= 2;
-  const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
-  const CUtensorMap* mb = get_map(cache, W, N, K, ldw, BN);
-  if (!ma || !mb) return cudaErrorInvalidValue;
+  const int MT = M > BM ? 2 : 1;
+  const int mgroups = (M + MT * BM - 1) / (MT * BM);
+  const int ktiles = (K + BK - 1) / BK;
   Params p{};
   p.M = M;
-  p.N = N;
   p.K = K;
   p.m_dev = m_dev;
-  p.C = C;
   p.ldc = ldc;
   p.ktiles = ktiles;
-  p.splits = splits;
   p.err = err;
-  const dim3 grid(ntiles, mgroups, splits);
+  p.nseg = nseg;
+  const CUtensorMap* mb[3] = {nullptr, nullptr, nullptr};
+  int tiles = 0;
+  for (int sgi = 0; sgi < 3; ++sgi) {
+    p.seg_start[sgi] = sgi < nseg ? tiles : 0x3FFFFFFF;
+    if (sgi < nseg) {
+      if (((uintptr_t)W[sgi] & 15) || N[sgi] < 1) return cudaErrorInvalidValue;
+      p.seg_N[sgi] = N[sgi];
+      p.seg_C[sgi] = C[sgi];
+      mb[sgi] = get_map(cache, W[sgi], N[sgi], K, ldw[sgi], BN);
+      if (!mb[sgi]) return cudaErrorInvalidValue;
+      tiles += (N[sgi] + BN - 1) / BN;
+    }
+  }
+  p.seg_start[3] = 0x3FFFFFFF;
+  for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
+  // split K over a cluster while the doubled grid still fits in one wave and
+  // every split keeps at least 8 K-tiles (cluster size <= 8): only grids that
+  // would leave most SMs idle pay for the cross-CTA reduction
+  const int base = tiles * mgroups, nsm = cache->num_sms;
+  int splits = 1;
+  while (splits < 8 && base * splits * 2 <= nsm && ktiles >= splits * 2 * 8) splits *= 2;
+  p.splits = splits;
+  const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
+  if (!ma) return cudaErrorInvalidValue;
+  const dim3 grid(tiles, mgroups, splits);
   if (MT == 2) return launch<2, 4>(ma, mb, p, grid, splits, st);
   return launch<1, 6>(ma, mb, p, grid, splits, st);
+}
+
+cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,
+                         int M, const int* m_dev, int N, int K, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  return tc_gemm_bf16_multi(cache, A, lda, 1, &W, &ldw, &N, &C, ldc, M, m_dev, K, st);
 }
 
 void tc_gemm_cache_clear(TcGemmCache* c) {

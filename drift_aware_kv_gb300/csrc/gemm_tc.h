@@ -43,6 +43,12 @@ bool tc_gemm_supported(int K, int lda, int ldw);
 cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,
                          int M, const int* m_dev, int N, int K, cudaStream_t st);
 
+// Up to three projections sharing the A operand in one launch: segment s
+// computes C[s][M, N[s]] = A * W[s]^T (all C[s] with row stride ldc).
+cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int nseg, const void* const* W,
+                               const int* ldw, const int* N, float* const* C, int ldc, int M, const int* m_dev,
+                               int K, cudaStream_t st);
+
 // Device word holding the code of the first timed-out wait (0 = none).
 int* tc_error_word(TcGemmCache* cache);
 

@@ -28,6 +28,7 @@ constexpr int ATT_TK = 64;    // keys per tile
 
 template <typename T, int DH>
 __global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
+  pdl_enter();
   extern __shared__ float smem[];
   constexpr int PITCH = DH + 1;
   float* Ks = smem;                       // [TK][PITCH]
@@ -235,6 +236,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 template <int DH>
 __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
+  pdl_enter();
   constexpr int KP = DH + 8;  // smem pitch (elements): 16-byte rows, conflict-free ldmatrix
   extern __shared__ __align__(16) __nv_bfloat16 sm_kv[];
   __nv_bfloat16* Ks = sm_kv;                   // [2][TK][KP]
@@ -312,11 +314,13 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
   float mrun[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
   float asum[2] = {0.f, 0.f}, sqs[2] = {0.f, 0.f}, esum[2] = {0.f, 0.f};
 
-  const int ntiles = (p.N + AM_TK - 1) / AM_TK;
-  load_tile(0, 0);
-  for (int t = 0; t < ntiles; ++t) {
-    const int buf = t & 1;
-    if (t + 1 < ntiles) {
+  const int ntiles_all = (p.N + AM_TK - 1) / AM_TK;
+  const int nsplit = gridDim.z, split = blockIdx.z;
+  const int tbeg = split * ntiles_all / nsplit, tend = (split + 1) * ntiles_all / nsplit;
+  load_tile(0, tbeg * AM_TK);
+  for (int t = tbeg; t < tend; ++t) {
+    const int buf = (t - tbeg) & 1;
+    if (t + 1 < tend) {
       load_tile(buf ^ 1, (t + 1) * AM_TK);
       cp_async_wait<1>();
     } else {
@@ -429,6 +433,28 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
       esum[i] += __shfl_xor_sync(0xffffffffu, esum[i], o);
     }
   }
+  if (nsplit > 1) {
+    // partial results of this key slice; the combine kernel finishes the rows
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int rl = i ? rl1 : rl0;
+      if (rl >= wk.y || !live[i]) continue;
+      float* pp = p.part + (((size_t)split * p.R + rows[i]) * p.H + h) * (5 + DH);
+      if (qc == 0) {
+        pp[0] = mrun[i];
+        pp[1] = lsum[i];
+        pp[2] = asum[i];
+        pp[3] = sqs[i];
+        pp[4] = esum[i];
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        pp[5 + nt * 8 + qc * 2] = acc[nt][2 * i];
+        pp[5 + nt * 8 + qc * 2 + 1] = acc[nt][2 * i + 1];
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     if (outp[i]) {
@@ -445,10 +471,70 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
   }
 }
 
+// Merge the key-split partials of attn_mma_kernel: one warp per (row, head).
+template <int DH>
+__global__ void attn_combine_kernel(AttnArgs p) {
+  pdl_enter();
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (gw >= p.R * p.H) return;
+  const int r = gw / p.H, h = gw % p.H;
+  const int4 m = p.rows[r];
+  if (m.z == ROW_NONE) return;
+  const int seq = m.x;
+  const size_t stride = (size_t)p.R * p.H * (5 + DH);
+  const float* base = p.part + ((size_t)r * p.H + h) * (5 + DH);
+  float M = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, base[s * stride]);
+  float l = 0.f, a = 0.f, sq = 0.f, e = 0.f;
+  constexpr int NV = DH / 32;
+  float acc[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+  for (int s = 0; s < p.splits; ++s) {
+    const float* pp = base + s * stride;
+    const float w = expf(pp[0] - M);
+    l += pp[1] * w;
+    a += pp[2] * w;
+    sq += pp[3];
+    e += pp[4];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) acc[i] += pp[5 + lane + 32 * i] * w;
+  }
+  if (m.z != ROW_PROXY) {
+    __nv_bfloat16* o = (__nv_bfloat16*)p.out + (size_t)r * p.ldo + h * DH;
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) o[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+  }
+  float* prev_lse = nullptr;
+  if (m.z == ROW_PROXY && p.proxy_prev)
+    prev_lse = p.proxy_prev_lse + ((size_t)seq * p.K + m.w) * p.H + h;
+  else if (m.z == ROW_ACTIVE && p.active_prev)
+    prev_lse = p.active_prev_lse + ((size_t)seq * p.B + m.w) * p.H + h;
+  if (prev_lse && lane == 0) {
+    if (p.measure) p.kl_out[(size_t)r * p.H + h] = a / l - log1pf(e / sq);
+    if (p.store) *prev_lse = M + logf(l);
+  }
+}
+
+int attention_splits(int R, int H, int N, int dh, size_t part_floats, int num_sms) {
+  const int ctas = ((R + 63) / 64) * H;
+  const int tiles = (N + AM_TK - 1) / AM_TK;
+  int s = 1;
+  while (s < 8 && ctas * s * 2 <= 4 * num_sms && tiles >= 2 * s * 2 &&
+         (size_t)(2 * s) * R * H * (5 + dh) <= part_floats)
+    s *= 2;
+  return s;
+}
+
 template <typename T>
 void launch_row_attention(const AttnArgs& a, cudaStream_t st) {
   if (sizeof(T) == 2 && a.work) {
-    const dim3 grid(a.n_work, a.H);
+    const int splits = (a.splits > 1 && a.part) ? a.splits : 1;
+    AttnArgs b = a;
+    b.splits = splits;
+    const dim3 grid(a.n_work, a.H, splits);
+    const int cw = (a.R * a.H * 32 + 255) / 256;
     if (a.dh == 128) {
       const size_t sm = 4 * AM_TK * (128 + 8) * sizeof(__nv_bfloat16);
       static bool cfg = false;
@@ -456,10 +542,12 @@ void launch_row_attention(const AttnArgs& a, cudaStream_t st) {
         cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         cfg = true;
       }
-      attn_mma_kernel<128><<<grid, 128, sm, st>>>(a);
+      launch_pdl(attn_mma_kernel<128>, dim3(grid), dim3(128), sm, st, b);
+      if (splits > 1) launch_pdl(attn_combine_kernel<128>, dim3(cw), dim3(256), 0, st, b);
     } else {
       const size_t sm = 4 * AM_TK * (64 + 8) * sizeof(__nv_bfloat16);
-      attn_mma_kernel<64><<<grid, 128, sm, st>>>(a);
+      launch_pdl(attn_mma_kernel<64>, dim3(grid), dim3(128), sm, st, b);
+      if (splits > 1) launch_pdl(attn_combine_kernel<64>, dim3(cw), dim3(256), 0, st, b);
     }
     return;
   }
@@ -471,10 +559,10 @@ void launch_row_attention(const AttnArgs& a, cudaStream_t st) {
       cudaFuncSetAttribute(row_attention_kernel<T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       cfg = true;
     }
-    row_attention_kernel<T, 128><<<grid, 256, sm, st>>>(a);
+    launch_pdl(row_attention_kernel<T, 128>, dim3(grid), dim3(256), sm, st, a);
   } else {
     const size_t sm = (2 * ATT_TK * 65 + ATT_ROWS * 64 + ATT_ROWS * ATT_TK) * sizeof(float);
-    row_attention_kernel<T, 64><<<grid, 256, sm, st>>>(a);
+    launch_pdl(row_attention_kernel<T, 64>, dim3(grid), dim3(256), sm, st, a);
   }
 }
 

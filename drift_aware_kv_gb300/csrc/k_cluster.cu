@@ -28,6 +28,7 @@ __device__ __forceinline__ uint64_t splitmix64_next(uint64_t& x) {
 }
 
 __global__ void __launch_bounds__(KM_THREADS) kmeans_encode_kernel(KmeansArgs a) {
+  pdl_enter();
   extern __shared__ float sm[];
   float* zs = sm;                                  // [K][d] centroids, later anchors
   float* inv = zs + (size_t)a.K * a.d;             // [KM_MAXW] 1/|x_i|
@@ -198,11 +199,12 @@ void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st) {
   const size_t sm = (size_t)a.K * a.d * sizeof(float) + KM_MAXW * sizeof(float) +
                     32 * KM_MAXK * sizeof(float) + (2 * KM_MAXW + KM_MAXK) * sizeof(int);
   cudaFuncSetAttribute(kmeans_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  kmeans_encode_kernel<<<a.L * a.batch, KM_THREADS, sm, st>>>(a);
+  launch_pdl(kmeans_encode_kernel, dim3(a.L * a.batch), dim3(KM_THREADS), sm, st, a);
 }
 
 // ---------------------------------------------------------------- within-block
 __global__ void window_patch_kernel(PatchArgs a) {
+  pdl_enter();
   __shared__ float red[32];
   const int j = blockIdx.x, f = blockIdx.y;
   const int s = a.fire_seqs[f];
@@ -264,6 +266,7 @@ __global__ void window_patch_kernel(PatchArgs a) {
 // s_c += sum over the patched member rows (window order) of their direction
 // change; one thread per channel, all clusters of one sequence per CTA column.
 __global__ void centroid_sum_kernel(PatchArgs a) {
+  pdl_enter();
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   const int s = a.fire_seqs[blockIdx.y];
   if (k >= a.d) return;
@@ -288,6 +291,7 @@ __global__ void centroid_sum_kernel(PatchArgs a) {
 
 // z_c = s_c / |s_c| for every cluster of a refreshing sequence
 __global__ void centroid_norm_kernel(PatchArgs a) {
+  pdl_enter();
   __shared__ float red[32];
   const int c = blockIdx.x, s = a.fire_seqs[blockIdx.y];
   const float* cs = a.csum + ((size_t)s * a.K + c) * a.d;
@@ -300,11 +304,11 @@ __global__ void centroid_norm_kernel(PatchArgs a) {
 }
 
 void launch_window_patch(const PatchArgs& a, cudaStream_t st) {
-  window_patch_kernel<<<dim3(a.nw, a.n_fire), 256, 0, st>>>(a);
+  launch_pdl(window_patch_kernel, dim3(a.nw, a.n_fire), dim3(256), 0, st, a);
 }
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st) {
-  centroid_sum_kernel<<<dim3((a.d + 127) / 128, a.n_fire), 128, 0, st>>>(a);
-  centroid_norm_kernel<<<dim3(a.K, a.n_fire), 256, 0, st>>>(a);
+  launch_pdl(centroid_sum_kernel, dim3((a.d + 127) / 128, a.n_fire), dim3(128), 0, st, a);
+  launch_pdl(centroid_norm_kernel, dim3(a.K, a.n_fire), dim3(256), 0, st, a);
 }
 
 }  // namespace polestar

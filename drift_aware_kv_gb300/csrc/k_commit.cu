@@ -13,6 +13,7 @@
 namespace polestar {
 
 __global__ void conf_partial_kernel(CommitArgs a) {
+  pdl_enter();
   __shared__ float sm_m[32], sm_s[32];
   const int row = blockIdx.x, sp = blockIdx.y;
   const int chunk = (a.V + a.splits - 1) / a.splits;
@@ -78,6 +79,7 @@ __global__ void conf_partial_kernel(CommitArgs a) {
 }
 
 __global__ void commit_gate_kernel(CommitArgs a) {
+  pdl_enter();
   const int s = blockIdx.x, j = threadIdx.x;
   const int B = a.B;
   if (j >= 2 * B) return;
@@ -140,8 +142,8 @@ __global__ void commit_gate_kernel(CommitArgs a) {
 }
 
 void launch_commit(const CommitArgs& a, cudaStream_t st) {
-  conf_partial_kernel<<<dim3(a.batch * 2 * a.B, a.splits), 256, 0, st>>>(a);
-  commit_gate_kernel<<<a.batch, 2 * a.B, 0, st>>>(a);
+  launch_pdl(conf_partial_kernel, dim3(a.batch * 2 * a.B, a.splits), dim3(256), 0, st, a);
+  launch_pdl(commit_gate_kernel, dim3(a.batch), dim3(2 * a.B), 0, st, a);
 }
 
 }  // namespace polestar

@@ -11,6 +11,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ A, int lda, const T* __restrict__ W,
                                                          int ldw, float* __restrict__ C, int ldc, int M,
                                                          const int* __restrict__ m_dev, int N, int K) {
+  pdl_enter();
   __shared__ float As[SG_BK][SG_BM + 4];
   __shared__ float Ws[SG_BK][SG_BN + 4];
   const int Mr = m_dev ? min(M, *m_dev) : M;
@@ -57,7 +58,7 @@ template <typename T>
 void launch_gemm_simt(const void* A, int lda, const void* W, int ldw, float* C, int ldc, int M, const int* m_dev,
                       int N, int K, cudaStream_t st) {
   const dim3 grid((N + SG_BN - 1) / SG_BN, (M + SG_BM - 1) / SG_BM);
-  gemm_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)A, lda, (const T*)W, ldw, C, ldc, M, m_dev, N, K);
+  launch_pdl(gemm_simt_kernel<T>, dim3(grid), dim3(256), 0, st, (const T*)A, lda, (const T*)W, ldw, C, ldc, M, m_dev, N, K);
 }
 
 template void launch_gemm_simt<float>(const void*, int, const void*, int, float*, int, int, const int*, int, int,

@@ -10,6 +10,7 @@ namespace polestar {
 template <typename T>
 __global__ void gather_input_kernel(const T* __restrict__ x0, const int4* __restrict__ rows, int R,
                                     int N, int d, float* __restrict__ h) {
+  pdl_enter();
   const int r = blockIdx.x;
   if (r >= R) return;
   const int4 m = rows[r];
@@ -28,6 +29,7 @@ template <typename T>
 __global__ void gather_window_kernel(const T* __restrict__ x0, const int* __restrict__ win_pos, int nw,
                                      const int* __restrict__ fire_seqs, int N, int d, int Wmax,
                                      float* __restrict__ U, uint8_t* __restrict__ sel) {
+  pdl_enter();
   const int j = blockIdx.x, f = blockIdx.y;
   const int s = fire_seqs[f];
   const T* src = x0 + ((size_t)s * N + win_pos[j]) * d;
@@ -44,6 +46,7 @@ __global__ void rmsnorm_kernel(const float* __restrict__ h, const int* __restric
                                const int* __restrict__ m_dev, const int4* __restrict__ rows,
                                const float* __restrict__ z, int K, const T* __restrict__ gain, int R,
                                int d, float eps, T* __restrict__ a) {
+  pdl_enter();
   __shared__ float red[32];
   const int r = blockIdx.x;
   const int Rm = m_dev ? min(R, *m_dev) : R;
@@ -78,6 +81,7 @@ __global__ void rope_scatter_kernel(const float* __restrict__ qkv, int ldq, cons
                                     const uint8_t* __restrict__ write_kv, int R, int H, int Hkv, int dh,
                                     const float2* __restrict__ rope_tab, T* __restrict__ qout,
                                     T* __restrict__ kv_layer, size_t kv_seq_stride, int kvdim) {
+  pdl_enter();
   const int r = blockIdx.x;
   if (r >= R) return;
   const int4 m = rows[r];
@@ -122,6 +126,7 @@ __global__ void residual_rmsnorm_kernel(const float* h, const int* __restrict__ 
                                         const int* __restrict__ m_dev, int R, const float* __restrict__ y,
                                         int ldy, const T* __restrict__ gain, int d, float eps,
                                         float* h1, T* __restrict__ a) {
+  pdl_enter();
   __shared__ float red[32];
   const int i = blockIdx.x;
   const int Rm = m_dev ? min(R, *m_dev) : R;
@@ -145,6 +150,7 @@ __global__ void residual_rmsnorm_kernel(const float* h, const int* __restrict__ 
 template <typename T>
 __global__ void swiglu_kernel(const float* __restrict__ gu, int ldg, const int* __restrict__ m_dev, int R,
                               int F, T* __restrict__ act) {
+  pdl_enter();
   const int i = blockIdx.y;
   const int Rm = m_dev ? min(R, *m_dev) : R;
   if (i >= Rm) return;
@@ -163,6 +169,7 @@ __global__ void residual_scatter_kernel(const float* __restrict__ h1, const floa
                                         const int* __restrict__ src, const int* __restrict__ m_dev, int R,
                                         const int4* __restrict__ rows, int d, int Wmax, float* h,
                                         float* __restrict__ U) {
+  pdl_enter();
   const int i = blockIdx.x;
   const int Rm = m_dev ? min(R, *m_dev) : R;
   if (i >= Rm) return;
@@ -182,6 +189,7 @@ __global__ void residual_scatter_kernel(const float* __restrict__ h1, const floa
 template <typename T>
 __global__ void gather_T_kernel(const T* __restrict__ src, const int* __restrict__ idx,
                                 const int* __restrict__ m_dev, int R, int w, T* __restrict__ dst) {
+  pdl_enter();
   const int i = blockIdx.x;
   const int Rm = m_dev ? min(R, *m_dev) : R;
   if (i >= Rm) return;
@@ -193,6 +201,7 @@ __global__ void gather_T_kernel(const T* __restrict__ src, const int* __restrict
 // Block-entry capture of the layer inputs of window rows: Hw[seq, widx, :] = h[r].
 __global__ void capture_window_kernel(const float* __restrict__ h, const int4* __restrict__ rows, int R,
                                       int d, int Wmax, float* __restrict__ Hw_layer, size_t seq_stride) {
+  pdl_enter();
   const int r = blockIdx.x;
   if (r >= R) return;
   const int4 m = rows[r];
@@ -205,48 +214,48 @@ __global__ void capture_window_kernel(const float* __restrict__ h, const int4* _
 // ------------------------------------------------------------------ launchers
 template <typename T>
 void launch_gather_input(const void* x0, const int4* rows, int R, int N, int d, float* h, cudaStream_t st) {
-  gather_input_kernel<T><<<R, 256, 0, st>>>((const T*)x0, rows, R, N, d, h);
+  launch_pdl(gather_input_kernel<T>, dim3(R), dim3(256), 0, st, (const T*)x0, rows, R, N, d, h);
 }
 template <typename T>
 void launch_gather_window(const void* x0, const int* win_pos, int nw, const int* fire_seqs, int n_fire,
                           int N, int d, int Wmax, float* U, uint8_t* sel, cudaStream_t st) {
-  gather_window_kernel<T><<<dim3(nw, n_fire), 256, 0, st>>>((const T*)x0, win_pos, nw, fire_seqs, N, d,
-                                                             Wmax, U, sel);
+  launch_pdl(gather_window_kernel<T>, dim3(nw, n_fire), dim3(256), 0, st, (const T*)x0, win_pos, nw, fire_seqs, N, d,
+                                   Wmax, U, sel);
 }
 template <typename T>
 void launch_rmsnorm(const float* h, const int* src, const int* m_dev, const int4* rows, const float* z,
                     int K, const void* gain, int R, int d, float eps, void* a, cudaStream_t st) {
-  rmsnorm_kernel<T><<<R, 256, 0, st>>>(h, src, m_dev, rows, z, K, (const T*)gain, R, d, eps, (T*)a);
+  launch_pdl(rmsnorm_kernel<T>, dim3(R), dim3(256), 0, st, h, src, m_dev, rows, z, K, (const T*)gain, R, d, eps, (T*)a);
 }
 template <typename T>
 void launch_rope_scatter(const float* qkv, int ldq, const int4* rows, const uint8_t* write_kv, int R, int H,
                          int Hkv, int dh, const float2* tab, void* qout, void* kv_layer, size_t kv_seq_stride,
                          int kvdim, cudaStream_t st) {
-  rope_scatter_kernel<T><<<R, 256, 0, st>>>(qkv, ldq, rows, write_kv, R, H, Hkv, dh, tab, (T*)qout,
+  launch_pdl(rope_scatter_kernel<T>, dim3(R), dim3(256), 0, st, qkv, ldq, rows, write_kv, R, H, Hkv, dh, tab, (T*)qout,
                                             (T*)kv_layer, kv_seq_stride, kvdim);
 }
 template <typename T>
 void launch_residual_rmsnorm(const float* h, const int* src, const int* m_dev, int R, const float* y, int ldy,
                              const void* gain, int d, float eps, float* h1, void* a, cudaStream_t st) {
-  residual_rmsnorm_kernel<T><<<R, 256, 0, st>>>(h, src, m_dev, R, y, ldy, (const T*)gain, d, eps, h1, (T*)a);
+  launch_pdl(residual_rmsnorm_kernel<T>, dim3(R), dim3(256), 0, st, h, src, m_dev, R, y, ldy, (const T*)gain, d, eps, h1, (T*)a);
 }
 template <typename T>
 void launch_swiglu(const float* gu, int ldg, const int* m_dev, int R, int F, void* act, cudaStream_t st) {
   dim3 grid((F + 1023) / 1024, R);
-  swiglu_kernel<T><<<grid, 256, 0, st>>>(gu, ldg, m_dev, R, F, (T*)act);
+  launch_pdl(swiglu_kernel<T>, dim3(grid), dim3(256), 0, st, gu, ldg, m_dev, R, F, (T*)act);
 }
 void launch_residual_scatter(const float* h1, const float* y, int ldy, const int* src, const int* m_dev, int R,
                              const int4* rows, int d, int Wmax, float* h, float* U, cudaStream_t st) {
-  residual_scatter_kernel<<<R, 256, 0, st>>>(h1, y, ldy, src, m_dev, R, rows, d, Wmax, h, U);
+  launch_pdl(residual_scatter_kernel, dim3(R), dim3(256), 0, st, h1, y, ldy, src, m_dev, R, rows, d, Wmax, h, U);
 }
 template <typename T>
 void launch_gather_T(const void* src, const int* idx, const int* m_dev, int R, int w, void* dst,
                      cudaStream_t st) {
-  gather_T_kernel<T><<<R, 256, 0, st>>>((const T*)src, idx, m_dev, R, w, (T*)dst);
+  launch_pdl(gather_T_kernel<T>, dim3(R), dim3(256), 0, st, (const T*)src, idx, m_dev, R, w, (T*)dst);
 }
 void launch_capture_window(const float* h, const int4* rows, int R, int d, int Wmax, float* Hw_layer,
                            size_t seq_stride, cudaStream_t st) {
-  capture_window_kernel<<<R, 256, 0, st>>>(h, rows, R, d, Wmax, Hw_layer, seq_stride);
+  launch_pdl(capture_window_kernel, dim3(R), dim3(256), 0, st, h, rows, R, d, Wmax, Hw_layer, seq_stride);
 }
 
 #define INST(T)                                                                                          \

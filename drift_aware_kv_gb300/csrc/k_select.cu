@@ -13,6 +13,7 @@
 namespace polestar {
 
 __global__ void select_kernel(SelectArgs a) {
+  pdl_enter();
   __shared__ int s_topk[32][16];
   __shared__ int s_count[33];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -90,11 +91,12 @@ __global__ void select_kernel(SelectArgs a) {
   }
 }
 
-void launch_select(const SelectArgs& a, cudaStream_t st) { select_kernel<<<1, 1024, 0, st>>>(a); }
+void launch_select(const SelectArgs& a, cudaStream_t st) { launch_pdl(select_kernel, dim3(1), dim3(1024), 0, st, a); }
 
 // delta_j = mean over heads of the last-layer active-row KL (Algorithm 1 line 28)
 __global__ void delta_kernel(const float* __restrict__ kl_rows, int batch, int B, int H,
                              float* __restrict__ delta) {
+  pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= batch * B) return;
   float sum = 0.f;
@@ -103,7 +105,7 @@ __global__ void delta_kernel(const float* __restrict__ kl_rows, int batch, int B
 }
 
 void launch_delta_finalize(const float* kl_rows, int batch, int B, int H, float* delta, cudaStream_t st) {
-  delta_kernel<<<(batch * B + 127) / 128, 128, 0, st>>>(kl_rows, batch, B, H, delta);
+  launch_pdl(delta_kernel, dim3((batch * B + 127) / 128), dim3(128), 0, st, kl_rows, batch, B, H, delta);
 }
 
 }  // namespace polestar

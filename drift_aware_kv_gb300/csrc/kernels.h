@@ -4,9 +4,28 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace polestar {
+
+// Launch with programmatic dependent launch enabled (see pdl_enter()).
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- row kernels (k_rows.cu) ----
 template <typename T>
@@ -60,7 +79,15 @@ struct AttnArgs {
   // a work item never spans two sequences (nullptr: CUDA-core path by rows)
   const int4* work;
   int n_work;
+  // key splits (grid z): > 1 writes per-split partials to `part` ([splits, R, H,
+  // 5 + dh] fp32: max, sum, KL numerator, q-mass, expm1 sum, unnormalised
+  // output) and a combine kernel finishes; `part` must hold splits*R*H*(5+dh)
+  int splits;
+  float* part;
 };
+// Largest key-split count the launcher may pick for R rows with a workspace of
+// `part_floats` floats (1 when the grid is already large).
+int attention_splits(int R, int H, int N, int dh, size_t part_floats, int num_sms);
 template <typename T>
 void launch_row_attention(const AttnArgs& a, cudaStream_t st);
 

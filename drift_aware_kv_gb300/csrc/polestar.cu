@@ -74,6 +74,9 @@ struct polestar_ctx {
   float* Hw = nullptr;           // [L, b, Wmax, d]
   // workspaces
   float *h_rows = nullptr, *h1 = nullptr, *gout = nullptr, *kl_rows = nullptr;
+  float* attn_part = nullptr;   // key-split partials of the attention kernel
+  size_t attn_part_floats = 0;
+  int num_sms = 148;
   void *a_in = nullptr, *q_rows = nullptr, *attn_out = nullptr;
   uint8_t* write_kv = nullptr;
   float *U = nullptr, *dn = nullptr;
@@ -288,6 +291,35 @@ void compute_window(polestar_ctx* c, int blk) {
 }
 
 // ---- GEMM dispatch: tcgen05 tensor cores for bf16, CUDA cores for fp32 ----
+// Several projections of the same rows (Q/K/V, gate/up): one tensor-core
+// launch for bf16, one CUDA-core launch per matrix for fp32.
+template <typename T>
+polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int ldw, float* C, int ldc, int M,
+                     const int* m_dev, int N, int K);
+
+template <typename T>
+polestar_status gemm_multi(polestar_ctx* c, const void* A, int lda, int nseg, const void* const* W, const int* N,
+                           float* const* C, int ldc, int M, const int* m_dev, int K) {
+  if (M <= 0) return POLESTAR_OK;
+  if (sizeof(T) == 2 && tc_gemm_supported(K, lda, K)) {
+    double bytes = 0.0, flops = 0.0;
+    int ldw[3];
+    for (int i = 0; i < nseg; ++i) {
+      ldw[i] = K;
+      bytes += ((double)N[i] * K + (double)M * K) * sizeof(T) + (double)M * N[i] * 4.0;
+      flops += 2.0 * M * N[i] * K;
+    }
+    const int pi = prof_start(c, c->gemm_cls);
+    cudaError_t e = tc_gemm_bf16_multi(&c->tc, A, lda, nseg, W, ldw, N, C, ldc, M, m_dev, K, c->sm);
+    prof_stop(c, pi, bytes, flops);
+    ++c->launches;
+    if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 gemm: ") + cudaGetErrorString(e));
+    return POLESTAR_OK;
+  }
+  for (int i = 0; i < nseg; ++i) TRY(gemm<T>(c, A, lda, W[i], K, C[i], ldc, M, m_dev, N[i], K));
+  return POLESTAR_OK;
+}
+
 template <typename T>
 polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int ldw, float* C, int ldc, int M,
                      const int* m_dev, int N, int K) {
@@ -388,9 +420,12 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
                             (size_t)c->Wmax * d, c->sm)));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
-      TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, R, nullptr, c->qdim, d));
-      TRY(gemm<T>(c, c->a_in, d, w.wk, d, c->gout + c->qdim, c->ldg, R, nullptr, c->kvdim, d));
-      TRY(gemm<T>(c, c->a_in, d, w.wv, d, c->gout + c->qdim + c->kvdim, c->ldg, R, nullptr, c->kvdim, d));
+      {
+        const void* Ws[3] = {w.wq, w.wk, w.wv};
+        const int Ns[3] = {c->qdim, c->kvdim, c->kvdim};
+        float* Cs[3] = {c->gout, c->gout + c->qdim, c->gout + c->qdim + c->kvdim};
+        TRY(gemm_multi<T>(c, c->a_in, d, 3, Ws, Ns, Cs, c->ldg, R, nullptr, d));
+      }
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, rows, nullptr, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
                              kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm)));
       AttnArgs aa{};
@@ -420,12 +455,19 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       }
       const double attn_bytes = (double)ns * N * 2 * c->kvdim * c->esz +
                                 (l == L - 1 ? (double)ns * c->B * c->H * N * 4.0 : 0.0);
+      aa.part = c->attn_part;
+      aa.splits = attention_splits(aa.R, c->H, N, c->dh, c->attn_part_floats, c->num_sms);
       RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
+      if (c->bf16 && aa.splits > 1) ++c->launches;  // combine kernel
       TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
                                  c->a_in, c->sm)));
-      TRY(gemm<T>(c, c->a_in, d, w.w_gate, d, c->gout, c->ldg, R, nullptr, c->F, d));
-      TRY(gemm<T>(c, c->a_in, d, w.w_up, d, c->gout + c->F, c->ldg, R, nullptr, c->F, d));
+      {
+        const void* Ws[2] = {w.w_gate, w.w_up};
+        const int Ns[2] = {c->F, c->F};
+        float* Cs[2] = {c->gout, c->gout + c->F};
+        TRY(gemm_multi<T>(c, c->a_in, d, 2, Ws, Ns, Cs, c->ldg, R, nullptr, d));
+      }
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, nullptr, R, c->F, c->a_in, c->sm)));
       TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, R, nullptr, d, c->F));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_scatter(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows, nullptr,
@@ -484,7 +526,10 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
     aa.work = work_d + proxy_work_off;
     aa.n_work = proxy_work_n;
     const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz + (double)b * c->K * c->H * N * 4.0;
+    aa.part = c->attn_part;
+    aa.splits = attention_splits(aa.R, c->H, N, c->dh, c->attn_part_floats, c->num_sms);
     RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
+    if (c->bf16 && aa.splits > 1) ++c->launches;  // combine kernel
   }
   std::fill(c->cum.begin(), c->cum.end(), 0);
   std::fill(c->fire.begin(), c->fire.end(), 0);
@@ -591,9 +636,12 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       ++c->launches;  // two kernels
     }
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, zl, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
-    TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, R, nullptr, c->qdim, d));
-    TRY(gemm<T>(c, c->a_in, d, w.wk, d, c->gout + c->qdim, c->ldg, R, nullptr, c->kvdim, d));
-    TRY(gemm<T>(c, c->a_in, d, w.wv, d, c->gout + c->qdim + c->kvdim, c->ldg, R, nullptr, c->kvdim, d));
+    {
+      const void* Ws[3] = {w.wq, w.wk, w.wv};
+      const int Ns[3] = {c->qdim, c->kvdim, c->kvdim};
+      float* Cs[3] = {c->gout, c->gout + c->qdim, c->gout + c->qdim + c->kvdim};
+      TRY(gemm_multi<T>(c, c->a_in, d, 3, Ws, Ns, Cs, c->ldg, R, nullptr, d));
+    }
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, rows, c->write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
                            kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm)));
     AttnArgs aa{};
@@ -628,7 +676,10 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz +
                               (double)n_fire * c->K * c->H * N * 8.0 +
                               (l == L - 1 ? (double)b * B * c->H * N * 8.0 : 0.0);
+    aa.part = c->attn_part;
+    aa.splits = attention_splits(aa.R, c->H, N, c->dh, c->attn_part_floats, c->num_sms);
     RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
+    if (c->bf16 && aa.splits > 1) ++c->launches;  // combine kernel
     SelectArgs sa{};
     sa.batch = b;
     sa.Wmax = c->Wmax;
@@ -659,8 +710,12 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     TRY(gemm<T>(c, c->a_in, c->qdim, w.wo, c->qdim, c->gout, c->ldg, Rc, c->m_o, d, c->qdim));
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, c->o_src, c->m_o, Rc, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
                                c->a_in, c->sm)));
-    TRY(gemm<T>(c, c->a_in, d, w.w_gate, d, c->gout, c->ldg, Rc, c->m_o, c->F, d));
-    TRY(gemm<T>(c, c->a_in, d, w.w_up, d, c->gout + c->F, c->ldg, Rc, c->m_o, c->F, d));
+    {
+      const void* Ws[2] = {w.w_gate, w.w_up};
+      const int Ns[2] = {c->F, c->F};
+      float* Cs[2] = {c->gout, c->gout + c->F};
+      TRY(gemm_multi<T>(c, c->a_in, d, 2, Ws, Ns, Cs, c->ldg, Rc, c->m_o, d));
+    }
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, c->m_o, Rc, c->F, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, Rc, c->m_o, d, c->F));
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_scatter(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows, c->U,
@@ -760,6 +815,14 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
     TRY(dalloc(c, &c->h1, sizeof(float) * (size_t)R * d));
     TRY(dalloc(c, &c->gout, sizeof(float) * (size_t)R * c->ldg));
     TRY(dalloc(c, &c->kl_rows, sizeof(float) * (size_t)R * H));
+    {
+      int dev = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+      // room for 8 key splits of the largest within-block row set
+      c->attn_part_floats = (size_t)8 * within_rows * H * (5 + c->dh);
+      TRY(dalloc(c, &c->attn_part, sizeof(float) * c->attn_part_floats));
+    }
     TRY(dalloc(c, &c->a_in, c->esz * (size_t)R * std::max(std::max(d, c->F), c->qdim)));
     TRY(dalloc(c, &c->q_rows, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->attn_out, c->esz * (size_t)R * c->qdim));
@@ -1079,6 +1142,15 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   a.kl_out = kl;
   a.work = d_work;
   a.n_work = (int)work.size();
+  int nsm = 148, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const size_t pf = (size_t)8 * R * H * (5 + head_dim);
+  float* d_part = nullptr;
+  if (dtype == POLESTAR_BF16 && cudaMalloc(&d_part, sizeof(float) * pf) == cudaSuccess) {
+    a.part = d_part;
+    a.splits = attention_splits(R, H, N, head_dim, pf, nsm);
+  }
   if (dtype == POLESTAR_BF16)
     launch_row_attention<__nv_bfloat16>(a, st);
   else
@@ -1087,6 +1159,7 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   cudaFree(d_rows);
   cudaFree(d_work);
+  if (d_part) cudaFree(d_part);
   return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 

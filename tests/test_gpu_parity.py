@@ -37,6 +37,6 @@ def test_tiny_fp32_trajectory():
 def test_mini_bf16_trajectory(name):
     """Two-layer bf16 stacks (MHA and 7:1 GQA): decisions exact up to counted near
     ties; K/V, active outputs and update packets within 1e-2 relative L2."""
-    rep = _run(name, kv_tol=1e-2, act_tol=1e-2, n_steps=26)
-    assert rep.compared >= 10 and rep.fires >= 3, rep
+    rep = _run(name, kv_tol=1e-2, act_tol=1e-2, n_steps=None)
+    assert rep.compared >= 8 and rep.fires >= 3, rep
     assert rep.near_ties <= 2
