@@ -7,8 +7,8 @@
 // KL(softmax(s) || softmax(s')), against the scores s' the same row produced at
 // the previous measurement, and replaces s' by the new scores:
 //   - proxy rows at every layer (per-cluster drift D, §4.1 "Measuring Drift");
-//   - active rows at the last layer (token drift delta_j, §4.2 / Algorithm 1
-//     line 28).
+//   - active rows at the last layer (token drift delta_j, §4.2 and the
+//     last-layer drift step of Algorithm 1).
 //
 // KL is evaluated in the cancellation-free form
 //   KL = sum_j p_j d_j - log1p( sum_j q~_j expm1(d_j) / sum_j q~_j ),

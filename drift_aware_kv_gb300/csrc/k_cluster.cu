@@ -1,6 +1,6 @@
 // Window clustering and the NVFP4 residual store (Polestar-Cache, §4.1
-// "Cluster and Quantize Hidden States"; App. C.3; Algorithm 1 lines 7-8, 16-17,
-// 24-25).
+// "Cluster and Quantize Hidden States"; App. C.3; Algorithm 1's clustering,
+// quantisation, dequantisation, patch and update steps).
 //
 //   kmeans_encode_kernel  one CTA per (layer, sequence): spherical K-means on the
 //                         block-entry window inputs, member sums, residual

@@ -1,4 +1,4 @@
-// Polestar-Commit (§4.2; Algorithm 1 lines 11-12 and 27-39).
+// Polestar-Commit (§4.2; the commit phases of Algorithm 1).
 //
 //   conf_partial_kernel  split-V online (max, sum exp) of every logit row
 //                        (the logits read dominates: 2B rows x V fp32 per sequence)

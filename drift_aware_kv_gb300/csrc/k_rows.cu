@@ -164,7 +164,7 @@ __global__ void swiglu_kernel(const float* __restrict__ gu, int ldg, const int* 
 
 // Final FFN residual: out = h1[i] + y[i]; written to h[src_i] when that row is an
 // active/other row (input of the next layer), or to the update packet
-// U[seq, widx] when it is a window row (U(t, l+1), Algorithm 1 line 23).
+// U[seq, widx] when it is a window row (U(t, l+1), the update packet of §4.1).
 __global__ void residual_scatter_kernel(const float* __restrict__ h1, const float* __restrict__ y, int ldy,
                                         const int* __restrict__ src, const int* __restrict__ m_dev, int R,
                                         const int4* __restrict__ rows, int d, int Wmax, float* h,

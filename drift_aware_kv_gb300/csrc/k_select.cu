@@ -1,6 +1,6 @@
 // Drift aggregation, top-k cluster selection and gathered-row compaction
 // (Polestar-Cache, §4.1 "Measuring Drift and Layer-wise KV Updates";
-// Algorithm 1 lines 20-22).
+// Algorithm 1, drift / TopK / member-index steps).
 //
 // One CTA serves the whole batch (at most a few thousand window rows): per
 // refreshing sequence it averages the per-head proxy KL into D_c, picks the k
@@ -93,7 +93,7 @@ __global__ void select_kernel(SelectArgs a) {
 
 void launch_select(const SelectArgs& a, cudaStream_t st) { launch_pdl(select_kernel, dim3(1), dim3(1024), 0, st, a); }
 
-// delta_j = mean over heads of the last-layer active-row KL (Algorithm 1 line 28)
+// delta_j = mean over heads of the last-layer active-row KL (§4.2; Algorithm 1, last-layer drift step)
 __global__ void delta_kernel(const float* __restrict__ kl_rows, int batch, int B, int H,
                              float* __restrict__ delta) {
   pdl_enter();

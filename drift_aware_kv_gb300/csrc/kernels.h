@@ -106,7 +106,7 @@ struct KmeansArgs {
 };
 void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st);
 
-// Within-block patch of layer l's window cache (Algorithm 1 lines 16-17):
+// Within-block patch of layer l's window cache (Algorithm 1, Dequantize + Patch steps):
 // decode every window row of each firing sequence, replace the rows of the
 // previous layer's selection by their update packet, re-encode those rows,
 // and write the patched hidden states into the step's row space.

@@ -3,11 +3,11 @@
 // One polestar_calibrate_step runs Algorithm 1 of "Polestar: Drift-Aware Cache
 // Calibration and Token Commitment for Efficient Inference of Diffusion LLMs"
 // for every sequence of the batch:
-//   block entry (lines 4-12): forward over E_b (full sequence at even b, window +
+//   block entry (block-entry phase): forward over E_b (full sequence at even b, window +
 //     block at odd b) writing the K/V cache and capturing the window's layer
 //     inputs; spherical K-means + residual NVFP4 of every layer (one batched
 //     launch); proxy-attention baseline of every layer.
-//   within-block step (lines 15-26, §4.1 "Update Schedule"): the tau_upd trigger
+//   within-block step (layer loop, §4.1 "Update Schedule"): the tau_upd trigger
 //     per sequence on the host; then for every layer l, on the device: patch the
 //     window with U(t, l) and re-project its K/V, incremental centroid update,
 //     one QKV projection for active rows + window rows + proxies, attention with

@@ -5,9 +5,9 @@
  * Commitment for Efficient Inference of Diffusion LLMs" (arXiv 2607.14107):
  *   - Polestar-Cache, §4.1 (block entry, spherical K-means, residual NVFP4 of
  *     App. C.3, proxy attention + KL drift of Eq. 4, top-k clusters, sparse
- *     layer-wise update packets, update schedule) and Algorithm 1 lines 4-26;
+ *     layer-wise update packets, update schedule) and Algorithm 1;
  *   - Polestar-Commit, §4.2 (drift history, dynamic threshold, current- and
- *     suffix-block commit) and Algorithm 1 lines 11-12, 27-39;
+ *     suffix-block commit) and the commit phases of Algorithm 1;
  *   - the system design of §4.3 (pinned-host NVFP4 store, side-stream prefetch).
  *
  * Conventions (all entry points):

@@ -415,7 +415,7 @@ class PolestarOracle:
         dec = nvfp4_decode(st.codes[l], st.sbytes[l])
         return to_f32(dec + st.A[l][st.labels[l]])
 
-    # ---- block entry (Algorithm 1 lines 4-12) -----------------------------------------
+    # ---- block entry (Algorithm 1, block-entry phase; §4.1 Block entry) ---------------
     def _block_entry(self, si, st, x0, b):
         c = self.cfg
         start, end = self._span(b)
@@ -463,7 +463,7 @@ class PolestarOracle:
         st.theta = [[] for _ in range(c.block)]
         return out
 
-    # ---- within-block step (Algorithm 1 lines 15-26, update schedule of §4.1) ---------
+    # ---- within-block step (Algorithm 1, layer loop; §4.1 Update Schedule) -------------
     def _step(self, si, st, x0, b, n_unmasked):
         c = self.cfg
         start, end = self._span(b)
@@ -546,7 +546,7 @@ class PolestarOracle:
                 recs.append(self._step(si, st, x0[si], block_index, n_unmasked[si]))
         return recs
 
-    # ---- Polestar-Commit (§4.2; Algorithm 1 lines 11-12 and 27-39) ----------------------
+    # ---- Polestar-Commit (§4.2; Algorithm 1, commit phases) ------------------------------
     def commit(self, logits, masked):
         """Commit mask for the 2B rows (active block, then suffix block) of every
         sequence; also returns c, Delta and tau_d per row."""

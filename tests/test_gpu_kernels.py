@@ -117,7 +117,7 @@ def test_kmeans_nvfp4_match_oracle(P_, nw, d):
 @pytest.mark.parametrize("V", [126464, 152064, 1000])
 def test_confidence_and_entry_commit_full_vocab(V):
     """Max-softmax confidence over the full vocabulary (§2) and the block-entry
-    commit (confidence only, Algorithm 1 line 12) through the public calls."""
+    commit (confidence only, Algorithm 1 block-entry phase) through the public calls."""
     from drift_aware_kv_gb300 import polestar as P
     from drift_aware_kv_gb300 import synth
     w = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(batch=2, vocab=V, embed_vocab=V)

@@ -27,7 +27,7 @@ def test_sparse_refresh_with_all_clusters_equals_block_entry_forward():
     """Closed-form special case of §4.1: when the refresh fires, every cluster is
     selected (k = K) and the cached hidden states are exact, the sparse layer-wise
     update of the window equals a forward of window + active block over the cached
-    context, i.e. the block-entry forward at an odd block (Algorithm 1 line 5)."""
+    context, i.e. the block-entry forward at an odd block (Algorithm 1, block-entry context)."""
     cfg = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(n_layers=3, topk=8, tau_upd=0)
     W = O.weights_to_numpy(synth.make_weights(cfg))
     tr = synth.Trajectory(cfg)
