@@ -23,7 +23,7 @@ FP32, BF16 = 0, 1
 EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
             "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
             "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
-            "polestar_debug_attention", "polestar_debug_kmeans")
+            "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows")
 
 
@@ -85,6 +85,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_debug_attention.argtypes = [P, P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, P, P,
                                              P, C.c_int32, C.c_int32, P, P, C.c_int32, P]
     lib.polestar_debug_attention.restype = C.c_int
+    lib.polestar_attention_noalloc.argtypes = [P, P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, P, P,
+                                               P, C.c_int32, C.c_int32, P, P, P]
+    lib.polestar_attention_noalloc.restype = C.c_int
     lib.polestar_debug_kmeans.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_uint64,
                                           C.c_int32, P, P, P, P, P, P, P]
     lib.polestar_debug_kmeans.restype = C.c_int
@@ -252,3 +255,17 @@ def debug_kmeans(Hw, K, iters, seed, block, stream=None):
                                      _ptr(out["z"]), _ptr(out["csum"]), _ptr(out["anchor"]),
                                      _ptr(out["codes"]), _ptr(out["scales"]), C.c_void_p(st.cuda_stream)))
     return out
+
+
+def attention_noalloc(q, kv, H, Hkv, tracked_dev, prev, prev_lse, measure, store, out, kl, stream=None):
+    """Row attention + KL drift using only the library's fixed device scratch
+    (no allocation); `tracked_dev` is a CUDA uint8 tensor [R] or None."""
+    import torch
+    lib = load()
+    R = q.shape[0]
+    N = kv.shape[0]
+    dh = q.shape[1] // H
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.polestar_attention_noalloc(_ptr(q), _ptr(kv), N, H, Hkv, dh, R, _ptr(tracked_dev), _ptr(prev),
+                                          _ptr(prev_lse), int(measure), int(store), _ptr(out), _ptr(kl),
+                                          C.c_void_p(st.cuda_stream)))

@@ -207,6 +207,29 @@ polestar_status polestar_debug_attention(const void *q, const void *kv, int32_t 
                                          float *prev_lse, int32_t measure, int32_t store, void *out, float *kl,
                                          int32_t dtype, void *stream);
 
+/* ---- row attention + KL drift that allocates nothing ----
+ * The paper has no counterpart to this call; it exists for callers that cannot
+ * let a library allocate device memory: a host application that owns every
+ * device allocation through its own pool or memory cap, or a latency-critical
+ * loop in which cudaMalloc/cudaFree may synchronise the device.  It computes the
+ * same thing as polestar_debug_attention (bf16 only, head_dim 64 or 128), with
+ * two differences: `tracked` is a DEVICE array [R] of flags (or NULL: no row
+ * tracked), and all scratch (row table, work list, key-split partials) lives in
+ * fixed file-scope device arrays of this library: at most 256 rows per call and
+ * 8 MiB of partials; R > 256 is rejected with POLESTAR_ERR_INVALID_ARG, and when
+ * the partials of a wider key split would not fit, fewer splits are used.
+ * Every GPU that loads the library holds these arrays (about 8 MiB) until the
+ * library is unloaded.  The first call on a device resolves their device
+ * addresses (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Calls share the arrays, which keep the last
+ * call's contents: calls that overlap on the GPU (on different streams or
+ * devices' shared state) race.  Asynchronous on `stream`; no cudaMalloc,
+ * cudaFree or allocating library routine is called. */
+polestar_status polestar_attention_noalloc(const void *q, const void *kv, int32_t N, int32_t H, int32_t Hkv,
+                                           int32_t head_dim, int32_t R, const uint8_t *tracked, float *prev,
+                                           float *prev_lse, int32_t measure, int32_t store, void *out, float *kl,
+                                           void *stream);
+
 /* ---- spherical K-means + residual NVFP4 on caller buffers (test hook) ----
  * P independent problems of nw rows: Hw [P, nw, d] fp32 -> labels [P, nw]
  * uint8, z / csum / anchor [P, K, d] fp32, codes [P, nw, d/2], scales
