@@ -229,6 +229,12 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// 2^x with the hardware approximation (relative error ~2^-22; 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *(const uint32_t*)&v;
@@ -275,6 +281,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
     if (prev[i] && p.measure) shift[i] = *prev_lse[i];
   }
   const bool warp_live = __any_sync(0xffffffffu, live[0] || live[1]);
+  const bool warp_tracked = __any_sync(0xffffffffu, prev[0] != nullptr || prev[1] != nullptr);
 
   // Q fragments (A operand) straight from global memory
   constexpr int KT = DH / 16;
@@ -346,15 +353,20 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
           mma16816(sc[nt], qa[kt + 1], b2, b3);
         }
       }
-      // scale, mask, online softmax
+      // scores in log2 units (s2 = q.k * scale * log2 e): the attention weights
+      // use the hardware exp2; tracked rows convert back to natural units for
+      // the stored scores and the KL terms
+      const float sl2 = p.scale * 1.4426950408889634f;
+      const bool full = (j0 + AM_TK <= p.N);
       float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int j = j0 + nt * 8 + qc * 2 + (e & 1);
-          sc[nt][e] = (j < p.N) ? sc[nt][e] * p.scale : -INFINITY;
-          tmax[e >> 1] = fmaxf(tmax[e >> 1], sc[nt][e]);
+          float v = sc[nt][e] * sl2;
+          if (!full && j0 + nt * 8 + qc * 2 + (e & 1) >= p.N) v = -INFINITY;
+          sc[nt][e] = v;
+          tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
         }
       }
       float corr[2];
@@ -363,7 +375,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
         tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
         tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
         const float mnew = fmaxf(mrun[i], tmax[i]);
-        corr[i] = expf(mrun[i] - mnew);
+        corr[i] = ex2_approx(mrun[i] - mnew);
         mrun[i] = mnew;
         lsum[i] *= corr[i];
         asum[i] *= corr[i];
@@ -375,26 +387,44 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
         acc[nt][2] *= corr[1];
         acc[nt][3] *= corr[1];
       }
+      // tracked rows: fetch the whole tile's previous scores before any store
+      float spv[8][4];
+      if (warp_tracked) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = e >> 1;
+            const int j = j0 + nt * 8 + qc * 2 + (e & 1);
+            spv[nt][e] = (prev[i] && p.measure && j < p.N) ? __ldcg(prev[i] + j) : 0.f;
+          }
+      }
       uint32_t pa[4][4];  // P as A fragments: 4 k-steps of 16 keys
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         float pv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i = e >> 1;
-          const int j = j0 + nt * 8 + qc * 2 + (e & 1);
-          pv[e] = (j < p.N) ? expf(sc[nt][e] - mrun[i]) : 0.f;
-          lsum[i] += pv[e];
-          if (prev[i] && j < p.N) {
-            if (p.measure) {
-              const float sp = prev[i][j];
-              const float dj = sc[nt][e] - sp;
-              const float qt = expf(sp - shift[i]);
-              asum[i] += pv[e] * dj;
-              sqs[i] += qt;
-              esum[i] += qt * expm1f(dj);
+          pv[e] = ex2_approx(sc[nt][e] - mrun[e >> 1]);  // exp2(-inf) = 0 for masked keys
+          lsum[e >> 1] += pv[e];
+        }
+        if (warp_tracked) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = e >> 1;
+            const int j = j0 + nt * 8 + qc * 2 + (e & 1);
+            if (prev[i] && j < p.N) {
+              const float s_nat = sc[nt][e] * 0.6931471805599453f;
+              if (p.measure) {
+                const float sp = spv[nt][e];
+                const float dj = s_nat - sp;
+                const float qt = expf(sp - shift[i]);
+                asum[i] += pv[e] * dj;
+                sqs[i] += qt;
+                esum[i] += qt * expm1f(dj);
+              }
+              spv[nt][e] = s_nat;
             }
-            if (p.store) prev[i][j] = sc[nt][e];
           }
         }
         const int kt = nt >> 1;
@@ -405,6 +435,25 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
           pa[kt][2] = pack_bf16(pv[0], pv[1]);
           pa[kt][3] = pack_bf16(pv[2], pv[3]);
         }
+      }
+      if (warp_tracked && p.store) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            // two adjacent keys per row: one 8-byte store
+            const int i = e;
+            const int j = j0 + nt * 8 + qc * 2;
+            if (prev[i] && j < p.N) {
+              float* dst = prev[i] + j;
+              if (j + 1 < p.N && (((uintptr_t)dst) & 7) == 0) {
+                *(float2*)dst = make_float2(spv[nt][2 * e], spv[nt][2 * e + 1]);
+              } else {
+                dst[0] = spv[nt][2 * e];
+                if (j + 1 < p.N) dst[1] = spv[nt][2 * e + 1];
+              }
+            }
+          }
       }
       // O += P V
 #pragma unroll
@@ -466,7 +515,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(AttnArgs p) {
     }
     if (prev[i] && qc == 0) {
       if (p.measure) p.kl_out[(size_t)rows[i] * p.H + h] = asum[i] / lsum[i] - log1pf(esum[i] / sqs[i]);
-      if (p.store) *prev_lse[i] = mrun[i] + logf(lsum[i]);
+      if (p.store) *prev_lse[i] = mrun[i] * 0.6931471805599453f + logf(lsum[i]);
     }
   }
 }
@@ -492,7 +541,7 @@ __global__ void attn_combine_kernel(AttnArgs p) {
   for (int i = 0; i < NV; ++i) acc[i] = 0.f;
   for (int s = 0; s < p.splits; ++s) {
     const float* pp = base + s * stride;
-    const float w = expf(pp[0] - M);
+    const float w = ex2_approx(pp[0] - M);  // partial maxima are in log2 units
     l += pp[1] * w;
     a += pp[2] * w;
     sq += pp[3];
@@ -513,7 +562,7 @@ __global__ void attn_combine_kernel(AttnArgs p) {
     prev_lse = p.active_prev_lse + ((size_t)seq * p.B + m.w) * p.H + h;
   if (prev_lse && lane == 0) {
     if (p.measure) p.kl_out[(size_t)r * p.H + h] = a / l - log1pf(e / sq);
-    if (p.store) *prev_lse = M + logf(l);
+    if (p.store) *prev_lse = M * 0.6931471805599453f + logf(l);
   }
 }
 

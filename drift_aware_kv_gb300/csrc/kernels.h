@@ -105,6 +105,8 @@ struct KmeansArgs {
   uint8_t* scales;         // [L, batch, Wmax, d/16]
 };
 void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st);
+// Thread-block cluster size of the K-means kernel for this shape (-1: unsupported).
+int kmeans_cluster_size(int d, int nw, int K);
 
 // Within-block patch of layer l's window cache (Algorithm 1, Dequantize + Patch steps):
 // decode every window row of each firing sequence, replace the rows of the

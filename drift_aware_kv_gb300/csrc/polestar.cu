@@ -184,6 +184,11 @@ polestar_status halloc(polestar_ctx* c, P** p, size_t bytes) {
 
 int prof_start(polestar_ctx* c, int cls) {
   if (!c->prof_armed) return -1;
+  if (c->gemm_cls == POLESTAR_KC_GEMM_ENTRY) {
+    if (cls == POLESTAR_KC_ATTENTION) cls = POLESTAR_KC_ATTENTION_ENTRY;
+    if (cls == POLESTAR_KC_CLUSTER) cls = POLESTAR_KC_CLUSTER_ENTRY;
+    if (cls == POLESTAR_KC_ROWS) cls = POLESTAR_KC_ROWS_ENTRY;
+  }
   if (c->prof_used >= c->prof_cap) {
     ++c->prof_dropped[cls];
     return -1;
@@ -250,6 +255,8 @@ std::string validate(const polestar_config* c) {
   if (c->topk < 1 || c->topk > c->K) return "topk must be in [1, K]";
   if (c->tau_upd < 0 || c->hist < 0 || c->hist > 64 || c->kmeans_iters < 1) return "bad schedule parameters";
   if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return "bad rms_eps / rope_base";
+  if (polestar::kmeans_cluster_size(c->d_model, c->prefix_win + c->suffix_win, c->K) < 0)
+    return "window x d_model too large for the clustering kernel";
   return "";
 }
 
@@ -1169,7 +1176,9 @@ extern "C" polestar_status polestar_debug_kmeans(const float* Hw, int32_t P, int
                                                  uint8_t* scales, void* stream) {
   if (!Hw || !labels || !z || !csum || !anchor || !codes || !scales || P < 1 || iters < 1)
     return POLESTAR_ERR_INVALID_ARG;
-  if (nw < 1 || nw > 128 || K < 1 || K > 8 || K > nw || d < 16 || d % 16 || d > 4096) return POLESTAR_ERR_UNSUPPORTED;
+  if (nw < 1 || nw > 128 || K < 1 || K > 8 || K > nw || d < 16 || d % 16 || d > 4096 ||
+      kmeans_cluster_size(d, nw, K) < 0)
+    return POLESTAR_ERR_UNSUPPORTED;
   KmeansArgs a{};
   a.Hw = Hw;
   a.L = P;

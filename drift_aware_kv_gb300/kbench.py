@@ -37,7 +37,10 @@ def bench_gemm(a):
     A = torch.randn(a.M, a.K, device="cuda", generator=g).to(torch.bfloat16)
     W = (0.02 * torch.randn(a.N, a.K, device="cuda", generator=g)).to(torch.bfloat16)
     C = torch.empty(a.M, a.N, device="cuda")
-    ms = _time(lambda: P.debug_gemm(A, W, C, a.path), a.iters)
+    if a.path == 2:  # library comparison point (cuBLAS through torch), not a path of the product
+        ms = _time(lambda: torch.matmul(A, W.t()), a.iters)
+    else:
+        ms = _time(lambda: P.debug_gemm(A, W, C, a.path), a.iters)
     byts = (a.N * a.K + a.M * a.K) * 2 + a.M * a.N * 4
     return dict(kernel="gemm", M=a.M, N=a.N, K=a.K, path=a.path, us=ms * 1e3, GBps=byts / ms / 1e6,
                 TFLOPs=2 * a.M * a.N * a.K / ms / 1e9)
@@ -49,16 +52,16 @@ def bench_attn(a):
     dh = a.dh
     q = (1.6 * torch.randn(a.R, a.H * dh, device="cuda", generator=g)).to(torch.bfloat16)
     kv = (1.6 * torch.randn(a.N, 2, a.Hkv * dh, device="cuda", generator=g)).to(torch.bfloat16)
-    tracked = [r >= a.R - a.tracked for r in range(a.R)]
+    tracked = torch.tensor([r >= a.R - a.tracked for r in range(a.R)], dtype=torch.uint8, device="cuda")
     prev = torch.zeros(a.R, a.H, a.N, device="cuda")
     plse = torch.zeros(a.R, a.H, device="cuda")
     out = torch.empty(a.R, a.H * dh, dtype=torch.bfloat16, device="cuda")
     kl = torch.empty(a.R, a.H, device="cuda")
-    P.debug_attention(q, kv, a.H, a.Hkv, tracked, prev, plse, 0, 1, out, kl)
-    ms = _time(lambda: P.debug_attention(q, kv, a.H, a.Hkv, tracked, prev, plse, 1, 1, out, kl), a.iters)
+    P.attention_noalloc(q, kv, a.H, a.Hkv, tracked, prev, plse, 0, 1, out, kl)
+    ms = _time(lambda: P.attention_noalloc(q, kv, a.H, a.Hkv, tracked, prev, plse, 1, 1, out, kl), a.iters)
     byts = a.N * 2 * a.Hkv * dh * 2 + a.R * a.H * dh * 4 + a.tracked * a.H * a.N * 8
     return dict(kernel="attention", R=a.R, N=a.N, H=a.H, Hkv=a.Hkv, us=ms * 1e3, GBps=byts / ms / 1e6,
-                note="includes the hook's host-side table upload and synchronisation")
+                TFLOPs=4 * a.R * a.N * a.H * dh / ms / 1e9)
 
 
 def bench_kmeans(a):
@@ -74,9 +77,9 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", choices=["gemm", "attn", "kmeans"])
     ap.add_argument("--M", type=int, default=136)
-    ap.add_argument("--N", type=int, default=4096)
+    ap.add_argument("--N", type=int, default=None, help="gemm N (default 4096) / attention keys (default 768)")
     ap.add_argument("--K", type=int, default=4096)
-    ap.add_argument("--path", type=int, default=1)
+    ap.add_argument("--path", type=int, default=1, help="0 CUDA cores, 1 tcgen05, 2 cuBLAS (reference point)")
     ap.add_argument("--R", type=int, default=136)
     ap.add_argument("--H", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=32)
@@ -87,6 +90,8 @@ def main():
     ap.add_argument("--d", type=int, default=4096)
     ap.add_argument("--iters", type=int, default=20)
     a = ap.parse_args()
+    if a.N is None:
+        a.N = 4096 if a.kernel == "gemm" else 768
     from drift_aware_kv_gb300.build import build
     build()
     fn = {"gemm": bench_gemm, "attn": bench_attn, "kmeans": bench_kmeans}[a.kernel]

@@ -164,12 +164,15 @@ uint64_t polestar_launch_count(const polestar_ctx *ctx);
 typedef enum {
   POLESTAR_KC_GEMM_STEP = 0,  /* projections of within-block steps           */
   POLESTAR_KC_GEMM_ENTRY = 1, /* projections of block-entry forwards          */
-  POLESTAR_KC_ATTENTION = 2,  /* row attention + KL drift                     */
+  POLESTAR_KC_ATTENTION = 2,  /* row attention + KL drift (within-block)      */
   POLESTAR_KC_CLUSTER = 3,    /* K-means/NVFP4, window patch, centroid update */
   POLESTAR_KC_SELECT = 4,     /* top-k + compaction, delta                    */
   POLESTAR_KC_COMMIT = 5,     /* confidence + commit gate                     */
   POLESTAR_KC_ROWS = 6,       /* norms, rotary/scatter, residuals, gathers    */
-  POLESTAR_KC_COUNT = 7
+  POLESTAR_KC_ATTENTION_ENTRY = 7, /* the same three classes during block entry */
+  POLESTAR_KC_CLUSTER_ENTRY = 8,
+  POLESTAR_KC_ROWS_ENTRY = 9,
+  POLESTAR_KC_COUNT = 10
 } polestar_kernel_class;
 
 typedef struct {
