@@ -34,7 +34,8 @@ constexpr int BM = 128;         // rows per UMMA
 constexpr int BN = 128;         // columns per CTA
 constexpr int BK = 64;          // K elements per stage (one 128-byte swizzle row)
 constexpr int THREADS = 192;    // 6 warps
-constexpr int SMEM_BYTES = 200 * 1024;
+// dynamic shared memory of a configuration: stages + barriers + alignment slack
+constexpr int smem_bytes(int mt, int stages) { return stages * (mt * 128 * 64 * 2 + 128 * 64 * 2) + 2048; }
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int RED_PITCH = BN + 4;                     // fp32 staging row pitch
 
@@ -163,7 +164,7 @@ __device__ __forceinline__ float4 ld_dsmem4(const float* local_ptr, uint32_t ran
 }
 
 template <int MT, int STAGES>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -398,6 +399,7 @@ template <int MT, int STAGES>
 cudaError_t launch(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid, int splits,
                    cudaStream_t st) {
   auto kern = gemm_kernel<MT, STAGES>;
+  constexpr int SMEM_BYTES = smem_bytes(MT, STAGES);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -485,7 +487,10 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
   if (!ma) return cudaErrorInvalidValue;
   const dim3 grid(tiles, mgroups, splits);
+  // stage rings: deep (one CTA per SM) unless a single row group has more
+  // tiles than SMs, where two CTAs per SM (3 stages each) avoid a second wave
   if (MT == 2) return launch<2, 4>(ma, mb, p, grid, splits, st);
+  if (mgroups == 1 && splits == 1 && tiles > nsm) return launch<1, 3>(ma, mb, p, grid, splits, st);
   return launch<1, 6>(ma, mb, p, grid, splits, st);
 }
 

@@ -302,6 +302,7 @@ void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------- within-block
+template <typename T>
 __global__ void window_patch_kernel(PatchArgs a) {
   pdl_enter();
   __shared__ float red[32];
@@ -335,12 +336,19 @@ __global__ void window_patch_kernel(PatchArgs a) {
       if (patched) dnrow[g * 16 + e] = old;  // stash old value; finished below
     }
   }
+  ss_old = block_sum(ss_old, red);
+  ss_new = block_sum(ss_new, red);
+  // fused input of the layer's projections: RMSNorm of the (patched) row
+  {
+    const float inv = 1.f / sqrtf(ss_new / (float)d + a.eps);
+    const T* gain = (const T*)a.gain;
+    T* ao = (T*)a.a_out + (size_t)row * d;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) ao[k] = from_f<T>(hrow[k] * inv * to_f<T>(gain[k]));
+  }
   if (!patched) {
     if (threadIdx.x == 0) a.write_kv[row] = 0;
     return;
   }
-  ss_old = block_sum(ss_old, red);
-  ss_new = block_sum(ss_new, red);
   const float io = 1.f / sqrtf(ss_old), in = 1.f / sqrtf(ss_new);
   // pass 2: direction change and re-encoding of the new residual
   for (int g = threadIdx.x; g < ng; g += blockDim.x) {
@@ -388,7 +396,9 @@ __global__ void centroid_sum_kernel(PatchArgs a) {
     if (c < a.K) cs[(size_t)c * a.d + k] += acc[c];
 }
 
-// z_c = s_c / |s_c| for every cluster of a refreshing sequence
+// z_c = s_c / |s_c| for every cluster of a refreshing sequence, and the proxy
+// row's projection input T(RMSNorm(z_c) * gain)
+template <typename T>
 __global__ void centroid_norm_kernel(PatchArgs a) {
   pdl_enter();
   __shared__ float red[32];
@@ -399,15 +409,31 @@ __global__ void centroid_norm_kernel(PatchArgs a) {
   for (int k = threadIdx.x; k < a.d; k += blockDim.x) ss = fmaf(cs[k], cs[k], ss);
   ss = block_sum(ss, red);
   const float nrm = sqrtf(ss);
-  for (int k = threadIdx.x; k < a.d; k += blockDim.x) z[k] = cs[k] / nrm;
+  float zz = 0.f;
+  for (int k = threadIdx.x; k < a.d; k += blockDim.x) {
+    const float v = cs[k] / nrm;
+    z[k] = v;
+    zz = fmaf(v, v, zz);
+  }
+  zz = block_sum(zz, red);
+  const float inv = 1.f / sqrtf(zz / (float)a.d + a.eps);
+  const T* gain = (const T*)a.gain;
+  T* ao = (T*)a.a_out + (size_t)(a.proxy_row[s] + c) * a.d;
+  for (int k = threadIdx.x; k < a.d; k += blockDim.x) ao[k] = from_f<T>(z[k] * inv * to_f<T>(gain[k]));
 }
 
+template <typename T>
 void launch_window_patch(const PatchArgs& a, cudaStream_t st) {
-  launch_pdl(window_patch_kernel, dim3(a.nw, a.n_fire), dim3(256), 0, st, a);
+  launch_pdl(window_patch_kernel<T>, dim3(a.nw, a.n_fire), dim3(256), 0, st, a);
 }
+template <typename T>
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st) {
   launch_pdl(centroid_sum_kernel, dim3((a.d + 127) / 128, a.n_fire), dim3(128), 0, st, a);
-  launch_pdl(centroid_norm_kernel, dim3(a.K, a.n_fire), dim3(256), 0, st, a);
+  launch_pdl(centroid_norm_kernel<T>, dim3(a.K, a.n_fire), dim3(256), 0, st, a);
 }
+template void launch_window_patch<float>(const PatchArgs&, cudaStream_t);
+template void launch_window_patch<__nv_bfloat16>(const PatchArgs&, cudaStream_t);
+template void launch_centroid_update<float>(const PatchArgs&, cudaStream_t);
+template void launch_centroid_update<__nv_bfloat16>(const PatchArgs&, cudaStream_t);
 
 }  // namespace polestar

@@ -6,11 +6,14 @@
 
 namespace polestar {
 
-// h[r, :] = x0[seq_r, pos_r, :] (storage type -> fp32), rows of kind NONE zeroed.
+// h[r, :] = x0[seq_r, pos_r, :] (storage type -> fp32), rows of kind NONE zeroed;
+// with `gain` also a[r] = T(RMSNorm(h[r]) * gain) (the first projection's input).
 template <typename T>
 __global__ void gather_input_kernel(const T* __restrict__ x0, const int4* __restrict__ rows, int R,
-                                    int N, int d, float* __restrict__ h) {
+                                    int N, int d, float* __restrict__ h, const T* __restrict__ gain, float eps,
+                                    T* __restrict__ a) {
   pdl_enter();
+  __shared__ float red[32];
   const int r = blockIdx.x;
   if (r >= R) return;
   const int4 m = rows[r];
@@ -20,7 +23,17 @@ __global__ void gather_input_kernel(const T* __restrict__ x0, const int4* __rest
     return;
   }
   const T* src = x0 + ((size_t)m.x * N + m.y) * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = to_f<T>(src[i]);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = to_f<T>(src[i]);
+    dst[i] = v;
+    ss += v * v;
+  }
+  if (!gain) return;
+  ss = block_sum(ss, red);
+  const float inv = 1.f / sqrtf(ss / (float)d + eps);
+  T* ao = a + (size_t)r * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) ao[i] = from_f<T>(dst[i] * inv * to_f<T>(gain[i]));
 }
 
 // Gather window rows of firing sequences from x0 into the update-packet buffer
@@ -165,24 +178,36 @@ __global__ void swiglu_kernel(const float* __restrict__ gu, int ldg, const int* 
 // Final FFN residual: out = h1[i] + y[i]; written to h[src_i] when that row is an
 // active/other row (input of the next layer), or to the update packet
 // U[seq, widx] when it is a window row (U(t, l+1), the update packet of §4.1).
+// With `gain` (the next layer's attention-norm gain), rows written to h also
+// get a[src_i] = T(RMSNorm(out) * gain), the next projection's input.
+template <typename T>
 __global__ void residual_scatter_kernel(const float* __restrict__ h1, const float* __restrict__ y, int ldy,
                                         const int* __restrict__ src, const int* __restrict__ m_dev, int R,
                                         const int4* __restrict__ rows, int d, int Wmax, float* h,
-                                        float* __restrict__ U) {
+                                        float* __restrict__ U, const T* __restrict__ gain, float eps,
+                                        T* __restrict__ an) {
   pdl_enter();
+  __shared__ float red[32];
   const int i = blockIdx.x;
   const int Rm = m_dev ? min(R, *m_dev) : R;
   if (i >= Rm) return;
   const int r = src ? src[i] : i;
   const int4 m = rows[r];
-  float* dst;
-  if (m.z == ROW_WINDOW && U)
-    dst = U + ((size_t)m.x * Wmax + m.w) * d;
-  else
-    dst = h + (size_t)r * d;
+  const bool to_u = (m.z == ROW_WINDOW && U);
+  float* dst = to_u ? U + ((size_t)m.x * Wmax + m.w) * d : h + (size_t)r * d;
   const float* a = h1 + (size_t)i * d;
   const float* b = y + (size_t)i * ldy;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) dst[k] = a[k] + b[k];
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) {
+    const float v = a[k] + b[k];
+    dst[k] = v;
+    ss += v * v;
+  }
+  if (!gain || to_u) return;  // uniform per block
+  ss = block_sum(ss, red);
+  const float inv = 1.f / sqrtf(ss / (float)d + eps);
+  T* ao = an + (size_t)r * d;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) ao[k] = from_f<T>(dst[k] * inv * to_f<T>(gain[k]));
 }
 
 // dst[i, :] = src[idx[i], :] (storage type rows)
@@ -213,8 +238,10 @@ __global__ void capture_window_kernel(const float* __restrict__ h, const int4* _
 
 // ------------------------------------------------------------------ launchers
 template <typename T>
-void launch_gather_input(const void* x0, const int4* rows, int R, int N, int d, float* h, cudaStream_t st) {
-  launch_pdl(gather_input_kernel<T>, dim3(R), dim3(256), 0, st, (const T*)x0, rows, R, N, d, h);
+void launch_gather_input(const void* x0, const int4* rows, int R, int N, int d, float* h, cudaStream_t st,
+                         const void* gain, float eps, void* a) {
+  launch_pdl(gather_input_kernel<T>, dim3(R), dim3(256), 0, st, (const T*)x0, rows, R, N, d, h, (const T*)gain,
+             eps, (T*)a);
 }
 template <typename T>
 void launch_gather_window(const void* x0, const int* win_pos, int nw, const int* fire_seqs, int n_fire,
@@ -244,9 +271,12 @@ void launch_swiglu(const float* gu, int ldg, const int* m_dev, int R, int F, voi
   dim3 grid((F + 1023) / 1024, R);
   launch_pdl(swiglu_kernel<T>, dim3(grid), dim3(256), 0, st, gu, ldg, m_dev, R, F, (T*)act);
 }
+template <typename T>
 void launch_residual_scatter(const float* h1, const float* y, int ldy, const int* src, const int* m_dev, int R,
-                             const int4* rows, int d, int Wmax, float* h, float* U, cudaStream_t st) {
-  launch_pdl(residual_scatter_kernel, dim3(R), dim3(256), 0, st, h1, y, ldy, src, m_dev, R, rows, d, Wmax, h, U);
+                             const int4* rows, int d, int Wmax, float* h, float* U, cudaStream_t st,
+                             const void* gain, float eps, void* an) {
+  launch_pdl(residual_scatter_kernel<T>, dim3(R), dim3(256), 0, st, h1, y, ldy, src, m_dev, R, rows, d, Wmax, h, U,
+             (const T*)gain, eps, (T*)an);
 }
 template <typename T>
 void launch_gather_T(const void* src, const int* idx, const int* m_dev, int R, int w, void* dst,
@@ -259,7 +289,11 @@ void launch_capture_window(const float* h, const int4* rows, int R, int d, int W
 }
 
 #define INST(T)                                                                                          \
-  template void launch_gather_input<T>(const void*, const int4*, int, int, int, float*, cudaStream_t);   \
+  template void launch_gather_input<T>(const void*, const int4*, int, int, int, float*, cudaStream_t,     \
+                                       const void*, float, void*);                                       \
+  template void launch_residual_scatter<T>(const float*, const float*, int, const int*, const int*, int,  \
+                                           const int4*, int, int, float*, float*, cudaStream_t,          \
+                                           const void*, float, void*);                                   \
   template void launch_gather_window<T>(const void*, const int*, int, const int*, int, int, int, int,    \
                                         float*, uint8_t*, cudaStream_t);                                 \
   template void launch_rmsnorm<T>(const float*, const int*, const int*, const int4*, const float*, int,  \

@@ -28,8 +28,10 @@ inline void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // ---- row kernels (k_rows.cu) ----
+// gain != nullptr also writes a[r] = T(RMSNorm(h[r]) * gain)
 template <typename T>
-void launch_gather_input(const void* x0, const int4* rows, int R, int N, int d, float* h, cudaStream_t st);
+void launch_gather_input(const void* x0, const int4* rows, int R, int N, int d, float* h, cudaStream_t st,
+                         const void* gain = nullptr, float eps = 0.f, void* a = nullptr);
 template <typename T>
 void launch_gather_window(const void* x0, const int* win_pos, int nw, const int* fire_seqs, int n_fire, int N,
                           int d, int Wmax, float* U, uint8_t* sel, cudaStream_t st);
@@ -45,8 +47,11 @@ void launch_residual_rmsnorm(const float* h, const int* src, const int* m_dev, i
                              const void* gain, int d, float eps, float* h1, void* a, cudaStream_t st);
 template <typename T>
 void launch_swiglu(const float* gu, int ldg, const int* m_dev, int R, int F, void* act, cudaStream_t st);
+// gain != nullptr: rows written to h also get an[row] = T(RMSNorm(out) * gain)
+template <typename T>
 void launch_residual_scatter(const float* h1, const float* y, int ldy, const int* src, const int* m_dev, int R,
-                             const int4* rows, int d, int Wmax, float* h, float* U, cudaStream_t st);
+                             const int4* rows, int d, int Wmax, float* h, float* U, cudaStream_t st,
+                             const void* gain = nullptr, float eps = 0.f, void* an = nullptr);
 template <typename T>
 void launch_gather_T(const void* src, const int* idx, const int* m_dev, int R, int w, void* dst,
                      cudaStream_t st);
@@ -127,8 +132,16 @@ struct PatchArgs {
   float* dn;               // [batch, Wmax, d]: normalise(new) - normalise(old) for patched rows
   float* csum;             // layer base [batch, K, d]
   float* z;                // layer base [batch, K, d]
+  // fused projection input: a_out[row] = T(RMSNorm(row) * gain) for every
+  // patched window row and every proxy row (proxy rows start at proxy_row[s])
+  const void* gain;
+  float eps;
+  void* a_out;
+  const int* proxy_row;
 };
+template <typename T>
 void launch_window_patch(const PatchArgs& a, cudaStream_t st);
+template <typename T>
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st);
 
 // ---- selection (k_select.cu) ----

@@ -477,8 +477,9 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       }
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, nullptr, R, c->F, c->a_in, c->sm)));
       TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, R, nullptr, d, c->F));
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_scatter(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows, nullptr,
-                              c->sm)));
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
+          (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows,
+                                      nullptr, c->sm)));
     }
   }
   // spherical K-means + residual NVFP4 for every (layer, sequence)
@@ -608,7 +609,8 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
   const float eps = c->cfg.rms_eps;
   const int n_active = b * B;
 
-  RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_input<T>(x0, rows, n_active, N, d, c->h_rows, c->sm)));
+  RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
+      (launch_gather_input<T>(x0, rows, n_active, N, d, c->h_rows, c->sm, c->W[0].attn_norm, eps, c->a_in)));
   uint8_t* sel_prev = c->sel_a;
   uint8_t* sel_cur = c->sel_b;
   if (n_fire > 0) {
@@ -638,11 +640,17 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       pa.dn = c->dn;
       pa.csum = c->csum + (size_t)l * b * c->K * d;
       pa.z = zl;
-      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_window_patch(pa, c->sm)));
-      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_centroid_update(pa, c->sm)));
+      pa.gain = w.attn_norm;
+      pa.eps = eps;
+      pa.a_out = c->a_in;
+      pa.proxy_row = proxy_row_d;
+      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_window_patch<T>(pa, c->sm)));
+      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_centroid_update<T>(pa, c->sm)));
       ++c->launches;  // two kernels
     }
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, zl, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
+    // the projections' input rows were normalised by their producers: active
+    // rows by the previous layer's final residual (or the input gather), window
+    // rows by the patch, proxy rows by the centroid update
     {
       const void* Ws[3] = {w.wq, w.wk, w.wv};
       const int Ns[3] = {c->qdim, c->kvdim, c->kvdim};
@@ -725,8 +733,9 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     }
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, c->m_o, Rc, c->F, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, Rc, c->m_o, d, c->F));
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_scatter(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows, c->U,
-                            c->sm)));
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
+        (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows,
+                                    c->U, c->sm, l + 1 < L ? c->W[l + 1].attn_norm : nullptr, eps, c->a_in)));
     std::swap(sel_prev, sel_cur);
   }
   c->sel_last = sel_prev;  // selection of the last layer
