@@ -22,6 +22,8 @@
 
 #include <algorithm>
 #include <cstring>
+#include <map>
+#include <mutex>
 
 #include "common.cuh"
 #include "gemm_tc.h"
@@ -34,8 +36,6 @@ constexpr int BM = 128;         // rows per UMMA
 constexpr int BN = 128;         // columns per CTA
 constexpr int BK = 64;          // K elements per stage (one 128-byte swizzle row)
 constexpr int THREADS = 192;    // 6 warps
-// dynamic shared memory of a configuration: stages + barriers + alignment slack
-constexpr int smem_bytes(int mt, int stages) { return stages * (mt * 128 * 64 * 2 + 128 * 64 * 2) + 2048; }
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int RED_PITCH = BN + 4;                     // fp32 staging row pitch
 
@@ -51,6 +51,12 @@ struct Params {
   int seg_start[4];
   int seg_N[3];
   float* seg_C[3];
+  // ring depth and TMEM columns; row-tiled kernel: columns per tile (bn);
+  // weight-stationary kernel: row box (np)
+  int bn;
+  int np;
+  int stages;
+  int tmem_cols;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -109,19 +115,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: kind::f16, bf16 x bf16 -> fp32, both K-major, M = 128, N = BN.
-__host__ __device__ constexpr uint32_t instr_desc() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
-      "l"(adesc), "l"(bdesc), "r"(instr_desc()), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -163,25 +156,61 @@ __device__ __forceinline__ float4 ld_dsmem4(const float* local_ptr, uint32_t ran
   return v;
 }
 
-template <int MT, int STAGES>
+__host__ __device__ constexpr uint32_t instr_desc_ws(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_id(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Row-tiled kernel: the gathered rows are the MMA's M side (MT sub-tiles of
+// 128), a CTA owns p.bn (a multiple of 16, at most 256) output columns of one
+// weight segment as the MMA's N side.  The column width is chosen per launch
+// so that the tiles fill the SMs evenly (no second, mostly idle wave).
+constexpr int RT_MAX_STAGES = 8;
+__host__ __device__ constexpr int rt_stage_bytes(int mt, int bn) { return mt * BM * BK * 2 + bn * BK * 2; }
+__host__ __device__ constexpr int rt_smem_bytes(int mt, int bn, int stages) {
+  return stages * rt_stage_bytes(mt, bn) + 2048;
+}
+
+template <int MT>
 __global__ void __launch_bounds__(THREADS)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   constexpr int A_BYTES = BM * BK * 2;  // 16 KB per row sub-tile
-  constexpr int B_BYTES = BN * BK * 2;  // 16 KB
-  constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  const int bn = p.bn, STAGES = p.stages;
+  const int STAGE_BYTES = rt_stage_bytes(MT, bn);
+  const int pitch = bn + 4;             // fp32 staging row pitch of the split-K reduction
   uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* accum = empty + STAGES;
+  uint64_t* empty = full + RT_MAX_STAGES;
+  uint64_t* accum = empty + RT_MAX_STAGES;
   uint32_t* tmem_slot = (uint32_t*)(accum + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
   const int seg = (tile >= p.seg_start[1]) + (tile >= p.seg_start[2]);
-  const int n0 = (tile - p.seg_start[seg]) * BN;
+  const int n0 = (tile - p.seg_start[seg]) * bn;
   const int segN = p.seg_N[seg];
   float* const Cseg = p.seg_C[seg];
   const CUtensorMap* tmB = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
@@ -204,7 +233,7 @@ __global__ void __launch_bounds__(THREADS)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(MT * BN));
+                 "r"(p.tmem_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -250,6 +279,7 @@ __global__ void __launch_bounds__(THREADS)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
+      const uint32_t idesc = instr_desc_ws(bn);  // M = 128, N = bn
       for (int i = 0; i < nk; ++i) {
         const int s = i % STAGES;
         if (!mbar_wait(smem_u32(&full[s]), (i / STAGES) & 1, p.err, 2, abort_flag)) break;
@@ -260,8 +290,8 @@ __global__ void __launch_bounds__(THREADS)
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            umma(tmem + mt * BN, smem_desc(st + mt * A_BYTES + kk * 32), smem_desc(bst + kk * 32),
-                 (i > 0 || kk > 0) ? 1u : 0u);
+            umma_id(tmem + mt * bn, smem_desc(st + mt * A_BYTES + kk * 32), smem_desc(bst + kk * 32), idesc,
+                    (i > 0 || kk > 0) ? 1u : 0u);
           }
         }
         umma_commit(smem_u32(&empty[s]));  // frees the stage once these MMAs have read it
@@ -279,23 +309,24 @@ __global__ void __launch_bounds__(THREADS)
     ok = (nk > 0) && mbar_wait(smem_u32(accum), 0, p.err, 3, abort_flag);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   }
+  const bool vec = ((p.ldc & 3) == 0) && ((((uintptr_t)Cseg) & 15) == 0);
   if (p.splits == 1) {
     if (epi && ok) {
 #pragma unroll 1
       for (int mt = 0; mt < MT; ++mt) {
         const int row = m0 + mt * BM + q * 32 + lane;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + mt * BN + c, v);
+        for (int c = 0; c < bn; c += 16) {
+          float v[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + mt * bn + c, v);
           if (row < M_eff) {
             float* dst = Cseg + (size_t)row * p.ldc + n0 + c;
-            if (n0 + c + 32 <= segN && ((p.ldc & 3) == 0) && ((((uintptr_t)Cseg) & 15) == 0)) {
+            if (n0 + c + 16 <= segN && vec) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 4) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              for (int j = 0; j < 16; j += 4) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
+              for (int j = 0; j < 16; ++j)
                 if (n0 + c + j < segN) dst[j] = v[j];
             }
           }
@@ -304,7 +335,7 @@ __global__ void __launch_bounds__(THREADS)
     }
   } else {
     // split-K: stage partials in shared memory, reduce across the cluster
-    float* red = (float*)smem;  // [BM][RED_PITCH] fp32, pipeline buffers are idle now
+    float* red = (float*)smem;  // [BM][pitch] fp32, pipeline buffers are idle now
     const uint32_t rank = cluster_rank();
 #pragma unroll 1
     for (int mt = 0; mt < MT; ++mt) {
@@ -312,32 +343,33 @@ __global__ void __launch_bounds__(THREADS)
       if (epi) {
         const int r = q * 32 + lane;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          if (ok) tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + mt * BN + c, v);
+        for (int c = 0; c < bn; c += 16) {
+          float v[16];
+          if (ok) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + mt * bn + c, v);
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *(float4*)(red + r * RED_PITCH + c + j) =
+          for (int j = 0; j < 16; j += 4)
+            *(float4*)(red + r * pitch + c + j) =
                 ok ? make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       cluster_sync();
       // this CTA reduces its share of the sub-tile's rows, splits in fixed order
       const int rbeg = (int)rank * BM / p.splits, rend = ((int)rank + 1) * BM / p.splits;
-      for (int idx = threadIdx.x; idx < (rend - rbeg) * (BN / 4); idx += THREADS) {
-        const int rr = rbeg + idx / (BN / 4), cc = (idx % (BN / 4)) * 4;
+      const int c4 = bn / 4;
+      for (int idx = threadIdx.x; idx < (rend - rbeg) * c4; idx += THREADS) {
+        const int rr = rbeg + idx / c4, cc = (idx % c4) * 4;
         const int row = m0 + mt * BM + rr;
         if (row >= M_eff) continue;
-        float4 acc = ld_dsmem4(red + rr * RED_PITCH + cc, 0u);
+        float4 acc = ld_dsmem4(red + rr * pitch + cc, 0u);
         for (int s = 1; s < p.splits; ++s) {
-          const float4 v = ld_dsmem4(red + rr * RED_PITCH + cc, (uint32_t)s);
+          const float4 v = ld_dsmem4(red + rr * pitch + cc, (uint32_t)s);
           acc.x += v.x;
           acc.y += v.y;
           acc.z += v.z;
           acc.w += v.w;
         }
         float* dst = Cseg + (size_t)row * p.ldc + n0 + cc;
-        if (n0 + cc + 4 <= segN && ((p.ldc & 3) == 0) && ((((uintptr_t)Cseg) & 15) == 0)) {
+        if (n0 + cc + 4 <= segN && vec) {
           *(float4*)dst = acc;
         } else {
           const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
@@ -358,7 +390,552 @@ __global__ void __launch_bounds__(THREADS)
   __syncthreads();
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MT * BN));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
+  }
+}
+
+// ---------------------------------------------------------------- weight-stationary tile
+// For at most 256 rows the operands swap roles: the 128 x 64 W tile is the
+// MMA's A operand (M = 128 output features) and the activation rows are its B
+// operand (N = the live row count rounded up to 16, read from m_dev on the
+// device), so the accumulator is [128 features][np tokens] and the tensor work
+// per streamed weight byte follows the live rows instead of a 128/256-row
+// padding.  The TMA box still covers p.np rows; rows past M are zero-filled.
+constexpr int WS_MAX_STAGES = 8;
+constexpr int WS_W_BYTES = BN * BK * 2;  // 16 KB weight tile per stage
+__host__ __device__ constexpr int ws_stage_bytes(int np) { return WS_W_BYTES + np * BK * 2; }
+__host__ __device__ constexpr int ws_smem_bytes(int np, int stages) { return stages * ws_stage_bytes(np) + 2048; }
+
+__global__ void __launch_bounds__(THREADS)
+    gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int NP = p.np, STAGES = p.stages;
+  const int STAGE_BYTES = ws_stage_bytes(NP);
+  uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + WS_MAX_STAGES;
+  uint64_t* accum = empty + WS_MAX_STAGES;
+  uint32_t* tmem_slot = (uint32_t*)(accum + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  const int seg = (tile >= p.seg_start[1]) + (tile >= p.seg_start[2]);
+  const int n0 = (tile - p.seg_start[seg]) * BN;
+  const int segN = p.seg_N[seg];
+  float* const Cseg = p.seg_C[seg];
+  const CUtensorMap* tmB = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
+  const int split = blockIdx.z;
+  const int kt0 = (int)((long long)split * p.ktiles / p.splits);
+  const int kt1 = (int)((long long)(split + 1) * p.ktiles / p.splits);
+  const int nk = kt1 - kt0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(accum), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(p.tmem_cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  // weight tiles of the first stages go out before waiting for the producer of A
+  const int npre = nk < STAGES ? nk : STAGES;
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < npre; ++i) {
+      const uint32_t fb = smem_u32(&full[i]);
+      mbar_expect_tx(fb, STAGE_BYTES);
+      tma_load_2d(smem_u32(smem + i * STAGE_BYTES), tmB, (kt0 + i) * BK, n0, fb);
+    }
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
+  const int np_eff = min(NP, max(16, (M_eff + 15) & ~15));
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      for (int i = 0; i < npre; ++i)
+        tma_load_2d(smem_u32(smem + i * STAGE_BYTES) + WS_W_BYTES, &tmA, (kt0 + i) * BK, 0, smem_u32(&full[i]));
+      for (int i = npre; i < nk; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) break;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_expect_tx(fb, STAGE_BYTES);
+        const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+        const int kx = (kt0 + i) * BK;
+        tma_load_2d(st, tmB, kx, n0, fb);
+        tma_load_2d(st + WS_W_BYTES, &tmA, kx, 0, fb);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = instr_desc_ws(np_eff);
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(smem_u32(&full[s]), (i / STAGES) & 1, p.err, 2, abort_flag)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_id(tmem, smem_desc(st + kk * 32), smem_desc(st + WS_W_BYTES + kk * 32), idesc,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(smem_u32(&empty[s]));
+      }
+      umma_commit(smem_u32(accum));
+    }
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: TMEM lane = output feature, column = row
+  const bool epi = warp >= 2;
+  const int q = warp & 3;
+  bool ok = true;
+  if (epi) {
+    ok = (nk > 0) && mbar_wait(smem_u32(accum), 0, p.err, 3, abort_flag);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  }
+  const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+  if (p.splits == 1) {
+    if (epi && ok) {
+      const int f = n0 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < np_eff; c += 16) {
+        float v[16];
+        tmem_ld16(tq + c, v);
+        if (f < segN) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c + j < M_eff) Cseg[(size_t)(c + j) * p.ldc + f] = v[j];
+        }
+      }
+    }
+  } else {
+    // split-K: stage [rows][features] partials, reduce across the cluster in rank order
+    float* red = (float*)smem;
+    const uint32_t rank = cluster_rank();
+    __syncthreads();
+    if (epi) {
+#pragma unroll 1
+      for (int c = 0; c < np_eff; c += 16) {
+        float v[16];
+        if (ok) tmem_ld16(tq + c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) red[(c + j) * RED_PITCH + q * 32 + lane] = ok ? v[j] : 0.f;
+      }
+    }
+    cluster_sync();
+    const int rbeg = (int)rank * np_eff / p.splits, rend = ((int)rank + 1) * np_eff / p.splits;
+    for (int idx = threadIdx.x; idx < (rend - rbeg) * (BN / 4); idx += THREADS) {
+      const int row = rbeg + idx / (BN / 4), cc = (idx % (BN / 4)) * 4;
+      if (row >= M_eff) continue;
+      float4 acc = ld_dsmem4(red + row * RED_PITCH + cc, 0u);
+      for (int s = 1; s < p.splits; ++s) {
+        const float4 v = ld_dsmem4(red + row * RED_PITCH + cc, (uint32_t)s);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      float* dst = Cseg + (size_t)row * p.ldc + n0 + cc;
+      if (n0 + cc + 4 <= segN && ((p.ldc & 3) == 0) && ((((uintptr_t)Cseg) & 15) == 0)) {
+        *(float4*)dst = acc;
+      } else {
+        const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+        for (int j = 0; j < 4; ++j)
+          if (n0 + cc + j < segN) dst[j] = vv[j];
+      }
+    }
+    cluster_sync();
+  }
+  if (*abort_flag && warp == 0 && lane == 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < 20000000LL) {
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
+  }
+}
+
+// ---------------------------------------------------------------- persistent stream-K, weight-stationary
+// One CTA per SM.  The (tile, k-tile) units of all weight segments are laid
+// out tile-major and cut into gridDim.x equal contiguous ranges, so every SM
+// streams the same number of weight bytes and its load ring never drains at a
+// tile boundary.  A CTA's run of units inside one tile is a "piece"; pieces
+// alternate between two TMEM accumulators so the epilogue of one overlaps the
+// MMAs of the next.  A tile covered by one piece is written straight to C.  A
+// tile cut between CTAs is finished by whichever of them arrives last at the
+// tile's counter: every piece is stored to the workspace first, and the last
+// arrival adds the others to its own in CTA order (deterministic; no CTA ever
+// waits for another).  A CTA takes its (possibly cut) first and last tiles
+// before its whole middle tiles, so both holders of a cut tile reach it early
+// and the fix-up overlaps the weight stream instead of trailing it.
+//
+// Weights come either through the 2D tensor map (128-byte row segments of 128
+// rows per load) or, when the caller supplies them in the packed tile layout
+// (pack_weight_tiles), as one contiguous 16 KB bulk copy per unit: a CTA's
+// units are then one contiguous stretch of memory.
+constexpr int SK_MAX_STAGES = 12;
+constexpr int UNIT_BYTES = BN * BK * 2;  // one packed 128 x 64 bf16 tile: 16 KB
+
+struct SkParams {
+  int M;
+  const int* m_dev;
+  int ldc;
+  int ktiles;        // k-tiles per tile
+  long long units;   // tiles * ktiles
+  int* err;
+  int seg_start[4];
+  int seg_N[3];
+  float* seg_C[3];
+  const uint8_t* wpack[3];  // packed weights per segment (null: tensor map)
+  int np, stages, acc_cols;
+  float* work;       // [gridDim.x][2][np][BN] partial pieces
+  int* counters;     // [tiles][4] arrivals per tile and epilogue warp, zero between launches
+};
+
+__device__ __forceinline__ long long sk_start(int c, long long units, int G) { return (long long)c * units / G; }
+
+// CTA whose unit range holds unit u
+__device__ __forceinline__ int sk_owner(long long u, long long units, int G) {
+  int c = (int)((u * G) / units);
+  while (c + 1 < G && sk_start(c + 1, units, G) <= u) ++c;
+  while (c > 0 && sk_start(c, units, G) > u) --c;
+  return c;
+}
+
+// Tile of the CTA's piece number `idx`: first tile, last tile, then the middle.
+__device__ __forceinline__ int sk_piece_tile(int idx, int t_first, int t_last) {
+  if (idx == 0) return t_first;
+  if (idx == 1) return t_last;
+  return t_first + idx - 1;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Warp roles: 0 and 6 load (each owns every other unit of the ring, so one
+// late copy never holds up the other stream of requests), 1 issues the MMAs,
+// 2-5 drain TMEM.
+constexpr int SK_THREADS = 224;
+
+template <bool PACKED>
+__global__ void __launch_bounds__(SK_THREADS, 1)
+    gemm_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, SkParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int NP = p.np, STAGES = p.stages;
+  const int STAGE_BYTES = ws_stage_bytes(NP);
+  uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + SK_MAX_STAGES;
+  uint64_t* acc_full = empty + SK_MAX_STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2]
+  uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const long long u0 = sk_start(cta, p.units, G), u1 = sk_start(cta + 1, p.units, G);
+  const int kt = p.ktiles;
+  const int t_first = (int)(u0 / kt), t_last = (int)((u1 - 1) / kt);
+  const int npieces = t_last - t_first + 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(2 * p.acc_cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  // unit range of a piece
+  auto piece_units = [&](int idx, int& t, long long& ua, long long& ub) {
+    t = sk_piece_tile(idx, t_first, t_last);
+    ua = max(u0, (long long)t * kt);
+    ub = min(u1, (long long)(t + 1) * kt);
+  };
+  // weight load of unit u (tile t) into the stage at smem address dst
+  auto load_w = [&](long long u, int t, uint32_t dst, uint32_t bar) {
+    const int sg = (t >= p.seg_start[1]) + (t >= p.seg_start[2]);
+    const int kk = (int)(u - (long long)t * kt);
+    if (PACKED) {
+      const uint8_t* src = p.wpack[sg] + ((size_t)(t - p.seg_start[sg]) * kt + kk) * UNIT_BYTES;
+      bulk_load_1d(dst, src, UNIT_BYTES, bar);
+    } else {
+      const CUtensorMap* map = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
+      tma_load_2d(dst, map, kk * BK, (t - p.seg_start[sg]) * BN, bar);
+    }
+  };
+
+  if (warp == 0 || warp == 6) {
+    // ---------------- producers: unit i of the CTA's piece order goes to warp 0
+    // when i is even, to warp 6 when odd
+    const int pw = warp == 0 ? 0 : 1;
+    if (lane == 0) {
+      // weights do not depend on the preceding kernel: the first stages' weight
+      // copies go out before waiting for the producer of A
+      int i = 0;
+      for (int pc = 0; pc < npieces && i < STAGES; ++pc) {
+        int t;
+        long long ua, ub;
+        piece_units(pc, t, ua, ub);
+        for (long long u = ua; u < ub && i < STAGES; ++u, ++i) {
+          if ((i & 1) != pw) continue;
+          const uint32_t fb = smem_u32(&full[i]);
+          mbar_expect_tx(fb, STAGE_BYTES);
+          load_w(u, t, smem_u32(smem + i * STAGE_BYTES), fb);
+        }
+      }
+      pdl_wait();
+      i = 0;
+      bool alive = true;
+      for (int pc = 0; pc < npieces && alive; ++pc) {
+        int t;
+        long long ua, ub;
+        piece_units(pc, t, ua, ub);
+        for (long long u = ua; u < ub; ++u, ++i) {
+          if ((i & 1) != pw) continue;
+          const int s = i % STAGES;
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t fb = smem_u32(&full[s]);
+          const int kx = (int)(u - (long long)t * kt) * BK;
+          if (i >= STAGES) {
+            if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) {
+              alive = false;
+              break;
+            }
+            mbar_expect_tx(fb, STAGE_BYTES);
+            load_w(u, t, st, fb);
+          }
+          tma_load_2d(st + WS_W_BYTES, &tmA, kx, 0, fb);
+        }
+      }
+    }
+    pdl_launch_dependents();
+  } else {
+    pdl_launch_dependents();
+    pdl_wait();
+  }
+  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
+  const int np_eff = min(NP, max(16, (M_eff + 15) & ~15));
+
+  if (warp == 1) {
+    // ---------------- MMA issuer: pieces alternate between the two accumulators
+    if (lane == 0) {
+      const uint32_t idesc = instr_desc_ws(np_eff);
+      int i = 0;
+      bool alive = true;
+      for (int pc = 0; pc < npieces && alive; ++pc) {
+        int t;
+        long long ua, ub;
+        piece_units(pc, t, ua, ub);
+        const int b = pc & 1, use = pc >> 1;
+        if (use > 0 && !mbar_wait(smem_u32(&acc_empty[b]), (use - 1) & 1, p.err, 4, abort_flag)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t dacc = tmem + b * p.acc_cols;
+        for (long long u = ua; u < ub; ++u, ++i) {
+          const int s = i % STAGES;
+          if (!mbar_wait(smem_u32(&full[s]), (i / STAGES) & 1, p.err, 2, abort_flag)) {
+            alive = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_id(dacc, smem_desc(st + kk * 32), smem_desc(st + WS_W_BYTES + kk * 32), idesc,
+                    (u > ua || kk > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty[s]));
+        }
+        if (!alive) break;
+        umma_commit(smem_u32(&acc_full[b]));
+      }
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---------------- epilogue: TMEM lane = feature, column = row
+    const int q = warp & 3;
+    const int fl = q * 32 + lane;  // feature within the tile
+    for (int pc = 0; pc < npieces; ++pc) {
+      int t;
+      long long ua, ub;
+      piece_units(pc, t, ua, ub);
+      const int b = pc & 1, use = pc >> 1;
+      const bool ok = mbar_wait(smem_u32(&acc_full[b]), use & 1, p.err, 3, abort_flag);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!ok) break;
+      const int sg = (t >= p.seg_start[1]) + (t >= p.seg_start[2]);
+      const int n0 = (t - p.seg_start[sg]) * BN;
+      const int segN = p.seg_N[sg];
+      float* const Cseg = p.seg_C[sg];
+      const int f = n0 + fl;
+      const int cf = sk_owner((long long)t * kt, p.units, G);
+      const int cl = sk_owner((long long)(t + 1) * kt - 1, p.units, G);
+      const uint32_t tq = tmem + b * p.acc_cols + ((uint32_t)(q * 32) << 16);
+      const bool whole = cf == cl;
+      // piece of a cut tile: [feature][row] fp32, so a lane's rows are contiguous
+      float* wk = p.work + ((size_t)cta * 2 + (t == t_first ? 0 : 1)) * NP * BN + (size_t)fl * NP;
+#pragma unroll 1
+      for (int c = 0; c < np_eff; c += 16) {
+        float v[16];
+        tmem_ld16(tq + c, v);
+        if (whole) {
+          if (f < segN) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c + j < M_eff) Cseg[(size_t)(c + j) * p.ldc + f] = v[j];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) *(float4*)(wk + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+      }
+      // accumulator drained: hand it back to the MMA warp
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
+      if (whole) continue;
+      // cut tile: count this warp's arrival (each warp has its own counter, so
+      // no epilogue warp ever waits for another one)
+      __threadfence();
+      __syncwarp();
+      int arrived = 0;
+      if (lane == 0) arrived = atomicAdd(&p.counters[t * 4 + q], 1) + 1;
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (arrived != cl - cf + 1) continue;
+      // last arrival: sum every piece in CTA order, 32 rows of up to four
+      // pieces in flight per load round
+      __threadfence();
+      const int mend = min(M_eff, np_eff);
+#pragma unroll 1
+      for (int m0 = 0; m0 < mend; m0 += 32) {
+        float4 acc[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int c0 = cf; c0 <= cl; c0 += 4) {
+          float4 v[4][8];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int c = c0 + x;
+            if (c > cl) continue;
+            const int slot = (t == (int)(sk_start(c, p.units, G) / kt)) ? 0 : 1;
+            const float* src = p.work + ((size_t)c * 2 + slot) * NP * BN + (size_t)fl * NP + m0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+              v[x][r] = (m0 + 4 * r < np_eff) ? __ldcg((const float4*)(src + 4 * r)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            if (c0 + x > cl) continue;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              acc[r].x += v[x][r].x;
+              acc[r].y += v[x][r].y;
+              acc[r].z += v[x][r].z;
+              acc[r].w += v[x][r].w;
+            }
+          }
+        }
+        if (f < segN) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float e[4] = {acc[r].x, acc[r].y, acc[r].z, acc[r].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (m0 + 4 * r + j < mend) Cseg[(size_t)(m0 + 4 * r + j) * p.ldc + f] = e[j];
+          }
+        }
+      }
+      if (lane == 0) p.counters[t * 4 + q] = 0;
+    }
+  }
+  if (*abort_flag && (warp == 0 || warp == 6) && lane == 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < 20000000LL) {
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * p.acc_cols));
+  }
+}
+
+// Packed tile layout of a weight matrix W[N, K] (bf16, row stride ldw): for
+// every 128-row tile and 64-column k-tile, 16 KB holding the 128 x 64 block
+// exactly as a 128-byte-swizzled TMA load would place it in shared memory
+// (row r at r * 128 bytes, 16-byte chunk j of that row at chunk j ^ (r % 8)),
+// zero outside W.  Tiles follow each other k-tile by k-tile, so one tile's
+// stream - and a run of consecutive tiles - is contiguous.
+__global__ void pack_weight_tiles_kernel(const __nv_bfloat16* __restrict__ W, int ldw, int N, int K,
+                                         uint4* __restrict__ out) {
+  const int ktiles = (K + BK - 1) / BK;
+  const long long chunks = (long long)((N + BN - 1) / BN) * ktiles * BN * 8;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int j = (int)(i & 7);                 // 16-byte chunk in the row (destination)
+    const int r = (int)((i >> 3) % BN);         // row in the tile
+    const long long unit = (i >> 3) / BN;       // tile * ktiles + k-tile
+    const int kk = (int)(unit % ktiles);
+    const int t = (int)(unit / ktiles);
+    const int src_chunk = j ^ (r & 7);
+    const int n = t * BN + r;
+    const int k0 = kk * BK + src_chunk * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N) {
+      const __nv_bfloat16* src = W + (size_t)n * ldw + k0;
+      if (k0 + 8 <= K && (((uintptr_t)src) & 15) == 0) {
+        v = *(const uint4*)src;
+      } else {
+        __nv_bfloat16 e[8];
+        for (int x = 0; x < 8; ++x) e[x] = (k0 + x < K) ? src[x] : __float2bfloat16_rn(0.f);
+        memcpy(&v, e, 16);
+      }
+    }
+    out[i] = v;
   }
 }
 
@@ -395,33 +972,203 @@ const CUtensorMap* get_map(TcGemmCache* cache, const void* ptr, int rows, int co
   return &cache->maps.emplace(key, m).first->second;
 }
 
-template <int MT, int STAGES>
-cudaError_t launch(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid, int splits,
-                   cudaStream_t st) {
-  auto kern = gemm_kernel<MT, STAGES>;
-  constexpr int SMEM_BYTES = smem_bytes(MT, STAGES);
+template <int MT>
+cudaError_t launch_rt(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid,
+                      cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  // at most 512 / tmem_cols CTAs may share an SM (see launch_ws)
+  const int resident = 512 / p.tmem_cols;
+  const int smem = std::max(rt_smem_bytes(MT, p.bn, p.stages), 233472 / (resident + 1) - 1024 + 16);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 1;
   at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = splits;
+  at[0].val.clusterDim.z = p.splits;
   at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, *a, *b[0], *b[1], *b[2], p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<MT>, *a, *b[0], *b[1], *b[2], p);
 }
+
+int rt_tiles(const int* N, int nseg, int bn) {
+  int t = 0;
+  for (int i = 0; i < nseg; ++i) t += (N[i] + bn - 1) / bn;
+  return t;
+}
+
+int rt_max_stages(int mt, int bn) { return std::min(RT_MAX_STAGES, (232448 - 2048) / rt_stage_bytes(mt, bn)); }
+
+// Ring depth of the weight-stationary kernel when `ctas` CTAs share an SM.
+int ws_stages_for(int np, int ctas, int splits) {
+  const int budget = ctas == 1 ? 232448 : 115712;  // per-CTA dynamic shared memory
+  int s = std::min(WS_MAX_STAGES, (budget - 2048) / ws_stage_bytes(np));
+  // the split-K reduction reuses the ring for np x RED_PITCH fp32 partials
+  if (splits > 1 && s * ws_stage_bytes(np) < np * RED_PITCH * 4) s = 0;
+  return s;
+}
+
+// Launch choice for at most 256 rows (one row group).  Among single-wave
+// configurations (at most one CTA per SM), estimate a CTA's time as the bytes
+// it streams - its weight columns plus, at half weight, its box of A rows read
+// from L2 - at one SM's share of the HBM bandwidth, plus 0.4 us per cluster
+// split for the reduction, and take the cheapest of the row-tiled kernel at
+// every column width and the weight-stationary kernel (128-column tiles).
+// (Measured on GB300 for the projection shapes of the layer loop: the choice is
+// the fastest configuration or within a few percent of it.)
+struct GemmPick {
+  int kernel;  // 1 row-tiled, 2 weight-stationary
+  int bn, splits;
+};
+
+// Clusters of `cluster` CTAs of `func` (with `smem` bytes of dynamic shared
+// memory) that the device runs at once; 0 when the query is unavailable.
+int max_active_clusters(const void* func, int threads, int smem, int cluster) {
+  struct Key {
+    const void* f;
+    int smem, cluster;
+    bool operator<(const Key& o) const {
+      return f != o.f ? f < o.f : (smem != o.smem ? smem < o.smem : cluster < o.cluster);
+    }
+  };
+  static std::map<Key, int> memo;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  const Key key{func, smem, cluster};
+  auto it = memo.find(key);
+  if (it != memo.end()) return it->second;
+  int n = 0;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, 1, cluster);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = cluster;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  memo[key] = n;
+  return n;
+}
+
+GemmPick pick_small_m(int MT, int M, const int* N, int nseg, int ktiles, int nsm) {
+  GemmPick best{1, 128, 1};
+  double tbest = 1e30;
+  const void* rt_func = MT == 2 ? (const void*)gemm_kernel<2> : (const void*)gemm_kernel<1>;
+  auto consider = [&](int kernel, int bn, int s, double a_rows) {
+    const long long ctas = (long long)rt_tiles(N, nseg, bn) * s;
+    if (ctas > nsm) return;
+    if (s > 1) {
+      // every cluster must be resident at once (a cluster size that does not
+      // divide the SMs of a GPC leaves some idle and forces a second wave)
+      int smem, tmem = 32;
+      if (kernel == 1) {
+        while (tmem < MT * bn) tmem *= 2;
+        smem = std::max(rt_smem_bytes(MT, bn, rt_max_stages(MT, bn)), 233472 / (512 / tmem + 1) - 1024 + 16);
+      } else {
+        const int np = std::max(16, (M + 15) & ~15);
+        while (tmem < np) tmem *= 2;
+        smem = std::max(ws_smem_bytes(np, ws_stages_for(np, 1, s)), 233472 / (512 / tmem + 1) - 1024 + 16);
+      }
+      const int mc = max_active_clusters(kernel == 1 ? rt_func : (const void*)gemm_ws_kernel, THREADS, smem, s);
+      if (mc <= 0 || ctas / s > mc) return;
+    }
+    const double kel = (double)ktiles * BK / s;
+    const double t = (bn + 0.5 * a_rows) * kel * 2.0 / 50e3 + 0.4 * s;
+    if (t < tbest * 0.999) {
+      tbest = t;
+      best = GemmPick{kernel, bn, s};
+    }
+  };
+  const int np = std::max(16, (M + 15) & ~15);
+  for (int s = 1; s <= 8; ++s) {
+    if (s > 1 && ktiles < 8 * s) break;
+    for (int bn = 16; bn <= 256; bn += 16) {
+      if (MT * bn > 512 || rt_max_stages(MT, bn) < 3) continue;
+      if (s > 1 && rt_max_stages(MT, bn) * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4) continue;
+      consider(1, bn, s, MT * BM);
+    }
+    if (ws_stages_for(np, 1, s) >= 2) consider(2, BN, s, np);
+  }
+  if (tbest >= 1e30) {
+    // more 16-column tiles than SMs even unsplit: widest tiles, several waves
+    best = GemmPick{1, 256 / MT, 1};
+  }
+  return best;
+}
+
+cudaError_t launch_ws(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid,
+                      cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  // CTAs that share an SM must never ask for more than its 512 TMEM columns
+  // between them (a blocked tcgen05.alloc inside a cluster that waits for its
+  // peers could wait forever): pad the shared memory so that at most
+  // 512 / tmem_cols CTAs fit on one SM (228 KB per SM, 1 KB reserved per CTA)
+  const int resident = 512 / p.tmem_cols;
+  const int smem = std::max(ws_smem_bytes(p.np, p.stages), 233472 / (resident + 1) - 1024 + 16);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = p.splits;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_ws_kernel, *a, *b[0], *b[1], *b[2], p);
+}
+
+template <bool PACKED>
+cudaError_t launch_sk(const CUtensorMap* a, const CUtensorMap* const* b, const SkParams& p, int grid,
+                      cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_sk_kernel<PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  // one CTA per SM: at least half of the SM's 228 KB, so two never share one
+  const int smem = std::max(p.stages * ws_stage_bytes(p.np) + 2048, 233472 / 2 - 1024 + 16);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(SK_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_sk_kernel<PACKED>, *a, *b[0], *b[1], *b[2], p);
+}
+
 
 }  // namespace tc
 
@@ -439,7 +1186,7 @@ bool tc_gemm_supported(int K, int lda, int ldw) {
 
 cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int nseg, const void* const* W,
                                const int* ldw, const int* N, float* const* C, int ldc, int M, const int* m_dev,
-                               int K, cudaStream_t st) {
+                               int K, cudaStream_t st, const TcGemmChoice* force, const void* const* Wpacked) {
   using namespace tc;
   if (M <= 0 || nseg < 1 || nseg > 3) return M <= 0 ? cudaSuccess : cudaErrorInvalidValue;
   if ((uintptr_t)A & 15) return cudaErrorInvalidValue;
@@ -462,6 +1209,27 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   p.ktiles = ktiles;
   p.err = err;
   p.nseg = nseg;
+  const int nsm = cache->num_sms;
+  int kind = force && force->kernel ? force->kernel : 0;
+  // columns per tile: 128 for the weight-stationary kernels (the MMA's M side),
+  // chosen per launch for the row-tiled kernel (its N side)
+  int bn = BN, auto_splits = 0;
+  if (kind == 0) {
+    if (mgroups == 1) {
+      const GemmPick pk = pick_small_m(MT, M, N, nseg, ktiles, nsm);
+      kind = pk.kernel;
+      bn = pk.bn;
+      auto_splits = pk.splits;
+    } else {
+      kind = 1;
+      bn = 256;  // many row groups: widest tiles for the fewest re-reads of A
+    }
+  } else if (kind == 1 && force->bn) {
+    bn = force->bn;
+    if (bn < 16 || bn > 256 || (bn & 15) || MT * bn > 512) return cudaErrorInvalidValue;
+  } else if (kind == 1) {
+    bn = mgroups == 1 ? pick_small_m(MT, M, N, nseg, ktiles, nsm).bn : 256;
+  }
   const CUtensorMap* mb[3] = {nullptr, nullptr, nullptr};
   int tiles = 0;
   for (int sgi = 0; sgi < 3; ++sgi) {
@@ -470,40 +1238,146 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
       if (((uintptr_t)W[sgi] & 15) || N[sgi] < 1) return cudaErrorInvalidValue;
       p.seg_N[sgi] = N[sgi];
       p.seg_C[sgi] = C[sgi];
-      mb[sgi] = get_map(cache, W[sgi], N[sgi], K, ldw[sgi], BN);
+      mb[sgi] = get_map(cache, W[sgi], N[sgi], K, ldw[sgi], bn);
       if (!mb[sgi]) return cudaErrorInvalidValue;
-      tiles += (N[sgi] + BN - 1) / BN;
+      tiles += (N[sgi] + bn - 1) / bn;
     }
   }
   p.seg_start[3] = 0x3FFFFFFF;
   for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
-  // split K over a cluster while the doubled grid still fits in one wave and
-  // every split keeps at least 8 K-tiles (cluster size <= 8): only grids that
-  // would leave most SMs idle pay for the cross-CTA reduction
-  const int base = tiles * mgroups, nsm = cache->num_sms;
-  int splits = 1;
-  while (splits < 8 && base * splits * 2 <= nsm && ktiles >= splits * 2 * 8) splits *= 2;
+  if (kind == 3) {
+    // persistent stream-K: stages = ring depth, splits = grid size override
+    if (M > 2 * BM) return cudaErrorInvalidValue;
+    SkParams q{};
+    q.M = M;
+    q.m_dev = m_dev;
+    q.ldc = ldc;
+    q.ktiles = ktiles;
+    q.units = (long long)tiles * ktiles;
+    q.err = err;
+    for (int i = 0; i < 4; ++i) q.seg_start[i] = p.seg_start[i];
+    for (int i = 0; i < 3; ++i) {
+      q.seg_N[i] = p.seg_N[i];
+      q.seg_C[i] = p.seg_C[i];
+    }
+    q.np = std::max(16, (M + 15) & ~15);
+    q.acc_cols = 32;
+    while (q.acc_cols < q.np) q.acc_cols *= 2;
+    const int max_stages = std::min(SK_MAX_STAGES, (232448 - 2048) / ws_stage_bytes(q.np));
+    q.stages = force && force->stages ? force->stages : max_stages;
+    if (q.stages < 2 || q.stages > max_stages) return cudaErrorInvalidValue;
+    int grid = force && force->splits ? force->splits : nsm;
+    if (grid < 1 || grid > nsm) return cudaErrorInvalidValue;
+    grid = (int)std::min<long long>(grid, q.units);
+    if (tiles * 4 > TcGemmCache::kMaxCounters) return cudaErrorInvalidValue;
+    const cudaError_t re = tc_gemm_reserve(cache);
+    if (re != cudaSuccess) return re;
+    q.work = cache->work;
+    q.counters = cache->counters;
+    const bool packed = Wpacked != nullptr;
+    for (int i = 0; i < nseg; ++i) {
+      q.wpack[i] = packed ? (const uint8_t*)Wpacked[i] : nullptr;
+      if (packed && (!Wpacked[i] || ((uintptr_t)Wpacked[i] & 15))) return cudaErrorInvalidValue;
+    }
+    const CUtensorMap* ma = get_map(cache, A, M, K, lda, q.np);
+    if (!ma) return cudaErrorInvalidValue;
+    return packed ? launch_sk<true>(ma, mb, q, grid, st) : launch_sk<false>(ma, mb, q, grid, st);
+  }
+  // the row-tiled kernel reads W through its tensor map; packed copies unused
+  if (kind == 2) {
+    if (M > 2 * BM) return cudaErrorInvalidValue;
+    p.np = std::max(16, (M + 15) & ~15);
+    p.tmem_cols = 32;
+    while (p.tmem_cols < p.np) p.tmem_cols *= 2;
+    int splits = auto_splits ? auto_splits : 1;
+    if (force && force->splits) {
+      splits = force->splits;
+    } else if (!auto_splits) {
+      while (splits < 8 && tiles * splits * 2 <= nsm && ktiles >= splits * 2 * 8) splits *= 2;
+    }
+    int stages = force && force->stages ? force->stages : ws_stages_for(p.np, 1, splits);
+    if (splits < 1 || splits > 8 || stages < 2 || stages > WS_MAX_STAGES ||
+        ws_smem_bytes(p.np, stages) > 232448 ||
+        (splits > 1 && stages * ws_stage_bytes(p.np) < p.np * RED_PITCH * 4))
+      return cudaErrorInvalidValue;
+    p.splits = splits;
+    p.stages = stages;
+    const CUtensorMap* ma = get_map(cache, A, M, K, lda, p.np);
+    if (!ma) return cudaErrorInvalidValue;
+    return launch_ws(ma, mb, p, dim3(tiles, 1, splits), st);
+  }
+  // row-tiled kernel
+  int splits = auto_splits ? auto_splits : 1;
+  if (force && force->splits) splits = force->splits;
+  if (splits < 1 || splits > 8) return cudaErrorInvalidValue;
+  p.bn = bn;
   p.splits = splits;
+  p.stages = force && force->stages ? force->stages : rt_max_stages(MT, bn);
+  if (p.stages < 2 || p.stages > RT_MAX_STAGES || rt_smem_bytes(MT, bn, p.stages) > 232448 ||
+      (splits > 1 && p.stages * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4))
+    return cudaErrorInvalidValue;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < MT * bn) p.tmem_cols *= 2;
   const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
   if (!ma) return cudaErrorInvalidValue;
   const dim3 grid(tiles, mgroups, splits);
-  // stage rings: deep (one CTA per SM) unless a single row group has more
-  // tiles than SMs, where two CTAs per SM (3 stages each) avoid a second wave
-  if (MT == 2) return launch<2, 4>(ma, mb, p, grid, splits, st);
-  if (mgroups == 1 && splits == 1 && tiles > nsm) return launch<1, 3>(ma, mb, p, grid, splits, st);
-  return launch<1, 6>(ma, mb, p, grid, splits, st);
+  return MT == 2 ? launch_rt<2>(ma, mb, p, grid, st) : launch_rt<1>(ma, mb, p, grid, st);
 }
 
 cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,
-                         int M, const int* m_dev, int N, int K, cudaStream_t st) {
+                         int M, const int* m_dev, int N, int K, cudaStream_t st, const TcGemmChoice* force,
+                         const void* Wpacked) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  return tc_gemm_bf16_multi(cache, A, lda, 1, &W, &ldw, &N, &C, ldc, M, m_dev, K, st);
+  return tc_gemm_bf16_multi(cache, A, lda, 1, &W, &ldw, &N, &C, ldc, M, m_dev, K, st, force,
+                            Wpacked ? &Wpacked : nullptr);
+}
+
+size_t tc_packed_bytes(int N, int K) {
+  return (size_t)((N + tc::BN - 1) / tc::BN) * ((K + tc::BK - 1) / tc::BK) * tc::UNIT_BYTES;
+}
+
+cudaError_t tc_pack_weights(const void* W, int ldw, int N, int K, void* out, cudaStream_t st) {
+  if (!W || !out || N < 1 || K < 1 || ldw < K || ((uintptr_t)out & 15)) return cudaErrorInvalidValue;
+  const long long chunks = (long long)tc_packed_bytes(N, K) / 16;
+  const int blocks = (int)std::min<long long>((chunks + 255) / 256, 4096);
+  tc::pack_weight_tiles_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)W, ldw, N, K, (uint4*)out);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_gemm_reserve(TcGemmCache* c) {
+  if (c->work) return cudaSuccess;
+  if (c->num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (c->num_sms <= 0) return cudaErrorInvalidValue;
+  }
+  // two partial pieces of up to 256 rows x 128 features per CTA
+  const size_t work_bytes = (size_t)c->num_sms * 2 * 256 * tc::BN * sizeof(float);
+  cudaError_t e = cudaMalloc(&c->work, work_bytes);
+  if (e != cudaSuccess) {
+    c->work = nullptr;
+    return e;
+  }
+  e = cudaMalloc(&c->counters, sizeof(int) * TcGemmCache::kMaxCounters);
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, sizeof(int) * TcGemmCache::kMaxCounters);
+  if (e != cudaSuccess) {
+    cudaFree(c->work);
+    if (c->counters) cudaFree(c->counters);
+    c->work = nullptr;
+    c->counters = nullptr;
+  }
+  return e;
 }
 
 void tc_gemm_cache_clear(TcGemmCache* c) {
   c->maps.clear();
   if (c->err) cudaFree(c->err);
   c->err = nullptr;
+  if (c->work) cudaFree(c->work);
+  if (c->counters) cudaFree(c->counters);
+  c->work = nullptr;
+  c->counters = nullptr;
 }
 
 }  // namespace polestar

@@ -2,14 +2,16 @@
 // "Cluster and Quantize Hidden States"; App. C.3; Algorithm 1's clustering,
 // quantisation, dequantisation, patch and update steps).
 //
-//   kmeans_encode_kernel  one CTA per (layer, sequence): spherical K-means on the
-//                         block-entry window inputs, member sums, residual
-//                         anchors, then NVFP4 encoding of every row's residual.
-//   window_patch_kernel   within-block: decode a window row, swap in its update
-//                         packet when the previous layer selected it, re-encode
-//                         it and record the change of its unit direction.
-//   centroid_sum/norm     s_c += sum of those changes (window order),
-//                         z_c = s_c / |s_c| (incremental centroid update).
+//   kmeans_encode_kernel    one thread-block cluster per (layer, sequence),
+//                           channel slices per CTA: spherical K-means on the
+//                           block-entry window inputs, member sums, residual
+//                           anchors, then NVFP4 encoding of every row's residual.
+//   window_patch_kernel     within-block: decode a window row, swap in its update
+//                           packet when the previous layer selected it, re-encode
+//                           it and record the change of its unit direction.
+//   centroid_update_kernel  one cluster per firing sequence: s_c += sum of those
+//                           changes, z_c = s_c / |s_c| (incremental centroid
+//                           update) and the proxy rows' projection inputs.
 #include "kernels.h"
 
 namespace polestar {
@@ -303,7 +305,38 @@ void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st) {
 
 // ---------------------------------------------------------------- within-block
 template <typename T>
-__global__ void window_patch_kernel(PatchArgs a) {
+__device__ __forceinline__ float4 cl_ld4t(const T* p);
+template <>
+__device__ __forceinline__ float4 cl_ld4t<float>(const float* p) {
+  return *(const float4*)p;
+}
+template <>
+__device__ __forceinline__ float4 cl_ld4t<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 u = *(const uint2*)p;
+  const float2 fa = __bfloat1622float2(*(const __nv_bfloat162*)&u.x), fb = __bfloat1622float2(*(const __nv_bfloat162*)&u.y);
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+template <typename T>
+__device__ __forceinline__ void cl_st4t(T* p, float4 v);
+template <>
+__device__ __forceinline__ void cl_st4t<float>(float* p, float4 v) {
+  *(float4*)p = v;
+}
+template <>
+__device__ __forceinline__ void cl_st4t<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *(const uint32_t*)&a;
+  u.y = *(const uint32_t*)&b;
+  *(uint2*)p = u;
+}
+
+// One window row per CTA; thread g owns NVFP4 group g (16 channels, d <= 4096
+// so one group per thread) and keeps its decoded and patched values in
+// registers through the decode, the RMSNorm of the projection input and the
+// re-encoding.
+template <typename T>
+__global__ void __launch_bounds__(256) window_patch_kernel(PatchArgs a) {
   pdl_enter();
   __shared__ float red[32];
   const int j = blockIdx.x, f = blockIdx.y;
@@ -318,48 +351,60 @@ __global__ void window_patch_kernel(PatchArgs a) {
   const float* Urow = a.U + ((size_t)s * a.Wmax + j) * d;
   float* hrow = a.h_rows + (size_t)row * d;
   float* dnrow = a.dn + ((size_t)s * a.Wmax + j) * d;
-
+  const int g = threadIdx.x;
+  const bool act = g < ng;
+  float av[16], old[16], nv[16];
   float ss_old = 0.f, ss_new = 0.f;
-  // pass 1: decode, write the patched row, norms
-  for (int g = threadIdx.x; g < ng; g += blockDim.x) {
+  if (act) {
     const float sc = e4m3_decode(srow[g]);
     const uint2 pk = *(const uint2*)(crow + g * 8);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) *(float4*)&av[4 * q] = *(const float4*)(A + g * 16 + 4 * q);
+    if (patched) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) *(float4*)&nv[4 * q] = *(const float4*)(Urow + g * 16 + 4 * q);
+    }
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const uint32_t word = (e < 8) ? pk.x : pk.y;
       const uint32_t code = (word >> (4 * (e & 7))) & 0xF;
-      const float old = A[g * 16 + e] + e2m1_decode(code) * sc;
-      const float nv = patched ? Urow[g * 16 + e] : old;
-      ss_old = fmaf(old, old, ss_old);
-      ss_new = fmaf(nv, nv, ss_new);
-      hrow[g * 16 + e] = nv;
-      if (patched) dnrow[g * 16 + e] = old;  // stash old value; finished below
+      old[e] = av[e] + e2m1_decode(code) * sc;
+      if (!patched) nv[e] = old[e];
+      ss_old = fmaf(old[e], old[e], ss_old);
+      ss_new = fmaf(nv[e], nv[e], ss_new);
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) *(float4*)(hrow + g * 16 + 4 * q) = *(const float4*)&nv[4 * q];
   }
   ss_old = block_sum(ss_old, red);
   ss_new = block_sum(ss_new, red);
   // fused input of the layer's projections: RMSNorm of the (patched) row
-  {
+  if (act) {
     const float inv = 1.f / sqrtf(ss_new / (float)d + a.eps);
-    const T* gain = (const T*)a.gain;
-    T* ao = (T*)a.a_out + (size_t)row * d;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) ao[k] = from_f<T>(hrow[k] * inv * to_f<T>(gain[k]));
+    const T* gain = (const T*)a.gain + g * 16;
+    T* ao = (T*)a.a_out + (size_t)row * d + g * 16;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 gv = cl_ld4t<T>(gain + 4 * q);
+      cl_st4t<T>(ao + 4 * q, make_float4(nv[4 * q] * inv * gv.x, nv[4 * q + 1] * inv * gv.y,
+                                         nv[4 * q + 2] * inv * gv.z, nv[4 * q + 3] * inv * gv.w));
+    }
   }
   if (!patched) {
     if (threadIdx.x == 0) a.write_kv[row] = 0;
     return;
   }
   const float io = 1.f / sqrtf(ss_old), in = 1.f / sqrtf(ss_new);
-  // pass 2: direction change and re-encoding of the new residual
-  for (int g = threadIdx.x; g < ng; g += blockDim.x) {
+  if (act) {
+    // direction change and re-encoding of the new residual
     float r[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int k = g * 16 + e;
-      const float nv = Urow[k];
-      dnrow[k] = nv * in - dnrow[k] * io;
-      r[e] = nv - A[k];
-    }
+    for (int e = 0; e < 16; ++e) r[e] = nv[e] - av[e];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *(float4*)(dnrow + g * 16 + 4 * q) =
+          make_float4(nv[4 * q] * in - old[4 * q] * io, nv[4 * q + 1] * in - old[4 * q + 1] * io,
+                      nv[4 * q + 2] * in - old[4 * q + 2] * io, nv[4 * q + 3] * in - old[4 * q + 3] * io);
     uint8_t packed[8];
     srow[g] = nvfp4_encode16(r, packed);
     uint2 pk;
@@ -370,56 +415,174 @@ __global__ void window_patch_kernel(PatchArgs a) {
   if (threadIdx.x == 0) a.write_kv[row] = 1;
 }
 
-// s_c += sum over the patched member rows (window order) of their direction
-// change; one thread per channel, all clusters of one sequence per CTA column.
-__global__ void centroid_sum_kernel(PatchArgs a) {
+// Incremental centroid update of one firing sequence on a thread-block cluster
+// of `nc` CTAs, CTA r owning channels [r*cw, (r+1)*cw):
+//   s_c += sum over selected window rows j with label c of dn_j   (window order
+//          within each of the RL row lanes, lanes added in order),
+//   z_c  = s_c / |s_c|   (|s_c| summed over the cluster in rank order),
+//   a_out[proxy_row + c] = T(RMSNorm(z_c) * gain)   (the proxy row's projection input).
+constexpr int CU_THREADS = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a, int nc, int cw) {
   pdl_enter();
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  __shared__ float4 part[CU_THREADS][KM_MAXK];  // [row lane * groups + group][cluster]
+  __shared__ float nrm_part[2][KM_MAXK], nrm_full[2][KM_MAXK];
+  __shared__ float wsum[CU_THREADS / 32][KM_MAXK];
+  __shared__ uint8_t sl[KM_MAXW], lb[KM_MAXW];
+  const int rank = (int)km_rank();
   const int s = a.fire_seqs[blockIdx.y];
-  if (k >= a.d) return;
-  const uint8_t* lab = a.labels + (size_t)s * a.Wmax;
-  const uint8_t* sel = a.sel_prev + (size_t)s * a.Wmax;
-  float acc[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-  for (int j = 0; j < a.nw; ++j) {
-    if (!sel[j]) continue;  // uniform across the CTA
-    const int c = lab[j];
-    const float v = a.dn[((size_t)s * a.Wmax + j) * a.d + k];
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc)
-      if (cc == c) acc[cc] += v;
+  const int d = a.d, K = a.K, nw = a.nw;
+  const int c0 = rank * cw;
+  const int G = cw / 4;                              // channel groups of this CTA
+  const int RL = G >= CU_THREADS ? 1 : CU_THREADS / G;  // row lanes sharing a group
+  const int t = threadIdx.x;
+  for (int i = t; i < nw; i += CU_THREADS) {
+    sl[i] = a.sel_prev[s * a.Wmax + i];
+    lb[i] = a.labels[s * a.Wmax + i];
   }
-  float* cs = a.csum + (size_t)s * a.K * a.d;
+  __syncthreads();
+  float* cs_base = a.csum + (size_t)s * K * d;
+  float ssl[KM_MAXK];
 #pragma unroll
-  for (int c = 0; c < 8; ++c)
-    if (c < a.K) cs[(size_t)c * a.d + k] += acc[c];
+  for (int c = 0; c < KM_MAXK; ++c) ssl[c] = 0.f;
+  // RL > 1: one pass, thread t = lane rl * G + group cg.  RL == 1: group
+  // cg = t + k * CU_THREADS in pass k.  Either way the thread that finishes
+  // group cg (rl == 0) is thread cg % CU_THREADS, which also normalises it below.
+  for (int cgb = 0; cgb < G; cgb += (RL > 1 ? G : CU_THREADS)) {
+    const int cg = RL > 1 ? t % G : cgb + t;
+    const int rl = RL > 1 ? t / G : 0;
+    const bool act = RL > 1 ? t < RL * G : cg < G;
+    float4 acc[KM_MAXK];
+#pragma unroll
+    for (int c = 0; c < KM_MAXK; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (act) {
+      const float* dn = a.dn + (size_t)s * a.Wmax * d + c0 + cg * 4;
+      for (int j0 = rl; j0 < nw; j0 += 8 * RL) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u * RL;
+          v[u] = (j < nw && sl[j]) ? *(const float4*)(dn + (size_t)j * d) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u * RL;
+          if (j >= nw || !sl[j]) continue;
+          const int lab = lb[j];
+#pragma unroll
+          for (int c = 0; c < KM_MAXK; ++c)
+            if (c == lab) {
+              acc[c].x += v[u].x;
+              acc[c].y += v[u].y;
+              acc[c].z += v[u].z;
+              acc[c].w += v[u].w;
+            }
+        }
+      }
+    }
+    // combine the row lanes in order through shared memory
+    if (RL > 1) {
+      __syncthreads();
+      if (act) {
+#pragma unroll
+        for (int c = 0; c < KM_MAXK; ++c) part[rl * G + cg][c] = acc[c];
+      }
+      __syncthreads();
+      if (act && rl == 0) {
+#pragma unroll
+        for (int c = 0; c < KM_MAXK; ++c) acc[c] = part[cg][c];
+        for (int q = 1; q < RL; ++q) {
+#pragma unroll
+          for (int c = 0; c < KM_MAXK; ++c) {
+            const float4 w = part[q * G + cg][c];
+            acc[c].x += w.x;
+            acc[c].y += w.y;
+            acc[c].z += w.z;
+            acc[c].w += w.w;
+          }
+        }
+      }
+    }
+    if (act && rl == 0) {
+#pragma unroll
+      for (int c = 0; c < KM_MAXK; ++c) {
+        if (c >= K) continue;
+        float* cs = cs_base + (size_t)c * d + c0 + cg * 4;
+        float4 v = *(const float4*)cs;
+        v.x += acc[c].x;
+        v.y += acc[c].y;
+        v.z += acc[c].z;
+        v.w += acc[c].w;
+        *(float4*)cs = v;
+        ssl[c] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
+    }
+  }
+  // |s_c|^2 of this CTA's channels, then over the cluster (rank order)
+  const int lane = t & 31, wid = t >> 5;
+#pragma unroll
+  for (int c = 0; c < KM_MAXK; ++c) {
+    float v = ssl[c];
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) wsum[wid][c] = v;
+  }
+  __syncthreads();
+  if (t < KM_MAXK) {
+    float v = 0.f;
+    for (int w = 0; w < CU_THREADS / 32; ++w) v += wsum[w][t];
+    nrm_part[0][t] = v;
+  }
+  km_allreduce(&nrm_part[0][0], &nrm_full[0][0], KM_MAXK, nc);
+  // z_c = s_c / |s_c| for this CTA's channels; sum of z^2 for the RMSNorm
+  float zz[KM_MAXK];
+#pragma unroll
+  for (int c = 0; c < KM_MAXK; ++c) zz[c] = 0.f;
+  for (int cg = t; cg < G; cg += CU_THREADS) {
+#pragma unroll
+    for (int c = 0; c < KM_MAXK; ++c) {
+      if (c >= K) continue;
+      const float nrm = sqrtf(nrm_full[0][c]);
+      const float4 v = *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4);
+      const float4 zv = make_float4(v.x / nrm, v.y / nrm, v.z / nrm, v.w / nrm);
+      *(float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4) = zv;
+      zz[c] += zv.x * zv.x + zv.y * zv.y + zv.z * zv.z + zv.w * zv.w;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < KM_MAXK; ++c) {
+    float v = zz[c];
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) wsum[wid][c] = v;
+  }
+  __syncthreads();
+  if (t < KM_MAXK) {
+    float v = 0.f;
+    for (int w = 0; w < CU_THREADS / 32; ++w) v += wsum[w][t];
+    nrm_part[1][t] = v;
+  }
+  km_allreduce(&nrm_part[1][0], &nrm_full[1][0], KM_MAXK, nc);
+  const T* gain = (const T*)a.gain;
+  for (int cg = t; cg < G; cg += CU_THREADS) {
+    const float4 gv = cl_ld4t<T>(gain + c0 + cg * 4);
+    for (int c = 0; c < K; ++c) {
+      const float inv = 1.f / sqrtf(nrm_full[1][c] / (float)d + a.eps);
+      const float4 zv = *(const float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4);
+      T* ao = (T*)a.a_out + (size_t)(a.proxy_row[s] + c) * d + c0 + cg * 4;
+      cl_st4t<T>(ao, make_float4(zv.x * inv * gv.x, zv.y * inv * gv.y, zv.z * inv * gv.z, zv.w * inv * gv.w));
+    }
+  }
 }
 
-// z_c = s_c / |s_c| for every cluster of a refreshing sequence, and the proxy
-// row's projection input T(RMSNorm(z_c) * gain)
-template <typename T>
-__global__ void centroid_norm_kernel(PatchArgs a) {
-  pdl_enter();
-  __shared__ float red[32];
-  const int c = blockIdx.x, s = a.fire_seqs[blockIdx.y];
-  const float* cs = a.csum + ((size_t)s * a.K + c) * a.d;
-  float* z = a.z + ((size_t)s * a.K + c) * a.d;
-  float ss = 0.f;
-  for (int k = threadIdx.x; k < a.d; k += blockDim.x) ss = fmaf(cs[k], cs[k], ss);
-  ss = block_sum(ss, red);
-  const float nrm = sqrtf(ss);
-  float zz = 0.f;
-  for (int k = threadIdx.x; k < a.d; k += blockDim.x) {
-    const float v = cs[k] / nrm;
-    z[k] = v;
-    zz = fmaf(v, v, zz);
-  }
-  zz = block_sum(zz, red);
-  const float inv = 1.f / sqrtf(zz / (float)a.d + a.eps);
-  const T* gain = (const T*)a.gain;
-  T* ao = (T*)a.a_out + (size_t)(a.proxy_row[s] + c) * a.d;
-  for (int k = threadIdx.x; k < a.d; k += blockDim.x) ao[k] = from_f<T>(z[k] * inv * to_f<T>(gain[k]));
+// Cluster size of the centroid update: the fewest CTAs (at most 16) that give
+// each CTA at most 256 channels in whole 4-channel groups, else the fewest with
+// whole groups.
+int centroid_cluster_size(int d) {
+  for (int nc = 1; nc <= 16; ++nc)
+    if (d % (4 * nc) == 0 && d / nc <= 256) return nc;
+  for (int nc = 16; nc >= 1; --nc)
+    if (d % (4 * nc) == 0) return nc;
+  return 1;
 }
 
 template <typename T>
@@ -428,8 +591,24 @@ void launch_window_patch(const PatchArgs& a, cudaStream_t st) {
 }
 template <typename T>
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st) {
-  launch_pdl(centroid_sum_kernel, dim3((a.d + 127) / 128, a.n_fire), dim3(128), 0, st, a);
-  launch_pdl(centroid_norm_kernel<T>, dim3(a.K, a.n_fire), dim3(256), 0, st, a);
+  const int nc = centroid_cluster_size(a.d);
+  const int cw = a.d / nc;
+  if (nc > 8) cudaFuncSetAttribute(centroid_update_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(nc, a.n_fire);
+  cfg.blockDim = dim3(CU_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = nc;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  cudaLaunchKernelEx(&cfg, centroid_update_kernel<T>, a, nc, cw);
 }
 template void launch_window_patch<float>(const PatchArgs&, cudaStream_t);
 template void launch_window_patch<__nv_bfloat16>(const PatchArgs&, cudaStream_t);

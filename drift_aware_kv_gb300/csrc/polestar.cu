@@ -22,6 +22,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/polestar.h"
@@ -244,7 +245,8 @@ std::string validate(const polestar_config* c) {
   if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
   if (c->d_model < 16 || c->d_model % 16) return "d_model must be a positive multiple of 16";
   if (c->d_model > 4096) return "d_model above 4096 is not supported by the clustering kernel";
-  if (c->ffn_dim < 1) return "ffn_dim must be >= 1";
+  if (c->ffn_dim < 8 || c->ffn_dim % 8) return "ffn_dim must be a positive multiple of 8";
+  if (c->n_heads * c->head_dim > 8192) return "n_heads * head_dim above 8192 is not supported";
   if (c->batch < 1 || c->batch > 32) return "batch must be in [1, 32]";
   if (c->block < 8 || c->block % 8) return "block must be a positive multiple of 8";
   if (c->gen_len < c->block || c->gen_len % c->block) return "gen_len must be a positive multiple of block";
@@ -646,7 +648,6 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       pa.proxy_row = proxy_row_d;
       RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_window_patch<T>(pa, c->sm)));
       RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_centroid_update<T>(pa, c->sm)));
-      ++c->launches;  // two kernels
     }
     // the projections' input rows were normalised by their producers: active
     // rows by the previous layer's final residual (or the input gather), window
@@ -891,6 +892,7 @@ extern "C" polestar_status polestar_calibrate_step(polestar_ctx* c, const void* 
                                                    polestar_step_out* out) {
   if (!c) return POLESTAR_ERR_INVALID_ARG;
   if (!x0) return fail(c, POLESTAR_ERR_INVALID_ARG, "x0 is NULL");
+  if ((uintptr_t)x0 & 15) return fail(c, POLESTAR_ERR_INVALID_ARG, "x0 must be 16-byte aligned");
   const int n_blocks = c->cfg.gen_len / c->B;
   if (block_index < 0 || block_index >= n_blocks)
     return fail(c, POLESTAR_ERR_INVALID_ARG, "block_index out of range");
@@ -1097,16 +1099,37 @@ extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const
   static TcGemmCache cache;
   if (!A || !W || !C || M < 0 || N < 1 || K < 1) return POLESTAR_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  if (path == 1) {
-    if (dtype != POLESTAR_BF16 || !tc_gemm_supported(K, lda, ldw)) return POLESTAR_ERR_UNSUPPORTED;
-    return tc_gemm_bf16(&cache, A, lda, W, ldw, C, ldc, M, m_dev, N, K, st) == cudaSuccess ? POLESTAR_OK
-                                                                                           : POLESTAR_ERR_CUDA;
+  const int kind = path & 0xFF;
+  if (kind >= 1 && kind <= 5) {
+    if (dtype != POLESTAR_BF16 || !tc_gemm_supported(K, lda, kind == 5 ? K : ldw)) return POLESTAR_ERR_UNSUPPORTED;
+    TcGemmChoice force;
+    force.kernel = kind == 5 ? 3 : kind - 1;
+    force.stages = (path >> 8) & 0xFF;
+    force.splits = (path >> 16) & 0xFF;
+    force.bn = ((path >> 24) & 0xFF) * 16;
+    const cudaError_t e = tc_gemm_bf16(&cache, A, lda, W, kind == 5 ? K : ldw, C, ldc, M, m_dev, N, K, st, &force,
+                                       kind == 5 ? W : nullptr);
+    if (e == cudaErrorInvalidValue) return POLESTAR_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
   }
+  if (kind != 0) return POLESTAR_ERR_UNSUPPORTED;
   if (dtype == POLESTAR_BF16)
     launch_gemm_simt<__nv_bfloat16>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, st);
   else
     launch_gemm_simt<float>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, st);
   return cudaGetLastError() == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
+extern "C" int64_t polestar_packed_weight_bytes(int32_t N, int32_t K) {
+  if (N < 1 || K < 1) return -1;
+  return (int64_t)tc_packed_bytes(N, K);
+}
+
+extern "C" polestar_status polestar_pack_weights(const void* W, int32_t ldw, int32_t N, int32_t K, void* out,
+                                                 void* stream) {
+  if (!W || !out || N < 1 || K < 1 || ldw < K) return POLESTAR_ERR_INVALID_ARG;
+  if ((uintptr_t)out & 15) return POLESTAR_ERR_INVALID_ARG;
+  return tc_pack_weights(W, ldw, N, K, out, (cudaStream_t)stream) == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 
 extern "C" polestar_status polestar_debug_attention(const void* q, const void* kv, int32_t N, int32_t H,

@@ -31,18 +31,36 @@ def _time(fn, iters, warmup=3):
     return e0.elapsed_time(e1) / iters
 
 
+L2_BYTES = 129 * 2**20
+
+
 def bench_gemm(a):
+    """Average launch time over a rotation of weight copies that together exceed
+    L2 (as in the layer loop, where every projection reads weights it has not
+    read since the previous step)."""
     from drift_aware_kv_gb300 import polestar as P
     g = torch.Generator(device="cuda").manual_seed(0)
     A = torch.randn(a.M, a.K, device="cuda", generator=g).to(torch.bfloat16)
-    W = (0.02 * torch.randn(a.N, a.K, device="cuda", generator=g)).to(torch.bfloat16)
+    wbytes = a.N * a.K * 2
+    ncopy = max(2, -(-3 * L2_BYTES // wbytes))
+    Ws = [(0.02 * torch.randn(a.N, a.K, device="cuda", generator=g)).to(torch.bfloat16) for _ in range(ncopy)]
     C = torch.empty(a.M, a.N, device="cuda")
-    if a.path == 2:  # library comparison point (cuBLAS through torch), not a path of the product
-        ms = _time(lambda: torch.matmul(A, W.t()), a.iters)
+    it = [0]
+
+    def nxt():
+        it[0] = (it[0] + 1) % ncopy
+        return Ws[it[0]]
+
+    if a.cublas:  # library comparison point (cuBLAS through torch), not a path of the product
+        ms = _time(lambda: torch.matmul(A, nxt().t()), a.iters)
     else:
-        ms = _time(lambda: P.debug_gemm(A, W, C, a.path), a.iters)
+        if a.path == 5:  # weights in the packed tile layout
+            Ws = [P.pack_weights(w) for w in Ws]
+        path = P.gemm_path(a.path, a.stages, a.splits, getattr(a, "bn", 0))
+        ms = _time(lambda: P.debug_gemm(A, nxt(), C, path, N=a.N), a.iters)
     byts = (a.N * a.K + a.M * a.K) * 2 + a.M * a.N * 4
-    return dict(kernel="gemm", M=a.M, N=a.N, K=a.K, path=a.path, us=ms * 1e3, GBps=byts / ms / 1e6,
+    return dict(kernel="gemm", M=a.M, N=a.N, K=a.K, path=-1 if a.cublas else a.path, stages=a.stages, splits=a.splits,
+                bn=getattr(a, "bn", 0), us=ms * 1e3, GBps=byts / ms / 1e6,
                 TFLOPs=2 * a.M * a.N * a.K / ms / 1e9)
 
 
@@ -79,7 +97,15 @@ def main():
     ap.add_argument("--M", type=int, default=136)
     ap.add_argument("--N", type=int, default=None, help="gemm N (default 4096) / attention keys (default 768)")
     ap.add_argument("--K", type=int, default=4096)
-    ap.add_argument("--path", type=int, default=1, help="0 CUDA cores, 1 tcgen05, 2 cuBLAS (reference point)")
+    ap.add_argument("--path", type=int, default=1,
+                    help="0 CUDA cores, 1 tcgen05 (library's choice), 2 row-tiled tcgen05, "
+                         "3 weight-stationary tcgen05, 4 stream-K weight-stationary tcgen05, "
+                         "5 stream-K on packed weights")
+    ap.add_argument("--cublas", action="store_true", help="time cuBLAS (through torch) instead: comparison point")
+    ap.add_argument("--stages", type=int, default=0, help="tcgen05 ring depth (0 = library's choice)")
+    ap.add_argument("--bn", type=int, default=0, help="row-tiled columns per tile (0 = library's choice)")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="tcgen05 cluster K split, or CTA count for path 4 (0 = library's choice)")
     ap.add_argument("--R", type=int, default=136)
     ap.add_argument("--H", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=32)

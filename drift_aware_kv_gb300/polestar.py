@@ -23,7 +23,8 @@ FP32, BF16 = 0, 1
 EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
             "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
             "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
-            "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc")
+            "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc",
+            "polestar_packed_weight_bytes", "polestar_pack_weights")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
 
@@ -92,6 +93,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_debug_kmeans.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_uint64,
                                           C.c_int32, P, P, P, P, P, P, P]
     lib.polestar_debug_kmeans.restype = C.c_int
+    lib.polestar_packed_weight_bytes.argtypes = [C.c_int32, C.c_int32]
+    lib.polestar_packed_weight_bytes.restype = C.c_int64
+    lib.polestar_pack_weights.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P]
+    lib.polestar_pack_weights.restype = C.c_int
     lib.polestar_profile_begin.argtypes = [P, C.c_int32]
     lib.polestar_profile_end.argtypes = [P, C.POINTER(polestar_kernel_stats), C.c_int32]
     for f in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
@@ -205,16 +210,42 @@ class Polestar:
                 for name, a in zip(KERNEL_CLASSES, arr)}
 
 
-def debug_gemm(A, W, out, path: int, m_dev=None, stream=None):
-    """out = A @ W^T through the library's projection kernel (path 0 CUDA cores,
-    1 tcgen05).  torch CUDA tensors, row-major with unit inner stride."""
+def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0) -> int:
+    """`path` of polestar_debug_gemm: kernel 0 CUDA cores, 1 tcgen05 (library's
+    choice), 2 row-tiled tcgen05, 3 weight-stationary tcgen05, 4 persistent
+    stream-K weight-stationary tcgen05 (5: the same on packed weights); stages /
+    splits override the ring depth and the cluster K split (kernels 2, 3) or the
+    CTA count (kernels 4, 5); bn the columns per tile of kernel 2 (a multiple of
+    16); 0 = automatic."""
+    return kernel | (stages << 8) | (splits << 16) | ((bn // 16) << 24)
+
+
+def pack_weights(W, stream=None):
+    """W [N, K] bf16 (CUDA, unit inner stride) -> new uint8 CUDA tensor holding
+    its packed tile layout (polestar_pack_weights)."""
+    import torch
+    lib = load()
+    N, K = W.shape
+    nbytes = int(lib.polestar_packed_weight_bytes(N, K))
+    out = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.polestar_pack_weights(C.c_void_p(W.data_ptr()), W.stride(0), N, K, C.c_void_p(out.data_ptr()),
+                                     C.c_void_p(st.cuda_stream)))
+    return out
+
+
+def debug_gemm(A, W, out, path: int, m_dev=None, stream=None, N=None):
+    """out = A @ W^T through the library's projection kernel (``path`` as built
+    by gemm_path).  torch CUDA tensors, row-major with unit inner stride."""
     import torch
     lib = load()
     M, K = A.shape
-    N = W.shape[0]
+    if N is None:
+        N = W.shape[0]
     st = stream if stream is not None else torch.cuda.current_stream()
     dt = BF16 if A.dtype == torch.bfloat16 else FP32
-    _check(lib.polestar_debug_gemm(C.c_void_p(A.data_ptr()), A.stride(0), C.c_void_p(W.data_ptr()), W.stride(0),
+    ldw = W.stride(0) if W.dim() == 2 else K
+    _check(lib.polestar_debug_gemm(C.c_void_p(A.data_ptr()), A.stride(0), C.c_void_p(W.data_ptr()), ldw,
                                    C.c_void_p(out.data_ptr()), out.stride(0), M,
                                    C.c_void_p(m_dev.data_ptr()) if m_dev is not None else None, N, K, dt,
                                    path, C.c_void_p(st.cuda_stream)))

@@ -107,8 +107,9 @@ polestar_status polestar_init(const polestar_config *cfg, const polestar_layer_w
                               void *stream_main, void *stream_side, polestar_ctx **out);
 
 /* One denoising step of Polestar-Cache over every layer (Algorithm 1).
- *   x0          device [batch, N, d] (config dtype): layer-0 hidden states of
- *               the current step (embeddings of the partially unmasked sequence)
+ *   x0          device [batch, N, d] (config dtype), 16-byte aligned: layer-0
+ *               hidden states of the current step (embeddings of the partially
+ *               unmasked sequence)
  *   n_unmasked  host [batch]: tokens unmasked since the previous step (drives the
  *               tau_upd trigger of §4.1 "Update Schedule"); ignored at block entry
  *   block_index active block b, 0 <= b < gen_len / block
@@ -189,13 +190,37 @@ polestar_status polestar_profile_end(polestar_ctx *ctx, polestar_kernel_stats *o
 /* ---- projection kernel on caller buffers (test hook) ----
  * C[M, N] (fp32, row stride ldc) = A[M, K] (row stride lda) * W[N, K]^T (row
  * stride ldw), A and W in `dtype`, all device pointers, on `stream`.
- * path 0: CUDA-core kernel; path 1: tcgen05 tensor-core kernel (bf16 only).
+ * path 0: CUDA-core kernel; path 1: tcgen05 tensor-core kernels (bf16 only)
+ * with the library's own choice of kernel, ring depth and K split; path 2 /
+ * 3 / 4: the row-tiled / weight-stationary (M <= 256) / persistent stream-K
+ * weight-stationary (M <= 256) tcgen05 kernel, with bits 8-15 of `path`
+ * giving the ring depth and bits 16-23 the K split over a cluster (paths 2
+ * and 3) or the number of CTAs (paths 4, 5), and bits 24-31 the columns per
+ * tile of path 2 in units of 16; 0 = automatic.  Path 5 is path 4
+ * with W given in the packed tile layout of polestar_pack_weights (ldw is
+ * then ignored).  A combination the kernel cannot run (too much shared
+ * memory, more than 8 splits, more CTAs than SMs) returns UNSUPPORTED.
  * m_dev (device int, may be NULL) lowers the row count on the device: rows at
  * or beyond min(M, *m_dev) are left untouched.  Asynchronous; returns
  * UNSUPPORTED for a path/dtype/stride combination the kernels do not cover. */
 polestar_status polestar_debug_gemm(const void *A, int32_t lda, const void *W, int32_t ldw, float *C,
                                     int32_t ldc, int32_t M, const int32_t *m_dev, int32_t N, int32_t K,
                                     int32_t dtype, int32_t path, void *stream);
+
+/* ---- packed tile layout of a projection matrix ----
+ * The weight-streaming projection kernel reads weights as contiguous 16 KB
+ * units: for each 128-row tile of W [N, K] (bf16, row stride ldw >= K) and
+ * each 64-column k-tile, the 128 x 64 block as a 128-byte-swizzled shared-
+ * memory image (row r at byte r*128 of the unit, 16-byte chunk j of the row
+ * stored at chunk j XOR (r mod 8)), zero outside W; the k-tiles of a tile are
+ * adjacent and tiles follow in order.  polestar_packed_weight_bytes gives the
+ * size (-1 for N < 1 or K < 1); polestar_pack_weights writes the layout of W
+ * into `out` (device, 16-byte aligned, that many bytes) asynchronously on
+ * `stream`.  (The library's own layer loop streams weights through 2D tensor
+ * maps of the caller's matrices; the packed layout serves callers and tests
+ * of the persistent weight-streaming kernel, path 5 of polestar_debug_gemm.) */
+int64_t polestar_packed_weight_bytes(int32_t N, int32_t K);
+polestar_status polestar_pack_weights(const void *W, int32_t ldw, int32_t N, int32_t K, void *out, void *stream);
 
 /* ---- row attention + KL drift on caller buffers (test hook) ----
  * One sequence: q [R, H*dh] (rotary applied), kv [N, 2, Hkv*dh] (K then V of

@@ -28,9 +28,117 @@ def _ref(A, W, rows):
     return a @ w.T
 
 
-@pytest.mark.parametrize("path", [1, 0])
+# path: 0 CUDA cores, 1 tcgen05 (library's choice), 2 row-tiled, 3 weight-stationary,
+# 4 persistent stream-K weight-stationary
+@pytest.mark.parametrize("path", [1, 0, 2, 3, 4])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_matches_definition(path, M, N, K):
+    if path in (3, 4) and M > 256:
+        pytest.skip("weight-stationary kernels hold at most 256 rows")
+    _check_gemm(path, M, N, K)
+
+
+# stream-K: grid sizes that cut tiles at every kind of boundary (one CTA, a
+# prime count, more CTAs than k-tiles in a tile, one per SM) and ring depths
+@pytest.mark.parametrize("stages,ctas", [(0, 1), (2, 7), (12, 5), (4, 148), (6, 0), (3, 97)])
+@pytest.mark.parametrize("M,N,K", [(136, 4096, 4096), (16, 640, 1024), (256, 384, 3584), (5, 200, 448)])
+def test_stream_k_configs(stages, ctas, M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    np_rows = max(16, (M + 15) // 16 * 16)
+    max_stages = min(12, (232448 - 2048) // (16384 + np_rows * 128))
+    if stages > max_stages:
+        with pytest.raises(P.PolestarError):
+            _check_gemm(P.gemm_path(4, stages, ctas), M, N, K)
+        return
+    _check_gemm(P.gemm_path(4, stages, ctas), M, N, K)
+
+
+@pytest.mark.parametrize("N,K", [(200, 200), (128, 64), (384, 1376)])
+def test_packed_layout_is_the_swizzled_tile_image(N, K):
+    """Unit (t, k) holds rows t*128.. and columns k*64.. of W; within the unit
+    row r sits at r*128 bytes and its 16-byte chunk j at chunk j ^ (r % 8)."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cpu").manual_seed(N + K)
+    W = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    packed = P.pack_weights(W.cuda()).cpu()
+    tiles, kts = -(-N // 128), -(-K // 64)
+    assert packed.numel() == tiles * kts * 16384
+    u = packed.view(torch.int16).view(tiles, kts, 128, 8, 8).numpy()  # [t, k, row, chunk, elem]
+    r = np.arange(128)[:, None]
+    logical = np.arange(8)[None, :] ^ (r % 8)             # chunk j of row r holds logical chunk j ^ (r % 8)
+    unswz = np.empty_like(u)
+    unswz[:, :, r, logical] = u[:, :, r, np.arange(8)[None, :]]
+    full = unswz.transpose(0, 2, 1, 3, 4).reshape(tiles * 128, kts * 64)
+    Wi = W.view(torch.int16).numpy()
+    assert np.array_equal(full[:N, :K], Wi)
+    assert not full[N:].any() and not full[:, K:].any()
+
+
+@pytest.mark.parametrize("ctas", [0, 1, 7, 97])
+@pytest.mark.parametrize("M,N,K", [(136, 4096, 4096), (16, 640, 1024), (256, 384, 3584), (5, 200, 448),
+                                   (33, 384, 1376)])
+def test_stream_k_packed_weights(ctas, M, N, K):
+    """Path 5: stream-K reading the packed copy with contiguous bulk loads."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cpu").manual_seed(M * 7919 + N * 31 + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W = (0.02 * torch.randn(N, K, generator=g)).to(torch.bfloat16).cuda()
+    Wp = P.pack_weights(W)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    P.debug_gemm(A, Wp, C, P.gemm_path(5, 0, ctas), N=N)
+    ref_C = torch.full((M, N), float("nan"), device="cuda")
+    P.debug_gemm(A, W, ref_C, P.gemm_path(4, 0, ctas))
+    torch.cuda.synchronize()
+    assert torch.equal(C, ref_C)  # same MMAs in the same order: bit-identical to the tensor-map path
+    ref = _ref(A, W, np.arange(M))
+    scale = np.sqrt((A.double().cpu().numpy() ** 2).sum(1))[:, None] * \
+        np.sqrt((W.double().cpu().numpy() ** 2).sum(1))[None, :]
+    assert (np.abs(C.double().cpu().numpy() - ref) / scale).max() < 2e-6
+
+
+def test_stream_k_repeated_launches_reset_counters():
+    """The per-tile arrival counters return to zero after every launch: many
+    back-to-back launches with pieces cut between CTAs stay exact."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cpu").manual_seed(11)
+    M, N, K = 100, 1024, 2048
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W = (0.02 * torch.randn(N, K, generator=g)).to(torch.bfloat16).cuda()
+    C = torch.empty(M, N, device="cuda")
+    ref = torch.empty(M, N, device="cuda")
+    P.debug_gemm(A, W, ref, P.gemm_path(4, 0, 13))
+    for _ in range(50):
+        C.fill_(float("nan"))
+        P.debug_gemm(A, W, C, P.gemm_path(4, 0, 13))
+    torch.cuda.synchronize()
+    assert torch.equal(C, ref)  # fixed summation order: bit-identical
+
+
+# column widths, K splits and ring depths of the row-tiled kernel, forced; one
+# and two 128-row sub-tiles, ragged columns and K
+@pytest.mark.parametrize("bn,splits,stages", [(16, 1, 0), (48, 3, 0), (176, 1, 0), (256, 2, 3), (144, 8, 4),
+                                              (80, 1, 2)])
+@pytest.mark.parametrize("M,N,K", [(100, 1000, 1376), (200, 4608, 2048), (33, 384, 4096)])
+def test_row_tiled_configs(bn, splits, stages, M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    _check_gemm(P.gemm_path(2, stages, splits, bn), M, N, K)
+
+
+# ring depths and cluster K splits of the weight-stationary kernel, forced
+@pytest.mark.parametrize("stages,splits", [(2, 1), (3, 2), (4, 4), (8, 1), (5, 8), (6, 3)])
+@pytest.mark.parametrize("M,N,K", [(136, 4096, 4096), (16, 640, 1024), (256, 384, 3584)])
+def test_weight_stationary_configs(stages, splits, M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    np_rows = max(16, (M + 15) // 16 * 16)
+    stage = 128 * 64 * 2 + np_rows * 64 * 2
+    if stages * stage + 2048 > 232448 or (splits > 1 and stages * stage < np_rows * 132 * 4):
+        with pytest.raises(P.PolestarError):  # does not fit in shared memory
+            _check_gemm(P.gemm_path(3, stages, splits), M, N, K)
+        return
+    _check_gemm(P.gemm_path(3, stages, splits), M, N, K)
+
+
+def _check_gemm(path, M, N, K):
     from drift_aware_kv_gb300 import polestar as P
     g = torch.Generator(device="cpu").manual_seed(M * 7919 + N * 31 + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
@@ -48,16 +156,37 @@ def test_gemm_matches_definition(path, M, N, K):
     assert err.max() < 2e-6, err.max()
 
 
-def test_gemm_device_row_count_leaves_tail_untouched():
+@pytest.mark.parametrize("path,m_live", [(1, 77), (2, 77), (3, 77), (3, 0), (3, 1), ((2 << 16) | 3, 17),
+                                         ((4 << 16) | 3, 200), (4, 77), (4, 0), ((9 << 16) | 4, 33)])
+def test_gemm_device_row_count_leaves_tail_untouched(path, m_live):
     from drift_aware_kv_gb300 import polestar as P
     g = torch.Generator(device="cpu").manual_seed(5)
-    M, N, K = 200, 256, 512
+    M, N, K = 200, 256, 1024
     A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
     W = (0.02 * torch.randn(N, K, generator=g)).to(torch.bfloat16).cuda()
     C = torch.full((M, N), -7.0, device="cuda")
-    m = torch.tensor([77], dtype=torch.int32, device="cuda")
-    P.debug_gemm(A, W, C, 1, m_dev=m)
+    m = torch.tensor([m_live], dtype=torch.int32, device="cuda")
+    P.debug_gemm(A, W, C, path, m_dev=m)
     torch.cuda.synchronize()
-    ref = _ref(A, W, np.arange(77))
-    assert np.allclose(C[:77].double().cpu().numpy(), ref, atol=1e-3)
-    assert torch.all(C[77:] == -7.0)
+    ref = _ref(A, W, np.arange(m_live))
+    assert np.allclose(C[:m_live].double().cpu().numpy(), ref, atol=1e-3)
+    assert torch.all(C[m_live:] == -7.0)
+
+
+def test_gemm_rejects_unrunnable_choice():
+    from drift_aware_kv_gb300 import polestar as P
+    A = torch.zeros(300, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(300, 128, device="cuda")
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A, W, C, P.gemm_path(3))          # more than 256 rows
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A[:64], W, C[:64], P.gemm_path(3, 9))   # ring deeper than the kernel's barriers
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A[:64], W, C[:64], P.gemm_path(3, 2, 9))  # cluster larger than 8
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A, W, C, P.gemm_path(4))          # more than 256 rows
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A[:64], W, C[:64], P.gemm_path(4, 13))  # ring deeper than the kernel's barriers
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A[:64], W, C[:64], P.gemm_path(4, 0, 255))  # more CTAs than SMs
