@@ -172,6 +172,9 @@ def run_device(args, w, peaks, ws, rank, local):
     if len(steps) < total:
         raise SystemExit(f"trajectory has only {len(steps)} steps < warmup + steps = {total}")
     stream = torch.cuda.current_stream(dev)
+    # the NVFP4 store's host traffic runs on a side stream of its own
+    offload = not args.device_store
+    side = torch.cuda.Stream(dev) if offload else None
     cm = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device=dev)
     timed = steps[args.warmup:]
 
@@ -180,7 +183,7 @@ def run_device(args, w, peaks, ws, rank, local):
         region runs without per-kernel events (they would serialise the
         programmatic dependent launches); the profiled region repeats the same
         steps with CUDA events around every launch for the per-class times."""
-        ps = P.Polestar(w, W, stream=stream)
+        ps = P.Polestar(w, W, stream=stream, side_stream=side, host_offload=offload)
 
         def do_step(st):
             ps.calibrate_step(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"])
@@ -228,7 +231,7 @@ def run_device(args, w, peaks, ws, rank, local):
     # ---- e2e: host buffers through polestar_step_host, copies in the timed region
     e2e = None
     if not args.no_e2e:
-        ps2 = P.Polestar(w, W, stream=stream)
+        ps2 = P.Polestar(w, W, stream=stream, side_stream=side, host_offload=offload)
         host = []
         for st in steps:
             host.append(dict(x0=st["x0"].cpu().pin_memory(), logits=st["logits"].cpu().pin_memory(),
@@ -278,6 +281,7 @@ def run_device(args, w, peaks, ws, rank, local):
                    "layers": w.n_layers, "d_model": w.d_model, "batch": w.batch, "seq_len": w.seq_len,
                    "block": w.block, "window": w.prefix_win + w.suffix_win, "K": w.K, "topk": w.topk,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "nvfp4_store": "pinned host, 2-layer device ring" if offload else "device",
                    "l2": "per-step working set (weights) >> L2; no flush needed",
                    "timed_block_entries": n_entry, "timed_within_block_steps": n_within},
         "window_tokens_per_s": value * w.batch * nw_mean,
@@ -373,6 +377,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--device-store", action="store_true",
+                    help="keep the NVFP4 residual store in device memory instead of pinned host memory")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

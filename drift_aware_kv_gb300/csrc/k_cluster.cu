@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(KM_THREADS) kmeans_encode_kernel(KmeansArgs a,
   const int d = a.d, K = a.K, nw = a.nw;
   const int ds = d / cs;
   const uint32_t rank = km_rank();
-  const int prob = blockIdx.x / cs;                    // = layer * batch + seq
+  const int local = blockIdx.x / cs;                   // problem of this launch
+  const int prob = a.layer0 * a.batch + local;         // = layer * batch + seq
   const int layer = prob / a.batch, seq = prob % a.batch;
   const int c0 = (int)rank * ds;
   float* Xs = sm;                                      // [nw][ds]
@@ -257,11 +258,11 @@ __global__ void __launch_bounds__(KM_THREADS) kmeans_encode_kernel(KmeansArgs a,
     for (int e = 0; e < 16; ++e) r[e] = Xs[(size_t)i * ds + g * 16 + e] - zs[c * ds + g * 16 + e];
     uint8_t packed[8];
     const int gg = c0 / 16 + g;
-    a.scales[((size_t)prob * a.Wmax + i) * ng + gg] = nvfp4_encode16(r, packed);
+    a.scales[((size_t)local * a.Wmax + i) * ng + gg] = nvfp4_encode16(r, packed);
     uint2 pk;
     pk.x = packed[0] | (packed[1] << 8) | (packed[2] << 16) | ((uint32_t)packed[3] << 24);
     pk.y = packed[4] | (packed[5] << 8) | (packed[6] << 16) | ((uint32_t)packed[7] << 24);
-    *(uint2*)(a.codes + ((size_t)prob * a.Wmax + i) * (d / 2) + gg * 8) = pk;
+    *(uint2*)(a.codes + ((size_t)local * a.Wmax + i) * (d / 2) + gg * 8) = pk;
   }
 }
 

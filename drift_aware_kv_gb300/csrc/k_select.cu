@@ -14,44 +14,56 @@ namespace polestar {
 
 __global__ void select_kernel(SelectArgs a) {
   pdl_enter();
-  __shared__ int s_topk[32][16];
+  __shared__ int s_taken[32];
   __shared__ int s_count[33];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  // 1. per sequence: D_c, top-k (thread s)
-  for (int s = tid; s < a.batch; s += blockDim.x) {
+  // 1. per sequence (one warp): D_c = mean over heads of the proxy KL (lanes
+  //    over heads, every cluster's loads in flight together), then top-k
+  for (int s = warp; s < a.batch; s += nwarps) {
     const int pr = a.proxy_row[s];
     float* D = a.drift + (size_t)s * a.K;
     int* tk = a.topk_out + (size_t)s * a.topk;
     if (pr < 0) {
-      for (int c = 0; c < a.K; ++c) D[c] = 0.f;
-      for (int i = 0; i < a.topk; ++i) tk[i] = -1;
+      if (lane < a.K) D[lane] = 0.f;
+      if (lane < a.topk) tk[lane] = -1;
       continue;
     }
-    float Dv[16];
-    for (int c = 0; c < a.K; ++c) {
-      float sum = 0.f;
-      for (int h = 0; h < a.H; ++h) sum += a.kl_rows[(size_t)(pr + c) * a.H + h];
-      Dv[c] = sum / (float)a.H;
-      D[c] = Dv[c];
+    float Dv[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) Dv[c] = 0.f;
+    for (int h0 = 0; h0 < a.H; h0 += 32) {
+      const int h = h0 + lane;
+      float v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) v[c] = (c < a.K && h < a.H) ? a.kl_rows[(size_t)(pr + c) * a.H + h] : 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) Dv[c] += v[c];
     }
-    unsigned taken = 0;
-    for (int i = 0; i < a.topk; ++i) {
-      int best = -1;
-      for (int c = 0; c < a.K; ++c) {
-        if (taken & (1u << c)) continue;
-        if (best < 0 || Dv[c] > Dv[best]) best = c;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      Dv[c] = warp_sum(Dv[c]) / (float)a.H;
+      if (lane == 0 && c < a.K) D[c] = Dv[c];
+    }
+    if (lane == 0) {
+      unsigned taken = 0;
+      for (int i = 0; i < a.topk; ++i) {
+        int best = -1;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (c >= a.K || (taken & (1u << c))) continue;
+          if (best < 0 || Dv[c] > Dv[best]) best = c;
+        }
+        taken |= 1u << best;
+        tk[i] = best;
       }
-      taken |= 1u << best;
-      tk[i] = best;
-      if (s < 32) s_topk[s][i] = best;
+      s_taken[s] = (int)taken;
     }
-    if (s < 32) s_topk[s][15] = (int)taken;
   }
   __syncthreads();
   // 2. selection masks and per-sequence counts (warp per sequence)
   for (int s = warp; s < a.batch; s += nwarps) {
     const bool fire = a.proxy_row[s] >= 0;
-    const unsigned taken = fire ? (unsigned)s_topk[s][15] : 0u;
+    const unsigned taken = fire ? (unsigned)s_taken[s] : 0u;
     int count = 0;
     for (int j0 = 0; j0 < a.Wmax; j0 += 32) {
       const int j = j0 + lane;

@@ -100,13 +100,14 @@ void launch_row_attention(const AttnArgs& a, cudaStream_t st);
 struct KmeansArgs {
   const float* Hw;         // [L, batch, Wmax, d] block-entry layer inputs of window rows
   int L, batch, Wmax, nw, d, K, iters;
+  int layer0;              // first layer of this launch (it covers layers layer0 .. layer0 + L - 1)
   uint64_t seed;
   int block;
   uint8_t* labels;         // [L, batch, Wmax]
   float* z;                // [L, batch, K, d]
   float* csum;             // [L, batch, K, d]
   float* anchor;           // [L, batch, K, d]
-  uint8_t* codes;          // [L, batch, Wmax, d/2]
+  uint8_t* codes;          // [L, batch, Wmax, d/2] of this launch's layers (from layer0)
   uint8_t* scales;         // [L, batch, Wmax, d/16]
 };
 void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st);

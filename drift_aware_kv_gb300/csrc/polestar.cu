@@ -66,8 +66,17 @@ struct polestar_ctx {
   float2* rope = nullptr;        // [N, dh/2]
   uint8_t* labels = nullptr;     // [L, b, Wmax]
   float *z = nullptr, *csum = nullptr, *anchor = nullptr;  // [L, b, K, d]
-  uint8_t *codes = nullptr, *scales = nullptr;             // device [L, b, Wmax, d/2], [.., d/16]
-  uint8_t *codes_host = nullptr, *scales_host = nullptr;   // pinned mirror (host_offload)
+  // NVFP4 residual store.  Without host_offload: device [L, b, Wmax, d/2] and
+  // [.., d/16].  With host_offload the store is pinned host memory of that shape
+  // and the device holds a ring of two layers [2, b, Wmax, ..], filled ahead of
+  // use and written back after each re-encode on the side stream.
+  uint8_t *codes = nullptr, *scales = nullptr;
+  uint8_t *codes_host = nullptr, *scales_host = nullptr;
+  uint8_t *codes_host_dev = nullptr, *scales_host_dev = nullptr;  // device addresses of the host store
+  bool offload = false;
+  cudaEvent_t ring_in[2] = {nullptr, nullptr};    // side: layer copied into the slot
+  cudaEvent_t ring_used[2] = {nullptr, nullptr};  // main: the slot's kernel is done
+  cudaEvent_t ring_out[2] = {nullptr, nullptr};   // side: the slot is copied out
   float *pprev = nullptr, *pprev_lse = nullptr;            // [L, b, K, H, N], [L, b, K, H]
   float *aprev = nullptr, *aprev_lse = nullptr;            // [b, B, H, N], [b, B, H]
   float* theta = nullptr;        // [b, B, hist]
@@ -233,6 +242,12 @@ void free_all(polestar_ctx* c) {
   if (c->meta_ev) cudaEventDestroy(c->meta_ev);
   if (c->side_ev) cudaEventDestroy(c->side_ev);
   if (c->main_ev) cudaEventDestroy(c->main_ev);
+  for (int i = 0; i < 2; ++i) {
+    if (c->ring_in[i]) cudaEventDestroy(c->ring_in[i]);
+    if (c->ring_used[i]) cudaEventDestroy(c->ring_used[i]);
+    if (c->ring_out[i]) cudaEventDestroy(c->ring_out[i]);
+    c->ring_in[i] = c->ring_used[i] = c->ring_out[i] = nullptr;
+  }
   c->meta_ev = c->side_ev = c->main_ev = nullptr;
   tc_gemm_cache_clear(&c->tc);
   prof_release(c);
@@ -344,6 +359,45 @@ polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int
     return POLESTAR_OK;
   }
   RUN(c->gemm_cls, bytes, flops, (launch_gemm_simt<T>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm)));
+  return POLESTAR_OK;
+}
+
+// ------------------------------------------------------------------ NVFP4 store offload
+// With host_offload the residual store lives in pinned host memory.  The block
+// entry's encoder writes it directly (device mapping of the pinned buffer, over
+// NVLink-C2C on Grace-Blackwell); within a block, layer l is fetched into device
+// ring slot l & 1 one layer ahead on the side stream and written back after its
+// patch.  Every main-stream use of a slot is followed by ring_writeback (side
+// stream, after the use), and the fetch of a later layer into that slot is
+// queued behind it on the side stream, so a slot is never refilled before its
+// previous contents reached the host.
+size_t code_layer_bytes(const polestar_ctx* c) { return (size_t)c->b * c->Wmax * (c->d / 2); }
+size_t scale_layer_bytes(const polestar_ctx* c) { return (size_t)c->b * c->Wmax * (c->d / 16); }
+uint8_t* layer_codes(polestar_ctx* c, int l) {
+  return c->codes + (size_t)(c->offload ? (l & 1) : l) * code_layer_bytes(c);
+}
+uint8_t* layer_scales(polestar_ctx* c, int l) {
+  return c->scales + (size_t)(c->offload ? (l & 1) : l) * scale_layer_bytes(c);
+}
+
+// side stream: host store layer l -> its ring slot; main waits before use
+polestar_status ring_fetch(polestar_ctx* c, int l) {
+  const size_t cb = code_layer_bytes(c), sb = scale_layer_bytes(c);
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(layer_codes(c, l), c->codes_host + (size_t)l * cb, cb, cudaMemcpyHostToDevice, c->ss));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(layer_scales(c, l), c->scales_host + (size_t)l * sb, sb, cudaMemcpyHostToDevice, c->ss));
+  CUDA_OR_FAIL(c, cudaEventRecord(c->ring_in[l & 1], c->ss));
+  CUDA_OR_FAIL(c, cudaStreamWaitEvent(c->sm, c->ring_in[l & 1], 0));
+  return POLESTAR_OK;
+}
+
+// after the main-stream kernel that wrote slot l & 1: slot -> host store layer l
+polestar_status ring_writeback(polestar_ctx* c, int l) {
+  const size_t cb = code_layer_bytes(c), sb = scale_layer_bytes(c);
+  CUDA_OR_FAIL(c, cudaEventRecord(c->ring_used[l & 1], c->sm));
+  CUDA_OR_FAIL(c, cudaStreamWaitEvent(c->ss, c->ring_used[l & 1], 0));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->codes_host + (size_t)l * cb, layer_codes(c, l), cb, cudaMemcpyDeviceToHost, c->ss));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->scales_host + (size_t)l * sb, layer_scales(c, l), sb, cudaMemcpyDeviceToHost, c->ss));
+  CUDA_OR_FAIL(c, cudaEventRecord(c->ring_out[l & 1], c->ss));
   return POLESTAR_OK;
 }
 
@@ -500,9 +554,22 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
   ka.z = c->z;
   ka.csum = c->csum;
   ka.anchor = c->anchor;
-  ka.codes = c->codes;
-  ka.scales = c->scales;
-  RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_kmeans_encode(ka, c->sm)));
+  if (!c->offload) {
+    ka.layer0 = 0;
+    ka.codes = c->codes;
+    ka.scales = c->scales;
+    RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_kmeans_encode(ka, c->sm)));
+  } else {
+    // every layer at once, the encoder storing straight into the pinned host
+    // store through its device mapping; the previous step's write-backs to
+    // that store (side stream) finish first
+    CUDA_OR_FAIL(c, cudaEventRecord(c->side_ev, c->ss));
+    CUDA_OR_FAIL(c, cudaStreamWaitEvent(c->sm, c->side_ev, 0));
+    ka.layer0 = 0;
+    ka.codes = c->codes_host_dev;
+    ka.scales = c->scales_host_dev;
+    RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_kmeans_encode(ka, c->sm)));
+  }
   // proxy-attention baseline P(t_b, l) of every layer
   const int Rp = (int)pad8((size_t)b * c->K);
   const int4* prow = meta_d<int4>(c, c->ml.prow_off);
@@ -619,10 +686,27 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_window<T>(x0, meta_d<int>(c, c->ml.win_pos_off), c->nw, fire_d, n_fire, N, d, c->Wmax, c->U,
                             sel_prev, c->sm)));
   }
+  if (n_fire > 0 && c->offload) {
+    // fetches read the host store only after everything queued on the main
+    // stream so far (the block entry's encoder writes it directly)
+    CUDA_OR_FAIL(c, cudaEventRecord(c->main_ev, c->sm));
+    CUDA_OR_FAIL(c, cudaStreamWaitEvent(c->ss, c->main_ev, 0));
+    TRY(ring_fetch(c, 0));
+  }
   for (int l = 0; l < L; ++l) {
     const polestar_layer_weights& w = c->W[l];
     float* zl = c->z + (size_t)l * b * c->K * d;
     if (n_fire > 0) {
+      // next layer's residual codes come in while this layer runs
+      if (c->offload && l + 1 < L) {
+        const size_t cb = code_layer_bytes(c), sb = scale_layer_bytes(c);
+        CUDA_OR_FAIL(c, cudaMemcpyAsync(layer_codes(c, l + 1), c->codes_host + (size_t)(l + 1) * cb, cb,
+                                        cudaMemcpyHostToDevice, c->ss));
+        CUDA_OR_FAIL(c, cudaMemcpyAsync(layer_scales(c, l + 1), c->scales_host + (size_t)(l + 1) * sb, sb,
+                                        cudaMemcpyHostToDevice, c->ss));
+        CUDA_OR_FAIL(c, cudaEventRecord(c->ring_in[(l + 1) & 1], c->ss));
+      }
+      if (c->offload && l > 0) CUDA_OR_FAIL(c, cudaStreamWaitEvent(c->sm, c->ring_in[l & 1], 0));
       PatchArgs pa{};
       pa.fire_seqs = fire_d;
       pa.n_fire = n_fire;
@@ -632,8 +716,8 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       pa.K = c->K;
       pa.labels = c->labels + (size_t)l * b * c->Wmax;
       pa.anchor = c->anchor + (size_t)l * b * c->K * d;
-      pa.codes = c->codes + (size_t)l * b * c->Wmax * (d / 2);
-      pa.scales = c->scales + (size_t)l * b * c->Wmax * (d / 16);
+      pa.codes = layer_codes(c, l);
+      pa.scales = layer_scales(c, l);
       pa.U = c->U;
       pa.sel_prev = sel_prev;
       pa.win_row = win_row_d;
@@ -647,6 +731,7 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       pa.a_out = c->a_in;
       pa.proxy_row = proxy_row_d;
       RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_window_patch<T>(pa, c->sm)));
+      if (c->offload) TRY(ring_writeback(c, l));
       RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_centroid_update<T>(pa, c->sm)));
     }
     // the projections' input rows were normalised by their producers: active
@@ -817,8 +902,17 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
     TRY(dalloc(c, &c->z, sizeof(float) * (size_t)L * b * K * d));
     TRY(dalloc(c, &c->csum, sizeof(float) * (size_t)L * b * K * d));
     TRY(dalloc(c, &c->anchor, sizeof(float) * (size_t)L * b * K * d));
-    TRY(dalloc(c, &c->codes, (size_t)L * b * Wmax * (d / 2)));
-    TRY(dalloc(c, &c->scales, (size_t)L * b * Wmax * (d / 16)));
+    c->offload = cfg->host_offload != 0;
+    const int code_layers = c->offload ? 2 : L;
+    TRY(dalloc(c, &c->codes, (size_t)code_layers * b * Wmax * (d / 2)));
+    TRY(dalloc(c, &c->scales, (size_t)code_layers * b * Wmax * (d / 16)));
+    if (c->offload) {
+      for (int i = 0; i < 2; ++i) {
+        CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->ring_in[i], cudaEventDisableTiming));
+        CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->ring_used[i], cudaEventDisableTiming));
+        CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->ring_out[i], cudaEventDisableTiming));
+      }
+    }
     TRY(dalloc(c, &c->pprev, sizeof(float) * (size_t)L * b * K * H * N));
     TRY(dalloc(c, &c->pprev_lse, sizeof(float) * (size_t)L * b * K * H));
     TRY(dalloc(c, &c->aprev, sizeof(float) * (size_t)b * B * H * N));
@@ -872,6 +966,8 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
     if (cfg->host_offload) {
       TRY(halloc(c, &c->codes_host, (size_t)L * b * Wmax * (d / 2)));
       TRY(halloc(c, &c->scales_host, (size_t)L * b * Wmax * (d / 16)));
+      CUDA_OR_FAIL(c, cudaHostGetDevicePointer((void**)&c->codes_host_dev, c->codes_host, 0));
+      CUDA_OR_FAIL(c, cudaHostGetDevicePointer((void**)&c->scales_host_dev, c->scales_host, 0));
     }
     CUDA_OR_FAIL(c, cudaDeviceSynchronize());
     return POLESTAR_OK;
@@ -1027,8 +1123,22 @@ extern "C" polestar_status polestar_debug_read(polestar_ctx* c, int32_t which, i
     case POLESTAR_BUF_CSUM: base = c->csum; per = b * K * d * 4; break;
     case POLESTAR_BUF_ANCHOR: base = c->anchor; per = b * K * d * 4; break;
     case POLESTAR_BUF_LABELS: base = c->labels; per = b * Wmax; break;
-    case POLESTAR_BUF_CODES: base = c->codes; per = b * Wmax * (d / 2); break;
-    case POLESTAR_BUF_SCALES: base = c->scales; per = b * Wmax * (d / 16); break;
+    case POLESTAR_BUF_CODES:
+    case POLESTAR_BUF_SCALES: {
+      const bool cd = which == POLESTAR_BUF_CODES;
+      const size_t pl = cd ? code_layer_bytes(c) : scale_layer_bytes(c);
+      if (layer < 0 || (size_t)layer >= L) return fail(c, POLESTAR_ERR_INVALID_ARG, "layer out of range");
+      if (bytes > pl) return fail(c, POLESTAR_ERR_INVALID_ARG, "bytes exceeds the buffer size");
+      if (c->offload) {  // the host store is authoritative
+        CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+        CUDA_OR_FAIL(c, cudaStreamSynchronize(c->ss));
+        std::memcpy(host_dst, (cd ? c->codes_host : c->scales_host) + (size_t)layer * pl, bytes);
+        return POLESTAR_OK;
+      }
+      base = cd ? c->codes : c->scales;
+      per = pl;
+      break;
+    }
     case POLESTAR_BUF_ACT_OUT: base = c->h_rows; per = b * B * d * 4; layered = false; break;
     case POLESTAR_BUF_UPDATE: base = c->U; per = b * Wmax * d * 4; layered = false; break;
     case POLESTAR_BUF_CONF: base = c->conf; per = b * 2 * B * 4; layered = false; break;
