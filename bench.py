@@ -34,6 +34,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "llada8b_p512_g256_b1"
+# DRAM bytes (read + write) per launch of a kernel class, from one Nsight Compute
+# capture of the current kernels (profiles/gemm_tc_projections_llada8b_b1.md:
+# mean over the four within-block projection launches of a layer).  Reset to
+# None whenever those kernels change.
+NCU_TRAFFIC_PER_LAUNCH = {("llada8b_p512_g256_b1", "gemm_step"): 112.8e6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -266,6 +271,9 @@ def run_device(args, w, peaks, ws, rank, local):
         achieved = s["bytes"] / (s["ms"] / 1e3) / 1e9 if s["ms"] > 0 else 0.0
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": None, "peak_source": peaks["_source"]}
+    roof["traffic"] = NCU_TRAFFIC_PER_LAUNCH.get((w.name, dom))
+    roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
+    roof["algorithmic_bytes_per_launch"] = s["bytes"] / max(1, s["launches"])
     roof["avg_launch_us"] = s["ms"] * 1e3 / max(1, s["launches"])
     roof["launches"] = s["launches"]
     roof["measured_in"] = "profiled timed region (same steps, CUDA events around each launch)"
