@@ -1018,40 +1018,32 @@ int ws_stages_for(int np, int ctas, int splits) {
   return s;
 }
 
-// Launch choice for at most 256 rows (one row group).  Among single-wave
-// configurations (at most one CTA per SM), estimate a CTA's time as the bytes
-// it streams - its weight columns plus, at half weight, its box of A rows read
-// from L2 - at one SM's share of the HBM bandwidth, plus 0.4 us per cluster
-// split for the reduction, and take the cheapest of the row-tiled kernel at
-// every column width and the weight-stationary kernel (128-column tiles).
-// (Measured on GB300 for the projection shapes of the layer loop: the choice is
-// the fastest configuration or within a few percent of it.)
-struct GemmPick {
-  int kernel;  // 1 row-tiled, 2 weight-stationary
-  int bn, splits;
-};
+// Stand-in for the occupancy queries below; never launched.  The occupancy
+// calculator treats any kernel that allocates tensor memory as one CTA per SM,
+// while the hardware runs as many as shared memory allows (measured: a
+// 3-stage weight-stationary launch shows no second wave up to 2 CTAs per SM).
+// The launchers pad shared memory so co-resident CTAs never ask for more than
+// 512 TMEM columns between them, so a kernel without tensor memory, with the
+// same threads and the same launch shared memory, gives the true capacity.
+__global__ void __launch_bounds__(THREADS) occupancy_standin_kernel(int* p) {
+  if (p) p[threadIdx.x] = threadIdx.x;
+}
 
-// Clusters of `cluster` CTAs of `func` (with `smem` bytes of dynamic shared
-// memory) that the device runs at once; 0 when the query is unavailable.
-int max_active_clusters(const void* func, int threads, int smem, int cluster) {
-  struct Key {
-    const void* f;
-    int smem, cluster;
-    bool operator<(const Key& o) const {
-      return f != o.f ? f < o.f : (smem != o.smem ? smem < o.smem : cluster < o.cluster);
-    }
-  };
-  static std::map<Key, int> memo;
+// Clusters of `cluster` CTAs of THREADS threads and `smem` bytes of dynamic
+// shared memory that the device runs at once; 0 when the query is unavailable.
+int max_active_clusters(int smem, int cluster) {
+  static std::map<std::pair<int, int>, int> memo;
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
-  const Key key{func, smem, cluster};
+  const std::pair<int, int> key{smem, cluster};
   auto it = memo.find(key);
   if (it != memo.end()) return it->second;
+  const void* func = (const void*)occupancy_standin_kernel;
   int n = 0;
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) == cudaSuccess) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(1, 1, cluster);
-    cfg.blockDim = dim3(threads);
+    cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1067,48 +1059,77 @@ int max_active_clusters(const void* func, int threads, int smem, int cluster) {
   return n;
 }
 
+// Launch choice for at most 256 rows (one row group).  Candidates: the
+// row-tiled kernel at every column width (one CTA per SM) and the
+// weight-stationary kernel (128-column tiles) with 1-4 CTAs resident per SM,
+// each with a K split of 1-8 and every CTA (and cluster) resident at once
+// (cudaOccupancyMaxActiveClusters).  A candidate's time is the bytes streamed
+// by the busiest SM - per CTA its weight columns plus, at half weight, its box
+// of A rows read from L2 - at one SM's share of the HBM bandwidth, credited 1.5x
+// (1.6x) when two (three or more) independent load pipelines share the SM,
+// plus 0.4 us per cluster split for the reduction.  (Measured on GB300 over the
+// projection shapes of the layer loop against forced sweeps of every
+// configuration: the pick is the fastest or within a few percent of it.)
+struct GemmPick {
+  int kernel;  // 1 row-tiled, 2 weight-stationary
+  int bn, splits, stages;
+};
+
 GemmPick pick_small_m(int MT, int M, const int* N, int nseg, int ktiles, int nsm) {
-  GemmPick best{1, 128, 1};
+  GemmPick best{1, 128, 1, 0};
   double tbest = 1e30;
-  const void* rt_func = MT == 2 ? (const void*)gemm_kernel<2> : (const void*)gemm_kernel<1>;
-  auto consider = [&](int kernel, int bn, int s, double a_rows) {
+  const int np = std::max(16, (M + 15) & ~15);
+  int ws_tmem = 32;
+  while (ws_tmem < np) ws_tmem *= 2;
+  // kernel 1: resident = 1; kernel 2: resident CTAs per SM and ring depth given
+  auto consider = [&](int kernel, int bn, int s, int resident, int stages, double a_rows) {
     const long long ctas = (long long)rt_tiles(N, nseg, bn) * s;
-    if (ctas > nsm) return;
+    if (ctas > (long long)nsm * resident) return;
+    int smem;
+    if (kernel == 1) {
+      int tmem = 32;
+      while (tmem < MT * bn) tmem *= 2;
+      smem = std::max(rt_smem_bytes(MT, bn, stages), 233472 / (512 / tmem + 1) - 1024 + 16);
+    } else {
+      smem = std::max(ws_smem_bytes(np, stages), 233472 / (512 / ws_tmem + 1) - 1024 + 16);
+    }
     if (s > 1) {
       // every cluster must be resident at once (a cluster size that does not
       // divide the SMs of a GPC leaves some idle and forces a second wave)
-      int smem, tmem = 32;
-      if (kernel == 1) {
-        while (tmem < MT * bn) tmem *= 2;
-        smem = std::max(rt_smem_bytes(MT, bn, rt_max_stages(MT, bn)), 233472 / (512 / tmem + 1) - 1024 + 16);
-      } else {
-        const int np = std::max(16, (M + 15) & ~15);
-        while (tmem < np) tmem *= 2;
-        smem = std::max(ws_smem_bytes(np, ws_stages_for(np, 1, s)), 233472 / (512 / tmem + 1) - 1024 + 16);
-      }
-      const int mc = max_active_clusters(kernel == 1 ? rt_func : (const void*)gemm_ws_kernel, THREADS, smem, s);
-      if (mc <= 0 || ctas / s > mc) return;
+      // (with a tenth of the capacity to spare: a grid that needs every last
+      // cluster slot was measured to spill clusters into a second wave)
+      const int mc = max_active_clusters(smem, s);
+      if (mc <= 0 || (double)(ctas / s) > 0.9 * mc) return;
     }
+    const long long per_sm = (ctas + nsm - 1) / nsm;
+    const double credit = per_sm >= 3 ? 1.6 : (per_sm == 2 ? 1.5 : 1.0);
     const double kel = (double)ktiles * BK / s;
-    const double t = (bn + 0.5 * a_rows) * kel * 2.0 / 50e3 + 0.4 * s;
+    const double t = per_sm * (bn + 0.5 * a_rows) * kel * 2.0 / 50e3 / credit + 0.4 * s;
     if (t < tbest * 0.999) {
       tbest = t;
-      best = GemmPick{kernel, bn, s};
+      best = GemmPick{kernel, bn, s, stages};
     }
   };
-  const int np = std::max(16, (M + 15) & ~15);
   for (int s = 1; s <= 8; ++s) {
     if (s > 1 && ktiles < 8 * s) break;
     for (int bn = 16; bn <= 256; bn += 16) {
       if (MT * bn > 512 || rt_max_stages(MT, bn) < 3) continue;
       if (s > 1 && rt_max_stages(MT, bn) * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4) continue;
-      consider(1, bn, s, MT * BM);
+      consider(1, bn, s, 1, rt_max_stages(MT, bn), MT * BM);
     }
-    if (ws_stages_for(np, 1, s) >= 2) consider(2, BN, s, np);
+    // (rings shallower than 3 stages and reductions over more than 4 CTAs were
+    // measured slower than the time estimate says; they are not candidates)
+    for (int r = 1; r <= 4 && r * ws_tmem <= 512 && s <= 4; ++r) {
+      const int budget = 233472 / r - 1024;  // dynamic shared memory per CTA for r per SM
+      const int stages = std::min(WS_MAX_STAGES, (budget - 2048) / ws_stage_bytes(np));
+      if (stages < 3) break;
+      if (s > 1 && stages * ws_stage_bytes(np) < np * RED_PITCH * 4) continue;
+      consider(2, BN, s, r, stages, np);
+    }
   }
   if (tbest >= 1e30) {
     // more 16-column tiles than SMs even unsplit: widest tiles, several waves
-    best = GemmPick{1, 256 / MT, 1};
+    best = GemmPick{1, 256 / MT, 1, 0};
   }
   return best;
 }
@@ -1213,13 +1234,14 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   int kind = force && force->kernel ? force->kernel : 0;
   // columns per tile: 128 for the weight-stationary kernels (the MMA's M side),
   // chosen per launch for the row-tiled kernel (its N side)
-  int bn = BN, auto_splits = 0;
+  int bn = BN, auto_splits = 0, auto_stages = 0;
   if (kind == 0) {
     if (mgroups == 1) {
       const GemmPick pk = pick_small_m(MT, M, N, nseg, ktiles, nsm);
       kind = pk.kernel;
       bn = pk.bn;
       auto_splits = pk.splits;
+      auto_stages = pk.stages;
     } else {
       kind = 1;
       bn = 256;  // many row groups: widest tiles for the fewest re-reads of A
@@ -1295,7 +1317,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     } else if (!auto_splits) {
       while (splits < 8 && tiles * splits * 2 <= nsm && ktiles >= splits * 2 * 8) splits *= 2;
     }
-    int stages = force && force->stages ? force->stages : ws_stages_for(p.np, 1, splits);
+    int stages = force && force->stages ? force->stages : (auto_stages ? auto_stages : ws_stages_for(p.np, 1, splits));
     if (splits < 1 || splits > 8 || stages < 2 || stages > WS_MAX_STAGES ||
         ws_smem_bytes(p.np, stages) > 232448 ||
         (splits > 1 && stages * ws_stage_bytes(p.np) < p.np * RED_PITCH * 4))
@@ -1330,6 +1352,32 @@ cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void*
   if (M <= 0 || N <= 0) return cudaSuccess;
   return tc_gemm_bf16_multi(cache, A, lda, 1, &W, &ldw, &N, &C, ldc, M, m_dev, K, st, force,
                             Wpacked ? &Wpacked : nullptr);
+}
+
+cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, int K, int* out) {
+  using namespace tc;
+  if (M <= 0 || nseg < 1 || nseg > 3 || K < 1 || !out) return cudaErrorInvalidValue;
+  if (cache->num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&cache->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  const int MT = M > BM ? 2 : 1;
+  const int mgroups = (M + MT * BM - 1) / (MT * BM);
+  const int ktiles = (K + BK - 1) / BK;
+  if (mgroups > 1) {
+    out[0] = 1;
+    out[1] = 256;
+    out[2] = 1;
+    out[3] = rt_max_stages(MT, 256);
+    return cudaSuccess;
+  }
+  const GemmPick pk = pick_small_m(MT, M, N, nseg, ktiles, cache->num_sms);
+  out[0] = pk.kernel;
+  out[1] = pk.bn;
+  out[2] = pk.splits;
+  out[3] = pk.stages;
+  return cudaSuccess;
 }
 
 size_t tc_packed_bytes(int N, int K) {

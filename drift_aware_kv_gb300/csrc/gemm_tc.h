@@ -81,6 +81,11 @@ size_t tc_packed_bytes(int N, int K);
 // Writes that layout of W (row stride ldw) to out (16-byte aligned), on st.
 cudaError_t tc_pack_weights(const void* W, int ldw, int N, int K, void* out, cudaStream_t st);
 
+// The launch the library picks for M rows, nseg weight segments of N[i]
+// output columns and inner size K: out = {kernel (1 row-tiled, 2
+// weight-stationary), columns per tile, K split, ring depth}.
+cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, int K, int* out);
+
 // Allocates the stream-K workspace and counters (once per cache).
 cudaError_t tc_gemm_reserve(TcGemmCache* cache);
 

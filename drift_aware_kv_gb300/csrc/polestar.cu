@@ -1230,6 +1230,13 @@ extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const
   return cudaGetLastError() == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 
+extern "C" polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, const int32_t* N, int32_t K,
+                                                      int32_t* out) {
+  static TcGemmCache cache;
+  if (!N || !out || M < 1 || nseg < 1 || nseg > 3 || K < 1) return POLESTAR_ERR_INVALID_ARG;
+  return tc_gemm_choice(&cache, M, nseg, N, K, out) == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
 extern "C" int64_t polestar_packed_weight_bytes(int32_t N, int32_t K) {
   if (N < 1 || K < 1) return -1;
   return (int64_t)tc_packed_bytes(N, K);

@@ -24,7 +24,7 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
             "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
             "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc",
-            "polestar_packed_weight_bytes", "polestar_pack_weights")
+            "polestar_packed_weight_bytes", "polestar_pack_weights", "polestar_debug_gemm_choice")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
 
@@ -97,6 +97,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_packed_weight_bytes.restype = C.c_int64
     lib.polestar_pack_weights.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P]
     lib.polestar_pack_weights.restype = C.c_int
+    lib.polestar_debug_gemm_choice.argtypes = [C.c_int32, C.c_int32, C.POINTER(C.c_int32), C.c_int32,
+                                               C.POINTER(C.c_int32)]
+    lib.polestar_debug_gemm_choice.restype = C.c_int
     lib.polestar_profile_begin.argtypes = [P, C.c_int32]
     lib.polestar_profile_end.argtypes = [P, C.POINTER(polestar_kernel_stats), C.c_int32]
     for f in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
@@ -218,6 +221,15 @@ def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0) -> int
     CTA count (kernels 4, 5); bn the columns per tile of kernel 2 (a multiple of
     16); 0 = automatic."""
     return kernel | (stages << 8) | (splits << 16) | ((bn // 16) << 24)
+
+
+def gemm_choice(M: int, Ns, K: int) -> dict:
+    """The projection launch the library picks (polestar_debug_gemm_choice)."""
+    lib = load()
+    arr = (C.c_int32 * len(Ns))(*[int(n) for n in Ns])
+    out = (C.c_int32 * 4)()
+    _check(lib.polestar_debug_gemm_choice(int(M), len(Ns), arr, int(K), out))
+    return dict(kernel=int(out[0]), bn=int(out[1]), splits=int(out[2]), stages=int(out[3]))
 
 
 def pack_weights(W, stream=None):

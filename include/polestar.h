@@ -207,6 +207,14 @@ polestar_status polestar_debug_gemm(const void *A, int32_t lda, const void *W, i
                                     int32_t ldc, int32_t M, const int32_t *m_dev, int32_t N, int32_t K,
                                     int32_t dtype, int32_t path, void *stream);
 
+/* ---- the projection launch the library picks (test hook) ----
+ * For M rows (bf16 tensor-core path), nseg (1..3) weight segments with N[i]
+ * (host array) output columns and inner size K: out[4] (host) = {kernel: 1
+ * row-tiled, 2 weight-stationary; output columns per tile; K split over a
+ * cluster; ring depth}.  Queries the current device's occupancy; launches
+ * nothing. */
+polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, const int32_t *N, int32_t K, int32_t *out);
+
 /* ---- packed tile layout of a projection matrix ----
  * The weight-streaming projection kernel reads weights as contiguous 16 KB
  * units: for each 128-row tile of W [N, K] (bf16, row stride ldw >= K) and

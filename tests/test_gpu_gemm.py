@@ -190,3 +190,26 @@ def test_gemm_rejects_unrunnable_choice():
         P.debug_gemm(A[:64], W, C[:64], P.gemm_path(4, 13))  # ring deeper than the kernel's barriers
     with pytest.raises(P.PolestarError):
         P.debug_gemm(A[:64], W, C[:64], P.gemm_path(4, 0, 255))  # more CTAs than SMs
+
+
+@pytest.mark.parametrize("M,Ns,K", [(136, [4096, 1024, 1024], 4096), (32, [12288, 12288], 4096), (128, [4096], 12288),
+                                    (80, [3584], 3584), (200, [512, 512], 1184)])
+def test_library_choice_is_valid_and_reproducible(M, Ns, K):
+    """The launch the library picks is a runnable configuration, and forcing
+    exactly that configuration reproduces the automatic launch bit for bit."""
+    from drift_aware_kv_gb300 import polestar as P
+    ch = P.gemm_choice(M, Ns, K)
+    assert ch["kernel"] in (1, 2) and ch["splits"] >= 1 and ch["stages"] >= 2
+    assert ch["bn"] % 16 == 0 and 16 <= ch["bn"] <= 256
+    N = Ns[0]
+    g = torch.Generator(device="cpu").manual_seed(M + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W = (0.02 * torch.randn(N, K, generator=g)).to(torch.bfloat16).cuda()
+    c1 = torch.empty(M, N, device="cuda")
+    c2 = torch.empty(M, N, device="cuda")
+    P.debug_gemm(A, W, c1, P.gemm_path(1))
+    ch1 = P.gemm_choice(M, [N], K)
+    path = P.gemm_path(1 + ch1["kernel"], ch1["stages"], ch1["splits"], ch1["bn"] if ch1["kernel"] == 1 else 0)
+    P.debug_gemm(A, W, c2, path)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
