@@ -1134,6 +1134,48 @@ GemmPick pick_small_m(int MT, int M, const int* N, int nseg, int ktiles, int nsm
   return best;
 }
 
+// More than 256 rows (several 256-row groups): the row-tiled kernel at the
+// column width and K split whose waves of (tiles x row groups x splits) CTAs,
+// one per SM, take the least time, a CTA costing the larger of its streamed
+// bytes (as in pick_small_m) and its MMA work at one SM's share of the bf16
+// tensor peak, plus 0.4 us per split.
+GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm) {
+  const int MT = 2, mgroups = (M + 2 * BM - 1) / (2 * BM);
+  GemmPick best{1, 256, 1, rt_max_stages(MT, 256)};
+  double tbest = 1e30;
+  for (int s = 1; s <= 4; s *= 2) {
+    if (s > 1 && ktiles < 8 * s) break;
+    for (int bn = 32; bn <= 256; bn += 16) {
+      if (rt_max_stages(MT, bn) < 3) continue;
+      if (s > 1 && rt_max_stages(MT, bn) * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4) continue;
+      const long long ctas = (long long)rt_tiles(N, nseg, bn) * mgroups * s;
+      long long waves = (ctas + nsm - 1) / nsm;
+      if (s > 1) {
+        // waves of resident clusters; a wave that needs nearly every cluster
+        // slot counts as two (see pick_small_m)
+        int tmem = 32;
+        while (tmem < MT * bn) tmem *= 2;
+        const int smem = std::max(rt_smem_bytes(MT, bn, rt_max_stages(MT, bn)), 233472 / (512 / tmem + 1) - 1024 + 16);
+        const int mc = max_active_clusters(smem, s);
+        if (mc <= 0) continue;
+        const long long clusters = ctas / s;
+        waves = (clusters + mc - 1) / mc;
+        if (waves == 1 && clusters > 0.9 * mc) waves = 2;
+      }
+      const double kel = (double)ktiles * BK / s;
+      const double t_mem = (bn + 0.5 * MT * BM) * kel * 2.0 / 50e3;
+      const double t_mma = 2.0 * MT * BM * bn * kel / 13.0e6;
+      const double t = waves * std::max(t_mem, t_mma) + 0.4 * s;
+      if (t < tbest * 0.999) {
+        tbest = t;
+        best = GemmPick{1, bn, s, rt_max_stages(MT, bn)};
+      }
+    }
+  }
+  return best;
+}
+
+
 cudaError_t launch_ws(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid,
                       cudaStream_t st) {
   static bool attr = false;
@@ -1243,14 +1285,16 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
       auto_splits = pk.splits;
       auto_stages = pk.stages;
     } else {
+      const GemmPick pk = pick_large_m(M, N, nseg, ktiles, nsm);
       kind = 1;
-      bn = 256;  // many row groups: widest tiles for the fewest re-reads of A
+      bn = pk.bn;
+      auto_splits = pk.splits;
     }
   } else if (kind == 1 && force->bn) {
     bn = force->bn;
     if (bn < 16 || bn > 256 || (bn & 15) || MT * bn > 512) return cudaErrorInvalidValue;
   } else if (kind == 1) {
-    bn = mgroups == 1 ? pick_small_m(MT, M, N, nseg, ktiles, nsm).bn : 256;
+    bn = mgroups == 1 ? pick_small_m(MT, M, N, nseg, ktiles, nsm).bn : pick_large_m(M, N, nseg, ktiles, nsm).bn;
   }
   const CUtensorMap* mb[3] = {nullptr, nullptr, nullptr};
   int tiles = 0;
@@ -1365,14 +1409,8 @@ cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, in
   const int MT = M > BM ? 2 : 1;
   const int mgroups = (M + MT * BM - 1) / (MT * BM);
   const int ktiles = (K + BK - 1) / BK;
-  if (mgroups > 1) {
-    out[0] = 1;
-    out[1] = 256;
-    out[2] = 1;
-    out[3] = rt_max_stages(MT, 256);
-    return cudaSuccess;
-  }
-  const GemmPick pk = pick_small_m(MT, M, N, nseg, ktiles, cache->num_sms);
+  const GemmPick pk = mgroups > 1 ? tc::pick_large_m(M, N, nseg, ktiles, cache->num_sms)
+                                  : tc::pick_small_m(MT, M, N, nseg, ktiles, cache->num_sms);
   out[0] = pk.kernel;
   out[1] = pk.bn;
   out[2] = pk.splits;

@@ -80,19 +80,26 @@ struct AttnArgs {
   int measure;             // 1: write KL(new || prev) to kl_out[r, h]
   int store;               // 1: replace prev by the new scores
   float* kl_out;           // [R, H]
-  // bf16 tensor-core path: CTA work list {row_start, row_count <= 64, seq, 0};
-  // a work item never spans two sequences (nullptr: CUDA-core path by rows)
+  // bf16 tensor-core path: work list of items {rowA, nA, rowB, nB}, each the
+  // rows [rowA, rowA + nA) and [rowB, rowB + nB) of ONE sequence, at most
+  // ATT_ITEM_ROWS in all (nullptr: CUDA-core path by rows)
   const int4* work;
   int n_work;
-  // key splits (grid z): > 1 writes per-split partials to `part` ([splits, R, H,
-  // 5 + dh] fp32: max, sum, KL numerator, q-mass, expm1 sum, unnormalised
-  // output) and a combine kernel finishes; `part` must hold splits*R*H*(5+dh)
+  int batch;               // sequences in the K/V view of kv_layer
+  // set by the launcher: key ranges per (item, head) (a thread-block cluster
+  // whose partials meet in distributed shared memory) and K/V ring depth
   int splits;
-  float* part;
+  int stages;
+  int* err;                // device word for the code of a timed-out wait (may be null)
 };
-// Largest key-split count the launcher may pick for R rows with a workspace of
-// `part_floats` floats (1 when the grid is already large).
-int attention_splits(int R, int H, int N, int dh, size_t part_floats, int num_sms);
+constexpr int ATT_ITEM_ROWS = 48;  // 3 compute warps x 16 rows
+// Work items for the rows [a0, a0 + na) ++ [b0, b0 + nb) of one sequence,
+// appended at w[n..]; returns the new count (items of near-equal size).
+int attention_items(int4* w, int n, int a0, int na, int b0, int nb);
+// Key splits and ring depth of the pipelined bf16 kernel for a grid of n_work
+// items x H heads.
+int attention_pipe_config(int n_work, int H, int N, int dh, int num_sms, int* stages);
+cudaError_t launch_attention_pipe(const AttnArgs& a, int batch, cudaStream_t st);
 template <typename T>
 void launch_row_attention(const AttnArgs& a, cudaStream_t st);
 

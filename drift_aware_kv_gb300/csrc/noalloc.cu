@@ -6,8 +6,8 @@
 // serving loop in which cudaMalloc / cudaFree may synchronise the whole device.
 // For them, polestar_attention_noalloc runs the same bf16 tensor-core attention
 // kernels as the rest of the library, but every piece of scratch it needs (the
-// row table, the work list and the key-split partial results) lives in the
-// fixed-size file-scope device arrays below.  Those arrays exist on every GPU
+// row table and the work list; key-split partial results stay in distributed
+// shared memory) lives in the fixed-size file-scope device arrays below.  Those arrays exist on every GPU
 // that loads the library, for as long as the library stays loaded.
 #include <mutex>
 
@@ -18,20 +18,16 @@ namespace polestar {
 namespace {
 
 constexpr int kMaxRows = 256;                               // rows per call
-constexpr size_t kPartFloats = (size_t)2 * 1024 * 1024;    // 8 MiB of key-split partials
-constexpr int kMaxWork = kMaxRows / 64;
+constexpr int kMaxWork = (kMaxRows + ATT_ITEM_ROWS - 1) / ATT_ITEM_ROWS;
 constexpr int kMaxDevices = 64;
 
-static __device__ __align__(256) float g_scratch_part[kPartFloats];
 static __device__ __align__(256) int4 g_scratch_rows[kMaxRows];
 static __device__ __align__(256) int4 g_scratch_work[kMaxWork];
 
 struct DeviceScratch {
   bool ready = false;
-  float* part = nullptr;
   int4* rows = nullptr;
   int4* work = nullptr;
-  int num_sms = 0;
 };
 DeviceScratch g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -43,11 +39,8 @@ polestar_status resolve(int dev, DeviceScratch** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceScratch& s = g_dev[dev];
   if (!s.ready) {
-    if (cudaGetSymbolAddress((void**)&s.part, g_scratch_part) != cudaSuccess) return POLESTAR_ERR_CUDA;
     if (cudaGetSymbolAddress((void**)&s.rows, g_scratch_rows) != cudaSuccess) return POLESTAR_ERR_CUDA;
     if (cudaGetSymbolAddress((void**)&s.work, g_scratch_work) != cudaSuccess) return POLESTAR_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return POLESTAR_ERR_CUDA;
     s.ready = true;
   }
   *out = &s;
@@ -55,11 +48,16 @@ polestar_status resolve(int dev, DeviceScratch** out) {
 }
 
 // Row table (tracked rows carry their history, the rest only produce output)
-// and work list (64-row items), written on the device from the caller's flags.
-__global__ void fill_tables_kernel(const uint8_t* __restrict__ tracked, int R, int4* rows, int4* work) {
+// and work list (near-equal items of the row range [0, R), as attention_items
+// builds them), written on the device from the caller's flags.
+__global__ void fill_tables_kernel(const uint8_t* __restrict__ tracked, int R, int n_work, int4* rows,
+                                   int4* work) {
   for (int r = threadIdx.x; r < R; r += blockDim.x)
     rows[r] = make_int4(0, 0, (tracked && tracked[r]) ? ROW_ACTIVE : ROW_OTHER, r);
-  for (int i = threadIdx.x; i * 64 < R; i += blockDim.x) work[i] = make_int4(i * 64, min(64, R - i * 64), 0, 0);
+  for (int i = threadIdx.x; i < n_work; i += blockDim.x) {
+    const int lo = i * R / n_work, hi = (i + 1) * R / n_work;
+    work[i] = make_int4(lo, hi - lo, 0, 0);
+  }
 }
 
 }  // namespace
@@ -82,7 +80,8 @@ extern "C" polestar_status polestar_attention_noalloc(const void* q, const void*
   const polestar_status st0 = resolve(dev, &s);
   if (st0 != POLESTAR_OK) return st0;
   cudaStream_t st = (cudaStream_t)stream;
-  fill_tables_kernel<<<1, 256, 0, st>>>(tracked, R, s->rows, s->work);
+  const int n_work = (R + ATT_ITEM_ROWS - 1) / ATT_ITEM_ROWS;
+  fill_tables_kernel<<<1, 256, 0, st>>>(tracked, R, n_work, s->rows, s->work);
   AttnArgs a{};
   a.q = q;
   a.ldq = H * head_dim;
@@ -107,9 +106,8 @@ extern "C" polestar_status polestar_attention_noalloc(const void* q, const void*
   a.store = store;
   a.kl_out = kl;
   a.work = s->work;
-  a.n_work = (R + 63) / 64;
-  a.part = s->part;
-  a.splits = attention_splits(R, H, N, head_dim, kPartFloats, s->num_sms);
+  a.n_work = n_work;
+  a.batch = 1;
   launch_row_attention<__nv_bfloat16>(a, st);
   return cudaGetLastError() == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }

@@ -41,12 +41,6 @@ struct MetaLayout {
   int work_cap;
 };
 
-// Attention work items {row_start, row_count <= 64, seq, 0} covering the rows
-// [start, start + count) of one sequence.
-int push_work(int4* w, int n, int start, int count, int seq) {
-  for (int k = 0; k < count; k += 64) w[n++] = make_int4(start + k, std::min(64, count - k), seq, 0);
-  return n;
-}
 }  // namespace
 
 struct polestar_ctx {
@@ -84,8 +78,6 @@ struct polestar_ctx {
   float* Hw = nullptr;           // [L, b, Wmax, d]
   // workspaces
   float *h_rows = nullptr, *h1 = nullptr, *gout = nullptr, *kl_rows = nullptr;
-  float* attn_part = nullptr;   // key-split partials of the attention kernel
-  size_t attn_part_floats = 0;
   int num_sms = 148;
   void *a_in = nullptr, *q_rows = nullptr, *attn_out = nullptr;
   uint8_t* write_kv = nullptr;
@@ -105,6 +97,10 @@ struct polestar_ctx {
   uint8_t* meta_h = nullptr;
   uint8_t* meta_d = nullptr;
   cudaEvent_t meta_ev = nullptr, side_ev = nullptr, main_ev = nullptr;
+  // device word of timed-out waits (tensor-core GEMM, attention), copied to
+  // pinned memory after every step and checked at the next call
+  int* err_host = nullptr;
+  cudaEvent_t err_ev = nullptr;
   // host bookkeeping
   std::vector<int> cum;
   std::vector<uint8_t> fire;
@@ -240,6 +236,8 @@ void free_all(polestar_ctx* c) {
   c->dev_allocs.clear();
   c->host_allocs.clear();
   if (c->meta_ev) cudaEventDestroy(c->meta_ev);
+  if (c->err_ev) cudaEventDestroy(c->err_ev);
+  c->err_ev = nullptr;
   if (c->side_ev) cudaEventDestroy(c->side_ev);
   if (c->main_ev) cudaEventDestroy(c->main_ev);
   for (int i = 0; i < 2; ++i) {
@@ -279,7 +277,9 @@ std::string validate(const polestar_config* c) {
 
 MetaLayout meta_layout(int rows_cap, int b, int K, int Wmax, int N) {
   MetaLayout m{};
-  m.work_cap = b * (N / 64 + 2) + b * ((Wmax + K + 7) / 64 + 2) + 2 * b + 64;
+  // attention items (at most ATT_ITEM_ROWS rows of one sequence): block-entry
+  // rows, within-block rows (active block + window + proxies), proxy baselines
+  m.work_cap = b * (N / ATT_ITEM_ROWS + 2) + b * ((Wmax + K) / ATT_ITEM_ROWS + 3) + 2 * b + 64;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t r = o;
@@ -359,6 +359,28 @@ polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int
     return POLESTAR_OK;
   }
   RUN(c->gemm_cls, bytes, flops, (launch_gemm_simt<T>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm)));
+  return POLESTAR_OK;
+}
+
+// A wait inside a kernel that ran out of time (the kernels record its code in
+// the device error word and return): reported as POLESTAR_ERR_TIMEOUT by the
+// first call after the step that hit it.
+polestar_status check_timeouts(polestar_ctx* c) {
+  if (!c->err_ev || cudaEventQuery(c->err_ev) != cudaSuccess) {
+    cudaGetLastError();  // not ready (or never recorded): nothing to report yet
+    return POLESTAR_OK;
+  }
+  const int code = *c->err_host;
+  if (code == 0) return POLESTAR_OK;
+  *c->err_host = 0;
+  cudaMemsetAsync(c->tc.err, 0, sizeof(int), c->sm);
+  return fail(c, POLESTAR_ERR_TIMEOUT, "a device wait timed out (code " + std::to_string(code) +
+                                           "); the step's results are not valid");
+}
+
+polestar_status record_timeouts(polestar_ctx* c) {
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->err_host, c->tc.err, sizeof(int), cudaMemcpyDeviceToHost, c->sm));
+  CUDA_OR_FAIL(c, cudaEventRecord(c->err_ev, c->sm));
   return POLESTAR_OK;
 }
 
@@ -456,11 +478,11 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
   for (int s0 = 0; s0 < b; s0 += chunk) {
     const int ns = std::min(chunk, b - s0);
     chunk_work_off.push_back(nwk);
-    for (int i = 0; i < ns; ++i) nwk = push_work(work_h, nwk, i * per_seq, (int)E.size(), s0 + i);
+    for (int i = 0; i < ns; ++i) nwk = attention_items(work_h, nwk, i * per_seq, (int)E.size(), 0, 0);
     chunk_work_n.push_back(nwk - chunk_work_off.back());
   }
   const int proxy_work_off = nwk;
-  for (int s = 0; s < b; ++s) nwk = push_work(work_h, nwk, s * c->K, c->K, s);
+  for (int s = 0; s < b; ++s) nwk = attention_items(work_h, nwk, s * c->K, c->K, 0, 0);
   const int proxy_work_n = nwk - proxy_work_off;
   if (nwk > c->ml.work_cap) return fail(c, POLESTAR_ERR_UNSUPPORTED, "attention work list overflow");
   CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
@@ -518,10 +540,9 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       }
       const double attn_bytes = (double)ns * N * 2 * c->kvdim * c->esz +
                                 (l == L - 1 ? (double)ns * c->B * c->H * N * 4.0 : 0.0);
-      aa.part = c->attn_part;
-      aa.splits = attention_splits(aa.R, c->H, N, c->dh, c->attn_part_floats, c->num_sms);
+      aa.batch = b;
+      aa.err = tc_error_word(&c->tc);
       RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
-      if (c->bf16 && aa.splits > 1) ++c->launches;  // combine kernel
       TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
                                  c->a_in, c->sm)));
@@ -603,10 +624,9 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
     aa.work = work_d + proxy_work_off;
     aa.n_work = proxy_work_n;
     const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz + (double)b * c->K * c->H * N * 4.0;
-    aa.part = c->attn_part;
-    aa.splits = attention_splits(aa.R, c->H, N, c->dh, c->attn_part_floats, c->num_sms);
+    aa.batch = b;
+    aa.err = tc_error_word(&c->tc);
     RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
-    if (c->bf16 && aa.splits > 1) ++c->launches;  // combine kernel
   }
   std::fill(c->cum.begin(), c->cum.end(), 0);
   std::fill(c->fire.begin(), c->fire.end(), 0);
@@ -659,11 +679,9 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
   for (int i = 0; i < c->nw; ++i) wp[i] = c->win_pos[i];
   int4* work_h = meta_h<int4>(c, c->ml.work_off);
   int nwk = 0;
-  for (int s = 0; s < b; ++s) nwk = push_work(work_h, nwk, s * B, B, s);
-  for (int f = 0; f < n_fire; ++f) {
-    const int s = fire_seqs[f];
-    nwk = push_work(work_h, nwk, win_row[s], c->nw + c->K, s);
-  }
+  // one sequence's active rows and (when it refreshes) its window + proxy rows
+  for (int s = 0; s < b; ++s)
+    nwk = attention_items(work_h, nwk, s * B, B, win_row[s] >= 0 ? win_row[s] : 0, win_row[s] >= 0 ? c->nw + c->K : 0);
   if (nwk > c->ml.work_cap) return fail(c, POLESTAR_ERR_UNSUPPORTED, "attention work list overflow");
   CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
   CUDA_OR_FAIL(c, cudaEventRecord(c->meta_ev, c->sm));
@@ -777,10 +795,9 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz +
                               (double)n_fire * c->K * c->H * N * 8.0 +
                               (l == L - 1 ? (double)b * B * c->H * N * 8.0 : 0.0);
-    aa.part = c->attn_part;
-    aa.splits = attention_splits(aa.R, c->H, N, c->dh, c->attn_part_floats, c->num_sms);
+    aa.batch = b;
+    aa.err = tc_error_word(&c->tc);
     RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
-    if (c->bf16 && aa.splits > 1) ++c->launches;  // combine kernel
     SelectArgs sa{};
     sa.batch = b;
     sa.Wmax = c->Wmax;
@@ -885,6 +902,10 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
     CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->meta_ev, cudaEventDisableTiming));
     CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->side_ev, cudaEventDisableTiming));
     CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->main_ev, cudaEventDisableTiming));
+    CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->err_ev, cudaEventDisableTiming));
+    if (!tc_error_word(&c->tc)) return fail(c, POLESTAR_ERR_OOM, "device error word");
+    TRY(halloc(c, &c->err_host, sizeof(int)));
+    *c->err_host = 0;
     TRY(dalloc(c, &c->kv, (size_t)L * b * N * 2 * c->kvdim * c->esz));
     CUDA_OR_FAIL(c, cudaMemsetAsync(c->kv, 0, (size_t)L * b * N * 2 * c->kvdim * c->esz, c->sm));
     TRY(dalloc(c, &c->rope, sizeof(float2) * (size_t)N * (c->dh / 2)));
@@ -930,9 +951,6 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
       int dev = 0;
       cudaGetDevice(&dev);
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
-      // room for 8 key splits of the largest within-block row set
-      c->attn_part_floats = (size_t)8 * within_rows * H * (5 + c->dh);
-      TRY(dalloc(c, &c->attn_part, sizeof(float) * c->attn_part_floats));
     }
     TRY(dalloc(c, &c->a_in, c->esz * (size_t)R * std::max(std::max(d, c->F), c->qdim)));
     TRY(dalloc(c, &c->q_rows, c->esz * (size_t)R * c->qdim));
@@ -1000,6 +1018,7 @@ extern "C" polestar_status polestar_calibrate_step(polestar_ctx* c, const void* 
       if (n_unmasked[s] < 0) return fail(c, POLESTAR_ERR_INVALID_ARG, "negative n_unmasked");
   // the host metadata buffer may still be in flight from the previous step
   CUDA_OR_FAIL(c, cudaEventSynchronize(c->meta_ev));
+  TRY(check_timeouts(c));
   compute_window(c, block_index);
   polestar_status st = c->bf16 ? step_impl<__nv_bfloat16>(c, x0, n_unmasked, block_index, block_entry)
                                : step_impl<float>(c, x0, n_unmasked, block_index, block_entry);
@@ -1007,6 +1026,7 @@ extern "C" polestar_status polestar_calibrate_step(polestar_ctx* c, const void* 
     c->stepped = 0;
     return st;
   }
+  TRY(record_timeouts(c));
   c->cur_block = block_index;
   c->cur_entry = block_entry ? 1 : 0;
   c->stepped = 1;
@@ -1263,7 +1283,8 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   std::vector<int4> rows(R), work;
   for (int r = 0; r < R; ++r)
     rows[r] = make_int4(0, 0, (tracked && tracked[r]) ? ROW_ACTIVE : ROW_OTHER, r);
-  for (int k = 0; k < R; k += 64) work.push_back(make_int4(k, std::min(64, R - k), 0, 0));
+  work.resize((R + ATT_ITEM_ROWS - 1) / ATT_ITEM_ROWS);
+  work.resize(attention_items(work.data(), 0, 0, R, 0, 0));
   int4* d_rows = nullptr;
   int4* d_work = nullptr;
   if (cudaMalloc(&d_rows, sizeof(int4) * R) != cudaSuccess) return POLESTAR_ERR_OOM;
@@ -1298,15 +1319,7 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   a.kl_out = kl;
   a.work = d_work;
   a.n_work = (int)work.size();
-  int nsm = 148, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const size_t pf = (size_t)8 * R * H * (5 + head_dim);
-  float* d_part = nullptr;
-  if (dtype == POLESTAR_BF16 && cudaMalloc(&d_part, sizeof(float) * pf) == cudaSuccess) {
-    a.part = d_part;
-    a.splits = attention_splits(R, H, N, head_dim, pf, nsm);
-  }
+  a.batch = 1;
   if (dtype == POLESTAR_BF16)
     launch_row_attention<__nv_bfloat16>(a, st);
   else
@@ -1315,7 +1328,6 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   cudaFree(d_rows);
   cudaFree(d_work);
-  if (d_part) cudaFree(d_part);
   return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 

@@ -250,12 +250,11 @@ polestar_status polestar_debug_attention(const void *q, const void *kv, int32_t 
  * loop in which cudaMalloc/cudaFree may synchronise the device.  It computes the
  * same thing as polestar_debug_attention (bf16 only, head_dim 64 or 128), with
  * two differences: `tracked` is a DEVICE array [R] of flags (or NULL: no row
- * tracked), and all scratch (row table, work list, key-split partials) lives in
- * fixed file-scope device arrays of this library: at most 256 rows per call and
- * 8 MiB of partials; R > 256 is rejected with POLESTAR_ERR_INVALID_ARG, and when
- * the partials of a wider key split would not fit, fewer splits are used.
- * Every GPU that loads the library holds these arrays (about 8 MiB) until the
- * library is unloaded.  The first call on a device resolves their device
+ * tracked), and all scratch (row table and work list; key-split partials meet
+ * in distributed shared memory) lives in fixed file-scope device arrays of this
+ * library: at most 256 rows per call; R > 256 is rejected with
+ * POLESTAR_ERR_INVALID_ARG.  Every GPU that loads the library holds these
+ * arrays (about 4 KB) until the library is unloaded.  The first call on a device resolves their device
  * addresses (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture.  Calls share the arrays, which keep the last
  * call's contents: calls that overlap on the GPU (on different streams or
