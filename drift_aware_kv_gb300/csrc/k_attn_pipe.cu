@@ -16,6 +16,9 @@
 //     needs and releases it when done, so warps never wait for each other.
 //   * S = Q K^T and O += P V run on mma.sync m16n8k16 (fp32 accumulation) with
 //     ldmatrix reads that undo the swizzle; online softmax in log2 units.
+//   * Rows under drift tracking fetch their previous scores for the tile with
+//     cp.async into a per-warp shared-memory tile when the tile starts, so the
+//     fetch overlaps the wait for K/V and the S = Q K^T products.
 //   * Key ranges of one (item, head) form a thread-block cluster; their partial
 //     results meet in distributed shared memory and every CTA of the cluster
 //     finishes a slice of the rows (ranks in fixed order: deterministic).  No
@@ -45,13 +48,20 @@ template <int DH>
 __host__ __device__ constexpr int tile_bytes() {
   return 2 * TK * DH * 2;  // K + V, bf16
 }
+constexpr int PREV_PITCH = 72;   // floats per row of a warp's previous-score tile (spreads banks)
+// Per-row partials of a key range: max (log2 units), sum, KL numerator,
+// q-mass, expm1 sum, then DH outputs; the pitch keeps rows 16-byte aligned and
+// holds a previous-score row, which shares the space during the tile loop.
 template <int DH>
-__host__ __device__ constexpr int part_floats_per_row() {
-  return 5 + DH;  // max (log2 units), sum, KL numerator, q-mass, expm1 sum, output
+__host__ __device__ constexpr int part_pitch() {
+  return ((5 + DH + 3) / 4) * 4 < PREV_PITCH ? PREV_PITCH : ((5 + DH + 3) / 4) * 4;
 }
+// aligned ring | barriers, abort flag, previous-score row pointers | partials
+// (key splits) or per-warp previous-score tiles
 template <int DH>
 __host__ __device__ constexpr int smem_bytes(int stages, bool split) {
-  return 1024 + stages * tile_bytes<DH>() + 256 + (split ? ATT_ITEM_ROWS * part_floats_per_row<DH>() * 4 : 0);
+  return 1024 + stages * tile_bytes<DH>() + 1024 +
+         (split ? ATT_ITEM_ROWS * part_pitch<DH>() * 4 : CW * 16 * PREV_PITCH * 4);
 }
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -117,6 +127,26 @@ __device__ __forceinline__ float ex2f(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// e^x - 1 for the KL drift term.  For |x| < 1/8 the Taylor series of e^x - 1
+// through x^6 (the remainder is below |x| 8e-10); elsewhere 2^(x log2 e) - 1,
+// where |e^x - 1| > 0.11 so the subtraction costs at most a few bits.
+__device__ __forceinline__ float expm1_drift(float x) {
+  float t = fmaf(x, 1.f / 720.f, 1.f / 120.f);
+  t = fmaf(x, t, 1.f / 24.f);
+  t = fmaf(x, t, 1.f / 6.f);
+  t = fmaf(x, t, 0.5f);
+  t = fmaf(x, t, 1.f);
+  const float big = ex2f(x * 1.4426950408889634f) - 1.f;
+  return fabsf(x) < 0.125f ? x * t : big;
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *(const uint32_t*)&v;
@@ -153,12 +183,13 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   constexpr int TB = tile_bytes<DH>();
-  constexpr int PF = part_floats_per_row<DH>();
+  constexpr int PF = part_pitch<DH>();
   const int STAGES = p.stages;
   uint64_t* full = (uint64_t*)(sm + STAGES * TB);
   uint64_t* empty = full + MAX_STAGES;
   volatile int* abort_flag = (volatile int*)(empty + MAX_STAGES);
-  float* part = (float*)(sm + STAGES * TB + 256);  // [ATT_ITEM_ROWS][PF] with key splits
+  const float** ptab_all = (const float**)(sm + STAGES * TB + 128);  // [CW][16] previous-score rows
+  float* part = (float*)(sm + STAGES * TB + 1024);  // [ATT_ITEM_ROWS][PF] with key splits
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
@@ -229,9 +260,22 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
         prev[i] = p.active_prev + idx * p.N;
         prev_lse[i] = p.active_prev_lse + idx;
       }
-      if (prev[i] && p.measure) shift[i] = *prev_lse[i];
+      if (prev[i] && p.measure) shift[i] = *prev_lse[i] * 1.4426950408889634f;  // log2 units
     }
     const bool warp_tracked = __any_sync(0xffffffffu, prev[0] != nullptr || prev[1] != nullptr);
+    // previous scores of this warp's tracked rows come in per tile through
+    // shared memory: row pointers (null = not tracked) and the tile buffer
+    const float** ptab = ptab_all + warp * 16;
+    float* pbuf = part + warp * 16 * (nsplit > 1 ? PF : PREV_PITCH);
+    const bool fetch = warp_tracked && p.measure;
+    const bool vec = (p.N & 3) == 0 && (((uintptr_t)p.active_prev | (uintptr_t)p.proxy_prev) & 15) == 0;
+    if (fetch) {
+      if (qc == 0) {
+        ptab[qr] = prev[0];
+        ptab[qr + 8] = prev[1];
+      }
+      __syncwarp();
+    }
 
     // Q fragments (A operand) straight from global memory
     constexpr int KT = DH / 16;
@@ -261,6 +305,29 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
     for (int i = 0; i < ntl; ++i) {
       const int s = i % STAGES;
       const int j0 = (tbeg + i) * TK;
+      if (fetch) {
+        // this tile's previous scores: 16 rows x 64 keys
+        if (vec) {
+          const int c = (lane & 15) * 4;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int r = (lane >> 4) + 2 * k;
+            const float* src = ptab[r];
+            if (src && j0 + c < p.N) cp_async16(su32(pbuf + r * PREV_PITCH + c), src + j0 + c);
+          }
+        } else {
+          for (int r = 0; r < 16; ++r) {
+            const float* src = ptab[r];
+            if (!src) continue;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int c = hh * 32 + lane;
+              if (j0 + c < p.N) cp_async4(su32(pbuf + r * PREV_PITCH + c), src + j0 + c);
+            }
+          }
+        }
+        cp_async_commit();
+      }
       if (!mbar_wait(su32(&full[s]), (i / STAGES) & 1, p.err, 12, abort_flag)) break;
       const uint32_t kb = su32(sm + s * TB), vb = kb + TB / 2;
       // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
@@ -288,17 +355,9 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
           tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
         }
       }
-      // tracked rows: the whole tile's previous scores, fetched before any store
-      float spv[8][4];
-      if (warp_tracked) {
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ii = e >> 1;
-            const int j = j0 + nt * 8 + qc * 2 + (e & 1);
-            spv[nt][e] = (prev[ii] && p.measure && j < p.N) ? __ldcg(prev[ii] + j) : 0.f;
-          }
+      if (fetch) {
+        cp_async_wait_all();
+        __syncwarp();
       }
       float corr[2];
 #pragma unroll
@@ -328,21 +387,34 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
           lsum[e >> 1] += pv[e];
         }
         if (warp_tracked) {
+          const int j = j0 + nt * 8 + qc * 2;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ii = e >> 1;
-            const int j = j0 + nt * 8 + qc * 2 + (e & 1);
-            if (prev[ii] && j < p.N) {
-              const float s_nat = sc[nt][e] * 0.6931471805599453f;
-              if (p.measure) {
-                const float sp = spv[nt][e];
-                const float dj = s_nat - sp;
-                const float qt = expf(sp - shift[ii]);
-                asum[ii] += pv[e] * dj;
-                sqs[ii] += qt;
-                esum[ii] += qt * expm1f(dj);
+          for (int ii = 0; ii < 2; ++ii) {
+            if (!prev[ii] || j >= p.N) continue;
+            const float s0 = sc[nt][2 * ii] * 0.6931471805599453f, s1 = sc[nt][2 * ii + 1] * 0.6931471805599453f;
+            if (p.measure) {
+              // Eq. 4 terms against the previous scores sp (natural-log units):
+              // d = s - sp, q~ = exp(sp - lse_prev)
+              const float2 sp = *(const float2*)(pbuf + (qr + 8 * ii) * PREV_PITCH + nt * 8 + qc * 2);
+              const float d0 = s0 - sp.x, q0 = ex2f(fmaf(sp.x, 1.4426950408889634f, -shift[ii]));
+              asum[ii] = fmaf(pv[2 * ii], d0, asum[ii]);
+              sqs[ii] += q0;
+              esum[ii] = fmaf(q0, expm1_drift(d0), esum[ii]);
+              if (j + 1 < p.N) {
+                const float d1 = s1 - sp.y, q1 = ex2f(fmaf(sp.y, 1.4426950408889634f, -shift[ii]));
+                asum[ii] = fmaf(pv[2 * ii + 1], d1, asum[ii]);
+                sqs[ii] += q1;
+                esum[ii] = fmaf(q1, expm1_drift(d1), esum[ii]);
               }
-              spv[nt][e] = s_nat;
+            }
+            if (p.store) {
+              float* dst = prev[ii] + j;
+              if (j + 1 < p.N && (((uintptr_t)dst) & 7) == 0) {
+                *(float2*)dst = make_float2(s0, s1);
+              } else {
+                dst[0] = s0;
+                if (j + 1 < p.N) dst[1] = s1;
+              }
             }
           }
         }
@@ -354,23 +426,6 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
           pa[kt][2] = pack2(pv[0], pv[1]);
           pa[kt][3] = pack2(pv[2], pv[3]);
         }
-      }
-      if (warp_tracked && p.store) {
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int ii = 0; ii < 2; ++ii) {
-            const int j = j0 + nt * 8 + qc * 2;
-            if (prev[ii] && j < p.N) {
-              float* dst = prev[ii] + j;
-              if (j + 1 < p.N && (((uintptr_t)dst) & 7) == 0) {
-                *(float2*)dst = make_float2(spv[nt][2 * ii], spv[nt][2 * ii + 1]);
-              } else {
-                dst[0] = spv[nt][2 * ii];
-                if (j + 1 < p.N) dst[1] = spv[nt][2 * ii + 1];
-              }
-            }
-          }
       }
       // O += P V
 #pragma unroll
@@ -553,9 +608,9 @@ cudaError_t launch(const AttnArgs& a, int batch, cudaStream_t st) {
 int attention_pipe_config(int n_work, int H, int N, int dh, int num_sms, int* stages) {
   const int tiles = (N + ap::TK - 1) / ap::TK;
   int s = 1;
-  // key splits (a power of two, at most 8) while the grid stays within one wave
-  // of two CTAs per SM and every split keeps at least two tiles
-  while (s < 8 && (long long)n_work * H * s * 2 <= 2LL * num_sms && tiles >= 2 * s * 2) s *= 2;
+  // key splits (at most 8, the portable cluster size) while the grid stays
+  // within one wave of two CTAs per SM and every split keeps at least two tiles
+  while (s < 8 && (long long)n_work * H * (s + 1) <= 2LL * num_sms && tiles >= 2 * (s + 1)) ++s;
   // ring depth: two CTAs per SM must fit in shared memory (a split also keeps
   // its partials there)
   const int per_cta = 233472 / 2 - 1024;
