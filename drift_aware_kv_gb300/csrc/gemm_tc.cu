@@ -57,6 +57,7 @@ struct Params {
   int np;
   int stages;
   int tmem_cols;
+  int ntn;  // persistent pair kernel: column tiles over all segments
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -904,6 +905,475 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- persistent pair tiles
+// For many row groups (block entries, large batches) the GEMM is bound by the
+// tensor cores, and what matters is keeping every SM's MMA pipe busy:
+//   * a thread-block cluster of two CTAs walks output tiles of 256 rows x bn
+//     columns (rows fastest, so concurrently running clusters share weight
+//     tiles in L2); CTA r of the pair owns rows [128 r, 128 r + 128) of the tile;
+//   * each CTA loads its own 128 x 64 A box and one half of the bn x 64 W box,
+//     multicast into both CTAs' stage (each weight tile is fetched once per
+//     pair); a stage is released when the MMAs of BOTH CTAs have read it, so
+//     every MMA commit arrives on the stage barrier of both CTAs;
+//   * two TMEM accumulators (2 x bn columns): the epilogue warps drain tile i
+//     while the MMA warp accumulates tile i + 1, so the tensor pipe never waits
+//     for the fp32 stores.
+// Warp roles as in the row-tiled kernel: 0 loads, 1 issues MMAs, 2-5 drain.
+constexpr int PC_MAX_STAGES = 8;
+__host__ __device__ constexpr int pc_stage_bytes(int bn) { return BM * BK * 2 + bn * BK * 2; }
+__host__ __device__ constexpr int pc_smem_bytes(int bn, int stages) { return stages * pc_stage_bytes(bn) + 2048; }
+
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+// Arrive on the same barrier of every CTA in `mask` once this thread's MMAs finish.
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_pc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  constexpr int A_BYTES = BM * BK * 2;
+  const int STAGES = p.stages, bn = p.bn;
+  const int SB = pc_stage_bytes(bn);
+  uint64_t* full = (uint64_t*)(smem + STAGES * SB);
+  uint64_t* empty = full + PC_MAX_STAGES;
+  uint64_t* acc_full = empty + PC_MAX_STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2]
+  uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_rank();  // 0 or 1 within the pair
+  const int cid = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
+  constexpr uint16_t PAIR = 3;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 2);  // the MMA warps of both CTAs
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(p.tmem_cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  // the peer multicasts into this CTA's stages and arrives on its barriers
+  cluster_sync();
+  pdl_launch_dependents();
+  pdl_wait();
+  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
+  const int mpairs = (M_eff + 2 * BM - 1) / (2 * BM);
+  const long long ntiles = (long long)mpairs * p.ntn;
+  const int nk = p.ktiles;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: own A box, half the W box to both CTAs
+    if (lane == 0) {
+      long long it = 0;
+      bool live = true;
+      for (long long t = cid; t < ntiles && live; t += ncl) {
+        const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
+        const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
+        const int n0 = (nb - p.seg_start[sg]) * bn;
+        const CUtensorMap* tmB = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
+        const int m0 = mp * 2 * BM + rank * BM;
+        for (int k = 0; k < nk; ++k, ++it) {
+          const int s = (int)(it % STAGES);
+          if (it >= STAGES && !mbar_wait(smem_u32(&empty[s]), (uint32_t)((it / STAGES) - 1) & 1u, p.err, 1, abort_flag)) {
+            live = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_expect_tx(fb, SB);
+          const uint32_t st = smem_u32(smem + (size_t)s * SB);
+          tma_load_2d(st, &tmA, k * BK, m0, fb);
+          tma_load_2d_mc(st + A_BYTES + rank * (bn / 2) * 128, tmB, k * BK, n0 + rank * (bn / 2), fb, PAIR);
+        }
+      }
+      // the last uses of every stage: both CTAs' MMAs must have read them, so no
+      // commit of the peer reaches this CTA after it exits
+      if (live)
+        for (long long u = (it > STAGES ? it - STAGES : 0); u < it; ++u)
+          if (!mbar_wait(smem_u32(&empty[u % STAGES]), (uint32_t)(u / STAGES) & 1u, p.err, 4, abort_flag)) break;
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: tile i into accumulator i % 2
+    if (lane == 0) {
+      const uint32_t idesc = instr_desc_ws(bn);  // M = 128, N = bn
+      long long it = 0;
+      int tl = 0;
+      bool live = true;
+      for (long long t = cid; t < ntiles && live; t += ncl, ++tl) {
+        const int b = tl & 1;
+        if (tl >= 2 && !mbar_wait(smem_u32(&acc_empty[b]), (uint32_t)((tl >> 1) - 1) & 1u, p.err, 5, abort_flag))
+          break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d = tmem + (uint32_t)(b * bn);
+        for (int k = 0; k < nk; ++k, ++it) {
+          const int s = (int)(it % STAGES);
+          if (!mbar_wait(smem_u32(&full[s]), (uint32_t)(it / STAGES) & 1u, p.err, 2, abort_flag)) {
+            live = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t st = smem_u32(smem + (size_t)s * SB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_id(d, smem_desc(st + kk * 32), smem_desc(st + A_BYTES + kk * 32), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_mc(smem_u32(&empty[s]), PAIR);  // frees stage s in both CTAs once read
+        }
+        if (live) umma_commit(smem_u32(&acc_full[b]));
+      }
+    }
+  } else {
+    // ---------------- epilogue: TMEM lane quarter q = warp & 3
+    const int q = warp & 3;
+    const bool vec = ((p.ldc & 3) == 0);
+    int tl = 0;
+    for (long long t = cid; t < ntiles; t += ncl, ++tl) {
+      const int b = tl & 1;
+      const bool ok = mbar_wait(smem_u32(&acc_full[b]), (uint32_t)(tl >> 1) & 1u, p.err, 3, abort_flag);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!ok) break;
+      const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
+      const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
+      const int n0 = (nb - p.seg_start[sg]) * bn;
+      const int segN = p.seg_N[sg];
+      float* const Cseg = p.seg_C[sg];
+      const bool vseg = vec && ((((uintptr_t)Cseg) & 15) == 0);
+      const int row = mp * 2 * BM + rank * BM + q * 32 + lane;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * bn);
+#pragma unroll 1
+      for (int c = 0; c < bn; c += 16) {
+        float v[16];
+        tmem_ld16(tq + c, v);
+        if (row < M_eff) {
+          float* dst = Cseg + (size_t)row * p.ldc + n0 + c;
+          if (n0 + c + 16 <= segN && vseg) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (n0 + c + j < segN) dst[j] = v[j];
+          }
+        }
+      }
+      // accumulator drained: hand it back to the MMA warp
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
+    }
+  }
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // let in-flight bulk copies land before the CTA's shared memory is released
+    const long long t0 = clock64();
+    while (clock64() - t0 < 20000000LL) {
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  // neither CTA of the pair leaves while the other may still write into it
+  cluster_sync();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
+  }
+}
+
+// ---------------------------------------------------------------- two-SM pair tiles
+// The same walk over 256-row x bn-column output tiles, with the pair's tensor
+// cores working as one (tcgen05 cta_group::2, M = 256): CTA r of the pair stages
+// only ITS 128 A rows and ITS half of the W tile, the leader CTA (rank 0)
+// issues every MMA, which reads both CTAs' shared memory and writes each CTA's
+// 128 accumulator rows into that CTA's TMEM.  Half the W bytes per stage buy a
+// deeper ring (up to 7 stages of 32 KB at bn = 256) than staging the whole W
+// tile in both CTAs.  Both CTAs' loads complete on the leader's stage barrier;
+// the leader's MMA commits release the stage (and, per tile, the accumulator)
+// in both CTAs; both CTAs' epilogue warps hand the accumulator back to the
+// leader.  TMEM is allocated and freed by the pair together (cta_group::2).
+constexpr int P2_MAX_STAGES = 8;
+__host__ __device__ constexpr int p2_stage_bytes(int bn) { return BM * BK * 2 + (bn / 2) * BK * 2; }
+__host__ __device__ constexpr int p2_smem_bytes(int bn, int stages) { return stages * p2_stage_bytes(bn) + 2048; }
+
+__host__ __device__ constexpr uint32_t instr_desc_m256(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+// tiled 2D load whose completion is counted on `bar`, an mbarrier of this CTA
+// or of its pair peer (shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void umma_pair(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (arrivals from the pair peer);
+// sleep_ns > 0 backs off between polls (waits that are long by design, so the
+// polling warp leaves the issue slots of its scheduler to the MMA warp).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* err, int code,
+                                                  volatile int* abort_flag, unsigned sleep_ns = 0) {
+  const long long t0 = clock64();
+  while (!mbar_try_cluster(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > TIMEOUT_CYCLES) {
+      atomicExch(err, code);
+      *abort_flag = 1;
+      return false;
+    }
+    if (sleep_ns) __nanosleep(sleep_ns);
+  }
+  return true;
+}
+
+constexpr int P2_THREADS = 224;  // + warp 6: second loader (W halves)
+__global__ void __launch_bounds__(P2_THREADS, 1)
+    gemm_p2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  constexpr int A_BYTES = BM * BK * 2;
+  const int STAGES = p.stages, bn = p.bn;
+  const int SB = p2_stage_bytes(bn);
+  uint64_t* full = (uint64_t*)(smem + STAGES * SB);  // used in the leader
+  uint64_t* empty = full + P2_MAX_STAGES;
+  uint64_t* acc_full = empty + P2_MAX_STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2], used in the leader
+  uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_rank();  // 0 (leader) or 1
+  const int cid = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
+  constexpr uint16_t PAIR = 3;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);   // the leader's expect-tx arrival; bytes of both CTAs
+      mbar_init(smem_u32(&empty[s]), 1);  // the leader's MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 8);  // four epilogue warps of each CTA
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    // the pair allocates together: one warp of each CTA, same column range
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(p.tmem_cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  cluster_sync();
+  // the pair's allocation must have given both CTAs the same columns (the MMA
+  // writes the same TMEM address in both); otherwise report and do nothing
+  if (threadIdx.x == 0) {
+    uint32_t peer;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                 : "=r"(peer)
+                 : "r"(map_to_rank(smem_u32(tmem_slot), (uint32_t)(rank ^ 1)))
+                 : "memory");
+    if (peer != tmem) {
+      atomicExch(p.err, 6);
+      *abort_flag = 1;
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
+  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
+  const int mpairs = (M_eff + 2 * BM - 1) / (2 * BM);
+  const long long ntiles = *abort_flag ? 0 : (long long)mpairs * p.ntn;
+  const int nk = p.ktiles;
+
+  if (warp == 0 || warp == 6) {
+    // ---------------- TMA producers (two issuing threads, each its own stream
+    // of requests): warp 0 the own A rows, warp 6 the own half of the W tile;
+    // both complete on the leader's stage barrier
+    if (lane == 0) {
+      const bool loads_a = warp == 0;
+      long long it = 0;
+      bool live = true;
+      for (long long t = cid; t < ntiles && live; t += ncl) {
+        const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
+        const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
+        const int n0 = (nb - p.seg_start[sg]) * bn;
+        const CUtensorMap* tmB = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
+        const int m0 = mp * 2 * BM + rank * BM;
+        for (int k = 0; k < nk; ++k, ++it) {
+          const int s = (int)(it % STAGES);
+          if (it >= STAGES && !mbar_wait_cluster(smem_u32(&empty[s]), (uint32_t)((it / STAGES) - 1) & 1u, p.err, 1,
+                                                 abort_flag)) {
+            live = false;
+            break;
+          }
+          const uint32_t fb_local = smem_u32(&full[s]);
+          if (rank == 0 && loads_a) mbar_expect_tx(fb_local, 2 * SB);
+          const uint32_t fb = map_to_rank(fb_local, 0);
+          const uint32_t st = smem_u32(smem + (size_t)s * SB);
+          if (loads_a)
+            tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
+          else
+            tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
+        }
+      }
+      // the last uses of every stage must be read before this CTA may exit
+      if (live)
+        for (long long u = (it > STAGES ? it - STAGES : 0); u < it; ++u)
+          if (!mbar_wait_cluster(smem_u32(&empty[u % STAGES]), (uint32_t)(u / STAGES) & 1u, p.err, 4, abort_flag))
+            break;
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader only): tile i into accumulator i % 2
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = instr_desc_m256(bn);
+      long long it = 0;
+      int tl = 0;
+      bool live = true;
+      for (long long t = cid; t < ntiles && live; t += ncl, ++tl) {
+        const int b = tl & 1;
+        if (tl >= 2 &&
+            !mbar_wait_cluster(smem_u32(&acc_empty[b]), (uint32_t)((tl >> 1) - 1) & 1u, p.err, 5, abort_flag))
+          break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d = tmem + (uint32_t)(b * bn);
+        for (int k = 0; k < nk; ++k, ++it) {
+          const int s = (int)(it % STAGES);
+          if (!mbar_wait_cluster(smem_u32(&full[s]), (uint32_t)(it / STAGES) & 1u, p.err, 2, abort_flag)) {
+            live = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t st = smem_u32(smem + (size_t)s * SB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_pair(d, smem_desc(st + kk * 32), smem_desc(st + A_BYTES + kk * 32), idesc,
+                      (k > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_pair(smem_u32(&empty[s]), PAIR);  // stage s free in both CTAs once read
+        }
+        if (live) umma_commit_pair(smem_u32(&acc_full[b]), PAIR);
+      }
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---------------- epilogue: TMEM lane quarter q = warp & 3 of this CTA's rows
+    const int q = warp & 3;
+    const bool vec = ((p.ldc & 3) == 0);
+    const uint32_t lead_acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
+    int tl = 0;
+    for (long long t = cid; t < ntiles; t += ncl, ++tl) {
+      const int b = tl & 1;
+      const bool ok =
+          mbar_wait_cluster(smem_u32(&acc_full[b]), (uint32_t)(tl >> 1) & 1u, p.err, 3, abort_flag, 256);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!ok) break;
+      const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
+      const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
+      const int n0 = (nb - p.seg_start[sg]) * bn;
+      const int segN = p.seg_N[sg];
+      float* const Cseg = p.seg_C[sg];
+      const bool vseg = vec && ((((uintptr_t)Cseg) & 15) == 0);
+      const int row = mp * 2 * BM + rank * BM + q * 32 + lane;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * bn);
+#pragma unroll 1
+      for (int c = 0; c < bn; c += 16) {
+        float v[16];
+        tmem_ld16(tq + c, v);
+        if (row < M_eff) {
+          float* dst = Cseg + (size_t)row * p.ldc + n0 + c;
+          if (n0 + c + 16 <= segN && vseg) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (n0 + c + j < segN) dst[j] = v[j];
+          }
+        }
+      }
+      // accumulator drained in this CTA: tell the leader's MMA warp
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lead_acc_empty0 + (uint32_t)(b * 8));
+    }
+  }
+  if (*abort_flag && (warp == 0 || warp == 6) && lane == 0) {
+    // let in-flight bulk copies land before the CTA's shared memory is released
+    const long long t0 = clock64();
+    while (clock64() - t0 < 20000000LL) {
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  // neither CTA of the pair leaves (or frees TMEM) while the other still works
+  cluster_sync();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
+  }
+}
+
 // Packed tile layout of a weight matrix W[N, K] (bf16, row stride ldw): for
 // every 128-row tile and 64-column k-tile, 16 KB holding the 128 x 64 block
 // exactly as a 128-byte-swizzled TMA load would place it in shared memory
@@ -1071,7 +1541,7 @@ int max_active_clusters(int smem, int cluster) {
 // projection shapes of the layer loop against forced sweeps of every
 // configuration: the pick is the fastest or within a few percent of it.)
 struct GemmPick {
-  int kernel;  // 1 row-tiled, 2 weight-stationary
+  int kernel;  // 1 row-tiled, 2 weight-stationary, 5 two-SM pair tiles
   int bn, splits, stages;
 };
 
@@ -1134,38 +1604,50 @@ GemmPick pick_small_m(int MT, int M, const int* N, int nseg, int ktiles, int nsm
   return best;
 }
 
-// More than 256 rows (several 256-row groups): the row-tiled kernel at the
-// column width and K split whose waves of (tiles x row groups x splits) CTAs,
-// one per SM, take the least time, a CTA costing the larger of its streamed
-// bytes (as in pick_small_m) and its MMA work at one SM's share of the bf16
-// tensor peak, plus 0.4 us per split.
+int p2_max_stages(int bn);
+int p2_clusters(int bn, int stages, long long pair_tiles, int nsm);
+
+// More than 256 rows (several 256-row groups): the GEMM is bound by how fast
+// the SMs' pipelines are fed, which measurements on GB300 put per k-step (64
+// K-elements) at about 0.415 us for a two-SM pair tile (256 x 256) and
+// 0.43 + 0.0022 (bn - 64) us for a row-tiled CTA (256 x bn), whatever the
+// operands' bytes.  Candidates: the two-SM pair kernel (persistent, 256 x bn
+// tiles, bn 256/224/192) at waves of its resident clusters x (k-steps x 0.415
+// + 2 us), and the row-tiled kernel at every column width, waves of one CTA
+// per SM x (k-steps x its step cost + 3 us), with a cluster K split of 2 or 4
+// costing another 12 us per wave for the reduction of the 256-row partials.
 GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm) {
   const int MT = 2, mgroups = (M + 2 * BM - 1) / (2 * BM);
   GemmPick best{1, 256, 1, rt_max_stages(MT, 256)};
   double tbest = 1e30;
+  for (int bn = 256; bn >= 192; bn -= 32) {
+    const int st = p2_max_stages(bn);
+    const long long tiles = (long long)mgroups * rt_tiles(N, nseg, bn);
+    const int ncl = p2_clusters(bn, st, tiles, nsm);
+    const long long waves = (tiles + ncl - 1) / ncl;
+    const double t = waves * (ktiles * 0.415 + 2.0);
+    if (t < tbest * 0.999) {
+      tbest = t;
+      best = GemmPick{5, bn, 1, st};
+    }
+  }
   for (int s = 1; s <= 4; s *= 2) {
     if (s > 1 && ktiles < 8 * s) break;
-    for (int bn = 32; bn <= 256; bn += 16) {
+    for (int bn = 64; bn <= 256; bn += 16) {
       if (rt_max_stages(MT, bn) < 3) continue;
       if (s > 1 && rt_max_stages(MT, bn) * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4) continue;
       const long long ctas = (long long)rt_tiles(N, nseg, bn) * mgroups * s;
       long long waves = (ctas + nsm - 1) / nsm;
       if (s > 1) {
-        // waves of resident clusters; a wave that needs nearly every cluster
-        // slot counts as two (see pick_small_m)
         int tmem = 32;
         while (tmem < MT * bn) tmem *= 2;
         const int smem = std::max(rt_smem_bytes(MT, bn, rt_max_stages(MT, bn)), 233472 / (512 / tmem + 1) - 1024 + 16);
         const int mc = max_active_clusters(smem, s);
         if (mc <= 0) continue;
-        const long long clusters = ctas / s;
-        waves = (clusters + mc - 1) / mc;
-        if (waves == 1 && clusters > 0.9 * mc) waves = 2;
+        waves = (ctas / s + mc - 1) / mc;
       }
-      const double kel = (double)ktiles * BK / s;
-      const double t_mem = (bn + 0.5 * MT * BM) * kel * 2.0 / 50e3;
-      const double t_mma = 2.0 * MT * BM * bn * kel / 13.0e6;
-      const double t = waves * std::max(t_mem, t_mma) + 0.4 * s;
+      const double step = 0.43 + 0.0022 * (bn - 64);
+      const double t = waves * ((double)ktiles / s * step + 3.0 + (s > 1 ? 12.0 : 0.0));
       if (t < tbest * 0.999) {
         tbest = t;
         best = GemmPick{1, bn, s, rt_max_stages(MT, bn)};
@@ -1175,6 +1657,100 @@ GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm) {
   return best;
 }
 
+
+// Dynamic shared memory of a persistent pair CTA: at least half an SM's, so
+// no two CTAs (each holding all 512 TMEM columns) ever share an SM - a second
+// one would block in its allocation while its pair partner waits for it.
+int pc_launch_smem(int bn, int stages) { return std::max(pc_smem_bytes(bn, stages), 233472 / 2 - 1024 + 16); }
+int p2_launch_smem(int bn, int stages) { return std::max(p2_smem_bytes(bn, stages), 233472 / 2 - 1024 + 16); }
+int p2_max_stages(int bn) { return std::min(P2_MAX_STAGES, (232448 - 2048) / p2_stage_bytes(bn)); }
+
+// Two-SM pair kernel: clusters of two CTAs, one CTA per SM.
+int p2_clusters(int bn, int stages, long long pair_tiles, int nsm) {
+  int mc = max_active_clusters(p2_launch_smem(bn, stages), 2);
+  if (mc <= 0) mc = nsm / 2;
+  return (int)std::max<long long>(1, std::min<long long>(mc, pair_tiles));
+}
+
+cudaError_t launch_p2(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, int nclusters,
+                      cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_p2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * nclusters, 1, 1);
+  cfg.blockDim = dim3(P2_THREADS);
+  cfg.dynamicSmemBytes = p2_launch_smem(p.bn, p.stages);
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_p2_kernel, *a, *b[0], *b[1], *b[2], p);
+}
+
+// Persistent pair kernel: clusters of two CTAs, one CTA per SM, as many
+// clusters as fit at once (at most one per pair of tiles).
+int pc_clusters(int bn, int stages, long long pair_tiles, int nsm) {
+  int mc = max_active_clusters(pc_launch_smem(bn, stages), 2);
+  if (mc <= 0) mc = nsm / 2;
+  return (int)std::max<long long>(1, std::min<long long>(mc, pair_tiles));
+}
+
+// Column width of the persistent pair kernel: the least work per cluster over
+// its waves of tiles (bn + 32 per tile: the A box streamed alongside every
+// tile), ties to the wider tile.
+GemmPick pick_pc(int M, const int* N, int nseg, int nsm) {
+  const int mpairs = (M + 2 * BM - 1) / (2 * BM);
+  GemmPick best{4, 256, 1, 4};
+  double cbest = 1e30;
+  for (int bn = 256; bn >= 64; bn -= 16) {
+    const int stages = std::min(PC_MAX_STAGES, (232448 - 2048) / pc_stage_bytes(bn));
+    if (stages < 3) continue;
+    const long long tiles = (long long)mpairs * rt_tiles(N, nseg, bn);
+    const int ncl = pc_clusters(bn, stages, tiles, nsm);
+    const long long waves = (tiles + ncl - 1) / ncl;
+    const double c = (double)waves * (bn + 32);
+    if (c < cbest * 0.999) {
+      cbest = c;
+      best = GemmPick{4, bn, 1, stages};
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_pc(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, int nclusters,
+                      cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_pc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * nclusters, 1, 1);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = pc_launch_smem(p.bn, p.stages);
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_pc_kernel, *a, *b[0], *b[1], *b[2], p);
+}
 
 cudaError_t launch_ws(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid,
                       cudaStream_t st) {
@@ -1286,9 +1862,10 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
       auto_stages = pk.stages;
     } else {
       const GemmPick pk = pick_large_m(M, N, nseg, ktiles, nsm);
-      kind = 1;
+      kind = pk.kernel;
       bn = pk.bn;
       auto_splits = pk.splits;
+      if (kind == 5) auto_stages = pk.stages;
     }
   } else if (kind == 1 && force->bn) {
     bn = force->bn;
@@ -1311,6 +1888,36 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   }
   p.seg_start[3] = 0x3FFFFFFF;
   for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
+  if (kind == 4 || kind == 5) {
+    // persistent pair tiles: each CTA's W box is half a tile (multicast to
+    // both CTAs for kernel 4, read by the pair's MMA for kernel 5)
+    const bool two_sm = kind == 5;
+    const GemmPick pk = pick_pc(M, N, nseg, nsm);
+    p.bn = force && force->bn ? force->bn : (auto_stages ? bn : (two_sm ? 256 : pk.bn));
+    if (p.bn < 16 || p.bn > 256 || (p.bn & 15)) return cudaErrorInvalidValue;
+    const int max_stages =
+        two_sm ? p2_max_stages(p.bn) : std::min(PC_MAX_STAGES, (232448 - 2048) / pc_stage_bytes(p.bn));
+    p.stages = force && force->stages ? force->stages : (auto_stages ? auto_stages : max_stages);
+    if (p.stages < 2 || p.stages > max_stages) return cudaErrorInvalidValue;
+    p.splits = 1;
+    p.tmem_cols = 32;
+    while (p.tmem_cols < 2 * p.bn) p.tmem_cols *= 2;
+    p.ntn = rt_tiles(N, nseg, p.bn);
+    for (int sgi = 0, t = 0; sgi < 3; ++sgi) {
+      p.seg_start[sgi] = sgi < nseg ? t : 0x3FFFFFFF;
+      if (sgi < nseg) {
+        mb[sgi] = get_map(cache, W[sgi], N[sgi], K, ldw[sgi], p.bn / 2);
+        if (!mb[sgi]) return cudaErrorInvalidValue;
+        t += (N[sgi] + p.bn - 1) / p.bn;
+      }
+    }
+    for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
+    const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * p.ntn;
+    const int ncl = two_sm ? p2_clusters(p.bn, p.stages, pair_tiles, nsm) : pc_clusters(p.bn, p.stages, pair_tiles, nsm);
+    const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
+    if (!ma) return cudaErrorInvalidValue;
+    return two_sm ? launch_p2(ma, mb, p, ncl, st) : launch_pc(ma, mb, p, ncl, st);
+  }
   if (kind == 3) {
     // persistent stream-K: stages = ring depth, splits = grid size override
     if (M > 2 * BM) return cudaErrorInvalidValue;
@@ -1401,10 +2008,16 @@ cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void*
 cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, int K, int* out) {
   using namespace tc;
   if (M <= 0 || nseg < 1 || nseg > 3 || K < 1 || !out) return cudaErrorInvalidValue;
-  if (cache->num_sms == 0) {
+  if (cache->num_sms <= 0) {
     int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&cache->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    cache->num_sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&cache->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cache->num_sms <= 0) {
+      cache->num_sms = 0;
+      cudaGetLastError();
+      return cudaErrorNoDevice;
+    }
   }
   const int MT = M > BM ? 2 : 1;
   const int mgroups = (M + MT * BM - 1) / (MT * BM);

@@ -43,7 +43,9 @@ struct TcGemmCache {
 // automatically.  kernel: 1 row-tiled (rows on the MMA's M side, up to two
 // 128-row sub-tiles per CTA), 2 weight-stationary (W rows on the M side, at most
 // 256 activation rows on the N side, one tile per CTA), 3 persistent stream-K
-// weight-stationary (one CTA per SM, equal shares of the weight stream).
+// weight-stationary (one CTA per SM, equal shares of the weight stream), 4 / 5
+// persistent pair tiles (two-CTA clusters over 256-row x bn tiles; 4 multicasts
+// each W tile into both CTAs, 5 runs the pair's MMA as one, cta_group::2).
 // stages: ring depth; splits: K split over a thread-block cluster (1..8), or
 // for kernel 3 the number of CTAs; bn: columns per tile of kernel 1 (a
 // multiple of 16, at most 256).
@@ -83,7 +85,8 @@ cudaError_t tc_pack_weights(const void* W, int ldw, int N, int K, void* out, cud
 
 // The launch the library picks for M rows, nseg weight segments of N[i]
 // output columns and inner size K: out = {kernel (1 row-tiled, 2
-// weight-stationary), columns per tile, K split, ring depth}.
+// weight-stationary, 5 two-SM pair tiles), columns per tile, K split, ring
+// depth}.
 cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, int K, int* out);
 
 // Allocates the stream-K workspace and counters (once per cache).

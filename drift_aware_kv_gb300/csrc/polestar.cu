@@ -1230,10 +1230,10 @@ extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const
   if (!A || !W || !C || M < 0 || N < 1 || K < 1) return POLESTAR_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   const int kind = path & 0xFF;
-  if (kind >= 1 && kind <= 5) {
+  if (kind >= 1 && kind <= 7) {
     if (dtype != POLESTAR_BF16 || !tc_gemm_supported(K, lda, kind == 5 ? K : ldw)) return POLESTAR_ERR_UNSUPPORTED;
     TcGemmChoice force;
-    force.kernel = kind == 5 ? 3 : kind - 1;
+    force.kernel = kind == 5 ? 3 : (kind >= 6 ? kind - 2 : kind - 1);
     force.stages = (path >> 8) & 0xFF;
     force.splits = (path >> 16) & 0xFF;
     force.bn = ((path >> 24) & 0xFF) * 16;

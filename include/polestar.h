@@ -196,10 +196,14 @@ polestar_status polestar_profile_end(polestar_ctx *ctx, polestar_kernel_stats *o
  * weight-stationary (M <= 256) tcgen05 kernel, with bits 8-15 of `path`
  * giving the ring depth and bits 16-23 the K split over a cluster (paths 2
  * and 3) or the number of CTAs (paths 4, 5), and bits 24-31 the columns per
- * tile of path 2 in units of 16; 0 = automatic.  Path 5 is path 4
+ * tile of paths 2 and 6 in units of 16; 0 = automatic.  Path 5 is path 4
  * with W given in the packed tile layout of polestar_pack_weights (ldw is
- * then ignored).  A combination the kernel cannot run (too much shared
- * memory, more than 8 splits, more CTAs than SMs) returns UNSUPPORTED.
+ * then ignored).  Paths 6 and 7: persistent pair-tile kernels (clusters of
+ * two CTAs walk 256-row x bn-column output tiles; any M): 6 multicasts each
+ * weight tile into both CTAs, 7 runs the pair's tensor cores as one MMA
+ * (cta_group::2) on each CTA's half; bits 8-15 the ring depth.  A combination the kernel cannot
+ * run (too much shared memory, more than 8 splits, more CTAs than SMs)
+ * returns UNSUPPORTED.
  * m_dev (device int, may be NULL) lowers the row count on the device: rows at
  * or beyond min(M, *m_dev) are left untouched.  Asynchronous; returns
  * UNSUPPORTED for a path/dtype/stride combination the kernels do not cover. */
@@ -210,9 +214,11 @@ polestar_status polestar_debug_gemm(const void *A, int32_t lda, const void *W, i
 /* ---- the projection launch the library picks (test hook) ----
  * For M rows (bf16 tensor-core path), nseg (1..3) weight segments with N[i]
  * (host array) output columns and inner size K: out[4] (host) = {kernel: 1
- * row-tiled, 2 weight-stationary; output columns per tile; K split over a
- * cluster; ring depth}.  Queries the current device's occupancy; launches
- * nothing. */
+ * row-tiled, 2 weight-stationary, 5 two-SM pair tiles (path 7 of
+ * polestar_debug_gemm); output columns per tile; K split over a cluster; ring
+ * depth}.  Queries the current device's
+ * occupancy; launches nothing.  CUDA error (no device) when no device is
+ * visible. */
 polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, const int32_t *N, int32_t K, int32_t *out);
 
 /* ---- packed tile layout of a projection matrix ----

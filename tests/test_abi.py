@@ -55,3 +55,14 @@ def test_packed_weight_size_is_whole_tiles():
     assert lib.polestar_packed_weight_bytes(128, 64) == 16384
     assert lib.polestar_packed_weight_bytes(4096, 12288) == 32 * 192 * 16384
     assert lib.polestar_packed_weight_bytes(0, 64) == -1
+
+
+def test_gemm_choice_without_a_device_is_an_error_not_a_crash():
+    """The launch choice needs the device's SM count; with no device the call
+    returns an error status instead of dividing by zero."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    from drift_aware_kv_gb300 import polestar as P
+    with pytest.raises(P.PolestarError):
+        P.gemm_choice(2560, [12288], 4096)

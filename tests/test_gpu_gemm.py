@@ -29,8 +29,9 @@ def _ref(A, W, rows):
 
 
 # path: 0 CUDA cores, 1 tcgen05 (library's choice), 2 row-tiled, 3 weight-stationary,
-# 4 persistent stream-K weight-stationary
-@pytest.mark.parametrize("path", [1, 0, 2, 3, 4])
+# 4 persistent stream-K weight-stationary, 6 persistent pair tiles (multicast W),
+# 7 persistent pair tiles on the pair's joint MMA
+@pytest.mark.parametrize("path", [1, 0, 2, 3, 4, 6, 7])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_matches_definition(path, M, N, K):
     if path in (3, 4) and M > 256:
@@ -138,6 +139,24 @@ def test_weight_stationary_configs(stages, splits, M, N, K):
     _check_gemm(P.gemm_path(3, stages, splits), M, N, K)
 
 
+# column widths and ring depths of the persistent pair kernel, forced: tiles cut
+# at ragged rows, columns and K, one pair tile and many waves of them
+@pytest.mark.parametrize("bn,stages", [(256, 0), (192, 2), (240, 3), (128, 0), (32, 8), (64, 5)])
+@pytest.mark.parametrize("M,N,K", [(700, 1000, 1376), (2560, 4096, 4096), (300, 4608, 2048), (1, 96, 64),
+                                   (513, 12288, 4096)])
+def test_pair_tile_configs(bn, stages, M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    _check_gemm(P.gemm_path(6, stages, 0, bn), M, N, K)
+
+
+@pytest.mark.parametrize("bn,stages", [(256, 0), (256, 7), (192, 2), (240, 3), (128, 0), (32, 8), (16, 4)])
+@pytest.mark.parametrize("M,N,K", [(700, 1000, 1376), (2560, 4096, 4096), (300, 4608, 2048), (1, 96, 64),
+                                   (513, 12288, 4096)])
+def test_two_sm_pair_configs(bn, stages, M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    _check_gemm(P.gemm_path(7, stages, 0, bn), M, N, K)
+
+
 def _check_gemm(path, M, N, K):
     from drift_aware_kv_gb300 import polestar as P
     g = torch.Generator(device="cpu").manual_seed(M * 7919 + N * 31 + K)
@@ -157,7 +176,8 @@ def _check_gemm(path, M, N, K):
 
 
 @pytest.mark.parametrize("path,m_live", [(1, 77), (2, 77), (3, 77), (3, 0), (3, 1), ((2 << 16) | 3, 17),
-                                         ((4 << 16) | 3, 200), (4, 77), (4, 0), ((9 << 16) | 4, 33)])
+                                         ((4 << 16) | 3, 200), (4, 77), (4, 0), ((9 << 16) | 4, 33),
+                                         (6, 77), (6, 0), (6, 129), (6, 200), (7, 77), (7, 0), (7, 129)])
 def test_gemm_device_row_count_leaves_tail_untouched(path, m_live):
     from drift_aware_kv_gb300 import polestar as P
     g = torch.Generator(device="cpu").manual_seed(5)
@@ -190,16 +210,21 @@ def test_gemm_rejects_unrunnable_choice():
         P.debug_gemm(A[:64], W, C[:64], P.gemm_path(4, 13))  # ring deeper than the kernel's barriers
     with pytest.raises(P.PolestarError):
         P.debug_gemm(A[:64], W, C[:64], P.gemm_path(4, 0, 255))  # more CTAs than SMs
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A, W, C, P.gemm_path(6, 5, 0, 256))  # five 48 KB stages do not fit
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A, W, C, P.gemm_path(7, 8, 0, 256))  # eight 32 KB stages do not fit
 
 
 @pytest.mark.parametrize("M,Ns,K", [(136, [4096, 1024, 1024], 4096), (32, [12288, 12288], 4096), (128, [4096], 12288),
-                                    (80, [3584], 3584), (200, [512, 512], 1184)])
+                                    (80, [3584], 3584), (200, [512, 512], 1184), (2560, [12288], 4096),
+                                    (768, [4096, 1024, 1024], 4096)])
 def test_library_choice_is_valid_and_reproducible(M, Ns, K):
     """The launch the library picks is a runnable configuration, and forcing
     exactly that configuration reproduces the automatic launch bit for bit."""
     from drift_aware_kv_gb300 import polestar as P
     ch = P.gemm_choice(M, Ns, K)
-    assert ch["kernel"] in (1, 2) and ch["splits"] >= 1 and ch["stages"] >= 2
+    assert ch["kernel"] in (1, 2, 5) and ch["splits"] >= 1 and ch["stages"] >= 2
     assert ch["bn"] % 16 == 0 and 16 <= ch["bn"] <= 256
     N = Ns[0]
     g = torch.Generator(device="cpu").manual_seed(M + K)
@@ -209,7 +234,8 @@ def test_library_choice_is_valid_and_reproducible(M, Ns, K):
     c2 = torch.empty(M, N, device="cuda")
     P.debug_gemm(A, W, c1, P.gemm_path(1))
     ch1 = P.gemm_choice(M, [N], K)
-    path = P.gemm_path(1 + ch1["kernel"], ch1["stages"], ch1["splits"], ch1["bn"] if ch1["kernel"] == 1 else 0)
+    kern = {1: 2, 2: 3, 5: 7}[ch1["kernel"]]
+    path = P.gemm_path(kern, ch1["stages"], ch1["splits"], ch1["bn"] if ch1["kernel"] in (1, 5) else 0)
     P.debug_gemm(A, W, c2, path)
     torch.cuda.synchronize()
     assert torch.equal(c1, c2)
