@@ -57,7 +57,8 @@ struct Params {
   int np;
   int stages;
   int tmem_cols;
-  int ntn;  // persistent pair kernel: column tiles over all segments
+  int ntn;    // persistent pair kernels: column tiles over all segments
+  int nload;  // two-SM pair kernel: loader warps (1, 2 or 4; divides stages)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -1182,7 +1183,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   return true;
 }
 
-constexpr int P2_THREADS = 224;  // + warp 6: second loader (W halves)
+// Loaders: one issuing warp keeps about one TMA box in flight (measured on
+// GB300: a warp completes one box per ~860 cycles from L2, whatever its size
+// and the ring depth), so up to four warps (p.nload) issue the k-steps.  Stage
+// s is always refilled by loader s % nload (the ring depth is a multiple of
+// nload), so each stage's uses are issued in order by one warp and its parity
+// waits never run more than one phase ahead of the barrier.
+constexpr int P2_LOADERS = 4;
+constexpr int P2_THREADS = (6 + P2_LOADERS - 1) * 32;  // warps 0 and 6.. load, 1 MMA, 2-5 drain
 __global__ void __launch_bounds__(P2_THREADS, 1)
     gemm_p2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
@@ -1248,12 +1256,12 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
   const long long ntiles = *abort_flag ? 0 : (long long)mpairs * p.ntn;
   const int nk = p.ktiles;
 
-  if (warp == 0 || warp == 6) {
-    // ---------------- TMA producers (two issuing threads, each its own stream
-    // of requests): warp 0 the own A rows, warp 6 the own half of the W tile;
-    // both complete on the leader's stage barrier
-    if (lane == 0) {
-      const bool loads_a = warp == 0;
+  if (warp == 0 || warp >= 6) {
+    // ---------------- TMA producers: loader j (warp 0, 6, 7, ...) issues the
+    // k-steps it with it % P2_LOADERS == j - own A rows and own half of the W
+    // tile - completing on the leader's stage barrier
+    const int lj = warp == 0 ? 0 : warp - 5;
+    if (lane == 0 && lj < p.nload) {
       long long it = 0;
       bool live = true;
       for (long long t = cid; t < ntiles && live; t += ncl) {
@@ -1264,25 +1272,25 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         const int m0 = mp * 2 * BM + rank * BM;
         for (int k = 0; k < nk; ++k, ++it) {
           const int s = (int)(it % STAGES);
+          if (s % p.nload != lj) continue;
           if (it >= STAGES && !mbar_wait_cluster(smem_u32(&empty[s]), (uint32_t)((it / STAGES) - 1) & 1u, p.err, 1,
                                                  abort_flag)) {
             live = false;
             break;
           }
           const uint32_t fb_local = smem_u32(&full[s]);
-          if (rank == 0 && loads_a) mbar_expect_tx(fb_local, 2 * SB);
+          if (rank == 0) mbar_expect_tx(fb_local, 2 * SB);
           const uint32_t fb = map_to_rank(fb_local, 0);
           const uint32_t st = smem_u32(smem + (size_t)s * SB);
-          if (loads_a)
-            tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
-          else
-            tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
+          tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
+          tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
         }
       }
-      // the last uses of every stage must be read before this CTA may exit
+      // the last uses of this loader's stages must be read before this CTA may exit
       if (live)
         for (long long u = (it > STAGES ? it - STAGES : 0); u < it; ++u)
-          if (!mbar_wait_cluster(smem_u32(&empty[u % STAGES]), (uint32_t)(u / STAGES) & 1u, p.err, 4, abort_flag))
+          if ((int)(u % STAGES) % p.nload == lj &&
+              !mbar_wait_cluster(smem_u32(&empty[u % STAGES]), (uint32_t)(u / STAGES) & 1u, p.err, 4, abort_flag))
             break;
     }
   } else if (warp == 1) {
@@ -1358,7 +1366,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(lead_acc_empty0 + (uint32_t)(b * 8));
     }
   }
-  if (*abort_flag && (warp == 0 || warp == 6) && lane == 0) {
+  if (*abort_flag && (warp == 0 || warp >= 6) && lane == 0) {
     // let in-flight bulk copies land before the CTA's shared memory is released
     const long long t0 = clock64();
     while (clock64() - t0 < 20000000LL) {
@@ -1604,7 +1612,7 @@ GemmPick pick_small_m(int MT, int M, const int* N, int nseg, int ktiles, int nsm
   return best;
 }
 
-int p2_max_stages(int bn);
+int p2_default_stages(int bn);
 int p2_clusters(int bn, int stages, long long pair_tiles, int nsm);
 
 // More than 256 rows (several 256-row groups): the GEMM is bound by how fast
@@ -1621,7 +1629,7 @@ GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm) {
   GemmPick best{1, 256, 1, rt_max_stages(MT, 256)};
   double tbest = 1e30;
   for (int bn = 256; bn >= 192; bn -= 32) {
-    const int st = p2_max_stages(bn);
+    const int st = p2_default_stages(bn);
     const long long tiles = (long long)mgroups * rt_tiles(N, nseg, bn);
     const int ncl = p2_clusters(bn, st, tiles, nsm);
     const long long waves = (tiles + ncl - 1) / ncl;
@@ -1664,6 +1672,9 @@ GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm) {
 int pc_launch_smem(int bn, int stages) { return std::max(pc_smem_bytes(bn, stages), 233472 / 2 - 1024 + 16); }
 int p2_launch_smem(int bn, int stages) { return std::max(p2_smem_bytes(bn, stages), 233472 / 2 - 1024 + 16); }
 int p2_max_stages(int bn) { return std::min(P2_MAX_STAGES, (232448 - 2048) / p2_stage_bytes(bn)); }
+// default ring depth: the deepest that fits (measured: depth, not loader
+// count, decides; 7 stages at bn = 256 beat 4 stages with four loaders)
+int p2_default_stages(int bn) { return p2_max_stages(bn); }
 
 // Two-SM pair kernel: clusters of two CTAs, one CTA per SM.
 int p2_clusters(int bn, int stages, long long pair_tiles, int nsm) {
@@ -1897,9 +1908,11 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     if (p.bn < 16 || p.bn > 256 || (p.bn & 15)) return cudaErrorInvalidValue;
     const int max_stages =
         two_sm ? p2_max_stages(p.bn) : std::min(PC_MAX_STAGES, (232448 - 2048) / pc_stage_bytes(p.bn));
-    p.stages = force && force->stages ? force->stages : (auto_stages ? auto_stages : max_stages);
+    const int def_stages = two_sm ? p2_default_stages(p.bn) : max_stages;
+    p.stages = force && force->stages ? force->stages : (auto_stages ? auto_stages : def_stages);
     if (p.stages < 2 || p.stages > max_stages) return cudaErrorInvalidValue;
     p.splits = 1;
+    p.nload = p.stages % 4 == 0 ? 4 : (p.stages % 2 == 0 ? 2 : 1);
     p.tmem_cols = 32;
     while (p.tmem_cols < 2 * p.bn) p.tmem_cols *= 2;
     p.ntn = rt_tiles(N, nseg, p.bn);
