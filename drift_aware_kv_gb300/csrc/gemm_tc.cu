@@ -58,7 +58,7 @@ struct Params {
   int stages;
   int tmem_cols;
   int ntn;    // persistent pair kernels: column tiles over all segments
-  int nload;  // two-SM pair kernel: loader warps (1, 2 or 4; divides stages)
+  int nload;  // loader warps (1, 2 or 4; divides stages)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -243,11 +243,17 @@ __global__ void __launch_bounds__(THREADS)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
+  // Loaders: warp 0 and, while the mainloop runs, epilogue warps 2-4; loader j
+  // owns the stages s with s % nload == j (nload divides the ring depth), so
+  // every stage is refilled in order by one warp.  One issuing warp keeps
+  // about one TMA box in flight, so several loaders stream faster.
+  const int lj = warp == 0 ? 0 : ((warp >= 2 && warp <= 4) ? warp - 1 : -1);
+  const bool loader = lj >= 0 && lj < p.nload && lane == 0;
   // Weights never depend on earlier kernels: the first stages' W tiles are
   // requested before waiting for the predecessor that produces A (and m_dev).
   const int npre = nk < STAGES ? nk : STAGES;
-  if (warp == 0 && lane == 0) {
-    for (int i = 0; i < npre; ++i) {
+  if (loader) {
+    for (int i = lj; i < npre; i += p.nload) {
       const uint32_t fb = smem_u32(&full[i]);
       mbar_expect_tx(fb, STAGE_BYTES);
       tma_load_2d(smem_u32(smem + i * STAGE_BYTES) + MT * A_BYTES, tmB, (kt0 + i) * BK, n0, fb);
@@ -257,28 +263,28 @@ __global__ void __launch_bounds__(THREADS)
   pdl_wait();
   const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
 
-  if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
-      for (int i = 0; i < npre; ++i) {
-        const uint32_t st = smem_u32(smem + i * STAGE_BYTES);
-        const int kx = (kt0 + i) * BK;
+  if (loader) {
+    // ---------------- TMA producers
+    for (int i = lj; i < npre; i += p.nload) {
+      const uint32_t st = smem_u32(smem + i * STAGE_BYTES);
+      const int kx = (kt0 + i) * BK;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, smem_u32(&full[i]));
-      }
-      for (int i = npre; i < nk; ++i) {
-        const int s = i % STAGES;
-        if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) break;
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_expect_tx(fb, STAGE_BYTES);
-        const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-        const int kx = (kt0 + i) * BK;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, fb);
-        tma_load_2d(st + MT * A_BYTES, tmB, kx, n0, fb);
-      }
+      for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, smem_u32(&full[i]));
     }
-  } else if (warp == 1) {
+    for (int i = npre; i < nk; ++i) {
+      const int s = i % STAGES;
+      if (s % p.nload != lj) continue;
+      if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) break;
+      const uint32_t fb = smem_u32(&full[s]);
+      mbar_expect_tx(fb, STAGE_BYTES);
+      const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+      const int kx = (kt0 + i) * BK;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, fb);
+      tma_load_2d(st + MT * A_BYTES, tmB, kx, n0, fb);
+    }
+  }
+  if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = instr_desc_ws(bn);  // M = 128, N = bn
@@ -453,10 +459,14 @@ __global__ void __launch_bounds__(THREADS)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
+  // loaders as in the row-tiled kernel: warp 0 and epilogue warps 2-4, each
+  // owning the stages s with s % nload == its index
+  const int lj = warp == 0 ? 0 : ((warp >= 2 && warp <= 4) ? warp - 1 : -1);
+  const bool loader = lj >= 0 && lj < p.nload && lane == 0;
   // weight tiles of the first stages go out before waiting for the producer of A
   const int npre = nk < STAGES ? nk : STAGES;
-  if (warp == 0 && lane == 0) {
-    for (int i = 0; i < npre; ++i) {
+  if (loader) {
+    for (int i = lj; i < npre; i += p.nload) {
       const uint32_t fb = smem_u32(&full[i]);
       mbar_expect_tx(fb, STAGE_BYTES);
       tma_load_2d(smem_u32(smem + i * STAGE_BYTES), tmB, (kt0 + i) * BK, n0, fb);
@@ -467,23 +477,23 @@ __global__ void __launch_bounds__(THREADS)
   const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
   const int np_eff = min(NP, max(16, (M_eff + 15) & ~15));
 
-  if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
-      for (int i = 0; i < npre; ++i)
-        tma_load_2d(smem_u32(smem + i * STAGE_BYTES) + WS_W_BYTES, &tmA, (kt0 + i) * BK, 0, smem_u32(&full[i]));
-      for (int i = npre; i < nk; ++i) {
-        const int s = i % STAGES;
-        if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) break;
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_expect_tx(fb, STAGE_BYTES);
-        const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-        const int kx = (kt0 + i) * BK;
-        tma_load_2d(st, tmB, kx, n0, fb);
-        tma_load_2d(st + WS_W_BYTES, &tmA, kx, 0, fb);
-      }
+  if (loader) {
+    // ---------------- TMA producers
+    for (int i = lj; i < npre; i += p.nload)
+      tma_load_2d(smem_u32(smem + i * STAGE_BYTES) + WS_W_BYTES, &tmA, (kt0 + i) * BK, 0, smem_u32(&full[i]));
+    for (int i = npre; i < nk; ++i) {
+      const int s = i % STAGES;
+      if (s % p.nload != lj) continue;
+      if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) break;
+      const uint32_t fb = smem_u32(&full[s]);
+      mbar_expect_tx(fb, STAGE_BYTES);
+      const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+      const int kx = (kt0 + i) * BK;
+      tma_load_2d(st, tmB, kx, n0, fb);
+      tma_load_2d(st + WS_W_BYTES, &tmA, kx, 0, fb);
     }
-  } else if (warp == 1) {
+  }
+  if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = instr_desc_ws(np_eff);
@@ -1548,6 +1558,10 @@ int max_active_clusters(int smem, int cluster) {
 // plus 0.4 us per cluster split for the reduction.  (Measured on GB300 over the
 // projection shapes of the layer loop against forced sweeps of every
 // configuration: the pick is the fastest or within a few percent of it.)
+// Loader warps for a ring of `stages`: four, two or one, whichever divides it
+// (each loader owns the stages s = j mod n).
+int loaders_for(int stages) { return stages % 4 == 0 ? 4 : (stages % 2 == 0 ? 2 : 1); }
+
 struct GemmPick {
   int kernel;  // 1 row-tiled, 2 weight-stationary, 5 two-SM pair tiles
   int bn, splits, stages;
@@ -1912,7 +1926,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     p.stages = force && force->stages ? force->stages : (auto_stages ? auto_stages : def_stages);
     if (p.stages < 2 || p.stages > max_stages) return cudaErrorInvalidValue;
     p.splits = 1;
-    p.nload = p.stages % 4 == 0 ? 4 : (p.stages % 2 == 0 ? 2 : 1);
+    p.nload = loaders_for(p.stages);
     p.tmem_cols = 32;
     while (p.tmem_cols < 2 * p.bn) p.tmem_cols *= 2;
     p.ntn = rt_tiles(N, nseg, p.bn);
@@ -1988,6 +2002,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
       return cudaErrorInvalidValue;
     p.splits = splits;
     p.stages = stages;
+    p.nload = loaders_for(stages);
     const CUtensorMap* ma = get_map(cache, A, M, K, lda, p.np);
     if (!ma) return cudaErrorInvalidValue;
     return launch_ws(ma, mb, p, dim3(tiles, 1, splits), st);
@@ -2004,6 +2019,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     return cudaErrorInvalidValue;
   p.tmem_cols = 32;
   while (p.tmem_cols < MT * bn) p.tmem_cols *= 2;
+  p.nload = loaders_for(p.stages);
   const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
   if (!ma) return cudaErrorInvalidValue;
   const dim3 grid(tiles, mgroups, splits);

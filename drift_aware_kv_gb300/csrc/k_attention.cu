@@ -194,10 +194,10 @@ __global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
   }
 }
 
-int attention_items(int4* w, int n, int a0, int na, int b0, int nb) {
+int attention_items(int4* w, int n, int a0, int na, int b0, int nb, int max_rows) {
   const int tot = na + nb;
   if (tot <= 0) return n;
-  const int k = (tot + ATT_ITEM_ROWS - 1) / ATT_ITEM_ROWS;
+  const int k = (tot + max_rows - 1) / max_rows;
   for (int i = 0; i < k; ++i) {
     const int lo = (int)((long long)i * tot / k), hi = (int)((long long)(i + 1) * tot / k);
     if (hi <= na)
@@ -210,16 +210,38 @@ int attention_items(int4* w, int n, int a0, int na, int b0, int nb) {
   return n;
 }
 
+static int g_attention_impl = 0;
+
+int attention_set_impl(int impl) {
+  const int old = g_attention_impl;
+  g_attention_impl = impl;
+  return old;
+}
+
+int attention_item_rows(bool bf16, int dh, long long items128, int H, bool measures) {
+  (void)items128;
+  (void)H;
+  (void)measures;
+  if (!bf16 || dh != 128) return ATT_ITEM_ROWS;
+  // The tcgen05 kernel runs when selected: measured on GB300 it is limited by
+  // its one-thread-per-row softmax (about 1.6 us per 64-key tile) and by KL
+  // rows (one thread does a row's drift terms), and it is slower than the
+  // pipelined mma.sync kernel at the layer-loop shapes (within 5-10 % faster
+  // only for untracked items of 256 rows), so the library's choice is the
+  // mma.sync kernel.
+  return g_attention_impl == 2 ? ATT_TC_ROWS : ATT_ITEM_ROWS;
+}
+
 template <typename T>
-void launch_row_attention(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_row_attention(const AttnArgs& a, cudaStream_t st) {
+  if (sizeof(T) == 2 && a.work && a.item_rows == ATT_TC_ROWS) return launch_attention_tc(a, a.batch, st);
   if (sizeof(T) == 2 && a.work) {
     AttnArgs b = a;
     int nsm = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     b.splits = attention_pipe_config(a.n_work, a.H, a.N, a.dh, nsm, &b.stages);
-    launch_attention_pipe(b, a.batch, st);
-    return;
+    return launch_attention_pipe(b, a.batch, st);
   }
   const dim3 grid((a.R + ATT_ROWS - 1) / ATT_ROWS, a.H);
   if (a.dh == 128) {
@@ -234,9 +256,10 @@ void launch_row_attention(const AttnArgs& a, cudaStream_t st) {
     const size_t sm = (2 * ATT_TK * 65 + ATT_ROWS * 64 + ATT_ROWS * ATT_TK) * sizeof(float);
     launch_pdl(row_attention_kernel<T, 64>, dim3(grid), dim3(256), sm, st, a);
   }
+  return cudaGetLastError();
 }
 
-template void launch_row_attention<float>(const AttnArgs&, cudaStream_t);
-template void launch_row_attention<__nv_bfloat16>(const AttnArgs&, cudaStream_t);
+template cudaError_t launch_row_attention<float>(const AttnArgs&, cudaStream_t);
+template cudaError_t launch_row_attention<__nv_bfloat16>(const AttnArgs&, cudaStream_t);
 
 }  // namespace polestar

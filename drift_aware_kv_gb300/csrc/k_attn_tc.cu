@@ -1,0 +1,567 @@
+// bf16 row attention + KL drift on the 5th-generation tensor cores (tcgen05,
+// TMEM accumulators), for work items of up to 128 rows of one sequence.
+//
+// Same computation as the rest of the row-attention family (Eq. 3 attention
+// over all N keys of the row's sequence; Eq. 4 KL drift against the previous
+// scores for tracked rows, in the cancellation-free form
+//   KL = sum_j p_j d_j - log1p( sum_j q~_j expm1(d_j) / sum_j q~_j ) ),
+// organised flash-attention style with every matrix product on tcgen05:
+//
+//   * CTA = one work item (<= 128 rows, given as at most two row ranges of one
+//     sequence) x one query head.  The item's Q rows are the MMA's M side
+//     (TMEM lane = row); keys come in tiles of 64.
+//   * warp 0 streams K and V tiles with TMA (128-byte swizzled 64 x 64 boxes
+//     of the [batch*N, 2*kvdim] cache view) into a five-stage mbarrier ring;
+//     warp 1 issues S_j = Q K_j^T into one of two TMEM score buffers and
+//     O += P_{j-1} V_{j-1} into the TMEM output, so the tensor cores compute
+//     tile j's scores while the softmax warps work on tile j-1;
+//   * warps 2-5 (one thread per row) read a row's 64 scores from TMEM, keep
+//     the running maximum (log2 units) and sum, write P (bf16) into one of two
+//     shared-memory buffers as the next product's A operand, and do the KL
+//     terms of tracked rows; the running maximum is raised lazily (only when a
+//     tile's maximum exceeds it by more than 8, i.e. p <= 2^8), and then the
+//     TMEM output row is rescaled before the next P V product;
+//   * V is the second product's B operand read N-major (dh contiguous) from
+//     the same swizzled boxes, so no transposition is needed.
+// Every mbarrier wait is bounded; a timeout records an error code and the
+// CTA's roles fall through to the final barrier.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "kernels.h"
+
+namespace polestar {
+namespace at {
+
+constexpr int ROWS = 128;   // rows per work item (MMA M)
+constexpr int TK = 64;      // keys per tile (MMA N of S, K of P V)
+constexpr int DH = 128;     // head dim
+constexpr int THREADS = 192;
+constexpr int STAGES = 5;
+constexpr int QBOX = 64 * ROWS * 2;           // 64 columns x 128 rows (Q, P)
+constexpr int KBOX = 64 * TK * 2;             // 64 columns x 64 keys (K, V)
+constexpr int Q_OFF = 0;                      // 2 boxes (dh 0-63, 64-127)
+constexpr int P_OFF = 2 * QBOX;               // 2 buffers x 1 box (64 keys)
+constexpr int RING_OFF = 4 * QBOX;            // STAGES x (K: 2 boxes, V: 2 boxes)
+constexpr int STAGE_BYTES = 4 * KBOX;
+constexpr int O_COL = 2 * TK;                 // TMEM: S buffers at 0 and TK, O after
+constexpr int CTL_OFF = RING_OFF + STAGES * STAGE_BYTES;
+constexpr int SMEM_BYTES = CTL_OFF + 256 + 1024;  // + control block + alignment
+constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err, int code,
+                                          volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > TIMEOUT_CYCLES) {
+      if (err) atomicExch(err, code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// UMMA shared-memory descriptor, 128-byte swizzle: K-major (lbo unused) or
+// N-major (lbo = bytes between 64-element groups along N); sbo = bytes between
+// 8-row groups.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16, bf16 x bf16 -> fp32, M = 128, N = n; B N-major when bmn
+__host__ __device__ constexpr uint32_t idesc(int n, bool bmn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((bmn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// 32 columns of a row without waiting (tcgen05_wait_ld() makes them usable)
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tcgen05_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st32_nw(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// e^x - 1 for the KL drift term: Taylor series through x^6 for |x| < 1/8,
+// 2^(x log2 e) - 1 elsewhere (as in the pipelined kernel)
+__device__ __forceinline__ float expm1_drift(float x) {
+  float t = fmaf(x, 1.f / 720.f, 1.f / 120.f);
+  t = fmaf(x, t, 1.f / 24.f);
+  t = fmaf(x, t, 1.f / 6.f);
+  t = fmaf(x, t, 0.5f);
+  t = fmaf(x, t, 1.f);
+  const float big = ex2f(x * 1.4426950408889634f) - 1.f;
+  return fabsf(x) < 0.125f ? x * t : big;
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *(const uint32_t*)&v;
+}
+// byte offset of 16-byte chunk c (columns 8c..8c+7) of row r in a 128-row x
+// 64-column swizzled box
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+__device__ __forceinline__ int item_row(const int4& wk, int lr) { return lr < wk.y ? wk.x + lr : wk.z + (lr - wk.y); }
+
+__global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, AttnArgs p) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint64_t* kv_full = (uint64_t*)(sm + CTL_OFF);
+  uint64_t* kv_empty = kv_full + STAGES;
+  uint64_t* s_full = kv_empty + STAGES;  // [2]
+  uint64_t* p_full = s_full + 2;         // [2]
+  uint64_t* pv_done = p_full + 2;        // [2]: P V of tiles j with j % 2 == b
+  uint64_t* q_full = pv_done + 2;
+  uint32_t* tmem_slot = (uint32_t*)(q_full + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int4 wk = p.work[blockIdx.x];  // {rowA, nA, rowB, nB}
+  const int nrows = wk.y + wk.w;
+  const int kvh = h / (p.H / p.Hkv);
+  const int ntl = (p.N + TK - 1) / TK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(su32(&kv_full[s]), 1);
+      mbar_init(su32(&kv_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(su32(&s_full[b]), 1);
+      mbar_init(su32(&p_full[b]), 4);
+      mbar_init(su32(&pv_done[b]), 1);
+    }
+    mbar_init(su32(q_full), 4);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  // K/V rows and queries come from the preceding kernels
+  pdl_launch_dependents();
+  pdl_wait();
+  const int seq = p.rows[wk.x].x;
+
+  if (warp == 0) {
+    // ---------------- loader: K then V boxes of each 128-key tile
+    if (lane == 0) {
+      for (int j = 0; j < ntl; ++j) {
+        const int s = j % STAGES;
+        if (j >= STAGES && !mbar_wait(su32(&kv_empty[s]), ((j / STAGES) - 1) & 1, p.err, 21, abort_flag)) break;
+        const uint32_t fb = su32(&kv_full[s]);
+        mbar_expect_tx(fb, STAGE_BYTES);
+        const uint32_t dst = su32(sm + RING_OFF + s * STAGE_BYTES);
+        const int y = seq * p.N + j * TK;
+        tma_load_2d(dst, &tm_kv, kvh * DH, y, fb);
+        tma_load_2d(dst + KBOX, &tm_kv, kvh * DH + 64, y, fb);
+        tma_load_2d(dst + 2 * KBOX, &tm_kv, p.kvdim + kvh * DH, y, fb);
+        tma_load_2d(dst + 3 * KBOX, &tm_kv, p.kvdim + kvh * DH + 64, y, fb);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t q = su32(sm + Q_OFF);
+      bool live = mbar_wait(su32(q_full), 0, p.err, 22, abort_flag);
+      auto issue_pv = [&](int t) -> bool {
+        if (!mbar_wait(su32(&p_full[t & 1]), (t >> 1) & 1, p.err, 23, abort_flag)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t v = su32(sm + RING_OFF + (t % STAGES) * STAGE_BYTES + 2 * KBOX);
+        const uint32_t pb = su32(sm + P_OFF + (t & 1) * QBOX);
+#pragma unroll
+        for (int kk = 0; kk < TK / 16; ++kk)
+          umma(tmem + O_COL, sdesc(pb + kk * 32, 16, 1024), sdesc(v + kk * 16 * 128, KBOX, 1024), idesc(DH, true),
+               (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(su32(&pv_done[t & 1]));
+        umma_commit(su32(&kv_empty[t % STAGES]));
+        return true;
+      };
+      for (int j = 0; j < ntl && live; ++j) {
+        const int s = j % STAGES, b = j & 1;
+        if (!mbar_wait(su32(&kv_full[s]), (j / STAGES) & 1, p.err, 24, abort_flag)) break;
+        // score buffer b is free once the softmax has finished tile j - 2
+        if (j >= 2 && !mbar_wait(su32(&p_full[b]), ((j - 2) >> 1) & 1, p.err, 25, abort_flag)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t kt = su32(sm + RING_OFF + s * STAGE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk)
+          umma(tmem + b * TK, sdesc(q + (kk >> 2) * QBOX + (kk & 3) * 32, 16, 1024),
+               sdesc(kt + (kk >> 2) * KBOX + (kk & 3) * 32, 16, 1024), idesc(TK, false), kk > 0 ? 1u : 0u);
+        umma_commit(su32(&s_full[b]));
+        if (j >= 1 && !issue_pv(j - 1)) live = false;
+      }
+      if (live && ntl > 0) issue_pv(ntl - 1);
+    }
+  } else {
+    // ---------------- softmax / epilogue: row r = TMEM lane
+    const int qd = warp & 3;
+    const int r = qd * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+    const bool has = r < nrows;
+    const int row = has ? item_row(wk, r) : item_row(wk, 0);
+    int4 m = make_int4(0, 0, ROW_NONE, 0);
+    if (has) m = p.rows[row];
+    const bool live = m.z != ROW_NONE && (m.z != ROW_OTHER || p.other_live);
+    const bool outp = live && m.z != ROW_PROXY;
+    float* prev = nullptr;
+    float* prev_lse = nullptr;
+    if (live && m.z == ROW_PROXY && p.proxy_prev) {
+      const size_t idx = ((size_t)seq * p.K + m.w) * p.H + h;
+      prev = p.proxy_prev + idx * p.N;
+      prev_lse = p.proxy_prev_lse + idx;
+    } else if (live && m.z == ROW_ACTIVE && p.active_prev) {
+      const size_t idx = ((size_t)seq * p.B + m.w) * p.H + h;
+      prev = p.active_prev + idx * p.N;
+      prev_lse = p.active_prev_lse + idx;
+    }
+    const float shift = (prev && p.measure) ? *prev_lse * 1.4426950408889634f : 0.f;
+    const bool vec_prev = (p.N & 3) == 0 && ((((uintptr_t)p.active_prev) | ((uintptr_t)p.proxy_prev)) & 15) == 0;
+
+    // 16-byte row accesses when the strides and bases allow them
+    const bool vec_io = ((p.ldq | p.ldo) & 7) == 0 && ((((uintptr_t)p.q) | ((uintptr_t)p.out)) & 15) == 0;
+    // Q row into the swizzled A-operand tile (zeros for padding rows)
+    {
+      const __nv_bfloat16* qrow = (const __nv_bfloat16*)p.q + (size_t)row * p.ldq + h * DH;
+#pragma unroll
+      for (int c = 0; c < DH / 8; ++c) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (live) {
+          if (vec_io) {
+            v = *(const uint4*)(qrow + c * 8);
+          } else {
+            uint16_t e[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) e[k] = ((const uint16_t*)qrow)[c * 8 + k];
+            v = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16), e[4] | ((uint32_t)e[5] << 16),
+                           e[6] | ((uint32_t)e[7] << 16));
+          }
+        }
+        *(uint4*)(sm + Q_OFF + (c >> 3) * QBOX + swz(r, c & 7)) = v;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(su32(q_full));
+    }
+
+    const float sl2 = p.scale * 1.4426950408889634f;
+    float mrun = -INFINITY, l = 0.f, asum = 0.f, sqs = 0.f, esum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntl && ok; ++j) {
+      const int b = j & 1, j0 = j * TK;
+      ok = mbar_wait(su32(&s_full[b]), (j >> 1) & 1, p.err, 26, abort_flag);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!ok) break;
+      // the row's scores of this tile: loads in flight together, one wait
+      uint32_t sv[TK];
+#pragma unroll
+      for (int c = 0; c < TK / 32; ++c) tmem_ld32_nw(tl + b * TK + c * 32, sv + c * 32);
+      tcgen05_wait_ld();
+      // pass 1: tile maximum (log2 units)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < TK; ++i)
+        if (j0 + i < p.N) mx = fmaxf(mx, __uint_as_float(sv[i]) * sl2);
+      // raise the running maximum only when it grows by more than 8 (p <= 2^8)
+      const bool raise = mx > mrun + 8.f;
+      const float mnew = raise ? mx : mrun;
+      const float corr = raise ? ex2f(mrun - mnew) : 1.f;  // exp2(-inf) = 0 on the first tile
+      l *= corr;
+      asum *= corr;
+      // P buffer b is free once P_{j-2} V_{j-2} is done; a raised maximum
+      // rescales the output, which must then hold P_{j-1} V_{j-1}
+      // (the products complete in order)
+      const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
+      if (rescale || j >= 2) {
+        const int t = rescale ? j - 1 : j - 2;
+        ok = mbar_wait(su32(&pv_done[t & 1]), (t >> 1) & 1, p.err, 27, abort_flag);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (!ok) break;
+        if (rescale) {
+          // output row rescale, two halves of 64 columns (loads and stores batched)
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[64];
+            tmem_ld32_nw(tl + O_COL + hf * 64, v);
+            tmem_ld32_nw(tl + O_COL + hf * 64 + 32, v + 32);
+            tcgen05_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+            tmem_st32_nw(tl + O_COL + hf * 64, v);
+            tmem_st32_nw(tl + O_COL + hf * 64 + 32, v + 32);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+      }
+      mrun = mnew;
+      // pass 2: probabilities into P, KL terms of tracked rows
+#pragma unroll
+      for (int c = 0; c < TK / 32; ++c) {
+        const uint32_t* v = sv + c * 32;
+        float pv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const bool in = j0 + c * 32 + i < p.N;
+          pv[i] = in ? ex2f(__uint_as_float(v[i]) * sl2 - mrun) : 0.f;
+          l += pv[i];
+        }
+        if (prev) {
+          const int jc = j0 + c * 32;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const int jj = jc + g * 4;
+            float sp[4] = {0.f, 0.f, 0.f, 0.f};
+            if (p.measure) {
+              if (vec_prev && jj + 3 < p.N) {
+                const float4 t = __ldcg((const float4*)(prev + jj));
+                sp[0] = t.x; sp[1] = t.y; sp[2] = t.z; sp[3] = t.w;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sp[e] = jj + e < p.N ? __ldcg(prev + jj + e) : 0.f;
+              }
+            }
+            float sn[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = g * 4 + e;
+              sn[e] = __uint_as_float(v[i]) * p.scale;  // natural-log units
+              if (p.measure && jj + e < p.N) {
+                const float d = sn[e] - sp[e];
+                const float qt = ex2f(fmaf(sp[e], 1.4426950408889634f, -shift));
+                asum = fmaf(pv[i], d, asum);
+                sqs += qt;
+                esum = fmaf(qt, expm1_drift(d), esum);
+              }
+            }
+            if (p.store) {
+              if (vec_prev && jj + 3 < p.N) {
+                *(float4*)(prev + jj) = make_float4(sn[0], sn[1], sn[2], sn[3]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (jj + e < p.N) prev[jj + e] = sn[e];
+              }
+            }
+          }
+        }
+        // P row, keys c*32 .. c*32+31: four 16-byte chunks
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int key = c * 32 + g * 8;
+          const uint4 w = make_uint4(pack2(pv[g * 8 + 0], pv[g * 8 + 1]), pack2(pv[g * 8 + 2], pv[g * 8 + 3]),
+                                     pack2(pv[g * 8 + 4], pv[g * 8 + 5]), pack2(pv[g * 8 + 6], pv[g * 8 + 7]));
+          *(uint4*)(sm + P_OFF + b * QBOX + swz(r, key >> 3)) = w;
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(su32(&p_full[b]));
+    }
+    // ---------------- epilogue: O / l, KL, log-sum-exp
+    if (ok && ntl > 0) {
+      ok = mbar_wait(su32(&pv_done[(ntl - 1) & 1]), ((ntl - 1) >> 1) & 1, p.err, 28, abort_flag);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    }
+    if (ok) {
+      const float inv = 1.f / l;
+      __nv_bfloat16* o = (__nv_bfloat16*)p.out + (size_t)row * p.ldo + h * DH;
+      uint32_t ov[DH];
+#pragma unroll
+      for (int c = 0; c < DH / 32; ++c) tmem_ld32_nw(tl + O_COL + c * 32, ov + c * 32);
+      tcgen05_wait_ld();
+#pragma unroll
+      for (int c = 0; c < DH / 32; ++c) {
+        const uint32_t* v = ov + c * 32;
+        if (outp) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint4 w = make_uint4(
+                pack2(__uint_as_float(v[g * 8 + 0]) * inv, __uint_as_float(v[g * 8 + 1]) * inv),
+                pack2(__uint_as_float(v[g * 8 + 2]) * inv, __uint_as_float(v[g * 8 + 3]) * inv),
+                pack2(__uint_as_float(v[g * 8 + 4]) * inv, __uint_as_float(v[g * 8 + 5]) * inv),
+                pack2(__uint_as_float(v[g * 8 + 6]) * inv, __uint_as_float(v[g * 8 + 7]) * inv));
+            if (vec_io) {
+              *(uint4*)(o + c * 32 + g * 8) = w;
+            } else {
+              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                ((uint16_t*)o)[c * 32 + g * 8 + 2 * k] = (uint16_t)(ww[k] & 0xFFFF);
+                ((uint16_t*)o)[c * 32 + g * 8 + 2 * k + 1] = (uint16_t)(ww[k] >> 16);
+              }
+            }
+          }
+        }
+      }
+      if (prev) {
+        if (p.measure) p.kl_out[(size_t)row * p.H + h] = asum / l - log1pf(esum / sqs);
+        if (p.store) *prev_lse = mrun * 0.6931471805599453f + logf(l);
+      }
+    }
+  }
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // let in-flight bulk copies land before the CTA's shared memory is released
+    const long long t0 = clock64();
+    while (clock64() - t0 < 20000000LL) {
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+// 2D tensor map of one layer's K/V cache viewed as [batch*N rows][2*kvdim] bf16
+// with 64-column x TK-row boxes and 128-byte swizzle (cached per buffer/shape).
+const CUtensorMap* kv_map_tiles(const void* base, int rows, int cols) {
+  static std::map<std::tuple<const void*, int, int>, CUtensorMap> cache;
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(base, rows, cols);
+  auto it = cache.find(key);
+  if (it != cache.end()) return &it->second;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  }
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)TK};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return nullptr;
+  return &cache.emplace(key, m).first->second;
+}
+
+}  // namespace at
+
+cudaError_t launch_attention_tc(const AttnArgs& a, int batch, cudaStream_t st) {
+  if (a.dh != at::DH || (a.kvdim & 7)) return cudaErrorInvalidValue;
+  const CUtensorMap* map = at::kv_map_tiles(a.kv_layer, batch * a.N, 2 * a.kvdim);
+  if (!map) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(at::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, at::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.n_work, a.H, 1);
+  cfg.blockDim = dim3(at::THREADS);
+  cfg.dynamicSmemBytes = at::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute att[1];
+  att[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  att[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = att;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, at::attn_tc_kernel, *map, a);
+}
+
+}  // namespace polestar

@@ -91,17 +91,30 @@ struct AttnArgs {
   int splits;
   int stages;
   int* err;                // device word for the code of a timed-out wait (may be null)
+  int item_rows;           // rows per work item the list was built with (ATT_ITEM_ROWS or ATT_TC_ROWS)
 };
-constexpr int ATT_ITEM_ROWS = 48;  // 3 compute warps x 16 rows
+constexpr int ATT_ITEM_ROWS = 48;  // pipelined mma.sync kernel: 3 compute warps x 16 rows
+constexpr int ATT_TC_ROWS = 128;   // tcgen05 kernel: one TMEM lane per row
 // Work items for the rows [a0, a0 + na) ++ [b0, b0 + nb) of one sequence,
-// appended at w[n..]; returns the new count (items of near-equal size).
-int attention_items(int4* w, int n, int a0, int na, int b0, int nb);
+// appended at w[n..]; returns the new count (items of near-equal size, at most
+// max_rows rows each).
+int attention_items(int4* w, int n, int a0, int na, int b0, int nb, int max_rows = ATT_ITEM_ROWS);
+// Rows per work item for a bf16/fp32 launch with head size dh whose items, at
+// ATT_TC_ROWS rows, would number about `items128` (all sequences) over H
+// heads, `measures` when some rows compute KL drift: ATT_TC_ROWS when the
+// tcgen05 kernel runs it (only when selected through attention_set_impl),
+// else ATT_ITEM_ROWS.
+int attention_item_rows(bool bf16, int dh, long long items128, int H, bool measures);
+// Test hook: 0 = library's choice, 1 = pipelined mma.sync kernel only, 2 =
+// tcgen05 kernel wherever it applies; returns the previous setting.
+int attention_set_impl(int impl);
+cudaError_t launch_attention_tc(const AttnArgs& a, int batch, cudaStream_t st);
 // Key splits and ring depth of the pipelined bf16 kernel for a grid of n_work
 // items x H heads.
 int attention_pipe_config(int n_work, int H, int N, int dh, int num_sms, int* stages);
 cudaError_t launch_attention_pipe(const AttnArgs& a, int batch, cudaStream_t st);
 template <typename T>
-void launch_row_attention(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_row_attention(const AttnArgs& a, cudaStream_t st);
 
 // ---- K-means + NVFP4 (k_cluster.cu) ----
 struct KmeansArgs {

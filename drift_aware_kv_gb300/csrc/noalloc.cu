@@ -80,7 +80,9 @@ extern "C" polestar_status polestar_attention_noalloc(const void* q, const void*
   const polestar_status st0 = resolve(dev, &s);
   if (st0 != POLESTAR_OK) return st0;
   cudaStream_t st = (cudaStream_t)stream;
-  const int n_work = (R + ATT_ITEM_ROWS - 1) / ATT_ITEM_ROWS;
+  const int item_rows =
+      attention_item_rows(true, head_dim, (R + ATT_TC_ROWS - 1) / ATT_TC_ROWS, H, tracked != nullptr && measure != 0);
+  const int n_work = (R + item_rows - 1) / item_rows;
   fill_tables_kernel<<<1, 256, 0, st>>>(tracked, R, n_work, s->rows, s->work);
   AttnArgs a{};
   a.q = q;
@@ -107,7 +109,8 @@ extern "C" polestar_status polestar_attention_noalloc(const void* q, const void*
   a.kl_out = kl;
   a.work = s->work;
   a.n_work = n_work;
+  a.item_rows = item_rows;
   a.batch = 1;
-  launch_row_attention<__nv_bfloat16>(a, st);
+  if (launch_row_attention<__nv_bfloat16>(a, st) != cudaSuccess) return POLESTAR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }

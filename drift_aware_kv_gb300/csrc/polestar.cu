@@ -475,14 +475,20 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
   int4* work_h = meta_h<int4>(c, c->ml.work_off);
   int nwk = 0;
   std::vector<int> chunk_work_off, chunk_work_n;
+  const bool bf16 = c->cfg.dtype == POLESTAR_BF16;
+  const int entry_rows =
+      attention_item_rows(bf16, c->dh, (long long)std::min(chunk, b) * ((E.size() + ATT_TC_ROWS - 1) / ATT_TC_ROWS),
+                          c->H, false);
   for (int s0 = 0; s0 < b; s0 += chunk) {
     const int ns = std::min(chunk, b - s0);
     chunk_work_off.push_back(nwk);
-    for (int i = 0; i < ns; ++i) nwk = attention_items(work_h, nwk, i * per_seq, (int)E.size(), 0, 0);
+    for (int i = 0; i < ns; ++i) nwk = attention_items(work_h, nwk, i * per_seq, (int)E.size(), 0, 0, entry_rows);
     chunk_work_n.push_back(nwk - chunk_work_off.back());
   }
   const int proxy_work_off = nwk;
-  for (int s = 0; s < b; ++s) nwk = attention_items(work_h, nwk, s * c->K, c->K, 0, 0);
+  const int proxy_rows =
+      attention_item_rows(bf16, c->dh, (long long)b * ((c->K + ATT_TC_ROWS - 1) / ATT_TC_ROWS), c->H, false);
+  for (int s = 0; s < b; ++s) nwk = attention_items(work_h, nwk, s * c->K, c->K, 0, 0, proxy_rows);
   const int proxy_work_n = nwk - proxy_work_off;
   if (nwk > c->ml.work_cap) return fail(c, POLESTAR_ERR_UNSUPPORTED, "attention work list overflow");
   CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
@@ -533,6 +539,7 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       aa.other_live = 1;
       aa.work = work_d + chunk_work_off[ci];
       aa.n_work = chunk_work_n[ci];
+      aa.item_rows = entry_rows;
       if (l == L - 1) {
         aa.active_prev = c->aprev;
         aa.active_prev_lse = c->aprev_lse;
@@ -542,7 +549,7 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
                                 (l == L - 1 ? (double)ns * c->B * c->H * N * 4.0 : 0.0);
       aa.batch = b;
       aa.err = tc_error_word(&c->tc);
-      RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
+      RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
       TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
                                  c->a_in, c->sm)));
@@ -623,10 +630,11 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
     aa.store = 1;
     aa.work = work_d + proxy_work_off;
     aa.n_work = proxy_work_n;
+    aa.item_rows = proxy_rows;
     const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz + (double)b * c->K * c->H * N * 4.0;
     aa.batch = b;
     aa.err = tc_error_word(&c->tc);
-    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
+    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
   }
   std::fill(c->cum.begin(), c->cum.end(), 0);
   std::fill(c->fire.begin(), c->fire.end(), 0);
@@ -680,8 +688,12 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
   int4* work_h = meta_h<int4>(c, c->ml.work_off);
   int nwk = 0;
   // one sequence's active rows and (when it refreshes) its window + proxy rows
+  long long items128 = 0;
+  for (int s = 0; s < b; ++s) items128 += (B + (win_row[s] >= 0 ? c->nw + c->K : 0) + ATT_TC_ROWS - 1) / ATT_TC_ROWS;
+  const int step_rows = attention_item_rows(c->cfg.dtype == POLESTAR_BF16, c->dh, items128, c->H, true);
   for (int s = 0; s < b; ++s)
-    nwk = attention_items(work_h, nwk, s * B, B, win_row[s] >= 0 ? win_row[s] : 0, win_row[s] >= 0 ? c->nw + c->K : 0);
+    nwk = attention_items(work_h, nwk, s * B, B, win_row[s] >= 0 ? win_row[s] : 0, win_row[s] >= 0 ? c->nw + c->K : 0,
+                          step_rows);
   if (nwk > c->ml.work_cap) return fail(c, POLESTAR_ERR_UNSUPPORTED, "attention work list overflow");
   CUDA_OR_FAIL(c, cudaMemcpyAsync(c->meta_d, c->meta_h, c->ml.total, cudaMemcpyHostToDevice, c->sm));
   CUDA_OR_FAIL(c, cudaEventRecord(c->meta_ev, c->sm));
@@ -792,12 +804,13 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     aa.kl_out = c->kl_rows;
     aa.work = meta_d<int4>(c, c->ml.work_off);
     aa.n_work = nwk;
+    aa.item_rows = step_rows;
     const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz +
                               (double)n_fire * c->K * c->H * N * 8.0 +
                               (l == L - 1 ? (double)b * B * c->H * N * 8.0 : 0.0);
     aa.batch = b;
     aa.err = tc_error_word(&c->tc);
-    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, (launch_row_attention<T>(aa, c->sm)));
+    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
     SelectArgs sa{};
     sa.batch = b;
     sa.Wmax = c->Wmax;
@@ -1283,8 +1296,10 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   std::vector<int4> rows(R), work;
   for (int r = 0; r < R; ++r)
     rows[r] = make_int4(0, 0, (tracked && tracked[r]) ? ROW_ACTIVE : ROW_OTHER, r);
-  work.resize((R + ATT_ITEM_ROWS - 1) / ATT_ITEM_ROWS);
-  work.resize(attention_items(work.data(), 0, 0, R, 0, 0));
+  const int item_rows = attention_item_rows(dtype == POLESTAR_BF16, head_dim, (R + ATT_TC_ROWS - 1) / ATT_TC_ROWS, H,
+                                            any_tracked && measure);
+  work.resize((R + item_rows - 1) / item_rows);
+  work.resize(attention_items(work.data(), 0, 0, R, 0, 0, item_rows));
   int4* d_rows = nullptr;
   int4* d_work = nullptr;
   if (cudaMalloc(&d_rows, sizeof(int4) * R) != cudaSuccess) return POLESTAR_ERR_OOM;
@@ -1319,16 +1334,19 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   a.kl_out = kl;
   a.work = d_work;
   a.n_work = (int)work.size();
+  a.item_rows = item_rows;
   a.batch = 1;
-  if (dtype == POLESTAR_BF16)
-    launch_row_attention<__nv_bfloat16>(a, st);
-  else
-    launch_row_attention<float>(a, st);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = dtype == POLESTAR_BF16 ? launch_row_attention<__nv_bfloat16>(a, st) : launch_row_attention<float>(a, st);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   cudaFree(d_rows);
   cudaFree(d_work);
   return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
+extern "C" int32_t polestar_debug_attention_impl(int32_t impl) {
+  if (impl < 0 || impl > 2) return -1;
+  return attention_set_impl(impl);
 }
 
 extern "C" polestar_status polestar_debug_kmeans(const float* Hw, int32_t P, int32_t nw, int32_t d, int32_t K,

@@ -75,10 +75,11 @@ def bench_attn(a):
     plse = torch.zeros(a.R, a.H, device="cuda")
     out = torch.empty(a.R, a.H * dh, dtype=torch.bfloat16, device="cuda")
     kl = torch.empty(a.R, a.H, device="cuda")
+    P.attention_impl(getattr(a, "impl", 0))
     P.attention_noalloc(q, kv, a.H, a.Hkv, tracked, prev, plse, 0, 1, out, kl)
     ms = _time(lambda: P.attention_noalloc(q, kv, a.H, a.Hkv, tracked, prev, plse, 1, 1, out, kl), a.iters)
     byts = a.N * 2 * a.Hkv * dh * 2 + a.R * a.H * dh * 4 + a.tracked * a.H * a.N * 8
-    return dict(kernel="attention", R=a.R, N=a.N, H=a.H, Hkv=a.Hkv, us=ms * 1e3, GBps=byts / ms / 1e6,
+    return dict(kernel="attention", impl=getattr(a, "impl", 0), R=a.R, N=a.N, H=a.H, Hkv=a.Hkv, us=ms * 1e3, GBps=byts / ms / 1e6,
                 TFLOPs=4 * a.R * a.N * a.H * dh / ms / 1e9)
 
 
@@ -106,6 +107,8 @@ def main():
     ap.add_argument("--bn", type=int, default=0, help="row-tiled columns per tile (0 = library's choice)")
     ap.add_argument("--splits", type=int, default=0,
                     help="tcgen05 cluster K split, or CTA count for path 4 (0 = library's choice)")
+    ap.add_argument("--impl", type=int, default=0,
+                    help="attention kernel: 0 library's choice, 1 pipelined mma.sync, 2 tcgen05")
     ap.add_argument("--R", type=int, default=136)
     ap.add_argument("--H", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=32)

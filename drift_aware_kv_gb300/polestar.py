@@ -24,7 +24,8 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
             "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
             "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc",
-            "polestar_packed_weight_bytes", "polestar_pack_weights", "polestar_debug_gemm_choice")
+            "polestar_packed_weight_bytes", "polestar_pack_weights", "polestar_debug_gemm_choice",
+            "polestar_debug_attention_impl")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
 
@@ -222,6 +223,19 @@ def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0) -> int
     CTA count (kernels 4, 5); bn the columns per tile of kernels 2 and 6 (a
     multiple of 16); 0 = automatic."""
     return kernel | (stages << 8) | (splits << 16) | ((bn // 16) << 24)
+
+
+def attention_impl(impl: int) -> int:
+    """Select the attention kernel (polestar_debug_attention_impl): 0 library's
+    choice, 1 pipelined mma.sync only, 2 tcgen05 wherever it applies; returns
+    the previous setting."""
+    lib = load()
+    lib.polestar_debug_attention_impl.argtypes = [C.c_int32]
+    lib.polestar_debug_attention_impl.restype = C.c_int32
+    old = lib.polestar_debug_attention_impl(int(impl))
+    if old < 0:
+        raise ValueError(f"invalid attention kernel selection {impl}")
+    return old
 
 
 def gemm_choice(M: int, Ns, K: int) -> dict:

@@ -249,6 +249,14 @@ polestar_status polestar_debug_attention(const void *q, const void *kv, int32_t 
                                          float *prev_lse, int32_t measure, int32_t store, void *out, float *kl,
                                          int32_t dtype, void *stream);
 
+/* ---- attention kernel selection (test hook) ----
+ * 0: the library's choice (the pipelined mma.sync kernel); 1: the mma.sync
+ * kernel; 2: the tcgen05 kernel (S and O accumulated in TMEM, work items of
+ * up to 128 rows) wherever it applies (bf16, head size 128).  Affects work lists built after the call (context steps and
+ * polestar_debug_attention); returns the previous setting, or -1 for an
+ * invalid value.  Process-wide; not for concurrent use with running steps. */
+int32_t polestar_debug_attention_impl(int32_t impl);
+
 /* ---- row attention + KL drift that allocates nothing ----
  * The paper has no counterpart to this call; it exists for callers that cannot
  * let a library allocate device memory: a host application that owns every

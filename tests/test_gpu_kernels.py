@@ -48,13 +48,25 @@ ATTN_CASES = [  # (R, N, H, Hkv, dh, dtype)
     (136, 768, 32, 32, 128, torch.bfloat16),   # LLaDA-8B within-block rows
     (40, 2048, 32, 32, 128, torch.bfloat16),   # long-context workload
     (104, 768, 28, 4, 128, torch.bfloat16),    # Dream-7B GQA
+    (300, 1000, 4, 4, 128, torch.bfloat16),    # three items, ragged 128-key tile tail
+    (129, 130, 2, 1, 128, torch.bfloat16),     # one-row item, two-key tail tile
     (70, 100, 4, 4, 64, torch.bfloat16),       # ragged tile tail
     (24, 192, 4, 4, 64, torch.float32),        # fp32 single-layer workload
 ]
 
 
+@pytest.fixture(params=[1, 2], ids=["mma_sync", "tcgen05"])
+def attention_kernel(request):
+    """Runs a test once per attention kernel (the tcgen05 kernel covers bf16,
+    head size 128; other cases fall back to the same kernel twice)."""
+    from drift_aware_kv_gb300 import polestar as P
+    old = P.attention_impl(request.param)
+    yield request.param
+    P.attention_impl(old)
+
+
 @pytest.mark.parametrize("R,N,H,Hkv,dh,dt", ATTN_CASES)
-def test_attention_and_kl_match_definition(R, N, H, Hkv, dh, dt):
+def test_attention_and_kl_match_definition(R, N, H, Hkv, dh, dt, attention_kernel):
     from drift_aware_kv_gb300 import polestar as P
     g = torch.Generator().manual_seed(R * 131 + N)
     scale = 1.6 if dh == 128 else 0.4  # score spread of the LLaDA-shaped projections

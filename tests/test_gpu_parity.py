@@ -40,3 +40,16 @@ def test_mini_bf16_trajectory(name):
     rep = _run(name, kv_tol=1e-2, act_tol=1e-2, n_steps=None)
     assert rep.compared >= 8 and rep.fires >= 3, rep
     assert rep.near_ties <= 2
+
+
+def test_mini_bf16_trajectory_tcgen05_attention():
+    """The same lockstep with every attention launch (within-block rows with KL,
+    block entries, proxy baselines) on the tcgen05 kernel (head size 128)."""
+    from drift_aware_kv_gb300 import polestar as P
+    old = P.attention_impl(2)
+    try:
+        rep = _run("mini_l2_d512_bf16", kv_tol=1e-2, act_tol=1e-2, n_steps=None)
+    finally:
+        P.attention_impl(old)
+    assert rep.compared >= 8 and rep.fires >= 3, rep
+    assert rep.near_ties <= 2
