@@ -59,6 +59,12 @@ struct Params {
   int tmem_cols;
   int ntn;    // persistent pair kernels: column tiles over all segments
   int nload;  // loader warps (1, 2 or 4; divides stages)
+  // row-tiled kernel, SwiGLU mode: segments 0 (gate) and 1 (up) of equal width
+  // seg_N[0]; tile t computes columns [t*bn/2, (t+1)*bn/2) of both (gate in
+  // the accumulator's first half, up in the second) and writes
+  // act[row, col] = bf16(silu(g) * u) (row stride ld_act) instead of C
+  __nv_bfloat16* act;
+  int ld_act;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -183,6 +189,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// silu(g) * u, as the unfused SwiGLU kernel computes it
+__device__ __forceinline__ float swiglu1(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
 // Row-tiled kernel: the gathered rows are the MMA's M side (MT sub-tiles of
 // 128), a CTA owns p.bn (a multiple of 16, at most 256) output columns of one
 // weight segment as the MMA's N side.  The column width is chosen per launch
@@ -211,13 +230,24 @@ __global__ void __launch_bounds__(THREADS)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
-  const int seg = (tile >= p.seg_start[1]) + (tile >= p.seg_start[2]);
-  const int n0 = (tile - p.seg_start[seg]) * bn;
+  const bool glu = p.act != nullptr;  // SwiGLU mode: gate and up halves of one tile
+  const int seg = glu ? 0 : (tile >= p.seg_start[1]) + (tile >= p.seg_start[2]);
+  const int n0 = glu ? tile * (bn / 2) : (tile - p.seg_start[seg]) * bn;
   const int segN = p.seg_N[seg];
   float* const Cseg = p.seg_C[seg];
   const CUtensorMap* tmB = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
   const int m0 = blockIdx.y * (MT * BM);
   const int split = blockIdx.z;
+  // W tile of a stage: one bn-row box, or in SwiGLU mode the gate and up boxes
+  // of bn/2 rows each (the up half at row bn/2 of the tile)
+  auto load_w = [&](uint32_t dst, int kx, uint32_t bar) {
+    if (glu) {
+      tma_load_2d(dst, &tmB0, kx, n0, bar);
+      tma_load_2d(dst + (bn / 2) * 128, &tmB1, kx, n0, bar);
+    } else {
+      tma_load_2d(dst, tmB, kx, n0, bar);
+    }
+  };
 
   const int kt0 = (int)((long long)split * p.ktiles / p.splits);
   const int kt1 = (int)((long long)(split + 1) * p.ktiles / p.splits);
@@ -256,7 +286,7 @@ __global__ void __launch_bounds__(THREADS)
     for (int i = lj; i < npre; i += p.nload) {
       const uint32_t fb = smem_u32(&full[i]);
       mbar_expect_tx(fb, STAGE_BYTES);
-      tma_load_2d(smem_u32(smem + i * STAGE_BYTES) + MT * A_BYTES, tmB, (kt0 + i) * BK, n0, fb);
+      load_w(smem_u32(smem + i * STAGE_BYTES) + MT * A_BYTES, (kt0 + i) * BK, fb);
     }
   }
   pdl_launch_dependents();
@@ -281,7 +311,7 @@ __global__ void __launch_bounds__(THREADS)
       const int kx = (kt0 + i) * BK;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, fb);
-      tma_load_2d(st + MT * A_BYTES, tmB, kx, n0, fb);
+      load_w(st + MT * A_BYTES, kx, fb);
     }
   }
   if (warp == 1) {
@@ -318,7 +348,41 @@ __global__ void __launch_bounds__(THREADS)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   }
   const bool vec = ((p.ldc & 3) == 0) && ((((uintptr_t)Cseg) & 15) == 0);
-  if (p.splits == 1) {
+  const int half = bn / 2;
+  const bool avec = glu && ((p.ld_act & 7) == 0) && ((((uintptr_t)p.act) & 15) == 0);
+  if (p.splits == 1 && glu) {
+    // SwiGLU epilogue: gate columns c and up columns half + c of each row
+    if (epi && ok) {
+#pragma unroll 1
+      for (int mt = 0; mt < MT; ++mt) {
+        const int row = m0 + mt * BM + q * 32 + lane;
+        const uint32_t tr = tmem + ((uint32_t)(q * 32) << 16) + mt * bn;
+#pragma unroll 1
+        for (int c = 0; c < half; c += 8) {
+          float g[8], u[8];
+          tmem_ld8(tr + c, g);
+          tmem_ld8(tr + half + c, u);
+          if (row < M_eff) {
+            __nv_bfloat16* dst = p.act + (size_t)row * p.ld_act + n0 + c;
+            if (n0 + c + 8 <= segN && avec) {
+              uint32_t w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 b2 =
+                    __floats2bfloat162_rn(swiglu1(g[2 * j], u[2 * j]), swiglu1(g[2 * j + 1], u[2 * j + 1]));
+                w[j] = *(const uint32_t*)&b2;
+              }
+              *(uint4*)dst = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (n0 + c + j < segN) dst[j] = __float2bfloat16_rn(swiglu1(g[j], u[j]));
+            }
+          }
+        }
+      }
+    }
+  } else if (p.splits == 1) {
     if (epi && ok) {
 #pragma unroll 1
       for (int mt = 0; mt < MT; ++mt) {
@@ -363,6 +427,34 @@ __global__ void __launch_bounds__(THREADS)
       cluster_sync();
       // this CTA reduces its share of the sub-tile's rows, splits in fixed order
       const int rbeg = (int)rank * BM / p.splits, rend = ((int)rank + 1) * BM / p.splits;
+      if (glu) {
+        // SwiGLU: gate columns cc.. and up columns half + cc.. of a row
+        const int h4 = half / 4;
+        for (int idx = threadIdx.x; idx < (rend - rbeg) * h4; idx += THREADS) {
+          const int rr = rbeg + idx / h4, cc = (idx % h4) * 4;
+          const int row = m0 + mt * BM + rr;
+          if (row >= M_eff) continue;
+          float4 ag = ld_dsmem4(red + rr * pitch + cc, 0u), au = ld_dsmem4(red + rr * pitch + half + cc, 0u);
+          for (int s = 1; s < p.splits; ++s) {
+            const float4 vg = ld_dsmem4(red + rr * pitch + cc, (uint32_t)s);
+            const float4 vu = ld_dsmem4(red + rr * pitch + half + cc, (uint32_t)s);
+            ag.x += vg.x;
+            ag.y += vg.y;
+            ag.z += vg.z;
+            ag.w += vg.w;
+            au.x += vu.x;
+            au.y += vu.y;
+            au.z += vu.z;
+            au.w += vu.w;
+          }
+          const float a4[4] = {swiglu1(ag.x, au.x), swiglu1(ag.y, au.y), swiglu1(ag.z, au.z), swiglu1(ag.w, au.w)};
+          __nv_bfloat16* dst = p.act + (size_t)row * p.ld_act + n0 + cc;
+          for (int j = 0; j < 4; ++j)
+            if (n0 + cc + j < segN) dst[j] = __float2bfloat16_rn(a4[j]);
+        }
+        cluster_sync();
+        continue;
+      }
       const int c4 = bn / 4;
       for (int idx = threadIdx.x; idx < (rend - rbeg) * c4; idx += THREADS) {
         const int rr = rbeg + idx / c4, cc = (idx % c4) * 4;
@@ -2023,6 +2115,71 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
   if (!ma) return cudaErrorInvalidValue;
   const dim3 grid(tiles, mgroups, splits);
+  return MT == 2 ? launch_rt<2>(ma, mb, p, grid, st) : launch_rt<1>(ma, mb, p, grid, st);
+}
+
+cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, const void* Wg, const void* Wu, int ldw,
+                                int F, void* act, int ld_act, int M, const int* m_dev, int K, cudaStream_t st,
+                                const TcGemmChoice* force) {
+  using namespace tc;
+  if (M <= 0 || F <= 0) return cudaSuccess;
+  if (!A || !Wg || !Wu || !act || ld_act < F || !tc_gemm_supported(K, lda, ldw)) return cudaErrorInvalidValue;
+  if (((uintptr_t)A | (uintptr_t)Wg | (uintptr_t)Wu) & 15) return cudaErrorInvalidValue;
+  int* err = tc_error_word(cache);
+  if (!err) return cudaErrorMemoryAllocation;
+  if (cache->num_sms <= 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&cache->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cache->num_sms <= 0) return cudaErrorNoDevice;
+  }
+  const int nsm = cache->num_sms;
+  const int MT = M > BM ? 2 : 1;
+  const int mgroups = (M + MT * BM - 1) / (MT * BM);
+  const int ktiles = (K + BK - 1) / BK;
+  const int Ns[2] = {F, F};
+  GemmPick pk{1, 0, 1, 0};
+  if (force && force->kernel) {
+    if (force->kernel != 1) return cudaErrorNotSupported;
+    pk.bn = force->bn;
+    pk.splits = force->splits ? force->splits : 1;
+    pk.stages = force->stages;
+  } else {
+    pk = mgroups == 1 ? pick_small_m(MT, M, Ns, 2, ktiles, nsm) : pick_large_m(M, Ns, 2, ktiles, nsm);
+    if (pk.kernel != 1) return cudaErrorNotSupported;  // only the row-tiled kernel fuses the activation
+  }
+  const int bn = pk.bn ? pk.bn : (mgroups == 1 ? pick_small_m(MT, M, Ns, 2, ktiles, nsm).bn : 256);
+  if (bn < 16 || bn > 256 || (bn & 15) || MT * bn > 512) return cudaErrorInvalidValue;
+  Params p{};
+  p.M = M;
+  p.K = K;
+  p.m_dev = m_dev;
+  p.ldc = 0;
+  p.ktiles = ktiles;
+  p.err = err;
+  p.nseg = 2;
+  p.seg_start[0] = 0;
+  p.seg_start[1] = p.seg_start[2] = p.seg_start[3] = 0x3FFFFFFF;
+  p.seg_N[0] = p.seg_N[1] = F;
+  p.act = (__nv_bfloat16*)act;
+  p.ld_act = ld_act;
+  p.bn = bn;
+  p.splits = pk.splits;
+  p.stages = pk.stages ? pk.stages : rt_max_stages(MT, bn);
+  if (p.splits < 1 || p.splits > 8 || p.stages < 2 || p.stages > RT_MAX_STAGES ||
+      rt_smem_bytes(MT, bn, p.stages) > 232448 ||
+      (p.splits > 1 && p.stages * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4))
+    return cudaErrorInvalidValue;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < MT * bn) p.tmem_cols *= 2;
+  p.nload = loaders_for(p.stages);
+  const CUtensorMap* mb[3];
+  mb[0] = get_map(cache, Wg, F, K, ldw, bn / 2);
+  mb[1] = get_map(cache, Wu, F, K, ldw, bn / 2);
+  mb[2] = mb[0];
+  const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
+  if (!mb[0] || !mb[1] || !ma) return cudaErrorInvalidValue;
+  const dim3 grid((F + bn / 2 - 1) / (bn / 2), mgroups, p.splits);
   return MT == 2 ? launch_rt<2>(ma, mb, p, grid, st) : launch_rt<1>(ma, mb, p, grid, st);
 }
 

@@ -75,6 +75,16 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
                                int K, cudaStream_t st, const TcGemmChoice* force = nullptr,
                                const void* const* Wpacked = nullptr);
 
+// Gate and up projections with the SwiGLU activation fused into the
+// row-tiled kernel's epilogue: act[m, f] = bf16(silu(g) * u) with
+// g = A * Wg^T, u = A * Wu^T (both [F, K], row stride ldw), act row stride
+// ld_act.  cudaErrorNotSupported when the library's choice for this shape is
+// not the row-tiled kernel (the caller then runs the projections and the
+// activation separately); force (kernel 1 only) overrides width/split/depth.
+cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, const void* Wg, const void* Wu, int ldw,
+                                int F, void* act, int ld_act, int M, const int* m_dev, int K, cudaStream_t st,
+                                const TcGemmChoice* force = nullptr);
+
 // Bytes of the packed tile layout of an N x K bf16 matrix: for each 128-row
 // tile and 64-column k-tile, 16 KB holding that block as a 128-byte-swizzled
 // shared-memory image (zero outside the matrix), k-tiles of a tile adjacent.

@@ -80,6 +80,7 @@ struct polestar_ctx {
   float *h_rows = nullptr, *h1 = nullptr, *gout = nullptr, *kl_rows = nullptr;
   int num_sms = 148;
   void *a_in = nullptr, *q_rows = nullptr, *attn_out = nullptr;
+  void* act = nullptr;  // bf16 SwiGLU output of the fused gate/up projection [Rmax][F]
   uint8_t* write_kv = nullptr;
   float *U = nullptr, *dn = nullptr;
   uint8_t *sel_a = nullptr, *sel_b = nullptr, *sel_last = nullptr;
@@ -362,6 +363,38 @@ polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int
   return POLESTAR_OK;
 }
 
+// Gate/up projections + SwiGLU: one fused tcgen05 launch writing the bf16
+// activation into *act_out for at most 128 rows when the library's kernel
+// choice is the row-tiled kernel (else the two projections into gout and the
+// activation kernel into a_in).  With more rows the fused tile's two half-width
+// weight boxes per stage made the projection slower than the launch it saves
+// (measured at LLaDA-8B batch 8 and Dream-7B batch 4).
+template <typename T>
+polestar_status gate_up_swiglu(polestar_ctx* c, const polestar_layer_weights& w, int R, const int* m_dev,
+                               const void** act_out) {
+  const int d = c->d, F = c->F;
+  const int Ns[2] = {F, F};
+  int ch[4] = {0, 0, 0, 0};
+  if (sizeof(T) == 2 && c->act && R > 0 && R <= 128 && tc_gemm_supported(d, d, d) &&
+      tc_gemm_choice(&c->tc, R, 2, Ns, d, ch) == cudaSuccess && ch[0] == 1) {
+    const double bytes = ((double)2 * F * d + (double)R * d) * sizeof(T) + (double)R * F * 2.0;
+    const double flops = 4.0 * R * F * d;
+    const int pi = prof_start(c, c->gemm_cls);
+    const cudaError_t e = tc_gemm_bf16_swiglu(&c->tc, c->a_in, d, w.w_gate, w.w_up, d, F, c->act, F, R, m_dev, d, c->sm);
+    prof_stop(c, pi, bytes, flops);
+    ++c->launches;
+    if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 gemm + SwiGLU: ") + cudaGetErrorString(e));
+    *act_out = c->act;
+    return POLESTAR_OK;
+  }
+  const void* Ws[2] = {w.w_gate, w.w_up};
+  float* Cs[2] = {c->gout, c->gout + F};
+  TRY(gemm_multi<T>(c, c->a_in, d, 2, Ws, Ns, Cs, c->ldg, R, m_dev, d));
+  RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, m_dev, R, F, c->a_in, c->sm)));
+  *act_out = c->a_in;
+  return POLESTAR_OK;
+}
+
 // A wait inside a kernel that ran out of time (the kernels record its code in
 // the device error word and return): reported as POLESTAR_ERR_TIMEOUT by the
 // first call after the step that hit it.
@@ -553,14 +586,9 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
                                  c->a_in, c->sm)));
-      {
-        const void* Ws[2] = {w.w_gate, w.w_up};
-        const int Ns[2] = {c->F, c->F};
-        float* Cs[2] = {c->gout, c->gout + c->F};
-        TRY(gemm_multi<T>(c, c->a_in, d, 2, Ws, Ns, Cs, c->ldg, R, nullptr, d));
-      }
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, nullptr, R, c->F, c->a_in, c->sm)));
-      TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, R, nullptr, d, c->F));
+      const void* act = nullptr;
+      TRY(gate_up_swiglu<T>(c, w, R, nullptr, &act));
+      TRY(gemm<T>(c, act, c->F, w.w_down, c->F, c->gout, c->ldg, R, nullptr, d, c->F));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
           (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows,
                                       nullptr, c->sm)));
@@ -841,14 +869,9 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     TRY(gemm<T>(c, c->a_in, c->qdim, w.wo, c->qdim, c->gout, c->ldg, Rc, c->m_o, d, c->qdim));
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, c->o_src, c->m_o, Rc, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
                                c->a_in, c->sm)));
-    {
-      const void* Ws[2] = {w.w_gate, w.w_up};
-      const int Ns[2] = {c->F, c->F};
-      float* Cs[2] = {c->gout, c->gout + c->F};
-      TRY(gemm_multi<T>(c, c->a_in, d, 2, Ws, Ns, Cs, c->ldg, Rc, c->m_o, d));
-    }
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, c->m_o, Rc, c->F, c->a_in, c->sm)));
-    TRY(gemm<T>(c, c->a_in, c->F, w.w_down, c->F, c->gout, c->ldg, Rc, c->m_o, d, c->F));
+    const void* act = nullptr;
+    TRY(gate_up_swiglu<T>(c, w, Rc, c->m_o, &act));
+    TRY(gemm<T>(c, act, c->F, w.w_down, c->F, c->gout, c->ldg, Rc, c->m_o, d, c->F));
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
         (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows,
                                     c->U, c->sm, l + 1 < L ? c->W[l + 1].attn_norm : nullptr, eps, c->a_in)));
@@ -966,6 +989,7 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
     }
     TRY(dalloc(c, &c->a_in, c->esz * (size_t)R * std::max(std::max(d, c->F), c->qdim)));
+    if (c->bf16) TRY(dalloc(c, &c->act, 2 * (size_t)R * c->F));
     TRY(dalloc(c, &c->q_rows, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->attn_out, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->write_kv, (size_t)R));
@@ -1261,6 +1285,26 @@ extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const
   else
     launch_gemm_simt<float>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, st);
   return cudaGetLastError() == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
+extern "C" polestar_status polestar_debug_gemm_swiglu(const void* A, int32_t lda, const void* Wg, const void* Wu,
+                                                      int32_t ldw, void* act, int32_t ld_act, int32_t M,
+                                                      const int32_t* m_dev, int32_t F, int32_t K, int32_t path,
+                                                      void* stream) {
+  static TcGemmCache cache;
+  if (!A || !Wg || !Wu || !act || M < 0 || F < 1 || K < 1 || ld_act < F) return POLESTAR_ERR_INVALID_ARG;
+  const int kind = path & 0xFF;
+  if (kind != 1 && kind != 2) return POLESTAR_ERR_UNSUPPORTED;
+  if (!tc_gemm_supported(K, lda, ldw)) return POLESTAR_ERR_UNSUPPORTED;
+  TcGemmChoice force;
+  force.kernel = kind == 2 ? 1 : 0;
+  force.stages = (path >> 8) & 0xFF;
+  force.splits = (path >> 16) & 0xFF;
+  force.bn = ((path >> 24) & 0xFF) * 16;
+  const cudaError_t e = tc_gemm_bf16_swiglu(&cache, A, lda, Wg, Wu, ldw, F, act, ld_act, M, m_dev, K,
+                                            (cudaStream_t)stream, kind == 2 ? &force : nullptr);
+  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) return POLESTAR_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 
 extern "C" polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, const int32_t* N, int32_t K,

@@ -25,7 +25,7 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
             "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc",
             "polestar_packed_weight_bytes", "polestar_pack_weights", "polestar_debug_gemm_choice",
-            "polestar_debug_attention_impl")
+            "polestar_debug_attention_impl", "polestar_debug_gemm_swiglu")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
 
@@ -223,6 +223,24 @@ def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0) -> int
     CTA count (kernels 4, 5); bn the columns per tile of kernels 2 and 6 (a
     multiple of 16); 0 = automatic."""
     return kernel | (stages << 8) | (splits << 16) | ((bn // 16) << 24)
+
+
+def debug_gemm_swiglu(A, Wg, Wu, act, path: int = 1, m_dev=None, stream=None):
+    """act = bf16(silu(A Wg^T) * (A Wu^T)) through polestar_debug_gemm_swiglu;
+    torch CUDA tensors (A [M, K], Wg/Wu [F, K], act [M, >= F] bf16, unit inner
+    stride); path as gemm_path with kernel 1 (library) or 2 (row-tiled)."""
+    lib = load()
+    lib.polestar_debug_gemm_swiglu.argtypes = [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
+                                               C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
+                                               C.c_void_p]
+    lib.polestar_debug_gemm_swiglu.restype = C.c_int
+    import torch
+    st = stream if stream is not None else torch.cuda.current_stream()
+    M, K = A.shape
+    F = Wg.shape[0]
+    _check(lib.polestar_debug_gemm_swiglu(_ptr(A), A.stride(0), _ptr(Wg), _ptr(Wu), Wg.stride(0), _ptr(act),
+                                          act.stride(0), M, _ptr(m_dev) if m_dev is not None else None, F, K,
+                                          int(path), C.c_void_p(st.cuda_stream)))
 
 
 def attention_impl(impl: int) -> int:

@@ -239,3 +239,60 @@ def test_library_choice_is_valid_and_reproducible(M, Ns, K):
     P.debug_gemm(A, W, c2, path)
     torch.cuda.synchronize()
     assert torch.equal(c1, c2)
+
+
+def _swiglu_ref(A, Wg, Wu, rows):
+    a = A[rows].double().cpu().numpy()
+    g = a @ Wg.double().cpu().numpy().T
+    u = a @ Wu.double().cpu().numpy().T
+    return g / (1.0 + np.exp(-g)) * u
+
+
+# gate/up projections with the activation fused into the epilogue: library
+# choice and forced row-tiled configurations (direct epilogue, K split over a
+# cluster, ragged widths and rows)
+@pytest.mark.parametrize("path", [1, (176 // 16) << 24 | 2, (48 // 16) << 24 | (3 << 16) | 2,
+                                  (128 // 16) << 24 | (6 << 16) | 2, (256 // 16) << 24 | 2])
+@pytest.mark.parametrize("M,F,K", [(128, 12288, 4096), (136, 1376, 512), (7, 200, 448), (300, 1000, 1184)])
+def test_gate_up_swiglu_fused(path, M, F, K):
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cpu").manual_seed(M * 31 + F + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    Wg = (0.05 * torch.randn(F, K, generator=g)).to(torch.bfloat16).cuda()
+    Wu = (0.05 * torch.randn(F, K, generator=g)).to(torch.bfloat16).cuda()
+    act = torch.full((M, F + 8), float("nan"), dtype=torch.bfloat16, device="cuda")
+    try:
+        P.debug_gemm_swiglu(A, Wg, Wu, act, path)
+    except P.PolestarError:
+        if path == 1:
+            pytest.skip("library picks a kernel without the fused epilogue for this shape")
+        raise
+    torch.cuda.synchronize()
+    rows = np.arange(M) if M * F * K <= 2**31 else np.unique(np.linspace(0, M - 1, 48).astype(int))
+    ref = _swiglu_ref(A, Wg, Wu, rows)
+    got = act[rows, :F].double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    # bf16 output: half an ulp of bf16 plus the fp32 accumulation
+    assert np.all(np.abs(got - ref) <= 4e-3 * np.abs(ref) + 1e-4 * np.abs(ref).max()), np.abs(got - ref).max()
+    assert torch.isnan(act[:, F:].float()).all()  # nothing written past F
+
+
+def test_gate_up_swiglu_matches_unfused():
+    """The fused epilogue computes silu(g) * u from the same fp32 accumulators as
+    the unfused projections (same kernel, same tile width), so the results agree
+    to the bf16 rounding of the activation."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cpu").manual_seed(3)
+    M, F, K = 128, 4096, 4096
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    Wg = (0.02 * torch.randn(F, K, generator=g)).to(torch.bfloat16).cuda()
+    Wu = (0.02 * torch.randn(F, K, generator=g)).to(torch.bfloat16).cuda()
+    act = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+    path = (128 // 16) << 24 | 2  # row-tiled, 64 gate + 64 up columns per tile, no K split
+    P.debug_gemm_swiglu(A, Wg, Wu, act, path)
+    C = torch.empty(M, 2 * F, device="cuda")
+    P.debug_gemm(A, torch.cat([Wg, Wu]), C, P.gemm_path(2, 0, 1, 128))
+    torch.cuda.synchronize()
+    gg, uu = C[:, :F], C[:, F:]
+    ref = (gg / (1.0 + torch.exp(-gg)) * uu).to(torch.bfloat16)
+    assert (act.float() - ref.float()).abs().max().item() <= 2 ** -7 * ref.float().abs().max().item()
