@@ -80,7 +80,7 @@ struct polestar_ctx {
   float *h_rows = nullptr, *h1 = nullptr, *gout = nullptr, *kl_rows = nullptr;
   int num_sms = 148;
   void *a_in = nullptr, *q_rows = nullptr, *attn_out = nullptr;
-  void* act = nullptr;  // bf16 SwiGLU output of the fused gate/up projection [Rmax][F]
+  void* act = nullptr;  // bf16 SwiGLU output of the fused gate/up projection [<= 128][F]
   uint8_t* write_kv = nullptr;
   float *U = nullptr, *dn = nullptr;
   uint8_t *sel_a = nullptr, *sel_b = nullptr, *sel_last = nullptr;
@@ -989,7 +989,7 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
     }
     TRY(dalloc(c, &c->a_in, c->esz * (size_t)R * std::max(std::max(d, c->F), c->qdim)));
-    if (c->bf16) TRY(dalloc(c, &c->act, 2 * (size_t)R * c->F));
+    if (c->bf16) TRY(dalloc(c, &c->act, 2 * (size_t)std::min(R, 128) * c->F));  // fused path: <= 128 rows
     TRY(dalloc(c, &c->q_rows, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->attn_out, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->write_kv, (size_t)R));
