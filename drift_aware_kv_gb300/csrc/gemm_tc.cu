@@ -1287,11 +1287,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 
 // Loaders: one issuing warp keeps about one TMA box in flight (measured on
 // GB300: a warp completes one box per ~860 cycles from L2, whatever its size
-// and the ring depth), so up to four warps (p.nload) issue the k-steps.  Stage
+// and the ring depth), so two warps (p.nload = 1: A / W split) issue the k-steps.  Stage
 // s is always refilled by loader s % nload (the ring depth is a multiple of
 // nload), so each stage's uses are issued in order by one warp and its parity
 // waits never run more than one phase ahead of the barrier.
-constexpr int P2_LOADERS = 4;
+constexpr int P2_LOADERS = 2;
 constexpr int P2_THREADS = (6 + P2_LOADERS - 1) * 32;  // warps 0 and 6.. load, 1 MMA, 2-5 drain
 __global__ void __launch_bounds__(P2_THREADS, 1)
     gemm_p2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -1359,11 +1359,15 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
   const int nk = p.ktiles;
 
   if (warp == 0 || warp >= 6) {
-    // ---------------- TMA producers: loader j (warp 0, 6, 7, ...) issues the
-    // k-steps it with it % P2_LOADERS == j - own A rows and own half of the W
-    // tile - completing on the leader's stage barrier
+    // ---------------- TMA producers, completing on the leader's stage barrier.
+    // nload == 1: warp 0 issues every k-step's own A rows and warp 6 its own
+    // half of the W tile (two issuing threads, each in stage order).  nload >
+    // 1: loader j (warp 0, 6, 7, ...) issues both for the stages s with
+    // s % nload == j.
     const int lj = warp == 0 ? 0 : warp - 5;
-    if (lane == 0 && lj < p.nload) {
+    const bool split_ab = p.nload == 1;
+    const bool loads_a = !split_ab || warp == 0, loads_w = !split_ab || warp == 6;
+    if (lane == 0 && (split_ab ? (warp == 0 || warp == 6) : lj < p.nload)) {
       long long it = 0;
       bool live = true;
       for (long long t = cid; t < ntiles && live; t += ncl) {
@@ -1374,24 +1378,24 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         const int m0 = mp * 2 * BM + rank * BM;
         for (int k = 0; k < nk; ++k, ++it) {
           const int s = (int)(it % STAGES);
-          if (s % p.nload != lj) continue;
+          if (!split_ab && s % p.nload != lj) continue;
           if (it >= STAGES && !mbar_wait_cluster(smem_u32(&empty[s]), (uint32_t)((it / STAGES) - 1) & 1u, p.err, 1,
                                                  abort_flag)) {
             live = false;
             break;
           }
           const uint32_t fb_local = smem_u32(&full[s]);
-          if (rank == 0) mbar_expect_tx(fb_local, 2 * SB);
+          if (rank == 0 && loads_a) mbar_expect_tx(fb_local, 2 * SB);
           const uint32_t fb = map_to_rank(fb_local, 0);
           const uint32_t st = smem_u32(smem + (size_t)s * SB);
-          tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
-          tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
+          if (loads_a) tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
+          if (loads_w) tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
         }
       }
       // the last uses of this loader's stages must be read before this CTA may exit
       if (live)
         for (long long u = (it > STAGES ? it - STAGES : 0); u < it; ++u)
-          if ((int)(u % STAGES) % p.nload == lj &&
+          if ((split_ab || (int)(u % STAGES) % p.nload == lj) &&
               !mbar_wait_cluster(smem_u32(&empty[u % STAGES]), (uint32_t)(u / STAGES) & 1u, p.err, 4, abort_flag))
             break;
     }
@@ -1650,9 +1654,14 @@ int max_active_clusters(int smem, int cluster) {
 // plus 0.4 us per cluster split for the reduction.  (Measured on GB300 over the
 // projection shapes of the layer loop against forced sweeps of every
 // configuration: the pick is the fastest or within a few percent of it.)
-// Loader warps for a ring of `stages`: four, two or one, whichever divides it
-// (each loader owns the stages s = j mod n).
-int loaders_for(int stages) { return stages % 4 == 0 ? 4 : (stages % 2 == 0 ? 2 : 1); }
+// Loader warps for a ring of `stages`.  The kernels take up to four (each
+// owning the stages s = j mod n), but on GB300 more loaders measured no faster
+// and a few percent slower at the layer-loop shapes (and ring depths that are
+// multiples of four are common), so one warp issues every stage.
+int loaders_for(int stages) {
+  (void)stages;
+  return 1;
+}
 
 struct GemmPick {
   int kernel;  // 1 row-tiled, 2 weight-stationary, 5 two-SM pair tiles

@@ -426,7 +426,6 @@ constexpr int CU_THREADS = 256;
 
 template <typename T>
 __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a, int nc, int cw) {
-  pdl_enter();
   __shared__ float4 part[CU_THREADS][KM_MAXK];  // [row lane * groups + group][cluster]
   __shared__ float nrm_part[2][KM_MAXK], nrm_full[2][KM_MAXK];
   __shared__ float wsum[CU_THREADS / 32][KM_MAXK];
@@ -438,10 +437,15 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
   const int G = cw / 4;                              // channel groups of this CTA
   const int RL = G >= CU_THREADS ? 1 : CU_THREADS / G;  // row lanes sharing a group
   const int t = threadIdx.x;
-  for (int i = t; i < nw; i += CU_THREADS) {
-    sl[i] = a.sel_prev[s * a.Wmax + i];
-    lb[i] = a.labels[s * a.Wmax + i];
-  }
+  // inputs that no preceding kernel of the step writes (the block's labels, the
+  // norm gain) are read before waiting for the window patch
+  const T* gain = (const T*)a.gain;
+  const bool one_pass = G <= CU_THREADS;  // each thread finishes at most one channel group
+  float4 gv0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (one_pass && t < G) gv0 = cl_ld4t<T>(gain + c0 + t * 4);
+  for (int i = t; i < nw; i += CU_THREADS) lb[i] = a.labels[s * a.Wmax + i];
+  pdl_enter();
+  for (int i = t; i < nw; i += CU_THREADS) sl[i] = a.sel_prev[s * a.Wmax + i];
   __syncthreads();
   float* cs_base = a.csum + (size_t)s * K * d;
   float ssl[KM_MAXK];
@@ -457,17 +461,23 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
     float4 acc[KM_MAXK];
 #pragma unroll
     for (int c = 0; c < KM_MAXK; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // the member sums this thread will update, requested alongside the rows
+    float4 csv[KM_MAXK];
+#pragma unroll
+    for (int c = 0; c < KM_MAXK; ++c)
+      csv[c] = (act && rl == 0 && c < K) ? *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
     if (act) {
       const float* dn = a.dn + (size_t)s * a.Wmax * d + c0 + cg * 4;
-      for (int j0 = rl; j0 < nw; j0 += 8 * RL) {
-        float4 v[8];
+      for (int j0 = rl; j0 < nw; j0 += 16 * RL) {
+        float4 v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const int j = j0 + u * RL;
           v[u] = (j < nw && sl[j]) ? *(const float4*)(dn + (size_t)j * d) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const int j = j0 + u * RL;
           if (j >= nw || !sl[j]) continue;
           const int lab = lb[j];
@@ -510,7 +520,7 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
       for (int c = 0; c < KM_MAXK; ++c) {
         if (c >= K) continue;
         float* cs = cs_base + (size_t)c * d + c0 + cg * 4;
-        float4 v = *(const float4*)cs;
+        float4 v = csv[c];
         v.x += acc[c].x;
         v.y += acc[c].y;
         v.z += acc[c].z;
@@ -537,6 +547,7 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
   km_allreduce(&nrm_part[0][0], &nrm_full[0][0], KM_MAXK, nc);
   // z_c = s_c / |s_c| for this CTA's channels; sum of z^2 for the RMSNorm
   float zz[KM_MAXK];
+  float4 zkeep[KM_MAXK];  // one-pass layout: this thread's z group, reused for the projection input
 #pragma unroll
   for (int c = 0; c < KM_MAXK; ++c) zz[c] = 0.f;
   for (int cg = t; cg < G; cg += CU_THREADS) {
@@ -547,6 +558,7 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
       const float4 v = *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4);
       const float4 zv = make_float4(v.x / nrm, v.y / nrm, v.z / nrm, v.w / nrm);
       *(float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4) = zv;
+      zkeep[c] = zv;
       zz[c] += zv.x * zv.x + zv.y * zv.y + zv.z * zv.z + zv.w * zv.w;
     }
   }
@@ -563,12 +575,13 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
     nrm_part[1][t] = v;
   }
   km_allreduce(&nrm_part[1][0], &nrm_full[1][0], KM_MAXK, nc);
-  const T* gain = (const T*)a.gain;
   for (int cg = t; cg < G; cg += CU_THREADS) {
-    const float4 gv = cl_ld4t<T>(gain + c0 + cg * 4);
-    for (int c = 0; c < K; ++c) {
+    const float4 gv = one_pass ? gv0 : cl_ld4t<T>(gain + c0 + cg * 4);
+#pragma unroll
+    for (int c = 0; c < KM_MAXK; ++c) {
+      if (c >= K) continue;
       const float inv = 1.f / sqrtf(nrm_full[1][c] / (float)d + a.eps);
-      const float4 zv = *(const float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4);
+      const float4 zv = one_pass ? zkeep[c] : *(const float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4);
       T* ao = (T*)a.a_out + (size_t)(a.proxy_row[s] + c) * d + c0 + cg * 4;
       cl_st4t<T>(ao, make_float4(zv.x * inv * gv.x, zv.y * inv * gv.y, zv.z * inv * gv.z, zv.w * inv * gv.w));
     }
