@@ -1285,11 +1285,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   return true;
 }
 
-// Loaders: one issuing warp keeps about one TMA box in flight (measured on
-// GB300: a warp completes one box per ~860 cycles from L2, whatever its size
-// and the ring depth), so two warps (p.nload = 1: A / W split) issue the k-steps.  Stage
-// s is always refilled by loader s % nload (the ring depth is a multiple of
-// nload), so each stage's uses are issued in order by one warp and its parity
+// Loaders: two issuing warps.  p.nload == 1 (the default): warp 0 issues every
+// stage's A box and warp 6 its W half, each in stage order (one warp issuing
+// both measured 7 % slower at LLaDA-8B batch 8).  p.nload == 2: warp 0 / 6
+// issue both boxes of the stages s with s % 2 == 0 / 1 (the ring depth then
+// even), so each stage's uses are issued in order by one warp and its parity
 // waits never run more than one phase ahead of the barrier.
 constexpr int P2_LOADERS = 2;
 constexpr int P2_THREADS = (6 + P2_LOADERS - 1) * 32;  // warps 0 and 6.. load, 1 MMA, 2-5 drain
