@@ -65,6 +65,9 @@ struct Params {
   // act[row, col] = bf16(silu(g) * u) (row stride ld_act) instead of C
   __nv_bfloat16* act;
   int ld_act;
+  // two-SM pair kernel: 64-column k-blocks per stage (1, or 2 read by one 3D
+  // TMA box per operand: fewer, larger copies per issuing warp)
+  int kpack;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -1235,6 +1238,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void umma_pair(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
@@ -1298,9 +1309,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  constexpr int A_BYTES = BM * BK * 2;
-  const int STAGES = p.stages, bn = p.bn;
-  const int SB = p2_stage_bytes(bn);
+  constexpr int A_BLK = BM * BK * 2;  // one 64-column k-block of the A rows
+  const int STAGES = p.stages, bn = p.bn, KP = p.kpack;
+  const int B_BLK = (bn / 2) * BK * 2;  // one k-block of this CTA's W half
+  const int A_BYTES = KP * A_BLK;
+  const int SB = KP * p2_stage_bytes(bn);
   uint64_t* full = (uint64_t*)(smem + STAGES * SB);  // used in the leader
   uint64_t* empty = full + P2_MAX_STAGES;
   uint64_t* acc_full = empty + P2_MAX_STAGES;  // [2]
@@ -1356,7 +1369,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
   const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
   const int mpairs = (M_eff + 2 * BM - 1) / (2 * BM);
   const long long ntiles = *abort_flag ? 0 : (long long)mpairs * p.ntn;
-  const int nk = p.ktiles;
+  const int nk = (p.ktiles + KP - 1) / KP;  // stages per tile
 
   if (warp == 0 || warp >= 6) {
     // ---------------- TMA producers, completing on the leader's stage barrier.
@@ -1388,8 +1401,14 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
           if (rank == 0 && loads_a) mbar_expect_tx(fb_local, 2 * SB);
           const uint32_t fb = map_to_rank(fb_local, 0);
           const uint32_t st = smem_u32(smem + (size_t)s * SB);
-          if (loads_a) tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
-          if (loads_w) tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
+          if (KP == 1) {
+            if (loads_a) tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
+            if (loads_w) tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
+          } else {
+            // {column in the k-block, row, k-block}: KP consecutive k-blocks per box
+            if (loads_a) tma_load_3d_pair(st, &tmA, 0, m0, k * KP, fb);
+            if (loads_w) tma_load_3d_pair(st + A_BYTES, tmB, 0, n0 + rank * (bn / 2), k * KP, fb);
+          }
         }
       }
       // the last uses of this loader's stages must be read before this CTA may exit
@@ -1421,10 +1440,13 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t st = smem_u32(smem + (size_t)s * SB);
+#pragma unroll 1
+          for (int kb = 0; kb < KP; ++kb) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_pair(d, smem_desc(st + kk * 32), smem_desc(st + A_BYTES + kk * 32), idesc,
-                      (k > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_pair(d, smem_desc(st + kb * A_BLK + kk * 32), smem_desc(st + A_BYTES + kb * B_BLK + kk * 32), idesc,
+                        (k > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+          }
           umma_commit_pair(smem_u32(&empty[s]), PAIR);  // stage s free in both CTAs once read
         }
         if (live) umma_commit_pair(smem_u32(&acc_full[b]), PAIR);
@@ -1535,6 +1557,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
   }
   return fn;
+}
+
+// 3D view {column within a 64-column k-block, row, k-block} of a row-major
+// bf16 matrix: a box of `kblocks` k-blocks lands as that many consecutive
+// 128B-swizzled [box_rows][64] tiles (the same image as separate 2D boxes).
+const CUtensorMap* get_map3(TcGemmCache* cache, const void* ptr, int rows, int cols, int ld, int box_rows,
+                            int kblocks) {
+  const TcMapKey key{ptr, rows, cols, ld, box_rows | (kblocks << 16)};
+  auto it = cache->maps.find(key);
+  if (it != cache->maps.end()) return &it->second;
+  auto fn = encode_fn();
+  if (!fn) return nullptr;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  const cuuint64_t dims[3] = {(cuuint64_t)BK, (cuuint64_t)rows, (cuuint64_t)((cols + BK - 1) / BK)};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)BK * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, (cuuint32_t)kblocks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return nullptr;
+  return &cache->maps.emplace(key, m).first->second;
 }
 
 const CUtensorMap* get_map(TcGemmCache* cache, const void* ptr, int rows, int cols, int ld, int box_rows) {
@@ -1728,6 +1773,7 @@ GemmPick pick_small_m(int MT, int M, const int* N, int nseg, int ktiles, int nsm
 }
 
 int p2_default_stages(int bn);
+int p2_max_stages(int bn, int kpack);
 int p2_clusters(int bn, int stages, long long pair_tiles, int nsm);
 
 // More than 256 rows (several 256-row groups): the GEMM is bound by how fast
@@ -1739,19 +1785,22 @@ int p2_clusters(int bn, int stages, long long pair_tiles, int nsm);
 // + 2 us), and the row-tiled kernel at every column width, waves of one CTA
 // per SM x (k-steps x its step cost + 3 us), with a cluster K split of 2 or 4
 // costing another 12 us per wave for the reduction of the 256-row partials.
-GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm) {
+GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm, int K) {
   const int MT = 2, mgroups = (M + 2 * BM - 1) / (2 * BM);
   GemmPick best{1, 256, 1, rt_max_stages(MT, 256)};
   double tbest = 1e30;
+  // pair kernel: two k-blocks per stage (one 3D box per operand) when K is
+  // whole k-blocks, measured at 0.355 us per k-block against 0.415 with one
+  const int kp = (ktiles * BK == K) ? 2 : 1;
   for (int bn = 256; bn >= 192; bn -= 32) {
-    const int st = p2_default_stages(bn);
+    const int st = kp == 2 ? p2_max_stages(bn, 2) : p2_default_stages(bn);
     const long long tiles = (long long)mgroups * rt_tiles(N, nseg, bn);
     const int ncl = p2_clusters(bn, st, tiles, nsm);
     const long long waves = (tiles + ncl - 1) / ncl;
-    const double t = waves * (ktiles * 0.415 + 2.0);
+    const double t = waves * (ktiles * (kp == 2 ? 0.355 : 0.415) + 2.0);
     if (t < tbest * 0.999) {
       tbest = t;
-      best = GemmPick{5, bn, 1, st};
+      best = GemmPick{5, bn, kp, st};  // splits field: k-blocks per stage
     }
   }
   for (int s = 1; s <= 4; s *= 2) {
@@ -1785,8 +1834,12 @@ GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm) {
 // no two CTAs (each holding all 512 TMEM columns) ever share an SM - a second
 // one would block in its allocation while its pair partner waits for it.
 int pc_launch_smem(int bn, int stages) { return std::max(pc_smem_bytes(bn, stages), 233472 / 2 - 1024 + 16); }
-int p2_launch_smem(int bn, int stages) { return std::max(p2_smem_bytes(bn, stages), 233472 / 2 - 1024 + 16); }
-int p2_max_stages(int bn) { return std::min(P2_MAX_STAGES, (232448 - 2048) / p2_stage_bytes(bn)); }
+int p2_launch_smem(int bn, int stages, int kpack = 1) {
+  return std::max(kpack * p2_smem_bytes(bn, stages) - (kpack - 1) * 2048, 233472 / 2 - 1024 + 16);
+}
+int p2_max_stages(int bn, int kpack = 1) {
+  return std::min(P2_MAX_STAGES, (232448 - 2048) / (kpack * p2_stage_bytes(bn)));
+}
 // default ring depth: the deepest that fits (measured: depth, not loader
 // count, decides; 7 stages at bn = 256 beat 4 stages with four loaders)
 int p2_default_stages(int bn) { return p2_max_stages(bn); }
@@ -1809,7 +1862,7 @@ cudaError_t launch_p2(const CUtensorMap* a, const CUtensorMap* const* b, const P
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   cfg.blockDim = dim3(P2_THREADS);
-  cfg.dynamicSmemBytes = p2_launch_smem(p.bn, p.stages);
+  cfg.dynamicSmemBytes = p2_launch_smem(p.bn, p.stages, p.kpack);
   cfg.stream = st;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1987,7 +2040,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
       auto_splits = pk.splits;
       auto_stages = pk.stages;
     } else {
-      const GemmPick pk = pick_large_m(M, N, nseg, ktiles, nsm);
+      const GemmPick pk = pick_large_m(M, N, nseg, ktiles, nsm, K);
       kind = pk.kernel;
       bn = pk.bn;
       auto_splits = pk.splits;
@@ -1997,7 +2050,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     bn = force->bn;
     if (bn < 16 || bn > 256 || (bn & 15) || MT * bn > 512) return cudaErrorInvalidValue;
   } else if (kind == 1) {
-    bn = mgroups == 1 ? pick_small_m(MT, M, N, nseg, ktiles, nsm).bn : pick_large_m(M, N, nseg, ktiles, nsm).bn;
+    bn = mgroups == 1 ? pick_small_m(MT, M, N, nseg, ktiles, nsm).bn : pick_large_m(M, N, nseg, ktiles, nsm, K).bn;
   }
   const CUtensorMap* mb[3] = {nullptr, nullptr, nullptr};
   int tiles = 0;
@@ -2021,9 +2074,13 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     const GemmPick pk = pick_pc(M, N, nseg, nsm);
     p.bn = force && force->bn ? force->bn : (auto_stages ? bn : (two_sm ? 256 : pk.bn));
     if (p.bn < 16 || p.bn > 256 || (p.bn & 15)) return cudaErrorInvalidValue;
-    const int max_stages =
-        two_sm ? p2_max_stages(p.bn) : std::min(PC_MAX_STAGES, (232448 - 2048) / pc_stage_bytes(p.bn));
-    const int def_stages = two_sm ? p2_default_stages(p.bn) : max_stages;
+    // two-SM kernel: k-blocks per stage (forced through the split field)
+    p.kpack = !two_sm ? 1 : (force && force->kernel == 5 && force->splits ? force->splits : (auto_splits ? auto_splits : 1));
+    // the 3D view has no out-of-range fill inside a k-block: whole k-blocks only
+    if (p.kpack < 1 || p.kpack > 2 || (p.kpack > 1 && K % BK)) return cudaErrorInvalidValue;
+    const int max_stages = two_sm ? p2_max_stages(p.bn, p.kpack)
+                                  : std::min(PC_MAX_STAGES, (232448 - 2048) / pc_stage_bytes(p.bn));
+    const int def_stages = two_sm ? (p.kpack == 1 ? p2_default_stages(p.bn) : max_stages) : max_stages;
     p.stages = force && force->stages ? force->stages : (auto_stages ? auto_stages : def_stages);
     if (p.stages < 2 || p.stages > max_stages) return cudaErrorInvalidValue;
     p.splits = 1;
@@ -2034,7 +2091,8 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     for (int sgi = 0, t = 0; sgi < 3; ++sgi) {
       p.seg_start[sgi] = sgi < nseg ? t : 0x3FFFFFFF;
       if (sgi < nseg) {
-        mb[sgi] = get_map(cache, W[sgi], N[sgi], K, ldw[sgi], p.bn / 2);
+        mb[sgi] = p.kpack == 1 ? get_map(cache, W[sgi], N[sgi], K, ldw[sgi], p.bn / 2)
+                               : get_map3(cache, W[sgi], N[sgi], K, ldw[sgi], p.bn / 2, p.kpack);
         if (!mb[sgi]) return cudaErrorInvalidValue;
         t += (N[sgi] + p.bn - 1) / p.bn;
       }
@@ -2042,7 +2100,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
     const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * p.ntn;
     const int ncl = two_sm ? p2_clusters(p.bn, p.stages, pair_tiles, nsm) : pc_clusters(p.bn, p.stages, pair_tiles, nsm);
-    const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
+    const CUtensorMap* ma = p.kpack == 1 ? get_map(cache, A, M, K, lda, BM) : get_map3(cache, A, M, K, lda, BM, p.kpack);
     if (!ma) return cudaErrorInvalidValue;
     return two_sm ? launch_p2(ma, mb, p, ncl, st) : launch_pc(ma, mb, p, ncl, st);
   }
@@ -2154,7 +2212,7 @@ cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, cons
     pk.splits = force->splits ? force->splits : 1;
     pk.stages = force->stages;
   } else {
-    pk = mgroups == 1 ? pick_small_m(MT, M, Ns, 2, ktiles, nsm) : pick_large_m(M, Ns, 2, ktiles, nsm);
+    pk = mgroups == 1 ? pick_small_m(MT, M, Ns, 2, ktiles, nsm) : pick_large_m(M, Ns, 2, ktiles, nsm, K);
     if (pk.kernel != 1) return cudaErrorNotSupported;  // only the row-tiled kernel fuses the activation
   }
   const int bn = pk.bn ? pk.bn : (mgroups == 1 ? pick_small_m(MT, M, Ns, 2, ktiles, nsm).bn : 256);
@@ -2217,7 +2275,7 @@ cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, in
   const int MT = M > BM ? 2 : 1;
   const int mgroups = (M + MT * BM - 1) / (MT * BM);
   const int ktiles = (K + BK - 1) / BK;
-  const GemmPick pk = mgroups > 1 ? tc::pick_large_m(M, N, nseg, ktiles, cache->num_sms)
+  const GemmPick pk = mgroups > 1 ? tc::pick_large_m(M, N, nseg, ktiles, cache->num_sms, K)
                                   : tc::pick_small_m(MT, M, N, nseg, ktiles, cache->num_sms);
   out[0] = pk.kernel;
   out[1] = pk.bn;

@@ -201,7 +201,9 @@ polestar_status polestar_profile_end(polestar_ctx *ctx, polestar_kernel_stats *o
  * then ignored).  Paths 6 and 7: persistent pair-tile kernels (clusters of
  * two CTAs walk 256-row x bn-column output tiles; any M): 6 multicasts each
  * weight tile into both CTAs, 7 runs the pair's tensor cores as one MMA
- * (cta_group::2) on each CTA's half; bits 8-15 the ring depth.  A combination the kernel cannot
+ * (cta_group::2) on each CTA's half; bits 8-15 the ring depth, for path 7
+ * bits 16-23 the 64-column k-blocks per stage (1, or 2 loaded by one 3D TMA
+ * box per operand; K must then be a multiple of 64).  A combination the kernel cannot
  * run (too much shared memory, more than 8 splits, more CTAs than SMs)
  * returns UNSUPPORTED.
  * m_dev (device int, may be NULL) lowers the row count on the device: rows at
@@ -228,8 +230,8 @@ polestar_status polestar_debug_gemm_swiglu(const void *A, int32_t lda, const voi
  * For M rows (bf16 tensor-core path), nseg (1..3) weight segments with N[i]
  * (host array) output columns and inner size K: out[4] (host) = {kernel: 1
  * row-tiled, 2 weight-stationary, 5 two-SM pair tiles (path 7 of
- * polestar_debug_gemm); output columns per tile; K split over a cluster; ring
- * depth}.  Queries the current device's
+ * polestar_debug_gemm); output columns per tile; K split over a cluster (for
+ * kernel 5: k-blocks per stage); ring depth}.  Queries the current device's
  * occupancy; launches nothing.  CUDA error (no device) when no device is
  * visible. */
 polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, const int32_t *N, int32_t K, int32_t *out);

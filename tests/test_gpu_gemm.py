@@ -296,3 +296,20 @@ def test_gate_up_swiglu_matches_unfused():
     gg, uu = C[:, :F], C[:, F:]
     ref = (gg / (1.0 + torch.exp(-gg)) * uu).to(torch.bfloat16)
     assert (act.float() - ref.float()).abs().max().item() <= 2 ** -7 * ref.float().abs().max().item()
+
+
+# two-SM pair kernel with two k-blocks per stage (one 3D TMA box per operand)
+@pytest.mark.parametrize("bn,stages", [(256, 0), (192, 2), (128, 3)])
+@pytest.mark.parametrize("M,N,K", [(2560, 4096, 4096), (700, 1000, 1408), (513, 12288, 4096), (1, 96, 128)])
+def test_two_sm_pair_two_kblocks(bn, stages, M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    _check_gemm(P.gemm_path(7, stages, 2, bn), M, N, K)
+
+
+def test_two_kblock_stages_need_whole_kblocks():
+    from drift_aware_kv_gb300 import polestar as P
+    A = torch.zeros(300, 100, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(256, 100, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(300, 256, device="cuda")
+    with pytest.raises(P.PolestarError):
+        P.debug_gemm(A, W, C, P.gemm_path(7, 0, 2, 256))  # K = 100 is not a multiple of 64
