@@ -115,6 +115,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   uint64_t d = 0;
@@ -221,9 +229,12 @@ __global__ void __launch_bounds__(THREADS)
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  constexpr int A_BYTES = BM * BK * 2;  // 16 KB per row sub-tile
+  constexpr int A_BLK = BM * BK * 2;  // 16 KB: one row sub-tile x one 64-column k-block
   const int bn = p.bn, STAGES = p.stages;
-  const int STAGE_BYTES = rt_stage_bytes(MT, bn);
+  const int KP = p.kpack > 1 ? p.kpack : 1;  // k-blocks per stage (KP > 1: one 3D box per operand)
+  const int A_BYTES = KP * A_BLK;            // one row sub-tile's k-blocks of a stage
+  const int W_BLK = bn * BK * 2;             // one k-block of the W tile
+  const int STAGE_BYTES = KP * rt_stage_bytes(MT, bn);
   const int pitch = bn + 4;             // fp32 staging row pitch of the split-K reduction
   uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + RT_MAX_STAGES;
@@ -243,18 +254,26 @@ __global__ void __launch_bounds__(THREADS)
   const int split = blockIdx.z;
   // W tile of a stage: one bn-row box, or in SwiGLU mode the gate and up boxes
   // of bn/2 rows each (the up half at row bn/2 of the tile)
-  auto load_w = [&](uint32_t dst, int kx, uint32_t bar) {
+  auto load_w = [&](uint32_t dst, int kb, uint32_t bar) {
     if (glu) {
-      tma_load_2d(dst, &tmB0, kx, n0, bar);
-      tma_load_2d(dst + (bn / 2) * 128, &tmB1, kx, n0, bar);
+      tma_load_2d(dst, &tmB0, kb * BK, n0, bar);
+      tma_load_2d(dst + (bn / 2) * 128, &tmB1, kb * BK, n0, bar);
+    } else if (KP == 1) {
+      tma_load_2d(dst, tmB, kb * BK, n0, bar);
     } else {
-      tma_load_2d(dst, tmB, kx, n0, bar);
+      tma_load_3d(dst, tmB, 0, n0, kb, bar);
     }
+  };
+  auto load_a = [&](uint32_t dst, int kb, int row, uint32_t bar) {
+    if (KP == 1)
+      tma_load_2d(dst, &tmA, kb * BK, row, bar);
+    else
+      tma_load_3d(dst, &tmA, 0, row, kb, bar);
   };
 
   const int kt0 = (int)((long long)split * p.ktiles / p.splits);
   const int kt1 = (int)((long long)(split + 1) * p.ktiles / p.splits);
-  const int nk = kt1 - kt0;
+  const int nk = (kt1 - kt0 + KP - 1) / KP;  // stages of this CTA's K range
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -289,7 +308,7 @@ __global__ void __launch_bounds__(THREADS)
     for (int i = lj; i < npre; i += p.nload) {
       const uint32_t fb = smem_u32(&full[i]);
       mbar_expect_tx(fb, STAGE_BYTES);
-      load_w(smem_u32(smem + i * STAGE_BYTES) + MT * A_BYTES, (kt0 + i) * BK, fb);
+      load_w(smem_u32(smem + i * STAGE_BYTES) + MT * A_BYTES, kt0 + i * KP, fb);
     }
   }
   pdl_launch_dependents();
@@ -300,9 +319,8 @@ __global__ void __launch_bounds__(THREADS)
     // ---------------- TMA producers
     for (int i = lj; i < npre; i += p.nload) {
       const uint32_t st = smem_u32(smem + i * STAGE_BYTES);
-      const int kx = (kt0 + i) * BK;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, smem_u32(&full[i]));
+      for (int mt = 0; mt < MT; ++mt) load_a(st + mt * A_BYTES, kt0 + i * KP, m0 + mt * BM, smem_u32(&full[i]));
     }
     for (int i = npre; i < nk; ++i) {
       const int s = i % STAGES;
@@ -311,10 +329,10 @@ __global__ void __launch_bounds__(THREADS)
       const uint32_t fb = smem_u32(&full[s]);
       mbar_expect_tx(fb, STAGE_BYTES);
       const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-      const int kx = (kt0 + i) * BK;
+      const int kb = kt0 + i * KP;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * A_BYTES, &tmA, kx, m0 + mt * BM, fb);
-      load_w(st + MT * A_BYTES, kx, fb);
+      for (int mt = 0; mt < MT; ++mt) load_a(st + mt * A_BYTES, kb, m0 + mt * BM, fb);
+      load_w(st + MT * A_BYTES, kb, fb);
     }
   }
   if (warp == 1) {
@@ -327,12 +345,18 @@ __global__ void __launch_bounds__(THREADS)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
         const uint32_t bst = st + MT * A_BYTES;
+        // k-blocks of this stage inside this CTA's K range (a stage past the
+        // range's end holds blocks of the next split: not multiplied)
+        const int nkb = min(KP, kt1 - (kt0 + i * KP));
+#pragma unroll 1
+        for (int kb = 0; kb < nkb; ++kb) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
+          for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            umma_id(tmem + mt * bn, smem_desc(st + mt * A_BYTES + kk * 32), smem_desc(bst + kk * 32), idesc,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              umma_id(tmem + mt * bn, smem_desc(st + mt * A_BYTES + kb * A_BLK + kk * 32),
+                      smem_desc(bst + kb * W_BLK + kk * 32), idesc, (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+            }
           }
         }
         umma_commit(smem_u32(&empty[s]));  // frees the stage once these MMAs have read it
@@ -1612,7 +1636,8 @@ cudaError_t launch_rt(const CUtensorMap* a, const CUtensorMap* const* b, const P
   }
   // at most 512 / tmem_cols CTAs may share an SM (see launch_ws)
   const int resident = 512 / p.tmem_cols;
-  const int smem = std::max(rt_smem_bytes(MT, p.bn, p.stages), 233472 / (resident + 1) - 1024 + 16);
+  const int kp = p.kpack > 1 ? p.kpack : 1;
+  const int smem = std::max(kp * p.stages * rt_stage_bytes(MT, p.bn) + 2048, 233472 / (resident + 1) - 1024 + 16);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(THREADS);
@@ -2172,14 +2197,25 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   if (splits < 1 || splits > 8) return cudaErrorInvalidValue;
   p.bn = bn;
   p.splits = splits;
-  p.stages = force && force->stages ? force->stages : rt_max_stages(MT, bn);
-  if (p.stages < 2 || p.stages > RT_MAX_STAGES || rt_smem_bytes(MT, bn, p.stages) > 232448 ||
-      (splits > 1 && p.stages * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4))
+  // k-blocks per stage: 2 reads each operand with one 3D box per stage (whole
+  // k-blocks of K only)
+  p.kpack = force && force->kpack ? force->kpack : 1;
+  if (p.kpack < 1 || p.kpack > 2 || (p.kpack > 1 && K % BK)) return cudaErrorInvalidValue;
+  const int rt_max_st = std::min(RT_MAX_STAGES, (232448 - 2048) / (p.kpack * rt_stage_bytes(MT, bn)));
+  p.stages = force && force->stages ? force->stages : rt_max_st;
+  if (p.stages < 2 || p.stages > rt_max_st ||
+      (splits > 1 && p.kpack * p.stages * rt_stage_bytes(MT, bn) < BM * (bn + 4) * 4))
     return cudaErrorInvalidValue;
   p.tmem_cols = 32;
   while (p.tmem_cols < MT * bn) p.tmem_cols *= 2;
   p.nload = loaders_for(p.stages);
-  const CUtensorMap* ma = get_map(cache, A, M, K, lda, BM);
+  if (p.kpack > 1)
+    for (int sgi = 0; sgi < nseg; ++sgi) {
+      mb[sgi] = get_map3(cache, W[sgi], N[sgi], K, ldw[sgi], bn, p.kpack);
+      if (!mb[sgi]) return cudaErrorInvalidValue;
+    }
+  for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
+  const CUtensorMap* ma = p.kpack > 1 ? get_map3(cache, A, M, K, lda, BM, p.kpack) : get_map(cache, A, M, K, lda, BM);
   if (!ma) return cudaErrorInvalidValue;
   const dim3 grid(tiles, mgroups, splits);
   return MT == 2 ? launch_rt<2>(ma, mb, p, grid, st) : launch_rt<1>(ma, mb, p, grid, st);

@@ -54,6 +54,7 @@ struct TcGemmChoice {
   int stages = 0;
   int splits = 0;
   int bn = 0;
+  int kpack = 0;  // row-tiled kernel: 64-column k-blocks per stage (0 = 1)
 };
 
 // True when the tensor-core path handles this shape: leading dimensions must

@@ -1266,11 +1266,12 @@ extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const
   static TcGemmCache cache;
   if (!A || !W || !C || M < 0 || N < 1 || K < 1) return POLESTAR_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  const int kind = path & 0xFF;
+  const int kind = path & 0xF;
   if (kind >= 1 && kind <= 7) {
     if (dtype != POLESTAR_BF16 || !tc_gemm_supported(K, lda, kind == 5 ? K : ldw)) return POLESTAR_ERR_UNSUPPORTED;
     TcGemmChoice force;
     force.kernel = kind == 5 ? 3 : (kind >= 6 ? kind - 2 : kind - 1);
+    force.kpack = (path >> 4) & 0xF;
     force.stages = (path >> 8) & 0xFF;
     force.splits = (path >> 16) & 0xFF;
     force.bn = ((path >> 24) & 0xFF) * 16;

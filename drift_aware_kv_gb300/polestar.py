@@ -214,15 +214,16 @@ class Polestar:
                 for name, a in zip(KERNEL_CLASSES, arr)}
 
 
-def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0) -> int:
+def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0, kpack: int = 0) -> int:
     """`path` of polestar_debug_gemm: kernel 0 CUDA cores, 1 tcgen05 (library's
     choice), 2 row-tiled tcgen05, 3 weight-stationary tcgen05, 4 persistent
     stream-K weight-stationary tcgen05 (5: the same on packed weights), 6
     persistent pair tiles (two-CTA clusters sharing each weight tile); stages /
     splits override the ring depth and the cluster K split (kernels 2, 3) or the
     CTA count (kernels 4, 5); bn the columns per tile of kernels 2 and 6 (a
-    multiple of 16); 0 = automatic."""
-    return kernel | (stages << 8) | (splits << 16) | ((bn // 16) << 24)
+    multiple of 16); kpack the 64-column k-blocks per stage of kernel 2 (1 or 2);
+    0 = automatic."""
+    return kernel | (kpack << 4) | (stages << 8) | (splits << 16) | ((bn // 16) << 24)
 
 
 def debug_gemm_swiglu(A, Wg, Wu, act, path: int = 1, m_dev=None, stream=None):

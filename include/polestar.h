@@ -196,7 +196,9 @@ polestar_status polestar_profile_end(polestar_ctx *ctx, polestar_kernel_stats *o
  * weight-stationary (M <= 256) tcgen05 kernel, with bits 8-15 of `path`
  * giving the ring depth and bits 16-23 the K split over a cluster (paths 2
  * and 3) or the number of CTAs (paths 4, 5), and bits 24-31 the columns per
- * tile of paths 2 and 6 in units of 16; 0 = automatic.  Path 5 is path 4
+ * tile of paths 2 and 6 in units of 16; bits 4-7 the 64-column k-blocks per
+ * stage of path 2 (1, or 2 loaded by one 3D TMA box per operand, K a multiple
+ * of 64); 0 = automatic.  Path 5 is path 4
  * with W given in the packed tile layout of polestar_pack_weights (ldw is
  * then ignored).  Paths 6 and 7: persistent pair-tile kernels (clusters of
  * two CTAs walk 256-row x bn-column output tiles; any M): 6 multicasts each

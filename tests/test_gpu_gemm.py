@@ -313,3 +313,20 @@ def test_two_kblock_stages_need_whole_kblocks():
     C = torch.zeros(300, 256, device="cuda")
     with pytest.raises(P.PolestarError):
         P.debug_gemm(A, W, C, P.gemm_path(7, 0, 2, 256))  # K = 100 is not a multiple of 64
+
+
+# row-tiled kernel with two k-blocks per stage: K splits whose ranges end inside
+# a stage (odd k-block counts), one and two row sub-tiles
+@pytest.mark.parametrize("bn,splits,stages", [(176, 1, 0), (128, 3, 0), (208, 6, 2), (256, 2, 0), (48, 8, 0)])
+@pytest.mark.parametrize("M,N,K", [(100, 1000, 1344), (200, 4608, 2048), (33, 384, 4096), (128, 24576, 4096)])
+def test_row_tiled_two_kblocks(bn, splits, stages, M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    mt = 2 if M > 128 else 1
+    stage = 2 * (mt * 128 * 64 * 2 + bn * 64 * 2)  # two k-blocks of the A sub-tiles and the W tile
+    max_stages = min(8, (232448 - 2048) // stage)
+    st = stages or max_stages
+    if st < 2 or st > max_stages or (splits > 1 and st * stage < 128 * (bn + 4) * 4):
+        with pytest.raises(P.PolestarError):  # does not fit in shared memory
+            _check_gemm(P.gemm_path(2, stages, splits, bn, kpack=2), M, N, K)
+        return
+    _check_gemm(P.gemm_path(2, stages, splits, bn, kpack=2), M, N, K)
