@@ -51,7 +51,12 @@ def bench_gemm(a):
         it[0] = (it[0] + 1) % ncopy
         return Ws[it[0]]
 
-    if a.cublas:  # library comparison point (cuBLAS through torch), not a path of the product
+    if getattr(a, "swiglu", False):
+        # gate and up halves of each weight copy, SwiGLU fused into the epilogue
+        F = a.N // 2
+        act = torch.empty(a.M, F, dtype=torch.bfloat16, device="cuda")
+        ms = _time(lambda: (lambda W: P.debug_gemm_swiglu(A, W[:F], W[F:], act, 1))(nxt()), a.iters)
+    elif a.cublas:  # library comparison point (cuBLAS through torch), not a path of the product
         ms = _time(lambda: torch.matmul(A, nxt().t()), a.iters)
     else:
         if a.path == 5:  # weights in the packed tile layout
@@ -103,6 +108,8 @@ def main():
                          "3 weight-stationary tcgen05, 4 stream-K weight-stationary tcgen05, "
                          "5 stream-K on packed weights")
     ap.add_argument("--cublas", action="store_true", help="time cuBLAS (through torch) instead: comparison point")
+    ap.add_argument("--swiglu", action="store_true",
+                    help="gate/up projection with the SwiGLU activation fused (N = 2F: gate and up halves)")
     ap.add_argument("--stages", type=int, default=0, help="tcgen05 ring depth (0 = library's choice)")
     ap.add_argument("--bn", type=int, default=0, help="row-tiled columns per tile (0 = library's choice)")
     ap.add_argument("--splits", type=int, default=0,
