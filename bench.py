@@ -207,9 +207,14 @@ def run_device(args, w, peaks, ws, rank, local):
         clk.start()
         t0 = time.perf_counter()
         ev[0].record(stream)
+        issue_first = None
         for i, st in enumerate(timed):
             do_step(st)
             ev[i + 1].record(stream)
+            if issue_first is None:
+                # host time to enqueue one step into an empty queue (later
+                # steps' enqueue times are bounded by the GPU once it fills)
+                issue_first = time.perf_counter() - t0
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
         barrier(ws)
@@ -220,7 +225,7 @@ def run_device(args, w, peaks, ws, rank, local):
         total_ms = ev[0].elapsed_time(ev[-1])
         ps.close()
         return dict(stats=stats, launches=launches, step_ms=step_ms, total_ms=total_ms, wall=wall,
-                    clocks=clocks)
+                    clocks=clocks, issue_first=issue_first)
 
     main = region(profile=False)
     prof = region(profile=True)
@@ -301,6 +306,8 @@ def run_device(args, w, peaks, ws, rank, local):
         "kernel_launches": {k: v["launches"] for k, v in stats.items()},
         "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
         "wall_s": wall,
+        "host_issue_ms_first_step": main["issue_first"] * 1e3,
+        "first_step_block_entry": bool(timed[0]["block_entry"]),
     }
     return out
 

@@ -1855,6 +1855,19 @@ GemmPick pick_large_m(int M, const int* N, int nseg, int ktiles, int nsm, int K)
 }
 
 
+// The automatic choice for M rows (one row group: pick_small_m, else
+// pick_large_m), memoised per shape in the context's cache.
+GemmPick pick_for(TcGemmCache* cache, int M, const int* N, int nseg, int ktiles, int nsm, int K) {
+  const std::array<int, 7> key{M, K, nseg, N[0], nseg > 1 ? N[1] : 0, nseg > 2 ? N[2] : 0, nsm};
+  auto it = cache->picks.find(key);
+  if (it != cache->picks.end()) return GemmPick{it->second[0], it->second[1], it->second[2], it->second[3]};
+  const int MT = M > BM ? 2 : 1;
+  const int mgroups = (M + MT * BM - 1) / (MT * BM);
+  const GemmPick pk = mgroups > 1 ? pick_large_m(M, N, nseg, ktiles, nsm, K) : pick_small_m(MT, M, N, nseg, ktiles, nsm);
+  cache->picks.emplace(key, std::array<int, 4>{pk.kernel, pk.bn, pk.splits, pk.stages});
+  return pk;
+}
+
 // Dynamic shared memory of a persistent pair CTA: at least half an SM's, so
 // no two CTAs (each holding all 512 TMEM columns) ever share an SM - a second
 // one would block in its allocation while its pair partner waits for it.
@@ -2059,13 +2072,13 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   int bn = BN, auto_splits = 0, auto_stages = 0;
   if (kind == 0) {
     if (mgroups == 1) {
-      const GemmPick pk = pick_small_m(MT, M, N, nseg, ktiles, nsm);
+      const GemmPick pk = pick_for(cache, M, N, nseg, ktiles, nsm, K);
       kind = pk.kernel;
       bn = pk.bn;
       auto_splits = pk.splits;
       auto_stages = pk.stages;
     } else {
-      const GemmPick pk = pick_large_m(M, N, nseg, ktiles, nsm, K);
+      const GemmPick pk = pick_for(cache, M, N, nseg, ktiles, nsm, K);
       kind = pk.kernel;
       bn = pk.bn;
       auto_splits = pk.splits;
@@ -2075,7 +2088,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     bn = force->bn;
     if (bn < 16 || bn > 256 || (bn & 15) || MT * bn > 512) return cudaErrorInvalidValue;
   } else if (kind == 1) {
-    bn = mgroups == 1 ? pick_small_m(MT, M, N, nseg, ktiles, nsm).bn : pick_large_m(M, N, nseg, ktiles, nsm, K).bn;
+    bn = pick_for(cache, M, N, nseg, ktiles, nsm, K).bn;
   }
   const CUtensorMap* mb[3] = {nullptr, nullptr, nullptr};
   int tiles = 0;
@@ -2248,10 +2261,10 @@ cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, cons
     pk.splits = force->splits ? force->splits : 1;
     pk.stages = force->stages;
   } else {
-    pk = mgroups == 1 ? pick_small_m(MT, M, Ns, 2, ktiles, nsm) : pick_large_m(M, Ns, 2, ktiles, nsm, K);
+    pk = pick_for(cache, M, Ns, 2, ktiles, nsm, K);
     if (pk.kernel != 1) return cudaErrorNotSupported;  // only the row-tiled kernel fuses the activation
   }
-  const int bn = pk.bn ? pk.bn : (mgroups == 1 ? pick_small_m(MT, M, Ns, 2, ktiles, nsm).bn : 256);
+  const int bn = pk.bn ? pk.bn : (mgroups == 1 ? pick_for(cache, M, Ns, 2, ktiles, nsm, K).bn : 256);
   if (bn < 16 || bn > 256 || (bn & 15) || MT * bn > 512) return cudaErrorInvalidValue;
   Params p{};
   p.M = M;
@@ -2308,11 +2321,8 @@ cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, in
       return cudaErrorNoDevice;
     }
   }
-  const int MT = M > BM ? 2 : 1;
-  const int mgroups = (M + MT * BM - 1) / (MT * BM);
   const int ktiles = (K + BK - 1) / BK;
-  const GemmPick pk = mgroups > 1 ? tc::pick_large_m(M, N, nseg, ktiles, cache->num_sms, K)
-                                  : tc::pick_small_m(MT, M, N, nseg, ktiles, cache->num_sms);
+  const GemmPick pk = tc::pick_for(cache, M, N, nseg, ktiles, cache->num_sms, K);
   out[0] = pk.kernel;
   out[1] = pk.bn;
   out[2] = pk.splits;

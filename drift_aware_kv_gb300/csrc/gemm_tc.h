@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <array>
+#include <map>
 #include <unordered_map>
 
 namespace polestar {
@@ -37,6 +39,9 @@ struct TcGemmCache {
   int num_sms = 0;
   float* work = nullptr;
   int* counters = nullptr;
+  // automatic launch choices by shape {M, K, segments, N0, N1, N2, SMs} ->
+  // {kernel, bn, splits, stages}: the search runs once per shape
+  std::map<std::array<int, 7>, std::array<int, 4>> picks;
 };
 
 // Kernel choice for tuning sweeps and tests; zero fields are chosen

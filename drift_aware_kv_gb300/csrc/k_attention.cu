@@ -237,9 +237,15 @@ cudaError_t launch_row_attention(const AttnArgs& a, cudaStream_t st) {
   if (sizeof(T) == 2 && a.work && a.item_rows == ATT_TC_ROWS) return launch_attention_tc(a, a.batch, st);
   if (sizeof(T) == 2 && a.work) {
     AttnArgs b = a;
-    int nsm = 0, dev = 0;
+    // SM count per device, queried once (a driver query per launch costs host time)
+    static int nsm_of[64] = {0};
+    int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    int nsm = dev >= 0 && dev < 64 ? nsm_of[dev] : 0;
+    if (nsm <= 0) {
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+      if (dev >= 0 && dev < 64) nsm_of[dev] = nsm;
+    }
     b.splits = attention_pipe_config(a.n_work, a.H, a.N, a.dh, nsm, &b.stages);
     return launch_attention_pipe(b, a.batch, st);
   }

@@ -607,7 +607,11 @@ template <typename T>
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st) {
   const int nc = centroid_cluster_size(a.d);
   const int cw = a.d / nc;
-  if (nc > 8) cudaFuncSetAttribute(centroid_update_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  static bool nonportable = false;  // set once per instantiation (a driver call per launch costs host time)
+  if (nc > 8 && !nonportable) {
+    cudaFuncSetAttribute(centroid_update_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    nonportable = true;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(nc, a.n_fire);
   cfg.blockDim = dim3(CU_THREADS);
