@@ -427,7 +427,7 @@ constexpr int CU_THREADS = 256;
 template <typename T>
 __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a, int nc, int cw) {
   __shared__ float4 part[CU_THREADS][KM_MAXK];  // [row lane * groups + group][cluster]
-  __shared__ float nrm_part[2][KM_MAXK], nrm_full[2][KM_MAXK];
+  __shared__ float nrm_part[1][KM_MAXK], nrm_full[1][KM_MAXK];
   __shared__ float wsum[CU_THREADS / 32][KM_MAXK];
   __shared__ uint8_t sl[KM_MAXW], lb[KM_MAXW];
   const int rank = (int)km_rank();
@@ -449,6 +449,7 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
   __syncthreads();
   float* cs_base = a.csum + (size_t)s * K * d;
   float ssl[KM_MAXK];
+  float4 ckeep[KM_MAXK];  // one-pass layout: this thread's updated member sums, reused for z
 #pragma unroll
   for (int c = 0; c < KM_MAXK; ++c) ssl[c] = 0.f;
   // RL > 1: one pass, thread t = lane rl * G + group cg.  RL == 1: group
@@ -526,6 +527,7 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
         v.z += acc[c].z;
         v.w += acc[c].w;
         *(float4*)cs = v;
+        ckeep[c] = v;
         ssl[c] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
       }
     }
@@ -545,43 +547,19 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
     nrm_part[0][t] = v;
   }
   km_allreduce(&nrm_part[0][0], &nrm_full[0][0], KM_MAXK, nc);
-  // z_c = s_c / |s_c| for this CTA's channels; sum of z^2 for the RMSNorm
-  float zz[KM_MAXK];
-  float4 zkeep[KM_MAXK];  // one-pass layout: this thread's z group, reused for the projection input
-#pragma unroll
-  for (int c = 0; c < KM_MAXK; ++c) zz[c] = 0.f;
-  for (int cg = t; cg < G; cg += CU_THREADS) {
-#pragma unroll
-    for (int c = 0; c < KM_MAXK; ++c) {
-      if (c >= K) continue;
-      const float nrm = sqrtf(nrm_full[0][c]);
-      const float4 v = *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4);
-      const float4 zv = make_float4(v.x / nrm, v.y / nrm, v.z / nrm, v.w / nrm);
-      *(float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4) = zv;
-      zkeep[c] = zv;
-      zz[c] += zv.x * zv.x + zv.y * zv.y + zv.z * zv.z + zv.w * zv.w;
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < KM_MAXK; ++c) {
-    float v = zz[c];
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) wsum[wid][c] = v;
-  }
-  __syncthreads();
-  if (t < KM_MAXK) {
-    float v = 0.f;
-    for (int w = 0; w < CU_THREADS / 32; ++w) v += wsum[w][t];
-    nrm_part[1][t] = v;
-  }
-  km_allreduce(&nrm_part[1][0], &nrm_full[1][0], KM_MAXK, nc);
+  // z_c = s_c / |s_c| for this CTA's channels, and the proxy rows' projection
+  // input RMSNorm(z_c) * gain.  z_c is a unit vector, so its mean square over
+  // the d channels is 1/d: no second reduction over the cluster.
+  const float inv = 1.f / sqrtf(1.f / (float)d + a.eps);
   for (int cg = t; cg < G; cg += CU_THREADS) {
     const float4 gv = one_pass ? gv0 : cl_ld4t<T>(gain + c0 + cg * 4);
 #pragma unroll
     for (int c = 0; c < KM_MAXK; ++c) {
       if (c >= K) continue;
-      const float inv = 1.f / sqrtf(nrm_full[1][c] / (float)d + a.eps);
-      const float4 zv = one_pass ? zkeep[c] : *(const float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4);
+      const float nrm = sqrtf(nrm_full[0][c]);
+      const float4 v = one_pass ? ckeep[c] : *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4);
+      const float4 zv = make_float4(v.x / nrm, v.y / nrm, v.z / nrm, v.w / nrm);
+      *(float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4) = zv;
       T* ao = (T*)a.a_out + (size_t)(a.proxy_row[s] + c) * d + c0 + cg * 4;
       cl_st4t<T>(ao, make_float4(zv.x * inv * gv.x, zv.y * inv * gv.y, zv.z * inv * gv.z, zv.w * inv * gv.w));
     }

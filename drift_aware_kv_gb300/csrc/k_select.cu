@@ -12,11 +12,22 @@
 
 namespace polestar {
 
+constexpr int SEL_MAX_SEQ = 32;    // sequences one launch serves
+constexpr int SEL_MAX_WORDS = 4;   // 32-row words of a sequence's window (up to 128 rows)
+
 __global__ void select_kernel(SelectArgs a) {
-  pdl_enter();
-  __shared__ int s_taken[32];
-  __shared__ int s_count[33];
+  __shared__ int s_taken[SEL_MAX_SEQ];
+  __shared__ int s_count[SEL_MAX_SEQ + 1];
+  __shared__ unsigned s_sel[SEL_MAX_SEQ][SEL_MAX_WORDS];  // selection ballots, reused by the compaction
+  __shared__ uint8_t s_lab[SEL_MAX_SEQ][SEL_MAX_WORDS * 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  // window labels are written at the block entry, never by a kernel of this
+  // step: they are read before waiting for the attention kernel
+  for (int i = tid; i < a.batch * a.nw; i += blockDim.x) {
+    const int s = i / a.nw, j = i % a.nw;
+    s_lab[s][j] = (uint8_t)a.labels[(size_t)s * a.Wmax + j];
+  }
+  pdl_enter();
   // 1. per sequence (one warp): D_c = mean over heads of the proxy KL (lanes
   //    over heads, every cluster's loads in flight together), then top-k
   for (int s = warp; s < a.batch; s += nwarps) {
@@ -68,12 +79,14 @@ __global__ void select_kernel(SelectArgs a) {
     for (int j0 = 0; j0 < a.Wmax; j0 += 32) {
       const int j = j0 + lane;
       bool sel = false;
-      if (fire && j < a.nw) sel = (taken >> a.labels[(size_t)s * a.Wmax + j]) & 1u;
+      if (fire && j < a.nw) sel = (taken >> s_lab[s][j]) & 1u;
       if (j < a.Wmax) {
         a.selected[(size_t)s * a.Wmax + j] = sel;
         a.sel_cur[(size_t)s * a.Wmax + j] = sel;
       }
-      count += __popc(__ballot_sync(0xffffffffu, sel));
+      const unsigned bal = __ballot_sync(0xffffffffu, sel);
+      if (lane == 0 && j0 / 32 < SEL_MAX_WORDS) s_sel[s][j0 / 32] = bal;
+      count += __popc(bal);
     }
     if (lane == 0) s_count[s] = count;
   }
@@ -94,10 +107,8 @@ __global__ void select_kernel(SelectArgs a) {
     if (a.proxy_row[s] < 0) continue;
     int base = s_count[s];
     for (int j0 = 0; j0 < a.nw; j0 += 32) {
-      const int j = j0 + lane;
-      const bool sel = (j < a.nw) && a.sel_cur[(size_t)s * a.Wmax + j];
-      const unsigned bal = __ballot_sync(0xffffffffu, sel);
-      if (sel) a.o_src[base + __popc(bal & ((1u << lane) - 1u))] = a.win_row[s] + j;
+      const unsigned bal = s_sel[s][j0 / 32];
+      if ((bal >> lane) & 1u) a.o_src[base + __popc(bal & ((1u << lane) - 1u))] = a.win_row[s] + j0 + lane;
       base += __popc(bal);
     }
   }
