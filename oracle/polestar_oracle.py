@@ -24,6 +24,8 @@ Parity status per function (what pins it, see tests/test_oracle_*.py):
   commit gate      pinned (worked value c=0.8 -> tau_d=0.1, limits)
   confidence       pinned (generator's target max-probability)
   sparse refresh   pinned (k = K, exact cache: equals the block-entry forward)
+  KV staleness     pinned (closed forms: 0 on itself, 2 on the negation, per-head rotation)
+  full forward     pinned (equals the even block-entry forward; zero staleness after it)
   whole step       parity unpinned beyond the pins above (no worked example exists)
 """
 from __future__ import annotations
@@ -287,6 +289,28 @@ def drift_threshold(c, tau_s, alpha):
     return alpha * (tau_s - c) ** 2
 
 
+def kv_staleness(kv, kv_ref, n_kv_heads, head_dim):
+    """KV-cache staleness of App. C.2 for every row of two caches.
+
+    kv, kv_ref: rows of K then V, [rows, 2, n_kv_heads * head_dim] or any shape
+    with the same element order (e.g. [L, batch, N, 2, Hkv, dh]).  For each row,
+    the cosine similarity of the cached and the recomputed vector is taken per KV
+    head and averaged over heads, separately for K and for V; the staleness is one
+    minus the mean of those two averages.  A zero vector has no direction: two zero
+    vectors count as identical (cos 1), a zero against a non-zero vector as
+    orthogonal (cos 0).  Returns E [rows]."""
+    a = np.asarray(kv, dtype=np.float64).reshape(-1, 2, n_kv_heads, head_dim)
+    b = np.asarray(kv_ref, dtype=np.float64).reshape(-1, 2, n_kv_heads, head_dim)
+    dot = np.sum(a * b, axis=-1)
+    na = np.sum(a * a, axis=-1)
+    nb = np.sum(b * b, axis=-1)
+    both = (na > 0) & (nb > 0)
+    cos = np.where(both, dot / np.sqrt(np.where(both, na * nb, 1.0)),
+                   np.where((na == 0) & (nb == 0), 1.0, 0.0))
+    per_kv = cos.mean(axis=-1)  # [..., 2]: head-averaged cosine of K and of V
+    return 1.0 - 0.5 * (per_kv[..., 0] + per_kv[..., 1])
+
+
 # --------------------------------------------------------------------------------------
 # the engine: block entry, within-block calibration step, commit gate
 # --------------------------------------------------------------------------------------
@@ -414,6 +438,31 @@ class PolestarOracle:
             return self.exact_H[seq_i][l].copy()
         dec = nvfp4_decode(st.codes[l], st.sbytes[l])
         return to_f32(dec + st.A[l][st.labels[l]])
+
+    # ---- full-sequence forward (no cache reuse; the reference of App. C.2) -------------
+    def full_forward_kv(self, x0_seq):
+        """Keys and values of every position at every layer from a forward pass over
+        the whole sequence x0_seq [N, d], recomputing everything (the no-cache
+        decoding of §3 against which App. C.2 measures staleness).  Returns a list
+        of [N, 2, Hkv, dh] arrays in the storage dtype; no state changes."""
+        pos = np.arange(self.N)
+        h = np.asarray(x0_seq, dtype=np.float64)
+        out = []
+        for l in range(self.cfg.n_layers):
+            q, k, v = self.qkv(l, h, pos)
+            kv = np.stack([k, v], axis=1)
+            out.append(kv)
+            o, _, _ = self.attend(q, kv)
+            h = self.post(l, h, o)
+        return out
+
+    def full_forward(self, x0):
+        """Replace every sequence's K/V cache by the full-sequence recompute from
+        x0 [batch, N, d]; window state, centroids, NVFP4 store and histories are
+        kept (a full refresh of the cache alone)."""
+        x0 = np.asarray(x0, dtype=np.float64)
+        for si, st in enumerate(self.seqs):
+            st.kv = self.full_forward_kv(x0[si])
 
     # ---- block entry (Algorithm 1, block-entry phase; §4.1 Block entry) ---------------
     def _block_entry(self, si, st, x0, b):
