@@ -205,6 +205,14 @@ struct CommitArgs {
 };
 void launch_commit(const CommitArgs& a, cudaStream_t st);
 
+// ---- KV-cache staleness (k_staleness.cu) ----
+// E[r] = 1 - (mean_h cos(K_r^h, Kref_r^h) + mean_h cos(V_r^h, Vref_r^h)) / 2 over
+// rows laid out [rows][2][Hkv * dh] (K then V); dh a multiple of 8, both
+// buffers 16-byte aligned.
+template <typename T>
+cudaError_t launch_kv_staleness(const void* kv, const void* ref, long long rows, int Hkv, int dh, float* E,
+                                cudaStream_t st);
+
 // ---- GEMM: C[M, N] (fp32, ldc) = A[M, K] (T, lda) * W[N, K]^T (T, ldw) ----
 // m_dev (nullable): device row count; rows >= min(M, *m_dev) are not computed.
 template <typename T>

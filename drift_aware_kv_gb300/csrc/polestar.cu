@@ -457,10 +457,13 @@ polestar_status ring_writeback(polestar_ctx* c, int l) {
 }
 
 // ------------------------------------------------------------------ block entry
+// fwd_only: the full-sequence forward alone (every position, every layer),
+// rewriting the K/V cache and nothing else -- no window capture, no active-row
+// score history, no K-means, proxies or trigger reset (polestar_full_forward).
 template <typename T>
-polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
+polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_only = false) {
   const int L = c->L, b = c->b, N = c->N, d = c->d;
-  const bool full = (blk % 2 == 0);
+  const bool full = fwd_only || (blk % 2 == 0);
   // rows of one sequence (E_b), padded to 8
   std::vector<int> E;
   if (full) {
@@ -485,7 +488,9 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       if (i < (int)E.size()) {
         const int p = E[i];
         m.y = p;
-        if (p >= c->start && p < c->end) {
+        if (fwd_only) {
+          m.z = ROW_OTHER;
+        } else if (p >= c->start && p < c->end) {
           m.z = ROW_ACTIVE;
           m.w = p - c->start;
         } else if (widx_of[p] >= 0) {
@@ -541,8 +546,9 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
     RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_input<T>(x0, rows, R, N, d, c->h_rows, c->sm)));
     for (int l = 0; l < L; ++l) {
       const polestar_layer_weights& w = c->W[l];
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
-                            (size_t)c->Wmax * d, c->sm)));
+      if (!fwd_only)
+        RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
+                              (size_t)c->Wmax * d, c->sm)));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
       {
         const void* Ws[3] = {w.wq, w.wk, w.wv};
@@ -573,13 +579,14 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
       aa.work = work_d + chunk_work_off[ci];
       aa.n_work = chunk_work_n[ci];
       aa.item_rows = entry_rows;
-      if (l == L - 1) {
+      const bool track = (l == L - 1) && !fwd_only;
+      if (track) {
         aa.active_prev = c->aprev;
         aa.active_prev_lse = c->aprev_lse;
         aa.store = 1;
       }
       const double attn_bytes = (double)ns * N * 2 * c->kvdim * c->esz +
-                                (l == L - 1 ? (double)ns * c->B * c->H * N * 4.0 : 0.0);
+                                (track ? (double)ns * c->B * c->H * N * 4.0 : 0.0);
       aa.batch = b;
       aa.err = tc_error_word(&c->tc);
       RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
@@ -594,6 +601,7 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk) {
                                       nullptr, c->sm)));
     }
   }
+  if (fwd_only) return POLESTAR_OK;
   // spherical K-means + residual NVFP4 for every (layer, sequence)
   KmeansArgs ka{};
   ka.Hw = c->Hw;
@@ -1151,6 +1159,53 @@ extern "C" polestar_status polestar_step_host(polestar_ctx* c, const void* x0_ho
   CUDA_OR_FAIL(c, cudaMemcpyAsync(commit_mask_host, c->st_commit, (size_t)c->b * 2 * c->B, cudaMemcpyDeviceToHost,
                                   c->sm));
   CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_full_forward(polestar_ctx* c, const void* x0) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!x0) return fail(c, POLESTAR_ERR_INVALID_ARG, "x0 is NULL");
+  if ((uintptr_t)x0 & 15) return fail(c, POLESTAR_ERR_INVALID_ARG, "x0 must be 16-byte aligned");
+  // the host metadata buffer may still be in flight from the previous call
+  CUDA_OR_FAIL(c, cudaEventSynchronize(c->meta_ev));
+  TRY(check_timeouts(c));
+  TRY(c->bf16 ? block_entry<__nv_bfloat16>(c, x0, 0, true) : block_entry<float>(c, x0, 0, true));
+  TRY(record_timeouts(c));
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_kv_staleness(const void* kv, const void* kv_ref, int64_t rows, int32_t n_kv_heads,
+                                                 int32_t head_dim, int32_t dtype, float* E, void* stream) {
+  if (rows < 0 || n_kv_heads < 1 || head_dim < 8 || head_dim % 8) return POLESTAR_ERR_INVALID_ARG;
+  if (dtype != POLESTAR_FP32 && dtype != POLESTAR_BF16) return POLESTAR_ERR_INVALID_ARG;
+  if (rows == 0) return POLESTAR_OK;
+  if (!kv || !kv_ref || !E) return POLESTAR_ERR_INVALID_ARG;
+  if (((uintptr_t)kv | (uintptr_t)kv_ref) & 15) return POLESTAR_ERR_INVALID_ARG;
+  if (rows > 0x7FFFFFFFLL) return POLESTAR_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaError_t e = dtype == POLESTAR_BF16
+                            ? launch_kv_staleness<__nv_bfloat16>(kv, kv_ref, rows, n_kv_heads, head_dim, E, st)
+                            : launch_kv_staleness<float>(kv, kv_ref, rows, n_kv_heads, head_dim, E, st);
+  return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
+extern "C" polestar_status polestar_cache_staleness(polestar_ctx* c, polestar_ctx* ref, float* E) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!ref || !E) return fail(c, POLESTAR_ERR_INVALID_ARG, "NULL reference context or output");
+  if (ref == c) return fail(c, POLESTAR_ERR_INVALID_ARG, "the reference must be another context");
+  if (ref->L != c->L || ref->b != c->b || ref->N != c->N || ref->Hkv != c->Hkv || ref->dh != c->dh ||
+      ref->bf16 != c->bf16)
+    return fail(c, POLESTAR_ERR_INVALID_ARG, "reference context has another cache shape or dtype");
+  // the reference's cache is complete once its main stream reaches this point
+  CUDA_OR_FAIL(c, cudaEventRecord(ref->main_ev, ref->sm));
+  CUDA_OR_FAIL(c, cudaStreamWaitEvent(c->sm, ref->main_ev, 0));
+  const long long rows = (long long)c->L * c->b * c->N;
+  const int pi = prof_start(c, POLESTAR_KC_ROWS);
+  const cudaError_t e = c->bf16 ? launch_kv_staleness<__nv_bfloat16>(c->kv, ref->kv, rows, c->Hkv, c->dh, E, c->sm)
+                                : launch_kv_staleness<float>(c->kv, ref->kv, rows, c->Hkv, c->dh, E, c->sm);
+  prof_stop(c, pi, (double)rows * 4 * c->kvdim * c->esz + (double)rows * 4.0, 0.0);
+  if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("staleness launch: ") + cudaGetErrorString(e));
+  c->launches += 1;
   return POLESTAR_OK;
 }
 

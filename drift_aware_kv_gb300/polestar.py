@@ -25,7 +25,8 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
             "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc",
             "polestar_packed_weight_bytes", "polestar_pack_weights", "polestar_debug_gemm_choice",
-            "polestar_debug_attention_impl", "polestar_debug_gemm_swiglu")
+            "polestar_debug_attention_impl", "polestar_debug_gemm_swiglu", "polestar_full_forward",
+            "polestar_kv_staleness", "polestar_cache_staleness")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
 
@@ -101,10 +102,14 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_debug_gemm_choice.argtypes = [C.c_int32, C.c_int32, C.POINTER(C.c_int32), C.c_int32,
                                                C.POINTER(C.c_int32)]
     lib.polestar_debug_gemm_choice.restype = C.c_int
+    lib.polestar_full_forward.argtypes = [P, P]
+    lib.polestar_kv_staleness.argtypes = [P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P]
+    lib.polestar_cache_staleness.argtypes = [P, P, P]
     lib.polestar_profile_begin.argtypes = [P, C.c_int32]
     lib.polestar_profile_end.argtypes = [P, C.POINTER(polestar_kernel_stats), C.c_int32]
     for f in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
-              "polestar_debug_read", "polestar_profile_begin", "polestar_profile_end"):
+              "polestar_debug_read", "polestar_profile_begin", "polestar_profile_end",
+              "polestar_full_forward", "polestar_kv_staleness", "polestar_cache_staleness"):
         getattr(lib, f).restype = C.c_int
     _lib = lib
     return lib
@@ -191,6 +196,21 @@ class Polestar:
                                            int(bool(block_entry)), C.c_void_p(logits_host.data_ptr()),
                                            int(logits_host.shape[-1]), C.c_void_p(masked_host.data_ptr()),
                                            C.c_void_p(commit_host.data_ptr())), self.ctx)
+
+    def full_forward(self, x0):
+        """Recompute the whole K/V cache from x0 by a full-sequence forward
+        (polestar_full_forward); nothing else of the context changes."""
+        _check(self.lib.polestar_full_forward(self.ctx, C.c_void_p(x0.data_ptr())), self.ctx)
+
+    def staleness(self, ref: "Polestar", out=None):
+        """KV-cache staleness E [n_layers, batch, N] (CUDA fp32 tensor) of this
+        context's cache against `ref`'s (polestar_cache_staleness)."""
+        import torch
+        w = self.w
+        if out is None:
+            out = torch.empty(w.n_layers, w.batch, w.seq_len, dtype=torch.float32, device="cuda")
+        _check(self.lib.polestar_cache_staleness(self.ctx, ref.ctx, C.c_void_p(out.data_ptr())), self.ctx)
+        return out
 
     def launch_count(self) -> int:
         return int(self.lib.polestar_launch_count(self.ctx))
@@ -347,3 +367,23 @@ def attention_noalloc(q, kv, H, Hkv, tracked_dev, prev, prev_lse, measure, store
     _check(lib.polestar_attention_noalloc(_ptr(q), _ptr(kv), N, H, Hkv, dh, R, _ptr(tracked_dev), _ptr(prev),
                                           _ptr(prev_lse), int(measure), int(store), _ptr(out), _ptr(kl),
                                           C.c_void_p(st.cuda_stream)))
+
+
+def kv_staleness(kv, kv_ref, n_kv_heads: int, E=None, stream=None):
+    """App. C.2 staleness of the rows of two caches laid out [rows, 2, Hkv*dh]
+    (CUDA tensors, fp32 or bf16, any leading shape) through polestar_kv_staleness;
+    returns E [rows] fp32 (CUDA)."""
+    import torch
+    lib = load()
+    assert kv.shape == kv_ref.shape and kv.dtype == kv_ref.dtype
+    assert kv.is_contiguous() and kv_ref.is_contiguous()
+    kvdim = kv.shape[-1]
+    rows = kv.numel() // (2 * kvdim)
+    dh = kvdim // n_kv_heads
+    if E is None:
+        E = torch.empty(rows, dtype=torch.float32, device=kv.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    dt = BF16 if kv.dtype == torch.bfloat16 else FP32
+    _check(lib.polestar_kv_staleness(_ptr(kv), _ptr(kv_ref), rows, int(n_kv_heads), int(dh), dt, _ptr(E),
+                                     C.c_void_p(st.cuda_stream)))
+    return E

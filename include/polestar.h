@@ -143,6 +143,41 @@ polestar_status polestar_step_host(polestar_ctx *ctx, const void *x0_host, const
                                    const float *logits_host, int32_t vocab,
                                    const uint8_t *masked_host, uint8_t *commit_mask_host);
 
+/* ---- KV-cache staleness (App. C.2 "KV-Cache Staleness Metric") ----
+ *
+ * polestar_full_forward: full-sequence forward of every position of every
+ * sequence through every layer from x0 (device [batch, N, d], config dtype,
+ * 16-byte aligned), rewriting the context's whole K/V cache with exactly
+ * recomputed keys and values -- the no-cache decoding of §3 that recomputes
+ * every position at every step, and the "fully recomputed" K/V that App. C.2
+ * measures a cache against.  On a context used as that reference, call it once
+ * per step with the step's x0; on a calibrating context it is a full refresh.
+ * Only the K/V cache changes: window state, centroids, NVFP4 store, drift
+ * histories, trigger counters and the results of the last step stay as they
+ * were, so calibration and commit continue normally (a call placed between
+ * polestar_calibrate_step and polestar_commit does not disturb that commit).
+ * Asynchronous on the main stream.
+ *
+ * polestar_kv_staleness: E[r] = 1 - (mean_h cos(K_r^h, Kref_r^h) +
+ * mean_h cos(V_r^h, Vref_r^h)) / 2 for `rows` rows of two caches laid out
+ * [rows][2][n_kv_heads * head_dim] (K then V of each row; `dtype` a
+ * polestar_dtype), cosines per KV head (h), averaged over the heads.  A pair
+ * of zero vectors counts as cos 1, one zero vector against a non-zero one as
+ * cos 0.  kv, kv_ref: device, 16-byte aligned; E: device [rows] fp32; head_dim
+ * a multiple of 8; rows <= 2^31 - 1 (else UNSUPPORTED).  Asynchronous on
+ * `stream`; no context, no allocation.
+ *
+ * polestar_cache_staleness: the same metric between the K/V caches of two
+ * contexts with the same n_layers, batch, N, n_kv_heads, head_dim and dtype:
+ * E device [n_layers, batch, N] fp32, E[l, s, i] = E_i(t, l) of sequence s
+ * with `ref` holding the reference (typically a context whose last call was
+ * polestar_full_forward on the same x0).  Runs on ctx's main stream after
+ * everything issued so far on ref's main stream. */
+polestar_status polestar_full_forward(polestar_ctx *ctx, const void *x0);
+polestar_status polestar_kv_staleness(const void *kv, const void *kv_ref, int64_t rows, int32_t n_kv_heads,
+                                      int32_t head_dim, int32_t dtype, float *E, void *stream);
+polestar_status polestar_cache_staleness(polestar_ctx *ctx, polestar_ctx *ref, float *E);
+
 /* Free everything the context owns.  NULL is accepted; the context pointer is
  * invalid afterwards.  Synchronises the context's streams first. */
 void polestar_release(polestar_ctx *ctx);
