@@ -183,15 +183,20 @@ def run_device(args, w, peaks, ws, rank, local):
     cm = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device=dev)
     timed = steps[args.warmup:]
 
-    def region(profile: bool):
+    def region(profile: bool, no_refresh: bool = False):
         """Fresh context: warm-up steps, then the timed steps.  The headline
         region runs without per-kernel events (they would serialise the
         programmatic dependent launches); the profiled region repeats the same
-        steps with CUDA events around every launch for the per-class times."""
-        ps = P.Polestar(w, W, stream=stream, side_stream=side, host_offload=offload)
+        steps with CUDA events around every launch for the per-class times.
+        no_refresh: the same steps with the tau_upd trigger out of reach (no
+        sparse refresh inside a block), for the calibration overhead."""
+        wr = w.replace(tau_upd=10 ** 6) if no_refresh else w
+        ps = P.Polestar(wr, W, stream=stream, side_stream=side, host_offload=offload)
+        fired = []
 
         def do_step(st):
-            ps.calibrate_step(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"])
+            o = ps.calibrate_step(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"])
+            fired.append(not st["block_entry"] and all(o.fire[s] for s in range(w.batch)))
             ps.commit(st["logits"], st["masked"], cm)
 
         for st in steps[: args.warmup]:
@@ -225,10 +230,23 @@ def run_device(args, w, peaks, ws, rank, local):
         total_ms = ev[0].elapsed_time(ev[-1])
         ps.close()
         return dict(stats=stats, launches=launches, step_ms=step_ms, total_ms=total_ms, wall=wall,
-                    clocks=clocks, issue_first=issue_first)
+                    clocks=clocks, issue_first=issue_first, fired=fired[args.warmup:])
 
     main = region(profile=False)
     prof = region(profile=True)
+    # calibration overhead (the pages' App. D.10 measure): within-block steps in
+    # which every sequence refreshed, against the same steps without refresh
+    base = region(profile=False, no_refresh=True)
+    fired_idx = [i for i, f in enumerate(main["fired"]) if f]
+    overhead = None
+    if fired_idx:
+        t_fire = statistics.mean(main["step_ms"][i] for i in fired_idx)
+        t_base = statistics.mean(base["step_ms"][i] for i in fired_idx)
+        overhead = {"ms_per_layer": (t_fire - t_base) / w.n_layers, "steps": len(fired_idx),
+                    "step_ms_refreshing": t_fire, "step_ms_same_steps_no_refresh": t_base,
+                    "what": "per-layer added time of a within-block step in which every sequence runs the "
+                            "sparse refresh (patch, centroid update, proxy attention + KL, top-k, update "
+                            "packets), against the same step with the trigger off"}
     stats = prof["stats"]
     launches = main["launches"]
     step_ms, total_ms, wall, clocks = main["step_ms"], main["total_ms"], main["wall"], main["clocks"]
@@ -304,6 +322,7 @@ def run_device(args, w, peaks, ws, rank, local):
         "kernel_ms_profiled_region": {k: round(v["ms"], 3) for k, v in stats.items()},
         "profiled_region_ms_per_step": prof["total_ms"] / len(timed),
         "kernel_launches": {k: v["launches"] for k, v in stats.items()},
+        "calibration_overhead": overhead,
         "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
         "wall_s": wall,
         "host_issue_ms_first_step": main["issue_first"] * 1e3,

@@ -8,6 +8,7 @@ Nsight Compute captures of one kernel, e.g.
   python -m drift_aware_kv_gb300.kbench gemm --M 136 --N 24576 --K 4096
   python -m drift_aware_kv_gb300.kbench attn --R 136 --N 768 --H 32 --Hkv 32
   python -m drift_aware_kv_gb300.kbench kmeans --P 32 --nw 96 --d 4096
+  python -m drift_aware_kv_gb300.kbench stale --rows 24576 --Hkv 32 --dh 128
 """
 from __future__ import annotations
 
@@ -97,9 +98,23 @@ def bench_kmeans(a):
     return dict(kernel="kmeans_nvfp4", P=a.P, nw=a.nw, d=a.d, us=ms * 1e3, GBps=byts / ms / 1e6)
 
 
+def bench_stale(a):
+    """KV-cache staleness kernel over a cache pair of `rows` rows [2, Hkv*dh] bf16
+    (LLaDA-8B, batch 1: 32 layers x 768 positions = 24576 rows, 805 MB)."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cuda").manual_seed(0)
+    kv = torch.randn(a.rows, 2, a.Hkv * a.dh, device="cuda", generator=g).to(torch.bfloat16)
+    ref = (kv.float() + 0.1 * torch.randn(kv.shape, device="cuda", generator=g)).to(torch.bfloat16)
+    E = torch.empty(a.rows, device="cuda")
+    ms = _time(lambda: P.kv_staleness(kv, ref, a.Hkv, E), a.iters)
+    byts = a.rows * (4 * a.Hkv * a.dh * 2 + 4)
+    return dict(kernel="kv_staleness", rows=a.rows, Hkv=a.Hkv, dh=a.dh, us=ms * 1e3, GBps=byts / ms / 1e6)
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemm", "attn", "kmeans"])
+    ap.add_argument("kernel", choices=["gemm", "attn", "kmeans", "stale"])
+    ap.add_argument("--rows", type=int, default=24576, help="staleness: cache rows (layers x positions)")
     ap.add_argument("--M", type=int, default=136)
     ap.add_argument("--N", type=int, default=None, help="gemm N (default 4096) / attention keys (default 768)")
     ap.add_argument("--K", type=int, default=4096)
@@ -130,7 +145,7 @@ def main():
         a.N = 4096 if a.kernel == "gemm" else 768
     from drift_aware_kv_gb300.build import build
     build()
-    fn = {"gemm": bench_gemm, "attn": bench_attn, "kmeans": bench_kmeans}[a.kernel]
+    fn = {"gemm": bench_gemm, "attn": bench_attn, "kmeans": bench_kmeans, "stale": bench_stale}[a.kernel]
     print(json.dumps(fn(a)))
 
 
