@@ -16,7 +16,7 @@
 
 namespace polestar {
 
-constexpr int KM_THREADS = 256;
+constexpr int KM_THREADS = 512;
 constexpr int KM_MAXK = 8;
 constexpr int KM_MAXW = 128;   // rows per problem
 constexpr int KM_SMEM_CAP = 220 * 1024;
@@ -61,6 +61,33 @@ __device__ __forceinline__ void km_allreduce(const float* part, float* out, int 
   km_cluster_sync();
 }
 
+// One reduce-scatter step of a warp over 2H values v[0 .. 2H) (H a power of
+// two), exchanging with lane ^ o: the lane keeps the half selected by bit o of
+// its lane index and adds its partner's copy of that half into v[0 .. H).
+constexpr int KM_ROWS = 6;  // rows per warp pass of the assignment (6 * KM_MAXK values per lane)
+static_assert(KM_MAXK == 8 && KM_ROWS == 6, "the assignment's butterflies map 32 + 16 values onto the lanes");
+template <int H>
+__device__ __forceinline__ void km_bfly(float* v, int lane, int o = H) {
+  const bool up = (lane & o) != 0;
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const float send = up ? v[j] : v[j + H];
+    const float keep = up ? v[j + H] : v[j];
+    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+  }
+}
+
+// Floats of each of the kernel's two reduction buffers: the assignment's row x
+// cluster dot products, and at least one value per (warp, cluster) for the
+// norm reduction.
+__host__ __device__ constexpr int km_pair_floats(int nw, int K) {
+  return nw * KM_MAXK > (KM_THREADS / 32) * KM_MAXK ? nw * KM_MAXK : (KM_THREADS / 32) * KM_MAXK;
+}
+__host__ __device__ constexpr size_t km_smem_bytes(int nw, int ds, int K) {
+  return ((size_t)nw * ds + (size_t)K * ds + 2 * (size_t)km_pair_floats(nw, K) + KM_MAXW + 32) * sizeof(float) +
+         (3 * KM_MAXW + 2 * KM_MAXK + 1) * sizeof(int);
+}
+
 // One thread-block cluster per (layer, sequence) problem; CTA r of the cluster
 // owns channels [r*ds, (r+1)*ds) of the window rows, held in shared memory for
 // the whole K-means, so the rows are read from memory once.
@@ -76,13 +103,14 @@ __global__ void __launch_bounds__(KM_THREADS) kmeans_encode_kernel(KmeansArgs a,
   const int c0 = (int)rank * ds;
   float* Xs = sm;                                      // [nw][ds]
   float* zs = Xs + (size_t)nw * ds;                    // [K][ds]
-  float* part = zs + (size_t)K * ds;                   // [KM_MAXW * KM_MAXK] partial sums
-  float* full = part + KM_MAXW * KM_MAXK;              // [KM_MAXW * KM_MAXK] reduced sums
-  float* inv = full + KM_MAXW * KM_MAXK;               // [KM_MAXW]
+  const int pk = km_pair_floats(nw, K);
+  float* part = zs + (size_t)K * ds;                   // [pk] partial sums
+  float* full = part + pk;                             // [pk] reduced sums
+  float* inv = full + pk;                              // [KM_MAXW]
   float* red = inv + KM_MAXW;                          // [32] block-reduction scratch
   int* lab = (int*)(red + 32);                         // [KM_MAXW]
   int* perm = lab + KM_MAXW;                           // [KM_MAXW]
-  int* cnt = perm + KM_MAXW;                           // [KM_MAXK]
+  int* cnt = perm + KM_MAXW;                           // [KM_MAXK] counts, then [KM_MAXK + 1] list starts
   const int tid = threadIdx.x;
   const float* X = a.Hw + (size_t)prob * a.Wmax * d;
 
@@ -105,177 +133,246 @@ __global__ void __launch_bounds__(KM_THREADS) kmeans_encode_kernel(KmeansArgs a,
   __syncthreads();
   km_allreduce(part, full, nw, cs);
   for (int i = tid; i < nw; i += KM_THREADS) inv[i] = 1.f / sqrtf(full[i]);
-  // seeded initialisation (every CTA draws the same permutation)
-  if (tid == 0) {
-    uint64_t st = a.seed ^ ((uint64_t)seq << 40) ^ ((uint64_t)a.block << 20) ^ (uint64_t)layer;
-    for (int i = 0; i < nw; ++i) perm[i] = i;
-    for (int i = nw - 1; i > 0; --i) {
-      const int j = (int)(splitmix64_next(st) % (uint64_t)(i + 1));
-      const int t = perm[i];
-      perm[i] = perm[j];
-      perm[j] = t;
+  // seeded initialisation (every CTA draws the same permutation).  Fisher-Yates
+  // step t (i = nw-1-t, swap perm[i] with perm[j], j = draw_t mod (i+1)) takes
+  // output t of splitmix64; output t is the mix of state st0 + (t+1) * golden,
+  // so the targets are computed in parallel (into lab, free until the first
+  // assignment) and only the swaps run in order.
+  {
+    const uint64_t st0 = a.seed ^ ((uint64_t)seq << 40) ^ ((uint64_t)a.block << 20) ^ (uint64_t)layer;
+    for (int t = tid; t < nw - 1; t += KM_THREADS) {
+      uint64_t st = st0 + (uint64_t)t * 0x9E3779B97F4A7C15ull;
+      const uint64_t x = splitmix64_next(st);
+      // x mod m with 32-bit operations (exact: m <= KM_MAXW): x = hi * 2^32 + lo,
+      // so x mod m = ((hi mod m) * (2^32 mod m) + lo mod m) mod m
+      const uint32_t m = (uint32_t)(nw - t), hi = (uint32_t)(x >> 32), lo = (uint32_t)x;
+      const uint32_t p32 = (uint32_t)((0x100000000ull) % m);
+      lab[t] = (int)(((hi % m) * p32 + lo % m) % m);
     }
+    for (int i = tid; i < nw; i += KM_THREADS) perm[i] = i;
+    __syncthreads();
+    if (tid == 0)
+      for (int t = 0; t < nw - 1; ++t) {
+        const int i = nw - 1 - t, j = lab[t];
+        const int v = perm[i];
+        perm[i] = perm[j];
+        perm[j] = v;
+      }
+    __syncthreads();
   }
-  __syncthreads();
   for (int idx = tid; idx < K * ds; idx += KM_THREADS) {
     const int c = idx / ds, k = idx % ds;
     zs[idx] = Xs[(size_t)perm[c] * ds + k] * inv[perm[c]];
   }
   __syncthreads();
 
-  constexpr int DPT = 2;  // channels per thread in the update (ds <= 512)
-  float acc[KM_MAXK][DPT];
+  // member lists of the last assignment: rows of cluster c, in row order, at
+  // mem[mstart[c] .. mstart[c + 1])
+  int* mem = perm;  // the permutation is only needed for the initialisation
+  int* mstart = cnt + KM_MAXK;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int k = tid;  // this thread's channel of the slice in the updates (ds <= KM_THREADS)
+  float accv[KM_MAXK];
   for (int it = 0; it < a.iters; ++it) {
     // assignment: cosine = (sum over slices of x.z) / |x|, argmax, ties to the lower id.
-    // Warp per row, lanes across channels (conflict-free shared-memory reads).
-    {
-      const int lane = tid & 31, warp = tid >> 5;
-      for (int i = warp; i < nw; i += KM_THREADS / 32) {
-        float dot[KM_MAXK];
+    // A warp takes KM_ROWS rows at a time, lanes across channels (conflict-free
+    // shared-memory reads), so each centroid element is read once per KM_ROWS
+    // rows; the per-lane partial dot products are summed over the warp by
+    // reduce-scatter butterflies (rows 0-3: 32 values, lane L ends with the
+    // total of value L; rows 4-5: 16 values, lanes 2v and 2v+1 with value v).
+    for (int i0 = warp * KM_ROWS; i0 < nw; i0 += (KM_THREADS / 32) * KM_ROWS) {
+      float dv[KM_ROWS * KM_MAXK];  // dv[r * KM_MAXK + c]
 #pragma unroll
-        for (int c = 0; c < KM_MAXK; ++c) dot[c] = 0.f;
-        for (int k = lane; k < ds; k += 32) {
-          const float x = Xs[(size_t)i * ds + k];
+      for (int q = 0; q < KM_ROWS * KM_MAXK; ++q) dv[q] = 0.f;
+      for (int kk = lane; kk < ds; kk += 32) {
+        float zc[KM_MAXK];
 #pragma unroll
-          for (int c = 0; c < KM_MAXK; ++c)
-            if (c < K) dot[c] = fmaf(x, zs[c * ds + k], dot[c]);
+        for (int c = 0; c < KM_MAXK; ++c) zc[c] = (c < K) ? zs[c * ds + kk] : 0.f;
+#pragma unroll
+        for (int r = 0; r < KM_ROWS; ++r) {
+          const float x = (i0 + r < nw) ? Xs[(size_t)(i0 + r) * ds + kk] : 0.f;
+#pragma unroll
+          for (int c = 0; c < KM_MAXK; ++c) dv[r * KM_MAXK + c] = fmaf(x, zc[c], dv[r * KM_MAXK + c]);
         }
-#pragma unroll
-        for (int c = 0; c < KM_MAXK; ++c) {
-          const float v = warp_sum(dot[c]);
-          if (lane == 0 && c < K) part[i * K + c] = v;
-        }
+      }
+      km_bfly<16>(dv, lane);
+      km_bfly<8>(dv, lane);
+      km_bfly<4>(dv, lane);
+      km_bfly<2>(dv, lane);
+      km_bfly<1>(dv, lane);
+      float* d2 = dv + 32;
+      km_bfly<8>(d2, lane, 16);
+      km_bfly<4>(d2, lane, 8);
+      km_bfly<2>(d2, lane, 4);
+      km_bfly<1>(d2, lane, 2);
+      d2[0] += __shfl_xor_sync(0xffffffffu, d2[0], 1);
+      {
+        const int r = lane >> 3, c = lane & 7;
+        if (i0 + r < nw) part[(i0 + r) * KM_MAXK + c] = dv[0];
+      }
+      {
+        const int v = lane >> 1, r = 4 + (v >> 3), c = v & 7;
+        if (!(lane & 1) && i0 + r < nw) part[(i0 + r) * KM_MAXK + c] = d2[0];
       }
     }
     __syncthreads();
-    km_allreduce(part, full, nw * K, cs);
-    if (tid < K) cnt[tid] = 0;
-    __syncthreads();
-    for (int i = tid; i < nw; i += KM_THREADS) {
-      int best = 0;
-      float bv = -INFINITY;
-      for (int c = 0; c < K; ++c) {
-        const float v = full[i * K + c] * inv[i];
-        if (v > bv) {
-          bv = v;
-          best = c;
+    km_allreduce(part, full, nw * KM_MAXK, cs);
+    // argmax and the member lists (stable counting sort by label): warp w
+    // takes rows 32w + lane; its per-cluster counts go to wcnt, and after one
+    // barrier each warp places its members behind those of the earlier
+    // clusters and of the earlier warps of the same cluster
+    int* wcnt = (int*)red;  // [KM_MAXW / 32][KM_MAXK]
+    const int nch = (nw + 31) / 32;
+    int best = -1;
+    unsigned bal[KM_MAXK];
+    if (warp < nch) {
+      const int i = warp * 32 + lane;
+      if (i < nw) {
+        float bv = -INFINITY;
+        best = 0;
+        const float4 f0 = *(const float4*)(full + i * KM_MAXK), f1 = *(const float4*)(full + i * KM_MAXK + 4);
+        const float fr[KM_MAXK] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+        const float w = inv[i];
+#pragma unroll
+        for (int c = 0; c < KM_MAXK; ++c) {
+          const float v = fr[c] * w;
+          if (c < K && v > bv) {
+            bv = v;
+            best = c;
+          }
         }
+        lab[i] = best;
       }
-      lab[i] = best;
-      atomicAdd(&cnt[best], 1);
+#pragma unroll
+      for (int c = 0; c < KM_MAXK; ++c) {
+        bal[c] = __ballot_sync(0xffffffffu, best == c);
+        if (lane == 0) wcnt[warp * KM_MAXK + c] = __popc(bal[c]);
+      }
+    }
+    __syncthreads();
+    if (warp < nch) {
+      int off = 0;  // members of clusters < c, then of earlier warps in cluster c
+      const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+      for (int c = 0; c < KM_MAXK; ++c) {
+        int before = 0, total = 0;
+        for (int w2 = 0; w2 < nch; ++w2) {
+          const int n = wcnt[w2 * KM_MAXK + c];
+          total += n;
+          if (w2 < warp) before += n;
+        }
+        if (best == c) mem[off + before + __popc(bal[c] & lt)] = warp * 32 + lane;
+        if (warp == 0 && lane == 0) {
+          cnt[c] = total;
+          mstart[c] = off;
+        }
+        off += total;
+      }
+      if (warp == 0 && lane == 0) mstart[KM_MAXK] = off;
     }
     __syncthreads();
     // update: s_c = sum of member unit rows (row order) on this slice
 #pragma unroll
-    for (int c = 0; c < KM_MAXK; ++c)
-#pragma unroll
-      for (int t = 0; t < DPT; ++t) acc[c][t] = 0.f;
-    for (int i = 0; i < nw; ++i) {
-      const int c = lab[i];
-      const float w = inv[i];
-#pragma unroll
-      for (int t = 0; t < DPT; ++t) {
-        const int k = tid + t * KM_THREADS;
-        if (k < ds) {
-          const float v = Xs[(size_t)i * ds + k] * w;
-#pragma unroll
-          for (int cc = 0; cc < KM_MAXK; ++cc)
-            if (cc == c) acc[cc][t] += v;
+    for (int c = 0; c < KM_MAXK; ++c) {
+      accv[c] = 0.f;
+      if (c < K && k < ds)
+        for (int j = mstart[c]; j < mstart[c + 1]; ++j) {
+          const int i = mem[j];
+          accv[c] += Xs[(size_t)i * ds + k] * inv[i];
         }
-      }
     }
-    // |s_c|^2: per-thread partials, block reduce per cluster, cluster sum
-    for (int c = 0; c < K; ++c) {
-      float ss = 0.f;
+    // |s_c|^2: warp partials (xor tree), then the warps' values (xor tree), cluster sum
 #pragma unroll
-      for (int t = 0; t < DPT; ++t) ss = fmaf(acc[c][t], acc[c][t], ss);
-      ss = block_sum(ss, red);
-      if (tid == 0) part[c] = ss;
+    for (int c = 0; c < KM_MAXK; ++c) {
+      const float v = warp_sum(accv[c] * accv[c]);
+      if (lane == 0 && c < K) full[warp * K + c] = v;
     }
+    __syncthreads();
+    if (warp == 0)
+      for (int c = 0; c < K; ++c) {
+        const float t = warp_sum(lane < KM_THREADS / 32 ? full[lane * K + c] : 0.f);
+        if (lane == 0) part[c] = t;
+      }
     __syncthreads();
     km_allreduce(part, full, K, cs);
     const bool last = (it == a.iters - 1);
-    for (int c = 0; c < K; ++c) {
-      const float nrm = sqrtf(full[c]);
-      float* csum = a.csum + ((size_t)prob * K + c) * d + c0;
+    if (k < ds)
 #pragma unroll
-      for (int t = 0; t < DPT; ++t) {
-        const int k = tid + t * KM_THREADS;
-        if (k < ds) {
-          if (cnt[c] > 0) zs[c * ds + k] = acc[c][t] / nrm;
-          if (last) csum[k] = (cnt[c] > 0) ? acc[c][t] : zs[c * ds + k];
-        }
+      for (int c = 0; c < KM_MAXK; ++c) {
+        if (c >= K) continue;
+        float* csum = a.csum + ((size_t)prob * K + c) * d + c0;
+        if (cnt[c] > 0) zs[c * ds + k] = accv[c] / sqrtf(full[c]);
+        if (last) csum[k] = (cnt[c] > 0) ? accv[c] : zs[c * ds + k];
       }
-    }
     __syncthreads();
   }
   // outputs: labels, centroid slices
   if (rank == 0)
     for (int i = tid; i < nw; i += KM_THREADS) a.labels[(size_t)prob * a.Wmax + i] = (uint8_t)lab[i];
   for (int idx = tid; idx < K * ds; idx += KM_THREADS) {
-    const int c = idx / ds, k = idx % ds;
-    a.z[((size_t)prob * K + c) * d + c0 + k] = zs[idx];
+    const int c = idx / ds, kk = idx % ds;
+    a.z[((size_t)prob * K + c) * d + c0 + kk] = zs[idx];
   }
   __syncthreads();
   // anchors A_c: raw member means on this slice (reuse zs)
+  if (k < ds)
 #pragma unroll
-  for (int c = 0; c < KM_MAXK; ++c)
-#pragma unroll
-    for (int t = 0; t < DPT; ++t) acc[c][t] = 0.f;
-  for (int i = 0; i < nw; ++i) {
-    const int c = lab[i];
-#pragma unroll
-    for (int t = 0; t < DPT; ++t) {
-      const int k = tid + t * KM_THREADS;
-      if (k < ds) {
-        const float v = Xs[(size_t)i * ds + k];
-#pragma unroll
-        for (int cc = 0; cc < KM_MAXK; ++cc)
-          if (cc == c) acc[cc][t] += v;
-      }
+    for (int c = 0; c < KM_MAXK; ++c) {
+      if (c >= K) continue;
+      float acc = 0.f;
+      for (int j = mstart[c]; j < mstart[c + 1]; ++j) acc += Xs[(size_t)mem[j] * ds + k];
+      const float v = (cnt[c] > 0) ? acc / (float)cnt[c] : 0.f;
+      zs[c * ds + k] = v;
+      a.anchor[((size_t)prob * K + c) * d + c0 + k] = v;
     }
-  }
-  for (int c = 0; c < K; ++c) {
-    float* an = a.anchor + ((size_t)prob * K + c) * d + c0;
-#pragma unroll
-    for (int t = 0; t < DPT; ++t) {
-      const int k = tid + t * KM_THREADS;
-      if (k < ds) {
-        const float v = (cnt[c] > 0) ? acc[c][t] / (float)cnt[c] : 0.f;
-        zs[c * ds + k] = v;
-        an[k] = v;
-      }
-    }
-  }
   __syncthreads();
-  // NVFP4 residual encoding of this slice: one thread per 16-channel group
+  // NVFP4 residual encoding of this slice: one thread per 16-channel group,
+  // groups of a row on consecutive threads (coalesced code writes).  The four
+  // 16-byte quarters of a group are read starting at quarter (g / 2) mod 4, so
+  // the eight groups of a quarter-warp hit eight different bank quads.
   const int ngs = ds / 16, ng = d / 16;
   for (int idx = tid; idx < nw * ngs; idx += KM_THREADS) {
     const int i = idx / ngs, g = idx % ngs;
     const int c = lab[i];
-    float r[16];
+    const int rot = (g >> 1) & 3;
+    const float* xr = Xs + (size_t)i * ds + g * 16;
+    const float* zr = zs + c * ds + g * 16;
+    float4 r4[4];  // r4[qq] = quarter (qq + rot) & 3 of the group
+    float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) r[e] = Xs[(size_t)i * ds + g * 16 + e] - zs[c * ds + g * 16 + e];
-    uint8_t packed[8];
+    for (int qq = 0; qq < 4; ++qq) {
+      const int q = (qq + rot) & 3;
+      const float4 xv = *(const float4*)(xr + q * 4), zv = *(const float4*)(zr + q * 4);
+      r4[qq] = make_float4(xv.x - zv.x, xv.y - zv.y, xv.z - zv.z, xv.w - zv.w);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(r4[qq].x), fabsf(r4[qq].y)), fmaxf(fabsf(r4[qq].z), fabsf(r4[qq].w))));
+    }
+    const uint8_t sb = e4m3_encode_rne(__fdiv_rn(amax, 6.f));
+    const float sc = e4m3_decode(sb);
+    uint64_t pk = 0;
+    if (sc > 0.f)
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        const int q = (qq + rot) & 3;
+        const uint32_t e0 = e2m1_encode_rne(__fdiv_rn(r4[qq].x, sc)), e1 = e2m1_encode_rne(__fdiv_rn(r4[qq].y, sc));
+        const uint32_t e2 = e2m1_encode_rne(__fdiv_rn(r4[qq].z, sc)), e3 = e2m1_encode_rne(__fdiv_rn(r4[qq].w, sc));
+        const uint64_t bits = (uint64_t)(e0 | (e1 << 4) | (e2 << 8) | (e3 << 12));
+        pk |= bits << (16 * q);  // elements 4q .. 4q+3 are bytes 2q, 2q+1
+      }
     const int gg = c0 / 16 + g;
-    a.scales[((size_t)local * a.Wmax + i) * ng + gg] = nvfp4_encode16(r, packed);
-    uint2 pk;
-    pk.x = packed[0] | (packed[1] << 8) | (packed[2] << 16) | ((uint32_t)packed[3] << 24);
-    pk.y = packed[4] | (packed[5] << 8) | (packed[6] << 16) | ((uint32_t)packed[7] << 24);
-    *(uint2*)(a.codes + ((size_t)local * a.Wmax + i) * (d / 2) + gg * 8) = pk;
+    a.scales[((size_t)local * a.Wmax + i) * ng + gg] = sb;
+    *(uint2*)(a.codes + ((size_t)local * a.Wmax + i) * (d / 2) + gg * 8) =
+        make_uint2((uint32_t)pk, (uint32_t)(pk >> 32));
   }
 }
 
 // Cluster size: the smallest divisor of d/16 (<= 16) whose channel slice fits
-// in shared memory and keeps <= 2 channels per thread.
+// in shared memory and gives each thread at most one channel in the updates.
 int kmeans_cluster_size(int d, int nw, int K) {
   const int groups = d / 16;
   for (int cs = 1; cs <= 16; ++cs) {
     if (groups % cs) continue;
     const int ds = d / cs;
-    const size_t sm = ((size_t)nw * ds + (size_t)K * ds + 2 * KM_MAXW * KM_MAXK + KM_MAXW + 32) * sizeof(float) +
-                      (3 * KM_MAXW + KM_MAXK) * sizeof(int);
-    if (ds <= 2 * KM_THREADS && sm <= (size_t)KM_SMEM_CAP) return cs;
+    if (ds <= KM_THREADS && km_smem_bytes(nw, ds, K) <= (size_t)KM_SMEM_CAP) return cs;
   }
   return -1;
 }
@@ -283,8 +380,7 @@ int kmeans_cluster_size(int d, int nw, int K) {
 void launch_kmeans_encode(const KmeansArgs& a, cudaStream_t st) {
   const int cs = kmeans_cluster_size(a.d, a.nw, a.K);
   const int ds = a.d / cs;
-  const size_t sm = ((size_t)a.nw * ds + (size_t)a.K * ds + 2 * KM_MAXW * KM_MAXK + KM_MAXW + 32) * sizeof(float) +
-                    (3 * KM_MAXW + KM_MAXK) * sizeof(int);
+  const size_t sm = km_smem_bytes(a.nw, ds, a.K);
   cudaFuncSetAttribute(kmeans_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (cs > 8) cudaFuncSetAttribute(kmeans_encode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaLaunchConfig_t cfg{};
