@@ -66,3 +66,26 @@ def test_gemm_choice_without_a_device_is_an_error_not_a_crash():
     from drift_aware_kv_gb300 import polestar as P
     with pytest.raises(P.PolestarError):
         P.gemm_choice(2560, [12288], 4096)
+
+
+def test_staleness_entry_points_reject_bad_arguments_on_the_host():
+    """KV-cache staleness (App. C.2) and the full-sequence forward check their
+    arguments before any device work: these calls fail on a machine with no GPU
+    exactly as on one with a GPU."""
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    E = ctypes.c_void_p(0x1000)
+    buf = ctypes.c_void_p(0x2000)
+    # head size not a multiple of 8, unknown dtype, negative rows, misaligned cache
+    assert lib.polestar_kv_staleness(buf, buf, 4, 2, 12, P.BF16, E, None) == P.ERR_INVALID_ARG
+    assert lib.polestar_kv_staleness(buf, buf, 4, 2, 16, 5, E, None) == P.ERR_INVALID_ARG
+    assert lib.polestar_kv_staleness(buf, buf, -1, 2, 16, P.BF16, E, None) == P.ERR_INVALID_ARG
+    assert lib.polestar_kv_staleness(ctypes.c_void_p(0x2004), buf, 4, 2, 16, P.BF16, E, None) == P.ERR_INVALID_ARG
+    assert lib.polestar_kv_staleness(None, buf, 4, 2, 16, P.BF16, E, None) == P.ERR_INVALID_ARG
+    # zero rows is an empty call: nothing to launch
+    assert lib.polestar_kv_staleness(None, None, 0, 2, 16, P.BF16, None, None) == P.OK
+    # more rows than one launch grid holds
+    assert lib.polestar_kv_staleness(buf, buf, 1 << 31, 2, 16, P.BF16, E, None) == P.ERR_UNSUPPORTED
+    # no context
+    assert lib.polestar_full_forward(None, buf) == P.ERR_INVALID_ARG
+    assert lib.polestar_cache_staleness(None, None, E) == P.ERR_INVALID_ARG
