@@ -37,8 +37,9 @@ def _events():
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
 
-def run(name: str, steps: int, kernel_iters: int = 10) -> dict:
-    w = synth.WORKLOADS[name].replace(n_steps=None)
+def run(name: str, steps: int, kernel_iters: int = 10, **overrides) -> dict:
+    """overrides: workload fields to change (e.g. topk, the refresh budget k)."""
+    w = synth.WORKLOADS[name].replace(n_steps=None, **overrides)
     dt = synth.torch_dtype(w)
     W = synth.make_weights(w, "cuda")
     ctx = {"polestar": P.Polestar(w, W), "none": P.Polestar(w.replace(tau_upd=10 ** 6), W),
@@ -96,7 +97,7 @@ def run(name: str, steps: int, kernel_iters: int = 10) -> dict:
     k_bytes = nrow * (4 * w.n_kv_heads * w.head_dim * esz + 4)
     within = [r for r in rows if not r["entry"]]
     summary = dict(
-        workload=name, steps=len(rows), within_block_steps=len(within),
+        workload=name, topk=w.topk, K=w.K, steps=len(rows), within_block_steps=len(within),
         window_staleness={k: sum(r[k]["window_mean"] for r in within) / max(1, len(within))
                           for k in ("polestar", "none")},
         all_positions_staleness={k: sum(r[k]["all_mean"] for r in within) / max(1, len(within))
@@ -116,10 +117,11 @@ def main():
     ap.add_argument("--workload", default="llada8b_p512_g256_b1", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--json", default=None, help="also write the summary to this file")
+    ap.add_argument("--topk", type=int, default=None, help="refresh budget k (clusters refreshed per layer)")
     a = ap.parse_args()
     from drift_aware_kv_gb300.build import build
     build()
-    s = run(a.workload, a.steps)
+    s = run(a.workload, a.steps, **({"topk": a.topk} if a.topk is not None else {}))
     brief = {k: v for k, v in s.items() if k != "per_step"}
     print(json.dumps(brief))
     if a.json:
