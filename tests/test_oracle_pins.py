@@ -188,6 +188,49 @@ def test_attention_matches_torch_sdpa_gqa():
     assert np.allclose(p.sum(-1), 1.0, atol=1e-12)
 
 
+def test_attention_first_order_drift_of_proposition_1():
+    """App. B, Proposition 1: when position s's layer input moves from x_s to
+    x_s + eta (every other input fixed), the attention output of a position i
+    that attends to s changes by a_is W_V eta + a_is (q_i^T W_K eta / sqrt(dh))
+    (v_s - o_i) to first order.  The oracle's attention, fed keys W_K x and values
+    W_V x, must follow that derivative: the finite-difference remainder shrinks
+    like eps^2 (halving eps quarters it)."""
+    dh, d, N = 8, 12, 7
+    cfg = _tiny_cfg(n_heads=1, n_kv_heads=1, head_dim=dh, d_model=d)
+    orc = O.PolestarOracle.__new__(O.PolestarOracle)
+    orc.cfg, orc.bf16 = cfg, False
+    g = rng(21)
+    x = g.standard_normal((N, d))
+    WK, WV = g.standard_normal((dh, d)) * 0.4, g.standard_normal((dh, d))
+    q = g.standard_normal((N, 1, dh))
+    eta = g.standard_normal(d)
+    s_pos = 3
+
+    def outputs(xx):
+        kv = np.stack([xx @ WK.T, xx @ WV.T], axis=1)[:, :, None, :]  # [N, 2, 1, dh]
+        o, sc, lse = orc.attend(q, kv)
+        return o, np.exp(sc - lse[..., None])[:, 0, :]  # o [N, dh], a [N, N]
+
+    o0, a = outputs(x)
+    v_s = WV @ x[s_pos]
+    rem = []
+    for eps in (1e-3, 5e-4):
+        xe = x.copy()
+        xe[s_pos] += eps * eta
+        o1, _ = outputs(xe)
+        for i in range(N):
+            if i == s_pos:
+                continue
+            lin = a[i, s_pos] * (WV @ eta) + a[i, s_pos] * (q[i, 0] @ (WK @ eta)) / math.sqrt(dh) * (v_s - o0[i])
+            err = np.linalg.norm((o1[i] - o0[i]) - eps * lin)
+            # a dropped or mis-scaled first-order term would leave an O(eps) residue
+            assert err < 5.0 * eps * eps
+            rem.append(err)
+    half = len(rem) // 2
+    ratio = np.array(rem[half:]) / np.maximum(np.array(rem[:half]), 1e-300)
+    assert np.all((ratio > 0.2) & (ratio < 0.3))  # second-order remainder: about 1/4
+
+
 def test_kl_closed_forms_and_scipy():
     """KL of Eq. 4: zero for identical scores, non-negative, equal to
     scipy.special.rel_entr, and Pinsker's bound ||p-q||_1 <= sqrt(2 KL) (App. B,
