@@ -1444,6 +1444,23 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 
+extern "C" int32_t polestar_debug_attention_items(int32_t a0, int32_t na, int32_t b0, int32_t nb, int32_t max_rows,
+                                                 int32_t* out, int32_t cap) {
+  if (na < 0 || nb < 0 || max_rows < 1 || cap < 0 || (cap > 0 && !out)) return -1;
+  const int tot = na + nb;
+  const int k = tot > 0 ? (tot + max_rows - 1) / max_rows : 0;
+  if (k > cap) return -1;
+  std::vector<int4> w((size_t)k + 1);
+  const int n = attention_items(w.data(), 0, a0, na, b0, nb, max_rows);
+  for (int i = 0; i < n; ++i) {
+    out[4 * i + 0] = w[i].x;
+    out[4 * i + 1] = w[i].y;
+    out[4 * i + 2] = w[i].z;
+    out[4 * i + 3] = w[i].w;
+  }
+  return n;
+}
+
 extern "C" int32_t polestar_debug_attention_impl(int32_t impl) {
   if (impl < 0 || impl > 2) return -1;
   return attention_set_impl(impl);

@@ -309,7 +309,18 @@ polestar_status polestar_debug_attention(const void *q, const void *kv, int32_t 
  * invalid value.  Process-wide; not for concurrent use with running steps. */
 int32_t polestar_debug_attention_impl(int32_t impl);
 
-/* ---- row attention + KL drift that allocates nothing ----
+/* ---- attention work items (host only; test hook) ----
+ * The split of one sequence's attention rows into work items that the row
+ * attention kernels take one per CTA group: rows [a0, a0 + na) followed by
+ * [b0, b0 + nb) are cut into ceil((na + nb) / max_rows) items of near-equal size
+ * (at most max_rows rows each), in order; an item that straddles the two ranges
+ * holds {rowA, nA, rowB, nB}, otherwise {row, n, 0, 0}.  Writes the items to
+ * out[4 * i .. 4 * i + 3] (host array of cap items) and returns their number, or
+ * -1 for a negative count, max_rows < 1 or too small a cap.  No device work. */
+int32_t polestar_debug_attention_items(int32_t a0, int32_t na, int32_t b0, int32_t nb, int32_t max_rows,
+                                       int32_t *out, int32_t cap);
+
+/* ---- row attention + KL drift that allocates nothing ----/* ---- row attention + KL drift that allocates nothing ----
  * The paper has no counterpart to this call; it exists for callers that cannot
  * let a library allocate device memory: a host application that owns every
  * device allocation through its own pool or memory cap, or a latency-critical

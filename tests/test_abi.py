@@ -89,3 +89,42 @@ def test_staleness_entry_points_reject_bad_arguments_on_the_host():
     # no context
     assert lib.polestar_full_forward(None, buf) == P.ERR_INVALID_ARG
     assert lib.polestar_cache_staleness(None, None, E) == P.ERR_INVALID_ARG
+
+
+def _items(a0, na, b0, nb, max_rows, cap=None):
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    lib.polestar_debug_attention_items.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_void_p, ctypes.c_int32]
+    lib.polestar_debug_attention_items.restype = ctypes.c_int32
+    cap = cap if cap is not None else (na + nb) // max(1, max_rows) + 2
+    buf = (ctypes.c_int32 * (4 * max(cap, 1)))()
+    n = lib.polestar_debug_attention_items(a0, na, b0, nb, max_rows, buf, cap)
+    return n, [tuple(buf[4 * i: 4 * i + 4]) for i in range(max(n, 0))]
+
+
+@pytest.mark.parametrize("na,nb,max_rows", [(32, 104, 48), (32, 0, 48), (0, 13, 48), (136, 0, 128), (96, 8, 48),
+                                            (1, 1, 1), (768, 0, 48), (5, 200, 7)])
+def test_attention_work_items_cover_rows_once(na, nb, max_rows):
+    """Host-side scheduling of the row attention (no device): the rows of one
+    sequence, active rows [a0, a0 + na) then window/proxy rows [b0, b0 + nb), are
+    cut into ceil(total / max_rows) items in order, each at most max_rows rows and
+    within one row of each other, together covering every row exactly once."""
+    a0, b0 = 1000, 5000
+    n, items = _items(a0, na, b0, nb, max_rows)
+    tot = na + nb
+    assert n == -(-tot // max_rows)
+    rows = []
+    for x, cx, y, cy in items:
+        rows += list(range(x, x + cx)) + list(range(y, y + cy))
+        assert 1 <= cx + cy <= max_rows
+        assert cy == 0 or (x + cx == a0 + na and y == b0)  # only the straddling item has two parts
+    assert rows == list(range(a0, a0 + na)) + list(range(b0, b0 + nb))
+    sizes = [cx + cy for _, cx, _, cy in items]
+    assert max(sizes) - min(sizes) <= 1
+
+
+def test_attention_work_items_reject_bad_arguments():
+    assert _items(0, -1, 0, 4, 48)[0] == -1
+    assert _items(0, 4, 0, 4, 0)[0] == -1
+    assert _items(0, 200, 0, 0, 48, cap=2)[0] == -1  # needs 5 items
+    assert _items(0, 0, 0, 0, 48)[0] == 0
