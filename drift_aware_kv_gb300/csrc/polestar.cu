@@ -304,14 +304,33 @@ T* meta_h(polestar_ctx* c, size_t off) { return (T*)(c->meta_h + off); }
 template <typename T>
 T* meta_d(polestar_ctx* c, size_t off) { return (T*)(c->meta_d + off); }
 
+// Local window of block blk (§4.1): the block is [start, end); the window holds
+// the `prefix` positions before it and the `suffix` positions after it that lie
+// inside [0, N), in position order.
+void window_of(int prompt_len, int N, int B, int prefix, int suffix, int blk, int* start, int* end,
+               std::vector<int>& pos) {
+  *start = prompt_len + blk * B;
+  *end = *start + B;
+  pos.clear();
+  for (int p = *start - prefix; p < *start; ++p)
+    if (p >= 0) pos.push_back(p);
+  for (int p = *end; p < *end + suffix; ++p)
+    if (p < N) pos.push_back(p);
+}
+
+// tau_upd trigger of one sequence (§4.1 "Update Schedule"): the tokens unmasked
+// since the last refresh accumulate, this step's included; the refresh fires
+// when they exceed tau_upd, and the count starts again.
+bool trigger_step(int& cum, int n_unmasked, int tau_upd) {
+  cum += n_unmasked;
+  const bool fire = cum > tau_upd;
+  if (fire) cum = 0;
+  return fire;
+}
+
 void compute_window(polestar_ctx* c, int blk) {
-  c->start = c->cfg.prompt_len + blk * c->B;
-  c->end = c->start + c->B;
-  c->win_pos.clear();
-  for (int p = c->start - c->cfg.prefix_win; p < c->start; ++p)
-    if (p >= 0) c->win_pos.push_back(p);
-  for (int p = c->end; p < c->end + c->cfg.suffix_win; ++p)
-    if (p < c->N) c->win_pos.push_back(p);
+  window_of(c->cfg.prompt_len, c->N, c->B, c->cfg.prefix_win, c->cfg.suffix_win, blk, &c->start, &c->end,
+            c->win_pos);
   c->nw = (int)c->win_pos.size();
 }
 
@@ -686,12 +705,8 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
   // refresh exceed tau_upd
   std::vector<int> fire_seqs;
   for (int s = 0; s < b; ++s) {
-    c->cum[s] += n_unmasked ? n_unmasked[s] : 0;
-    c->fire[s] = c->cum[s] > c->cfg.tau_upd;
-    if (c->fire[s]) {
-      c->cum[s] = 0;
-      fire_seqs.push_back(s);
-    }
+    c->fire[s] = trigger_step(c->cum[s], n_unmasked ? n_unmasked[s] : 0, c->cfg.tau_upd);
+    if (c->fire[s]) fire_seqs.push_back(s);
   }
   const int n_fire = (int)fire_seqs.size();
   c->gemm_cls = POLESTAR_KC_GEMM_STEP;
@@ -1442,6 +1457,33 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   cudaFree(d_rows);
   cudaFree(d_work);
   return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+
+extern "C" int32_t polestar_debug_window(int32_t prompt_len, int32_t gen_len, int32_t block, int32_t prefix_win,
+                                        int32_t suffix_win, int32_t block_index, int32_t* span, int32_t* pos,
+                                        int32_t cap) {
+  if (prompt_len < 0 || gen_len < 1 || block < 1 || gen_len % block || prefix_win < 0 || suffix_win < 0 ||
+      block_index < 0 || block_index >= gen_len / block || !span || cap < 0 || (cap > 0 && !pos))
+    return -1;
+  std::vector<int> w;
+  int start = 0, end = 0;
+  window_of(prompt_len, prompt_len + gen_len, block, prefix_win, suffix_win, block_index, &start, &end, w);
+  if ((int)w.size() > cap) return -1;
+  span[0] = start;
+  span[1] = end;
+  for (size_t i = 0; i < w.size(); ++i) pos[i] = w[i];
+  return (int32_t)w.size();
+}
+
+extern "C" polestar_status polestar_debug_trigger(int32_t tau_upd, const int32_t* n_unmasked, int32_t steps,
+                                                  uint8_t* fire) {
+  if (steps < 0 || (steps > 0 && (!n_unmasked || !fire))) return POLESTAR_ERR_INVALID_ARG;
+  int cum = 0;
+  for (int t = 0; t < steps; ++t) {
+    if (n_unmasked[t] < 0) return POLESTAR_ERR_INVALID_ARG;
+    fire[t] = trigger_step(cum, n_unmasked[t], tau_upd) ? 1 : 0;
+  }
+  return POLESTAR_OK;
 }
 
 extern "C" int32_t polestar_debug_attention_items(int32_t a0, int32_t na, int32_t b0, int32_t nb, int32_t max_rows,

@@ -26,7 +26,8 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc",
             "polestar_packed_weight_bytes", "polestar_pack_weights", "polestar_debug_gemm_choice",
             "polestar_debug_attention_impl", "polestar_debug_gemm_swiglu", "polestar_full_forward",
-            "polestar_kv_staleness", "polestar_cache_staleness", "polestar_debug_attention_items")
+            "polestar_kv_staleness", "polestar_cache_staleness", "polestar_debug_attention_items",
+            "polestar_debug_window", "polestar_debug_trigger")
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
 

@@ -309,7 +309,23 @@ polestar_status polestar_debug_attention(const void *q, const void *kv, int32_t 
  * invalid value.  Process-wide; not for concurrent use with running steps. */
 int32_t polestar_debug_attention_impl(int32_t impl);
 
-/* ---- attention work items (host only; test hook) ----
+/* ---- window and trigger (host only; test hooks) ----
+ * polestar_debug_window: the local window of block `block_index` (§4.1) as the
+ * library computes it for a context with these sizes: span[0..1] = the block's
+ * positions [start, end); pos[] (host, cap entries) = the prefix_win positions
+ * before the block and the suffix_win positions after it that lie inside
+ * [0, prompt_len + gen_len), in order.  Returns their number, or -1 for sizes
+ * that polestar_init would reject, a block index out of range or too small a
+ * cap.
+ * polestar_debug_trigger: the tau_upd refresh trigger of §4.1 "Update
+ * Schedule" for one sequence over `steps` within-block steps that start right
+ * after a block entry: n_unmasked[t] (host) tokens unmasked since the previous
+ * step; fire[t] (host) = 1 when the refresh runs at step t.  No device work. */
+int32_t polestar_debug_window(int32_t prompt_len, int32_t gen_len, int32_t block, int32_t prefix_win,
+                              int32_t suffix_win, int32_t block_index, int32_t *span, int32_t *pos, int32_t cap);
+polestar_status polestar_debug_trigger(int32_t tau_upd, const int32_t *n_unmasked, int32_t steps, uint8_t *fire);
+
+/* ---- attention work items (host only; test hook) ----/* ---- attention work items (host only; test hook) ----
  * The split of one sequence's attention rows into work items that the row
  * attention kernels take one per CTA group: rows [a0, a0 + na) followed by
  * [b0, b0 + nb) are cut into ceil((na + nb) / max_rows) items of near-equal size

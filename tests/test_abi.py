@@ -128,3 +128,60 @@ def test_attention_work_items_reject_bad_arguments():
     assert _items(0, 4, 0, 4, 0)[0] == -1
     assert _items(0, 200, 0, 0, 48, cap=2)[0] == -1  # needs 5 items
     assert _items(0, 0, 0, 0, 48)[0] == 0
+
+
+def _window(prompt_len, gen_len, block, pre, suf, b):
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    lib.polestar_debug_window.argtypes = [ctypes.c_int32] * 6 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+    lib.polestar_debug_window.restype = ctypes.c_int32
+    span = (ctypes.c_int32 * 2)()
+    pos = (ctypes.c_int32 * 512)()
+    n = lib.polestar_debug_window(prompt_len, gen_len, block, pre, suf, b, span, pos, 512)
+    return n, (span[0], span[1]), list(pos[: max(n, 0)])
+
+
+def test_library_window_equals_oracle_window_for_every_workload_block():
+    """Local window (§4.1, clipped at the sequence ends): the library's host
+    computation against the oracle's, for every block of every workload."""
+    from drift_aware_kv_gb300 import synth
+    from oracle import polestar_oracle as O
+    for w in synth.WORKLOADS.values():
+        orc = O.PolestarOracle.__new__(O.PolestarOracle)
+        orc.cfg, orc.N = w, w.seq_len
+        for b in range(w.n_blocks):
+            n, span, pos = _window(w.prompt_len, w.gen_len, w.block, w.prefix_win, w.suffix_win, b)
+            assert span == orc._span(b) and pos == orc.window(b) and n == len(pos)
+            assert pos == synth.window_positions(w, b)
+
+
+def test_window_edges_closed_form():
+    # prompt shorter than the prefix window: the prefix is clipped at position 0
+    n, span, pos = _window(16, 64, 32, 64, 32, 0)
+    assert span == (16, 48) and pos == list(range(0, 16)) + list(range(48, 80))
+    # last block: no suffix past the sequence end
+    n, span, pos = _window(64, 128, 32, 64, 32, 3)
+    assert span == (160, 192) and pos == list(range(96, 160))
+    assert _window(64, 128, 32, 64, 32, 4)[0] == -1  # block index out of range
+
+
+@pytest.mark.parametrize("tau,ns,expect", [
+    (3, [1, 1, 1, 1, 1], [0, 0, 0, 1, 0]),      # cumulative count passes tau_upd at the 4th token
+    (3, [4, 0, 4], [1, 0, 1]),                   # more than tau_upd in one step
+    (3, [3, 0, 1, 3, 3], [0, 0, 1, 0, 1]),       # exactly tau_upd does not fire; reset after firing
+    (0, [0, 1, 0, 2], [0, 1, 0, 1]),             # tau_upd = 0: any unmasked token fires
+    (10 ** 6, [6] * 8, [0] * 8),                 # out of reach: never
+])
+def test_trigger_closed_form(tau, ns, expect):
+    """The tau_upd trigger of §4.1 "Update Schedule": refresh after a step that
+    unmasks more than tau_upd tokens, or once the tokens unmasked since the last
+    refresh exceed tau_upd (this step's count included); the count restarts."""
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    lib.polestar_debug_trigger.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+    arr = (ctypes.c_int32 * len(ns))(*ns)
+    out = (ctypes.c_uint8 * len(ns))()
+    assert lib.polestar_debug_trigger(tau, arr, len(ns), out) == P.OK
+    assert list(out) == expect
+    neg = (ctypes.c_int32 * 1)(-1)
+    assert lib.polestar_debug_trigger(tau, neg, 1, out) == P.ERR_INVALID_ARG
