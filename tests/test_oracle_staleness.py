@@ -139,3 +139,14 @@ def test_study_polestar_is_fresher_than_no_refresh():
     assert np.all(none[-1] > 0)
     # over the whole run and at every layer, the refreshed cache is fresher
     assert np.all(pol.mean(axis=0) < none.mean(axis=0))
+
+
+def test_study_refresh_budget_and_trigger_move_staleness_monotonically():
+    """The two knobs of Polestar-Cache (Table 5): refreshing more clusters per layer
+    (k) keeps the window fresher, and a higher refresh trigger tau_upd (fewer
+    refreshes) lets it go staler; tau_upd out of reach is block-wise reuse."""
+    base = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(n_layers=2)
+    by_k = [float(_study(base.replace(topk=k), "polestar", 12)[0].mean()) for k in (1, 4, 8)]
+    by_tau = [float(_study(base.replace(tau_upd=t), "polestar", 12)[0].mean()) for t in (3, 4, 10 ** 6)]
+    assert by_k[0] > by_k[1] > by_k[2] > 0
+    assert by_tau[0] < by_tau[1] < by_tau[2]
