@@ -88,3 +88,34 @@ def test_mini_bf16_runs(name):
         for rec in recs:
             if "act_out" in rec:
                 assert np.all(np.isfinite(rec["act_out"]))
+
+
+def test_incremental_centroid_update_closed_form_at_layer_0():
+    """§4.1 "Compute Update Packets" with the readings R5/R6: at layer 0 the update
+    packet of every window row is the caller's current input, and a refreshing
+    step patches all of them, so with an exact cache the member sums become
+    s_c = sum over members of x_i / |x_i| of this step's inputs (the K-means sums
+    at block entry minus the old directions plus the new), and z_c = s_c / |s_c|."""
+    cfg = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(n_layers=2)
+    W = O.weights_to_numpy(synth.make_weights(cfg))
+    orc = O.PolestarOracle(cfg, W, exact_cache=True)
+    tr = synth.Trajectory(cfg)
+    checked = 0
+    for _ in range(10):
+        st = tr.next_step()
+        x0 = st["x0"].double().numpy()
+        rec = orc.calibrate_step(x0, st["n_unmasked"], st["block_index"], st["block_entry"])[0]
+        if st["block_entry"] or not rec["fire"]:
+            continue
+        s0 = orc.seqs[0]
+        X = x0[0][orc.window(st["block_index"])]
+        Xh = X / np.linalg.norm(X, axis=1, keepdims=True)
+        for c in range(cfg.K):
+            mem = s0.labels[0] == c
+            if not mem.any():
+                continue
+            assert np.allclose(s0.s[0][c], Xh[mem].sum(0), rtol=1e-10, atol=1e-10)
+            zc = Xh[mem].sum(0)
+            assert np.allclose(s0.z[0][c], zc / np.linalg.norm(zc), rtol=1e-10, atol=1e-12)
+        checked += 1
+    assert checked >= 3
