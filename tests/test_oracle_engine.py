@@ -119,3 +119,50 @@ def test_incremental_centroid_update_closed_form_at_layer_0():
             assert np.allclose(s0.z[0][c], zc / np.linalg.norm(zc), rtol=1e-10, atol=1e-12)
         checked += 1
     assert checked >= 3
+
+
+def test_proxy_query_of_a_token_at_position_0_equals_its_query():
+    """§4.1 "Measuring Drift" with reading R2: a proxy query is W_q RMSNorm(z_c)
+    with no rotary (a centroid has no position).  The rotary of position 0 is the
+    identity, so a proxy built from the input of the token at position 0 scores
+    every key exactly as that token's own query does."""
+    cfg = synth.WORKLOADS["tiny_l1_d256_fp32"]
+    W = O.weights_to_numpy(synth.make_weights(cfg))
+    orc = O.PolestarOracle(cfg, W)
+    tr = synth.Trajectory(cfg)
+    st = tr.next_step()
+    x0 = st["x0"].double().numpy()
+    orc.calibrate_step(x0, st["n_unmasked"], 0, True)
+    kv = orc.seqs[0].kv[0]
+    h0 = x0[0, :1]
+    s_proxy, lse_proxy = orc.proxy_scores(0, h0, kv)
+    q, _, _ = orc.qkv(0, h0, np.array([0]))
+    s_tok = orc.scores(q, kv)
+    assert np.allclose(s_proxy, s_tok, rtol=1e-12, atol=1e-12)
+    # any other position rotates the query: scores differ
+    q7, _, _ = orc.qkv(0, h0, np.array([7]))
+    assert not np.allclose(orc.scores(q7, kv), s_tok, atol=1e-6)
+
+
+def test_oracle_trigger_equals_library_host_trigger():
+    """The oracle's refresh decisions over a trajectory equal the library's host
+    trigger (polestar_debug_trigger) fed the same unmasked counts, block by block."""
+    import ctypes
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    lib.polestar_debug_trigger.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+    for tau in (0, 3, 5):
+        cfg = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(tau_upd=tau)
+        orc, out = _run(cfg)
+        blocks = {}
+        for st, recs, _ in out:
+            if st["block_entry"]:
+                blocks[st["block_index"]] = ([], [])
+            else:
+                blocks[st["block_index"]][0].append(st["n_unmasked"][0])
+                blocks[st["block_index"]][1].append(bool(recs[0]["fire"]))
+        for ns, fires in blocks.values():
+            arr = (ctypes.c_int32 * max(1, len(ns)))(*ns)
+            res = (ctypes.c_uint8 * max(1, len(ns)))()
+            assert lib.polestar_debug_trigger(tau, arr, len(ns), res) == P.OK
+            assert [bool(v) for v in list(res)[:len(ns)]] == fires
