@@ -21,7 +21,11 @@ Parity status per function (what pins it, see tests/test_oracle_*.py):
   spherical kmeans pinned (brute force on tiny inputs, unit norms, objective monotone)
   top-k            pinned (full sort)
   NVFP4 residual   pinned (grid membership, round trip, error bound, Table 11 ordering)
-  commit gate      pinned (worked value c=0.8 -> tau_d=0.1, limits)
+  commit gate      pinned (worked value c=0.8 -> tau_d=0.1, limits; closed-form cases of the
+                   current-block, history, suffix and block-entry rules)
+  centroid update  pinned (exact cache: layer-0 member sums equal the closed form)
+  proxy query      pinned (no rotary: equals the position-0 token's query)
+  trigger          pinned (equals the library's host trigger on the same counts)
   confidence       pinned (generator's target max-probability)
   sparse refresh   pinned (k = K, exact cache: equals the block-entry forward)
   KV staleness     pinned (closed forms: 0 on itself, 2 on the negation, per-head rotation)
