@@ -314,9 +314,9 @@ int32_t polestar_debug_attention_impl(int32_t impl);
  * library computes it for a context with these sizes: span[0..1] = the block's
  * positions [start, end); pos[] (host, cap entries) = the prefix_win positions
  * before the block and the suffix_win positions after it that lie inside
- * [0, prompt_len + gen_len), in order.  Returns their number, or -1 for sizes
- * that polestar_init would reject, a block index out of range or too small a
- * cap.
+ * [0, prompt_len + gen_len), in order.  Returns their number, or -1 for a
+ * negative size, a generation length that is not a positive whole number of
+ * blocks, a block index out of range or too small a cap.
  * polestar_debug_trigger: the tau_upd refresh trigger of §4.1 "Update
  * Schedule" for one sequence over `steps` within-block steps that start right
  * after a block entry: n_unmasked[t] (host) tokens unmasked since the previous
