@@ -37,8 +37,9 @@ def _events():
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
 
-def run(name: str, steps: int, kernel_iters: int = 10, **overrides) -> dict:
-    """overrides: workload fields to change (e.g. topk, the refresh budget k)."""
+def run(name: str, steps: int, kernel_iters: int = 10, progress: bool = False, **overrides) -> dict:
+    """overrides: workload fields to change (e.g. topk, the refresh budget k);
+    progress: print each step's record to stderr as it completes."""
     w = synth.WORKLOADS[name].replace(n_steps=None, **overrides)
     dt = synth.torch_dtype(w)
     W = synth.make_weights(w, "cuda")
@@ -84,6 +85,10 @@ def run(name: str, steps: int, kernel_iters: int = 10, **overrides) -> dict:
             rec[k] = dict(window_mean=float(ew.mean()), window_per_layer=[round(float(v), 6) for v in ew],
                           all_mean=float(E[k].mean()))
         rows.append(rec)
+        if progress:
+            print(json.dumps({"t": rec["t"], "block": rec["block"], "entry": rec["entry"],
+                              "polestar": round(rec["polestar"]["window_mean"], 6),
+                              "none": round(rec["none"]["window_mean"], 6)}), file=sys.stderr, flush=True)
     # the staleness kernel alone (cache pair already resident)
     e0, e1 = _events()
     e0.record(stream)
@@ -118,10 +123,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--json", default=None, help="also write the summary to this file")
     ap.add_argument("--topk", type=int, default=None, help="refresh budget k (clusters refreshed per layer)")
+    ap.add_argument("--progress", action="store_true", help="print every step's staleness to stderr")
     a = ap.parse_args()
     from drift_aware_kv_gb300.build import build
     build()
-    s = run(a.workload, a.steps, **({"topk": a.topk} if a.topk is not None else {}))
+    s = run(a.workload, a.steps, progress=a.progress, **({"topk": a.topk} if a.topk is not None else {}))
     brief = {k: v for k, v in s.items() if k != "per_step"}
     print(json.dumps(brief))
     if a.json:
