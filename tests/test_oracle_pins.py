@@ -106,6 +106,17 @@ def test_nvfp4_grid_membership_and_error_bound():
     assert np.all((err <= bound * (1 + 1e-6)) | amax_over)
 
 
+def test_nvfp4_encode_of_decoded_is_identity():
+    """App. C.3: a group's scale is E4M3(amax / 6), so its largest element always
+    encodes to 6 (amax / s lies within E4M3's relative step of 6); re-encoding the
+    decoded group therefore finds the same scale and the same codes."""
+    r = O.to_f32(rng(10).standard_normal((32, 128)) * rng(11).uniform(1e-3, 50, (32, 1)))
+    codes, sb, _ = O.nvfp4_encode(r)
+    assert np.all(np.max(codes.reshape(32, 8, 16) & 7, axis=-1) == 7)  # index 7 is magnitude 6
+    c2, s2, _ = O.nvfp4_encode(O.nvfp4_decode(codes, sb))
+    assert np.array_equal(c2, codes) and np.array_equal(s2, sb)
+
+
 def test_nvfp4_zero_group_and_sign():
     r = np.zeros((1, 32))
     r[0, 16:] = rng(8).standard_normal(16)
