@@ -5,7 +5,29 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace polestar {
+
+// ---- kernel attributes, once per device -------------------------------------------
+// A kernel attribute (dynamic shared memory limit, non-portable cluster size)
+// applies to the device that is current when it is set, so each launch site
+// keeps one flag per device and sets the attribute the first time it launches
+// on that device.
+struct PerDeviceOnce {
+  static constexpr int kDevices = 64;
+  std::atomic<bool> done[kDevices] = {};
+};
+inline cudaError_t func_attr_once(PerDeviceOnce& once, const void* func, cudaFuncAttribute attr, int value) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= PerDeviceOnce::kDevices) return cudaFuncSetAttribute(func, attr, value);
+  if (once.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, attr, value);
+  if (e == cudaSuccess) once.done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // ---- storage types: fp32 or bf16, arithmetic always fp32 ---------------------
 template <typename T>

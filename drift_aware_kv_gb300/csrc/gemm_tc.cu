@@ -706,535 +706,6 @@ __global__ void __launch_bounds__(THREADS)
   }
 }
 
-// ---------------------------------------------------------------- persistent stream-K, weight-stationary
-// One CTA per SM.  The (tile, k-tile) units of all weight segments are laid
-// out tile-major and cut into gridDim.x equal contiguous ranges, so every SM
-// streams the same number of weight bytes and its load ring never drains at a
-// tile boundary.  A CTA's run of units inside one tile is a "piece"; pieces
-// alternate between two TMEM accumulators so the epilogue of one overlaps the
-// MMAs of the next.  A tile covered by one piece is written straight to C.  A
-// tile cut between CTAs is finished by whichever of them arrives last at the
-// tile's counter: every piece is stored to the workspace first, and the last
-// arrival adds the others to its own in CTA order (deterministic; no CTA ever
-// waits for another).  A CTA takes its (possibly cut) first and last tiles
-// before its whole middle tiles, so both holders of a cut tile reach it early
-// and the fix-up overlaps the weight stream instead of trailing it.
-//
-// Weights come either through the 2D tensor map (128-byte row segments of 128
-// rows per load) or, when the caller supplies them in the packed tile layout
-// (pack_weight_tiles), as one contiguous 16 KB bulk copy per unit: a CTA's
-// units are then one contiguous stretch of memory.
-constexpr int SK_MAX_STAGES = 12;
-constexpr int UNIT_BYTES = BN * BK * 2;  // one packed 128 x 64 bf16 tile: 16 KB
-
-struct SkParams {
-  int M;
-  const int* m_dev;
-  int ldc;
-  int ktiles;        // k-tiles per tile
-  long long units;   // tiles * ktiles
-  int* err;
-  int seg_start[4];
-  int seg_N[3];
-  float* seg_C[3];
-  const uint8_t* wpack[3];  // packed weights per segment (null: tensor map)
-  int np, stages, acc_cols;
-  float* work;       // [gridDim.x][2][np][BN] partial pieces
-  int* counters;     // [tiles][4] arrivals per tile and epilogue warp, zero between launches
-};
-
-__device__ __forceinline__ long long sk_start(int c, long long units, int G) { return (long long)c * units / G; }
-
-// CTA whose unit range holds unit u
-__device__ __forceinline__ int sk_owner(long long u, long long units, int G) {
-  int c = (int)((u * G) / units);
-  while (c + 1 < G && sk_start(c + 1, units, G) <= u) ++c;
-  while (c > 0 && sk_start(c, units, G) > u) --c;
-  return c;
-}
-
-// Tile of the CTA's piece number `idx`: first tile, last tile, then the middle.
-__device__ __forceinline__ int sk_piece_tile(int idx, int t_first, int t_last) {
-  if (idx == 0) return t_first;
-  if (idx == 1) return t_last;
-  return t_first + idx - 1;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Warp roles: 0 and 6 load (each owns every other unit of the ring, so one
-// late copy never holds up the other stream of requests), 1 issues the MMAs,
-// 2-5 drain TMEM.
-constexpr int SK_THREADS = 224;
-
-template <bool PACKED>
-__global__ void __launch_bounds__(SK_THREADS, 1)
-    gemm_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, SkParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const int NP = p.np, STAGES = p.stages;
-  const int STAGE_BYTES = ws_stage_bytes(NP);
-  uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + SK_MAX_STAGES;
-  uint64_t* acc_full = empty + SK_MAX_STAGES;  // [2]
-  uint64_t* acc_empty = acc_full + 2;          // [2]
-  uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
-  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x, cta = blockIdx.x;
-  const long long u0 = sk_start(cta, p.units, G), u1 = sk_start(cta + 1, p.units, G);
-  const int kt = p.ktiles;
-  const int t_first = (int)(u0 / kt), t_last = (int)((u1 - 1) / kt);
-  const int npieces = t_last - t_first + 1;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), 4);
-    }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(2 * p.acc_cols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tmem_slot;
-
-  // unit range of a piece
-  auto piece_units = [&](int idx, int& t, long long& ua, long long& ub) {
-    t = sk_piece_tile(idx, t_first, t_last);
-    ua = max(u0, (long long)t * kt);
-    ub = min(u1, (long long)(t + 1) * kt);
-  };
-  // weight load of unit u (tile t) into the stage at smem address dst
-  auto load_w = [&](long long u, int t, uint32_t dst, uint32_t bar) {
-    const int sg = (t >= p.seg_start[1]) + (t >= p.seg_start[2]);
-    const int kk = (int)(u - (long long)t * kt);
-    if (PACKED) {
-      const uint8_t* src = p.wpack[sg] + ((size_t)(t - p.seg_start[sg]) * kt + kk) * UNIT_BYTES;
-      bulk_load_1d(dst, src, UNIT_BYTES, bar);
-    } else {
-      const CUtensorMap* map = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
-      tma_load_2d(dst, map, kk * BK, (t - p.seg_start[sg]) * BN, bar);
-    }
-  };
-
-  if (warp == 0 || warp == 6) {
-    // ---------------- producers: unit i of the CTA's piece order goes to warp 0
-    // when i is even, to warp 6 when odd
-    const int pw = warp == 0 ? 0 : 1;
-    if (lane == 0) {
-      // weights do not depend on the preceding kernel: the first stages' weight
-      // copies go out before waiting for the producer of A
-      int i = 0;
-      for (int pc = 0; pc < npieces && i < STAGES; ++pc) {
-        int t;
-        long long ua, ub;
-        piece_units(pc, t, ua, ub);
-        for (long long u = ua; u < ub && i < STAGES; ++u, ++i) {
-          if ((i & 1) != pw) continue;
-          const uint32_t fb = smem_u32(&full[i]);
-          mbar_expect_tx(fb, STAGE_BYTES);
-          load_w(u, t, smem_u32(smem + i * STAGE_BYTES), fb);
-        }
-      }
-      pdl_wait();
-      i = 0;
-      bool alive = true;
-      for (int pc = 0; pc < npieces && alive; ++pc) {
-        int t;
-        long long ua, ub;
-        piece_units(pc, t, ua, ub);
-        for (long long u = ua; u < ub; ++u, ++i) {
-          if ((i & 1) != pw) continue;
-          const int s = i % STAGES;
-          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-          const uint32_t fb = smem_u32(&full[s]);
-          const int kx = (int)(u - (long long)t * kt) * BK;
-          if (i >= STAGES) {
-            if (!mbar_wait(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1, p.err, 1, abort_flag)) {
-              alive = false;
-              break;
-            }
-            mbar_expect_tx(fb, STAGE_BYTES);
-            load_w(u, t, st, fb);
-          }
-          tma_load_2d(st + WS_W_BYTES, &tmA, kx, 0, fb);
-        }
-      }
-    }
-    pdl_launch_dependents();
-  } else {
-    pdl_launch_dependents();
-    pdl_wait();
-  }
-  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
-  const int np_eff = min(NP, max(16, (M_eff + 15) & ~15));
-
-  if (warp == 1) {
-    // ---------------- MMA issuer: pieces alternate between the two accumulators
-    if (lane == 0) {
-      const uint32_t idesc = instr_desc_ws(np_eff);
-      int i = 0;
-      bool alive = true;
-      for (int pc = 0; pc < npieces && alive; ++pc) {
-        int t;
-        long long ua, ub;
-        piece_units(pc, t, ua, ub);
-        const int b = pc & 1, use = pc >> 1;
-        if (use > 0 && !mbar_wait(smem_u32(&acc_empty[b]), (use - 1) & 1, p.err, 4, abort_flag)) break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t dacc = tmem + b * p.acc_cols;
-        for (long long u = ua; u < ub; ++u, ++i) {
-          const int s = i % STAGES;
-          if (!mbar_wait(smem_u32(&full[s]), (i / STAGES) & 1, p.err, 2, abort_flag)) {
-            alive = false;
-            break;
-          }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_id(dacc, smem_desc(st + kk * 32), smem_desc(st + WS_W_BYTES + kk * 32), idesc,
-                    (u > ua || kk > 0) ? 1u : 0u);
-          umma_commit(smem_u32(&empty[s]));
-        }
-        if (!alive) break;
-        umma_commit(smem_u32(&acc_full[b]));
-      }
-    }
-  } else if (warp >= 2 && warp <= 5) {
-    // ---------------- epilogue: TMEM lane = feature, column = row
-    const int q = warp & 3;
-    const int fl = q * 32 + lane;  // feature within the tile
-    for (int pc = 0; pc < npieces; ++pc) {
-      int t;
-      long long ua, ub;
-      piece_units(pc, t, ua, ub);
-      const int b = pc & 1, use = pc >> 1;
-      const bool ok = mbar_wait(smem_u32(&acc_full[b]), use & 1, p.err, 3, abort_flag);
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      if (!ok) break;
-      const int sg = (t >= p.seg_start[1]) + (t >= p.seg_start[2]);
-      const int n0 = (t - p.seg_start[sg]) * BN;
-      const int segN = p.seg_N[sg];
-      float* const Cseg = p.seg_C[sg];
-      const int f = n0 + fl;
-      const int cf = sk_owner((long long)t * kt, p.units, G);
-      const int cl = sk_owner((long long)(t + 1) * kt - 1, p.units, G);
-      const uint32_t tq = tmem + b * p.acc_cols + ((uint32_t)(q * 32) << 16);
-      const bool whole = cf == cl;
-      // piece of a cut tile: [feature][row] fp32, so a lane's rows are contiguous
-      float* wk = p.work + ((size_t)cta * 2 + (t == t_first ? 0 : 1)) * NP * BN + (size_t)fl * NP;
-#pragma unroll 1
-      for (int c = 0; c < np_eff; c += 16) {
-        float v[16];
-        tmem_ld16(tq + c, v);
-        if (whole) {
-          if (f < segN) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c + j < M_eff) Cseg[(size_t)(c + j) * p.ldc + f] = v[j];
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) *(float4*)(wk + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        }
-      }
-      // accumulator drained: hand it back to the MMA warp
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
-      if (whole) continue;
-      // cut tile: count this warp's arrival (each warp has its own counter, so
-      // no epilogue warp ever waits for another one)
-      __threadfence();
-      __syncwarp();
-      int arrived = 0;
-      if (lane == 0) arrived = atomicAdd(&p.counters[t * 4 + q], 1) + 1;
-      arrived = __shfl_sync(0xffffffffu, arrived, 0);
-      if (arrived != cl - cf + 1) continue;
-      // last arrival: sum every piece in CTA order, 32 rows of up to four
-      // pieces in flight per load round
-      __threadfence();
-      const int mend = min(M_eff, np_eff);
-#pragma unroll 1
-      for (int m0 = 0; m0 < mend; m0 += 32) {
-        float4 acc[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-        for (int c0 = cf; c0 <= cl; c0 += 4) {
-          float4 v[4][8];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int c = c0 + x;
-            if (c > cl) continue;
-            const int slot = (t == (int)(sk_start(c, p.units, G) / kt)) ? 0 : 1;
-            const float* src = p.work + ((size_t)c * 2 + slot) * NP * BN + (size_t)fl * NP + m0;
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-              v[x][r] = (m0 + 4 * r < np_eff) ? __ldcg((const float4*)(src + 4 * r)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            if (c0 + x > cl) continue;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              acc[r].x += v[x][r].x;
-              acc[r].y += v[x][r].y;
-              acc[r].z += v[x][r].z;
-              acc[r].w += v[x][r].w;
-            }
-          }
-        }
-        if (f < segN) {
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const float e[4] = {acc[r].x, acc[r].y, acc[r].z, acc[r].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (m0 + 4 * r + j < mend) Cseg[(size_t)(m0 + 4 * r + j) * p.ldc + f] = e[j];
-          }
-        }
-      }
-      if (lane == 0) p.counters[t * 4 + q] = 0;
-    }
-  }
-  if (*abort_flag && (warp == 0 || warp == 6) && lane == 0) {
-    const long long t0 = clock64();
-    while (clock64() - t0 < 20000000LL) {
-    }
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  if (warp == 1) {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * p.acc_cols));
-  }
-}
-
-// ---------------------------------------------------------------- persistent pair tiles
-// For many row groups (block entries, large batches) the GEMM is bound by the
-// tensor cores, and what matters is keeping every SM's MMA pipe busy:
-//   * a thread-block cluster of two CTAs walks output tiles of 256 rows x bn
-//     columns (rows fastest, so concurrently running clusters share weight
-//     tiles in L2); CTA r of the pair owns rows [128 r, 128 r + 128) of the tile;
-//   * each CTA loads its own 128 x 64 A box and one half of the bn x 64 W box,
-//     multicast into both CTAs' stage (each weight tile is fetched once per
-//     pair); a stage is released when the MMAs of BOTH CTAs have read it, so
-//     every MMA commit arrives on the stage barrier of both CTAs;
-//   * two TMEM accumulators (2 x bn columns): the epilogue warps drain tile i
-//     while the MMA warp accumulates tile i + 1, so the tensor pipe never waits
-//     for the fp32 stores.
-// Warp roles as in the row-tiled kernel: 0 loads, 1 issues MMAs, 2-5 drain.
-constexpr int PC_MAX_STAGES = 8;
-__host__ __device__ constexpr int pc_stage_bytes(int bn) { return BM * BK * 2 + bn * BK * 2; }
-__host__ __device__ constexpr int pc_smem_bytes(int bn, int stages) { return stages * pc_stage_bytes(bn) + 2048; }
-
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
-      "%3}], [%4], %5;" ::"r"(dst),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-// Arrive on the same barrier of every CTA in `mask` once this thread's MMAs finish.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_pc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  constexpr int A_BYTES = BM * BK * 2;
-  const int STAGES = p.stages, bn = p.bn;
-  const int SB = pc_stage_bytes(bn);
-  uint64_t* full = (uint64_t*)(smem + STAGES * SB);
-  uint64_t* empty = full + PC_MAX_STAGES;
-  uint64_t* acc_full = empty + PC_MAX_STAGES;  // [2]
-  uint64_t* acc_empty = acc_full + 2;          // [2]
-  uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
-  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = (int)cluster_rank();  // 0 or 1 within the pair
-  const int cid = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
-  constexpr uint16_t PAIR = 3;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 2);  // the MMA warps of both CTAs
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), 4);
-    }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(p.tmem_cols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tmem_slot;
-  // the peer multicasts into this CTA's stages and arrives on its barriers
-  cluster_sync();
-  pdl_launch_dependents();
-  pdl_wait();
-  const int M_eff = p.m_dev ? min(p.M, *p.m_dev) : p.M;
-  const int mpairs = (M_eff + 2 * BM - 1) / (2 * BM);
-  const long long ntiles = (long long)mpairs * p.ntn;
-  const int nk = p.ktiles;
-
-  if (warp == 0) {
-    // ---------------- TMA producer: own A box, half the W box to both CTAs
-    if (lane == 0) {
-      long long it = 0;
-      bool live = true;
-      for (long long t = cid; t < ntiles && live; t += ncl) {
-        const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
-        const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
-        const int n0 = (nb - p.seg_start[sg]) * bn;
-        const CUtensorMap* tmB = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
-        const int m0 = mp * 2 * BM + rank * BM;
-        for (int k = 0; k < nk; ++k, ++it) {
-          const int s = (int)(it % STAGES);
-          if (it >= STAGES && !mbar_wait(smem_u32(&empty[s]), (uint32_t)((it / STAGES) - 1) & 1u, p.err, 1, abort_flag)) {
-            live = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(&full[s]);
-          mbar_expect_tx(fb, SB);
-          const uint32_t st = smem_u32(smem + (size_t)s * SB);
-          tma_load_2d(st, &tmA, k * BK, m0, fb);
-          tma_load_2d_mc(st + A_BYTES + rank * (bn / 2) * 128, tmB, k * BK, n0 + rank * (bn / 2), fb, PAIR);
-        }
-      }
-      // the last uses of every stage: both CTAs' MMAs must have read them, so no
-      // commit of the peer reaches this CTA after it exits
-      if (live)
-        for (long long u = (it > STAGES ? it - STAGES : 0); u < it; ++u)
-          if (!mbar_wait(smem_u32(&empty[u % STAGES]), (uint32_t)(u / STAGES) & 1u, p.err, 4, abort_flag)) break;
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: tile i into accumulator i % 2
-    if (lane == 0) {
-      const uint32_t idesc = instr_desc_ws(bn);  // M = 128, N = bn
-      long long it = 0;
-      int tl = 0;
-      bool live = true;
-      for (long long t = cid; t < ntiles && live; t += ncl, ++tl) {
-        const int b = tl & 1;
-        if (tl >= 2 && !mbar_wait(smem_u32(&acc_empty[b]), (uint32_t)((tl >> 1) - 1) & 1u, p.err, 5, abort_flag))
-          break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t d = tmem + (uint32_t)(b * bn);
-        for (int k = 0; k < nk; ++k, ++it) {
-          const int s = (int)(it % STAGES);
-          if (!mbar_wait(smem_u32(&full[s]), (uint32_t)(it / STAGES) & 1u, p.err, 2, abort_flag)) {
-            live = false;
-            break;
-          }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t st = smem_u32(smem + (size_t)s * SB);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_id(d, smem_desc(st + kk * 32), smem_desc(st + A_BYTES + kk * 32), idesc, (k > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_mc(smem_u32(&empty[s]), PAIR);  // frees stage s in both CTAs once read
-        }
-        if (live) umma_commit(smem_u32(&acc_full[b]));
-      }
-    }
-  } else {
-    // ---------------- epilogue: TMEM lane quarter q = warp & 3
-    const int q = warp & 3;
-    const bool vec = ((p.ldc & 3) == 0);
-    int tl = 0;
-    for (long long t = cid; t < ntiles; t += ncl, ++tl) {
-      const int b = tl & 1;
-      const bool ok = mbar_wait(smem_u32(&acc_full[b]), (uint32_t)(tl >> 1) & 1u, p.err, 3, abort_flag);
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      if (!ok) break;
-      const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
-      const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
-      const int n0 = (nb - p.seg_start[sg]) * bn;
-      const int segN = p.seg_N[sg];
-      float* const Cseg = p.seg_C[sg];
-      const bool vseg = vec && ((((uintptr_t)Cseg) & 15) == 0);
-      const int row = mp * 2 * BM + rank * BM + q * 32 + lane;
-      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * bn);
-#pragma unroll 1
-      for (int c = 0; c < bn; c += 16) {
-        float v[16];
-        tmem_ld16(tq + c, v);
-        if (row < M_eff) {
-          float* dst = Cseg + (size_t)row * p.ldc + n0 + c;
-          if (n0 + c + 16 <= segN && vseg) {
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (n0 + c + j < segN) dst[j] = v[j];
-          }
-        }
-      }
-      // accumulator drained: hand it back to the MMA warp
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
-    }
-  }
-  if (*abort_flag && warp == 0 && lane == 0) {
-    // let in-flight bulk copies land before the CTA's shared memory is released
-    const long long t0 = clock64();
-    while (clock64() - t0 < 20000000LL) {
-    }
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  // neither CTA of the pair leaves while the other may still write into it
-  cluster_sync();
-  if (warp == 1) {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
-  }
-}
-
 // ---------------------------------------------------------------- two-SM pair tiles
 // The same walk over 256-row x bn-column output tiles, with the pair's tensor
 // cores working as one (tcgen05 cta_group::2, M = 256): CTA r of the pair stages
@@ -1534,41 +1005,6 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
   }
 }
 
-// Packed tile layout of a weight matrix W[N, K] (bf16, row stride ldw): for
-// every 128-row tile and 64-column k-tile, 16 KB holding the 128 x 64 block
-// exactly as a 128-byte-swizzled TMA load would place it in shared memory
-// (row r at r * 128 bytes, 16-byte chunk j of that row at chunk j ^ (r % 8)),
-// zero outside W.  Tiles follow each other k-tile by k-tile, so one tile's
-// stream - and a run of consecutive tiles - is contiguous.
-__global__ void pack_weight_tiles_kernel(const __nv_bfloat16* __restrict__ W, int ldw, int N, int K,
-                                         uint4* __restrict__ out) {
-  const int ktiles = (K + BK - 1) / BK;
-  const long long chunks = (long long)((N + BN - 1) / BN) * ktiles * BN * 8;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int j = (int)(i & 7);                 // 16-byte chunk in the row (destination)
-    const int r = (int)((i >> 3) % BN);         // row in the tile
-    const long long unit = (i >> 3) / BN;       // tile * ktiles + k-tile
-    const int kk = (int)(unit % ktiles);
-    const int t = (int)(unit / ktiles);
-    const int src_chunk = j ^ (r & 7);
-    const int n = t * BN + r;
-    const int k0 = kk * BK + src_chunk * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (n < N) {
-      const __nv_bfloat16* src = W + (size_t)n * ldw + k0;
-      if (k0 + 8 <= K && (((uintptr_t)src) & 15) == 0) {
-        v = *(const uint4*)src;
-      } else {
-        __nv_bfloat16 e[8];
-        for (int x = 0; x < 8; ++x) e[x] = (k0 + x < K) ? src[x] : __float2bfloat16_rn(0.f);
-        memcpy(&v, e, 16);
-      }
-    }
-    out[i] = v;
-  }
-}
-
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1628,11 +1064,11 @@ const CUtensorMap* get_map(TcGemmCache* cache, const void* ptr, int rows, int co
 template <int MT>
 cudaError_t launch_rt(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid,
                       cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e =
+        func_attr_once(attr, (const void*)gemm_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   // at most 512 / tmem_cols CTAs may share an SM (see launch_ws)
   const int resident = 512 / p.tmem_cols;
@@ -1868,10 +1304,6 @@ GemmPick pick_for(TcGemmCache* cache, int M, const int* N, int nseg, int ktiles,
   return pk;
 }
 
-// Dynamic shared memory of a persistent pair CTA: at least half an SM's, so
-// no two CTAs (each holding all 512 TMEM columns) ever share an SM - a second
-// one would block in its allocation while its pair partner waits for it.
-int pc_launch_smem(int bn, int stages) { return std::max(pc_smem_bytes(bn, stages), 233472 / 2 - 1024 + 16); }
 int p2_launch_smem(int bn, int stages, int kpack = 1) {
   return std::max(kpack * p2_smem_bytes(bn, stages) - (kpack - 1) * 2048, 233472 / 2 - 1024 + 16);
 }
@@ -1891,11 +1323,11 @@ int p2_clusters(int bn, int stages, long long pair_tiles, int nsm) {
 
 cudaError_t launch_p2(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, int nclusters,
                       cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_p2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e =
+        func_attr_once(attr, (const void*)gemm_p2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
@@ -1914,68 +1346,13 @@ cudaError_t launch_p2(const CUtensorMap* a, const CUtensorMap* const* b, const P
   return cudaLaunchKernelEx(&cfg, gemm_p2_kernel, *a, *b[0], *b[1], *b[2], p);
 }
 
-// Persistent pair kernel: clusters of two CTAs, one CTA per SM, as many
-// clusters as fit at once (at most one per pair of tiles).
-int pc_clusters(int bn, int stages, long long pair_tiles, int nsm) {
-  int mc = max_active_clusters(pc_launch_smem(bn, stages), 2);
-  if (mc <= 0) mc = nsm / 2;
-  return (int)std::max<long long>(1, std::min<long long>(mc, pair_tiles));
-}
-
-// Column width of the persistent pair kernel: the least work per cluster over
-// its waves of tiles (bn + 32 per tile: the A box streamed alongside every
-// tile), ties to the wider tile.
-GemmPick pick_pc(int M, const int* N, int nseg, int nsm) {
-  const int mpairs = (M + 2 * BM - 1) / (2 * BM);
-  GemmPick best{4, 256, 1, 4};
-  double cbest = 1e30;
-  for (int bn = 256; bn >= 64; bn -= 16) {
-    const int stages = std::min(PC_MAX_STAGES, (232448 - 2048) / pc_stage_bytes(bn));
-    if (stages < 3) continue;
-    const long long tiles = (long long)mpairs * rt_tiles(N, nseg, bn);
-    const int ncl = pc_clusters(bn, stages, tiles, nsm);
-    const long long waves = (tiles + ncl - 1) / ncl;
-    const double c = (double)waves * (bn + 32);
-    if (c < cbest * 0.999) {
-      cbest = c;
-      best = GemmPick{4, bn, 1, stages};
-    }
-  }
-  return best;
-}
-
-cudaError_t launch_pc(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, int nclusters,
-                      cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_pc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(2 * nclusters, 1, 1);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = pc_launch_smem(p.bn, p.stages);
-  cfg.stream = st;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_pc_kernel, *a, *b[0], *b[1], *b[2], p);
-}
-
 cudaError_t launch_ws(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, dim3 grid,
                       cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e =
+        func_attr_once(attr, (const void*)gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   // CTAs that share an SM must never ask for more than its 512 TMEM columns
   // between them (a blocked tcgen05.alloc inside a cluster that waits for its
@@ -2000,32 +1377,6 @@ cudaError_t launch_ws(const CUtensorMap* a, const CUtensorMap* const* b, const P
   return cudaLaunchKernelEx(&cfg, gemm_ws_kernel, *a, *b[0], *b[1], *b[2], p);
 }
 
-template <bool PACKED>
-cudaError_t launch_sk(const CUtensorMap* a, const CUtensorMap* const* b, const SkParams& p, int grid,
-                      cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_sk_kernel<PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  // one CTA per SM: at least half of the SM's 228 KB, so two never share one
-  const int smem = std::max(p.stages * ws_stage_bytes(p.np) + 2048, 233472 / 2 - 1024 + 16);
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(SK_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_sk_kernel<PACKED>, *a, *b[0], *b[1], *b[2], p);
-}
-
-
 }  // namespace tc
 
 int* tc_error_word(TcGemmCache* cache) {
@@ -2042,7 +1393,7 @@ bool tc_gemm_supported(int K, int lda, int ldw) {
 
 cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int nseg, const void* const* W,
                                const int* ldw, const int* N, float* const* C, int ldc, int M, const int* m_dev,
-                               int K, cudaStream_t st, const TcGemmChoice* force, const void* const* Wpacked) {
+                               int K, cudaStream_t st, const TcGemmChoice* force) {
   using namespace tc;
   if (M <= 0 || nseg < 1 || nseg > 3) return M <= 0 ? cudaSuccess : cudaErrorInvalidValue;
   if ((uintptr_t)A & 15) return cudaErrorInvalidValue;
@@ -2105,20 +1456,16 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
   }
   p.seg_start[3] = 0x3FFFFFFF;
   for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
-  if (kind == 4 || kind == 5) {
-    // persistent pair tiles: each CTA's W box is half a tile (multicast to
-    // both CTAs for kernel 4, read by the pair's MMA for kernel 5)
-    const bool two_sm = kind == 5;
-    const GemmPick pk = pick_pc(M, N, nseg, nsm);
-    p.bn = force && force->bn ? force->bn : (auto_stages ? bn : (two_sm ? 256 : pk.bn));
+  if (kind == 5) {
+    // two-SM pair tiles: each CTA's W box is half a tile, read by the pair's MMA
+    p.bn = force && force->bn ? force->bn : (auto_stages ? bn : 256);
     if (p.bn < 16 || p.bn > 256 || (p.bn & 15)) return cudaErrorInvalidValue;
-    // two-SM kernel: k-blocks per stage (forced through the split field)
-    p.kpack = !two_sm ? 1 : (force && force->kernel == 5 && force->splits ? force->splits : (auto_splits ? auto_splits : 1));
+    // k-blocks per stage (forced through the split field)
+    p.kpack = force && force->kernel == 5 && force->splits ? force->splits : (auto_splits ? auto_splits : 1);
     // the 3D view has no out-of-range fill inside a k-block: whole k-blocks only
     if (p.kpack < 1 || p.kpack > 2 || (p.kpack > 1 && K % BK)) return cudaErrorInvalidValue;
-    const int max_stages = two_sm ? p2_max_stages(p.bn, p.kpack)
-                                  : std::min(PC_MAX_STAGES, (232448 - 2048) / pc_stage_bytes(p.bn));
-    const int def_stages = two_sm ? (p.kpack == 1 ? p2_default_stages(p.bn) : max_stages) : max_stages;
+    const int max_stages = p2_max_stages(p.bn, p.kpack);
+    const int def_stages = p.kpack == 1 ? p2_default_stages(p.bn) : max_stages;
     p.stages = force && force->stages ? force->stages : (auto_stages ? auto_stages : def_stages);
     if (p.stages < 2 || p.stages > max_stages) return cudaErrorInvalidValue;
     p.splits = 1;
@@ -2137,50 +1484,12 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     }
     for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
     const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * p.ntn;
-    const int ncl = two_sm ? p2_clusters(p.bn, p.stages, pair_tiles, nsm) : pc_clusters(p.bn, p.stages, pair_tiles, nsm);
+    const int ncl = p2_clusters(p.bn, p.stages, pair_tiles, nsm);
     const CUtensorMap* ma = p.kpack == 1 ? get_map(cache, A, M, K, lda, BM) : get_map3(cache, A, M, K, lda, BM, p.kpack);
     if (!ma) return cudaErrorInvalidValue;
-    return two_sm ? launch_p2(ma, mb, p, ncl, st) : launch_pc(ma, mb, p, ncl, st);
+    return launch_p2(ma, mb, p, ncl, st);
   }
-  if (kind == 3) {
-    // persistent stream-K: stages = ring depth, splits = grid size override
-    if (M > 2 * BM) return cudaErrorInvalidValue;
-    SkParams q{};
-    q.M = M;
-    q.m_dev = m_dev;
-    q.ldc = ldc;
-    q.ktiles = ktiles;
-    q.units = (long long)tiles * ktiles;
-    q.err = err;
-    for (int i = 0; i < 4; ++i) q.seg_start[i] = p.seg_start[i];
-    for (int i = 0; i < 3; ++i) {
-      q.seg_N[i] = p.seg_N[i];
-      q.seg_C[i] = p.seg_C[i];
-    }
-    q.np = std::max(16, (M + 15) & ~15);
-    q.acc_cols = 32;
-    while (q.acc_cols < q.np) q.acc_cols *= 2;
-    const int max_stages = std::min(SK_MAX_STAGES, (232448 - 2048) / ws_stage_bytes(q.np));
-    q.stages = force && force->stages ? force->stages : max_stages;
-    if (q.stages < 2 || q.stages > max_stages) return cudaErrorInvalidValue;
-    int grid = force && force->splits ? force->splits : nsm;
-    if (grid < 1 || grid > nsm) return cudaErrorInvalidValue;
-    grid = (int)std::min<long long>(grid, q.units);
-    if (tiles * 4 > TcGemmCache::kMaxCounters) return cudaErrorInvalidValue;
-    const cudaError_t re = tc_gemm_reserve(cache);
-    if (re != cudaSuccess) return re;
-    q.work = cache->work;
-    q.counters = cache->counters;
-    const bool packed = Wpacked != nullptr;
-    for (int i = 0; i < nseg; ++i) {
-      q.wpack[i] = packed ? (const uint8_t*)Wpacked[i] : nullptr;
-      if (packed && (!Wpacked[i] || ((uintptr_t)Wpacked[i] & 15))) return cudaErrorInvalidValue;
-    }
-    const CUtensorMap* ma = get_map(cache, A, M, K, lda, q.np);
-    if (!ma) return cudaErrorInvalidValue;
-    return packed ? launch_sk<true>(ma, mb, q, grid, st) : launch_sk<false>(ma, mb, q, grid, st);
-  }
-  // the row-tiled kernel reads W through its tensor map; packed copies unused
+  if (kind != 1 && kind != 2) return cudaErrorInvalidValue;
   if (kind == 2) {
     if (M > 2 * BM) return cudaErrorInvalidValue;
     p.np = std::max(16, (M + 15) & ~15);
@@ -2300,11 +1609,9 @@ cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, cons
 }
 
 cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,
-                         int M, const int* m_dev, int N, int K, cudaStream_t st, const TcGemmChoice* force,
-                         const void* Wpacked) {
+                         int M, const int* m_dev, int N, int K, cudaStream_t st, const TcGemmChoice* force) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  return tc_gemm_bf16_multi(cache, A, lda, 1, &W, &ldw, &N, &C, ldc, M, m_dev, K, st, force,
-                            Wpacked ? &Wpacked : nullptr);
+  return tc_gemm_bf16_multi(cache, A, lda, 1, &W, &ldw, &N, &C, ldc, M, m_dev, K, st, force);
 }
 
 cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, int K, int* out) {
@@ -2330,52 +1637,10 @@ cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, in
   return cudaSuccess;
 }
 
-size_t tc_packed_bytes(int N, int K) {
-  return (size_t)((N + tc::BN - 1) / tc::BN) * ((K + tc::BK - 1) / tc::BK) * tc::UNIT_BYTES;
-}
-
-cudaError_t tc_pack_weights(const void* W, int ldw, int N, int K, void* out, cudaStream_t st) {
-  if (!W || !out || N < 1 || K < 1 || ldw < K || ((uintptr_t)out & 15)) return cudaErrorInvalidValue;
-  const long long chunks = (long long)tc_packed_bytes(N, K) / 16;
-  const int blocks = (int)std::min<long long>((chunks + 255) / 256, 4096);
-  tc::pack_weight_tiles_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)W, ldw, N, K, (uint4*)out);
-  return cudaGetLastError();
-}
-
-cudaError_t tc_gemm_reserve(TcGemmCache* c) {
-  if (c->work) return cudaSuccess;
-  if (c->num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (c->num_sms <= 0) return cudaErrorInvalidValue;
-  }
-  // two partial pieces of up to 256 rows x 128 features per CTA
-  const size_t work_bytes = (size_t)c->num_sms * 2 * 256 * tc::BN * sizeof(float);
-  cudaError_t e = cudaMalloc(&c->work, work_bytes);
-  if (e != cudaSuccess) {
-    c->work = nullptr;
-    return e;
-  }
-  e = cudaMalloc(&c->counters, sizeof(int) * TcGemmCache::kMaxCounters);
-  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, sizeof(int) * TcGemmCache::kMaxCounters);
-  if (e != cudaSuccess) {
-    cudaFree(c->work);
-    if (c->counters) cudaFree(c->counters);
-    c->work = nullptr;
-    c->counters = nullptr;
-  }
-  return e;
-}
-
 void tc_gemm_cache_clear(TcGemmCache* c) {
   c->maps.clear();
   if (c->err) cudaFree(c->err);
   c->err = nullptr;
-  if (c->work) cudaFree(c->work);
-  if (c->counters) cudaFree(c->counters);
-  c->work = nullptr;
-  c->counters = nullptr;
 }
 
 }  // namespace polestar

@@ -30,15 +30,10 @@ struct TcMapKeyHash {
 
 // Per-context state of the tensor-core GEMM: encoded TMA descriptors (keyed by
 // buffer, shape and box), the device error word of the bounded waits, SM count.
-// The stream-K kernel also keeps its partial-tile workspace (two pieces of up
-// to 256 x 128 fp32 per SM) and per-tile arrival counters here.
 struct TcGemmCache {
-  static constexpr int kMaxCounters = 4 * 4096;  // 4 per 128-column tile
   std::unordered_map<TcMapKey, CUtensorMap, TcMapKeyHash> maps;
   int* err = nullptr;
   int num_sms = 0;
-  float* work = nullptr;
-  int* counters = nullptr;
   // automatic launch choices by shape {M, K, segments, N0, N1, N2, SMs} ->
   // {kernel, bn, splits, stages}: the search runs once per shape
   std::map<std::array<int, 7>, std::array<int, 4>> picks;
@@ -47,13 +42,11 @@ struct TcGemmCache {
 // Kernel choice for tuning sweeps and tests; zero fields are chosen
 // automatically.  kernel: 1 row-tiled (rows on the MMA's M side, up to two
 // 128-row sub-tiles per CTA), 2 weight-stationary (W rows on the M side, at most
-// 256 activation rows on the N side, one tile per CTA), 3 persistent stream-K
-// weight-stationary (one CTA per SM, equal shares of the weight stream), 4 / 5
-// persistent pair tiles (two-CTA clusters over 256-row x bn tiles; 4 multicasts
-// each W tile into both CTAs, 5 runs the pair's MMA as one, cta_group::2).
-// stages: ring depth; splits: K split over a thread-block cluster (1..8), or
-// for kernel 3 the number of CTAs; bn: columns per tile of kernel 1 (a
-// multiple of 16, at most 256).
+// 256 activation rows on the N side, one tile per CTA), 5 persistent pair tiles
+// (two-CTA clusters over 256-row x bn tiles, the pair's MMA run as one,
+// cta_group::2).  stages: ring depth; splits: K split over a thread-block
+// cluster (1..8), or for kernel 5 the 64-column k-blocks per stage; bn: columns
+// per tile of kernels 1 and 5 (a multiple of 16, at most 256).
 struct TcGemmChoice {
   int kernel = 0;
   int stages = 0;
@@ -67,19 +60,16 @@ struct TcGemmChoice {
 bool tc_gemm_supported(int K, int lda, int ldw);
 
 // C[M, N] (fp32, ldc) = A[M, K] (bf16, lda) * W[N, K]^T (bf16, ldw); rows at or
-// beyond min(M, *m_dev) are not written (m_dev may be null).  Wpacked, when
-// given, is W in the packed tile layout (tc_pack_weights); the stream-K kernel
-// then streams it with contiguous bulk copies (other kernels reject it).
+// beyond min(M, *m_dev) are not written (m_dev may be null).
 cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,
                          int M, const int* m_dev, int N, int K, cudaStream_t st,
-                         const TcGemmChoice* force = nullptr, const void* Wpacked = nullptr);
+                         const TcGemmChoice* force = nullptr);
 
 // Up to three projections sharing the A operand in one launch: segment s
 // computes C[s][M, N[s]] = A * W[s]^T (all C[s] with row stride ldc).
 cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int nseg, const void* const* W,
                                const int* ldw, const int* N, float* const* C, int ldc, int M, const int* m_dev,
-                               int K, cudaStream_t st, const TcGemmChoice* force = nullptr,
-                               const void* const* Wpacked = nullptr);
+                               int K, cudaStream_t st, const TcGemmChoice* force = nullptr);
 
 // Gate and up projections with the SwiGLU activation fused into the
 // row-tiled kernel's epilogue: act[m, f] = bf16(silu(g) * u) with
@@ -91,22 +81,11 @@ cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, cons
                                 int F, void* act, int ld_act, int M, const int* m_dev, int K, cudaStream_t st,
                                 const TcGemmChoice* force = nullptr);
 
-// Bytes of the packed tile layout of an N x K bf16 matrix: for each 128-row
-// tile and 64-column k-tile, 16 KB holding that block as a 128-byte-swizzled
-// shared-memory image (zero outside the matrix), k-tiles of a tile adjacent.
-size_t tc_packed_bytes(int N, int K);
-
-// Writes that layout of W (row stride ldw) to out (16-byte aligned), on st.
-cudaError_t tc_pack_weights(const void* W, int ldw, int N, int K, void* out, cudaStream_t st);
-
 // The launch the library picks for M rows, nseg weight segments of N[i]
 // output columns and inner size K: out = {kernel (1 row-tiled, 2
 // weight-stationary, 5 two-SM pair tiles), columns per tile, K split, ring
 // depth}.
 cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, int K, int* out);
-
-// Allocates the stream-K workspace and counters (once per cache).
-cudaError_t tc_gemm_reserve(TcGemmCache* cache);
 
 // Device word holding the code of the first timed-out wait (0 = none).
 int* tc_error_word(TcGemmCache* cache);

@@ -252,11 +252,10 @@ cudaError_t launch_row_attention(const AttnArgs& a, cudaStream_t st) {
   const dim3 grid((a.R + ATT_ROWS - 1) / ATT_ROWS, a.H);
   if (a.dh == 128) {
     const size_t sm = (2 * ATT_TK * 129 + ATT_ROWS * 128 + ATT_ROWS * ATT_TK) * sizeof(float);
-    static bool cfg = false;
-    if (!cfg) {
-      cudaFuncSetAttribute(row_attention_kernel<T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      cfg = true;
-    }
+    static PerDeviceOnce cfg;
+    const cudaError_t e = func_attr_once(cfg, (const void*)row_attention_kernel<T, 128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
     launch_pdl(row_attention_kernel<T, 128>, dim3(grid), dim3(256), sm, st, a);
   } else {
     const size_t sm = (2 * ATT_TK * 65 + ATT_ROWS * 64 + ATT_ROWS * ATT_TK) * sizeof(float);

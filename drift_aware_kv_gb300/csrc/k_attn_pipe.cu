@@ -194,13 +194,18 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const int split = blockIdx.z, nsplit = gridDim.z;
-  const int4 wk = p.work[blockIdx.x];  // {rowA, nA, rowB, nB}
-  const int nrows = wk.y + wk.w;
-  const int nwl = (nrows + 15) >> 4;   // compute warps with rows
   const int kvh = h / (p.H / p.Hkv);
   const int ntiles_all = (p.N + TK - 1) / TK;
   const int tbeg = split * ntiles_all / nsplit, tend = (split + 1) * ntiles_all / nsplit;
   const int ntl = tend - tbeg;
+  // K/V rows, queries and (for callers that build them on the device) the work
+  // list and row table come from the preceding kernels: nothing of them is read
+  // before the dependency wait
+  pdl_launch_dependents();
+  pdl_wait();
+  const int4 wk = p.work[blockIdx.x];  // {rowA, nA, rowB, nB}
+  const int nrows = wk.y + wk.w;
+  const int nwl = (nrows + 15) >> 4;   // compute warps with rows
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -212,9 +217,6 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  // K/V rows and queries come from the preceding kernels
-  pdl_launch_dependents();
-  pdl_wait();
   const int seq = p.rows[wk.x].x;
 
   if (warp == CW) {
@@ -580,11 +582,11 @@ cudaError_t launch(const AttnArgs& a, int batch, cudaStream_t st) {
   if (!map) return cudaErrorInvalidValue;
   const bool split = a.splits > 1;
   const int smem = smem_bytes<DH>(a.stages, split);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_pipe_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e =
+        func_attr_once(attr, (const void*)attn_pipe_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.n_work, a.H, a.splits);

@@ -204,8 +204,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int4 wk = p.work[blockIdx.x];  // {rowA, nA, rowB, nB}
-  const int nrows = wk.y + wk.w;
   const int kvh = h / (p.H / p.Hkv);
   const int ntl = (p.N + TK - 1) / TK;
 
@@ -232,9 +230,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
-  // K/V rows and queries come from the preceding kernels
+  // K/V rows, queries and (for callers that build them on the device) the work
+  // list and row table come from the preceding kernels: read after the wait
   pdl_launch_dependents();
   pdl_wait();
+  const int4 wk = p.work[blockIdx.x];  // {rowA, nA, rowB, nB}
+  const int nrows = wk.y + wk.w;
   const int seq = p.rows[wk.x].x;
 
   if (warp == 0) {
@@ -545,11 +546,11 @@ cudaError_t launch_attention_tc(const AttnArgs& a, int batch, cudaStream_t st) {
   if (a.dh != at::DH || (a.kvdim & 7)) return cudaErrorInvalidValue;
   const CUtensorMap* map = at::kv_map_tiles(a.kv_layer, batch * a.N, 2 * a.kvdim);
   if (!map) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(at::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, at::SMEM_BYTES);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = func_attr_once(attr, (const void*)at::attn_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, at::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.n_work, a.H, 1);

@@ -681,11 +681,10 @@ template <typename T>
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st) {
   const int nc = centroid_cluster_size(a.d);
   const int cw = a.d / nc;
-  static bool nonportable = false;  // set once per instantiation (a driver call per launch costs host time)
-  if (nc > 8 && !nonportable) {
-    cudaFuncSetAttribute(centroid_update_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    nonportable = true;
-  }
+  static PerDeviceOnce nonportable;  // a driver call per launch costs host time
+  if (nc > 8)
+    func_attr_once(nonportable, (const void*)centroid_update_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                   1);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(nc, a.n_fire);
   cfg.blockDim = dim3(CU_THREADS);

@@ -1337,16 +1337,15 @@ extern "C" polestar_status polestar_debug_gemm(const void* A, int32_t lda, const
   if (!A || !W || !C || M < 0 || N < 1 || K < 1) return POLESTAR_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   const int kind = path & 0xF;
-  if (kind >= 1 && kind <= 7) {
-    if (dtype != POLESTAR_BF16 || !tc_gemm_supported(K, lda, kind == 5 ? K : ldw)) return POLESTAR_ERR_UNSUPPORTED;
+  if (kind == 1 || kind == 2 || kind == 3 || kind == 7) {
+    if (dtype != POLESTAR_BF16 || !tc_gemm_supported(K, lda, ldw)) return POLESTAR_ERR_UNSUPPORTED;
     TcGemmChoice force;
-    force.kernel = kind == 5 ? 3 : (kind >= 6 ? kind - 2 : kind - 1);
+    force.kernel = kind == 7 ? 5 : kind - 1;
     force.kpack = (path >> 4) & 0xF;
     force.stages = (path >> 8) & 0xFF;
     force.splits = (path >> 16) & 0xFF;
     force.bn = ((path >> 24) & 0xFF) * 16;
-    const cudaError_t e = tc_gemm_bf16(&cache, A, lda, W, kind == 5 ? K : ldw, C, ldc, M, m_dev, N, K, st, &force,
-                                       kind == 5 ? W : nullptr);
+    const cudaError_t e = tc_gemm_bf16(&cache, A, lda, W, ldw, C, ldc, M, m_dev, N, K, st, &force);
     if (e == cudaErrorInvalidValue) return POLESTAR_ERR_UNSUPPORTED;
     return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
   }
@@ -1383,18 +1382,6 @@ extern "C" polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, c
   static TcGemmCache cache;
   if (!N || !out || M < 1 || nseg < 1 || nseg > 3 || K < 1) return POLESTAR_ERR_INVALID_ARG;
   return tc_gemm_choice(&cache, M, nseg, N, K, out) == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
-}
-
-extern "C" int64_t polestar_packed_weight_bytes(int32_t N, int32_t K) {
-  if (N < 1 || K < 1) return -1;
-  return (int64_t)tc_packed_bytes(N, K);
-}
-
-extern "C" polestar_status polestar_pack_weights(const void* W, int32_t ldw, int32_t N, int32_t K, void* out,
-                                                 void* stream) {
-  if (!W || !out || N < 1 || K < 1 || ldw < K) return POLESTAR_ERR_INVALID_ARG;
-  if ((uintptr_t)out & 15) return POLESTAR_ERR_INVALID_ARG;
-  return tc_pack_weights(W, ldw, N, K, out, (cudaStream_t)stream) == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 
 extern "C" polestar_status polestar_debug_attention(const void* q, const void* kv, int32_t N, int32_t H,

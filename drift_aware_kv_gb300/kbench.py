@@ -60,8 +60,6 @@ def bench_gemm(a):
     elif a.cublas:  # library comparison point (cuBLAS through torch), not a path of the product
         ms = _time(lambda: torch.matmul(A, nxt().t()), a.iters)
     else:
-        if a.path == 5:  # weights in the packed tile layout
-            Ws = [P.pack_weights(w) for w in Ws]
         path = P.gemm_path(a.path, a.stages, a.splits, getattr(a, "bn", 0))
         ms = _time(lambda: P.debug_gemm(A, nxt(), C, path, N=a.N), a.iters)
     byts = (a.N * a.K + a.M * a.K) * 2 + a.M * a.N * 4
@@ -120,15 +118,14 @@ def main():
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--path", type=int, default=1,
                     help="0 CUDA cores, 1 tcgen05 (library's choice), 2 row-tiled tcgen05, "
-                         "3 weight-stationary tcgen05, 4 stream-K weight-stationary tcgen05, "
-                         "5 stream-K on packed weights")
+                         "3 weight-stationary tcgen05, 7 two-SM pair tiles")
     ap.add_argument("--cublas", action="store_true", help="time cuBLAS (through torch) instead: comparison point")
     ap.add_argument("--swiglu", action="store_true",
                     help="gate/up projection with the SwiGLU activation fused (N = 2F: gate and up halves)")
     ap.add_argument("--stages", type=int, default=0, help="tcgen05 ring depth (0 = library's choice)")
     ap.add_argument("--bn", type=int, default=0, help="row-tiled columns per tile (0 = library's choice)")
     ap.add_argument("--splits", type=int, default=0,
-                    help="tcgen05 cluster K split, or CTA count for path 4 (0 = library's choice)")
+                    help="tcgen05 cluster K split, or k-blocks per stage for path 7 (0 = library's choice)")
     ap.add_argument("--impl", type=int, default=0,
                     help="attention kernel: 0 library's choice, 1 pipelined mma.sync, 2 tcgen05")
     ap.add_argument("--R", type=int, default=136)

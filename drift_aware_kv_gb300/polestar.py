@@ -24,7 +24,7 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
             "polestar_profile_begin", "polestar_profile_end", "polestar_debug_gemm",
             "polestar_debug_attention", "polestar_debug_kmeans", "polestar_attention_noalloc",
-            "polestar_packed_weight_bytes", "polestar_pack_weights", "polestar_debug_gemm_choice",
+            "polestar_debug_gemm_choice",
             "polestar_debug_attention_impl", "polestar_debug_gemm_swiglu", "polestar_full_forward",
             "polestar_kv_staleness", "polestar_cache_staleness", "polestar_debug_attention_items",
             "polestar_debug_window", "polestar_debug_trigger")
@@ -96,10 +96,6 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_debug_kmeans.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_uint64,
                                           C.c_int32, P, P, P, P, P, P, P]
     lib.polestar_debug_kmeans.restype = C.c_int
-    lib.polestar_packed_weight_bytes.argtypes = [C.c_int32, C.c_int32]
-    lib.polestar_packed_weight_bytes.restype = C.c_int64
-    lib.polestar_pack_weights.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P]
-    lib.polestar_pack_weights.restype = C.c_int
     lib.polestar_debug_gemm_choice.argtypes = [C.c_int32, C.c_int32, C.POINTER(C.c_int32), C.c_int32,
                                                C.POINTER(C.c_int32)]
     lib.polestar_debug_gemm_choice.restype = C.c_int
@@ -237,13 +233,11 @@ class Polestar:
 
 def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0, kpack: int = 0) -> int:
     """`path` of polestar_debug_gemm: kernel 0 CUDA cores, 1 tcgen05 (library's
-    choice), 2 row-tiled tcgen05, 3 weight-stationary tcgen05, 4 persistent
-    stream-K weight-stationary tcgen05 (5: the same on packed weights), 6
-    persistent pair tiles (two-CTA clusters sharing each weight tile); stages /
-    splits override the ring depth and the cluster K split (kernels 2, 3) or the
-    CTA count (kernels 4, 5); bn the columns per tile of kernels 2 and 6 (a
-    multiple of 16); kpack the 64-column k-blocks per stage of kernel 2 (1 or 2);
-    0 = automatic."""
+    choice), 2 row-tiled tcgen05, 3 weight-stationary tcgen05, 7 persistent
+    two-SM pair tiles (cta_group::2); stages / splits override the ring depth
+    and the cluster K split (kernels 2, 3) or the k-blocks per stage (kernel 7);
+    bn the columns per tile of kernels 2 and 7 (a multiple of 16); kpack the
+    64-column k-blocks per stage of kernel 2 (1 or 2); 0 = automatic."""
     return kernel | (kpack << 4) | (stages << 8) | (splits << 16) | ((bn // 16) << 24)
 
 
@@ -285,20 +279,6 @@ def gemm_choice(M: int, Ns, K: int) -> dict:
     out = (C.c_int32 * 4)()
     _check(lib.polestar_debug_gemm_choice(int(M), len(Ns), arr, int(K), out))
     return dict(kernel=int(out[0]), bn=int(out[1]), splits=int(out[2]), stages=int(out[3]))
-
-
-def pack_weights(W, stream=None):
-    """W [N, K] bf16 (CUDA, unit inner stride) -> new uint8 CUDA tensor holding
-    its packed tile layout (polestar_pack_weights)."""
-    import torch
-    lib = load()
-    N, K = W.shape
-    nbytes = int(lib.polestar_packed_weight_bytes(N, K))
-    out = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
-    st = stream if stream is not None else torch.cuda.current_stream()
-    _check(lib.polestar_pack_weights(C.c_void_p(W.data_ptr()), W.stride(0), N, K, C.c_void_p(out.data_ptr()),
-                                     C.c_void_p(st.cuda_stream)))
-    return out
 
 
 def debug_gemm(A, W, out, path: int, m_dev=None, stream=None, N=None):

@@ -224,28 +224,24 @@ polestar_status polestar_profile_end(polestar_ctx *ctx, polestar_kernel_stats *o
 
 /* ---- projection kernel on caller buffers (test hook) ----
  * C[M, N] (fp32, row stride ldc) = A[M, K] (row stride lda) * W[N, K]^T (row
- * stride ldw), A and W in `dtype`, all device pointers, on `stream`.
- * path 0: CUDA-core kernel; path 1: tcgen05 tensor-core kernels (bf16 only)
- * with the library's own choice of kernel, ring depth and K split; path 2 /
- * 3 / 4: the row-tiled / weight-stationary (M <= 256) / persistent stream-K
- * weight-stationary (M <= 256) tcgen05 kernel, with bits 8-15 of `path`
- * giving the ring depth and bits 16-23 the K split over a cluster (paths 2
- * and 3) or the number of CTAs (paths 4, 5), and bits 24-31 the columns per
- * tile of paths 2 and 6 in units of 16; bits 4-7 the 64-column k-blocks per
- * stage of path 2 (1, or 2 loaded by one 3D TMA box per operand, K a multiple
- * of 64); 0 = automatic.  Path 5 is path 4
- * with W given in the packed tile layout of polestar_pack_weights (ldw is
- * then ignored).  Paths 6 and 7: persistent pair-tile kernels (clusters of
- * two CTAs walk 256-row x bn-column output tiles; any M): 6 multicasts each
- * weight tile into both CTAs, 7 runs the pair's tensor cores as one MMA
- * (cta_group::2) on each CTA's half; bits 8-15 the ring depth, for path 7
- * bits 16-23 the 64-column k-blocks per stage (1, or 2 loaded by one 3D TMA
- * box per operand; K must then be a multiple of 64).  A combination the kernel cannot
- * run (too much shared memory, more than 8 splits, more CTAs than SMs)
- * returns UNSUPPORTED.
+ * stride ldw), A and W in `dtype`, all device pointers, on `stream` -- the
+ * Q/K/V, O and FFN projections of the decoder layer (§2 Eq. 3) that the sparse
+ * forward of §4.1 runs over gathered rows.
+ * Bits 0-3 of `path` select the kernel: 0 CUDA cores; 1 the tcgen05
+ * tensor-core kernels (bf16 only) with the library's own choice of kernel,
+ * ring depth and K split; 2 the row-tiled tcgen05 kernel; 3 the
+ * weight-stationary tcgen05 kernel (M <= 256); 7 the persistent two-SM
+ * pair-tile kernel (clusters of two CTAs walk 256-row x bn-column output
+ * tiles with the pair's tensor cores run as one MMA, cta_group::2; any M).
+ * Bits 8-15: ring depth.  Bits 16-23: the K split over a cluster (paths 2, 3)
+ * or the 64-column k-blocks per stage of path 7 (1, or 2 loaded by one 3D TMA
+ * box per operand; K must then be a multiple of 64).  Bits 24-31: columns per
+ * tile of paths 2 and 7 in units of 16.  Bits 4-7: the 64-column k-blocks per
+ * stage of path 2.  0 = automatic.  Any other kernel number, or a combination
+ * the kernel cannot run (too much shared memory, more than 8 splits), returns
+ * UNSUPPORTED.
  * m_dev (device int, may be NULL) lowers the row count on the device: rows at
- * or beyond min(M, *m_dev) are left untouched.  Asynchronous; returns
- * UNSUPPORTED for a path/dtype/stride combination the kernels do not cover. */
+ * or beyond min(M, *m_dev) are left untouched.  Asynchronous. */
 polestar_status polestar_debug_gemm(const void *A, int32_t lda, const void *W, int32_t ldw, float *C,
                                     int32_t ldc, int32_t M, const int32_t *m_dev, int32_t N, int32_t K,
                                     int32_t dtype, int32_t path, void *stream);
@@ -272,21 +268,6 @@ polestar_status polestar_debug_gemm_swiglu(const void *A, int32_t lda, const voi
  * occupancy; launches nothing.  CUDA error (no device) when no device is
  * visible. */
 polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, const int32_t *N, int32_t K, int32_t *out);
-
-/* ---- packed tile layout of a projection matrix ----
- * The weight-streaming projection kernel reads weights as contiguous 16 KB
- * units: for each 128-row tile of W [N, K] (bf16, row stride ldw >= K) and
- * each 64-column k-tile, the 128 x 64 block as a 128-byte-swizzled shared-
- * memory image (row r at byte r*128 of the unit, 16-byte chunk j of the row
- * stored at chunk j XOR (r mod 8)), zero outside W; the k-tiles of a tile are
- * adjacent and tiles follow in order.  polestar_packed_weight_bytes gives the
- * size (-1 for N < 1 or K < 1); polestar_pack_weights writes the layout of W
- * into `out` (device, 16-byte aligned, that many bytes) asynchronously on
- * `stream`.  (The library's own layer loop streams weights through 2D tensor
- * maps of the caller's matrices; the packed layout serves callers and tests
- * of the persistent weight-streaming kernel, path 5 of polestar_debug_gemm.) */
-int64_t polestar_packed_weight_bytes(int32_t N, int32_t K);
-polestar_status polestar_pack_weights(const void *W, int32_t ldw, int32_t N, int32_t K, void *out, void *stream);
 
 /* ---- row attention + KL drift on caller buffers (test hook) ----
  * One sequence: q [R, H*dh] (rotary applied), kv [N, 2, Hkv*dh] (K then V of
@@ -325,7 +306,7 @@ int32_t polestar_debug_window(int32_t prompt_len, int32_t gen_len, int32_t block
                               int32_t suffix_win, int32_t block_index, int32_t *span, int32_t *pos, int32_t cap);
 polestar_status polestar_debug_trigger(int32_t tau_upd, const int32_t *n_unmasked, int32_t steps, uint8_t *fire);
 
-/* ---- attention work items (host only; test hook) ----/* ---- attention work items (host only; test hook) ----
+/* ---- attention work items (host only; test hook) ----
  * The split of one sequence's attention rows into work items that the row
  * attention kernels take one per CTA group: rows [a0, a0 + na) followed by
  * [b0, b0 + nb) are cut into ceil((na + nb) / max_rows) items of near-equal size
@@ -336,7 +317,7 @@ polestar_status polestar_debug_trigger(int32_t tau_upd, const int32_t *n_unmaske
 int32_t polestar_debug_attention_items(int32_t a0, int32_t na, int32_t b0, int32_t nb, int32_t max_rows,
                                        int32_t *out, int32_t cap);
 
-/* ---- row attention + KL drift that allocates nothing ----/* ---- row attention + KL drift that allocates nothing ----
+/* ---- row attention + KL drift that allocates nothing ----
  * The paper has no counterpart to this call; it exists for callers that cannot
  * let a library allocate device memory: a host application that owns every
  * device allocation through its own pool or memory cap, or a latency-critical

@@ -46,17 +46,6 @@ def test_init_rejects_bad_config_without_touching_the_device():
     lib.polestar_release(None)
 
 
-def test_packed_weight_size_is_whole_tiles():
-    """16 KB per (128-row tile, 64-column k-tile), rounded up in both directions;
-    a host-only computation, no device involved."""
-    from drift_aware_kv_gb300 import polestar as P
-    lib = P.load()
-    assert lib.polestar_packed_weight_bytes(200, 448) == 2 * 7 * 16384
-    assert lib.polestar_packed_weight_bytes(128, 64) == 16384
-    assert lib.polestar_packed_weight_bytes(4096, 12288) == 32 * 192 * 16384
-    assert lib.polestar_packed_weight_bytes(0, 64) == -1
-
-
 def test_gemm_choice_without_a_device_is_an_error_not_a_crash():
     """The launch choice needs the device's SM count; with no device the call
     returns an error status instead of dividing by zero."""
