@@ -89,6 +89,7 @@ class Workload:
     flips: tuple = (3, 6)
     extra_frac: tuple = (0.1, 0.1)  # U(lo, hi) per sequence; (0.1, 0.1) = fixed 10 %
     n_steps: Optional[int] = None  # None: run until every block is decoded
+    norm_gain_std: float = 0.0  # RMSNorm gains 1 + N(0, std) (0: gains 1, as in the benchmark shapes)
 
     @property
     def seq_len(self) -> int:
@@ -167,15 +168,23 @@ def weight_shapes(w: Workload) -> Dict[str, tuple]:
 
 
 def make_layer_weights(w: Workload, layer: int, device="cpu") -> Dict[str, torch.Tensor]:
-    """Random-init weights of one decoder layer: matrices N(0, 0.02), norm gains 1.
+    """Random-init weights of one decoder layer: matrices N(0, 0.02), norm gains 1
+    (or 1 + N(0, norm_gain_std), distinct per norm and layer, in test variants).
 
     Matrices are row-major [out_features, in_features] (y = x @ W^T)."""
     dt = torch_dtype(w)
     out = {}
     for i, (name, shape) in enumerate(weight_shapes(w).items()):
         out[name] = _randn(shape, derive_seed(w.seed, 0x57, layer, i), device, 0.02).to(dt)
-    out["attn_norm"] = torch.ones(w.d_model, dtype=dt, device=device)
-    out["ffn_norm"] = torch.ones(w.d_model, dtype=dt, device=device)
+    if w.norm_gain_std > 0:
+        # distinct, non-unit gains for the two norms of every layer (test variant)
+        out["attn_norm"] = (1.0 + _randn((w.d_model,), derive_seed(w.seed, 0x6A1, layer), device,
+                                          w.norm_gain_std)).to(dt)
+        out["ffn_norm"] = (1.0 + _randn((w.d_model,), derive_seed(w.seed, 0x6A2, layer), device,
+                                         w.norm_gain_std)).to(dt)
+    else:
+        out["attn_norm"] = torch.ones(w.d_model, dtype=dt, device=device)
+        out["ffn_norm"] = torch.ones(w.d_model, dtype=dt, device=device)
     return out
 
 

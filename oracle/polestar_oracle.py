@@ -4,7 +4,10 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the C
 baseline legs of ``bench.py`` may import this module.  It shares no code with the
 CUDA library (``drift_aware_kv_gb300/csrc``) and never imports it.
 
-Plain, slow, obviously-correct numpy in float64.  Citations name the paper
+Plain, slow, obviously-correct numpy in float64 (the pages fix no precision; float64
+is at least as strict as the single-precision oracle the build plan names, and
+numpy's BLAS may use several threads -- the timed legs report the thread count).
+Citations name the paper
 "Polestar: Drift-Aware Cache Calibration and Token Commitment for Efficient
 Inference of Diffusion LLMs" (arXiv 2607.14107) by section / equation / Algorithm 1.
 
@@ -17,6 +20,8 @@ code choice, Appendix C.3) are taken here in IEEE fp32 as well.
 Parity status per function (what pins it, see tests/test_oracle_*.py):
   number formats   pinned (torch float8_e4m3fn table / RNE, E2M1 grid of the format)
   rmsnorm / rope   pinned (torch rms_norm, complex-rotation form)
+  decoder layer    pinned (qkv -> attention -> O + residual -> RMSNorm -> SwiGLU -> down +
+                   residual equals per-element loops, distinct non-unit norm gains; silu vs torch)
   attention / KL   pinned (torch sdpa, scipy rel_entr, KL(a||a)=0, Pinsker bound)
   spherical kmeans pinned (brute force on tiny inputs, unit norms, objective monotone)
   top-k            pinned (full sort)
@@ -25,7 +30,8 @@ Parity status per function (what pins it, see tests/test_oracle_*.py):
                    current-block, history, suffix and block-entry rules)
   centroid update  pinned (exact cache: layer-0 member sums equal the closed form)
   proxy query      pinned (no rotary: equals the position-0 token's query)
-  trigger          pinned (equals the library's host trigger on the same counts)
+  trigger          pinned (closed-form refresh sequences of the tau_upd rule on the engine itself,
+                   restart at block entry)
   confidence       pinned (generator's target max-probability)
   sparse refresh   pinned (k = K, exact cache: equals the block-entry forward)
   KV staleness     pinned (closed forms: 0 on itself, 2 on the negation, per-head rotation)
@@ -346,12 +352,28 @@ class PolestarOracle:
     weights: per layer dict of float64 arrays (values already in the storage dtype).
     """
 
-    def __init__(self, cfg, weights, exact_cache: bool = False):
+    def __init__(self, cfg, weights, exact_cache: bool = False, store_noise: float = 0.0, noise_seed: int = 0):
         self.cfg = cfg
         self.W = weights
         self.bf16 = cfg.dtype == "bf16"
         # exact_cache=True keeps window hidden states unquantised (test switch)
         self.exact_cache = exact_cache
+        # store_noise > 0 (test switch, bf16 workloads only): every value is
+        # multiplied by (1 + u * store_noise), u ~ U(-1, 1) drawn from a seeded
+        # generator, just before it is rounded to bf16.  This models an fp32
+        # computation of the same value, whose last-bit differences decide the
+        # bf16 rounding of values that lie close to a rounding midpoint; running
+        # perturbed copies beside an unperturbed one measures how far each output
+        # of the method moves under such differences.  0 = exact float64 values.
+        self.store_noise = float(store_noise)
+        self._noise_rng = np.random.default_rng(noise_seed) if store_noise > 0 else None
+        # follow (test switch): another oracle on the same inputs, stepped first,
+        # whose decisions -- the K-means labels and the top-k clusters -- this one
+        # adopts instead of its own (which it still reports: "own_labels",
+        # "own_topk"), so that a perturbed copy keeps the leader's decision path
+        # and differs from it by rounding alone.
+        self.follow: Optional["PolestarOracle"] = None
+        self.last_recs = None
         c = cfg
         self.N = c.prompt_len + c.gen_len
         self.seqs: List[SeqState] = []
@@ -364,7 +386,12 @@ class PolestarOracle:
 
     # ---- helpers --------------------------------------------------------------------
     def _store(self, x):
-        return to_bf16(x) if self.bf16 else np.asarray(x, dtype=np.float64)
+        if not self.bf16:
+            return np.asarray(x, dtype=np.float64)
+        if self._noise_rng is not None:
+            x = np.asarray(x, dtype=np.float64)
+            x = x * (1.0 + self.store_noise * self._noise_rng.uniform(-1.0, 1.0, x.shape))
+        return to_bf16(x)
 
     def _span(self, b):
         start = self.cfg.prompt_len + b * self.cfg.block
@@ -494,11 +521,14 @@ class PolestarOracle:
         nw = len(win)
         st.labels, st.z, st.s, st.A = [], [], [], []
         st.codes, st.sbytes, st.code_margin, st.P_prev = [], [], [], []
-        out = dict(kmeans_margin=[], labels=[], z=[], A=[])
+        out = dict(kmeans_margin=[], labels=[], z=[], A=[], own_labels=[])
         self.exact_H[si] = [x.copy() for x in Hw]
         for l in range(c.n_layers):
             init = kmeans_init(c.seed, si, b, l, nw, c.K)
             lab, z, s, A, gap = spherical_kmeans(Hw[l], c.K, c.kmeans_iters, init)
+            out["own_labels"].append(lab)
+            if self.follow is not None:
+                lab, z, s, A = self._adopt_labels(Hw[l], self.follow.seqs[si].labels[l], z)
             st.labels.append(lab)
             st.z.append(z)
             st.s.append(s)
@@ -516,6 +546,23 @@ class PolestarOracle:
         st.theta = [[] for _ in range(c.block)]
         return out
 
+    @staticmethod
+    def _adopt_labels(H, labels, z_own):
+        """The last update of spherical K-means for given final labels: member
+        sums of the unit rows, their normalisation, and the raw member means
+        (an empty cluster keeps this oracle's own centroid)."""
+        H = np.asarray(H, dtype=np.float64)
+        X = H / np.linalg.norm(H, axis=1, keepdims=True)
+        K = len(z_own)
+        z, s, A = z_own.copy(), z_own.copy(), np.zeros_like(z_own)
+        for c in range(K):
+            mem = labels == c
+            if np.any(mem):
+                s[c] = X[mem].sum(axis=0)
+                z[c] = s[c] / np.linalg.norm(s[c])
+                A[c] = H[mem].mean(axis=0)
+        return np.asarray(labels).copy(), z, s, to_f32(A)
+
     # ---- within-block step (Algorithm 1, layer loop; §4.1 Update Schedule) -------------
     def _step(self, si, st, x0, b, n_unmasked):
         c = self.cfg
@@ -532,7 +579,7 @@ class PolestarOracle:
         act = np.asarray(x0[start:end], dtype=np.float64)
         U = np.asarray(x0[win], dtype=np.float64)  # layer-0 packet: current inputs
         sel = np.ones(nw, dtype=bool)
-        rec = dict(fire=fire, D=[], topk=[], topk_margin=[], sel=[])
+        rec = dict(fire=fire, D=[], topk=[], topk_margin=[], sel=[], own_topk=[])
         for l in range(c.n_layers):
             kv = st.kv[l]
             if fire:
@@ -561,6 +608,9 @@ class PolestarOracle:
                 D = np.mean(kl_div(s, lse, ps, plse), axis=1)
                 st.P_prev[l] = (s, lse)
                 ids, margin = topk_clusters(D, c.topk)
+                rec["own_topk"].append(ids)
+                if self.follow is not None:
+                    ids = list(self.follow.last_recs[si]["topk"][l])
                 sel = np.isin(st.labels[l], ids)
                 rec["D"].append(D)
                 rec["topk"].append(ids)
@@ -597,6 +647,7 @@ class PolestarOracle:
                 recs.append(self._block_entry(si, st, x0[si], block_index))
             else:
                 recs.append(self._step(si, st, x0[si], block_index, n_unmasked[si]))
+        self.last_recs = recs
         return recs
 
     # ---- Polestar-Commit (§4.2; Algorithm 1, commit phases) ------------------------------

@@ -22,7 +22,7 @@ def _run(name, kv_tol, act_tol, **kw):
     ls = Lockstep(w, kv_tol=kv_tol, act_tol=act_tol)
     rep = ls.run()
     ls.lib.close()
-    print(name, rep)
+    print(name, f"near ties {rep.near_ties}, sensitivity ties {rep.sensitivity_ties}", rep)
     return rep
 
 
@@ -36,10 +36,21 @@ def test_tiny_fp32_trajectory():
 @pytest.mark.parametrize("name", ["mini_l2_d512_bf16", "mini_gqa_l2_d448_bf16"])
 def test_mini_bf16_trajectory(name):
     """Two-layer bf16 stacks (MHA and 7:1 GQA): decisions exact up to counted near
-    ties; K/V, active outputs and update packets within 1e-2 relative L2."""
+    ties and sensitivity ties (the oracle's own perturbed copies); KL within
+    1e-5 + 1e-3 rel plus the oracle-measured band; K/V, active outputs and
+    update packets within 1e-2 relative L2."""
     rep = _run(name, kv_tol=1e-2, act_tol=1e-2, n_steps=None)
     assert rep.compared >= 8 and rep.fires >= 3, rep
-    assert rep.near_ties <= 2
+    assert rep.near_ties + rep.sensitivity_ties <= 3
+
+
+def test_mini_bf16_trajectory_nonunit_norm_gains():
+    """The same lockstep with distinct, non-unit RMSNorm gains per norm and layer
+    (the benchmark shapes use gains 1): a swap of the attention and FFN norms,
+    or a gain applied twice or not at all, cannot pass."""
+    rep = _run("mini_l2_d512_bf16", kv_tol=1e-2, act_tol=1e-2, n_steps=None, norm_gain_std=0.3)
+    assert rep.compared >= 8 and rep.fires >= 3, rep
+    assert rep.near_ties + rep.sensitivity_ties <= 3
 
 
 def test_mini_bf16_trajectory_tcgen05_attention():
@@ -52,4 +63,4 @@ def test_mini_bf16_trajectory_tcgen05_attention():
     finally:
         P.attention_impl(old)
     assert rep.compared >= 8 and rep.fires >= 3, rep
-    assert rep.near_ties <= 2
+    assert rep.near_ties + rep.sensitivity_ties <= 3

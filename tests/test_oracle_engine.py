@@ -144,25 +144,39 @@ def test_proxy_query_of_a_token_at_position_0_equals_its_query():
     assert not np.allclose(orc.scores(q7, kv), s_tok, atol=1e-6)
 
 
-def test_oracle_trigger_equals_library_host_trigger():
-    """The oracle's refresh decisions over a trajectory equal the library's host
-    trigger (polestar_debug_trigger) fed the same unmasked counts, block by block."""
-    import ctypes
-    from drift_aware_kv_gb300 import polestar as P
-    lib = P.load()
-    lib.polestar_debug_trigger.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
-    for tau in (0, 3, 5):
-        cfg = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(tau_upd=tau)
-        orc, out = _run(cfg)
-        blocks = {}
-        for st, recs, _ in out:
-            if st["block_entry"]:
-                blocks[st["block_index"]] = ([], [])
-            else:
-                blocks[st["block_index"]][0].append(st["n_unmasked"][0])
-                blocks[st["block_index"]][1].append(bool(recs[0]["fire"]))
-        for ns, fires in blocks.values():
-            arr = (ctypes.c_int32 * max(1, len(ns)))(*ns)
-            res = (ctypes.c_uint8 * max(1, len(ns)))()
-            assert lib.polestar_debug_trigger(tau, arr, len(ns), res) == P.OK
-            assert [bool(v) for v in list(res)[:len(ns)]] == fires
+def _oracle_fires(tau_upd, counts_per_block):
+    """Refresh decisions of the oracle engine itself over hand-chosen unmasked
+    counts: each entry of counts_per_block is one block (a block entry, then one
+    within-block step per count).  The inputs do not change between steps; only
+    the counts drive the trigger."""
+    cfg = synth.WORKLOADS["tiny_l1_d256_fp32"].replace(tau_upd=tau_upd)
+    W = O.weights_to_numpy(synth.make_weights(cfg))
+    orc = O.PolestarOracle(cfg, W)
+    x0 = synth.Trajectory(cfg).next_step()["x0"].double().numpy()
+    out = []
+    for b, counts in enumerate(counts_per_block):
+        orc.calibrate_step(x0, [0], b, True)
+        out.append([bool(orc.calibrate_step(x0, [n], b, False)[0]["fire"]) for n in counts])
+    return out
+
+
+@pytest.mark.parametrize("tau,counts,expected", [
+    # §4.1 "Update Schedule": refresh once the tokens unmasked since the last
+    # refresh exceed tau_upd (R10: this step's count included), then restart
+    (3, [1, 1, 1, 1, 1, 1, 1, 1], [0, 0, 0, 1, 0, 0, 0, 1]),
+    (3, [4, 0, 0, 5], [1, 0, 0, 1]),          # more than tau_upd in one step
+    (3, [3, 0, 0, 0, 1], [0, 0, 0, 0, 1]),    # exactly tau_upd is not enough ("exceeds")
+    (3, [2, 2, 2, 2], [0, 1, 0, 1]),
+    (3, [0, 0, 0], [0, 0, 0]),                # nothing unmasked: never
+    (0, [1, 0, 2, 0], [1, 0, 1, 0]),          # tau_upd = 0: every step that unmasks
+    (5, [6, 3, 3, 5, 1], [1, 0, 1, 0, 1]),
+])
+def test_oracle_trigger_closed_form(tau, counts, expected):
+    assert _oracle_fires(tau, [counts]) == [[bool(e) for e in expected]]
+
+
+def test_oracle_trigger_restarts_at_block_entry():
+    """A block entry rebuilds every cluster and proxy baseline, so the count
+    since the last refresh restarts there: 3 tokens left over from block 0 do
+    not add to block 1's first count of 1."""
+    assert _oracle_fires(3, [[1, 1, 1], [1, 3]]) == [[False, False, False], [False, True]]
