@@ -33,13 +33,25 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "llada8b_p512_g256_b1"
-# DRAM bytes (read + write) per launch of a kernel class, from one Nsight Compute
-# capture of the current kernels (profiles/gemm_tc_projections_llada8b_b1.md:
-# mean over the four within-block projection launches of a layer).  Reset to
-# None whenever those kernels change.
-NCU_TRAFFIC_PER_LAUNCH = {("llada8b_p512_g256_b1", "gemm_step"): 114.5e6}
+# the largest workload that fits one GPU: LLaDA-8B shape, batch 32, prompt 1024,
+# generation 1024 (the stress configuration: the sparse refresh fires every step)
+DEFAULT_WORKLOAD = "llada8b_p1024_g1024_b32"
+# the other full-size workloads, measured after the headline (their own lines in
+# "other_workloads"; fewer steps each)
+DEFAULT_ALSO = "llada8b_p512_g256_b1,llada8b_p512_g512_b8,dream7b_p512_g256_b4"
+# DRAM bytes (read + write) per launch of a kernel class, taken from one Nsight
+# Compute capture of the current kernels (dram__bytes_read.sum +
+# dram__bytes_write.sum, mean over the class's launches in the captured step),
+# keyed by workload and class; an entry is removed whenever those kernels change,
+# and the line then reports traffic null.
+NCU_TRAFFIC_PER_LAUNCH = {}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+_T0 = time.perf_counter()
+
+
+def log(msg):
+    """Progress on stderr (the JSON line alone goes to stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
 
 
 def load_peaks():
@@ -143,10 +155,10 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 def make_inputs(w, n_steps, device):
-    """Trajectory inputs of the first n_steps steps, moved to `device`."""
+    """Trajectory inputs of the first n_steps steps, drawn on `device`."""
     import torch
     from drift_aware_kv_gb300 import synth
-    tr = synth.Trajectory(w)
+    tr = synth.Trajectory(w, device=device)
     dt = synth.torch_dtype(w)
     steps = []
     for _ in range(n_steps):
@@ -154,34 +166,62 @@ def make_inputs(w, n_steps, device):
         if st is None:
             break
         steps.append(dict(
-            x0=st["x0"].to(dt).to(device), logits=st["logits"].to(device),
-            masked=st["masked"].to(torch.uint8).to(device), n_unmasked=st["n_unmasked"],
-            block_index=st["block_index"], block_entry=st["block_entry"]))
+            x0=st["x0"].to(dt), logits=st["logits"], masked=st["masked"].to(torch.uint8),
+            n_unmasked=st["n_unmasked"], block_index=st["block_index"], block_entry=st["block_entry"]))
     return steps
 
 
-def run_device(args, w, peaks, ws, rank, local):
+# classes whose roofline the line reports, with their bound: projections are
+# tensor-bound at batch >= 8 and at block entries, HBM-bound (weight stream)
+# below; everything else moves bytes
+def class_roofline(name, s, w, peaks):
+    if s["launches"] == 0 or s["ms"] <= 0:
+        return None
+    tensor = name == "gemm_entry" or (name == "gemm_step" and w.batch >= 8)
+    if tensor:
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        achieved = s["flops"] / (s["ms"] / 1e3) / 1e12
+        r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+             "peak_source": peaks["_source"] + " bf16 sustained"}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = s["bytes"] / (s["ms"] / 1e3) / 1e9
+        r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+             "peak_source": peaks["_source"] + " copy"}
+    r["traffic"] = NCU_TRAFFIC_PER_LAUNCH.get((w.name, name))
+    r["algorithmic_bytes_per_launch"] = s["bytes"] / s["launches"]
+    r["algorithmic_flops_per_launch"] = s["flops"] / s["launches"]
+    r["avg_launch_us"] = s["ms"] * 1e3 / s["launches"]
+    r["launches"] = s["launches"]
+    if s["flops"] > 0:
+        r["tflops"] = s["flops"] / (s["ms"] / 1e3) / 1e12
+    if s["bytes"] > 0:
+        r["gbs"] = s["bytes"] / (s["ms"] / 1e3) / 1e9
+    return r
+
+
+def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
+    """Warm-up + timed steps of one workload.  full: also the calibration-
+    overhead region and the end-to-end region (the headline workload)."""
     import torch
     from drift_aware_kv_gb300 import polestar as P
     from drift_aware_kv_gb300 import synth
-    from drift_aware_kv_gb300.build import build
 
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if rank == 0 or ws == 1:
-        build()
-    barrier(ws)
+    log(f"{w.name}: weights")
     W = synth.make_weights(w, dev)
-    total = args.warmup + args.steps
+    total = n_warmup + n_timed
+    log(f"{w.name}: inputs of {total} steps")
     steps = make_inputs(w.replace(seed=w.seed + rank), total, dev)
     if len(steps) < total:
-        raise SystemExit(f"trajectory has only {len(steps)} steps < warmup + steps = {total}")
+        raise SystemExit(f"{w.name}: trajectory has only {len(steps)} steps < warmup + steps = {total}")
+    torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     # the NVFP4 store's host traffic runs on a side stream of its own
     offload = not args.device_store
     side = torch.cuda.Stream(dev) if offload else None
     cm = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device=dev)
-    timed = steps[args.warmup:]
+    timed = steps[n_warmup:]
 
     def region(profile: bool, no_refresh: bool = False):
         """Fresh context: warm-up steps, then the timed steps.  The headline
@@ -199,7 +239,7 @@ def run_device(args, w, peaks, ws, rank, local):
             fired.append(not st["block_entry"] and all(o.fire[s] for s in range(w.batch)))
             ps.commit(st["logits"], st["masked"], cm)
 
-        for st in steps[: args.warmup]:
+        for st in steps[:n_warmup]:
             do_step(st)
         torch.cuda.synchronize(dev)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(timed) + 1)]
@@ -230,25 +270,28 @@ def run_device(args, w, peaks, ws, rank, local):
         total_ms = ev[0].elapsed_time(ev[-1])
         ps.close()
         return dict(stats=stats, launches=launches, step_ms=step_ms, total_ms=total_ms, wall=wall,
-                    clocks=clocks, issue_first=issue_first, fired=fired[args.warmup:])
+                    clocks=clocks, issue_first=issue_first, fired=fired[n_warmup:])
 
+    log(f"{w.name}: timed region")
     main = region(profile=False)
+    log(f"{w.name}: profiled region")
     prof = region(profile=True)
-    # calibration overhead (the pages' App. D.10 measure): within-block steps in
-    # which every sequence refreshed, against the same steps without refresh
-    base = region(profile=False, no_refresh=True)
-    fired_idx = [i for i, f in enumerate(main["fired"]) if f]
     overhead = None
-    if fired_idx:
-        t_fire = statistics.mean(main["step_ms"][i] for i in fired_idx)
-        t_base = statistics.mean(base["step_ms"][i] for i in fired_idx)
-        overhead = {"ms_per_layer": (t_fire - t_base) / w.n_layers, "steps": len(fired_idx),
-                    "step_ms_refreshing": t_fire, "step_ms_same_steps_no_refresh": t_base,
-                    "what": "per-layer added time of a within-block step in which every sequence runs the "
-                            "sparse refresh (patch, centroid update, proxy attention + KL, top-k, update "
-                            "packets), against the same step with the trigger off"}
+    if full:
+        # calibration overhead (the pages' App. D.10 measure): within-block steps
+        # in which every sequence refreshed, against the same steps without refresh
+        log(f"{w.name}: same steps without refresh")
+        base = region(profile=False, no_refresh=True)
+        fired_idx = [i for i, f in enumerate(main["fired"]) if f]
+        if fired_idx:
+            t_fire = statistics.mean(main["step_ms"][i] for i in fired_idx)
+            t_base = statistics.mean(base["step_ms"][i] for i in fired_idx)
+            overhead = {"ms_per_layer": (t_fire - t_base) / w.n_layers, "steps": len(fired_idx),
+                        "step_ms_refreshing": t_fire, "step_ms_same_steps_no_refresh": t_base,
+                        "what": "per-layer added time of a within-block step in which every sequence runs the "
+                                "sparse refresh (patch, centroid update, proxy attention + KL, top-k, update "
+                                "packets), against the same step with the trigger off"}
     stats = prof["stats"]
-    launches = main["launches"]
     step_ms, total_ms, wall, clocks = main["step_ms"], main["total_ms"], main["wall"], main["clocks"]
     total_s = max_over_ranks(total_ms / 1e3, ws, dev)
     n_entry = sum(1 for st in timed if st["block_entry"])
@@ -258,57 +301,58 @@ def run_device(args, w, peaks, ws, rank, local):
 
     # ---- e2e: host buffers through polestar_step_host, copies in the timed region
     e2e = None
-    if not args.no_e2e:
-        ps2 = P.Polestar(w, W, stream=stream, side_stream=side, host_offload=offload)
+    if full and not args.no_e2e:
+        # the first e2e_steps timed steps again, from pinned host buffers, after
+        # the same warm-up (the last three warm-up steps also through the host path)
+        n_e = min(args.e2e_steps, len(timed))
+        ew = min(n_warmup, 3)
+        log(f"{w.name}: pinned host copies of {ew + n_e} steps' inputs")
         host = []
-        for st in steps:
+        for st in steps[n_warmup - ew: n_warmup + n_e]:
             host.append(dict(x0=st["x0"].cpu().pin_memory(), logits=st["logits"].cpu().pin_memory(),
                              masked=st["masked"].cpu().pin_memory(), n_unmasked=st["n_unmasked"],
                              block_index=st["block_index"], block_entry=st["block_entry"]))
+        ps2 = P.Polestar(w, W, stream=stream, side_stream=side, host_offload=offload)
         cmh = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8).pin_memory()
-        for st in host[: args.warmup]:
+        for st in steps[:n_warmup - ew]:
+            ps2.calibrate_step(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"])
+            ps2.commit(st["logits"], st["masked"], cm)
+        for st in host[:ew]:
             ps2.step_host(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"], st["logits"],
                           st["masked"], cmh)
+        log(f"{w.name}: end-to-end region")
         barrier(ws)
         t0 = time.perf_counter()
-        for st in host[args.warmup:]:
+        for st in host[ew:]:
             ps2.step_host(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"], st["logits"],
                           st["masked"], cmh)
         e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
         ps2.close()
         h2d = host[0]["x0"].numel() * host[0]["x0"].element_size() + \
             host[0]["logits"].numel() * 4 + host[0]["masked"].numel()
-        e2e = {"value": aggregate_line(len(timed), ws, e2e_s), "unit": "steps/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(cmh.numel())}
+        n_e_entry = sum(1 for st in host[ew:] if st["block_entry"])
+        dev_ms = sum(step_ms[:n_e])
+        e2e = {"value": aggregate_line(n_e, ws, e2e_s), "unit": "steps/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(cmh.numel()),
+               "steps": n_e, "block_entries": n_e_entry,
+               "device_value_same_steps": 1e3 * n_e / dev_ms if dev_ms > 0 else None,
+               "what": f"the first {n_e} timed steps through polestar_step_host from pinned host buffers "
+                       "(x0, logits and mask in, commit mask out, copies inside the timed region)"}
+        del host
 
-    # ---- roofline of the dominant kernel class
+    rooflines = {k: class_roofline(k, v, w, peaks) for k, v in stats.items()}
+    rooflines = {k: v for k, v in rooflines.items() if v is not None}
     dom = max(stats, key=lambda k: stats[k]["ms"])
-    s = stats[dom]
-    if dom in ("gemm_entry",) or (dom == "gemm_step" and w.batch >= 8):
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-        achieved = s["flops"] / (s["ms"] / 1e3) / 1e12 if s["ms"] > 0 else 0.0
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "peak_source": peaks["_source"] + " sustained"}
-    else:
-        peak = peaks["hbm_gbs"]
-        achieved = s["bytes"] / (s["ms"] / 1e3) / 1e9 if s["ms"] > 0 else 0.0
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None, "peak_source": peaks["_source"]}
-    roof["traffic"] = NCU_TRAFFIC_PER_LAUNCH.get((w.name, dom))
+    roof = dict(rooflines[dom])
+    roof["kernel"] = dom
     roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
-    roof["algorithmic_bytes_per_launch"] = s["bytes"] / max(1, s["launches"])
-    roof["avg_launch_us"] = s["ms"] * 1e3 / max(1, s["launches"])
-    roof["launches"] = s["launches"]
     roof["measured_in"] = "profiled timed region (same steps, CUDA events around each launch)"
 
     nw_mean = statistics.mean(len(synth.window_positions(w, st["block_index"])) for st in timed)
     value = aggregate_line(len(timed), ws, total_s)
-    out = {
-        "metric": "calibration steps/s", "value": value, "unit": "steps/s", "n_gpus": ws,
-        "steps": len(timed), "warmup": args.warmup, "ms_per_step": total_ms / len(timed),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic (seeded trajectory, random-init N(0,0.02) weights)",
-        "config": {"workload": w.name, "model": "LLaDA-8B-shaped" if "llada" in w.name else w.name,
+    return {
+        "value": value, "ms_per_step": total_ms / len(timed), "steps": len(timed), "warmup": n_warmup,
+        "config": {"workload": w.name, "model": "LLaDA-8B-shaped" if "llada" in w.name else "Dream-7B-shaped",
                    "layers": w.n_layers, "d_model": w.d_model, "batch": w.batch, "seq_len": w.seq_len,
                    "block": w.block, "window": w.prefix_win + w.suffix_win, "K": w.K, "topk": w.topk,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -323,27 +367,59 @@ def run_device(args, w, peaks, ws, rank, local):
         "profiled_region_ms_per_step": prof["total_ms"] / len(timed),
         "kernel_launches": {k: v["launches"] for k, v in stats.items()},
         "calibration_overhead": overhead,
-        "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
-        "wall_s": wall,
+        "roofline": roof, "rooflines": rooflines, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": int(main["launches"]), "wall_s": wall,
         "host_issue_ms_first_step": main["issue_first"] * 1e3,
         "first_step_block_entry": bool(timed[0]["block_entry"]),
     }
+
+
+def run_device(args, w, peaks, ws, rank, local):
+    import torch
+    from drift_aware_kv_gb300 import synth
+    from drift_aware_kv_gb300.build import build
+
+    torch.cuda.set_device(local)
+    if rank == 0 or ws == 1:
+        build()
+    barrier(ws)
+    out = run_workload(args, w, peaks, ws, rank, local, args.warmup, args.steps, full=True)
+    out.update({"metric": "calibration steps/s", "unit": "steps/s", "n_gpus": ws, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+                "data": "synthetic (seeded trajectory drawn on the GPU, random-init N(0,0.02) weights)"})
+    others = {}
+    for name in [n for n in args.also.split(",") if n and n != w.name]:
+        torch.cuda.empty_cache()
+        wo = synth.WORKLOADS[name]
+        r = run_workload(args, wo, peaks, ws, rank, local, 3, args.also_steps, full=False)
+        others[name] = {k: r[k] for k in ("value", "ms_per_step", "steps", "warmup", "window_tokens_per_s",
+                                          "block_entry_ms", "within_block_ms", "within_block_steps_per_s",
+                                          "kernel_ms_profiled_region", "roofline", "rooflines", "clocks",
+                                          "gpu_launches")}
+        others[name]["config"] = r["config"]
+    out["other_workloads"] = others
     return out
 
 
 # ------------------------------------------------------------------ CPU oracle
+def oracle_sample_workload(w, n_layers_sample):
+    """The bounded sample the CPU oracle runs: sequence 0 of the workload (its own
+    seeded drift schedule) on the first n_layers_sample layers.  Every other knob
+    of the workload stays as it is."""
+    return w.replace(batch=1, n_layers=min(n_layers_sample, w.n_layers))
+
+
 def oracle_sample(w, n_layers_sample, n_steps, warmup=0):
-    """Time the unmodified CPU oracle on the workload truncated to the first
-    n_layers_sample layers; returns per-step seconds scaled to all layers."""
-    import numpy as np
+    """Time the unmodified CPU oracle over the first warmup + n_steps trajectory
+    steps of the sample workload; returns the seconds of each timed step (what
+    was run, unscaled) and whether it was a block entry."""
     from drift_aware_kv_gb300 import synth
     from oracle import polestar_oracle as O
-    ws = w.replace(n_layers=n_layers_sample)
+    ws = oracle_sample_workload(w, n_layers_sample)
     W = O.weights_to_numpy(synth.make_weights(ws, "cpu"))
     orc = O.PolestarOracle(ws, W)
     tr = synth.Trajectory(ws)
     dt = synth.torch_dtype(ws)
-    scale = w.n_layers / n_layers_sample
     times, kinds = [], []
     for i in range(warmup + n_steps):
         st = tr.next_step()
@@ -357,7 +433,7 @@ def oracle_sample(w, n_layers_sample, n_steps, warmup=0):
         orc.commit(lg, mk)
         dtm = time.perf_counter() - t0
         if i >= warmup:
-            times.append(dtm * scale)
+            times.append(dtm)
             kinds.append(bool(st["block_entry"]))
     return times, kinds
 
@@ -401,39 +477,65 @@ def oracle_pieces(w, seed=0):
     return out
 
 
+CPU_SAMPLE_LAYERS = 1
+
+
 def cpu_baseline(w, n_entry, n_within, budget_steps=3):
+    """The oracle on a bounded sample (sequence 0, first layer, the first
+    budget_steps trajectory steps: a block entry and within-block steps), plus
+    its separate pieces at full size.  `value` converts the sample's measured
+    per-step seconds to whole-workload steps/s -- every layer of every sequence,
+    with the timed GPU steps' mix of block entries and within-block steps -- by
+    plain multiplication (the oracle runs sequences and layers one after the
+    other); that conversion is an estimate and is labelled so."""
     try:
         oracle_pieces(w)  # first touch of the large arrays, thread pools
         pieces = oracle_pieces(w)
     except Exception as e:  # an auxiliary figure never stops the bench line
         pieces = {"error": repr(e)}
-    times, kinds = oracle_sample(w, min(2, w.n_layers), budget_steps)
+    t0 = time.perf_counter()
+    times, kinds = oracle_sample(w, CPU_SAMPLE_LAYERS, budget_steps)
+    wall = time.perf_counter() - t0
     te = [t for t, k in zip(times, kinds) if k]
     tw = [t for t, k in zip(times, kinds) if not k]
     te_m = statistics.mean(te) if te else None
     tw_m = statistics.mean(tw) if tw else None
+    scale = w.batch * w.n_layers / min(CPU_SAMPLE_LAYERS, w.n_layers)
     n = n_entry + n_within
-    est = ((n_entry * (te_m or 0)) + (n_within * (tw_m or te_m or 0))) / max(1, n)
+    est = scale * ((n_entry * (te_m or 0)) + (n_within * (tw_m or te_m or 0))) / max(1, n)
     return {"value": 1.0 / est if est > 0 else None, "unit": "steps/s", "cores": blas_threads(),
             "kind": "oracle",
-            "sample": (f"first {len(times)} steps of the {w.name} trajectory on {min(2, w.n_layers)} of "
-                       f"{w.n_layers} layers (numpy float64), times x{w.n_layers / min(2, w.n_layers):g}, mixed {n_entry} entry : {n_within} "
-                       f"within-block like the timed GPU steps"),
-            "entry_s_per_step": te_m, "within_s_per_step": tw_m, "pieces_full_size": pieces}
+            "value_is": (f"estimate: the sample's measured seconds per step x {scale:g} (batch {w.batch} x "
+                         f"{w.n_layers} layers / {min(CPU_SAMPLE_LAYERS, w.n_layers)} sampled), weighted "
+                         f"{n_entry} entry : {n_within} within-block like the timed GPU steps"),
+            "sample": (f"sequence 0 of {w.name}, layer 0 only, first {len(times)} trajectory steps "
+                       f"(numpy float64 on the host's BLAS threads)"),
+            "sample_s_per_step": {"block_entry": te_m, "within_block": tw_m},
+            "sample_wall_s": wall, "pieces_full_size": pieces}
 
 
 def run_reference(args, w):
-    """Reference arm: the CPU oracle as it stands, on the same workload and metric."""
-    times, kinds = oracle_sample(w, min(2, w.n_layers), args.steps, warmup=args.warmup)
+    """Reference arm: the CPU oracle as it stands, timed step by step.  Each step
+    is a bounded sample of the workload -- one trajectory step of sequence 0 on
+    the first layer -- and `value` is those sample steps per second, exactly as
+    timed.  The whole-workload equivalent (every layer of every sequence) is a
+    separately named estimate."""
+    t0 = time.perf_counter()
+    times, kinds = oracle_sample(w, CPU_SAMPLE_LAYERS, args.steps, warmup=args.warmup)
+    wall = time.perf_counter() - t0
     total = sum(times)
     value = len(times) / total
-    cb = {"value": value, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
-          "sample": f"{len(times)} trajectory steps of {w.name} on {min(2, w.n_layers)} of "
-                    f"{w.n_layers} layers, times x{w.n_layers / min(2, w.n_layers):g}"}
+    scale = w.batch * w.n_layers / min(CPU_SAMPLE_LAYERS, w.n_layers)
+    sample = (f"each step: one trajectory step (calibrate + commit) of sequence 0 of {w.name} on layer 0 "
+              f"only; {sum(kinds)} of the {len(times)} timed steps are block entries")
+    cb = {"value": value, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle", "sample": sample}
     return {"impl": "reference", "metric": "calibration steps/s", "value": value, "unit": "steps/s",
             "n_gpus": 1, "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name}, "cpu_baseline": cb,
+            "data": "synthetic", "config": {"workload": w.name, "sample": sample}, "cpu_baseline": cb,
+            "whole_step_estimate": {"steps_per_s": value / scale,
+                                    "is": f"estimate: sample steps/s / {scale:g} (batch x layers / sampled layers)"},
+            "wall_s": wall,
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -444,7 +546,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="polestar", choices=["polestar", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--also", default=DEFAULT_ALSO,
+                    help="comma-separated further workloads measured after the headline ('' for none)")
+    ap.add_argument("--also-steps", type=int, default=8, help="timed steps of each further workload")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=8,
+                    help="timed steps replayed end to end from pinned host buffers (1.6 GB each at batch 32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--device-store", action="store_true",
                     help="keep the NVFP4 residual store in device memory instead of pinned host memory")
@@ -463,8 +570,10 @@ def main():
     out = run_device(args, w, peaks, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
+            log("cpu baseline (oracle sample)")
             out["cpu_baseline"] = cpu_baseline(w, out["config"]["timed_block_entries"],
                                                out["config"]["timed_within_block_steps"])
+        log("done")
         print(json.dumps(out), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -36,7 +36,12 @@ constexpr int BM = 128;         // rows per UMMA
 constexpr int BN = 128;         // columns per CTA
 constexpr int BK = 64;          // K elements per stage (one 128-byte swizzle row)
 constexpr int THREADS = 192;    // 6 warps
-constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+// Bound of every mbarrier wait of the kernels in this file, in SM clock cycles
+// (default ~2 s at 2 GHz).  A device variable rather than a constant so that a
+// test can shorten it and make a wait run out (tc_debug_stalled_wait); it is
+// read only while a wait is already spinning.
+constexpr long long TIMEOUT_CYCLES = 4000000000LL;
+__device__ long long g_wait_limit_cycles = TIMEOUT_CYCLES;
 constexpr int RED_PITCH = BN + 4;                     // fp32 staging row pitch
 
 struct Params {
@@ -98,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > TIMEOUT_CYCLES) {
+    if (clock64() - t0 > g_wait_limit_cycles) {
       atomicExch(err, code);
       *abort_flag = 1;
       return false;
@@ -781,7 +786,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   const long long t0 = clock64();
   while (!mbar_try_cluster(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > TIMEOUT_CYCLES) {
+    if (clock64() - t0 > g_wait_limit_cycles) {
       atomicExch(err, code);
       *abort_flag = 1;
       return false;
@@ -1377,7 +1382,35 @@ cudaError_t launch_ws(const CUtensorMap* a, const CUtensorMap* const* b, const P
   return cudaLaunchKernelEx(&cfg, gemm_ws_kernel, *a, *b[0], *b[1], *b[2], p);
 }
 
+// A wait that nothing ever satisfies: one thread initialises an mbarrier with
+// one expected arrival, never arrives, and waits for its first phase with the
+// same bounded wait as the GEMM kernels, which gives up after the limit and
+// records `code` in the error word.
+__global__ void stalled_wait_kernel(int* err, int code) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(smem_u32(&bar), 0, err, code, (volatile int*)&abort_flag);
+  }
+}
+
 }  // namespace tc
+
+cudaError_t tc_debug_stalled_wait(int* err, int code, long long limit_cycles, cudaStream_t st) {
+  if (!err || limit_cycles < 1) return cudaErrorInvalidValue;
+  const long long lim = limit_cycles, def = tc::TIMEOUT_CYCLES;
+  cudaError_t e = cudaMemcpyToSymbolAsync(tc::g_wait_limit_cycles, &lim, sizeof(lim), 0, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  tc::stalled_wait_kernel<<<1, 32, 0, st>>>(err, code);
+  e = cudaGetLastError();
+  // the default bound again for every later launch on this stream
+  const cudaError_t e2 = cudaMemcpyToSymbolAsync(tc::g_wait_limit_cycles, &def, sizeof(def), 0,
+                                                 cudaMemcpyHostToDevice, st);
+  return e != cudaSuccess ? e : e2;
+}
 
 int* tc_error_word(TcGemmCache* cache) {
   if (!cache->err) {

@@ -90,6 +90,13 @@ cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, in
 // Device word holding the code of the first timed-out wait (0 = none).
 int* tc_error_word(TcGemmCache* cache);
 
+// Test of the bounded waits: on `st`, shortens the wait bound of this file's
+// kernels to limit_cycles, runs one kernel whose mbarrier wait can never be
+// satisfied (it gives up after the bound and writes `code` to *err), then
+// restores the default bound.  The bound is a per-device variable shared by
+// every stream: other work in flight meanwhile sees the short bound too.
+cudaError_t tc_debug_stalled_wait(int* err, int code, long long limit_cycles, cudaStream_t st);
+
 void tc_gemm_cache_clear(TcGemmCache* cache);
 
 }  // namespace polestar

@@ -1462,6 +1462,16 @@ extern "C" int32_t polestar_debug_window(int32_t prompt_len, int32_t gen_len, in
   return (int32_t)w.size();
 }
 
+extern "C" polestar_status polestar_debug_stalled_wait(polestar_ctx* c, int64_t limit_cycles) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (limit_cycles < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "limit_cycles must be positive");
+  int* err = tc_error_word(&c->tc);
+  if (!err) return fail(c, POLESTAR_ERR_OOM, "device error word");
+  const cudaError_t e = tc_debug_stalled_wait(err, 99, (long long)limit_cycles, c->sm);
+  if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("stalled wait: ") + cudaGetErrorString(e));
+  return record_timeouts(c);
+}
+
 extern "C" polestar_status polestar_debug_trigger(int32_t tau_upd, const int32_t* n_unmasked, int32_t steps,
                                                   uint8_t* fire) {
   if (steps < 0 || (steps > 0 && (!n_unmasked || !fire))) return POLESTAR_ERR_INVALID_ARG;

@@ -109,9 +109,32 @@ def bench_stale(a):
     return dict(kernel="kv_staleness", rows=a.rows, Hkv=a.Hkv, dh=a.dh, us=ms * 1e3, GBps=byts / ms / 1e6)
 
 
+def bench_codec(a):
+    """Encode + decode of one storage format over `rows` window rows of width d
+    (residual against 8 anchors), bytes moved = the fp32 states read and written
+    plus the codes and scales written and read back."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cuda").manual_seed(0)
+    h = torch.randn(a.rows, a.d, device="cuda", generator=g)
+    anchors = torch.randn(8, a.d, device="cuda", generator=g)
+    labels = torch.randint(0, 8, (a.rows,), device="cuda", generator=g).to(torch.uint8)
+    out = torch.empty_like(h)
+    codes, scales = P.codec_encode(a.fmt, h, anchors, labels)
+
+    def run():
+        P.codec_encode(a.fmt, h, anchors, labels)
+        P.codec_decode(a.fmt, codes, scales, a.rows, a.d, anchors, labels, out=out)
+
+    ms = _time(run, a.iters)
+    nc, ns = P.codec_bytes(a.fmt, a.rows, a.d)
+    byts = 2 * a.rows * a.d * 4 + 2 * (nc + ns)
+    return dict(kernel="codec", fmt=a.fmt, rows=a.rows, d=a.d, us=ms * 1e3, GBps=byts / ms / 1e6)
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemm", "attn", "kmeans", "stale"])
+    ap.add_argument("kernel", choices=["gemm", "attn", "kmeans", "stale", "codec"])
+    ap.add_argument("--fmt", default="nvfp4", help="codec: fp16, fp8, int8, mxfp4, int2, nvfp4")
     ap.add_argument("--rows", type=int, default=24576, help="staleness: cache rows (layers x positions)")
     ap.add_argument("--M", type=int, default=136)
     ap.add_argument("--N", type=int, default=None, help="gemm N (default 4096) / attention keys (default 768)")
@@ -142,7 +165,8 @@ def main():
         a.N = 4096 if a.kernel == "gemm" else 768
     from drift_aware_kv_gb300.build import build
     build()
-    fn = {"gemm": bench_gemm, "attn": bench_attn, "kmeans": bench_kmeans, "stale": bench_stale}[a.kernel]
+    fn = {"gemm": bench_gemm, "attn": bench_attn, "kmeans": bench_kmeans, "stale": bench_stale,
+          "codec": bench_codec}[a.kernel]
     print(json.dumps(fn(a)))
 
 

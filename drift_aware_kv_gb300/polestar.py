@@ -27,7 +27,9 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_debug_gemm_choice",
             "polestar_debug_attention_impl", "polestar_debug_gemm_swiglu", "polestar_full_forward",
             "polestar_kv_staleness", "polestar_cache_staleness", "polestar_debug_attention_items",
-            "polestar_debug_window", "polestar_debug_trigger")
+            "polestar_debug_window", "polestar_debug_trigger", "polestar_debug_stalled_wait",
+            "polestar_codec_bytes", "polestar_codec_encode", "polestar_codec_decode")
+CODECS = {"fp16": 0, "fp8": 1, "int8": 2, "mxfp4": 3, "int2": 4, "nvfp4": 5}
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
 
@@ -99,6 +101,15 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_debug_gemm_choice.argtypes = [C.c_int32, C.c_int32, C.POINTER(C.c_int32), C.c_int32,
                                                C.POINTER(C.c_int32)]
     lib.polestar_debug_gemm_choice.restype = C.c_int
+    lib.polestar_codec_bytes.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_int64),
+                                         C.POINTER(C.c_int64)]
+    lib.polestar_codec_bytes.restype = C.c_int64
+    lib.polestar_codec_encode.argtypes = [C.c_int32, P, C.c_int32, C.c_int32, P, P, P, P, P]
+    lib.polestar_codec_encode.restype = C.c_int
+    lib.polestar_codec_decode.argtypes = [C.c_int32, P, P, C.c_int32, C.c_int32, P, P, P, P]
+    lib.polestar_codec_decode.restype = C.c_int
+    lib.polestar_debug_stalled_wait.argtypes = [P, C.c_int64]
+    lib.polestar_debug_stalled_wait.restype = C.c_int
     lib.polestar_full_forward.argtypes = [P, P]
     lib.polestar_kv_staleness.argtypes = [P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P]
     lib.polestar_cache_staleness.argtypes = [P, P, P]
@@ -368,3 +379,42 @@ def kv_staleness(kv, kv_ref, n_kv_heads: int, E=None, stream=None):
     _check(lib.polestar_kv_staleness(_ptr(kv), _ptr(kv_ref), rows, int(n_kv_heads), int(dh), dt, _ptr(E),
                                      C.c_void_p(st.cuda_stream)))
     return E
+
+
+def codec_bytes(fmt: str, rows: int, d: int):
+    """(code bytes, scale bytes) of `rows` rows of width d (polestar_codec_bytes)."""
+    lib = load()
+    cb, sb = C.c_int64(), C.c_int64()
+    if lib.polestar_codec_bytes(CODECS[fmt], int(rows), int(d), C.byref(cb), C.byref(sb)) < 0:
+        raise PolestarError(ERR_INVALID_ARG, f"codec {fmt}: unsupported size {rows} x {d}")
+    return int(cb.value), int(sb.value)
+
+
+def codec_encode(fmt: str, h, anchors=None, labels=None, stream=None):
+    """Encode h [rows, d] fp32 (CUDA) in a storage format, as the residual
+    against anchors[labels] when given; returns (codes, scales) uint8 tensors."""
+    import torch
+    lib = load()
+    rows, d = h.shape
+    nc, ns = codec_bytes(fmt, rows, d)
+    codes = torch.empty(max(nc, 16), dtype=torch.uint8, device=h.device)
+    scales = torch.empty(max(ns, 16), dtype=torch.uint8, device=h.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.polestar_codec_encode(CODECS[fmt], _ptr(h), rows, d, _ptr(anchors) if anchors is not None else None,
+                                     _ptr(labels) if labels is not None else None, _ptr(codes), _ptr(scales),
+                                     C.c_void_p(st.cuda_stream)))
+    return codes[:nc], scales[:ns]
+
+
+def codec_decode(fmt: str, codes, scales, rows: int, d: int, anchors=None, labels=None, out=None, stream=None):
+    """Decode (codes, scales) of codec_encode back to fp32 [rows, d] (CUDA)."""
+    import torch
+    lib = load()
+    if out is None:
+        out = torch.empty(rows, d, dtype=torch.float32, device=codes.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.polestar_codec_decode(CODECS[fmt], _ptr(codes), _ptr(scales), rows, d,
+                                     _ptr(anchors) if anchors is not None else None,
+                                     _ptr(labels) if labels is not None else None, _ptr(out),
+                                     C.c_void_p(st.cuda_stream)))
+    return out

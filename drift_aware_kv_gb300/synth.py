@@ -207,27 +207,34 @@ def window_positions(w: Workload, b: int) -> List[int]:
 
 
 class Trajectory:
-    """Seeded synthetic masked-diffusion trajectory (inputs of every step)."""
+    """Seeded synthetic masked-diffusion trajectory (inputs of every step).
 
-    def __init__(self, w: Workload):
+    device "cpu" (the default) draws every value from per-sequence CPU generators:
+    the inputs the CPU oracle and the parity tests share.  Another device draws
+    the same recipe from per-sequence generators of that device (other values,
+    same distributions), which keeps the large workloads' inputs -- a gigabyte
+    of logits per step at batch 32 -- off the host in the throughput benchmark."""
+
+    def __init__(self, w: Workload, device="cpu"):
         self.w = w
+        self.dev = torch.device(device)
         N, d = w.seq_len, w.d_model
         self.gens = []
         for s in range(w.batch):
-            g = torch.Generator(device="cpu")
+            g = torch.Generator(device=self.dev)
             g.manual_seed(derive_seed(w.seed, 0x5E0, s))
             self.gens.append(g)
-        self.mask_emb = _randn((d,), derive_seed(w.seed, 0x3A5), "cpu")
-        self.X = torch.empty(w.batch, N, d, dtype=torch.float32)
-        self.masked = torch.zeros(w.batch, N, dtype=torch.bool)
+        self.mask_emb = _randn((d,), derive_seed(w.seed, 0x3A5), "cpu").to(self.dev)
+        self.X = torch.empty(w.batch, N, d, dtype=torch.float32, device=self.dev)
+        self.masked = torch.zeros(w.batch, N, dtype=torch.bool, device=self.dev)
         self.frac = []
         for s in range(w.batch):
             g = self.gens[s]
-            self.X[s, : w.prompt_len] = torch.randn(w.prompt_len, d, generator=g)
+            self.X[s, : w.prompt_len] = torch.randn(w.prompt_len, d, generator=g, device=self.dev)
             self.X[s, w.prompt_len:] = self.mask_emb
             self.masked[s, w.prompt_len:] = True
             lo, hi = w.extra_frac
-            self.frac.append(lo + (hi - lo) * float(torch.rand((), generator=g)))
+            self.frac.append(lo + (hi - lo) * float(torch.rand((), generator=g, device=self.dev)))
         self.block = 0
         self.block_entry = True
         self.n_unmasked = [0] * w.batch
@@ -235,19 +242,21 @@ class Trajectory:
         self.done = False
 
     def _vocab_row(self, vid: int) -> torch.Tensor:
-        return _randn((self.w.d_model,), derive_seed(self.w.seed, 0xE3B, vid), "cpu")
+        return _randn((self.w.d_model,), derive_seed(self.w.seed, 0xE3B, vid), "cpu").to(self.dev)
 
     def _logits(self, s: int):
         """[2B, V] fp32 logits with row max-prob c ~ U(0.5, 0.99); returns (logits, c)."""
         w, g = self.w, self.gens[s]
         rows = 2 * w.block
-        lg = torch.randn(rows, w.vocab, generator=g, dtype=torch.float32)
-        c = 0.5 + 0.49 * torch.rand(rows, generator=g, dtype=torch.float64)
+        dev = self.dev
+        lg = torch.randn(rows, w.vocab, generator=g, dtype=torch.float32, device=dev)
+        c = 0.5 + 0.49 * torch.rand(rows, generator=g, dtype=torch.float64, device=dev)
         a = lg.argmax(dim=1)
         l64 = lg.double()
-        l64[torch.arange(rows), a] = -math.inf
+        ar = torch.arange(rows, device=dev)
+        l64[ar, a] = -math.inf
         rest = torch.logsumexp(l64, dim=1)
-        lg[torch.arange(rows), a] = (torch.log(c / (1 - c)) + rest).float()
+        lg[ar, a] = (torch.log(c / (1 - c)) + rest).float()
         return lg, c
 
     def next_step(self) -> Optional[dict]:
@@ -276,22 +285,23 @@ class Trajectory:
     def _advance(self):
         w = self.w
         start, end = block_span(w, self.block)
-        win = torch.tensor(window_positions(w, self.block), dtype=torch.long)
+        dev = self.dev
+        win = torch.tensor(window_positions(w, self.block), dtype=torch.long, device=dev)
         lo, hi = w.flips
         for s in range(w.batch):
             g = self.gens[s]
             nw = len(win)
-            self.X[s, win] += 0.05 * torch.randn(nw, w.d_model, generator=g)
-            kick = torch.rand(nw, generator=g) < self.frac[s]
+            self.X[s, win] += 0.05 * torch.randn(nw, w.d_model, generator=g, device=dev)
+            kick = torch.rand(nw, generator=g, device=dev) < self.frac[s]
             if bool(kick.any()):
                 rows = win[kick]
-                self.X[s, rows] += 0.3 * torch.randn(len(rows), w.d_model, generator=g)
+                self.X[s, rows] += 0.3 * torch.randn(len(rows), w.d_model, generator=g, device=dev)
             still = torch.nonzero(self.masked[s, start:end]).flatten() + start
-            m = int(torch.randint(lo, hi + 1, (), generator=g))
+            m = int(torch.randint(lo, hi + 1, (), generator=g, device=dev))
             m = min(m, len(still))
             if m > 0:
-                pick = still[torch.randperm(len(still), generator=g)[:m]]
-                ids = torch.randint(0, w.embed_vocab, (m,), generator=g)
+                pick = still[torch.randperm(len(still), generator=g, device=dev)[:m]]
+                ids = torch.randint(0, w.embed_vocab, (m,), generator=g, device=dev)
                 for p, vid in zip(pick.tolist(), ids.tolist()):
                     self.X[s, p] = self._vocab_row(vid)
                     self.masked[s, p] = False

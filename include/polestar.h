@@ -306,6 +306,21 @@ int32_t polestar_debug_window(int32_t prompt_len, int32_t gen_len, int32_t block
                               int32_t suffix_win, int32_t block_index, int32_t *span, int32_t *pos, int32_t cap);
 polestar_status polestar_debug_trigger(int32_t tau_upd, const int32_t *n_unmasked, int32_t steps, uint8_t *fire);
 
+/* ---- bounded device waits (test hook) ----
+ * Every mbarrier wait of the projection kernels gives up after a bound (about
+ * 2 s), records a code in the context's device error word and lets its kernel
+ * return; the next polestar_calibrate_step / polestar_commit on the context
+ * then fails with POLESTAR_ERR_TIMEOUT (leaving the context as it was, so the
+ * call can be repeated).  This hook exercises that path without a fault: on
+ * the context's main stream it shortens the bound to limit_cycles SM clock
+ * cycles, runs one kernel that waits on an mbarrier nobody ever arrives on (the
+ * wait runs out and records code 99), restores the default bound and queues
+ * the read-back of the error word.  Returns POLESTAR_OK; the timeout is
+ * reported by the next call.  The bound is shared by every stream of the
+ * device while the hook's kernel runs: call it with no other work in flight.
+ * INVALID_ARG for ctx NULL or limit_cycles < 1. */
+polestar_status polestar_debug_stalled_wait(polestar_ctx *ctx, int64_t limit_cycles);
+
 /* ---- attention work items (host only; test hook) ----
  * The split of one sequence's attention rows into work items that the row
  * attention kernels take one per CTA group: rows [a0, a0 + na) followed by
@@ -347,6 +362,53 @@ polestar_status polestar_attention_noalloc(const void *q, const void *kv, int32_
 polestar_status polestar_debug_kmeans(const float *Hw, int32_t P, int32_t nw, int32_t d, int32_t K,
                                       int32_t iters, uint64_t seed, int32_t block, uint8_t *labels, float *z,
                                       float *csum, float *anchor, uint8_t *codes, uint8_t *scales, void *stream);
+
+/* ---- storage formats of the window states (Table 11 ablation) ----
+ * Encoders and decoders of the hidden-state storage formats that the paper's
+ * quantization ablation compares (Table 11; NVFP4 as in App. C.3), on caller
+ * buffers.  `h` / `out`: device [rows, d] fp32, 16-byte aligned; d a multiple of
+ * 32.  With `anchors` (device [K, d] fp32, 16-byte aligned) and `labels`
+ * (device [rows] uint8 cluster ids) a format holds the residual
+ * r = fp32(h - anchors[labels[i]]) and decoding adds the anchor back
+ * (App. C.3 / §4.1); with anchors NULL it holds h itself.  Layouts (row-major):
+ *   FP16   codes uint16 [rows, d] binary16, nearest even; no scales.
+ *   FP8    codes uint8 [rows, d]: bit 7 sign, bits 0-6 the E4M3 magnitude
+ *          (nearest even, saturating at 448) of fp32(r / s); scales fp32 [rows],
+ *          s = fp32(amax / 448).
+ *   INT8   codes int8 [rows, d] = clamp(rint(fp32(r / s)), -127, 127); scales
+ *          fp32 [rows], s = fp32(amax / 127).
+ *   MXFP4  codes uint8 [rows, d/2], two E2M1 codes per byte (element 2i in the
+ *          low nibble; bit 3 sign, bits 0-2 index into {0,.5,1,1.5,2,3,4,6},
+ *          nearest with ties to the even index, saturating at 6) of r / 2^e;
+ *          scales uint8 [rows, d/32] = e + 127 (OCP E8M0) with
+ *          e = clamp(floor(log2 amax) - 2, -127, 127) per block of 32.
+ *   INT2   codes uint8 [rows, d/4], element 4i+j at bits 2j..2j+1 as 2-bit two's
+ *          complement of t in {-1, 0, +1}: t = sign(r) where |r| > s/2, else 0;
+ *          scales fp32 [rows], s = amax.
+ *   NVFP4  codes uint8 [rows, d/2] as MXFP4 but of fp32(r / s) with
+ *          s = E4M3(fp32(amax / 6)) per group of 16 (scales uint8 [rows, d/16]),
+ *          the library's own window-store format.
+ * amax is the largest |r| of the row (FP8, INT8, INT2), block or group; a zero
+ * amax stores zero codes and a zero scale.  Decoded values are
+ * fp32(code value * scale) (+ anchor, fp32).
+ * polestar_codec_bytes: the code and scale bytes of `rows` rows (either output
+ * may be NULL); returns their sum, or -1 for an unknown format, rows < 0 or a d
+ * that is not a positive multiple of 32.  encode / decode: asynchronous on
+ * `stream`; INVALID_ARG for such sizes, a NULL buffer (scales may be NULL for
+ * FP16), labels NULL with anchors given, or a misaligned pointer. */
+typedef enum {
+  POLESTAR_CODEC_FP16 = 0,
+  POLESTAR_CODEC_FP8 = 1,
+  POLESTAR_CODEC_INT8 = 2,
+  POLESTAR_CODEC_MXFP4 = 3,
+  POLESTAR_CODEC_INT2 = 4,
+  POLESTAR_CODEC_NVFP4 = 5
+} polestar_codec;
+int64_t polestar_codec_bytes(int32_t fmt, int32_t rows, int32_t d, int64_t *code_bytes, int64_t *scale_bytes);
+polestar_status polestar_codec_encode(int32_t fmt, const float *h, int32_t rows, int32_t d, const float *anchors,
+                                      const uint8_t *labels, void *codes, void *scales, void *stream);
+polestar_status polestar_codec_decode(int32_t fmt, const void *codes, const void *scales, int32_t rows, int32_t d,
+                                      const float *anchors, const uint8_t *labels, float *out, void *stream);
 
 /* ---- inspection (used by parity tests; synchronises the main stream) ---- */
 typedef enum {

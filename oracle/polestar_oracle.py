@@ -420,8 +420,10 @@ class PolestarOracle:
         (grouped-query: head h reads kv head h // (H / Hkv)). Returns [R, H, N]."""
         c = self.cfg
         grp = c.n_heads // c.n_kv_heads
-        Kx = np.repeat(kv[:, 0], grp, axis=1)  # [N, H, dh]
-        return np.einsum("rhd,nhd->rhn", q, Kx) / math.sqrt(c.head_dim)
+        s = np.empty((len(q), c.n_heads, len(kv)))
+        for h in range(c.n_heads):  # s[r, h, n] = sum_d q[r, h, d] K[n, h // grp, d]
+            s[:, h, :] = q[:, h, :] @ kv[:, 0, h // grp, :].T
+        return s / math.sqrt(c.head_dim)
 
     def attend(self, q, kv):
         """Bidirectional attention over all N positions (Eq. 3). Returns the output
@@ -429,11 +431,13 @@ class PolestarOracle:
         c = self.cfg
         grp = c.n_heads // c.n_kv_heads
         s = self.scores(q, kv)
-        lse = logsumexp(s)
-        p = np.exp(s - lse[..., None])
-        Vx = np.repeat(kv[:, 1], grp, axis=1)
-        o = np.einsum("rhn,nhd->rhd", p, Vx).reshape(len(q), -1)
-        return self._store(o), s, lse
+        lse = np.empty((len(q), c.n_heads))
+        o = np.empty((len(q), c.n_heads, c.head_dim))
+        for h in range(c.n_heads):  # o[r, h, :] = sum_n softmax(s[r, h, :])_n V[n, h // grp, :]
+            lse[:, h] = logsumexp(s[:, h, :])
+            p = np.exp(s[:, h, :] - lse[:, h, None])
+            o[:, h, :] = p @ kv[:, 1, h // grp, :]
+        return self._store(o.reshape(len(q), -1)), s, lse
 
     def post(self, l, h, attn):
         """Output projection + residual, then the SwiGLU FFN + residual."""

@@ -14,9 +14,9 @@ the others follow their usual definitions, with these readings:
   INT8     symmetric integers in [-127, 127] (nearest even) with one fp32 scale per
            row, s = fp32(amax / 127).
   MXFP4    the OCP microscaling format: blocks of 32 elements share a power-of-two
-           scale X = 2^(floor(log2 amax) - 2) (2 = the largest E2M1 exponent);
-           elements E2M1, nearest even, saturating at 6; an all-zero block keeps
-           zero codes.
+           scale X = 2^(floor(log2 amax) - 2) (2 = the largest E2M1 exponent),
+           the exponent held to the E8M0 scale range [-127, 127]; elements E2M1,
+           nearest even, saturating at 6; an all-zero block keeps zero codes.
   INT2     symmetric ternary {-1, 0, +1} (two bits) with one fp32 scale per row,
            s = amax: an element becomes sign(r) * s when |r| > s / 2, else 0
            (nearest; a tie at s / 2 goes to the even value 0).
@@ -94,7 +94,7 @@ def mxfp4_encode(r):
     amax = np.max(np.abs(g), axis=-1)
     with np.errstate(divide="ignore"):
         e = np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2
-    e = np.where(amax > 0, e, 0).astype(np.int64)
+    e = np.clip(np.where(amax > 0, e, 0), -127, 127).astype(np.int64)  # E8M0 scale range
     q = g / np.power(2.0, e)[..., None]  # exact: a power-of-two scale
     codes, _ = e2m1_round(q)
     codes = np.where(amax[..., None] > 0, codes, 0).astype(np.uint8)

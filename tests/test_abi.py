@@ -174,3 +174,10 @@ def test_trigger_closed_form(tau, ns, expect):
     assert list(out) == expect
     neg = (ctypes.c_int32 * 1)(-1)
     assert lib.polestar_debug_trigger(tau, neg, 1, out) == P.ERR_INVALID_ARG
+
+
+def test_stalled_wait_hook_without_context_is_an_argument_error():
+    """Host-side argument check of the bounded-wait test hook (no device work)."""
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    assert lib.polestar_debug_stalled_wait(None, 1000) == P.ERR_INVALID_ARG

@@ -125,3 +125,17 @@ def test_table11_ordering_on_clustered_window_states(seed, d, scale):
     assert err["nvfp4"] < err["nvfp4_plain"] < err["int2"]
     assert math.isclose(size["nvfp4"], 0.5625) and math.isclose(size["mxfp4"], 0.53125)
     assert size["fp16"] == 2.0 and size["fp8"] == size["int8"] == 1.0 + 4.0 / d
+
+
+def test_mxfp4_scale_exponent_stays_in_the_e8m0_range():
+    """OCP MX scales are E8M0 bytes, 2^-127 .. 2^127: a block whose maximum is
+    below 2^-125 keeps the smallest scale 2^-127 (its elements then round to 0
+    or small codes), and the stored exponent never leaves the range."""
+    r = np.zeros((1, 64))
+    r[0, :32] = 2.0 ** -140 * np.arange(1, 33)      # block 0: amax = 2^-135
+    r[0, 32:] = 2.0 ** 100 * np.linspace(-1, 1, 32)  # block 1: amax = 2^100
+    codes, e = R.mxfp4_encode(O.to_f32(r))
+    assert e[0, 0] == -127 and e[0, 1] == 98
+    assert np.all(codes[0, :32] == 0)  # 2^-135..2^-130 over 2^-127 is below 0.25
+    dec = R.mxfp4_decode(codes, e)
+    assert np.all(np.isfinite(dec)) and np.all(dec[0, :32] == 0)
