@@ -1277,6 +1277,11 @@ extern "C" polestar_status polestar_debug_read(polestar_ctx* c, int32_t which, i
     case POLESTAR_BUF_TOPK: base = c->topk_out; per = b * c->cfg.topk * 4; break;
     case POLESTAR_BUF_SELECTED: base = c->selected; per = b * Wmax; break;
     case POLESTAR_BUF_DELTA: base = c->delta; per = b * B * 4; layered = false; break;
+    case POLESTAR_BUF_PROXY_LSE: base = c->pprev_lse; per = b * K * H * 4; break;
+    case POLESTAR_BUF_ACTIVE_PREV: base = c->aprev; per = b * B * H * N * 4; layered = false; break;
+    case POLESTAR_BUF_ACTIVE_LSE: base = c->aprev_lse; per = b * B * H * 4; layered = false; break;
+    case POLESTAR_BUF_THETA: base = c->theta; per = b * B * std::max(1, c->cfg.hist) * 4; layered = false; break;
+    case POLESTAR_BUF_THETA_N: base = c->theta_n; per = b * B * 4; layered = false; break;
     default: return fail(c, POLESTAR_ERR_INVALID_ARG, "unknown buffer id");
   }
   if (layered && (layer < 0 || (size_t)layer >= L)) return fail(c, POLESTAR_ERR_INVALID_ARG, "layer out of range");
@@ -1284,6 +1289,72 @@ extern "C" polestar_status polestar_debug_read(polestar_ctx* c, int32_t which, i
   const char* src = (const char*)base + (layered ? (size_t)layer * per : 0);
   CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
   CUDA_OR_FAIL(c, cudaMemcpy(host_dst, src, bytes, cudaMemcpyDeviceToHost));
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_debug_write(polestar_ctx* c, int32_t which, int32_t layer, const void* host_src,
+                                                size_t bytes) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!host_src) return fail(c, POLESTAR_ERR_INVALID_ARG, "host_src is NULL");
+  const size_t L = c->L, b = c->b, N = c->N, d = c->d, Wmax = c->Wmax, K = c->K, H = c->H, B = c->B;
+  void* base = nullptr;
+  size_t per = 0;
+  bool layered = true;
+  switch (which) {
+    case POLESTAR_BUF_KV: base = c->kv; per = b * N * 2 * c->kvdim * c->esz; break;
+    case POLESTAR_BUF_CENTROID: base = c->z; per = b * K * d * 4; break;
+    case POLESTAR_BUF_CSUM: base = c->csum; per = b * K * d * 4; break;
+    case POLESTAR_BUF_ANCHOR: base = c->anchor; per = b * K * d * 4; break;
+    case POLESTAR_BUF_LABELS: base = c->labels; per = b * Wmax; break;
+    case POLESTAR_BUF_CODES:
+    case POLESTAR_BUF_SCALES: {
+      const bool cd = which == POLESTAR_BUF_CODES;
+      const size_t pl = cd ? code_layer_bytes(c) : scale_layer_bytes(c);
+      if (layer < 0 || (size_t)layer >= L) return fail(c, POLESTAR_ERR_INVALID_ARG, "layer out of range");
+      if (bytes > pl) return fail(c, POLESTAR_ERR_INVALID_ARG, "bytes exceeds the buffer size");
+      CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+      if (c->offload) {  // the host store is authoritative; the device ring refills from it
+        CUDA_OR_FAIL(c, cudaStreamSynchronize(c->ss));
+        std::memcpy((cd ? c->codes_host : c->scales_host) + (size_t)layer * pl, host_src, bytes);
+        return POLESTAR_OK;
+      }
+      CUDA_OR_FAIL(c, cudaMemcpy((cd ? c->codes : c->scales) + (size_t)layer * pl, host_src, bytes,
+                                 cudaMemcpyHostToDevice));
+      return POLESTAR_OK;
+    }
+    case POLESTAR_BUF_PROXY: base = c->pprev; per = b * K * H * N * 4; break;
+    case POLESTAR_BUF_PROXY_LSE: base = c->pprev_lse; per = b * K * H * 4; break;
+    case POLESTAR_BUF_WINDOW_H: base = c->Hw; per = b * Wmax * d * 4; break;
+    case POLESTAR_BUF_ACTIVE_PREV: base = c->aprev; per = b * B * H * N * 4; layered = false; break;
+    case POLESTAR_BUF_ACTIVE_LSE: base = c->aprev_lse; per = b * B * H * 4; layered = false; break;
+    case POLESTAR_BUF_THETA: base = c->theta; per = b * B * std::max(1, c->cfg.hist) * 4; layered = false; break;
+    case POLESTAR_BUF_THETA_N: base = c->theta_n; per = b * B * 4; layered = false; break;
+    default: return fail(c, POLESTAR_ERR_INVALID_ARG, "buffer is not part of the calibration state");
+  }
+  if (layered && (layer < 0 || (size_t)layer >= L)) return fail(c, POLESTAR_ERR_INVALID_ARG, "layer out of range");
+  if (bytes > per) return fail(c, POLESTAR_ERR_INVALID_ARG, "bytes exceeds the buffer size");
+  char* dst = (char*)base + (layered ? (size_t)layer * per : 0);
+  CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  CUDA_OR_FAIL(c, cudaMemcpy(dst, host_src, bytes, cudaMemcpyHostToDevice));
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_debug_enter_block(polestar_ctx* c, int32_t block_index, const int32_t* cum) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (block_index < 0 || block_index >= c->cfg.gen_len / c->B)
+    return fail(c, POLESTAR_ERR_INVALID_ARG, "block_index out of range");
+  for (int s = 0; cum && s < c->b; ++s)
+    if (cum[s] < 0) return fail(c, POLESTAR_ERR_INVALID_ARG, "negative count");
+  CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  compute_window(c, block_index);
+  for (int s = 0; s < c->b; ++s) {
+    c->cum[s] = cum ? cum[s] : 0;
+    c->fire[s] = 0;
+  }
+  c->sel_last = nullptr;
+  c->cur_block = block_index;
+  c->cur_entry = 1;
+  c->stepped = 0;
   return POLESTAR_OK;
 }
 

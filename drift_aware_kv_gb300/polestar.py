@@ -18,7 +18,8 @@ OK, ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_STATE, ERR_TIMEOUT, ERR_UNSUPPORTED 
 FP32, BF16 = 0, 1
 (BUF_KV, BUF_CENTROID, BUF_CSUM, BUF_ANCHOR, BUF_LABELS, BUF_CODES, BUF_SCALES, BUF_ACT_OUT,
  BUF_UPDATE, BUF_CONF, BUF_DREL, BUF_TAUD, BUF_PROXY, BUF_WINDOW_H, BUF_DRIFT, BUF_TOPK,
- BUF_SELECTED, BUF_DELTA) = range(18)
+ BUF_SELECTED, BUF_DELTA, BUF_PROXY_LSE, BUF_ACTIVE_PREV, BUF_ACTIVE_LSE, BUF_THETA,
+ BUF_THETA_N) = range(23)
 
 EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
             "polestar_release", "polestar_last_error", "polestar_launch_count", "polestar_debug_read",
@@ -28,7 +29,8 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_debug_attention_impl", "polestar_debug_gemm_swiglu", "polestar_full_forward",
             "polestar_kv_staleness", "polestar_cache_staleness", "polestar_debug_attention_items",
             "polestar_debug_window", "polestar_debug_trigger", "polestar_debug_stalled_wait",
-            "polestar_codec_bytes", "polestar_codec_encode", "polestar_codec_decode")
+            "polestar_codec_bytes", "polestar_codec_encode", "polestar_codec_decode",
+            "polestar_debug_write", "polestar_debug_enter_block")
 CODECS = {"fp16": 0, "fp8": 1, "int8": 2, "mxfp4": 3, "int2": 4, "nvfp4": 5}
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
@@ -86,6 +88,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_launch_count.argtypes = [P]
     lib.polestar_launch_count.restype = C.c_uint64
     lib.polestar_debug_read.argtypes = [P, C.c_int32, C.c_int32, P, C.c_size_t]
+    lib.polestar_debug_write.argtypes = [P, C.c_int32, C.c_int32, P, C.c_size_t]
+    lib.polestar_debug_enter_block.argtypes = [P, C.c_int32, C.POINTER(C.c_int32)]
     lib.polestar_debug_gemm.argtypes = [P, C.c_int32, P, C.c_int32, P, C.c_int32, C.c_int32, P, C.c_int32,
                                         C.c_int32, C.c_int32, C.c_int32, P]
     lib.polestar_debug_gemm.restype = C.c_int
@@ -116,7 +120,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.polestar_profile_begin.argtypes = [P, C.c_int32]
     lib.polestar_profile_end.argtypes = [P, C.POINTER(polestar_kernel_stats), C.c_int32]
     for f in ("polestar_init", "polestar_calibrate_step", "polestar_commit", "polestar_step_host",
-              "polestar_debug_read", "polestar_profile_begin", "polestar_profile_end",
+              "polestar_debug_read", "polestar_debug_write", "polestar_debug_enter_block",
+              "polestar_profile_begin", "polestar_profile_end",
               "polestar_full_forward", "polestar_kv_staleness", "polestar_cache_staleness"):
         getattr(lib, f).restype = C.c_int
     _lib = lib
@@ -230,6 +235,17 @@ class Polestar:
         _check(self.lib.polestar_debug_read(self.ctx, which, layer, C.c_void_p(out.data_ptr()),
                                             out.numel() * out.element_size()), self.ctx)
         return out
+
+    def write(self, which: int, layer: int, src):
+        """Copy a CPU torch tensor into an internal state buffer (polestar_debug_write)."""
+        src = src.contiguous()
+        _check(self.lib.polestar_debug_write(self.ctx, which, layer, C.c_void_p(src.data_ptr()),
+                                             src.numel() * src.element_size()), self.ctx)
+
+    def enter_block(self, block_index: int, cum=None):
+        """Host bookkeeping as after block_index's entry step (polestar_debug_enter_block)."""
+        arr = (C.c_int32 * self.w.batch)(*(cum or [0] * self.w.batch))
+        _check(self.lib.polestar_debug_enter_block(self.ctx, int(block_index), arr), self.ctx)
 
     def profile_begin(self, capacity: int):
         _check(self.lib.polestar_profile_begin(self.ctx, int(capacity)), self.ctx)

@@ -430,7 +430,15 @@ typedef enum {
   POLESTAR_BUF_DRIFT = 14,    /* layer l: [batch, K] fp32 (same data as step_out.drift) */
   POLESTAR_BUF_TOPK = 15,     /* layer l: [batch, topk] int32                       */
   POLESTAR_BUF_SELECTED = 16, /* layer l: [batch, win_max] uint8                    */
-  POLESTAR_BUF_DELTA = 17     /* [batch, block] fp32 token drift delta_j            */
+  POLESTAR_BUF_DELTA = 17,    /* [batch, block] fp32 token drift delta_j            */
+  POLESTAR_BUF_PROXY_LSE = 18,   /* layer l: [batch, K, H] fp32 log-sum-exp of the last
+                                    proxy scores                                       */
+  POLESTAR_BUF_ACTIVE_PREV = 19, /* [batch, block, H, N] fp32 last-layer scores of the
+                                    active rows at the previous step                   */
+  POLESTAR_BUF_ACTIVE_LSE = 20,  /* [batch, block, H] fp32 their log-sum-exp            */
+  POLESTAR_BUF_THETA = 21,       /* [batch, block, max(hist, 1)] fp32 drift history Theta_j,
+                                    oldest entry first                                 */
+  POLESTAR_BUF_THETA_N = 22      /* [batch, block] int32 entries held in Theta_j        */
 } polestar_buffer;
 
 /* Copy `bytes` bytes of an internal buffer (layer `layer` where the buffer is
@@ -438,6 +446,28 @@ typedef enum {
  * buffer size or the layer is out of range. */
 polestar_status polestar_debug_read(polestar_ctx *ctx, int32_t which, int32_t layer, void *host_dst,
                                     size_t bytes);
+
+/* ---- calibration state import (test hooks; snapshot parity) ----
+ * The state one within-block step of Algorithm 1 reads and writes is: the K/V
+ * cache of every layer, the window's cluster labels, unit centroids z_c,
+ * member sums s_c and anchors A_c, the NVFP4 residual store, the proxy scores
+ * and log-sum-exps of the last refresh (every layer), the last layer's
+ * active-row scores and log-sum-exps, the drift histories Theta_j, and on the
+ * host the active block and each sequence's count of tokens unmasked since the
+ * last refresh.  Exporting it is polestar_debug_read of the buffers
+ * KV, LABELS, CENTROID, CSUM, ANCHOR, CODES, SCALES, PROXY, PROXY_LSE,
+ * ACTIVE_PREV, ACTIVE_LSE, THETA and THETA_N; importing it is
+ * polestar_debug_write of the same buffers (same layouts, host memory,
+ * synchronous; INVALID_ARG for any other buffer id, a layer out of range or
+ * bytes beyond the buffer) followed by polestar_debug_enter_block, which sets
+ * the host side as if block `block_index`'s entry step had just run: its local
+ * window (§4.1), the trigger counts cum[batch] (host, >= 0; NULL = all 0) and
+ * no pending commit, so the next call is a within-block
+ * polestar_calibrate_step of that block.  INVALID_ARG for a block out of
+ * range or a negative count. */
+polestar_status polestar_debug_write(polestar_ctx *ctx, int32_t which, int32_t layer, const void *host_src,
+                                     size_t bytes);
+polestar_status polestar_debug_enter_block(polestar_ctx *ctx, int32_t block_index, const int32_t *cum);
 
 #ifdef __cplusplus
 }

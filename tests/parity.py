@@ -85,12 +85,22 @@ class Report:
     commits: int = 0
     sensitivity_ties: int = 0
     max_band_rel: float = 0.0
+    max_centroid_err: float = 0.0
     notes: list = dataclasses.field(default_factory=list)
 
 
 class Lockstep:
-    def __init__(self, w: synth.Workload, kv_tol: float, act_tol: float, n_perturbed=None):
+    """start_block > 0: the trajectory's inputs are drawn from its start, but the
+    engines join at that block's entry, with every layer's K/V cache first set
+    (on both sides: the oracle's arrays and the library's buffers through
+    polestar_debug_write) to the same seeded N(0, 1) values in the storage
+    dtype.  An odd start block's entry forwards only window + block rows, so the
+    rest of the cache stays the seeded one: the within-block path runs at full
+    width without a full-sequence forward on the CPU."""
+
+    def __init__(self, w: synth.Workload, kv_tol: float, act_tol: float, n_perturbed=None, start_block=0):
         self.w = w
+        self.start_block = start_block
         self.kv_tol, self.act_tol = kv_tol, act_tol
         # block-entry centroids/anchors: fp32 path ~1e-6; bf16 path inherits the
         # bf16 rounding of the A operands of the preceding layers
@@ -115,11 +125,34 @@ class Lockstep:
     def read_layer(self, which, layer, shape, dtype):
         return self.lib.read(which, layer, shape, dtype)
 
+    def _seed_caches(self):
+        """The same seeded K/V cache on both sides (see the class docstring)."""
+        w = self.w
+        dt = synth.torch_dtype(w)
+        g = torch.Generator(device="cpu").manual_seed(synth.derive_seed(w.seed, 0xCAC4E))
+        for l in range(w.n_layers):
+            kv = torch.randn(w.batch, self.N, 2, w.n_kv_heads * w.head_dim, generator=g).to(dt)
+            self.lib.write(P.BUF_KV, l, kv)
+            kvn = kv.double().numpy().reshape(w.batch, self.N, 2, w.n_kv_heads, w.head_dim)
+            for o in [self.orc] + self.pert:
+                for s in range(w.batch):
+                    o.seqs[s].kv[l] = kvn[s].copy()
+
     def run(self, max_steps=None):
         w, rep = self.w, self.rep
         dt = synth.torch_dtype(w)
+        if self.start_block > 0:
+            while True:  # inputs of the earlier blocks are drawn but not run
+                st = self.tr.next_step()
+                if st["block_entry"] and st["block_index"] == self.start_block:
+                    break
+            self._seed_caches()
+            pending = st
+        else:
+            pending = None
         while True:
-            st = self.tr.next_step()
+            st = pending if pending is not None else self.tr.next_step()
+            pending = None
             if st is None or (max_steps is not None and rep.steps >= max_steps):
                 break
             x0 = st["x0"].to(dt)
@@ -256,6 +289,21 @@ class Lockstep:
                 rep.max_act_err = max(rep.max_act_err, e)
                 assert e < self.act_tol, f"active-row output rel err {e}"
             if any(fire):
+                # unit centroids and member sums after this step's incremental update
+                for l in range(L):
+                    zg = self.read_layer(P.BUF_CENTROID, l, (b, K, d), torch.float32).numpy()
+                    sg = self.read_layer(P.BUF_CSUM, l, (b, K, d), torch.float32).numpy()
+                    for s in range(b):
+                        if not fire[s]:
+                            continue
+                        o = self.orc.seqs[s]
+                        for name, got, ref, pert in (("z", zg[s], o.z[l], [q.seqs[s].z[l] for q in self.pert]),
+                                                     ("s", sg[s], o.s[l], [q.seqs[s].s[l] for q in self.pert])):
+                            band = BAND_FACTOR * max([rel_l2(x, ref) for x in pert] or [0.0])
+                            e = rel_l2(got, ref)
+                            rep.max_centroid_err = max(rep.max_centroid_err, e)
+                            assert e < max(self.state_tol, band), \
+                                f"centroid {name} after the update rel err {e} (layer {l}, seq {s}, band {band})"
                 U = self.read_layer(P.BUF_UPDATE, 0, (b, self.Wmax, d), torch.float32).numpy()
                 for s in range(b):
                     if not fire[s]:
