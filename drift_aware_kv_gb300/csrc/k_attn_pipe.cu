@@ -98,11 +98,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
   }
   return true;
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// One K/V tile of a head in a single copy: the 4D view {64 columns, row,
+// 64-column block within the K (or V) half, K/V} of the cache (see kv_map4)
+// lands as [K/V][block][row][64] swizzled boxes.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void ldsm_x4a(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, uint32_t a) {
@@ -229,11 +233,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
         mbar_expect_tx(fb, TB);
         const uint32_t dst = su32(sm + s * TB);
         const int y = seq * p.N + (tbeg + i) * TK;
-#pragma unroll
-        for (int b = 0; b < DH / 64; ++b) {
-          tma_load_2d(dst + b * TK * 128, &tm_kv, kvh * DH + b * 64, y, fb);
-          tma_load_2d(dst + TB / 2 + b * TK * 128, &tm_kv, p.kvdim + kvh * DH + b * 64, y, fb);
-        }
+        tma_load_4d(dst, &tm_kv, 0, y, kvh * (DH / 64), 0, fb);  // K then V, DH/64 boxes each
       }
     }
   } else if (warp < nwl) {
@@ -544,15 +544,17 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
     }
   }
 }
-
-// 2D tensor map of one layer's K/V cache viewed as [batch*N rows][2*kvdim] bf16
-// with 64 x 64 boxes and 128-byte swizzle (cached per buffer and shape).
-const CUtensorMap* kv_map(const void* base, int rows, int cols) {
-  static std::map<std::tuple<const void*, int, int>, CUtensorMap> cache;
+// 4D tensor map of one layer's K/V cache ([batch*N rows][2 * kvdim] bf16, K
+// then V of each row) viewed as {64 columns, row, 64-column block of the K or
+// V half, K/V}: a box {64, TK, dh / 64, 2} at (0, row, head * dh / 64, 0) is one
+// head's K and V for TK keys, as 128-byte-swizzled [TK][64] boxes in the order
+// K block 0, K block 1, .., V block 0, ..  (cached per buffer and shape).
+const CUtensorMap* kv_map(const void* base, int rows, int kvdim, int dh) {
+  static std::map<std::tuple<const void*, int, int, int>, CUtensorMap> cache;
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   std::lock_guard<std::mutex> lk(mu);
-  const auto key = std::make_tuple(base, rows, cols);
+  const auto key = std::make_tuple(base, rows, kvdim, dh);
   auto it = cache.find(key);
   if (it != cache.end()) return &it->second;
   if (!fn) {
@@ -565,11 +567,11 @@ const CUtensorMap* kv_map(const void* base, int rows, int cols) {
   }
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)TK};
-  const cuuint32_t estr[2] = {1, 1};
-  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(kvdim / 64), 2};
+  const cuuint64_t strides[3] = {(cuuint64_t)kvdim * 4, 128, (cuuint64_t)kvdim * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)TK, (cuuint32_t)(dh / 64), 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return nullptr;
@@ -578,7 +580,8 @@ const CUtensorMap* kv_map(const void* base, int rows, int cols) {
 
 template <int DH>
 cudaError_t launch(const AttnArgs& a, int batch, cudaStream_t st) {
-  const CUtensorMap* map = kv_map(a.kv_layer, batch * a.N, 2 * a.kvdim);
+  if (a.kvdim % 64) return cudaErrorInvalidValue;
+  const CUtensorMap* map = kv_map(a.kv_layer, batch * a.N, a.kvdim, DH);
   if (!map) return cudaErrorInvalidValue;
   const bool split = a.splits > 1;
   const int smem = smem_bytes<DH>(a.stages, split);

@@ -8,21 +8,26 @@
 // organised flash-attention style with every matrix product on tcgen05:
 //
 //   * CTA = one work item (<= 128 rows, given as at most two row ranges of one
-//     sequence) x one query head.  The item's Q rows are the MMA's M side
-//     (TMEM lane = row); keys come in tiles of 64.
+//     sequence) x one query head; the item's Q rows are the MMA's M side
+//     (TMEM lane = row); keys come in tiles of 64.  Two CTAs share an SM (256
+//     TMEM columns and under half the shared memory each), so one SM runs
+//     eight softmax warps.
 //   * warp 0 streams K and V tiles with TMA (128-byte swizzled 64 x 64 boxes
-//     of the [batch*N, 2*kvdim] cache view) into a five-stage mbarrier ring;
+//     of the [batch*N, 2*kvdim] cache view) into a two-stage mbarrier ring;
 //     warp 1 issues S_j = Q K_j^T into one of two TMEM score buffers and
-//     O += P_{j-1} V_{j-1} into the TMEM output, so the tensor cores compute
-//     tile j's scores while the softmax warps work on tile j-1;
+//     O += P_{j-1} V_{j-1} into the TMEM output, taking P straight from TMEM
+//     (the A operand), so the tensor cores compute tile j's scores while the
+//     softmax warps work on tile j-1;
 //   * warps 2-5 (one thread per row) read a row's 64 scores from TMEM, keep
-//     the running maximum (log2 units) and sum, write P (bf16) into one of two
-//     shared-memory buffers as the next product's A operand, and do the KL
-//     terms of tracked rows; the running maximum is raised lazily (only when a
-//     tile's maximum exceeds it by more than 8, i.e. p <= 2^8), and then the
-//     TMEM output row is rescaled before the next P V product;
+//     the running maximum (log2 units) and sum, and write P (bf16 pairs) back
+//     over the first half of the same score buffer; the running maximum is
+//     raised lazily (only when a tile's maximum exceeds it by more than 8, i.e.
+//     p <= 2^8), and then the TMEM output row is rescaled before the next P V;
+//   * tracked rows (drift terms) take their previous scores of tile j + 1 into
+//     shared memory with cp.async while tile j is processed (two buffers of up
+//     to 24 rows per item; further tracked rows read global memory directly);
 //   * V is the second product's B operand read N-major (dh contiguous) from
-//     the same swizzled boxes, so no transposition is needed.
+//     the swizzled boxes, so no transposition is needed.
 // Every mbarrier wait is bounded; a timeout records an error code and the
 // CTA's roles fall through to the final barrier.
 #include <cuda.h>
@@ -42,17 +47,21 @@ constexpr int ROWS = 128;   // rows per work item (MMA M)
 constexpr int TK = 64;      // keys per tile (MMA N of S, K of P V)
 constexpr int DH = 128;     // head dim
 constexpr int THREADS = 192;
-constexpr int STAGES = 5;
-constexpr int QBOX = 64 * ROWS * 2;           // 64 columns x 128 rows (Q, P)
+constexpr int STAGES = 2;
+constexpr int QBOX = 64 * ROWS * 2;           // 64 columns x 128 rows (Q)
 constexpr int KBOX = 64 * TK * 2;             // 64 columns x 64 keys (K, V)
 constexpr int Q_OFF = 0;                      // 2 boxes (dh 0-63, 64-127)
-constexpr int P_OFF = 2 * QBOX;               // 2 buffers x 1 box (64 keys)
-constexpr int RING_OFF = 4 * QBOX;            // STAGES x (K: 2 boxes, V: 2 boxes)
+constexpr int RING_OFF = 2 * QBOX;            // STAGES x (K: 2 boxes, V: 2 boxes)
 constexpr int STAGE_BYTES = 4 * KBOX;
-constexpr int O_COL = 2 * TK;                 // TMEM: S buffers at 0 and TK, O after
-constexpr int CTL_OFF = RING_OFF + STAGES * STAGE_BYTES;
+constexpr int SLOTS = 24;                     // tracked rows whose previous scores are staged
+constexpr int SLOT_BYTES = TK * 4;
+constexpr int PREV_OFF = RING_OFF + STAGES * STAGE_BYTES;  // [2 buffers][SLOTS][TK] fp32
+constexpr int O_COL = 2 * TK;                 // TMEM: S/P buffers at 0 and TK, O after
+constexpr int TMEM_COLS = O_COL + DH;         // 256
+constexpr int CTL_OFF = PREV_OFF + 2 * SLOTS * SLOT_BYTES;
 constexpr int SMEM_BYTES = CTL_OFF + 256 + 1024;  // + control block + alignment
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s
+static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -86,11 +95,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
   }
   return true;
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// One K/V tile of a head in a single copy: the 4D view {64 columns, row,
+// 64-column block within the K (or V) half, K/V} of the cache (see kv_map4)
+// lands as [K/V][block][row][64] swizzled boxes.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
 }
 // UMMA shared-memory descriptor, 128-byte swizzle: K-major (lbo unused) or
@@ -121,6 +134,19 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
+// D (TMEM) += A (TMEM, M = 128 lanes x K = 16 bf16 in 8 columns) * B (shared memory)
+__device__ __forceinline__ void umma_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -152,6 +178,14 @@ __device__ __forceinline__ void tmem_st32_nw(uint32_t taddr, const uint32_t* r) 
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
       "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
       "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16_nw(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
@@ -190,7 +224,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 __device__ __forceinline__ int item_row(const int4& wk, int lr) { return lr < wk.y ? wk.x + lr : wk.z + (lr - wk.y); }
 
-__global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, AttnArgs p) {
+__global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, AttnArgs p) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   uint64_t* kv_full = (uint64_t*)(sm + CTL_OFF);
@@ -201,6 +235,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   uint64_t* q_full = pv_done + 2;
   uint32_t* tmem_slot = (uint32_t*)(q_full + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  int* slot_count = (int*)(tmem_slot + 2);  // [4] tracked rows per lane quarter
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
@@ -223,7 +258,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(tmem_slot)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -239,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   const int seq = p.rows[wk.x].x;
 
   if (warp == 0) {
-    // ---------------- loader: K then V boxes of each 128-key tile
+    // ---------------- loader: K then V boxes of each 64-key tile
     if (lane == 0) {
       for (int j = 0; j < ntl; ++j) {
         const int s = j % STAGES;
@@ -248,10 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
         mbar_expect_tx(fb, STAGE_BYTES);
         const uint32_t dst = su32(sm + RING_OFF + s * STAGE_BYTES);
         const int y = seq * p.N + j * TK;
-        tma_load_2d(dst, &tm_kv, kvh * DH, y, fb);
-        tma_load_2d(dst + KBOX, &tm_kv, kvh * DH + 64, y, fb);
-        tma_load_2d(dst + 2 * KBOX, &tm_kv, p.kvdim + kvh * DH, y, fb);
-        tma_load_2d(dst + 3 * KBOX, &tm_kv, p.kvdim + kvh * DH + 64, y, fb);
+        tma_load_4d(dst, &tm_kv, 0, y, kvh * (DH / 64), 0, fb);  // K0, K1, V0, V1 boxes
       }
     }
   } else if (warp == 1) {
@@ -263,11 +296,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
         if (!mbar_wait(su32(&p_full[t & 1]), (t >> 1) & 1, p.err, 23, abort_flag)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t v = su32(sm + RING_OFF + (t % STAGES) * STAGE_BYTES + 2 * KBOX);
-        const uint32_t pb = su32(sm + P_OFF + (t & 1) * QBOX);
+        const uint32_t pt = tmem + (t & 1) * TK;  // P_t: bf16 pairs in the first TK/2 columns of S_t's buffer
 #pragma unroll
         for (int kk = 0; kk < TK / 16; ++kk)
-          umma(tmem + O_COL, sdesc(pb + kk * 32, 16, 1024), sdesc(v + kk * 16 * 128, KBOX, 1024), idesc(DH, true),
-               (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ta(tmem + O_COL, pt + kk * 8, sdesc(v + kk * 16 * 128, KBOX, 1024), idesc(DH, true),
+                  (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(su32(&pv_done[t & 1]));
         umma_commit(su32(&kv_empty[t % STAGES]));
         return true;
@@ -275,7 +308,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       for (int j = 0; j < ntl && live; ++j) {
         const int s = j % STAGES, b = j & 1;
         if (!mbar_wait(su32(&kv_full[s]), (j / STAGES) & 1, p.err, 24, abort_flag)) break;
-        // score buffer b is free once the softmax has finished tile j - 2
+        // score buffer b holds P_{j-2} until P_{j-2} V_{j-2} has read it; that
+        // product was issued before this one and the products run in order,
+        // and the softmax has read S_{j-2} once it signalled P_{j-2}
         if (j >= 2 && !mbar_wait(su32(&p_full[b]), ((j - 2) >> 1) & 1, p.err, 25, abort_flag)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t kt = su32(sm + RING_OFF + s * STAGE_BYTES);
@@ -312,6 +347,27 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
     }
     const float shift = (prev && p.measure) ? *prev_lse * 1.4426950408889634f : 0.f;
     const bool vec_prev = (p.N & 3) == 0 && ((((uintptr_t)p.active_prev) | ((uintptr_t)p.proxy_prev)) & 15) == 0;
+    // staging slot of this row's previous scores: rank among the item's rows
+    // that measure drift (lane quarters in order), -1 beyond SLOTS or unstaged
+    const bool meas = prev && p.measure;
+    const unsigned bal = __ballot_sync(0xffffffffu, meas);
+    if (lane == 0) slot_count[qd] = __popc(bal);
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    int base = 0;
+    for (int k = 0; k < qd; ++k) base += slot_count[k];
+    const int rank = base + __popc(bal & ((1u << lane) - 1u));
+    const int slot = (meas && vec_prev && rank < SLOTS) ? rank : -1;
+    // tile t's previous scores of this row into staging buffer t & 1
+    auto stage_prev = [&](int t) {
+      if (slot < 0 || t >= ntl) return;
+      const int j0 = t * TK;
+      const uint32_t dst = su32(sm + PREV_OFF + ((t & 1) * SLOTS + slot) * SLOT_BYTES);
+#pragma unroll
+      for (int c = 0; c < TK / 4; ++c)
+        if (j0 + c * 4 < p.N) cp_async16(dst + c * 16, prev + j0 + c * 4);
+    };
+    stage_prev(0);
+    cp_async_commit();
 
     // 16-byte row accesses when the strides and bases allow them
     const bool vec_io = ((p.ldq | p.ldo) & 7) == 0 && ((((uintptr_t)p.q) | ((uintptr_t)p.out)) & 15) == 0;
@@ -344,6 +400,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
     bool ok = true;
     for (int j = 0; j < ntl && ok; ++j) {
       const int b = j & 1, j0 = j * TK;
+      // the next tile's previous scores start coming in now
+      stage_prev(j + 1);
+      cp_async_commit();
       ok = mbar_wait(su32(&s_full[b]), (j >> 1) & 1, p.err, 26, abort_flag);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (!ok) break;
@@ -363,96 +422,91 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       const float corr = raise ? ex2f(mrun - mnew) : 1.f;  // exp2(-inf) = 0 on the first tile
       l *= corr;
       asum *= corr;
-      // P buffer b is free once P_{j-2} V_{j-2} is done; a raised maximum
-      // rescales the output, which must then hold P_{j-1} V_{j-1}
-      // (the products complete in order)
+      // a raised maximum rescales the output, which must then hold P_{j-1} V_{j-1}
       const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
-      if (rescale || j >= 2) {
-        const int t = rescale ? j - 1 : j - 2;
+      if (rescale) {
+        const int t = j - 1;
         ok = mbar_wait(su32(&pv_done[t & 1]), (t >> 1) & 1, p.err, 27, abort_flag);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (!ok) break;
-        if (rescale) {
-          // output row rescale, two halves of 64 columns (loads and stores batched)
+        // output row rescale, four chunks of 32 columns
 #pragma unroll 1
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[64];
-            tmem_ld32_nw(tl + O_COL + hf * 64, v);
-            tmem_ld32_nw(tl + O_COL + hf * 64 + 32, v + 32);
-            tcgen05_wait_ld();
+        for (int c = 0; c < DH / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32_nw(tl + O_COL + c * 32, v);
+          tcgen05_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-            tmem_st32_nw(tl + O_COL + hf * 64, v);
-            tmem_st32_nw(tl + O_COL + hf * 64 + 32, v + 32);
-          }
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+          tmem_st32_nw(tl + O_COL + c * 32, v);
         }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       mrun = mnew;
-      // pass 2: probabilities into P, KL terms of tracked rows
+      // this tile's staged previous scores have landed (the next tile's may not)
+      if (slot >= 0) asm volatile("cp.async.wait_group 1;" ::: "memory");
+      const float* sp_tile = (const float*)(sm + PREV_OFF + (b * SLOTS + (slot >= 0 ? slot : 0)) * SLOT_BYTES);
+      // pass 2: probabilities as bf16 pairs (P, written over the score buffer),
+      // and the drift terms / new stored scores of tracked rows
 #pragma unroll
-      for (int c = 0; c < TK / 32; ++c) {
-        const uint32_t* v = sv + c * 32;
-        float pv[32];
+      for (int hk = 0; hk < 2; ++hk) {  // two halves of 32 keys, 16 packed columns each
+      uint32_t pk[TK / 4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool in = j0 + c * 32 + i < p.N;
-          pv[i] = in ? ex2f(__uint_as_float(v[i]) * sl2 - mrun) : 0.f;
-          l += pv[i];
+      for (int gg = 0; gg < TK / 8; ++gg) {
+        const int g = hk * (TK / 8) + gg;
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = g * 4 + e;
+          pv[e] = j0 + i < p.N ? ex2f(__uint_as_float(sv[i]) * sl2 - mrun) : 0.f;
+          l += pv[e];
         }
+        pk[2 * gg] = pack2(pv[0], pv[1]);
+        pk[2 * gg + 1] = pack2(pv[2], pv[3]);
         if (prev) {
-          const int jc = j0 + c * 32;
+          const int jj = j0 + g * 4;
+          float sp[4] = {0.f, 0.f, 0.f, 0.f};
+          if (p.measure) {
+            if (slot >= 0) {
+              const float4 t = *(const float4*)(sp_tile + g * 4);
+              sp[0] = t.x; sp[1] = t.y; sp[2] = t.z; sp[3] = t.w;
+            } else {
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const int jj = jc + g * 4;
-            float sp[4] = {0.f, 0.f, 0.f, 0.f};
-            if (p.measure) {
-              if (vec_prev && jj + 3 < p.N) {
-                const float4 t = __ldcg((const float4*)(prev + jj));
-                sp[0] = t.x; sp[1] = t.y; sp[2] = t.z; sp[3] = t.w;
-              } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sp[e] = jj + e < p.N ? __ldcg(prev + jj + e) : 0.f;
-              }
+              for (int e = 0; e < 4; ++e) sp[e] = jj + e < p.N ? __ldcg(prev + jj + e) : 0.f;
             }
-            float sn[4];
+          }
+          float sn[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = g * 4 + e;
-              sn[e] = __uint_as_float(v[i]) * p.scale;  // natural-log units
-              if (p.measure && jj + e < p.N) {
-                const float d = sn[e] - sp[e];
-                const float qt = ex2f(fmaf(sp[e], 1.4426950408889634f, -shift));
-                asum = fmaf(pv[i], d, asum);
-                sqs += qt;
-                esum = fmaf(qt, expm1_drift(d), esum);
-              }
+          for (int e = 0; e < 4; ++e) {
+            sn[e] = __uint_as_float(sv[g * 4 + e]) * p.scale;  // natural-log units
+            if (p.measure && jj + e < p.N) {
+              const float d = sn[e] - sp[e];
+              const float qt = ex2f(fmaf(sp[e], 1.4426950408889634f, -shift));
+              asum = fmaf(pv[e], d, asum);
+              sqs += qt;
+              esum = fmaf(qt, expm1_drift(d), esum);
             }
-            if (p.store) {
-              if (vec_prev && jj + 3 < p.N) {
-                *(float4*)(prev + jj) = make_float4(sn[0], sn[1], sn[2], sn[3]);
-              } else {
+          }
+          if (p.store) {
+            if (vec_prev && jj + 3 < p.N) {
+              *(float4*)(prev + jj) = make_float4(sn[0], sn[1], sn[2], sn[3]);
+            } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  if (jj + e < p.N) prev[jj + e] = sn[e];
-              }
+              for (int e = 0; e < 4; ++e)
+                if (jj + e < p.N) prev[jj + e] = sn[e];
             }
           }
         }
-        // P row, keys c*32 .. c*32+31: four 16-byte chunks
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int key = c * 32 + g * 8;
-          const uint4 w = make_uint4(pack2(pv[g * 8 + 0], pv[g * 8 + 1]), pack2(pv[g * 8 + 2], pv[g * 8 + 3]),
-                                     pack2(pv[g * 8 + 4], pv[g * 8 + 5]), pack2(pv[g * 8 + 6], pv[g * 8 + 7]));
-          *(uint4*)(sm + P_OFF + b * QBOX + swz(r, key >> 3)) = w;
-        }
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // keys 32 hk .. 32 hk + 31 as bf16 pairs: columns 16 hk .. 16 hk + 15 of the
+      // score buffer, whose scores are all in registers by now
+      tmem_st16_nw(tl + b * TK + hk * 16, pk);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(su32(&p_full[b]));
     }
+    cp_async_wait_all();
     // ---------------- epilogue: O / l, KL, log-sum-exp
     if (ok && ntl > 0) {
       ok = mbar_wait(su32(&pv_done[(ntl - 1) & 1]), ((ntl - 1) >> 1) & 1, p.err, 28, abort_flag);
@@ -461,29 +515,29 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
     if (ok) {
       const float inv = 1.f / l;
       __nv_bfloat16* o = (__nv_bfloat16*)p.out + (size_t)row * p.ldo + h * DH;
-      uint32_t ov[DH];
-#pragma unroll
-      for (int c = 0; c < DH / 32; ++c) tmem_ld32_nw(tl + O_COL + c * 32, ov + c * 32);
-      tcgen05_wait_ld();
-#pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        const uint32_t* v = ov + c * 32;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t ov[64];
+        tmem_ld32_nw(tl + O_COL + hf * 64, ov);
+        tmem_ld32_nw(tl + O_COL + hf * 64 + 32, ov + 32);
+        tcgen05_wait_ld();
         if (outp) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint4 w = make_uint4(
-                pack2(__uint_as_float(v[g * 8 + 0]) * inv, __uint_as_float(v[g * 8 + 1]) * inv),
-                pack2(__uint_as_float(v[g * 8 + 2]) * inv, __uint_as_float(v[g * 8 + 3]) * inv),
-                pack2(__uint_as_float(v[g * 8 + 4]) * inv, __uint_as_float(v[g * 8 + 5]) * inv),
-                pack2(__uint_as_float(v[g * 8 + 6]) * inv, __uint_as_float(v[g * 8 + 7]) * inv));
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t* v = ov + g * 8;
+            const uint4 w = make_uint4(pack2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                                       pack2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                                       pack2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                                       pack2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+            const int col = hf * 64 + g * 8;
             if (vec_io) {
-              *(uint4*)(o + c * 32 + g * 8) = w;
+              *(uint4*)(o + col) = w;
             } else {
               const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                ((uint16_t*)o)[c * 32 + g * 8 + 2 * k] = (uint16_t)(ww[k] & 0xFFFF);
-                ((uint16_t*)o)[c * 32 + g * 8 + 2 * k + 1] = (uint16_t)(ww[k] >> 16);
+                ((uint16_t*)o)[col + 2 * k] = (uint16_t)(ww[k] & 0xFFFF);
+                ((uint16_t*)o)[col + 2 * k + 1] = (uint16_t)(ww[k] >> 16);
               }
             }
           }
@@ -505,18 +559,20 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   __syncthreads();
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
   }
 }
-
-// 2D tensor map of one layer's K/V cache viewed as [batch*N rows][2*kvdim] bf16
-// with 64-column x TK-row boxes and 128-byte swizzle (cached per buffer/shape).
-const CUtensorMap* kv_map_tiles(const void* base, int rows, int cols) {
-  static std::map<std::tuple<const void*, int, int>, CUtensorMap> cache;
+// 4D tensor map of one layer's K/V cache ([batch*N rows][2 * kvdim] bf16, K
+// then V of each row) viewed as {64 columns, row, 64-column block of the K or
+// V half, K/V}: a box {64, TK, dh / 64, 2} at (0, row, head * dh / 64, 0) is one
+// head's K and V for TK keys, as 128-byte-swizzled [TK][64] boxes in the order
+// K block 0, K block 1, .., V block 0, ..  (cached per buffer and shape).
+const CUtensorMap* kv_map_tiles(const void* base, int rows, int kvdim, int dh) {
+  static std::map<std::tuple<const void*, int, int, int>, CUtensorMap> cache;
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   std::lock_guard<std::mutex> lk(mu);
-  const auto key = std::make_tuple(base, rows, cols);
+  const auto key = std::make_tuple(base, rows, kvdim, dh);
   auto it = cache.find(key);
   if (it != cache.end()) return &it->second;
   if (!fn) {
@@ -529,11 +585,11 @@ const CUtensorMap* kv_map_tiles(const void* base, int rows, int cols) {
   }
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)TK};
-  const cuuint32_t estr[2] = {1, 1};
-  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(kvdim / 64), 2};
+  const cuuint64_t strides[3] = {(cuuint64_t)kvdim * 4, 128, (cuuint64_t)kvdim * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)TK, (cuuint32_t)(dh / 64), 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return nullptr;
@@ -543,8 +599,8 @@ const CUtensorMap* kv_map_tiles(const void* base, int rows, int cols) {
 }  // namespace at
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int batch, cudaStream_t st) {
-  if (a.dh != at::DH || (a.kvdim & 7)) return cudaErrorInvalidValue;
-  const CUtensorMap* map = at::kv_map_tiles(a.kv_layer, batch * a.N, 2 * a.kvdim);
+  if (a.dh != at::DH || (a.kvdim % 64)) return cudaErrorInvalidValue;
+  const CUtensorMap* map = at::kv_map_tiles(a.kv_layer, batch * a.N, a.kvdim, at::DH);
   if (!map) return cudaErrorInvalidValue;
   static PerDeviceOnce attr;
   {

@@ -4,11 +4,13 @@ oracle on the same seeded trajectory and compares every step.
 Exactness bar: cluster ids, top-k sets, selected rows, NVFP4 codes/scales and
 commit masks are compared exactly; a mismatch is accepted only when the
 oracle's decision margin is below NEAR_TIE (a near tie), and is then counted.
-After a near-tie divergence the two states legitimately differ.  Both engines
-keep running on the same inputs, and comparison resumes at the next block
-entry with an even block index: that entry recomputes every position's K/V,
-the window cache, centroids, proxy baselines and histories from x0 alone, so
-the states coincide again without taking anything from the GPU side.
+After a near-tie divergence the two states legitimately differ.  The library
+then takes over the oracle's state through the state import (labels,
+centroids, NVFP4 store, K/V caches, score and drift histories, trigger counts:
+oracle -> GPU only, nothing flows back) and lockstep comparison goes on from the
+next step (resync=False: both engines keep running and comparison resumes at
+the next block entry with an even block index, which recomputes every state
+from x0 alone).
 Floating-point outputs use the tolerances below (K/V, hidden states and update
 packets by relative L2 error).
 
@@ -86,6 +88,7 @@ class Report:
     sensitivity_ties: int = 0
     max_band_rel: float = 0.0
     max_centroid_err: float = 0.0
+    resyncs: int = 0
     notes: list = dataclasses.field(default_factory=list)
 
 
@@ -98,13 +101,19 @@ class Lockstep:
     rest of the cache stays the seeded one: the within-block path runs at full
     width without a full-sequence forward on the CPU."""
 
-    def __init__(self, w: synth.Workload, kv_tol: float, act_tol: float, n_perturbed=None, start_block=0):
+    def __init__(self, w: synth.Workload, kv_tol: float, act_tol: float, n_perturbed=None, start_block=0,
+                 resync=True):
         self.w = w
         self.start_block = start_block
+        self.resync = resync
         self.kv_tol, self.act_tol = kv_tol, act_tol
         # block-entry centroids/anchors: fp32 path ~1e-6; bf16 path inherits the
         # bf16 rounding of the A operands of the preceding layers
         self.state_tol = 1e-5 if w.dtype == "fp32" else 1e-3
+        # member sums after incremental updates accumulate every refresh of the
+        # block in fp32 (up to Wmax unit rows per update, a few updates): about
+        # 1000 roundings of 2^-24 -> 1e-4 relative
+        self.update_tol = 1e-4 if w.dtype == "fp32" else 1e-3
         W_cpu = synth.make_weights(w, "cpu")
         Wn = O.weights_to_numpy(W_cpu)
         self.orc = O.PolestarOracle(w, Wn)
@@ -186,8 +195,56 @@ class Lockstep:
             if not ok:
                 if rep.diverged_at < 0:
                     rep.diverged_at = st["t"]
-                self.diverged = True
+                if self.resync:
+                    # the library takes over the oracle's state (labels, centroids,
+                    # store, caches, histories: oracle -> GPU only) and lockstep
+                    # comparison goes on from the next step
+                    self._import_oracle_state(st)
+                    rep.resyncs += 1
+                else:
+                    self.diverged = True
         return rep
+
+    def _import_oracle_state(self, st):
+        """The oracle's calibration state after this step, written into the
+        library's context through the state import (polestar_debug_write +
+        polestar_debug_enter_block)."""
+        w, o = self.w, self.orc
+        b, L, N, K, H, B, d, Wm = w.batch, w.n_layers, self.N, w.K, w.n_heads, w.block, w.d_model, self.Wmax
+        dt = synth.torch_dtype(w)
+        nw = len(o.window(st["block_index"]))
+        f32 = lambda a: torch.tensor(np.asarray(a, dtype=np.float64), dtype=torch.float64).to(torch.float32)
+        for l in range(L):
+            self.lib.write(P.BUF_KV, l, torch.tensor(
+                np.stack([o.seqs[s].kv[l].reshape(N, 2, -1) for s in range(b)])).to(dt))
+            lab = np.zeros((b, Wm), dtype=np.uint8)
+            codes = np.zeros((b, Wm, d // 2), dtype=np.uint8)
+            scales = np.zeros((b, Wm, d // 16), dtype=np.uint8)
+            for s in range(b):
+                q = o.seqs[s]
+                lab[s, :nw] = q.labels[l]
+                codes[s, :nw] = q.codes[l][:, 0::2] | (q.codes[l][:, 1::2] << 4)
+                scales[s, :nw] = q.sbytes[l]
+            self.lib.write(P.BUF_LABELS, l, torch.tensor(lab))
+            self.lib.write(P.BUF_CODES, l, torch.tensor(codes))
+            self.lib.write(P.BUF_SCALES, l, torch.tensor(scales))
+            for which, attr in ((P.BUF_CENTROID, "z"), (P.BUF_CSUM, "s"), (P.BUF_ANCHOR, "A")):
+                self.lib.write(which, l, f32(np.stack([getattr(o.seqs[s], attr)[l] for s in range(b)])))
+            self.lib.write(P.BUF_PROXY, l, f32(np.stack([o.seqs[s].P_prev[l][0] for s in range(b)])))
+            self.lib.write(P.BUF_PROXY_LSE, l, f32(np.stack([o.seqs[s].P_prev[l][1] for s in range(b)])))
+        self.lib.write(P.BUF_ACTIVE_PREV, 0, f32(np.stack([o.seqs[s].A_prev[0] for s in range(b)])))
+        self.lib.write(P.BUF_ACTIVE_LSE, 0, f32(np.stack([o.seqs[s].A_prev[1] for s in range(b)])))
+        hist = max(1, w.hist)
+        th = np.zeros((b, B, hist))
+        thn = np.zeros((b, B), dtype=np.int32)
+        for s in range(b):
+            for j in range(B):
+                t = o.seqs[s].theta[j][-hist:] if w.hist > 0 else []
+                th[s, j, :len(t)] = t
+                thn[s, j] = len(t)
+        self.lib.write(P.BUF_THETA, 0, f32(th))
+        self.lib.write(P.BUF_THETA_N, 0, torch.tensor(thn))
+        self.lib.enter_block(st["block_index"], [o.seqs[s].cum for s in range(b)])
 
     # ---- the oracle's own sensitivity (perturbed copies) --------------------------
     def _live(self):
@@ -237,9 +294,14 @@ class Lockstep:
                 for s in range(b):
                     o = self.orc.seqs[s]
                     ea, ez = rel_l2(anchor[s], o.A[l]), rel_l2(z[s], o.z[l])
-                    assert ea < self.state_tol, f"anchors rel err {ea} (layer {l}, seq {s})"
-                    assert ez < self.state_tol, f"centroids rel err {ez} (layer {l}, seq {s})"
-                    self._check_codes(codes[s, :nw], scales[s, :nw], o, l)
+                    # the oracle's own spread of these states under fp32-level
+                    # rounding noise (perturbed copies), times BAND_FACTOR
+                    band_a = BAND_FACTOR * max([rel_l2(q.seqs[s].A[l], o.A[l]) for q in self.pert] or [0.0])
+                    band_z = BAND_FACTOR * max([rel_l2(q.seqs[s].z[l], o.z[l]) for q in self.pert] or [0.0])
+                    rep.max_centroid_err = max(rep.max_centroid_err, ea, ez)
+                    assert ea < max(self.state_tol, band_a), f"anchors rel err {ea} (layer {l}, seq {s}, band {band_a})"
+                    assert ez < max(self.state_tol, band_z), f"centroids rel err {ez} (layer {l}, seq {s}, band {band_z})"
+                    self._check_codes(codes[s, :nw], scales[s, :nw], o, l, s=s, nw=nw)
         else:
             fire = [bool(out.fire[s]) for s in range(b)]
             assert fire == [bool(r["fire"]) for r in recs], "trigger"
@@ -302,7 +364,7 @@ class Lockstep:
                             band = BAND_FACTOR * max([rel_l2(x, ref) for x in pert] or [0.0])
                             e = rel_l2(got, ref)
                             rep.max_centroid_err = max(rep.max_centroid_err, e)
-                            assert e < max(self.state_tol, band), \
+                            assert e < max(self.update_tol, band), \
                                 f"centroid {name} after the update rel err {e} (layer {l}, seq {s}, band {band})"
                 U = self.read_layer(P.BUF_UPDATE, 0, (b, self.Wmax, d), torch.float32).numpy()
                 for s in range(b):
@@ -348,7 +410,12 @@ class Lockstep:
             dec_o = O.nvfp4_decode(oc, osb) + o.A[l][lab]
             e = rel_l2(dec_g, dec_o)
             self.rep.max_dec_err = max(self.rep.max_dec_err, e)
-            assert e < self.act_tol, f"decoded window states rel err {e} (layer {l})"
+            # NVFP4 rounding amplifies the upstream bf16 differences of the rows
+            # it encodes; the oracle's perturbed copies measure that amplification
+            si = s
+            band = BAND_FACTOR * max([rel_l2(O.nvfp4_decode(q.seqs[si].codes[l], q.seqs[si].sbytes[l]) + o.A[l][lab],
+                                             dec_o) for q in self.pert] or [0.0])
+            assert e < max(self.act_tol, band), f"decoded window states rel err {e} (layer {l}, band {band})"
             return
         bad = codes != oc
         sbad = np.repeat(scales != osb, 16, axis=1)

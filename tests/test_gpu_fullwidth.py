@@ -42,8 +42,10 @@ def test_full_width_lockstep(name, trunc, steps, npert, start):
     ls.lib.close()
     print(name, trunc, f"near ties {rep.near_ties}, sensitivity ties {rep.sensitivity_ties}", rep)
     assert rep.steps == steps
-    assert rep.compared >= 3 and rep.fires >= 2, rep
-    assert rep.near_ties + rep.sensitivity_ties <= 1, rep
+    # every step is compared in full, or ends in a counted tie after which the
+    # library takes over the oracle's state and comparison goes on
+    assert rep.compared + rep.resyncs == steps and rep.compared >= steps - 2 and rep.fires >= 2, rep
+    assert rep.near_ties + rep.sensitivity_ties == rep.resyncs, rep
 
 
 def test_state_import_round_trip():
