@@ -218,7 +218,7 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     # the NVFP4 store's host traffic runs on a side stream of its own
-    offload = not args.device_store
+    offload = args.host_store
     side = torch.cuda.Stream(dev) if offload else None
     cm = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device=dev)
     timed = steps[n_warmup:]
@@ -282,15 +282,27 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
         # in which every sequence refreshed, against the same steps without refresh
         log(f"{w.name}: same steps without refresh")
         base = region(profile=False, no_refresh=True)
+        log(f"{w.name}: same steps without refresh, profiled")
+        base_prof = region(profile=True, no_refresh=True)
         fired_idx = [i for i, f in enumerate(main["fired"]) if f]
         if fired_idx:
             t_fire = statistics.mean(main["step_ms"][i] for i in fired_idx)
             t_base = statistics.mean(base["step_ms"][i] for i in fired_idx)
-            overhead = {"ms_per_layer": (t_fire - t_base) / w.n_layers, "steps": len(fired_idx),
+            # the same difference with every launch bracketed by events (the
+            # launches then run one after another, as without any overlap)
+            s_fire = statistics.mean(prof["step_ms"][i] for i in fired_idx)
+            s_base = statistics.mean(base_prof["step_ms"][i] for i in fired_idx)
+            per_layer = (t_fire - t_base) / w.n_layers
+            serial = (s_fire - s_base) / w.n_layers
+            overhead = {"ms_per_layer": per_layer, "steps": len(fired_idx),
                         "step_ms_refreshing": t_fire, "step_ms_same_steps_no_refresh": t_base,
+                        "ms_per_layer_serialized": serial,
+                        "overlap_fraction": (1.0 - per_layer / serial) if serial > 0 else None,
                         "what": "per-layer added time of a within-block step in which every sequence runs the "
                                 "sparse refresh (patch, centroid update, proxy attention + KL, top-k, update "
-                                "packets), against the same step with the trigger off"}
+                                "packets), against the same step with the trigger off; 'serialized' is the same "
+                                "difference with every launch bracketed by CUDA events (no launch overlaps the "
+                                "next), and overlap_fraction = 1 - ms_per_layer / ms_per_layer_serialized"}
     stats = prof["stats"]
     step_ms, total_ms, wall, clocks = main["step_ms"], main["total_ms"], main["wall"], main["clocks"]
     total_s = max_over_ranks(total_ms / 1e3, ws, dev)
@@ -553,8 +565,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=8,
                     help="timed steps replayed end to end from pinned host buffers (1.6 GB each at batch 32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--device-store", action="store_true",
-                    help="keep the NVFP4 residual store in device memory instead of pinned host memory")
+    ap.add_argument("--host-store", action="store_true",
+                    help="keep the NVFP4 residual store in pinned host memory (2-layer device ring) instead of "
+                         "device memory")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

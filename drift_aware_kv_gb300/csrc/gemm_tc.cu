@@ -1339,15 +1339,18 @@ cudaError_t launch_p2(const CUtensorMap* a, const CUtensorMap* const* b, const P
   cfg.blockDim = dim3(P2_THREADS);
   cfg.dynamicSmemBytes = p2_launch_smem(p.bn, p.stages, p.kpack);
   cfg.stream = st;
-  cudaLaunchAttribute at[2];
+  // No programmatic dependent launch for this kernel: with it (and the row
+  // kernels around it launched the same way) the layer loop of the LLaDA-8B
+  // batch-32 workload stalled on GB300 within a few steps, with no bounded
+  // wait giving up; launched in plain stream order it did not.  The kernel runs
+  // only for more than 256 rows, where a launch gap is small against its work.
+  cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_p2_kernel, *a, *b[0], *b[1], *b[2], p);
 }
 

@@ -89,6 +89,7 @@ class Report:
     max_band_rel: float = 0.0
     max_centroid_err: float = 0.0
     resyncs: int = 0
+    max_u_band: float = 0.0
     notes: list = dataclasses.field(default_factory=list)
 
 
@@ -371,9 +372,16 @@ class Lockstep:
                     if not fire[s]:
                         continue
                     selm = recs[s]["sel"][-1]
-                    e = rel_l2(U[s, :nw][selm], recs[s]["U_last"][selm])
+                    ref = recs[s]["U_last"][selm]
+                    e = rel_l2(U[s, :nw][selm], ref)
                     rep.max_u_err = max(rep.max_u_err, e)
-                    assert e < self.act_tol, f"update packet rel err {e}"
+                    # the packets are computed from NVFP4-decoded window states, whose
+                    # code choices amplify upstream bf16 differences: the oracle's
+                    # perturbed copies give the spread that this alone causes
+                    band = BAND_FACTOR * max([rel_l2(self.recs_p[i][s]["U_last"][selm], ref)
+                                              for i in self._live()] or [0.0])
+                    rep.max_u_band = max(rep.max_u_band, band)
+                    assert e < max(self.act_tol, band), f"update packet rel err {e} (band {band})"
                     for l in range(L):
                         self._check_codes(None, None, self.orc.seqs[s], l, s=s, nw=nw)
         # K/V cache of every layer
