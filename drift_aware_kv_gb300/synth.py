@@ -90,6 +90,9 @@ class Workload:
     extra_frac: tuple = (0.1, 0.1)  # U(lo, hi) per sequence; (0.1, 0.1) = fixed 10 %
     n_steps: Optional[int] = None  # None: run until every block is decoded
     norm_gain_std: float = 0.0  # RMSNorm gains 1 + N(0, std) (0: gains 1, as in the benchmark shapes)
+    qk_std: float = 0.02  # std of the query/key projections
+    vo_std: float = 0.02  # std of the value/output projections
+    lm_std: Optional[float] = None  # LM head std for closed-loop decoding (None: 4 / sqrt(d))
 
     @property
     def seq_len(self) -> int:
@@ -138,6 +141,19 @@ WORKLOADS: Dict[str, Workload] = {
         head_dim=128, ffn_dim=1376, rope_base=500000.0, rms_eps=1e-5, dtype="bf16",
         batch=2, prompt_len=64, gen_len=128, vocab=2048, embed_vocab=2048, n_steps=14,
         extra_frac=(0.05, 0.2)),
+    # closed-loop decoding (embedding -> layer stack -> LM head -> gate -> tokens):
+    # attention weights raised so that positions differ, LM head scaled so that
+    # confidences spread over the gate's branches
+    "loop_l1_d256_fp32": Workload(
+        name="loop_l1_d256_fp32", n_layers=1, d_model=256, n_heads=4, n_kv_heads=4,
+        head_dim=64, ffn_dim=688, rope_base=10000.0, rms_eps=1e-6, dtype="fp32",
+        batch=2, prompt_len=64, gen_len=128, vocab=512, embed_vocab=512,
+        qk_std=0.16, vo_std=0.12, lm_std=0.5),
+    "loop_l2_d512_bf16": Workload(
+        name="loop_l2_d512_bf16", n_layers=2, d_model=512, n_heads=4, n_kv_heads=4,
+        head_dim=128, ffn_dim=1376, rope_base=500000.0, rms_eps=1e-5, dtype="bf16",
+        batch=2, prompt_len=64, gen_len=128, vocab=2048, embed_vocab=2048,
+        qk_std=0.1, vo_std=0.08, lm_std=0.35),
     "mini_gqa_l2_d448_bf16": Workload(
         name="mini_gqa_l2_d448_bf16", n_layers=2, d_model=448, n_heads=7, n_kv_heads=1,
         head_dim=64, ffn_dim=1184, rope_base=1000000.0, rms_eps=1e-6, dtype="bf16",
@@ -168,14 +184,18 @@ def weight_shapes(w: Workload) -> Dict[str, tuple]:
 
 
 def make_layer_weights(w: Workload, layer: int, device="cpu") -> Dict[str, torch.Tensor]:
-    """Random-init weights of one decoder layer: matrices N(0, 0.02), norm gains 1
-    (or 1 + N(0, norm_gain_std), distinct per norm and layer, in test variants).
+    """Random-init weights of one decoder layer: matrices N(0, 0.02) (query/key
+    and value/output projections N(0, qk_std) / N(0, vo_std): the closed-loop
+    decoding variants raise them so that attention, not the residual stream
+    alone, shapes each position's output), norm gains 1 (or 1 + N(0,
+    norm_gain_std), distinct per norm and layer, in test variants).
 
     Matrices are row-major [out_features, in_features] (y = x @ W^T)."""
     dt = torch_dtype(w)
     out = {}
+    stds = {"wq": w.qk_std, "wk": w.qk_std, "wv": w.vo_std, "wo": w.vo_std}
     for i, (name, shape) in enumerate(weight_shapes(w).items()):
-        out[name] = _randn(shape, derive_seed(w.seed, 0x57, layer, i), device, 0.02).to(dt)
+        out[name] = _randn(shape, derive_seed(w.seed, 0x57, layer, i), device, stds.get(name, 0.02)).to(dt)
     if w.norm_gain_std > 0:
         # distinct, non-unit gains for the two norms of every layer (test variant)
         out["attn_norm"] = (1.0 + _randn((w.d_model,), derive_seed(w.seed, 0x6A1, layer), device,
@@ -190,6 +210,42 @@ def make_layer_weights(w: Workload, layer: int, device="cpu") -> Dict[str, torch
 
 def make_weights(w: Workload, device="cpu") -> List[Dict[str, torch.Tensor]]:
     return [make_layer_weights(w, l, device) for l in range(w.n_layers)]
+
+
+def make_decode_weights(w: Workload, device="cpu", lm_std: Optional[float] = None) -> Dict[str, torch.Tensor]:
+    """Random-init tensors around the layer stack for closed-loop decoding, in the
+    storage dtype: token embedding [V, d] N(0, 1) (the scale of the trajectory's
+    prompt rows), the [MASK] embedding [d] (the trajectory's mask embedding), the
+    LM head [V, d] N(0, lm_std) and the final norm gain [d] (1, or
+    1 + N(0, norm_gain_std)).  lm_std defaults to 4 / sqrt(d): a unit-RMS row then
+    gives logits of standard deviation 4, whose max-softmax confidences spread
+    over (0, 1) at the parity vocabularies, so the gate's branches all occur."""
+    dt = torch_dtype(w)
+    V, d = w.vocab, w.d_model
+    if lm_std is None:
+        lm_std = w.lm_std if w.lm_std is not None else 4.0 / math.sqrt(d)
+    out = {
+        "embed": _randn((V, d), derive_seed(w.seed, 0xE3B), device).to(dt),
+        "mask_emb": _randn((d,), derive_seed(w.seed, 0x3A5), "cpu").to(device).to(dt),
+        "lm_head": _randn((V, d), derive_seed(w.seed, 0x1A4), device, lm_std).to(dt),
+    }
+    if w.norm_gain_std > 0:
+        out["final_norm"] = (1.0 + _randn((d,), derive_seed(w.seed, 0x6A3), device, w.norm_gain_std)).to(dt)
+    else:
+        out["final_norm"] = torch.ones(d, dtype=dt, device=device)
+    return out
+
+
+def make_prompt(w: Workload, device="cpu"):
+    """Prompt tokens U[0, V) per sequence, generated positions masked: returns
+    (tokens [batch, N] int32 with 0 at masked positions, masked [batch, N] bool)."""
+    N = w.seq_len
+    g = torch.Generator(device="cpu").manual_seed(derive_seed(w.seed, 0x9A0))
+    tokens = torch.zeros(w.batch, N, dtype=torch.int32)
+    tokens[:, : w.prompt_len] = torch.randint(0, w.vocab, (w.batch, w.prompt_len), generator=g, dtype=torch.int32)
+    masked = torch.zeros(w.batch, N, dtype=torch.bool)
+    masked[:, w.prompt_len:] = True
+    return tokens.to(device), masked.to(device)
 
 
 def block_span(w: Workload, b: int):

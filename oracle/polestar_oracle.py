@@ -437,7 +437,7 @@ class PolestarOracle:
             lse[:, h] = logsumexp(s[:, h, :])
             p = np.exp(s[:, h, :] - lse[:, h, None])
             o[:, h, :] = p @ kv[:, 1, h // grp, :]
-        return self._store(o.reshape(len(q), -1)), s, lse
+        return self._store(o.reshape(len(q), c.n_heads * c.head_dim)), s, lse
 
     def post(self, l, h, attn):
         """Output projection + residual, then the SwiGLU FFN + residual."""
@@ -525,7 +525,7 @@ class PolestarOracle:
         nw = len(win)
         st.labels, st.z, st.s, st.A = [], [], [], []
         st.codes, st.sbytes, st.code_margin, st.P_prev = [], [], [], []
-        out = dict(kmeans_margin=[], labels=[], z=[], A=[], own_labels=[])
+        out = dict(kmeans_margin=[], labels=[], z=[], A=[], own_labels=[], act_out=h[aidx].copy())
         self.exact_H[si] = [x.copy() for x in Hw]
         for l in range(c.n_layers):
             init = kmeans_init(c.seed, si, b, l, nw, c.K)
@@ -654,6 +654,28 @@ class PolestarOracle:
         self.last_recs = recs
         return recs
 
+    def decode_rows(self, recs):
+        """Last-layer hidden states of the 2B rows the commit gate scores, per
+        sequence [2B, d]: the active block's outputs, and for the suffix block the
+        update packets U(t, L) of the rows the last layer refreshed (Algorithm 1,
+        suffix commit); rows without a fresh state are zero (they cannot commit)."""
+        c = self.cfg
+        B = c.block
+        start, end = self._span(self.block)
+        win = self.window(self.block)
+        out = []
+        for si, st in enumerate(self.seqs):
+            rows = np.zeros((2 * B, c.d_model))
+            rec = recs[si]
+            if "act_out" in rec:
+                rows[:B] = rec["act_out"]
+                if rec.get("U_last") is not None and st.sel_last is not None:
+                    for wi, p in enumerate(win):
+                        if end <= p < start + 2 * B and st.sel_last[wi]:
+                            rows[p - start] = rec["U_last"][wi]
+            out.append(rows)
+        return out
+
     # ---- Polestar-Commit (§4.2; Algorithm 1, commit phases) ------------------------------
     def commit(self, logits, masked):
         """Commit mask for the 2B rows (active block, then suffix block) of every
@@ -702,6 +724,76 @@ class PolestarOracle:
             out.append(dict(commit=m, conf=conf, delta_rel=delta_rel, tau_d=tau_d,
                             margin=margin, margin_drift=margin_drift))
         return out
+
+
+# --------------------------------------------------------------------------------------
+# closed-loop decoding: LM head, greedy tokens, the progress rule (Algorithm 1 in full)
+# --------------------------------------------------------------------------------------
+
+
+def lm_logits(h, w_lm, gain, eps, bf16):
+    """Logits m_theta(v | y, i) of the LM head (Eq. 1) for hidden states h [R, d]:
+    RMSNorm with the final gain, rounded to the storage dtype like every
+    projection input, then W_lm [V, d]."""
+    x = rmsnorm(h, gain, eps)
+    if bf16:
+        x = to_bf16(x)
+    return x @ np.asarray(w_lm, dtype=np.float64).T
+
+
+def greedy_tokens(logits):
+    """y^_i = argmax_v logits (Eq. 1; the synthetic vocabulary has no [MASK] id),
+    ties to the lower id; also the gap between the two largest logits relative
+    to the largest magnitude (the decision's margin)."""
+    l = np.asarray(logits, dtype=np.float64)
+    ids = np.argmax(l, axis=-1)  # first maximum: the lower id on ties
+    top2 = np.sort(l, axis=-1)[..., -2:]
+    margin = (top2[..., 1] - top2[..., 0]) / np.maximum(np.abs(top2[..., 1]), 1e-300)
+    return ids, margin
+
+
+def progress_rule(commit, conf, masked_cur):
+    """Every step makes progress.  The paper builds its decoder on the
+    Fast-dLLM-style block decoder (App. D.1) without spelling out the case in
+    which the gate commits nothing; read here as that decoder's fallback: a step
+    that commits no token of the current block while some are still masked
+    commits the masked one of highest confidence (ties to the lower position).
+    commit / masked_cur: [B] bool of the current block; returns the new
+    current-block commit flags."""
+    out = np.array(commit, dtype=bool).copy()
+    m = np.asarray(masked_cur, dtype=bool)
+    if m.any() and not (out & m).any():
+        c = np.where(m, np.asarray(conf, dtype=np.float64), -np.inf)
+        out[int(np.argmax(c))] = True
+    return out
+
+
+def embed_inputs(tokens, masked, embed, mask_emb):
+    """Layer-0 hidden states of one step (§2: the model reads the partially
+    unmasked sequence): the embedding row of every decoded token, the [MASK]
+    embedding at masked positions.  tokens [N] int, masked [N] bool,
+    embed [V, d], mask_emb [d]; returns [N, d]."""
+    E = np.asarray(embed, dtype=np.float64)
+    out = E[np.asarray(tokens)].copy()
+    out[np.asarray(masked, dtype=bool)] = np.asarray(mask_emb, dtype=np.float64)
+    return out
+
+
+def apply_commits(tokens, masked, commit, ids, start):
+    """Committed positions take their greedy tokens and leave the mask
+    (Algorithm 1: y_i <- y^_i for committed i).  commit / ids: the 2B rows from
+    `start` (active block, then suffix block); rows past the sequence end are
+    ignored.  Updates tokens [N] / masked [N] in place; returns the number of
+    tokens committed."""
+    n = 0
+    N = len(tokens)
+    for j in range(len(commit)):
+        p = start + j
+        if p < N and commit[j] and masked[p]:
+            tokens[p] = int(ids[j])
+            masked[p] = False
+            n += 1
+    return n
 
 
 def weights_to_numpy(layer_weights):
