@@ -177,7 +177,10 @@ def make_inputs(w, n_steps, device):
 def class_roofline(name, s, w, peaks):
     if s["launches"] == 0 or s["ms"] <= 0:
         return None
-    tensor = name == "gemm_entry" or (name == "gemm_step" and w.batch >= 8)
+    # the roof that bounds the class: its flops at the tensor peak against its
+    # algorithmic bytes at the copy rate, whichever takes longer
+    tf_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    tensor = s["flops"] / (tf_peak * 1e12) > s["bytes"] / (peaks["hbm_gbs"] * 1e9)
     if tensor:
         peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
         achieved = s["flops"] / (s["ms"] / 1e3) / 1e12
@@ -370,7 +373,8 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "nvfp4_store": "pinned host, 2-layer device ring" if offload else "device",
                    "l2": "per-step working set (weights) >> L2; no flush needed",
-                   "timed_block_entries": n_entry, "timed_within_block_steps": n_within},
+                   "timed_block_entries": n_entry, "timed_within_block_steps": n_within,
+                   "attention_kernel": {0: "library choice", 1: "pipelined mma.sync", 2: "tcgen05"}[args.attn_impl]},
         "window_tokens_per_s": value * w.batch * nw_mean,
         "block_entry_ms": statistics.mean(entry_ms) if entry_ms else None,
         "within_block_ms": statistics.mean(within_ms) if within_ms else None,
@@ -395,6 +399,9 @@ def run_device(args, w, peaks, ws, rank, local):
     if rank == 0 or ws == 1:
         build()
     barrier(ws)
+    if args.attn_impl:
+        from drift_aware_kv_gb300 import polestar as P
+        P.attention_impl(args.attn_impl)
     out = run_workload(args, w, peaks, ws, rank, local, args.warmup, args.steps, full=True)
     out.update({"metric": "calibration steps/s", "unit": "steps/s", "n_gpus": ws, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
@@ -565,6 +572,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=8,
                     help="timed steps replayed end to end from pinned host buffers (1.6 GB each at batch 32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-impl", type=int, default=0, choices=[0, 1, 2],
+                    help="attention kernel: 0 the library's choice, 1 pipelined mma.sync, 2 tcgen05 (comparison runs)")
     ap.add_argument("--host-store", action="store_true",
                     help="keep the NVFP4 residual store in pinned host memory (2-layer device ring) instead of "
                          "device memory")

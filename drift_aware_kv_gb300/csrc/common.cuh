@@ -157,4 +157,13 @@ __device__ __forceinline__ void pdl_enter() {
 // ---- row metadata -------------------------------------------------------------
 enum RowKind : int { ROW_NONE = 0, ROW_ACTIVE = 1, ROW_WINDOW = 2, ROW_PROXY = 3, ROW_OTHER = 4 };
 
+// log sum_j q_j e^(d_j) of the KL drift (Eq. 4 with q = the previous softmax and
+// d = new minus previous score), from x = sum_j q_j expm1(d_j) / sum_j q_j:
+// log1p(x) while x > -1/2.  Below that the sum is the ratio e^(lse_new - lse_prev)
+// near zero, and 1 + x would cancel the digits that matter, so the difference
+// of the two log-sum-exps (natural units) is taken instead.
+__device__ __forceinline__ float kl_log_mass(float x, float lse_new, float lse_prev) {
+  return x > -0.5f ? log1pf(x) : lse_new - lse_prev;
+}
+
 }  // namespace polestar

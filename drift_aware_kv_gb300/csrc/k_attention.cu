@@ -58,16 +58,26 @@ __global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
   // tracking: where the previous scores of this (row, head) live
   float* prev = nullptr;
   float* prev_lse = nullptr;
+  // where the new scores / log-sum-exp go: the deferred-drift buffers when the
+  // drift pass measures the KL, else over the previous ones
+  float* sdst = nullptr;
+  float* ldst = nullptr;
+  const bool deferred = p.measure && (p.proxy_new != nullptr || p.active_new != nullptr);
   if (live && m.z == ROW_PROXY && p.proxy_prev) {
     const size_t idx = ((size_t)seq * p.K + m.w) * p.H + h;
     prev = p.proxy_prev + idx * p.N;
     prev_lse = p.proxy_prev_lse + idx;
+    sdst = deferred ? p.proxy_new + idx * p.N : prev;
+    ldst = deferred ? p.proxy_new_lse + idx : prev_lse;
   } else if (live && m.z == ROW_ACTIVE && p.active_prev) {
     const size_t idx = ((size_t)seq * p.B + m.w) * p.H + h;
     prev = p.active_prev + idx * p.N;
     prev_lse = p.active_prev_lse + idx;
+    sdst = deferred ? p.active_new + idx * p.N : prev;
+    ldst = deferred ? p.active_new_lse + idx : prev_lse;
   }
-  const bool do_kl = prev && p.measure;
+  const bool do_kl = prev && p.measure && !deferred;
+  const bool put = p.store || deferred;
   const float shift_prev = do_kl ? *prev_lse : 0.f;
 
   // stage this warp's query (fp32)
@@ -161,7 +171,7 @@ __global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
           sq_part += qt;
           e_part += qt * expm1f(dj);
         }
-        if (p.store) prev[j] = s[t];
+        if (put) sdst[j] = s[t];
       }
     }
     __syncwarp();
@@ -188,8 +198,9 @@ __global__ void __launch_bounds__(256) row_attention_kernel(AttnArgs p) {
     const float sq_tot = warp_sum(sq_part);
     const float e_tot = warp_sum(e_part);
     if (lane == 0) {
-      if (do_kl) p.kl_out[(size_t)r * p.H + h] = a_tot / l_tot - log1pf(e_tot / sq_tot);
-      if (p.store) *prev_lse = mrun + logf(l_tot);
+      if (do_kl)
+        p.kl_out[(size_t)r * p.H + h] = a_tot / l_tot - kl_log_mass(e_tot / sq_tot, mrun + logf(l_tot), shift_prev);
+      if (put) *ldst = mrun + logf(l_tot);
     }
   }
 }
@@ -218,18 +229,25 @@ int attention_set_impl(int impl) {
   return old;
 }
 
-int attention_item_rows(bool bf16, int dh, long long items128, int H, bool measures) {
-  (void)items128;
-  (void)H;
-  (void)measures;
+int attention_item_rows(bool bf16, int dh, long long items128, int H, bool measures, bool deferred) {
   if (!bf16 || dh != 128) return ATT_ITEM_ROWS;
-  // The tcgen05 kernel runs when selected: measured on GB300 it is limited by
-  // its one-thread-per-row softmax (about 1.6 us per 64-key tile) and by KL
-  // rows (one thread does a row's drift terms), and it is slower than the
-  // pipelined mma.sync kernel at the layer-loop shapes (within 5-10 % faster
-  // only for untracked items of 256 rows), so the library's choice is the
-  // mma.sync kernel.
-  return g_attention_impl == 2 ? ATT_TC_ROWS : ATT_ITEM_ROWS;
+  // the tcgen05 kernel leaves KL drift to the deferred drift pass
+  if (measures && !deferred) return ATT_ITEM_ROWS;
+  if (g_attention_impl == 1) return ATT_ITEM_ROWS;
+  if (g_attention_impl == 2) return ATT_TC_ROWS;
+  // Library's choice: the tcgen05 kernel when its items fill every SM twice
+  // (two CTAs per SM); below that the pipelined mma.sync kernel, whose smaller
+  // items and key splits keep all SMs busy.  Measured on GB300 at LLaDA-8B
+  // batch 32 (N = 2048): 270 vs 398 us per layer for attention + drift pass.
+  static int nsm_of[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int nsm = dev >= 0 && dev < 64 ? nsm_of[dev] : 0;
+  if (nsm <= 0) {
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64) nsm_of[dev] = nsm;
+  }
+  return items128 * H >= 2LL * nsm ? ATT_TC_ROWS : ATT_ITEM_ROWS;
 }
 
 template <typename T>

@@ -16,9 +16,11 @@
 //     needs and releases it when done, so warps never wait for each other.
 //   * S = Q K^T and O += P V run on mma.sync m16n8k16 (fp32 accumulation) with
 //     ldmatrix reads that undo the swizzle; online softmax in log2 units.
-//   * Rows under drift tracking fetch their previous scores for the tile with
-//     cp.async into a per-warp shared-memory tile when the tile starts, so the
-//     fetch overlaps the wait for K/V and the S = Q K^T products.
+//   * Rows under drift tracking either compute their KL terms here (they fetch
+//     their previous scores for the tile with cp.async into a per-warp
+//     shared-memory tile when the tile starts, so the fetch overlaps the wait
+//     for K/V and the S = Q K^T products), or, in deferred mode (the layer
+//     loop), only write their new scores and log-sum-exp for the drift pass.
 //   * Key ranges of one (item, head) form a thread-block cluster; their partial
 //     results meet in distributed shared memory and every CTA of the cluster
 //     finishes a slice of the rows (ranks in fixed order: deterministic).  No
@@ -244,7 +246,13 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
     bool live[2], outp[2];
     float* prev[2] = {nullptr, nullptr};
     float* prev_lse[2] = {nullptr, nullptr};
+    // where a tracked row's new scores / log-sum-exp go: the deferred-drift
+    // buffers when the drift pass measures it, else over the previous ones
+    float* sdst[2] = {nullptr, nullptr};
+    float* ldst[2] = {nullptr, nullptr};
     float shift[2] = {0.f, 0.f};
+    const bool deferred = p.measure && (p.proxy_new != nullptr || p.active_new != nullptr);
+    const bool inl = p.measure && !deferred;  // KL terms computed here
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int rl = i ? rl1 : rl0;
@@ -257,19 +265,24 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
         const size_t idx = ((size_t)seq * p.K + m.w) * p.H + h;
         prev[i] = p.proxy_prev + idx * p.N;
         prev_lse[i] = p.proxy_prev_lse + idx;
+        sdst[i] = deferred ? p.proxy_new + idx * p.N : prev[i];
+        ldst[i] = deferred ? p.proxy_new_lse + idx : prev_lse[i];
       } else if (live[i] && m.z == ROW_ACTIVE && p.active_prev) {
         const size_t idx = ((size_t)seq * p.B + m.w) * p.H + h;
         prev[i] = p.active_prev + idx * p.N;
         prev_lse[i] = p.active_prev_lse + idx;
+        sdst[i] = deferred ? p.active_new + idx * p.N : prev[i];
+        ldst[i] = deferred ? p.active_new_lse + idx : prev_lse[i];
       }
-      if (prev[i] && p.measure) shift[i] = *prev_lse[i] * 1.4426950408889634f;  // log2 units
+      if (prev[i] && inl) shift[i] = *prev_lse[i] * 1.4426950408889634f;  // log2 units
     }
+    const bool put = p.store || deferred;  // tracked rows write their scores
     const bool warp_tracked = __any_sync(0xffffffffu, prev[0] != nullptr || prev[1] != nullptr);
     // previous scores of this warp's tracked rows come in per tile through
     // shared memory: row pointers (null = not tracked) and the tile buffer
     const float** ptab = ptab_all + warp * 16;
     float* pbuf = part + warp * 16 * (nsplit > 1 ? PF : PREV_PITCH);
-    const bool fetch = warp_tracked && p.measure;
+    const bool fetch = warp_tracked && inl;
     const bool vec = (p.N & 3) == 0 && (((uintptr_t)p.active_prev | (uintptr_t)p.proxy_prev) & 15) == 0;
     if (fetch) {
       if (qc == 0) {
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
           for (int ii = 0; ii < 2; ++ii) {
             if (!prev[ii] || j >= p.N) continue;
             const float s0 = sc[nt][2 * ii] * 0.6931471805599453f, s1 = sc[nt][2 * ii + 1] * 0.6931471805599453f;
-            if (p.measure) {
+            if (inl) {
               // Eq. 4 terms against the previous scores sp (natural-log units):
               // d = s - sp, q~ = exp(sp - lse_prev)
               const float2 sp = *(const float2*)(pbuf + (qr + 8 * ii) * PREV_PITCH + nt * 8 + qc * 2);
@@ -409,8 +422,8 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
                 esum[ii] = fmaf(q1, expm1_drift(d1), esum[ii]);
               }
             }
-            if (p.store) {
-              float* dst = prev[ii] + j;
+            if (put) {
+              float* dst = sdst[ii] + j;
               if (j + 1 < p.N && (((uintptr_t)dst) & 7) == 0) {
                 *(float2*)dst = make_float2(s0, s1);
               } else {
@@ -485,8 +498,11 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
             *(uint32_t*)(o + nt * 8 + qc * 2) = pack2(acc[nt][2 * ii] * inv, acc[nt][2 * ii + 1] * inv);
         }
         if (prev[ii] && qc == 0) {
-          if (p.measure) p.kl_out[(size_t)rows[ii] * p.H + h] = asum[ii] / lsum[ii] - log1pf(esum[ii] / sqs[ii]);
-          if (p.store) *prev_lse[ii] = mrun[ii] * 0.6931471805599453f + logf(lsum[ii]);
+          if (inl)
+            p.kl_out[(size_t)rows[ii] * p.H + h] =
+                asum[ii] / lsum[ii] - kl_log_mass(esum[ii] / sqs[ii], mrun[ii] * 0.6931471805599453f + logf(lsum[ii]),
+                                                  shift[ii] * 0.6931471805599453f);
+          if (put) *ldst[ii] = mrun[ii] * 0.6931471805599453f + logf(lsum[ii]);
         }
       }
     }
@@ -525,14 +541,22 @@ __global__ void __launch_bounds__(THREADS, 2) attn_pipe_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < NV; ++i) o[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
       }
+      const bool deferred = p.measure && (p.proxy_new != nullptr || p.active_new != nullptr);
       float* prev_lse = nullptr;
-      if (m.z == ROW_PROXY && p.proxy_prev)
-        prev_lse = p.proxy_prev_lse + ((size_t)seq * p.K + m.w) * p.H + h;
-      else if (m.z == ROW_ACTIVE && p.active_prev)
-        prev_lse = p.active_prev_lse + ((size_t)seq * p.B + m.w) * p.H + h;
+      float* lse_dst = nullptr;
+      if (m.z == ROW_PROXY && p.proxy_prev) {
+        const size_t idx = ((size_t)seq * p.K + m.w) * p.H + h;
+        prev_lse = p.proxy_prev_lse + idx;
+        lse_dst = deferred ? p.proxy_new_lse + idx : prev_lse;
+      } else if (m.z == ROW_ACTIVE && p.active_prev) {
+        const size_t idx = ((size_t)seq * p.B + m.w) * p.H + h;
+        prev_lse = p.active_prev_lse + idx;
+        lse_dst = deferred ? p.active_new_lse + idx : prev_lse;
+      }
       if (prev_lse && lane == 0) {
-        if (p.measure) p.kl_out[(size_t)r * p.H + h] = a / l - log1pf(e / sq);
-        if (p.store) *prev_lse = M * 0.6931471805599453f + logf(l);
+        if (p.measure && !deferred)
+          p.kl_out[(size_t)r * p.H + h] = a / l - kl_log_mass(e / sq, M * 0.6931471805599453f + logf(l), *prev_lse);
+        if (p.store || deferred) *lse_dst = M * 0.6931471805599453f + logf(l);
       }
     }
     cl_sync();  // no CTA leaves while another still reads its partials

@@ -1,11 +1,13 @@
-// bf16 row attention + KL drift on the 5th-generation tensor cores (tcgen05,
-// TMEM accumulators), for work items of up to 128 rows of one sequence.
+// bf16 row attention on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators), for work items of up to 128 rows of one sequence.
 //
 // Same computation as the rest of the row-attention family (Eq. 3 attention
-// over all N keys of the row's sequence; Eq. 4 KL drift against the previous
-// scores for tracked rows, in the cancellation-free form
-//   KL = sum_j p_j d_j - log1p( sum_j q~_j expm1(d_j) / sum_j q~_j ) ),
-// organised flash-attention style with every matrix product on tcgen05:
+// over all N keys of the row's sequence), organised flash-attention style with
+// every matrix product on tcgen05.  The KL drift of tracked rows (Eq. 4) is not
+// computed here: a tracked row's scores and log-sum-exp are written out (to the
+// deferred-drift buffers when the launch measures drift, which the drift pass
+// then compares with the previous ones; over the previous ones when it only
+// stores them), so the softmax threads do the same work for every row.
 //
 //   * CTA = one work item (<= 128 rows, given as at most two row ranges of one
 //     sequence) x one query head; the item's Q rows are the MMA's M side
@@ -19,13 +21,11 @@
 //     (the A operand), so the tensor cores compute tile j's scores while the
 //     softmax warps work on tile j-1;
 //   * warps 2-5 (one thread per row) read a row's 64 scores from TMEM, keep
-//     the running maximum (log2 units) and sum, and write P (bf16 pairs) back
-//     over the first half of the same score buffer; the running maximum is
-//     raised lazily (only when a tile's maximum exceeds it by more than 8, i.e.
-//     p <= 2^8), and then the TMEM output row is rescaled before the next P V;
-//   * tracked rows (drift terms) take their previous scores of tile j + 1 into
-//     shared memory with cp.async while tile j is processed (two buffers of up
-//     to 24 rows per item; further tracked rows read global memory directly);
+//     the running maximum (log2 units, eight independent chains per tile) and
+//     sum (four chains), and write P (bf16 pairs) back over the first half of
+//     the same score buffer; the running maximum is raised lazily (only when a
+//     tile's maximum exceeds it by more than 8, i.e. p <= 2^8), and then the
+//     TMEM output row is rescaled before the next P V;
 //   * V is the second product's B operand read N-major (dh contiguous) from
 //     the swizzled boxes, so no transposition is needed.
 // Every mbarrier wait is bounded; a timeout records an error code and the
@@ -53,12 +53,9 @@ constexpr int KBOX = 64 * TK * 2;             // 64 columns x 64 keys (K, V)
 constexpr int Q_OFF = 0;                      // 2 boxes (dh 0-63, 64-127)
 constexpr int RING_OFF = 2 * QBOX;            // STAGES x (K: 2 boxes, V: 2 boxes)
 constexpr int STAGE_BYTES = 4 * KBOX;
-constexpr int SLOTS = 24;                     // tracked rows whose previous scores are staged
-constexpr int SLOT_BYTES = TK * 4;
-constexpr int PREV_OFF = RING_OFF + STAGES * STAGE_BYTES;  // [2 buffers][SLOTS][TK] fp32
 constexpr int O_COL = 2 * TK;                 // TMEM: S/P buffers at 0 and TK, O after
 constexpr int TMEM_COLS = O_COL + DH;         // 256
-constexpr int CTL_OFF = PREV_OFF + 2 * SLOTS * SLOT_BYTES;
+constexpr int CTL_OFF = RING_OFF + STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = CTL_OFF + 256 + 1024;  // + control block + alignment
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s
 static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
@@ -142,11 +139,6 @@ __device__ __forceinline__ void umma_ta(uint32_t d, uint32_t a_tmem, uint64_t b,
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -204,17 +196,6 @@ __device__ __forceinline__ float ex2f(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// e^x - 1 for the KL drift term: Taylor series through x^6 for |x| < 1/8,
-// 2^(x log2 e) - 1 elsewhere (as in the pipelined kernel)
-__device__ __forceinline__ float expm1_drift(float x) {
-  float t = fmaf(x, 1.f / 720.f, 1.f / 120.f);
-  t = fmaf(x, t, 1.f / 24.f);
-  t = fmaf(x, t, 1.f / 6.f);
-  t = fmaf(x, t, 0.5f);
-  t = fmaf(x, t, 1.f);
-  const float big = ex2f(x * 1.4426950408889634f) - 1.f;
-  return fabsf(x) < 0.125f ? x * t : big;
-}
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *(const uint32_t*)&v;
@@ -235,7 +216,6 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
   uint64_t* q_full = pv_done + 2;
   uint32_t* tmem_slot = (uint32_t*)(q_full + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  int* slot_count = (int*)(tmem_slot + 2);  // [4] tracked rows per lane quarter
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
@@ -334,40 +314,23 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
     if (has) m = p.rows[row];
     const bool live = m.z != ROW_NONE && (m.z != ROW_OTHER || p.other_live);
     const bool outp = live && m.z != ROW_PROXY;
-    float* prev = nullptr;
-    float* prev_lse = nullptr;
+    // tracked rows write their scores (natural-log units) and log-sum-exp: to
+    // the deferred-drift buffers when the launch measures drift (the drift pass
+    // compares them with the previous ones), else over the previous ones
+    const bool defer = p.measure != 0;
+    float* sdst = nullptr;
+    float* ldst = nullptr;
     if (live && m.z == ROW_PROXY && p.proxy_prev) {
       const size_t idx = ((size_t)seq * p.K + m.w) * p.H + h;
-      prev = p.proxy_prev + idx * p.N;
-      prev_lse = p.proxy_prev_lse + idx;
+      sdst = (defer ? p.proxy_new : p.proxy_prev) + idx * p.N;
+      ldst = (defer ? p.proxy_new_lse : p.proxy_prev_lse) + idx;
     } else if (live && m.z == ROW_ACTIVE && p.active_prev) {
       const size_t idx = ((size_t)seq * p.B + m.w) * p.H + h;
-      prev = p.active_prev + idx * p.N;
-      prev_lse = p.active_prev_lse + idx;
+      sdst = (defer ? p.active_new : p.active_prev) + idx * p.N;
+      ldst = (defer ? p.active_new_lse : p.active_prev_lse) + idx;
     }
-    const float shift = (prev && p.measure) ? *prev_lse * 1.4426950408889634f : 0.f;
-    const bool vec_prev = (p.N & 3) == 0 && ((((uintptr_t)p.active_prev) | ((uintptr_t)p.proxy_prev)) & 15) == 0;
-    // staging slot of this row's previous scores: rank among the item's rows
-    // that measure drift (lane quarters in order), -1 beyond SLOTS or unstaged
-    const bool meas = prev && p.measure;
-    const unsigned bal = __ballot_sync(0xffffffffu, meas);
-    if (lane == 0) slot_count[qd] = __popc(bal);
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    int base = 0;
-    for (int k = 0; k < qd; ++k) base += slot_count[k];
-    const int rank = base + __popc(bal & ((1u << lane) - 1u));
-    const int slot = (meas && vec_prev && rank < SLOTS) ? rank : -1;
-    // tile t's previous scores of this row into staging buffer t & 1
-    auto stage_prev = [&](int t) {
-      if (slot < 0 || t >= ntl) return;
-      const int j0 = t * TK;
-      const uint32_t dst = su32(sm + PREV_OFF + ((t & 1) * SLOTS + slot) * SLOT_BYTES);
-#pragma unroll
-      for (int c = 0; c < TK / 4; ++c)
-        if (j0 + c * 4 < p.N) cp_async16(dst + c * 16, prev + j0 + c * 4);
-    };
-    stage_prev(0);
-    cp_async_commit();
+    if (!defer && !p.store) sdst = ldst = nullptr;
+    const bool vec_sc = (p.N & 3) == 0 && (((uintptr_t)sdst) & 15) == 0;
 
     // 16-byte row accesses when the strides and bases allow them
     const bool vec_io = ((p.ldq | p.ldo) & 7) == 0 && ((((uintptr_t)p.q) | ((uintptr_t)p.out)) & 15) == 0;
@@ -396,13 +359,10 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
     }
 
     const float sl2 = p.scale * 1.4426950408889634f;
-    float mrun = -INFINITY, l = 0.f, asum = 0.f, sqs = 0.f, esum = 0.f;
+    float mrun = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntl && ok; ++j) {
       const int b = j & 1, j0 = j * TK;
-      // the next tile's previous scores start coming in now
-      stage_prev(j + 1);
-      cp_async_commit();
       ok = mbar_wait(su32(&s_full[b]), (j >> 1) & 1, p.err, 26, abort_flag);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (!ok) break;
@@ -411,17 +371,26 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < TK / 32; ++c) tmem_ld32_nw(tl + b * TK + c * 32, sv + c * 32);
       tcgen05_wait_ld();
-      // pass 1: tile maximum (log2 units)
-      float mx = -INFINITY;
+      // pass 1: scores in log2 units (keys past N at -inf), tile maximum over
+      // eight independent chains
+      const bool fullt = j0 + TK <= p.N;
+      float mx8[8];
 #pragma unroll
-      for (int i = 0; i < TK; ++i)
-        if (j0 + i < p.N) mx = fmaxf(mx, __uint_as_float(sv[i]) * sl2);
+      for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < TK; ++i) {
+        float v = __uint_as_float(sv[i]) * sl2;
+        if (!fullt && j0 + i >= p.N) v = -INFINITY;
+        sv[i] = __float_as_uint(v);
+        mx8[i & 7] = fmaxf(mx8[i & 7], v);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // raise the running maximum only when it grows by more than 8 (p <= 2^8)
       const bool raise = mx > mrun + 8.f;
       const float mnew = raise ? mx : mrun;
       const float corr = raise ? ex2f(mrun - mnew) : 1.f;  // exp2(-inf) = 0 on the first tile
       l *= corr;
-      asum *= corr;
       // a raised maximum rescales the output, which must then hold P_{j-1} V_{j-1}
       const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
       if (rescale) {
@@ -442,72 +411,48 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       mrun = mnew;
-      // this tile's staged previous scores have landed (the next tile's may not)
-      if (slot >= 0) asm volatile("cp.async.wait_group 1;" ::: "memory");
-      const float* sp_tile = (const float*)(sm + PREV_OFF + (b * SLOTS + (slot >= 0 ? slot : 0)) * SLOT_BYTES);
       // pass 2: probabilities as bf16 pairs (P, written over the score buffer),
-      // and the drift terms / new stored scores of tracked rows
+      // the running sum over four chains, and a tracked row's scores
 #pragma unroll
       for (int hk = 0; hk < 2; ++hk) {  // two halves of 32 keys, 16 packed columns each
-      uint32_t pk[TK / 4];
+        uint32_t pk[TK / 4];
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int gg = 0; gg < TK / 8; ++gg) {
-        const int g = hk * (TK / 8) + gg;
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = g * 4 + e;
-          pv[e] = j0 + i < p.N ? ex2f(__uint_as_float(sv[i]) * sl2 - mrun) : 0.f;
-          l += pv[e];
-        }
-        pk[2 * gg] = pack2(pv[0], pv[1]);
-        pk[2 * gg + 1] = pack2(pv[2], pv[3]);
-        if (prev) {
-          const int jj = j0 + g * 4;
-          float sp[4] = {0.f, 0.f, 0.f, 0.f};
-          if (p.measure) {
-            if (slot >= 0) {
-              const float4 t = *(const float4*)(sp_tile + g * 4);
-              sp[0] = t.x; sp[1] = t.y; sp[2] = t.z; sp[3] = t.w;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) sp[e] = jj + e < p.N ? __ldcg(prev + jj + e) : 0.f;
-            }
-          }
-          float sn[4];
+        for (int gg = 0; gg < TK / 8; ++gg) {
+          const int g = hk * (TK / 8) + gg;
+          float pv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            sn[e] = __uint_as_float(sv[g * 4 + e]) * p.scale;  // natural-log units
-            if (p.measure && jj + e < p.N) {
-              const float d = sn[e] - sp[e];
-              const float qt = ex2f(fmaf(sp[e], 1.4426950408889634f, -shift));
-              asum = fmaf(pv[e], d, asum);
-              sqs += qt;
-              esum = fmaf(qt, expm1_drift(d), esum);
-            }
+            pv[e] = ex2f(__uint_as_float(sv[g * 4 + e]) - mrun);  // exp2(-inf) = 0 past N
+            l4[e] += pv[e];
           }
-          if (p.store) {
-            if (vec_prev && jj + 3 < p.N) {
-              *(float4*)(prev + jj) = make_float4(sn[0], sn[1], sn[2], sn[3]);
+          pk[2 * gg] = pack2(pv[0], pv[1]);
+          pk[2 * gg + 1] = pack2(pv[2], pv[3]);
+          if (sdst) {
+            const int jj = j0 + g * 4;
+            float sn[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sn[e] = __uint_as_float(sv[g * 4 + e]) * 0.6931471805599453f;
+            if (vec_sc && jj + 3 < p.N) {
+              *(float4*)(sdst + jj) = make_float4(sn[0], sn[1], sn[2], sn[3]);
             } else {
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                if (jj + e < p.N) prev[jj + e] = sn[e];
+                if (jj + e < p.N) sdst[jj + e] = sn[e];
             }
           }
         }
-      }
-      // keys 32 hk .. 32 hk + 31 as bf16 pairs: columns 16 hk .. 16 hk + 15 of the
-      // score buffer, whose scores are all in registers by now
-      tmem_st16_nw(tl + b * TK + hk * 16, pk);
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        // keys 32 hk .. 32 hk + 31 as bf16 pairs: columns 16 hk .. 16 hk + 15 of the
+        // score buffer, whose scores are all in registers by now
+        tmem_st16_nw(tl + b * TK + hk * 16, pk);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(su32(&p_full[b]));
     }
-    cp_async_wait_all();
-    // ---------------- epilogue: O / l, KL, log-sum-exp
+    // ---------------- epilogue: O / l, log-sum-exp
     if (ok && ntl > 0) {
       ok = mbar_wait(su32(&pv_done[(ntl - 1) & 1]), ((ntl - 1) >> 1) & 1, p.err, 28, abort_flag);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -543,10 +488,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
           }
         }
       }
-      if (prev) {
-        if (p.measure) p.kl_out[(size_t)row * p.H + h] = asum / l - log1pf(esum / sqs);
-        if (p.store) *prev_lse = mrun * 0.6931471805599453f + logf(l);
-      }
+      if (ldst) *ldst = mrun * 0.6931471805599453f + logf(l);
     }
   }
   if (*abort_flag && warp == 0 && lane == 0) {
@@ -600,6 +542,10 @@ const CUtensorMap* kv_map_tiles(const void* base, int rows, int kvdim, int dh) {
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int batch, cudaStream_t st) {
   if (a.dh != at::DH || (a.kvdim % 64)) return cudaErrorInvalidValue;
+  // drift is measured by the deferred pass only
+  if (a.measure && ((a.proxy_prev && (!a.proxy_new || !a.proxy_new_lse)) ||
+                    (a.active_prev && (!a.active_new || !a.active_new_lse))))
+    return cudaErrorInvalidValue;
   const CUtensorMap* map = at::kv_map_tiles(a.kv_layer, batch * a.N, a.kvdim, at::DH);
   if (!map) return cudaErrorInvalidValue;
   static PerDeviceOnce attr;

@@ -55,6 +55,36 @@ void launch_residual_scatter(const float* h1, const float* y, int ldy, const int
 template <typename T>
 void launch_gather_T(const void* src, const int* idx, const int* m_dev, int R, int w, void* dst,
                      cudaStream_t st);
+// ---- closed-loop decoding (k_decode.cu) ----
+struct DecodeRowsArgs {
+  const float* act;        // [batch, B, d] last-layer outputs of the active rows
+  const float* U;          // [batch, Wmax, d] update packets U(t, L)
+  const uint8_t* sel;      // [batch, Wmax] rows the last layer refreshed (null: none)
+  const uint8_t* fire;     // [batch] sequences whose window the step refreshed
+  int suffix_widx[64];     // window index of position start + B + i, or -1
+  int batch, B, d, Wmax, N, start;
+  const void* gain;        // [d] final norm gain (storage type)
+  float eps;
+  void* out;               // [batch * 2B, d] storage type: the LM head's input rows
+};
+struct ApplyArgs {
+  uint8_t* commit;         // [batch, 2B] commit mask, progress rule applied in place
+  const float* conf;       // [batch, 2B]
+  const int* ids;          // [batch, 2B] greedy tokens
+  int* tokens;             // [batch, N]
+  uint8_t* masked;         // [batch, N]
+  int* counts;             // [batch, 2]: tokens committed this step, current-block tokens still masked
+  int batch, B, N, start;
+};
+template <typename T>
+void launch_decode_rows(const DecodeRowsArgs& a, cudaStream_t st);
+void launch_argmax(const float* logits, int V, int R, int* ids, cudaStream_t st);
+void launch_apply_commits(const ApplyArgs& a, cudaStream_t st);
+template <typename T>
+void launch_embed(const void* embed, const void* mask_emb, const int* tokens, const uint8_t* masked, int vocab,
+                  int rows, int d, void* x0, cudaStream_t st);
+void launch_capture_active(const float* h, const int4* rows, int R, int d, int B, float* act, cudaStream_t st);
+
 void launch_capture_window(const float* h, const int4* rows, int R, int d, int Wmax, float* Hw_layer,
                            size_t seq_stride, cudaStream_t st);
 
@@ -80,6 +110,13 @@ struct AttnArgs {
   int measure;             // 1: write KL(new || prev) to kl_out[r, h]
   int store;               // 1: replace prev by the new scores
   float* kl_out;           // [R, H]
+  // deferred drift (all four set, with measure): a tracked row's new scores and
+  // log-sum-exp go to these buffers (the layout of the *_prev ones) and the
+  // kernel neither reads *_prev nor computes KL; launch_drift then does both
+  float* proxy_new;        // [batch, K, H, N]
+  float* proxy_new_lse;    // [batch, K, H]
+  float* active_new;       // [batch, B, H, N]
+  float* active_new_lse;   // [batch, B, H]
   // bf16 tensor-core path: work list of items {rowA, nA, rowB, nB}, each the
   // rows [rowA, rowA + nA) and [rowB, rowB + nB) of ONE sequence, at most
   // ATT_ITEM_ROWS in all (nullptr: CUDA-core path by rows)
@@ -101,10 +138,33 @@ constexpr int ATT_TC_ROWS = 128;   // tcgen05 kernel: one TMEM lane per row
 int attention_items(int4* w, int n, int a0, int na, int b0, int nb, int max_rows = ATT_ITEM_ROWS);
 // Rows per work item for a bf16/fp32 launch with head size dh whose items, at
 // ATT_TC_ROWS rows, would number about `items128` (all sequences) over H
-// heads, `measures` when some rows compute KL drift: ATT_TC_ROWS when the
-// tcgen05 kernel runs it (only when selected through attention_set_impl),
-// else ATT_ITEM_ROWS.
-int attention_item_rows(bool bf16, int dh, long long items128, int H, bool measures);
+// heads, `measures` when some rows compute KL drift and `deferred` when that
+// drift goes to the deferred drift pass: ATT_TC_ROWS when the tcgen05 kernel
+// runs it (bf16, head size 128, no in-kernel drift, and either selected
+// through attention_set_impl or enough items to fill every SM twice), else
+// ATT_ITEM_ROWS.
+int attention_item_rows(bool bf16, int dh, long long items128, int H, bool measures, bool deferred = false);
+
+// ---- KL drift of tracked rows from their new and previous scores (k_drift.cu) ----
+// Eq. 4 for each tracked (row, head): KL(softmax(new) || softmax(prev)) from the
+// scores an attention launch wrote in deferred mode; with store, the new scores
+// and log-sum-exps then replace the previous ones.
+struct DriftArgs {
+  const int4* track;       // [n_track] {step row r (kl_out row), seq, kind (ROW_PROXY / ROW_ACTIVE), idx}
+  int n_track;
+  int H, N, K, B;
+  float* proxy_prev;       // [batch, K, H, N] / [batch, K, H]
+  float* proxy_prev_lse;
+  float* active_prev;      // [batch, B, H, N] / [batch, B, H]
+  float* active_prev_lse;
+  const float* proxy_new;  // same layouts: this step's scores
+  const float* proxy_new_lse;
+  const float* active_new;
+  const float* active_new_lse;
+  float* kl_out;           // [rows, H]
+  int store;
+};
+void launch_drift(const DriftArgs& a, cudaStream_t st);
 // Test hook: 0 = library's choice, 1 = pipelined mma.sync kernel only, 2 =
 // tcgen05 kernel wherever it applies; returns the previous setting.
 int attention_set_impl(int impl);

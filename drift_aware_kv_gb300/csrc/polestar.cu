@@ -37,7 +37,8 @@ thread_local std::string g_init_error;
 size_t pad8(size_t x) { return (x + 7) & ~size_t(7); }
 
 struct MetaLayout {
-  size_t rows_off, prow_off, win_row_off, proxy_row_off, fire_seqs_off, win_pos_off, fire_off, work_off, total;
+  size_t rows_off, prow_off, win_row_off, proxy_row_off, fire_seqs_off, win_pos_off, fire_off, work_off, track_off,
+      total;
   int work_cap;
 };
 
@@ -73,6 +74,10 @@ struct polestar_ctx {
   cudaEvent_t ring_out[2] = {nullptr, nullptr};   // side: the slot is copied out
   float *pprev = nullptr, *pprev_lse = nullptr;            // [L, b, K, H, N], [L, b, K, H]
   float *aprev = nullptr, *aprev_lse = nullptr;            // [b, B, H, N], [b, B, H]
+  // this step's scores of the tracked rows, written by the attention launch and
+  // compared with the ones above by the drift pass (same layouts, one layer)
+  float *pnew = nullptr, *pnew_lse = nullptr;              // [b, K, H, N], [b, K, H]
+  float *anew = nullptr, *anew_lse = nullptr;              // [b, B, H, N], [b, B, H]
   float* theta = nullptr;        // [b, B, hist]
   int* theta_n = nullptr;        // [b, B]
   float* Hw = nullptr;           // [L, b, Wmax, d]
@@ -83,6 +88,14 @@ struct polestar_ctx {
   void* act = nullptr;  // bf16 SwiGLU output of the fused gate/up projection [<= 128][F]
   uint8_t* write_kv = nullptr;
   float *U = nullptr, *dn = nullptr;
+  // closed-loop decoding: active rows' last-layer outputs of a block entry, the
+  // LM head's input rows, greedy tokens, committed counts (device + pinned host)
+  float* act_last = nullptr;    // [b, B, d]
+  void* dec_rows = nullptr;     // [b * 2B, d] storage type
+  int* dec_ids = nullptr;       // [b * 2B]
+  int* dec_counts = nullptr;    // [b, 2]: committed, still masked in the block
+  int* dec_counts_h = nullptr;  // [b, 2] pinned
+  int committed = 0;            // polestar_commit ran after the last calibrate step
   uint8_t *sel_a = nullptr, *sel_b = nullptr, *sel_last = nullptr;
   int *o_src = nullptr, *m_o = nullptr;
   // outputs
@@ -119,10 +132,17 @@ struct polestar_ctx {
   TcGemmCache tc;
 
   // live per-kernel timing
+  // A projection whose row count lives on the device (m_dev: the compacted
+  // refresh rows) is charged bytes + rows x row_bytes and rows x row_flops, the
+  // rows read back (stream-ordered, into prof_rows) when the launch is recorded.
   struct ProfRec {
     int cls;
     double bytes, flops;
+    double row_bytes = 0.0, row_flops = 0.0;
+    int max_rows = 0;
+    bool device_rows = false;
   };
+  int* prof_rows = nullptr;  // pinned [prof_cap]
   bool prof_armed = false;
   int prof_cap = 0, prof_used = 0, gemm_cls = POLESTAR_KC_GEMM_STEP;
   std::vector<cudaEvent_t> prof_ev;
@@ -202,7 +222,7 @@ int prof_start(polestar_ctx* c, int cls) {
   }
   const int i = c->prof_used++;
   cudaEventRecord(c->prof_ev[2 * i], c->sm);
-  c->prof_rec[i] = {cls, 0.0, 0.0};
+  c->prof_rec[i] = polestar_ctx::ProfRec{cls, 0.0, 0.0};
   return i;
 }
 
@@ -213,8 +233,26 @@ void prof_stop(polestar_ctx* c, int i, double bytes, double flops) {
   c->prof_rec[i].flops = flops;
 }
 
+// A row-count-dependent launch: M rows (m_dev == nullptr) or the count at
+// m_dev (at most M) when the launch runs.
+void prof_stop_rows(polestar_ctx* c, int i, double fixed_bytes, double row_bytes, double row_flops, int M,
+                    const int* m_dev) {
+  if (i < 0) return;
+  cudaEventRecord(c->prof_ev[2 * i + 1], c->sm);
+  polestar_ctx::ProfRec& r = c->prof_rec[i];
+  r.bytes = fixed_bytes;
+  r.flops = 0.0;
+  r.row_bytes = row_bytes;
+  r.row_flops = row_flops;
+  r.max_rows = M;
+  r.device_rows = m_dev != nullptr && c->prof_rows != nullptr;
+  if (r.device_rows) cudaMemcpyAsync(c->prof_rows + i, m_dev, sizeof(int), cudaMemcpyDeviceToHost, c->sm);
+}
+
 void prof_release(polestar_ctx* c) {
   for (cudaEvent_t e : c->prof_ev) cudaEventDestroy(e);
+  if (c->prof_rows) cudaFreeHost(c->prof_rows);
+  c->prof_rows = nullptr;
   c->prof_ev.clear();
   c->prof_rec.clear();
   c->prof_armed = false;
@@ -295,6 +333,7 @@ MetaLayout meta_layout(int rows_cap, int b, int K, int Wmax, int N) {
   m.win_pos_off = take(sizeof(int) * Wmax);
   m.fire_off = take(b);
   m.work_off = take(sizeof(int4) * m.work_cap);
+  m.track_off = take(sizeof(int4) * ((size_t)b * K + (size_t)rows_cap));  // rows_cap >= b * block
   m.total = o;
   return m;
 }
@@ -346,16 +385,17 @@ polestar_status gemm_multi(polestar_ctx* c, const void* A, int lda, int nseg, co
                            float* const* C, int ldc, int M, const int* m_dev, int K) {
   if (M <= 0) return POLESTAR_OK;
   if (sizeof(T) == 2 && tc_gemm_supported(K, lda, K)) {
-    double bytes = 0.0, flops = 0.0;
+    double wbytes = 0.0, row_bytes = 0.0, row_flops = 0.0;
     int ldw[3];
     for (int i = 0; i < nseg; ++i) {
       ldw[i] = K;
-      bytes += ((double)N[i] * K + (double)M * K) * sizeof(T) + (double)M * N[i] * 4.0;
-      flops += 2.0 * M * N[i] * K;
+      wbytes += (double)N[i] * K * sizeof(T);
+      row_bytes += (double)K * sizeof(T) + (double)N[i] * 4.0;
+      row_flops += 2.0 * N[i] * K;
     }
     const int pi = prof_start(c, c->gemm_cls);
     cudaError_t e = tc_gemm_bf16_multi(&c->tc, A, lda, nseg, W, ldw, N, C, ldc, M, m_dev, K, c->sm);
-    prof_stop(c, pi, bytes, flops);
+    prof_stop_rows(c, pi, wbytes, row_bytes, row_flops, M, m_dev);
     ++c->launches;
     if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 gemm: ") + cudaGetErrorString(e));
     return POLESTAR_OK;
@@ -368,17 +408,21 @@ template <typename T>
 polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int ldw, float* C, int ldc, int M,
                      const int* m_dev, int N, int K) {
   if (M <= 0) return POLESTAR_OK;
-  const double bytes = ((double)N * K + (double)M * K) * sizeof(T) + (double)M * N * 4.0;
-  const double flops = 2.0 * M * N * K;
+  const double wbytes = (double)N * K * sizeof(T);
+  const double row_bytes = (double)K * sizeof(T) + (double)N * 4.0;
+  const double row_flops = 2.0 * N * K;
   if (sizeof(T) == 2 && tc_gemm_supported(K, lda, ldw)) {
     const int pi = prof_start(c, c->gemm_cls);
     cudaError_t e = tc_gemm_bf16(&c->tc, A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm);
-    prof_stop(c, pi, bytes, flops);
+    prof_stop_rows(c, pi, wbytes, row_bytes, row_flops, M, m_dev);
     ++c->launches;
     if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 gemm: ") + cudaGetErrorString(e));
     return POLESTAR_OK;
   }
-  RUN(c->gemm_cls, bytes, flops, (launch_gemm_simt<T>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm)));
+  const int pi = prof_start(c, c->gemm_cls);
+  launch_gemm_simt<T>(A, lda, W, ldw, C, ldc, M, m_dev, N, K, c->sm);
+  prof_stop_rows(c, pi, wbytes, row_bytes, row_flops, M, m_dev);
+  LAUNCHED(c);
   return POLESTAR_OK;
 }
 
@@ -396,11 +440,10 @@ polestar_status gate_up_swiglu(polestar_ctx* c, const polestar_layer_weights& w,
   int ch[4] = {0, 0, 0, 0};
   if (sizeof(T) == 2 && c->act && R > 0 && R <= 128 && tc_gemm_supported(d, d, d) &&
       tc_gemm_choice(&c->tc, R, 2, Ns, d, ch) == cudaSuccess && ch[0] == 1) {
-    const double bytes = ((double)2 * F * d + (double)R * d) * sizeof(T) + (double)R * F * 2.0;
-    const double flops = 4.0 * R * F * d;
     const int pi = prof_start(c, c->gemm_cls);
     const cudaError_t e = tc_gemm_bf16_swiglu(&c->tc, c->a_in, d, w.w_gate, w.w_up, d, F, c->act, F, R, m_dev, d, c->sm);
-    prof_stop(c, pi, bytes, flops);
+    prof_stop_rows(c, pi, (double)2 * F * d * sizeof(T), (double)d * sizeof(T) + (double)F * 2.0, 4.0 * F * d, R,
+                   m_dev);
     ++c->launches;
     if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 gemm + SwiGLU: ") + cudaGetErrorString(e));
     *act_out = c->act;
@@ -608,7 +651,7 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
                                 (track ? (double)ns * c->B * c->H * N * 4.0 : 0.0);
       aa.batch = b;
       aa.err = tc_error_word(&c->tc);
-      RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
+      RUN(POLESTAR_KC_ATTENTION, attn_bytes, 4.0 * R * N * c->qdim, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
       TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
                                  c->a_in, c->sm)));
@@ -619,6 +662,9 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
           (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows,
                                       nullptr, c->sm)));
     }
+    // the active rows' last-layer outputs: the rows the commit gate scores
+    if (!fwd_only)
+      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_active(c->h_rows, rows, R, d, c->B, c->act_last, c->sm)));
   }
   if (fwd_only) return POLESTAR_OK;
   // spherical K-means + residual NVFP4 for every (layer, sequence)
@@ -689,7 +735,7 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
     const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz + (double)b * c->K * c->H * N * 4.0;
     aa.batch = b;
     aa.err = tc_error_word(&c->tc);
-    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
+    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 4.0 * Rp * N * c->qdim, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
   }
   std::fill(c->cum.begin(), c->cum.end(), 0);
   std::fill(c->fire.begin(), c->fire.end(), 0);
@@ -735,13 +781,23 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     for (int k = 0; k < c->K; ++k) rows_h[R++] = make_int4(s, 0, ROW_PROXY, k);
     while (R % 8) rows_h[R++] = make_int4(s, 0, ROW_NONE, 0);
   }
+  {
+    // rows whose drift the deferred pass measures: the refreshing sequences'
+    // proxies (every layer), then the active rows (last layer)
+    int4* track = meta_h<int4>(c, c->ml.track_off);
+    int n = 0;
+    for (int f = 0; f < n_fire; ++f)
+      for (int k = 0; k < c->K; ++k) track[n++] = make_int4(proxy_row[fire_seqs[f]] + k, fire_seqs[f], ROW_PROXY, k);
+    for (int s = 0; s < b; ++s)
+      for (int j = 0; j < B; ++j) track[n++] = make_int4(s * B + j, s, ROW_ACTIVE, j);
+  }
   for (int i = 0; i < c->nw; ++i) wp[i] = c->win_pos[i];
   int4* work_h = meta_h<int4>(c, c->ml.work_off);
   int nwk = 0;
   // one sequence's active rows and (when it refreshes) its window + proxy rows
   long long items128 = 0;
   for (int s = 0; s < b; ++s) items128 += (B + (win_row[s] >= 0 ? c->nw + c->K : 0) + ATT_TC_ROWS - 1) / ATT_TC_ROWS;
-  const int step_rows = attention_item_rows(c->cfg.dtype == POLESTAR_BF16, c->dh, items128, c->H, true);
+  const int step_rows = attention_item_rows(c->cfg.dtype == POLESTAR_BF16, c->dh, items128, c->H, true, true);
   for (int s = 0; s < b; ++s)
     nwk = attention_items(work_h, nwk, s * B, B, win_row[s] >= 0 ? win_row[s] : 0, win_row[s] >= 0 ? c->nw + c->K : 0,
                           step_rows);
@@ -850,18 +906,44 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       aa.active_prev = c->aprev;
       aa.active_prev_lse = c->aprev_lse;
     }
+    // drift deferred to the pass below: the attention writes the tracked rows'
+    // new scores, the drift pass compares them with the stored ones and
+    // replaces those
     aa.measure = 1;
     aa.store = 1;
+    aa.proxy_new = c->pnew;
+    aa.proxy_new_lse = c->pnew_lse;
+    aa.active_new = c->anew;
+    aa.active_new_lse = c->anew_lse;
     aa.kl_out = c->kl_rows;
     aa.work = meta_d<int4>(c, c->ml.work_off);
     aa.n_work = nwk;
     aa.item_rows = step_rows;
-    const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz +
-                              (double)n_fire * c->K * c->H * N * 8.0 +
-                              (l == L - 1 ? (double)b * B * c->H * N * 8.0 : 0.0);
+    const double tracked_keys = (double)n_fire * c->K * c->H * N + (l == L - 1 ? (double)b * B * c->H * N : 0.0);
+    const double attn_bytes = (double)b * N * 2 * c->kvdim * c->esz + tracked_keys * 4.0;
     aa.batch = b;
     aa.err = tc_error_word(&c->tc);
-    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 0.0, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
+    RUN(POLESTAR_KC_ATTENTION, attn_bytes, 4.0 * R * N * c->qdim, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
+    {
+      DriftArgs da{};
+      da.track = meta_d<int4>(c, c->ml.track_off);
+      da.n_track = n_fire * c->K + (l == L - 1 ? b * B : 0);
+      da.H = c->H;
+      da.N = N;
+      da.K = c->K;
+      da.B = B;
+      da.proxy_prev = aa.proxy_prev;
+      da.proxy_prev_lse = aa.proxy_prev_lse;
+      da.active_prev = c->aprev;
+      da.active_prev_lse = c->aprev_lse;
+      da.proxy_new = c->pnew;
+      da.proxy_new_lse = c->pnew_lse;
+      da.active_new = c->anew;
+      da.active_new_lse = c->anew_lse;
+      da.kl_out = c->kl_rows;
+      da.store = 1;
+      RUN(POLESTAR_KC_ATTENTION, tracked_keys * 12.0, 0.0, (launch_drift(da, c->sm)));
+    }
     SelectArgs sa{};
     sa.batch = b;
     sa.Wmax = c->Wmax;
@@ -997,6 +1079,10 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
     TRY(dalloc(c, &c->pprev_lse, sizeof(float) * (size_t)L * b * K * H));
     TRY(dalloc(c, &c->aprev, sizeof(float) * (size_t)b * B * H * N));
     TRY(dalloc(c, &c->aprev_lse, sizeof(float) * (size_t)b * B * H));
+    TRY(dalloc(c, &c->pnew, sizeof(float) * (size_t)b * K * H * N));
+    TRY(dalloc(c, &c->pnew_lse, sizeof(float) * (size_t)b * K * H));
+    TRY(dalloc(c, &c->anew, sizeof(float) * (size_t)b * B * H * N));
+    TRY(dalloc(c, &c->anew_lse, sizeof(float) * (size_t)b * B * H));
     TRY(dalloc(c, &c->theta, sizeof(float) * (size_t)b * B * std::max(1, cfg->hist)));
     TRY(dalloc(c, &c->theta_n, sizeof(int) * (size_t)b * B));
     CUDA_OR_FAIL(c, cudaMemset(c->theta_n, 0, sizeof(int) * (size_t)b * B));
@@ -1017,6 +1103,11 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
     TRY(dalloc(c, &c->attn_out, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->write_kv, (size_t)R));
     TRY(dalloc(c, &c->U, sizeof(float) * (size_t)b * Wmax * d));
+    TRY(dalloc(c, &c->act_last, sizeof(float) * (size_t)b * B * d));
+    TRY(dalloc(c, &c->dec_rows, c->esz * (size_t)b * 2 * B * d));
+    TRY(dalloc(c, &c->dec_ids, sizeof(int) * (size_t)b * 2 * B));
+    TRY(dalloc(c, &c->dec_counts, sizeof(int) * 2 * (size_t)b));
+    TRY(halloc(c, &c->dec_counts_h, sizeof(int) * 2 * (size_t)b));
     TRY(dalloc(c, &c->dn, sizeof(float) * (size_t)b * Wmax * d));
     TRY(dalloc(c, &c->sel_a, (size_t)b * Wmax));
     TRY(dalloc(c, &c->sel_b, (size_t)b * Wmax));
@@ -1090,6 +1181,7 @@ extern "C" polestar_status polestar_calibrate_step(polestar_ctx* c, const void* 
   c->cur_block = block_index;
   c->cur_entry = block_entry ? 1 : 0;
   c->stepped = 1;
+  c->committed = 0;
   if (out) {
     out->drift = c->drift;
     out->topk = c->topk_out;
@@ -1144,6 +1236,97 @@ extern "C" polestar_status polestar_commit(polestar_ctx* c, const float* logits,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("commit launch: ") + cudaGetErrorString(e));
   c->stepped = 0;
+  c->committed = 1;
+  return POLESTAR_OK;
+}
+
+// ------------------------------------------------------------------ closed-loop decoding
+namespace {
+template <typename T>
+polestar_status decode_logits_impl(polestar_ctx* c, const void* lm_head, const void* final_norm, int vocab,
+                                   float* logits) {
+  const int b = c->b, B = c->B, d = c->d;
+  DecodeRowsArgs a{};
+  a.act = c->cur_entry ? c->act_last : c->h_rows;
+  a.U = c->U;
+  a.sel = c->cur_entry ? nullptr : c->sel_last;
+  a.fire = meta_d<uint8_t>(c, c->ml.fire_off);
+  for (int i = 0; i < 64; ++i) a.suffix_widx[i] = -1;
+  for (int w = 0; w < c->nw; ++w) {
+    const int i = c->win_pos[w] - (c->start + B);
+    if (i >= 0 && i < B) a.suffix_widx[i] = w;
+  }
+  a.batch = b;
+  a.B = B;
+  a.d = d;
+  a.Wmax = c->Wmax;
+  a.N = c->N;
+  a.start = c->start;
+  a.gain = final_norm;
+  a.eps = c->cfg.rms_eps;
+  a.out = c->dec_rows;
+  RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_decode_rows<T>(a, c->sm)));
+  TRY(gemm<T>(c, c->dec_rows, d, lm_head, d, logits, vocab, b * 2 * B, nullptr, vocab, d));
+  return POLESTAR_OK;
+}
+}  // namespace
+
+extern "C" polestar_status polestar_decode_logits(polestar_ctx* c, const void* lm_head, const void* final_norm,
+                                                  int32_t vocab, float* logits) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!lm_head || !final_norm || !logits) return fail(c, POLESTAR_ERR_INVALID_ARG, "NULL buffer");
+  if (vocab < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "vocab must be >= 1");
+  if (c->B > 64) return fail(c, POLESTAR_ERR_UNSUPPORTED, "block size above 64");
+  if (!c->stepped) return fail(c, POLESTAR_ERR_STATE, "polestar_decode_logits needs a calibrate step not yet committed");
+  c->gemm_cls = c->cur_entry ? POLESTAR_KC_GEMM_ENTRY : POLESTAR_KC_GEMM_STEP;
+  return c->bf16 ? decode_logits_impl<__nv_bfloat16>(c, lm_head, final_norm, vocab, logits)
+                 : decode_logits_impl<float>(c, lm_head, final_norm, vocab, logits);
+}
+
+extern "C" polestar_status polestar_decode_tokens(polestar_ctx* c, const float* logits, int32_t vocab,
+                                                  uint8_t* commit_mask, int32_t* tokens, uint8_t* masked,
+                                                  int32_t* n_committed, int32_t* n_block_masked) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!logits || !commit_mask || !tokens || !masked || !n_committed || !n_block_masked)
+    return fail(c, POLESTAR_ERR_INVALID_ARG, "NULL buffer");
+  if (vocab < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "vocab must be >= 1");
+  if (!c->committed) return fail(c, POLESTAR_ERR_STATE, "polestar_decode_tokens needs a preceding polestar_commit");
+  const int b = c->b, B = c->B;
+  RUN(POLESTAR_KC_COMMIT, 0.0, 0.0, (launch_argmax(logits, vocab, b * 2 * B, c->dec_ids, c->sm)));
+  ApplyArgs a{};
+  a.commit = commit_mask;
+  a.conf = c->conf;
+  a.ids = c->dec_ids;
+  a.tokens = tokens;
+  a.masked = masked;
+  a.counts = c->dec_counts;
+  a.batch = b;
+  a.B = B;
+  a.N = c->N;
+  a.start = c->start;
+  RUN(POLESTAR_KC_COMMIT, 0.0, 0.0, (launch_apply_commits(a, c->sm)));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->dec_counts_h, c->dec_counts, sizeof(int) * 2 * b, cudaMemcpyDeviceToHost,
+                                  c->sm));
+  CUDA_OR_FAIL(c, cudaStreamSynchronize(c->sm));
+  for (int s = 0; s < b; ++s) {
+    n_committed[s] = c->dec_counts_h[2 * s];
+    n_block_masked[s] = c->dec_counts_h[2 * s + 1];
+  }
+  c->committed = 0;
+  return POLESTAR_OK;
+}
+
+extern "C" polestar_status polestar_embed(polestar_ctx* c, const void* embed, int32_t vocab, const void* mask_emb,
+                                          const int32_t* tokens, const uint8_t* masked, void* x0) {
+  if (!c) return POLESTAR_ERR_INVALID_ARG;
+  if (!embed || !mask_emb || !tokens || !masked || !x0) return fail(c, POLESTAR_ERR_INVALID_ARG, "NULL buffer");
+  if (vocab < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "vocab must be >= 1");
+  const int rows = c->b * c->N;
+  if (c->bf16)
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
+        (launch_embed<__nv_bfloat16>(embed, mask_emb, tokens, masked, vocab, rows, c->d, x0, c->sm)));
+  else
+    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_embed<float>(embed, mask_emb, tokens, masked, vocab, rows, c->d, x0, c->sm)));
   return POLESTAR_OK;
 }
 
@@ -1372,7 +1555,15 @@ extern "C" polestar_status polestar_profile_begin(polestar_ctx* c, int32_t capac
       return fail(c, POLESTAR_ERR_CUDA, std::string("cudaEventCreate: ") + cudaGetErrorString(e));
     }
   }
-  c->prof_rec.assign(capacity, {0, 0.0, 0.0});
+  c->prof_rec.assign(capacity, polestar_ctx::ProfRec{0, 0.0, 0.0});
+  {
+    cudaError_t e = cudaHostAlloc(&c->prof_rows, sizeof(int) * (size_t)capacity, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      c->prof_rows = nullptr;
+      prof_release(c);
+      return fail(c, POLESTAR_ERR_OOM, std::string("cudaHostAlloc: ") + cudaGetErrorString(e));
+    }
+  }
   c->prof_cap = capacity;
   c->prof_used = 0;
   for (auto& d : c->prof_dropped) d = 0;
@@ -1393,8 +1584,9 @@ extern "C" polestar_status polestar_profile_end(polestar_ctx* c, polestar_kernel
     CUDA_OR_FAIL(c, cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]));
     out[r.cls].launches += 1;
     out[r.cls].ms += ms;
-    out[r.cls].bytes += r.bytes;
-    out[r.cls].flops += r.flops;
+    const double rows = r.device_rows ? (double)std::min(std::max(c->prof_rows[i], 0), r.max_rows) : (double)r.max_rows;
+    out[r.cls].bytes += r.bytes + rows * r.row_bytes;
+    out[r.cls].flops += r.flops + rows * r.row_flops;
   }
   for (int k = 0; k < n_classes && k < POLESTAR_KC_COUNT; ++k) out[k].dropped = c->prof_dropped[k];
   prof_release(c);
@@ -1455,40 +1647,70 @@ extern "C" polestar_status polestar_debug_gemm_choice(int32_t M, int32_t nseg, c
   return tc_gemm_choice(&cache, M, nseg, N, K, out) == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }
 
-extern "C" polestar_status polestar_debug_attention(const void* q, const void* kv, int32_t N, int32_t H,
-                                                    int32_t Hkv, int32_t head_dim, int32_t R,
-                                                    const uint8_t* tracked, float* prev, float* prev_lse,
-                                                    int32_t measure, int32_t store, void* out, float* kl,
-                                                    int32_t dtype, void* stream) {
-  if (!q || !kv || !out || R < 1 || N < 1 || H < 1 || Hkv < 1 || H % Hkv) return POLESTAR_ERR_INVALID_ARG;
+namespace {
+polestar_status debug_attention(const void* q, const void* kv, int batch, int N, int H, int Hkv, int head_dim, int R,
+                                const uint8_t* tracked, float* prev, float* prev_lse, int measure, int store,
+                                void* out, float* kl, int dtype, cudaStream_t st) {
+  if (!q || !kv || !out || batch < 1 || R < 1 || N < 1 || H < 1 || Hkv < 1 || H % Hkv) return POLESTAR_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return POLESTAR_ERR_UNSUPPORTED;
   bool any_tracked = false;
   for (int r = 0; tracked && r < R; ++r) any_tracked |= tracked[r] != 0;
   if (any_tracked && (!prev || !prev_lse || (measure && !kl))) return POLESTAR_ERR_INVALID_ARG;
-  cudaStream_t st = (cudaStream_t)stream;
-  std::vector<int4> rows(R), work;
-  for (int r = 0; r < R; ++r)
-    rows[r] = make_int4(0, 0, (tracked && tracked[r]) ? ROW_ACTIVE : ROW_OTHER, r);
-  const int item_rows = attention_item_rows(dtype == POLESTAR_BF16, head_dim, (R + ATT_TC_ROWS - 1) / ATT_TC_ROWS, H,
-                                            any_tracked && measure);
-  work.resize((R + item_rows - 1) / item_rows);
-  work.resize(attention_items(work.data(), 0, 0, R, 0, 0, item_rows));
+  const size_t rows_total = (size_t)batch * R;
+  std::vector<int4> rows(rows_total), work;
+  for (int s = 0; s < batch; ++s)
+    for (int r = 0; r < R; ++r)
+      rows[(size_t)s * R + r] = make_int4(s, 0, (tracked && tracked[r]) ? ROW_ACTIVE : ROW_OTHER, r);
+  const int item_rows = attention_item_rows(dtype == POLESTAR_BF16, head_dim,
+                                            (long long)batch * ((R + ATT_TC_ROWS - 1) / ATT_TC_ROWS), H,
+                                            any_tracked && measure, true);
+  work.resize((size_t)batch * ((R + item_rows - 1) / item_rows));
+  int nw = 0;
+  for (int s = 0; s < batch; ++s) nw = attention_items(work.data(), nw, s * R, R, 0, 0, item_rows);
+  work.resize(nw);
   int4* d_rows = nullptr;
   int4* d_work = nullptr;
-  if (cudaMalloc(&d_rows, sizeof(int4) * R) != cudaSuccess) return POLESTAR_ERR_OOM;
+  if (cudaMalloc(&d_rows, sizeof(int4) * rows_total) != cudaSuccess) return POLESTAR_ERR_OOM;
   if (cudaMalloc(&d_work, sizeof(int4) * work.size()) != cudaSuccess) {
     cudaFree(d_rows);
     return POLESTAR_ERR_OOM;
   }
-  cudaMemcpy(d_rows, rows.data(), sizeof(int4) * R, cudaMemcpyHostToDevice);
+  cudaMemcpy(d_rows, rows.data(), sizeof(int4) * rows_total, cudaMemcpyHostToDevice);
   cudaMemcpy(d_work, work.data(), sizeof(int4) * work.size(), cudaMemcpyHostToDevice);
+  // drift measured as in the layer loop: the attention writes the tracked rows'
+  // new scores, the drift pass compares them with prev and replaces those
+  const bool defer = any_tracked && measure;
+  std::vector<int4> track;
+  if (defer)
+    for (int s = 0; s < batch; ++s)
+      for (int r = 0; r < R; ++r)
+        if (tracked[r]) track.push_back(make_int4(s * R + r, s, ROW_ACTIVE, r));
+  float* d_new = nullptr;
+  float* d_new_lse = nullptr;
+  int4* d_track = nullptr;
+  auto release = [&]() {
+    cudaFree(d_rows);
+    cudaFree(d_work);
+    if (d_new) cudaFree(d_new);
+    if (d_new_lse) cudaFree(d_new_lse);
+    if (d_track) cudaFree(d_track);
+  };
+  if (defer) {
+    if (cudaMalloc(&d_new, sizeof(float) * rows_total * H * N) != cudaSuccess ||
+        cudaMalloc(&d_new_lse, sizeof(float) * rows_total * H) != cudaSuccess ||
+        cudaMalloc(&d_track, sizeof(int4) * track.size()) != cudaSuccess) {
+      release();
+      return POLESTAR_ERR_OOM;
+    }
+    cudaMemcpy(d_track, track.data(), sizeof(int4) * track.size(), cudaMemcpyHostToDevice);
+  }
   AttnArgs a{};
   a.q = q;
   a.ldq = H * head_dim;
   a.rows = d_rows;
-  a.R = R;
+  a.R = (int)rows_total;
   a.kv_layer = kv;
-  a.kv_seq_stride = 0;
+  a.kv_seq_stride = (size_t)N * 2 * Hkv * head_dim;
   a.kvdim = Hkv * head_dim;
   a.N = N;
   a.H = H;
@@ -1508,13 +1730,52 @@ extern "C" polestar_status polestar_debug_attention(const void* q, const void* k
   a.work = d_work;
   a.n_work = (int)work.size();
   a.item_rows = item_rows;
-  a.batch = 1;
+  a.batch = batch;
+  if (defer) {
+    a.active_new = d_new;
+    a.active_new_lse = d_new_lse;
+  }
   cudaError_t e = dtype == POLESTAR_BF16 ? launch_row_attention<__nv_bfloat16>(a, st) : launch_row_attention<float>(a, st);
   if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess && defer) {
+    DriftArgs da{};
+    da.track = d_track;
+    da.n_track = (int)track.size();
+    da.H = H;
+    da.N = N;
+    da.K = 1;
+    da.B = R;
+    da.active_prev = prev;
+    da.active_prev_lse = prev_lse;
+    da.active_new = d_new;
+    da.active_new_lse = d_new_lse;
+    da.kl_out = kl;
+    da.store = store;
+    launch_drift(da, st);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  cudaFree(d_rows);
-  cudaFree(d_work);
+  release();
   return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" polestar_status polestar_debug_attention(const void* q, const void* kv, int32_t N, int32_t H,
+                                                    int32_t Hkv, int32_t head_dim, int32_t R,
+                                                    const uint8_t* tracked, float* prev, float* prev_lse,
+                                                    int32_t measure, int32_t store, void* out, float* kl,
+                                                    int32_t dtype, void* stream) {
+  return debug_attention(q, kv, 1, N, H, Hkv, head_dim, R, tracked, prev, prev_lse, measure, store, out, kl, dtype,
+                         (cudaStream_t)stream);
+}
+
+extern "C" polestar_status polestar_debug_attention_batch(const void* q, const void* kv, int32_t batch, int32_t N,
+                                                          int32_t H, int32_t Hkv, int32_t head_dim, int32_t R,
+                                                          const uint8_t* tracked, float* prev, float* prev_lse,
+                                                          int32_t measure, int32_t store, void* out, float* kl,
+                                                          int32_t dtype, void* stream) {
+  return debug_attention(q, kv, batch, N, H, Hkv, head_dim, R, tracked, prev, prev_lse, measure, store, out, kl, dtype,
+                         (cudaStream_t)stream);
 }
 
 extern "C" int32_t polestar_debug_window(int32_t prompt_len, int32_t gen_len, int32_t block, int32_t prefix_win,

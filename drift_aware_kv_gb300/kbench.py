@@ -69,6 +69,8 @@ def bench_gemm(a):
 
 
 def bench_attn(a):
+    if a.batch > 1:
+        return bench_attn_batch(a)
     from drift_aware_kv_gb300 import polestar as P
     g = torch.Generator(device="cuda").manual_seed(0)
     dh = a.dh
@@ -85,6 +87,28 @@ def bench_attn(a):
     byts = a.N * 2 * a.Hkv * dh * 2 + a.R * a.H * dh * 4 + a.tracked * a.H * a.N * 8
     return dict(kernel="attention", impl=getattr(a, "impl", 0), R=a.R, N=a.N, H=a.H, Hkv=a.Hkv, us=ms * 1e3, GBps=byts / ms / 1e6,
                 TFLOPs=4 * a.R * a.N * a.H * dh / ms / 1e9)
+
+
+def bench_attn_batch(a):
+    """The layer loop's launch shape: `batch` sequences of R rows (the last
+    `tracked` of each with KL drift) over N keys each, one launch."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cuda").manual_seed(0)
+    dh, S = a.dh, a.batch
+    q = (1.6 * torch.randn(S * a.R, a.H * dh, device="cuda", generator=g)).to(torch.bfloat16)
+    kv = (1.6 * torch.randn(S, a.N, 2, a.Hkv * dh, device="cuda", generator=g)).to(torch.bfloat16)
+    tracked = [r >= a.R - a.tracked for r in range(a.R)]
+    prev = torch.zeros(S * a.R, a.H, a.N, device="cuda")
+    plse = torch.zeros(S * a.R, a.H, device="cuda")
+    out = torch.empty(S * a.R, a.H * dh, dtype=torch.bfloat16, device="cuda")
+    kl = torch.empty(S * a.R, a.H, device="cuda")
+    P.attention_impl(getattr(a, "impl", 0))
+    P.debug_attention_batch(q, kv, a.H, a.Hkv, tracked, prev, plse, 0, 1, out, kl)
+    ms = _time(lambda: P.debug_attention_batch(q, kv, a.H, a.Hkv, tracked, prev, plse, 1, 1, out, kl), a.iters)
+    byts = S * (a.N * 2 * a.Hkv * dh * 2 + a.R * a.H * dh * 4 + a.tracked * a.H * a.N * 8)
+    return dict(kernel="attention", impl=getattr(a, "impl", 0), batch=S, R=a.R, N=a.N, H=a.H, Hkv=a.Hkv,
+                us=ms * 1e3, GBps=byts / ms / 1e6, TFLOPs=4 * S * a.R * a.N * a.H * dh / ms / 1e9,
+                note="includes the hook's host-side table build and a stream synchronise per call")
 
 
 def bench_kmeans(a):
@@ -152,6 +176,7 @@ def main():
     ap.add_argument("--impl", type=int, default=0,
                     help="attention kernel: 0 library's choice, 1 pipelined mma.sync, 2 tcgen05")
     ap.add_argument("--R", type=int, default=136)
+    ap.add_argument("--batch", type=int, default=1, help="attention: sequences in one launch")
     ap.add_argument("--H", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=32)
     ap.add_argument("--dh", type=int, default=128)

@@ -30,7 +30,8 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_kv_staleness", "polestar_cache_staleness", "polestar_debug_attention_items",
             "polestar_debug_window", "polestar_debug_trigger", "polestar_debug_stalled_wait",
             "polestar_codec_bytes", "polestar_codec_encode", "polestar_codec_decode",
-            "polestar_debug_write", "polestar_debug_enter_block")
+            "polestar_debug_write", "polestar_debug_enter_block", "polestar_decode_logits",
+            "polestar_decode_tokens", "polestar_embed", "polestar_debug_attention_batch")
 CODECS = {"fp16": 0, "fp8": 1, "int8": 2, "mxfp4": 3, "int2": 4, "nvfp4": 5}
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
@@ -81,6 +82,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                             C.POINTER(polestar_step_out)]
     lib.polestar_commit.argtypes = [P, P, C.c_int32, P, P, P]
     lib.polestar_step_host.argtypes = [P, P, C.POINTER(C.c_int32), C.c_int32, C.c_int32, P, C.c_int32, P, P]
+    lib.polestar_decode_logits.argtypes = [P, P, P, C.c_int32, P]
+    lib.polestar_decode_tokens.argtypes = [P, P, C.c_int32, P, P, P, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
+    lib.polestar_embed.argtypes = [P, P, C.c_int32, P, P, P, P]
     lib.polestar_release.argtypes = [P]
     lib.polestar_release.restype = None
     lib.polestar_last_error.argtypes = [P]
@@ -201,6 +205,33 @@ class Polestar:
                                         C.c_void_p(commit_mask_u8.data_ptr()),
                                         C.c_void_p(conf.data_ptr()) if conf is not None else None),
                self.ctx)
+
+    def decode_logits(self, lm_head, final_norm, logits):
+        """LM-head logits [batch, 2B, vocab] (fp32, written) of the rows the commit
+        gate scores for the step just calibrated (polestar_decode_logits)."""
+        _check(self.lib.polestar_decode_logits(self.ctx, C.c_void_p(lm_head.data_ptr()),
+                                               C.c_void_p(final_norm.data_ptr()), int(lm_head.shape[0]),
+                                               C.c_void_p(logits.data_ptr())), self.ctx)
+
+    def decode_tokens(self, logits, commit_mask_u8, tokens_i32, masked_u8):
+        """Greedy tokens into the committed positions after the progress rule
+        (polestar_decode_tokens); returns (tokens committed this step, active-block
+        positions still masked), one list entry per sequence."""
+        b = self.w.batch
+        cnt = (C.c_int32 * b)()
+        left = (C.c_int32 * b)()
+        _check(self.lib.polestar_decode_tokens(self.ctx, C.c_void_p(logits.data_ptr()), int(logits.shape[-1]),
+                                               C.c_void_p(commit_mask_u8.data_ptr()),
+                                               C.c_void_p(tokens_i32.data_ptr()),
+                                               C.c_void_p(masked_u8.data_ptr()), cnt, left), self.ctx)
+        return [int(v) for v in cnt], [int(v) for v in left]
+
+    def embed(self, embedding, mask_emb, tokens_i32, masked_u8, x0):
+        """Layer-0 inputs x0 [batch, N, d] from the tokens and the mask
+        (polestar_embed)."""
+        _check(self.lib.polestar_embed(self.ctx, C.c_void_p(embedding.data_ptr()), int(embedding.shape[0]),
+                                       C.c_void_p(mask_emb.data_ptr()), C.c_void_p(tokens_i32.data_ptr()),
+                                       C.c_void_p(masked_u8.data_ptr()), C.c_void_p(x0.data_ptr())), self.ctx)
 
     def step_host(self, x0_host, n_unmasked, block_index, block_entry, logits_host, masked_host,
                   commit_host):
@@ -342,6 +373,23 @@ def debug_attention(q, kv, H, Hkv, tracked, prev, prev_lse, measure, store, out,
     _check(lib.polestar_debug_attention(_ptr(q), _ptr(kv), N, H, Hkv, dh, R, tr, _ptr(prev), _ptr(prev_lse),
                                         int(measure), int(store), _ptr(out), _ptr(kl), dt,
                                         C.c_void_p(st.cuda_stream)))
+
+
+def debug_attention_batch(q, kv, H, Hkv, tracked, prev, prev_lse, measure, store, out, kl, stream=None):
+    """The same over kv [batch, N, 2, Hkv*dh] and q [batch * R, H*dh] in one
+    launch; tracked has R entries (the same rows of every sequence); see
+    polestar_debug_attention_batch."""
+    import torch
+    lib = load()
+    batch, N = kv.shape[0], kv.shape[1]
+    R = q.shape[0] // batch
+    dh = q.shape[1] // H
+    st = stream if stream is not None else torch.cuda.current_stream()
+    tr = (C.c_uint8 * R)(*[int(bool(v)) for v in tracked])
+    dt = BF16 if q.dtype == torch.bfloat16 else FP32
+    _check(lib.polestar_debug_attention_batch(_ptr(q), _ptr(kv), batch, N, H, Hkv, dh, R, tr, _ptr(prev),
+                                              _ptr(prev_lse), int(measure), int(store), _ptr(out), _ptr(kl), dt,
+                                              C.c_void_p(st.cuda_stream)))
 
 
 def debug_kmeans(Hw, K, iters, seed, block, stream=None):

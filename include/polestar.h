@@ -132,6 +132,65 @@ polestar_status polestar_calibrate_step(polestar_ctx *ctx, const void *x0, const
 polestar_status polestar_commit(polestar_ctx *ctx, const float *logits, int32_t vocab,
                                 const uint8_t *masked, uint8_t *commit_mask, float *conf);
 
+/* ---- closed-loop decoding (Algorithm 1 in full; Eq. 1; App. D.1) ----
+ *
+ * The three calls that close the loop around polestar_calibrate_step and
+ * polestar_commit, so that a whole generation runs on the device:
+ *
+ *   polestar_embed(x0) -> polestar_calibrate_step -> polestar_decode_logits
+ *     -> polestar_commit -> polestar_decode_tokens -> (next step)
+ *
+ * polestar_decode_logits: logits of the 2*block rows the commit gate scores,
+ * for the step just calibrated (between polestar_calibrate_step and
+ * polestar_commit).  Rows 0..B-1 of each sequence are the active block's
+ * last-layer outputs; rows B..2B-1 are the suffix block's update packets
+ * U(t, L) for the positions the last layer refreshed this step (a sequence
+ * whose sparse refresh ran), zero rows elsewhere (such rows cannot commit:
+ * Algorithm 1's suffix commit reads only refreshed rows).  Each row is
+ * RMS-normalised with final_norm (eps = cfg.rms_eps), rounded to the config
+ * dtype, and multiplied by the LM head:
+ *   lm_head     device [vocab, d] config dtype, 16-byte aligned (row-major,
+ *               one row per token id)
+ *   final_norm  device [d] config dtype
+ *   logits      device [batch, 2*block, vocab] fp32, written (the input of
+ *               polestar_commit)
+ * Needs block <= 64.  POLESTAR_ERR_STATE without a calibrated, uncommitted step.
+ *
+ * polestar_decode_tokens: after polestar_commit, the greedy tokens of Eq. 1
+ * (argmax over the vocabulary, ties to the lower id) are written into `tokens`
+ * at every committed position, which leaves the mask.  Before that, the
+ * progress rule: a step whose gate committed no token of the active block while
+ * some are still masked commits the masked one of highest confidence (ties to
+ * the lower position), so every step makes progress (the greedy fallback of
+ * the decoder Polestar builds on, App. D.1).
+ *   logits      device [batch, 2*block, vocab] fp32 (as given to commit)
+ *   commit_mask device [batch, 2*block] uint8: polestar_commit's output, updated
+ *               in place by the progress rule
+ *   tokens      device [batch, N] int32, updated at committed positions
+ *   masked      device [batch, N] uint8, 1 -> 0 at committed positions
+ *   n_committed host [batch], written: tokens committed this step (the
+ *               tokens-per-forward numerator of App. D.1)
+ *   n_block_masked host [batch], written: positions of the active block still
+ *               masked after this step (0 = the block is decoded)
+ * Synchronises the main stream (the counts come back to the host).
+ * POLESTAR_ERR_STATE unless polestar_commit ran since the last calibrate step.
+ *
+ * polestar_embed: layer-0 inputs of the next step, x0[s, p] = embed[tokens[s,
+ * p]] where masked[s, p] = 0, else mask_emb (the [MASK] embedding).  A token
+ * id outside [0, vocab) gives a zero row.
+ *   embed     device [vocab, d] config dtype
+ *   mask_emb  device [d] config dtype
+ *   tokens    device [batch, N] int32;  masked device [batch, N] uint8
+ *   x0        device [batch, N, d] config dtype, written
+ * All three run on the context's main stream; buffers are the caller's. */
+polestar_status polestar_decode_logits(polestar_ctx *ctx, const void *lm_head, const void *final_norm,
+                                       int32_t vocab, float *logits);
+polestar_status polestar_decode_tokens(polestar_ctx *ctx, const float *logits, int32_t vocab,
+                                       uint8_t *commit_mask, int32_t *tokens, uint8_t *masked,
+                                       int32_t *n_committed, int32_t *n_block_masked);
+polestar_status polestar_embed(polestar_ctx *ctx, const void *embed, int32_t vocab, const void *mask_emb,
+                               const int32_t *tokens, const uint8_t *masked, void *x0);
+
 /* End-to-end step on HOST buffers: copies x0 (host [batch, N, d], config dtype),
  * logits (host [batch, 2B, vocab] fp32) and masked (host [batch, N] uint8) to the
  * device on the main stream, runs polestar_calibrate_step + polestar_commit,
@@ -281,6 +340,14 @@ polestar_status polestar_debug_attention(const void *q, const void *kv, int32_t 
                                          int32_t head_dim, int32_t R, const uint8_t *tracked, float *prev,
                                          float *prev_lse, int32_t measure, int32_t store, void *out, float *kl,
                                          int32_t dtype, void *stream);
+/* The same for `batch` sequences of R rows each, in one launch (the layer
+ * loop's launch shape): q [batch * R, H*dh] (sequence-major), kv [batch, N, 2,
+ * Hkv*dh], out [batch * R, H*dh]; tracked (host, [R]) marks the same rows of
+ * every sequence; prev [batch * R, H, N], prev_lse / kl [batch * R, H]. */
+polestar_status polestar_debug_attention_batch(const void *q, const void *kv, int32_t batch, int32_t N, int32_t H,
+                                               int32_t Hkv, int32_t head_dim, int32_t R, const uint8_t *tracked,
+                                               float *prev, float *prev_lse, int32_t measure, int32_t store,
+                                               void *out, float *kl, int32_t dtype, void *stream);
 
 /* ---- attention kernel selection (test hook) ----
  * 0: the library's choice (the pipelined mma.sync kernel); 1: the mma.sync

@@ -96,6 +96,74 @@ def test_attention_and_kl_match_definition(R, N, H, Hkv, dh, dt, attention_kerne
     assert np.all(np.isnan(kl.cpu().numpy()[~tr]))
 
 
+@pytest.mark.parametrize("R,N,H,Hkv,dh,dt", [(136, 768, 32, 32, 128, torch.bfloat16),
+                                            (24, 192, 4, 4, 64, torch.float32)])
+def test_kl_large_drift_with_falling_log_sum_exp(R, N, H, Hkv, dh, dt, attention_kernel):
+    """Eq. 4 where the new scores fall far below the previous ones (peaky
+    previous queries, flat new ones): sum_j q_j e^(d_j) is then close to zero and
+    1 + sum_j q_j expm1(d_j) cancels; KL still within 1e-5 + 1e-3 rel of the
+    definition.  Also the closed form: previous scores = new scores + 15 (a
+    shifted copy of the same distribution) gives KL = 0."""
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator().manual_seed(R + 7 * N)
+    q1 = (6.0 * torch.randn(R, H * dh, generator=g)).to(dt)
+    q2 = (0.3 * torch.randn(R, H * dh, generator=g)).to(dt)
+    kv = (1.6 * torch.randn(N, 2, Hkv * dh, generator=g)).to(dt)
+    tracked = [True] * R
+    prev = torch.zeros(R, H, N, device="cuda")
+    plse = torch.zeros(R, H, device="cuda")
+    out = torch.empty(R, H * dh, dtype=dt, device="cuda")
+    kl = torch.empty(R, H, device="cuda")
+    kvg = kv.cuda()
+    P.debug_attention(q1.cuda(), kvg, H, Hkv, tracked, prev, plse, 0, 1, out, kl)
+    P.debug_attention(q2.cuda(), kvg, H, Hkv, tracked, prev, plse, 1, 0, out, kl)
+    s1, lse1, _ = _oracle_attention(q1, kv, H, Hkv)
+    s2, lse2, _ = _oracle_attention(q2, kv, H, Hkv)
+    assert np.min(lse1 - lse2) > 1.0  # the regime under test
+    kl_o = O.kl_div(s2, lse2, s1, lse1)
+    kl_g = kl.cpu().numpy()
+    err = np.abs(kl_g - kl_o)
+    assert np.all(err <= 1e-5 + 1e-3 * np.abs(kl_o)), (err.max(), kl_o.flat[np.argmax(err)])
+    # shifted copy: q2's own scores + 15 as the previous scores
+    P.debug_attention(q2.cuda(), kvg, H, Hkv, tracked, prev, plse, 0, 1, out, kl)
+    prev += 15.0
+    plse += 15.0
+    P.debug_attention(q2.cuda(), kvg, H, Hkv, tracked, prev, plse, 1, 0, out, kl)
+    k0 = kl.cpu().numpy()
+    assert np.all(np.abs(k0) <= 1e-4), np.abs(k0).max()
+
+
+def test_batched_attention_matches_definition():
+    """polestar_debug_attention_batch (three sequences of 100 rows, one launch,
+    the layer loop's launch shape) against the definition per sequence."""
+    from drift_aware_kv_gb300 import polestar as P
+    S, R, N, H, Hkv, dh = 3, 100, 700, 8, 2, 128
+    g = torch.Generator().manual_seed(99)
+    q1 = (1.6 * torch.randn(S * R, H * dh, generator=g)).to(torch.bfloat16)
+    q2 = (q1.float() + 0.2 * torch.randn(S * R, H * dh, generator=g)).to(torch.bfloat16)
+    kv = (1.6 * torch.randn(S, N, 2, Hkv * dh, generator=g)).to(torch.bfloat16)
+    tracked = [r % 4 == 1 for r in range(R)]
+    prev = torch.zeros(S * R, H, N, device="cuda")
+    plse = torch.zeros(S * R, H, device="cuda")
+    out = torch.empty(S * R, H * dh, dtype=torch.bfloat16, device="cuda")
+    kl = torch.full((S * R, H), float("nan"), device="cuda")
+    kvg = kv.cuda()
+    P.debug_attention_batch(q1.cuda(), kvg, H, Hkv, tracked, prev, plse, 0, 1, out, kl)
+    P.debug_attention_batch(q2.cuda(), kvg, H, Hkv, tracked, prev, plse, 1, 1, out, kl)
+    got = out.double().cpu().numpy()
+    klg = kl.cpu().numpy()
+    tr = np.array(tracked)
+    for s in range(S):
+        rs = slice(s * R, (s + 1) * R)
+        s1, lse1, _ = _oracle_attention(q1[rs], kv[s], H, Hkv)
+        s2, lse2, o2 = _oracle_attention(q2[rs], kv[s], H, Hkv)
+        err = np.linalg.norm(got[rs] - o2, axis=1) / np.linalg.norm(o2, axis=1)
+        assert err.max() < 8e-3, (s, err.max())
+        kl_o = O.kl_div(s2, lse2, s1, lse1)[tr]
+        assert np.all(np.abs(klg[rs][tr] - kl_o) <= 1e-5 + 1e-3 * np.abs(kl_o)), s
+        assert np.all(np.isnan(klg[rs][~tr]))
+
+
 @pytest.mark.parametrize("P_,nw,d", [(32, 96, 4096), (4, 96, 3584), (3, 64, 256), (2, 70, 448)])
 def test_kmeans_nvfp4_match_oracle(P_, nw, d):
     from drift_aware_kv_gb300 import polestar as P
