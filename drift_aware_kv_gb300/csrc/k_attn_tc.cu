@@ -361,11 +361,20 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
     const float sl2 = p.scale * 1.4426950408889634f;
     float mrun = -INFINITY, l = 0.f;
     bool ok = true;
+    // a warp whose 32 rows all lie past the item's rows (items of fewer than
+    // 128 rows) only keeps pace with the tiles: its lanes' P and O are never
+    // read back, so it leaves the issue slots to the warps with rows
+    const bool wdead = !__any_sync(0xffffffffu, has);
     for (int j = 0; j < ntl && ok; ++j) {
       const int b = j & 1, j0 = j * TK;
       ok = mbar_wait(su32(&s_full[b]), (j >> 1) & 1, p.err, 26, abort_flag);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (!ok) break;
+      if (wdead) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(su32(&p_full[b]));
+        continue;
+      }
       // the row's scores of this tile: loads in flight together, one wait
       uint32_t sv[TK];
 #pragma unroll
@@ -373,16 +382,23 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
       tcgen05_wait_ld();
       // pass 1: scores in log2 units (keys past N at -inf), tile maximum over
       // eight independent chains
-      const bool fullt = j0 + TK <= p.N;
       float mx8[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
+      if (j0 + TK <= p.N) {
 #pragma unroll
-      for (int i = 0; i < TK; ++i) {
-        float v = __uint_as_float(sv[i]) * sl2;
-        if (!fullt && j0 + i >= p.N) v = -INFINITY;
-        sv[i] = __float_as_uint(v);
-        mx8[i & 7] = fmaxf(mx8[i & 7], v);
+        for (int i = 0; i < TK; ++i) {
+          const float v = __uint_as_float(sv[i]) * sl2;
+          sv[i] = __float_as_uint(v);
+          mx8[i & 7] = fmaxf(mx8[i & 7], v);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < TK; ++i) {
+          const float v = j0 + i < p.N ? __uint_as_float(sv[i]) * sl2 : -INFINITY;
+          sv[i] = __float_as_uint(v);
+          mx8[i & 7] = fmaxf(mx8[i & 7], v);
+        }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
