@@ -380,28 +380,23 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < TK / 32; ++c) tmem_ld32_nw(tl + b * TK + c * 32, sv + c * 32);
       tcgen05_wait_ld();
-      // pass 1: scores in log2 units (keys past N at -inf), tile maximum over
-      // eight independent chains
+      // pass 1: tile maximum of the raw scores (keys past N at -inf) over eight
+      // independent chains; the scale (> 0) applies after the maximum
       float mx8[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
       if (j0 + TK <= p.N) {
 #pragma unroll
-        for (int i = 0; i < TK; ++i) {
-          const float v = __uint_as_float(sv[i]) * sl2;
-          sv[i] = __float_as_uint(v);
-          mx8[i & 7] = fmaxf(mx8[i & 7], v);
-        }
+        for (int i = 0; i < TK; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
       } else {
 #pragma unroll
         for (int i = 0; i < TK; ++i) {
-          const float v = j0 + i < p.N ? __uint_as_float(sv[i]) * sl2 : -INFINITY;
-          sv[i] = __float_as_uint(v);
-          mx8[i & 7] = fmaxf(mx8[i & 7], v);
+          if (j0 + i >= p.N) sv[i] = __float_as_uint(-INFINITY);
+          mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
         }
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mx = sl2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));  // log2 units
       // raise the running maximum only when it grows by more than 8 (p <= 2^8)
       const bool raise = mx > mrun + 8.f;
       const float mnew = raise ? mx : mrun;
@@ -439,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
           float pv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            pv[e] = ex2f(__uint_as_float(sv[g * 4 + e]) - mrun);  // exp2(-inf) = 0 past N
+            pv[e] = ex2f(fmaf(__uint_as_float(sv[g * 4 + e]), sl2, -mrun));  // exp2(-inf) = 0 past N
             l4[e] += pv[e];
           }
           pk[2 * gg] = pack2(pv[0], pv[1]);
@@ -448,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
             const int jj = j0 + g * 4;
             float sn[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sn[e] = __uint_as_float(sv[g * 4 + e]) * 0.6931471805599453f;
+            for (int e = 0; e < 4; ++e) sn[e] = __uint_as_float(sv[g * 4 + e]) * p.scale;
             if (vec_sc && jj + 3 < p.N) {
               *(float4*)(sdst + jj) = make_float4(sn[0], sn[1], sn[2], sn[3]);
             } else {
