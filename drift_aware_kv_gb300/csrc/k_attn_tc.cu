@@ -46,7 +46,8 @@ namespace at {
 constexpr int ROWS = 128;   // rows per work item (MMA M)
 constexpr int TK = 64;      // keys per tile (MMA N of S, K of P V)
 constexpr int DH = 128;     // head dim
-constexpr int THREADS = 192;
+constexpr int SOFT_WARPS = 8;                 // two warps per TMEM lane quarter, each half of a tile's keys
+constexpr int THREADS = (2 + SOFT_WARPS) * 32;
 constexpr int STAGES = 2;
 constexpr int QBOX = 64 * ROWS * 2;           // 64 columns x 128 rows (Q)
 constexpr int KBOX = 64 * TK * 2;             // 64 columns x 64 keys (K, V)
@@ -56,7 +57,8 @@ constexpr int STAGE_BYTES = 4 * KBOX;
 constexpr int O_COL = 2 * TK;                 // TMEM: S/P buffers at 0 and TK, O after
 constexpr int TMEM_COLS = O_COL + DH;         // 256
 constexpr int CTL_OFF = RING_OFF + STAGES * STAGE_BYTES;
-constexpr int SMEM_BYTES = CTL_OFF + 256 + 1024;  // + control block + alignment
+constexpr int XCH_OFF = CTL_OFF + 256;          // [2 tile parities][2 halves][ROWS] partial maxima, then [2][ROWS] sums
+constexpr int SMEM_BYTES = XCH_OFF + 6 * ROWS * 4 + 1024;  // + alignment
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s
 static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
 
@@ -229,10 +231,10 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(su32(&s_full[b]), 1);
-      mbar_init(su32(&p_full[b]), 4);
+      mbar_init(su32(&p_full[b]), SOFT_WARPS);
       mbar_init(su32(&pv_done[b]), 1);
     }
-    mbar_init(su32(q_full), 4);
+    mbar_init(su32(q_full), SOFT_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -304,10 +306,16 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
       if (live && ntl > 0) issue_pv(ntl - 1);
     }
   } else {
-    // ---------------- softmax / epilogue: row r = TMEM lane
+    // ---------------- softmax / epilogue: row r = TMEM lane; the warp pair of
+    // a lane quarter splits each tile's 64 keys (half = 0: keys 0-31, 1: 32-63)
+    // and the output's 128 columns
     const int qd = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = qd * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+    float* xmax = (float*)(sm + XCH_OFF);  // [2][2][ROWS]
+    float* xsum = xmax + 4 * ROWS;         // [2][ROWS]
+    const uint32_t pair_bar = 1 + qd;      // named barrier of the warp pair (64 threads)
     const bool has = r < nrows;
     const int row = has ? item_row(wk, r) : item_row(wk, 0);
     int4 m = make_int4(0, 0, ROW_NONE, 0);
@@ -334,11 +342,13 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
 
     // 16-byte row accesses when the strides and bases allow them
     const bool vec_io = ((p.ldq | p.ldo) & 7) == 0 && ((((uintptr_t)p.q) | ((uintptr_t)p.out)) & 15) == 0;
-    // Q row into the swizzled A-operand tile (zeros for padding rows)
+    // this half's 64 Q columns of the row into the swizzled A-operand tile
+    // (zeros for padding rows)
     {
       const __nv_bfloat16* qrow = (const __nv_bfloat16*)p.q + (size_t)row * p.ldq + h * DH;
 #pragma unroll
-      for (int c = 0; c < DH / 8; ++c) {
+      for (int cc = 0; cc < DH / 16; ++cc) {
+        const int c = half * (DH / 16) + cc;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (live) {
           if (vec_io) {
@@ -361,84 +371,97 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
     const float sl2 = p.scale * 1.4426950408889634f;
     float mrun = -INFINITY, l = 0.f;
     bool ok = true;
-    // a warp whose 32 rows all lie past the item's rows (items of fewer than
-    // 128 rows) only keeps pace with the tiles: its lanes' P and O are never
-    // read back, so it leaves the issue slots to the warps with rows
+    // a warp pair whose 32 rows all lie past the item's rows (items of fewer
+    // than 128 rows) only keeps pace with the tiles: its lanes' P and O are
+    // never read back, so it leaves the issue slots to the warps with rows
     const bool wdead = !__any_sync(0xffffffffu, has);
-    for (int j = 0; j < ntl && ok; ++j) {
-      const int b = j & 1, j0 = j * TK;
-      ok = mbar_wait(su32(&s_full[b]), (j >> 1) & 1, p.err, 26, abort_flag);
+    for (int j = 0; j < ntl; ++j) {
+      const int b = j & 1, j0 = j * TK + half * 32;
+      // a failed wait anywhere is carried to the partner as a NaN maximum, and
+      // the pair leaves together after the exchange (never alone: the pair's
+      // named barrier would otherwise wait for a warp that left)
+      ok = ok && mbar_wait(su32(&s_full[b]), (j >> 1) & 1, p.err, 26, abort_flag);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      if (!ok) break;
       if (wdead) {
+        if (!ok) break;  // a dead pair exchanges nothing: each warp leaves on its own
         __syncwarp();
         if (lane == 0) mbar_arrive(su32(&p_full[b]));
         continue;
       }
-      // the row's scores of this tile: loads in flight together, one wait
-      uint32_t sv[TK];
+      // this half's 32 scores of the row, pass 1: their maximum (raw scores,
+      // keys past N at -inf) over eight independent chains
+      uint32_t sv[32];
+      float pmax = -INFINITY;
+      if (ok) {
+        tmem_ld32_nw(tl + b * TK + half * 32, sv);
+        tcgen05_wait_ld();
+        float mx8[8];
 #pragma unroll
-      for (int c = 0; c < TK / 32; ++c) tmem_ld32_nw(tl + b * TK + c * 32, sv + c * 32);
-      tcgen05_wait_ld();
-      // pass 1: tile maximum of the raw scores (keys past N at -inf) over eight
-      // independent chains; the scale (> 0) applies after the maximum
-      float mx8[8];
+        for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
+        if (j0 + 32 <= p.N) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
-      if (j0 + TK <= p.N) {
+          for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
+        } else {
 #pragma unroll
-        for (int i = 0; i < TK; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < TK; ++i) {
-          if (j0 + i >= p.N) sv[i] = __float_as_uint(-INFINITY);
-          mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
+          for (int i = 0; i < 32; ++i) {
+            if (j0 + i >= p.N) sv[i] = __float_as_uint(-INFINITY);
+            mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
+          }
         }
+        pmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      } else {
+        pmax = __int_as_float(0x7fc00000);  // NaN: this warp gave up
       }
-      const float mx = sl2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));  // log2 units
+      xmax[(b * 2 + half) * ROWS + r] = pmax;
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+      const float omax = xmax[(b * 2 + (half ^ 1)) * ROWS + r];
+      if (__any_sync(0xffffffffu, pmax != pmax || omax != omax)) {  // either warp gave up
+        ok = false;
+        break;
+      }
+      const float mx = sl2 * fmaxf(pmax, omax);  // log2 units; both halves compute the same value
       // raise the running maximum only when it grows by more than 8 (p <= 2^8)
       const bool raise = mx > mrun + 8.f;
       const float mnew = raise ? mx : mrun;
       const float corr = raise ? ex2f(mrun - mnew) : 1.f;  // exp2(-inf) = 0 on the first tile
       l *= corr;
-      // a raised maximum rescales the output, which must then hold P_{j-1} V_{j-1}
+      // a raised maximum rescales the output, which must then hold P_{j-1} V_{j-1};
+      // each half rescales its 64 output columns
       const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
       if (rescale) {
         const int t = j - 1;
         ok = mbar_wait(su32(&pv_done[t & 1]), (t >> 1) & 1, p.err, 27, abort_flag);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (!ok) break;
-        // output row rescale, four chunks of 32 columns
+        if (ok) {
 #pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32_nw(tl + O_COL + c * 32, v);
-          tcgen05_wait_ld();
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32_nw(tl + O_COL + half * 64 + c * 32, v);
+            tcgen05_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-          tmem_st32_nw(tl + O_COL + c * 32, v);
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+            tmem_st32_nw(tl + O_COL + half * 64 + c * 32, v);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       mrun = mnew;
-      // pass 2: probabilities as bf16 pairs (P, written over the score buffer),
-      // the running sum over four chains, and a tracked row's scores
-#pragma unroll
-      for (int hk = 0; hk < 2; ++hk) {  // two halves of 32 keys, 16 packed columns each
-        uint32_t pk[TK / 4];
+      if (ok) {
+        // pass 2: this half's probabilities as bf16 pairs (P, written over the
+        // score buffer), the running sum over four chains, a tracked row's scores
+        uint32_t pk[16];
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int gg = 0; gg < TK / 8; ++gg) {
-          const int g = hk * (TK / 8) + gg;
+        for (int g = 0; g < 8; ++g) {
           float pv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             pv[e] = ex2f(fmaf(__uint_as_float(sv[g * 4 + e]), sl2, -mrun));  // exp2(-inf) = 0 past N
             l4[e] += pv[e];
           }
-          pk[2 * gg] = pack2(pv[0], pv[1]);
-          pk[2 * gg + 1] = pack2(pv[2], pv[3]);
+          pk[2 * g] = pack2(pv[0], pv[1]);
+          pk[2 * g + 1] = pack2(pv[2], pv[3]);
           if (sdst) {
             const int jj = j0 + g * 4;
             float sn[4];
@@ -454,38 +477,46 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
           }
         }
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-        // keys 32 hk .. 32 hk + 31 as bf16 pairs: columns 16 hk .. 16 hk + 15 of the
-        // score buffer, whose scores are all in registers by now
-        tmem_st16_nw(tl + b * TK + hk * 16, pk);
+        // keys 32 half .. 32 half + 31 as bf16 pairs: columns 16 half .. 16 half + 15
+        // of the score buffer (this half's scores are all in registers by now; the
+        // partner writes the other 16 columns from its own registers)
+        tmem_st16_nw(tl + b * TK + half * 16, pk);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(su32(&p_full[b]));
       }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(su32(&p_full[b]));
     }
-    // ---------------- epilogue: O / l, log-sum-exp
+    // ---------------- epilogue: O / l (each half its 64 columns), log-sum-exp
     if (ok && ntl > 0) {
       ok = mbar_wait(su32(&pv_done[(ntl - 1) & 1]), ((ntl - 1) >> 1) & 1, p.err, 28, abort_flag);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     }
-    if (ok) {
+    if (!wdead) {
+      // the row's sum is the two halves' sums (same running maximum)
+      xsum[half * ROWS + r] = ok ? l : __int_as_float(0x7fc00000);
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+      const float lo = xsum[(half ^ 1) * ROWS + r];
+      if (lo != lo) ok = false;
+      l += lo;
+    }
+    if (ok && !wdead) {
       const float inv = 1.f / l;
       __nv_bfloat16* o = (__nv_bfloat16*)p.out + (size_t)row * p.ldo + h * DH;
 #pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t ov[64];
-        tmem_ld32_nw(tl + O_COL + hf * 64, ov);
-        tmem_ld32_nw(tl + O_COL + hf * 64 + 32, ov + 32);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ov[32];
+        tmem_ld32_nw(tl + O_COL + half * 64 + c * 32, ov);
         tcgen05_wait_ld();
         if (outp) {
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
+          for (int g = 0; g < 4; ++g) {
             const uint32_t* v = ov + g * 8;
             const uint4 w = make_uint4(pack2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
                                        pack2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
                                        pack2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
                                        pack2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
-            const int col = hf * 64 + g * 8;
+            const int col = half * 64 + c * 32 + g * 8;
             if (vec_io) {
               *(uint4*)(o + col) = w;
             } else {
@@ -499,7 +530,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
           }
         }
       }
-      if (ldst) *ldst = mrun * 0.6931471805599453f + logf(l);
+      if (ldst && half == 0) *ldst = mrun * 0.6931471805599453f + logf(l);
     }
   }
   if (*abort_flag && warp == 0 && lane == 0) {
