@@ -13,18 +13,21 @@
 //     sequence) x one query head; the item's Q rows are the MMA's M side
 //     (TMEM lane = row); keys come in tiles of 64.  Two CTAs share an SM (256
 //     TMEM columns and under half the shared memory each), so one SM runs
-//     eight softmax warps.
+//     sixteen softmax warps.
 //   * warp 0 streams K and V tiles with TMA (128-byte swizzled 64 x 64 boxes
-//     of the [batch*N, 2*kvdim] cache view) into a two-stage mbarrier ring;
+//     of the [batch*N, 2*kvdim] cache view) into a two-stage ring whose K and
+//     V halves have barriers of their own (K runs a tile ahead: K_j is free
+//     once S_j is done, V_j only after P_j V_j);
 //     warp 1 issues S_j = Q K_j^T into one of two TMEM score buffers and
 //     O += P_{j-1} V_{j-1} into the TMEM output, taking P straight from TMEM
 //     (the A operand), so the tensor cores compute tile j's scores while the
 //     softmax warps work on tile j-1;
-//   * warps 2-5 (one thread per row) read a row's 64 scores from TMEM, keep
-//     the running maximum (log2 units, eight independent chains per tile) and
-//     sum (four chains), and write P (bf16 pairs) back over the first half of
-//     the same score buffer; the running maximum is raised lazily (only when a
-//     tile's maximum exceeds it by more than 8, i.e. p <= 2^8), and then the
+//   * warps 2-9 (a warp pair per TMEM lane quarter, each thread half of its
+//     row's keys and output columns) read the row's scores from TMEM, keep the
+//     running maximum (log2 units; the pair exchanges tile maxima through
+//     shared memory) and sum, and write P (bf16 pairs) back over the first half
+//     of the same score buffer; the running maximum is raised lazily (only when
+//     a tile's maximum exceeds it by more than 8, i.e. p <= 2^8), and then the
 //     TMEM output row is rescaled before the next P V;
 //   * V is the second product's B operand read N-major (dh contiguous) from
 //     the swizzled boxes, so no transposition is needed.
@@ -210,9 +213,14 @@ __device__ __forceinline__ int item_row(const int4& wk, int lr) { return lr < wk
 __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, AttnArgs p) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-  uint64_t* kv_full = (uint64_t*)(sm + CTL_OFF);
-  uint64_t* kv_empty = kv_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;  // [2]
+  // K and V of a stage have barriers of their own: K_j is free once S_j is
+  // done, long before P_j V_j has read V_j, so the next K tiles stream in while
+  // the softmax still works on earlier tiles
+  uint64_t* k_full = (uint64_t*)(sm + CTL_OFF);
+  uint64_t* k_empty = k_full + STAGES;
+  uint64_t* v_full = k_empty + STAGES;
+  uint64_t* v_empty = v_full + STAGES;
+  uint64_t* s_full = v_empty + STAGES;   // [2]
   uint64_t* p_full = s_full + 2;         // [2]
   uint64_t* pv_done = p_full + 2;        // [2]: P V of tiles j with j % 2 == b
   uint64_t* q_full = pv_done + 2;
@@ -226,8 +234,10 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(su32(&kv_full[s]), 1);
-      mbar_init(su32(&kv_empty[s]), 1);
+      mbar_init(su32(&k_full[s]), 1);
+      mbar_init(su32(&k_empty[s]), 1);
+      mbar_init(su32(&v_full[s]), 1);
+      mbar_init(su32(&v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(su32(&s_full[b]), 1);
@@ -259,14 +269,21 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
   if (warp == 0) {
     // ---------------- loader: K then V boxes of each 64-key tile
     if (lane == 0) {
-      for (int j = 0; j < ntl; ++j) {
+      // K runs one tile ahead of V: K_{i+1}, then V_i
+      auto load = [&](int j, int w) -> bool {
         const int s = j % STAGES;
-        if (j >= STAGES && !mbar_wait(su32(&kv_empty[s]), ((j / STAGES) - 1) & 1, p.err, 21, abort_flag)) break;
-        const uint32_t fb = su32(&kv_full[s]);
-        mbar_expect_tx(fb, STAGE_BYTES);
-        const uint32_t dst = su32(sm + RING_OFF + s * STAGE_BYTES);
-        const int y = seq * p.N + j * TK;
-        tma_load_4d(dst, &tm_kv, 0, y, kvh * (DH / 64), 0, fb);  // K0, K1, V0, V1 boxes
+        uint64_t* empty = w ? v_empty : k_empty;
+        uint64_t* full = w ? v_full : k_full;
+        if (j >= STAGES && !mbar_wait(su32(&empty[s]), ((j / STAGES) - 1) & 1, p.err, 21, abort_flag)) return false;
+        mbar_expect_tx(su32(&full[s]), STAGE_BYTES / 2);
+        const uint32_t dst = su32(sm + RING_OFF + s * STAGE_BYTES + w * (STAGE_BYTES / 2));
+        tma_load_4d(dst, &tm_kv, 0, seq * p.N + j * TK, kvh * (DH / 64), w, su32(&full[s]));  // two 64-column boxes
+        return true;
+      };
+      bool go = ntl > 0 && load(0, 0);
+      for (int i = 0; i < ntl && go; ++i) {
+        if (i + 1 < ntl) go = load(i + 1, 0);
+        go = go && load(i, 1);
       }
     }
   } else if (warp == 1) {
@@ -276,6 +293,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
       bool live = mbar_wait(su32(q_full), 0, p.err, 22, abort_flag);
       auto issue_pv = [&](int t) -> bool {
         if (!mbar_wait(su32(&p_full[t & 1]), (t >> 1) & 1, p.err, 23, abort_flag)) return false;
+        if (!mbar_wait(su32(&v_full[t % STAGES]), (t / STAGES) & 1, p.err, 29, abort_flag)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t v = su32(sm + RING_OFF + (t % STAGES) * STAGE_BYTES + 2 * KBOX);
         const uint32_t pt = tmem + (t & 1) * TK;  // P_t: bf16 pairs in the first TK/2 columns of S_t's buffer
@@ -284,12 +302,12 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
           umma_ta(tmem + O_COL, pt + kk * 8, sdesc(v + kk * 16 * 128, KBOX, 1024), idesc(DH, true),
                   (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(su32(&pv_done[t & 1]));
-        umma_commit(su32(&kv_empty[t % STAGES]));
+        umma_commit(su32(&v_empty[t % STAGES]));
         return true;
       };
       for (int j = 0; j < ntl && live; ++j) {
         const int s = j % STAGES, b = j & 1;
-        if (!mbar_wait(su32(&kv_full[s]), (j / STAGES) & 1, p.err, 24, abort_flag)) break;
+        if (!mbar_wait(su32(&k_full[s]), (j / STAGES) & 1, p.err, 24, abort_flag)) break;
         // score buffer b holds P_{j-2} until P_{j-2} V_{j-2} has read it; that
         // product was issued before this one and the products run in order,
         // and the softmax has read S_{j-2} once it signalled P_{j-2}
@@ -301,6 +319,7 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
           umma(tmem + b * TK, sdesc(q + (kk >> 2) * QBOX + (kk & 3) * 32, 16, 1024),
                sdesc(kt + (kk >> 2) * KBOX + (kk & 3) * 32, 16, 1024), idesc(TK, false), kk > 0 ? 1u : 0u);
         umma_commit(su32(&s_full[b]));
+        umma_commit(su32(&k_empty[s]));
         if (j >= 1 && !issue_pv(j - 1)) live = false;
       }
       if (live && ntl > 0) issue_pv(ntl - 1);
@@ -548,9 +567,9 @@ __global__ void __launch_bounds__(THREADS, 2) attn_tc_kernel(const __grid_consta
 }
 // 4D tensor map of one layer's K/V cache ([batch*N rows][2 * kvdim] bf16, K
 // then V of each row) viewed as {64 columns, row, 64-column block of the K or
-// V half, K/V}: a box {64, TK, dh / 64, 2} at (0, row, head * dh / 64, 0) is one
-// head's K and V for TK keys, as 128-byte-swizzled [TK][64] boxes in the order
-// K block 0, K block 1, .., V block 0, ..  (cached per buffer and shape).
+// V half, K/V}: a box {64, TK, dh / 64, 1} at (0, row, head * dh / 64, w) is one
+// head's K (w = 0) or V (w = 1) for TK keys, as 128-byte-swizzled [TK][64]
+// boxes, one per 64-column block (cached per buffer and shape).
 const CUtensorMap* kv_map_tiles(const void* base, int rows, int kvdim, int dh) {
   static std::map<std::tuple<const void*, int, int, int>, CUtensorMap> cache;
   static std::mutex mu;
@@ -571,7 +590,7 @@ const CUtensorMap* kv_map_tiles(const void* base, int rows, int kvdim, int dh) {
   std::memset(&m, 0, sizeof(m));
   const cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(kvdim / 64), 2};
   const cuuint64_t strides[3] = {(cuuint64_t)kvdim * 4, 128, (cuuint64_t)kvdim * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)TK, (cuuint32_t)(dh / 64), 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)TK, (cuuint32_t)(dh / 64), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
