@@ -886,8 +886,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
       for (long long t = cid; t < ntiles && live; t += ncl) {
         const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
         const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
-        const int n0 = (nb - p.seg_start[sg]) * bn;
-        const CUtensorMap* tmB = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
+        // W rows of this CTA's half tile: rows n0 + rank bn/2 of segment sg, or
+        // in SwiGLU mode gate (rank 0) / up (rank 1) rows of act columns n0..
+        const CUtensorMap* tmB = p.act ? (rank == 0 ? &tmB0 : &tmB1) : (sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2));
+        const int wrow = p.act ? nb * (bn / 2) : (nb - p.seg_start[sg]) * bn + rank * (bn / 2);
         const int m0 = mp * 2 * BM + rank * BM;
         for (int k = 0; k < nk; ++k, ++it) {
           const int s = (int)(it % STAGES);
@@ -903,11 +905,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
           const uint32_t st = smem_u32(smem + (size_t)s * SB);
           if (KP == 1) {
             if (loads_a) tma_load_2d_pair(st, &tmA, k * BK, m0, fb);
-            if (loads_w) tma_load_2d_pair(st + A_BYTES, tmB, k * BK, n0 + rank * (bn / 2), fb);
+            if (loads_w) tma_load_2d_pair(st + A_BYTES, tmB, k * BK, wrow, fb);
           } else {
             // {column in the k-block, row, k-block}: KP consecutive k-blocks per box
             if (loads_a) tma_load_3d_pair(st, &tmA, 0, m0, k * KP, fb);
-            if (loads_w) tma_load_3d_pair(st + A_BYTES, tmB, 0, n0 + rank * (bn / 2), k * KP, fb);
+            if (loads_w) tma_load_3d_pair(st + A_BYTES, tmB, 0, wrow, k * KP, fb);
           }
         }
       }
@@ -972,6 +974,39 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
       const bool vseg = vec && ((((uintptr_t)Cseg) & 15) == 0);
       const int row = mp * 2 * BM + rank * BM + q * 32 + lane;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * bn);
+      if (p.act) {
+        // SwiGLU mode: gate in the accumulator's first bn/2 columns, up in the
+        // second; act[row, nb bn/2 + c] = bf16(silu(g) * u)
+        const int a0 = nb * (bn / 2), F = p.seg_N[0];
+        const bool va = ((p.ld_act & 7) == 0) && ((((uintptr_t)p.act) & 15) == 0);
+#pragma unroll 1
+        for (int c = 0; c < bn / 2; c += 16) {
+          float g[16], u[16];
+          tmem_ld16(tq + c, g);
+          tmem_ld16(tq + bn / 2 + c, u);
+          if (row < M_eff) {
+            __nv_bfloat16* dst = p.act + (size_t)row * p.ld_act + a0 + c;
+            if (a0 + c + 16 <= F && va) {
+              uint32_t w[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const __nv_bfloat162 v2 = __floats2bfloat162_rn(swiglu1(g[2 * j], u[2 * j]), swiglu1(g[2 * j + 1], u[2 * j + 1]));
+                w[j] = *(const uint32_t*)&v2;
+              }
+              *(uint4*)dst = make_uint4(w[0], w[1], w[2], w[3]);
+              *(uint4*)(dst + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (a0 + c + j < F) dst[j] = __float2bfloat16_rn(swiglu1(g[j], u[j]));
+            }
+          }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_acc_empty0 + (uint32_t)(b * 8));
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < bn; c += 16) {
         float v[16];
@@ -1601,13 +1636,54 @@ cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, cons
   const int Ns[2] = {F, F};
   GemmPick pk{1, 0, 1, 0};
   if (force && force->kernel) {
-    if (force->kernel != 1) return cudaErrorNotSupported;
+    if (force->kernel != 1 && force->kernel != 5) return cudaErrorNotSupported;
+    pk.kernel = force->kernel;
     pk.bn = force->bn;
-    pk.splits = force->splits ? force->splits : 1;
+    pk.splits = force->splits ? force->splits : (force->kernel == 5 ? 0 : 1);
     pk.stages = force->stages;
   } else {
     pk = pick_for(cache, M, Ns, 2, ktiles, nsm, K);
-    if (pk.kernel != 1) return cudaErrorNotSupported;  // only the row-tiled kernel fuses the activation
+    // the row-tiled and the two-SM pair kernels fuse the activation
+    if (pk.kernel != 1 && pk.kernel != 5) return cudaErrorNotSupported;
+  }
+  if (pk.kernel == 5) {
+    // two-SM pair tiles in SwiGLU mode: rank 0 of a pair reads gate rows, rank
+    // 1 up rows of the same bn/2 output columns, so the M = 256 accumulator
+    // holds both and the epilogue writes the bf16 activation
+    Params p{};
+    p.M = M;
+    p.K = K;
+    p.m_dev = m_dev;
+    p.ldc = 0;
+    p.ktiles = ktiles;
+    p.err = err;
+    p.nseg = 2;
+    p.seg_start[0] = 0;
+    p.seg_start[1] = p.seg_start[2] = p.seg_start[3] = 0x3FFFFFFF;
+    p.seg_N[0] = p.seg_N[1] = F;
+    p.act = (__nv_bfloat16*)act;
+    p.ld_act = ld_act;
+    p.bn = pk.bn ? pk.bn : 256;
+    if (p.bn < 32 || p.bn > 256 || (p.bn & 31)) return cudaErrorInvalidValue;
+    p.kpack = pk.splits ? pk.splits : 1;
+    if (p.kpack < 1 || p.kpack > 2 || (p.kpack > 1 && K % BK)) return cudaErrorInvalidValue;
+    const int max_stages = p2_max_stages(p.bn, p.kpack);
+    p.stages = pk.stages ? pk.stages : (p.kpack == 1 ? p2_default_stages(p.bn) : max_stages);
+    if (p.stages < 2 || p.stages > max_stages) return cudaErrorInvalidValue;
+    p.splits = 1;
+    p.nload = loaders_for(p.stages);
+    p.tmem_cols = 32;
+    while (p.tmem_cols < 2 * p.bn) p.tmem_cols *= 2;
+    p.ntn = (F + p.bn / 2 - 1) / (p.bn / 2);
+    const CUtensorMap* mb[3];
+    mb[0] = p.kpack == 1 ? get_map(cache, Wg, F, K, ldw, p.bn / 2) : get_map3(cache, Wg, F, K, ldw, p.bn / 2, p.kpack);
+    mb[1] = p.kpack == 1 ? get_map(cache, Wu, F, K, ldw, p.bn / 2) : get_map3(cache, Wu, F, K, ldw, p.bn / 2, p.kpack);
+    mb[2] = mb[0];
+    const CUtensorMap* ma = p.kpack == 1 ? get_map(cache, A, M, K, lda, BM) : get_map3(cache, A, M, K, lda, BM, p.kpack);
+    if (!mb[0] || !mb[1] || !ma) return cudaErrorInvalidValue;
+    const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * p.ntn;
+    const int ncl = p2_clusters(p.bn, p.stages, pair_tiles, nsm);
+    return launch_p2(ma, mb, p, ncl, st);
   }
   const int bn = pk.bn ? pk.bn : (mgroups == 1 ? pick_for(cache, M, Ns, 2, ktiles, nsm, K).bn : 256);
   if (bn < 16 || bn > 256 || (bn & 15) || MT * bn > 512) return cudaErrorInvalidValue;

@@ -438,8 +438,8 @@ polestar_status gate_up_swiglu(polestar_ctx* c, const polestar_layer_weights& w,
   const int d = c->d, F = c->F;
   const int Ns[2] = {F, F};
   int ch[4] = {0, 0, 0, 0};
-  if (sizeof(T) == 2 && c->act && R > 0 && R <= 128 && tc_gemm_supported(d, d, d) &&
-      tc_gemm_choice(&c->tc, R, 2, Ns, d, ch) == cudaSuccess && ch[0] == 1) {
+  if (sizeof(T) == 2 && c->act && R > 0 && tc_gemm_supported(d, d, d) &&
+      tc_gemm_choice(&c->tc, R, 2, Ns, d, ch) == cudaSuccess && ((R <= 128 && ch[0] == 1) || ch[0] == 5)) {
     const int pi = prof_start(c, c->gemm_cls);
     const cudaError_t e = tc_gemm_bf16_swiglu(&c->tc, c->a_in, d, w.w_gate, w.w_up, d, F, c->act, F, R, m_dev, d, c->sm);
     prof_stop_rows(c, pi, (double)2 * F * d * sizeof(T), (double)d * sizeof(T) + (double)F * 2.0, 4.0 * F * d, R,
@@ -1098,7 +1098,9 @@ extern "C" polestar_status polestar_init(const polestar_config* cfg, const poles
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
     }
     TRY(dalloc(c, &c->a_in, c->esz * (size_t)R * std::max(std::max(d, c->F), c->qdim)));
-    if (c->bf16) TRY(dalloc(c, &c->act, 2 * (size_t)std::min(R, 128) * c->F));  // fused path: <= 128 rows
+    // SwiGLU activation written by the fused gate/up epilogue (row-tiled kernel
+    // up to 128 rows, two-SM pair kernel above 256)
+    if (c->bf16) TRY(dalloc(c, &c->act, 2 * (size_t)R * c->F));
     TRY(dalloc(c, &c->q_rows, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->attn_out, c->esz * (size_t)R * c->qdim));
     TRY(dalloc(c, &c->write_kv, (size_t)R));
@@ -1626,16 +1628,16 @@ extern "C" polestar_status polestar_debug_gemm_swiglu(const void* A, int32_t lda
                                                       void* stream) {
   static TcGemmCache cache;
   if (!A || !Wg || !Wu || !act || M < 0 || F < 1 || K < 1 || ld_act < F) return POLESTAR_ERR_INVALID_ARG;
-  const int kind = path & 0xFF;
-  if (kind != 1 && kind != 2) return POLESTAR_ERR_UNSUPPORTED;
+  const int kind = path & 0xF;
+  if (kind != 1 && kind != 2 && kind != 7) return POLESTAR_ERR_UNSUPPORTED;
   if (!tc_gemm_supported(K, lda, ldw)) return POLESTAR_ERR_UNSUPPORTED;
   TcGemmChoice force;
-  force.kernel = kind == 2 ? 1 : 0;
+  force.kernel = kind == 2 ? 1 : (kind == 7 ? 5 : 0);
   force.stages = (path >> 8) & 0xFF;
   force.splits = (path >> 16) & 0xFF;
   force.bn = ((path >> 24) & 0xFF) * 16;
   const cudaError_t e = tc_gemm_bf16_swiglu(&cache, A, lda, Wg, Wu, ldw, F, act, ld_act, M, m_dev, K,
-                                            (cudaStream_t)stream, kind == 2 ? &force : nullptr);
+                                            (cudaStream_t)stream, kind != 1 ? &force : nullptr);
   if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) return POLESTAR_ERR_UNSUPPORTED;
   return e == cudaSuccess ? POLESTAR_OK : POLESTAR_ERR_CUDA;
 }

@@ -302,7 +302,8 @@ def gemm_path(kernel: int, stages: int = 0, splits: int = 0, bn: int = 0, kpack:
 def debug_gemm_swiglu(A, Wg, Wu, act, path: int = 1, m_dev=None, stream=None):
     """act = bf16(silu(A Wg^T) * (A Wu^T)) through polestar_debug_gemm_swiglu;
     torch CUDA tensors (A [M, K], Wg/Wu [F, K], act [M, >= F] bf16, unit inner
-    stride); path as gemm_path with kernel 1 (library) or 2 (row-tiled)."""
+    stride); path as gemm_path with kernel 1 (library), 2 (row-tiled) or 7
+    (two-SM pair tiles)."""
     lib = load()
     lib.polestar_debug_gemm_swiglu.argtypes = [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
                                                C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,

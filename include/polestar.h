@@ -309,11 +309,15 @@ polestar_status polestar_debug_gemm(const void *A, int32_t lda, const void *W, i
  * act[m, f] = bf16(silu(g) * u), g = sum_k A[m, k] Wg[f, k], u = sum_k A[m, k]
  * Wu[f, k] (A, Wg, Wu bf16 device matrices with row strides lda, ldw; act bf16,
  * row stride ld_act >= F), the activation computed from the fp32 accumulators
- * in the row-tiled tcgen05 kernel's epilogue (after the split-K reduction when
- * K is split).  path 1: the library's choice (UNSUPPORTED when that is not the
- * row-tiled kernel); path 2: the row-tiled kernel with bits 8-15 the ring
- * depth, 16-23 the K split, 24-31 the tile width / 16 (gate and up get half
- * of it each).  m_dev as in polestar_debug_gemm.  Asynchronous. */
+ * in a tcgen05 kernel's epilogue (after the split-K reduction when K is split).
+ * path 1: the library's choice (UNSUPPORTED when that is neither the row-tiled
+ * nor the two-SM pair kernel); path 2: the row-tiled kernel with bits 8-15 the
+ * ring depth, 16-23 the K split, 24-31 the tile width / 16 (gate and up get
+ * half of it each); path 7: the two-SM pair kernel (the pair's first CTA reads
+ * the gate rows, the second the up rows of the same output columns) with bits
+ * 8-15 the ring depth, 16-23 the k-blocks per stage (1 or 2), 24-31 the pair
+ * tile width / 16 (a multiple of 32).  m_dev as in polestar_debug_gemm.
+ * Asynchronous. */
 polestar_status polestar_debug_gemm_swiglu(const void *A, int32_t lda, const void *Wg, const void *Wu, int32_t ldw,
                                            void *act, int32_t ld_act, int32_t M, const int32_t *m_dev, int32_t F,
                                            int32_t K, int32_t path, void *stream);

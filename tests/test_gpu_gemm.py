@@ -186,6 +186,15 @@ def test_gate_up_swiglu_fused(path, M, F, K):
     assert torch.isnan(act[:, F:].float()).all()  # nothing written past F
 
 
+# the same through the two-SM pair kernel (path 7: bn / 2 gate and bn / 2 up
+# columns per pair tile; one or two k-blocks per stage; ragged F and rows)
+@pytest.mark.parametrize("path", [(256 // 16) << 24 | (2 << 16) | 7, (192 // 16) << 24 | (1 << 16) | 7,
+                                  (128 // 16) << 24 | (2 << 16) | (3 << 8) | 7])
+@pytest.mark.parametrize("M,F,K", [(513, 1000, 1408), (300, 1376, 512), (2560, 4096, 4096)])
+def test_gate_up_swiglu_pair_kernel(path, M, F, K):
+    test_gate_up_swiglu_fused(path, M, F, K)
+
+
 def test_gate_up_swiglu_matches_unfused():
     """The fused epilogue computes silu(g) * u from the same fp32 accumulators as
     the unfused projections (same kernel, same tile width), so the results agree
