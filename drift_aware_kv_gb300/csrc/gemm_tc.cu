@@ -73,6 +73,10 @@ struct Params {
   // two-SM pair kernel: 64-column k-blocks per stage (1, or 2 read by one 3D
   // TMA box per operand: fewer, larger copies per issuing warp)
   int kpack;
+  // two-SM pair kernel: tiles walk groups of `group` row pairs, every column
+  // block of a group before the next group (so a group's A rows stay in L2
+  // while the weights stream past them)
+  int group;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -803,6 +807,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 // even), so each stage's uses are issued in order by one warp and its parity
 // waits never run more than one phase ahead of the barrier.
 constexpr int P2_LOADERS = 2;
+// Tile t of the pair kernel's walk -> (row pair, column block): groups of g
+// row pairs (the last one shorter), row pairs fastest inside a group.
+__device__ __forceinline__ void p2_tile(long long t, int mpairs, int ntn, int g, int* mp, int* nb) {
+  const long long per = (long long)g * ntn;
+  const int grp = (int)(t / per);
+  const int rem = (int)(t - (long long)grp * per);
+  const int gm = min(g, mpairs - grp * g);
+  *mp = grp * g + rem % gm;
+  *nb = rem / gm;
+}
 constexpr int P2_THREADS = (6 + P2_LOADERS - 1) * 32;  // warps 0 and 6.. load, 1 MMA, 2-5 drain
 __global__ void __launch_bounds__(P2_THREADS, 1)
     gemm_p2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -884,7 +898,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
       long long it = 0;
       bool live = true;
       for (long long t = cid; t < ntiles && live; t += ncl) {
-        const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
+        int mp, nb;
+        p2_tile(t, mpairs, p.ntn, p.group, &mp, &nb);
         const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
         // W rows of this CTA's half tile: rows n0 + rank bn/2 of segment sg, or
         // in SwiGLU mode gate (rank 0) / up (rank 1) rows of act columns n0..
@@ -966,7 +981,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
           mbar_wait_cluster(smem_u32(&acc_full[b]), (uint32_t)(tl >> 1) & 1u, p.err, 3, abort_flag, 256);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (!ok) break;
-      const int mp = (int)(t % mpairs), nb = (int)(t / mpairs);
+      int mp, nb;
+      p2_tile(t, mpairs, p.ntn, p.group, &mp, &nb);
       const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
       const int n0 = (nb - p.seg_start[sg]) * bn;
       const int segN = p.seg_N[sg];
@@ -1361,6 +1377,18 @@ int p2_clusters(int bn, int stages, long long pair_tiles, int nsm) {
   return (int)std::max<long long>(1, std::min<long long>(mc, pair_tiles));
 }
 
+// Row pairs per group of the pair kernel's tile walk: about 48 MB of A rows
+// (2 x 128 rows x K bf16 per pair), so that a group's rows stay in the 129 MB
+// L2 while every weight column block passes them once.  Walking row pairs
+// fastest over all of A instead (A re-read from DRAM for every column block)
+// read 4.5 GB for a 16384 x 12288 x 4096 launch whose operands hold 234 MB.
+int p2_group(int M, int K) {
+  const int mpairs = (M + 2 * BM - 1) / (2 * BM);
+  const long long pair_bytes = 2LL * BM * K * 2;
+  const int g = (int)std::max(1LL, (48LL << 20) / std::max(1LL, pair_bytes));
+  return std::max(1, std::min(mpairs, g));
+}
+
 cudaError_t launch_p2(const CUtensorMap* a, const CUtensorMap* const* b, const Params& p, int nclusters,
                       cudaStream_t st) {
   static PerDeviceOnce attr;
@@ -1556,6 +1584,7 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     for (int sgi = nseg; sgi < 3; ++sgi) mb[sgi] = mb[0];
     const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * p.ntn;
     const int ncl = p2_clusters(p.bn, p.stages, pair_tiles, nsm);
+    p.group = p2_group(M, K);
     const CUtensorMap* ma = p.kpack == 1 ? get_map(cache, A, M, K, lda, BM) : get_map3(cache, A, M, K, lda, BM, p.kpack);
     if (!ma) return cudaErrorInvalidValue;
     return launch_p2(ma, mb, p, ncl, st);
@@ -1683,6 +1712,7 @@ cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, cons
     if (!mb[0] || !mb[1] || !ma) return cudaErrorInvalidValue;
     const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * p.ntn;
     const int ncl = p2_clusters(p.bn, p.stages, pair_tiles, nsm);
+    p.group = p2_group(M, K);
     return launch_p2(ma, mb, p, ncl, st);
   }
   const int bn = pk.bn ? pk.bn : (mgroups == 1 ? pick_for(cache, M, Ns, 2, ktiles, nsm, K).bn : 256);

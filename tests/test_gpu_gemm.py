@@ -195,6 +195,16 @@ def test_gate_up_swiglu_pair_kernel(path, M, F, K):
     test_gate_up_swiglu_fused(path, M, F, K)
 
 
+# the pair kernel's tile walk in groups of row pairs (about 48 MB of A rows per
+# group): K = 12288 gives groups of 8 row pairs, so 2560 rows walk two groups
+# (8 + 2 pairs) and 4352 rows three (8 + 8 + 1); every output element once
+@pytest.mark.parametrize("M,N,K", [(2560, 1000, 12288), (4352, 512, 12288)])
+def test_two_sm_pair_grouped_walk(M, N, K):
+    from drift_aware_kv_gb300 import polestar as P
+    _check_gemm(P.gemm_path(7, 0, 2, 256), M, N, K)
+    _check_gemm(P.gemm_path(7, 0, 1, 192), M, N, K)
+
+
 def test_gate_up_swiglu_matches_unfused():
     """The fused epilogue computes silu(g) * u from the same fp32 accumulators as
     the unfused projections (same kernel, same tile width), so the results agree
