@@ -355,6 +355,11 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
                        "(x0, logits and mask in, commit mask out, copies inside the timed region)"}
         del host
 
+    closed = None
+    if full and not args.no_closed_loop:
+        log(f"{w.name}: closed-loop region")
+        closed = closed_loop_region(w, W, dev, stream, ws, args.closed_loop_steps)
+
     rooflines = {k: class_roofline(k, v, w, peaks) for k, v in stats.items()}
     rooflines = {k: v for k, v in rooflines.items() if v is not None}
     dom = max(stats, key=lambda k: stats[k]["ms"])
@@ -383,11 +388,69 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
         "profiled_region_ms_per_step": prof["total_ms"] / len(timed),
         "kernel_launches": {k: v["launches"] for k, v in stats.items()},
         "calibration_overhead": overhead,
+        "closed_loop": closed,
         "roofline": roof, "rooflines": rooflines, "clocks": clocks, "e2e": e2e,
         "gpu_launches": int(main["launches"]), "wall_s": wall,
         "host_issue_ms_first_step": main["issue_first"] * 1e3,
         "first_step_block_entry": bool(timed[0]["block_entry"]),
     }
+
+
+def closed_loop_region(w, W, dev, stream, ws, n_timed, n_warmup=3):
+    """Closed-loop decoding (Algorithm 1 in full) on the same weights: every step
+    embeds the current tokens, calibrates, runs the final norm + LM head over
+    the 2B gate rows, gates and writes the greedy tokens (the host reads the
+    committed counts back every step).  A seeded prompt, random-init token
+    embedding and LM head of the workload's vocabulary; with these weights the
+    masked rows predict alike, so most commits come from the progress rule and
+    tokens per forward stays near 1.  Times the steps after the warm-up with
+    CUDA events, then the same number of further steps with per-launch events
+    for the classes."""
+    import torch
+    from drift_aware_kv_gb300 import polestar as P
+    from drift_aware_kv_gb300 import synth
+    from drift_aware_kv_gb300.decode import Generator
+
+    ps = P.Polestar(w, W, stream=stream)
+    dw = synth.make_decode_weights(w, dev)
+    gen = Generator(ps, dw)
+    tok, msk = synth.make_prompt(w, dev)
+    tok = tok.to(torch.int32)
+    msk = msk.to(torch.uint8)
+    it = gen.steps(tok, msk)
+    for _ in range(n_warmup):
+        next(it)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    n = committed = entries = 0
+    for blk, entry, counts, left in it:
+        n += 1
+        committed += sum(counts)
+        entries += int(entry)
+        if n == n_timed:
+            break
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    total_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, dev)
+    ps.profile_begin(40 * w.n_layers * n_timed + 256)
+    m = 0
+    for _ in it:
+        m += 1
+        if m == n_timed:
+            break
+    stats = ps.profile_end()
+    ps.close()
+    del gen, dw
+    torch.cuda.empty_cache()
+    return {"steps_per_s": aggregate_line(n, ws, total_s), "ms_per_step": total_s * 1e3 / max(n, 1), "steps": n,
+            "block_entries": entries, "tokens_committed": committed,
+            "tokens_per_forward": committed / w.batch / max(n, 1), "vocab": w.vocab,
+            "kernel_ms_profiled_steps": {k: round(v["ms"], 3) for k, v in stats.items()},
+            "what": "embed + calibrate + final norm and LM head over the 2B gate rows + commit + progress rule "
+                    "and greedy tokens, per step, committed counts read back each step; random-init weights "
+                    "(tokens per forward near 1: the progress rule commits most tokens)"}
 
 
 def run_device(args, w, peaks, ws, rank, local):
@@ -572,6 +635,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=8,
                     help="timed steps replayed end to end from pinned host buffers (1.6 GB each at batch 32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-closed-loop", action="store_true")
+    ap.add_argument("--closed-loop-steps", type=int, default=8, help="timed closed-loop decoding steps")
     ap.add_argument("--attn-impl", type=int, default=0, choices=[0, 1, 2],
                     help="attention kernel: 0 the library's choice, 1 pipelined mma.sync, 2 tcgen05 (comparison runs)")
     ap.add_argument("--host-store", action="store_true",

@@ -67,26 +67,37 @@ class Generator:
         ps.commit(self.logits, masked_u8, self.commit, self.conf)
         return ps.decode_tokens(self.logits, self.commit, tokens, masked_u8)
 
-    def generate(self, tokens, masked_u8) -> GenerationStats:
-        """Decode every block of the generated region (Algorithm 1)."""
+    def steps(self, tokens, masked_u8):
+        """Iterate the generation step by step (Algorithm 1): yields after every
+        step (block index, whether it was the block's entry, per-sequence
+        committed counts, per-sequence tokens still masked in the block)."""
         w = self.ps.w
-        st = GenerationStats()
         for blk in range(w.n_blocks):
             entry = True
             n_unmasked = [0] * w.batch
-            steps = 0
             # the progress rule commits at least one token of the block per step
             for _ in range(w.block):
                 counts, left = self.step(tokens, masked_u8, blk, entry, n_unmasked)
-                st.steps += 1
-                st.block_entries += int(entry)
-                st.committed += sum(counts)
-                steps += 1
+                yield blk, entry, counts, left
                 n_unmasked = counts
                 entry = False
                 if max(left) == 0:
                     break
             else:
                 raise RuntimeError(f"block {blk} still has masked tokens after {w.block} steps")
+
+    def generate(self, tokens, masked_u8) -> GenerationStats:
+        """Decode every block of the generated region (Algorithm 1)."""
+        st = GenerationStats()
+        steps = 0
+        for blk, entry, counts, left in self.steps(tokens, masked_u8):
+            if entry and steps:
+                st.per_block_steps.append(steps)
+                steps = 0
+            st.steps += 1
+            st.block_entries += int(entry)
+            st.committed += sum(counts)
+            steps += 1
+        if steps:
             st.per_block_steps.append(steps)
         return st
