@@ -354,11 +354,14 @@ polestar_status polestar_debug_attention_batch(const void *q, const void *kv, in
                                                void *out, float *kl, int32_t dtype, void *stream);
 
 /* ---- attention kernel selection (test hook) ----
- * 0: the library's choice (the pipelined mma.sync kernel); 1: the mma.sync
- * kernel; 2: the tcgen05 kernel (S and O accumulated in TMEM, work items of
- * up to 128 rows) wherever it applies (bf16, head size 128).  Affects work lists built after the call (context steps and
- * polestar_debug_attention); returns the previous setting, or -1 for an
- * invalid value.  Process-wide; not for concurrent use with running steps. */
+ * 0: the library's choice (the tcgen05 kernel for bf16 head size 128 when
+ * its work items fill every SM twice, else the pipelined mma.sync kernel); 1:
+ * the mma.sync kernel; 2: the tcgen05 kernel (S and O accumulated in TMEM,
+ * work items of up to 128 rows) wherever it applies (bf16, head size 128;
+ * drift measured by the deferred pass).  Affects work lists built after the
+ * call (context steps and polestar_debug_attention); returns the previous
+ * setting, or -1 for an invalid value.  Process-wide; not for concurrent use
+ * with running steps. */
 int32_t polestar_debug_attention_impl(int32_t impl);
 
 /* ---- window and trigger (host only; test hooks) ----
