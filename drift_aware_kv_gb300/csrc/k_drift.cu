@@ -6,22 +6,24 @@
 // q = softmax(sp) and d = s - sp:
 //   KL(p || q) = sum_j p_j d_j - log sum_j q_j e^(d_j),
 // the second term as log1p(sum_j q_j expm1(d_j) / sum_j q_j) while that stays
-// accurate, else as lse - lse_p (kl_log_mass).  One CTA per (tracked row,
-// head): its threads stride over the N keys, then a fixed-order block
-// reduction (deterministic).  With store, the new scores and log-sum-exp then
-// replace the previous ones.  Memory-bound: 8 bytes read (+ 4 written with
-// store) per key.
+// accurate, else as lse - lse_p (kl_log_mass).  One warp per (tracked row,
+// head): its lanes stride over the N keys with 16-byte loads, then
+// fixed-order butterfly sums (deterministic).  With store, the new scores and
+// log-sum-exp then replace the previous ones.  Memory-bound: 8 bytes read (+ 4
+// written with store) per key.
 #include "kernels.h"
 
 namespace polestar {
 
-constexpr int DRIFT_THREADS = 256;
+constexpr int DRIFT_WARPS = 8;  // (tracked row, head) pairs per CTA, one warp each
 
-__global__ void __launch_bounds__(DRIFT_THREADS) drift_kernel(DriftArgs a) {
-  __shared__ float red[32];
+__global__ void __launch_bounds__(DRIFT_WARPS * 32) drift_kernel(DriftArgs a) {
   pdl_enter();
-  const int4 t = a.track[blockIdx.x];
-  const int h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long u = (long long)blockIdx.x * DRIFT_WARPS + warp;  // (tracked row, head) index
+  if (u >= (long long)a.n_track * a.H) return;
+  const int4 t = a.track[u / a.H];
+  const int h = (int)(u % a.H);
   const bool proxy = t.z == ROW_PROXY;
   const size_t idx = proxy ? ((size_t)t.y * a.K + t.w) * a.H + h : ((size_t)t.y * a.B + t.w) * a.H + h;
   float* prev = (proxy ? a.proxy_prev : a.active_prev) + idx * a.N;
@@ -32,7 +34,7 @@ __global__ void __launch_bounds__(DRIFT_THREADS) drift_kernel(DriftArgs a) {
   float pd = 0.f, qs = 0.f, qe = 0.f;
   const bool vec = (a.N & 3) == 0 && ((((uintptr_t)prev) | ((uintptr_t)cur)) & 15) == 0;
   if (vec) {
-    for (int j = threadIdx.x * 4; j < a.N; j += DRIFT_THREADS * 4) {
+    for (int j = lane * 4; j < a.N; j += 32 * 4) {
       const float4 s4 = *(const float4*)(cur + j);
       const float4 p4 = *(const float4*)(prev + j);
       const float s[4] = {s4.x, s4.y, s4.z, s4.w}, sp[4] = {p4.x, p4.y, p4.z, p4.w};
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(DRIFT_THREADS) drift_kernel(DriftArgs a) {
       if (a.store) *(float4*)(prev + j) = s4;
     }
   } else {
-    for (int j = threadIdx.x; j < a.N; j += DRIFT_THREADS) {
+    for (int j = lane; j < a.N; j += 32) {
       const float s = cur[j], sp = prev[j];
       const float d = s - sp;
       const float q = expf(sp - lse_p);
@@ -57,10 +59,9 @@ __global__ void __launch_bounds__(DRIFT_THREADS) drift_kernel(DriftArgs a) {
       if (a.store) prev[j] = s;
     }
   }
-  const float PD = block_sum(pd, red);
-  const float QS = block_sum(qs, red);
-  const float QE = block_sum(qe, red);
-  if (threadIdx.x == 0) {
+  // fixed-order butterfly sums (deterministic)
+  const float PD = warp_sum(pd), QS = warp_sum(qs), QE = warp_sum(qe);
+  if (lane == 0) {
     a.kl_out[(size_t)t.x * a.H + h] = PD - kl_log_mass(QE / QS, lse, lse_p);
     if (a.store) *prev_lse = lse;
   }
@@ -68,7 +69,8 @@ __global__ void __launch_bounds__(DRIFT_THREADS) drift_kernel(DriftArgs a) {
 
 void launch_drift(const DriftArgs& a, cudaStream_t st) {
   if (a.n_track <= 0) return;
-  launch_pdl(drift_kernel, dim3(a.n_track, a.H), dim3(DRIFT_THREADS), 0, st, a);
+  const long long pairs = (long long)a.n_track * a.H;
+  launch_pdl(drift_kernel, dim3((unsigned)((pairs + DRIFT_WARPS - 1) / DRIFT_WARPS)), dim3(DRIFT_WARPS * 32), 0, st, a);
 }
 
 }  // namespace polestar
