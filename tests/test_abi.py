@@ -181,3 +181,27 @@ def test_stalled_wait_hook_without_context_is_an_argument_error():
     from drift_aware_kv_gb300 import polestar as P
     lib = P.load()
     assert lib.polestar_debug_stalled_wait(None, 1000) == P.ERR_INVALID_ARG
+
+
+def test_closed_loop_entry_points_without_context_are_argument_errors():
+    """Host-side argument checks of the closed-loop calls (no device work)."""
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    buf = ctypes.c_void_p(0x2000)
+    n = (ctypes.c_int32 * 4)()
+    assert lib.polestar_decode_logits(None, buf, buf, 1000, buf) == P.ERR_INVALID_ARG
+    assert lib.polestar_decode_tokens(None, buf, 1000, buf, buf, buf, n, n) == P.ERR_INVALID_ARG
+    assert lib.polestar_embed(None, buf, 1000, buf, buf, buf, buf) == P.ERR_INVALID_ARG
+
+
+def test_batched_attention_hook_rejects_bad_arguments_on_the_host():
+    """polestar_debug_attention_batch checks its sizes before any device work."""
+    from drift_aware_kv_gb300 import polestar as P
+    lib = P.load()
+    lib.polestar_debug_attention_batch.restype = ctypes.c_int
+    buf = ctypes.c_void_p(0x2000)
+    args = lambda batch, N, H, Hkv, dh, R: (buf, buf, batch, N, H, Hkv, dh, R, None, None, None, 0, 0, buf, None,
+                                            P.BF16, None)
+    assert lib.polestar_debug_attention_batch(*args(0, 64, 4, 4, 128, 8)) == P.ERR_INVALID_ARG
+    assert lib.polestar_debug_attention_batch(*args(2, 64, 6, 4, 128, 8)) == P.ERR_INVALID_ARG  # H % Hkv
+    assert lib.polestar_debug_attention_batch(*args(2, 64, 4, 4, 96, 8)) == P.ERR_UNSUPPORTED   # head size
