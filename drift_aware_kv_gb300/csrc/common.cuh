@@ -166,4 +166,12 @@ __device__ __forceinline__ float kl_log_mass(float x, float lse_new, float lse_p
   return x > -0.5f ? log1pf(x) : lse_new - lse_prev;
 }
 
+// Rotate-half rotary embedding of one pair (x_k, x_{k+dh/2}) by (cos, sin):
+// explicit fused multiply-adds, so every kernel that applies it (the row
+// kernel and the projection epilogue) rounds identically.
+__device__ __forceinline__ void rope_rotate(float a, float b, float c, float s, float& y1, float& y2) {
+  y1 = fmaf(a, c, -(b * s));
+  y2 = fmaf(b, c, a * s);
+}
+
 }  // namespace polestar

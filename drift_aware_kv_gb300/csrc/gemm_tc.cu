@@ -77,6 +77,17 @@ struct Params {
   // block of a group before the next group (so a group's A rows stay in L2
   // while the weights stream past them)
   int group;
+  // two-SM pair kernel, Q/K/V mode (segments Q, K, V of one layer, tiles of a
+  // whole number of heads): the epilogue applies the rotary embedding and
+  // writes bf16 Q rows and the K/V cache entries of the rows (as the row
+  // kernel rope_scatter does) instead of C
+  __nv_bfloat16* q_out;  // [M, qdim]
+  const int4* qkv_rows;  // [M] {seq, pos, kind, aux}
+  const uint8_t* qkv_write_kv;
+  const float2* rope;    // [N][dh / 2] (cos, sin)
+  __nv_bfloat16* kv_layer;
+  long long kv_seq_stride;
+  int kvdim, dh;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -990,6 +1001,68 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
       const bool vseg = vec && ((((uintptr_t)Cseg) & 15) == 0);
       const int row = mp * 2 * BM + rank * BM + q * 32 + lane;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * bn);
+      if (p.q_out) {
+        // Q/K/V mode: segment sg 0 = Q, 1 = K (both rotated; proxy rows' Q is
+        // not), 2 = V; K and V go to the cache row (seq, pos) of active,
+        // other and (when flagged) window rows
+        int4 m = make_int4(0, 0, ROW_NONE, 0);
+        if (row < M_eff) m = p.qkv_rows[row];
+        const bool rot = sg == 1 || m.z != ROW_PROXY;
+        const bool wkv = (m.z == ROW_ACTIVE || m.z == ROW_OTHER) ||
+                         (m.z == ROW_WINDOW && (!p.qkv_write_kv || p.qkv_write_kv[row]));
+        const bool put = m.z != ROW_NONE && (sg == 0 || wkv);
+        __nv_bfloat16* dst = sg == 0 ? p.q_out + (size_t)row * p.seg_N[0] + n0
+                                     : p.kv_layer + (size_t)m.x * p.kv_seq_stride + (size_t)m.y * 2 * p.kvdim +
+                                           (sg == 2 ? p.kvdim : 0) + n0;
+        auto put16 = [&](__nv_bfloat16* o, const float* y) {
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+            w[e] = *(const uint32_t*)&v2;
+          }
+          *(uint4*)o = make_uint4(w[0], w[1], w[2], w[3]);
+          *(uint4*)(o + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+        };
+        if (sg < 2) {
+          const int hd = p.dh / 2;
+#pragma unroll 1
+          for (int hh = 0; hh < bn / p.dh; ++hh) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < hd; c0 += 16) {
+              float a[16], b2[16];
+              tmem_ld16(tq + hh * p.dh + c0, a);
+              tmem_ld16(tq + hh * p.dh + hd + c0, b2);
+              if (put) {
+                if (rot) {
+                  const float2* tab = p.rope + (size_t)m.y * hd + c0;
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) {
+                    const float2 cs = tab[e];
+                    float y1, y2;
+                    rope_rotate(a[e], b2[e], cs.x, cs.y, y1, y2);
+                    a[e] = y1;
+                    b2[e] = y2;
+                  }
+                }
+                put16(dst + hh * p.dh + c0, a);
+                put16(dst + hh * p.dh + hd + c0, b2);
+              }
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < bn; c += 16) {
+            float v[16];
+            tmem_ld16(tq + c, v);
+            if (put) put16(dst + c, v);
+          }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_acc_empty0 + (uint32_t)(b * 8));
+        continue;
+      }
       if (p.act) {
         // SwiGLU mode: gate in the accumulator's first bn/2 columns, up in the
         // second; act[row, nb bn/2 + c] = bf16(silu(g) * u)
@@ -1748,6 +1821,71 @@ cudaError_t tc_gemm_bf16_swiglu(TcGemmCache* cache, const void* A, int lda, cons
   if (!mb[0] || !mb[1] || !ma) return cudaErrorInvalidValue;
   const dim3 grid((F + bn / 2 - 1) / (bn / 2), mgroups, p.splits);
   return MT == 2 ? launch_rt<2>(ma, mb, p, grid, st) : launch_rt<1>(ma, mb, p, grid, st);
+}
+
+cudaError_t tc_gemm_bf16_qkv_rope(TcGemmCache* cache, const void* A, int lda, const void* const* W, const int* N,
+                                  int M, int K, const TcQkvRope& q, cudaStream_t st) {
+  using namespace tc;
+  if (M <= 0) return cudaSuccess;
+  if (!A || !q.rows || !q.rope || !q.q_out || !q.kv_layer || !tc_gemm_supported(K, lda, K)) return cudaErrorInvalidValue;
+  if (((uintptr_t)A | (uintptr_t)q.q_out | (uintptr_t)q.kv_layer) & 15) return cudaErrorInvalidValue;
+  // tiles of whole heads (256 columns), rotary pairs in 16-column chunks
+  constexpr int PBN = 256;
+  if (q.dh < 32 || q.dh % 32 || PBN % q.dh || q.kvdim % 8 || N[1] != q.kvdim || N[2] != q.kvdim) return cudaErrorNotSupported;
+  for (int sgi = 0; sgi < 3; ++sgi)
+    if (N[sgi] % PBN || ((uintptr_t)W[sgi] & 15)) return cudaErrorNotSupported;
+  int* err = tc_error_word(cache);
+  if (!err) return cudaErrorMemoryAllocation;
+  if (cache->num_sms <= 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&cache->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cache->num_sms <= 0) return cudaErrorNoDevice;
+  }
+  const int nsm = cache->num_sms;
+  const int ktiles = (K + BK - 1) / BK;
+  const GemmPick pk = pick_for(cache, M, N, 3, ktiles, nsm, K);
+  if (pk.kernel != 5) return cudaErrorNotSupported;  // the pair kernel carries the mode
+  Params p{};
+  p.M = M;
+  p.K = K;
+  p.m_dev = nullptr;
+  p.ldc = 0;
+  p.ktiles = ktiles;
+  p.err = err;
+  p.nseg = 3;
+  p.bn = PBN;
+  p.kpack = (ktiles * BK == K) ? 2 : 1;
+  p.stages = p.kpack == 1 ? p2_default_stages(p.bn) : p2_max_stages(p.bn, p.kpack);
+  p.splits = 1;
+  p.nload = loaders_for(p.stages);
+  p.tmem_cols = 512;
+  const CUtensorMap* mb[3];
+  for (int sgi = 0, t = 0; sgi < 3; ++sgi) {
+    p.seg_start[sgi] = t;
+    p.seg_N[sgi] = N[sgi];
+    p.seg_C[sgi] = nullptr;
+    mb[sgi] = p.kpack == 1 ? get_map(cache, W[sgi], N[sgi], K, K, p.bn / 2)
+                           : get_map3(cache, W[sgi], N[sgi], K, K, p.bn / 2, p.kpack);
+    if (!mb[sgi]) return cudaErrorInvalidValue;
+    t += N[sgi] / p.bn;
+  }
+  p.seg_start[3] = 0x3FFFFFFF;
+  p.ntn = (N[0] + N[1] + N[2]) / p.bn;
+  p.q_out = (__nv_bfloat16*)q.q_out;
+  p.qkv_rows = q.rows;
+  p.qkv_write_kv = q.write_kv;
+  p.rope = q.rope;
+  p.kv_layer = (__nv_bfloat16*)q.kv_layer;
+  p.kv_seq_stride = (long long)q.kv_seq_stride;
+  p.kvdim = q.kvdim;
+  p.dh = q.dh;
+  const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * p.ntn;
+  const int ncl = p2_clusters(p.bn, p.stages, pair_tiles, nsm);
+  p.group = p2_group(M, K);
+  const CUtensorMap* ma = p.kpack == 1 ? get_map(cache, A, M, K, lda, BM) : get_map3(cache, A, M, K, lda, BM, p.kpack);
+  if (!ma) return cudaErrorInvalidValue;
+  return launch_p2(ma, mb, p, ncl, st);
 }
 
 cudaError_t tc_gemm_bf16(TcGemmCache* cache, const void* A, int lda, const void* W, int ldw, float* C, int ldc,

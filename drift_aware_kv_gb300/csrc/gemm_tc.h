@@ -71,6 +71,29 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
                                const int* ldw, const int* N, float* const* C, int ldc, int M, const int* m_dev,
                                int K, cudaStream_t st, const TcGemmChoice* force = nullptr);
 
+// Q/K/V projection of one layer with the rotary embedding and the scatter
+// fused into the two-SM pair kernel's epilogue: segments W[0] (Q, N[0] rows),
+// W[1] (K) and W[2] (V) (row stride K); row r of A is the row rows[r]
+// {seq, pos, kind, aux}; its Q (rotated unless a proxy row) goes to
+// q_out[r, N[0]] bf16, its K (rotated) and V to the cache row (seq, pos) of
+// kv_layer (bf16 [.., N, 2, kvdim], seq stride kv_seq_stride elements) when
+// the row is active, other, or a window row with write_kv[r] set (every
+// window row when write_kv is null).  cudaErrorNotSupported when the
+// library's choice for the shape is not the pair kernel or the widths are not
+// whole 256-column tiles of whole heads (the caller then runs the projection
+// and the row kernel).
+struct TcQkvRope {
+  const int4* rows = nullptr;
+  const uint8_t* write_kv = nullptr;
+  const float2* rope = nullptr;  // [N][dh / 2] (cos, sin)
+  void* q_out = nullptr;
+  void* kv_layer = nullptr;
+  size_t kv_seq_stride = 0;
+  int kvdim = 0, dh = 0;
+};
+cudaError_t tc_gemm_bf16_qkv_rope(TcGemmCache* cache, const void* A, int lda, const void* const* W, const int* N,
+                                  int M, int K, const TcQkvRope& q, cudaStream_t st);
+
 // Gate and up projections with the SwiGLU activation fused into the
 // row-tiled kernel's epilogue: act[m, f] = bf16(silu(g) * u) with
 // g = A * Wg^T, u = A * Wu^T (both [F, K], row stride ldw), act row stride

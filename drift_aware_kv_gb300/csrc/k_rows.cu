@@ -225,8 +225,10 @@ __global__ void __launch_bounds__(ROW_THREADS)
     float4 y1 = x1[q], y2 = x2[q];
     if (kind[q] == 1 || rot) {
       const float4 a = x1[q], b = x2[q], c = c4[q], s = s4[q];
-      y1 = make_float4(a.x * c.x - b.x * s.x, a.y * c.y - b.y * s.y, a.z * c.z - b.z * s.z, a.w * c.w - b.w * s.w);
-      y2 = make_float4(b.x * c.x + a.x * s.x, b.y * c.y + a.y * s.y, b.z * c.z + a.z * s.z, b.w * c.w + a.w * s.w);
+      rope_rotate(a.x, b.x, c.x, s.x, y1.x, y2.x);
+      rope_rotate(a.y, b.y, c.y, s.y, y1.y, y2.y);
+      rope_rotate(a.z, b.z, c.z, s.z, y1.z, y2.z);
+      rope_rotate(a.w, b.w, c.w, s.w, y1.w, y2.w);
     }
     T* o = kind[q] == 0 ? qo : kdst;
     st4t<T>(o + off[q], y1);

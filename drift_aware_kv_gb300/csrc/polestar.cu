@@ -426,6 +426,50 @@ polestar_status gemm(polestar_ctx* c, const void* A, int lda, const void* W, int
   return POLESTAR_OK;
 }
 
+// Q/K/V projection of R rows (A = a_in, rows table `rows`) with the rotary
+// embedding and the scatter of Q rows and K/V cache entries: fused into the
+// two-SM pair kernel's epilogue when that kernel runs (more than 256 rows,
+// bf16), else the projection into gout followed by the row kernel.  Both give
+// the same bits (the same accumulators, the same rotation arithmetic).
+bool g_qkv_fusion = true;
+
+template <typename T>
+polestar_status qkv_rope(polestar_ctx* c, const polestar_layer_weights& w, const int4* rows, const uint8_t* write_kv,
+                         int R, void* kv_layer, size_t kv_seq) {
+  const int d = c->d;
+  const void* Ws[3] = {w.wq, w.wk, w.wv};
+  const int Ns[3] = {c->qdim, c->kvdim, c->kvdim};
+  int ch[4] = {0, 0, 0, 0};
+  if (sizeof(T) == 2 && g_qkv_fusion && R > 256 && tc_gemm_supported(d, d, d) && c->qdim % 256 == 0 &&
+      c->kvdim % 256 == 0 && 256 % c->dh == 0 && tc_gemm_choice(&c->tc, R, 3, Ns, d, ch) == cudaSuccess &&
+      ch[0] == 5) {
+    TcQkvRope q;
+    q.rows = rows;
+    q.write_kv = write_kv;
+    q.rope = c->rope;
+    q.q_out = c->q_rows;
+    q.kv_layer = kv_layer;
+    q.kv_seq_stride = kv_seq;
+    q.kvdim = c->kvdim;
+    q.dh = c->dh;
+    const double wbytes = (double)(c->qdim + 2 * c->kvdim) * d * sizeof(T);
+    const double row_bytes = (double)d * sizeof(T) + (double)(c->qdim + 2 * c->kvdim) * sizeof(T);
+    const double row_flops = 2.0 * (c->qdim + 2 * c->kvdim) * d;
+    const int pi = prof_start(c, c->gemm_cls);
+    const cudaError_t e = tc_gemm_bf16_qkv_rope(&c->tc, c->a_in, d, Ws, Ns, R, d, q, c->sm);
+    prof_stop_rows(c, pi, wbytes, row_bytes, row_flops, R, nullptr);
+    ++c->launches;
+    if (e != cudaSuccess) return fail(c, POLESTAR_ERR_CUDA, std::string("tcgen05 Q/K/V + rotary: ") + cudaGetErrorString(e));
+    return POLESTAR_OK;
+  }
+  float* Cs[3] = {c->gout, c->gout + c->qdim, c->gout + c->qdim + c->kvdim};
+  TRY(gemm_multi<T>(c, c->a_in, d, 3, Ws, Ns, Cs, c->ldg, R, nullptr, d));
+  RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
+      (launch_rope_scatter<T>(c->gout, c->ldg, rows, write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows, kv_layer,
+                              kv_seq, c->kvdim, c->sm)));
+  return POLESTAR_OK;
+}
+
 // Gate/up projections + SwiGLU: one fused tcgen05 launch writing the bf16
 // activation into *act_out for at most 128 rows when the library's kernel
 // choice is the row-tiled kernel (else the two projections into gout and the
@@ -612,14 +656,7 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
         RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
                               (size_t)c->Wmax * d, c->sm)));
       RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
-      {
-        const void* Ws[3] = {w.wq, w.wk, w.wv};
-        const int Ns[3] = {c->qdim, c->kvdim, c->kvdim};
-        float* Cs[3] = {c->gout, c->gout + c->qdim, c->gout + c->qdim + c->kvdim};
-        TRY(gemm_multi<T>(c, c->a_in, d, 3, Ws, Ns, Cs, c->ldg, R, nullptr, d));
-      }
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, rows, nullptr, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
-                             kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm)));
+      TRY(qkv_rope<T>(c, w, rows, nullptr, R, kv + (size_t)l * kv_layer, kv_seq));
       AttnArgs aa{};
       aa.q = c->q_rows;
       aa.ldq = c->qdim;
@@ -874,14 +911,7 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     // the projections' input rows were normalised by their producers: active
     // rows by the previous layer's final residual (or the input gather), window
     // rows by the patch, proxy rows by the centroid update
-    {
-      const void* Ws[3] = {w.wq, w.wk, w.wv};
-      const int Ns[3] = {c->qdim, c->kvdim, c->kvdim};
-      float* Cs[3] = {c->gout, c->gout + c->qdim, c->gout + c->qdim + c->kvdim};
-      TRY(gemm_multi<T>(c, c->a_in, d, 3, Ws, Ns, Cs, c->ldg, R, nullptr, d));
-    }
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, rows, c->write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
-                           kv + (size_t)l * kv_layer, kv_seq, c->kvdim, c->sm)));
+    TRY(qkv_rope<T>(c, w, rows, c->write_kv, R, kv + (size_t)l * kv_layer, kv_seq));
     AttnArgs aa{};
     aa.q = c->q_rows;
     aa.ldq = c->qdim;
@@ -1832,6 +1862,12 @@ extern "C" int32_t polestar_debug_attention_items(int32_t a0, int32_t na, int32_
     out[4 * i + 3] = w[i].w;
   }
   return n;
+}
+
+extern "C" int32_t polestar_debug_qkv_fusion(int32_t on) {
+  const int32_t old = g_qkv_fusion ? 1 : 0;
+  g_qkv_fusion = on != 0;
+  return old;
 }
 
 extern "C" int32_t polestar_debug_attention_impl(int32_t impl) {

@@ -31,7 +31,8 @@ EXPORTED = ("polestar_init", "polestar_calibrate_step", "polestar_commit", "pole
             "polestar_debug_window", "polestar_debug_trigger", "polestar_debug_stalled_wait",
             "polestar_codec_bytes", "polestar_codec_encode", "polestar_codec_decode",
             "polestar_debug_write", "polestar_debug_enter_block", "polestar_decode_logits",
-            "polestar_decode_tokens", "polestar_embed", "polestar_debug_attention_batch")
+            "polestar_decode_tokens", "polestar_embed", "polestar_debug_attention_batch",
+            "polestar_debug_qkv_fusion")
 CODECS = {"fp16": 0, "fp8": 1, "int8": 2, "mxfp4": 3, "int2": 4, "nvfp4": 5}
 KERNEL_CLASSES = ("gemm_step", "gemm_entry", "attention", "cluster", "select", "commit", "rows",
                   "attention_entry", "cluster_entry", "rows_entry")
@@ -316,6 +317,16 @@ def debug_gemm_swiglu(A, Wg, Wu, act, path: int = 1, m_dev=None, stream=None):
     _check(lib.polestar_debug_gemm_swiglu(_ptr(A), A.stride(0), _ptr(Wg), _ptr(Wu), Wg.stride(0), _ptr(act),
                                           act.stride(0), M, _ptr(m_dev) if m_dev is not None else None, F, K,
                                           int(path), C.c_void_p(st.cuda_stream)))
+
+
+def qkv_fusion(on: int) -> int:
+    """Q/K/V projection with the rotary embedding in the pair kernel's epilogue
+    (polestar_debug_qkv_fusion): 1 on (default), 0 projection + row kernel;
+    returns the previous setting."""
+    lib = load()
+    lib.polestar_debug_qkv_fusion.argtypes = [C.c_int32]
+    lib.polestar_debug_qkv_fusion.restype = C.c_int32
+    return int(lib.polestar_debug_qkv_fusion(int(on)))
 
 
 def attention_impl(impl: int) -> int:

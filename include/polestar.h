@@ -353,6 +353,14 @@ polestar_status polestar_debug_attention_batch(const void *q, const void *kv, in
                                                float *prev, float *prev_lse, int32_t measure, int32_t store,
                                                void *out, float *kl, int32_t dtype, void *stream);
 
+/* ---- Q/K/V projection with the rotary embedding fused (test hook) ----
+ * 1 (the default): above 256 rows, where the two-SM pair kernel runs the Q/K/V
+ * projection, its epilogue applies the rotary embedding and writes the bf16 Q
+ * rows and K/V cache entries; 0: the projection writes fp32 and the row kernel
+ * does that.  Both give the same bits.  Returns the previous setting.
+ * Process-wide; not for concurrent use with running steps. */
+int32_t polestar_debug_qkv_fusion(int32_t on);
+
 /* ---- attention kernel selection (test hook) ----
  * 0: the library's choice (the tcgen05 kernel for bf16 head size 128 when
  * its work items fill every SM twice, else the pipelined mma.sync kernel); 1:
