@@ -177,6 +177,9 @@ def make_inputs(w, n_steps, device):
 def class_roofline(name, s, w, peaks):
     if s["launches"] == 0 or s["ms"] <= 0:
         return None
+    if s["bytes"] <= 0 and s["flops"] <= 0:
+        return {"bound": None, "frac": None, "avg_launch_us": s["ms"] * 1e3 / s["launches"],
+                "launches": s["launches"], "note": "no algorithmic byte or flop model for this class"}
     # the roof that bounds the class: its flops at the tensor peak against its
     # algorithmic bytes at the copy rate, whichever takes longer
     tf_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))

@@ -267,6 +267,15 @@ void prof_release(polestar_ctx* c) {
     LAUNCHED(c);                            \
   } while (0)
 
+// A launch over M rows (or the device count at m_dev): fixed + rows x row_bytes.
+#define RUN_ROWS(cls, fixed, row_bytes, M, m_dev, stmt)                 \
+  do {                                                                \
+    const int pi_ = prof_start(c, (cls));                             \
+    stmt;                                                             \
+    prof_stop_rows(c, pi_, (fixed), (row_bytes), 0.0, (M), (m_dev));  \
+    LAUNCHED(c);                                                      \
+  } while (0)
+
 void free_all(polestar_ctx* c) {
   if (c->sm) cudaStreamSynchronize(c->sm);
   if (c->ss && c->ss != c->sm) cudaStreamSynchronize(c->ss);
@@ -464,9 +473,10 @@ polestar_status qkv_rope(polestar_ctx* c, const polestar_layer_weights& w, const
   }
   float* Cs[3] = {c->gout, c->gout + c->qdim, c->gout + c->qdim + c->kvdim};
   TRY(gemm_multi<T>(c, c->a_in, d, 3, Ws, Ns, Cs, c->ldg, R, nullptr, d));
-  RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
-      (launch_rope_scatter<T>(c->gout, c->ldg, rows, write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows, kv_layer,
-                              kv_seq, c->kvdim, c->sm)));
+  // fp32 Q/K/V read, bf16 Q written (the K/V rows written depend on the rows' kinds: not counted)
+  RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)(c->qdim + 2 * c->kvdim) * 4.0 + (double)c->qdim * c->esz, R, nullptr,
+           (launch_rope_scatter<T>(c->gout, c->ldg, rows, write_kv, R, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
+                                   kv_layer, kv_seq, c->kvdim, c->sm)));
   return POLESTAR_OK;
 }
 
@@ -496,7 +506,8 @@ polestar_status gate_up_swiglu(polestar_ctx* c, const polestar_layer_weights& w,
   const void* Ws[2] = {w.w_gate, w.w_up};
   float* Cs[2] = {c->gout, c->gout + F};
   TRY(gemm_multi<T>(c, c->a_in, d, 2, Ws, Ns, Cs, c->ldg, R, m_dev, d));
-  RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_swiglu<T>(c->gout, c->ldg, m_dev, R, F, c->a_in, c->sm)));
+  RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)F * (8.0 + sizeof(T)), R, m_dev,
+           (launch_swiglu<T>(c->gout, c->ldg, m_dev, R, F, c->a_in, c->sm)));
   *act_out = c->a_in;
   return POLESTAR_OK;
 }
@@ -649,13 +660,17 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
     const int ns = std::min(chunk, b - s0);
     const int R = ns * per_seq;
     const int4* rows = rows_all + (size_t)s0 * per_seq;
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_input<T>(x0, rows, R, N, d, c->h_rows, c->sm)));
+    RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * (c->esz + 4), R, nullptr,
+             (launch_gather_input<T>(x0, rows, R, N, d, c->h_rows, c->sm)));
     for (int l = 0; l < L; ++l) {
       const polestar_layer_weights& w = c->W[l];
       if (!fwd_only)
-        RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
-                              (size_t)c->Wmax * d, c->sm)));
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in, c->sm)));
+        RUN(POLESTAR_KC_ROWS, (double)ns * c->nw * d * 8.0, 0.0,
+            (launch_capture_window(c->h_rows, rows, R, d, c->Wmax, c->Hw + (size_t)l * b * c->Wmax * d,
+                                   (size_t)c->Wmax * d, c->sm)));
+      RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * (4 + c->esz), R, nullptr,
+               (launch_rmsnorm<T>(c->h_rows, nullptr, nullptr, rows, nullptr, c->K, w.attn_norm, R, d, eps, c->a_in,
+                                  c->sm)));
       TRY(qkv_rope<T>(c, w, rows, nullptr, R, kv + (size_t)l * kv_layer, kv_seq));
       AttnArgs aa{};
       aa.q = c->q_rows;
@@ -690,18 +705,20 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
       aa.err = tc_error_word(&c->tc);
       RUN(POLESTAR_KC_ATTENTION, attn_bytes, 4.0 * R * N * c->qdim, CUDA_OR_FAIL(c, (launch_row_attention<T>(aa, c->sm))));
       TRY(gemm<T>(c, c->attn_out, c->qdim, w.wo, c->qdim, c->gout, c->ldg, R, nullptr, d, c->qdim));
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
-                                 c->a_in, c->sm)));
+      RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * (12 + c->esz), R, nullptr,
+               (launch_residual_rmsnorm<T>(c->h_rows, nullptr, nullptr, R, c->gout, c->ldg, w.ffn_norm, d, eps,
+                                           c->h1, c->a_in, c->sm)));
       const void* act = nullptr;
       TRY(gate_up_swiglu<T>(c, w, R, nullptr, &act));
       TRY(gemm<T>(c, act, c->F, w.w_down, c->F, c->gout, c->ldg, R, nullptr, d, c->F));
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
-          (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows,
-                                      nullptr, c->sm)));
+      RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * 12.0, R, nullptr,
+               (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, nullptr, nullptr, R, rows, d, c->Wmax, c->h_rows,
+                                           nullptr, c->sm)));
     }
     // the active rows' last-layer outputs: the rows the commit gate scores
     if (!fwd_only)
-      RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_capture_active(c->h_rows, rows, R, d, c->B, c->act_last, c->sm)));
+      RUN(POLESTAR_KC_ROWS, (double)ns * c->B * d * 8.0, 0.0,
+          (launch_capture_active(c->h_rows, rows, R, d, c->B, c->act_last, c->sm)));
   }
   if (fwd_only) return POLESTAR_OK;
   // spherical K-means + residual NVFP4 for every (layer, sequence)
@@ -720,11 +737,15 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
   ka.z = c->z;
   ka.csum = c->csum;
   ka.anchor = c->anchor;
+  // window rows read once, labels / codes / scales written, z, member sums and
+  // anchors written (the iterations' re-reads of the rows are not counted)
+  const double km_bytes = (double)L * b *
+                          ((double)c->nw * d * (4.0 + 0.5 + 1.0 / 16) + (double)c->nw + 3.0 * c->K * d * 4.0);
   if (!c->offload) {
     ka.layer0 = 0;
     ka.codes = c->codes;
     ka.scales = c->scales;
-    RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_kmeans_encode(ka, c->sm)));
+    RUN(POLESTAR_KC_CLUSTER, km_bytes, 0.0, (launch_kmeans_encode(ka, c->sm)));
   } else {
     // every layer at once, the encoder storing straight into the pinned host
     // store through its device mapping; the previous step's write-backs to
@@ -734,18 +755,20 @@ polestar_status block_entry(polestar_ctx* c, const void* x0, int blk, bool fwd_o
     ka.layer0 = 0;
     ka.codes = c->codes_host_dev;
     ka.scales = c->scales_host_dev;
-    RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_kmeans_encode(ka, c->sm)));
+    RUN(POLESTAR_KC_CLUSTER, km_bytes, 0.0, (launch_kmeans_encode(ka, c->sm)));
   }
   // proxy-attention baseline P(t_b, l) of every layer
   const int Rp = (int)pad8((size_t)b * c->K);
   const int4* prow = meta_d<int4>(c, c->ml.prow_off);
   for (int l = 0; l < L; ++l) {
     const polestar_layer_weights& w = c->W[l];
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rmsnorm<T>(nullptr, nullptr, nullptr, prow, c->z + (size_t)l * b * c->K * d, c->K, w.attn_norm, Rp, d,
-                      eps, c->a_in, c->sm)));
+    RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * (4 + c->esz), b * c->K, nullptr,
+             (launch_rmsnorm<T>(nullptr, nullptr, nullptr, prow, c->z + (size_t)l * b * c->K * d, c->K, w.attn_norm,
+                                Rp, d, eps, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, d, w.wq, d, c->gout, c->ldg, Rp, nullptr, c->qdim, d));
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_rope_scatter<T>(c->gout, c->ldg, prow, nullptr, Rp, c->H, c->Hkv, c->dh, c->rope, c->q_rows, nullptr,
-                           0, c->kvdim, c->sm)));
+    RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)c->qdim * (4 + c->esz), b * c->K, nullptr,
+             (launch_rope_scatter<T>(c->gout, c->ldg, prow, nullptr, Rp, c->H, c->Hkv, c->dh, c->rope, c->q_rows,
+                                     nullptr, 0, c->kvdim, c->sm)));
     AttnArgs aa{};
     aa.q = c->q_rows;
     aa.ldq = c->qdim;
@@ -852,13 +875,14 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
   const float eps = c->cfg.rms_eps;
   const int n_active = b * B;
 
-  RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
-      (launch_gather_input<T>(x0, rows, n_active, N, d, c->h_rows, c->sm, c->W[0].attn_norm, eps, c->a_in)));
+  RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * (2 * c->esz + 4), n_active, nullptr,
+           (launch_gather_input<T>(x0, rows, n_active, N, d, c->h_rows, c->sm, c->W[0].attn_norm, eps, c->a_in)));
   uint8_t* sel_prev = c->sel_a;
   uint8_t* sel_cur = c->sel_b;
   if (n_fire > 0) {
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_gather_window<T>(x0, meta_d<int>(c, c->ml.win_pos_off), c->nw, fire_d, n_fire, N, d, c->Wmax, c->U,
-                            sel_prev, c->sm)));
+    RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * (c->esz + 4), n_fire * c->nw, nullptr,
+             (launch_gather_window<T>(x0, meta_d<int>(c, c->ml.win_pos_off), c->nw, fire_d, n_fire, N, d, c->Wmax,
+                                      c->U, sel_prev, c->sm)));
   }
   if (n_fire > 0 && c->offload) {
     // fetches read the host store only after everything queued on the main
@@ -904,9 +928,16 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
       pa.eps = eps;
       pa.a_out = c->a_in;
       pa.proxy_row = proxy_row_d;
-      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_window_patch<T>(pa, c->sm)));
+      // lower bound: every window row's codes read, its layer input and
+      // projection input written, the anchors read once; a patched row also
+      // reads its packet and writes its direction change and new codes
+      RUN_ROWS(POLESTAR_KC_CLUSTER, (double)n_fire * c->K * d * 4.0, (double)d * (0.5 + 1.0 / 16 + 4 + c->esz),
+               n_fire * c->nw, nullptr, (launch_window_patch<T>(pa, c->sm)));
       if (c->offload) TRY(ring_writeback(c, l));
-      RUN(POLESTAR_KC_CLUSTER, 0.0, 0.0, (launch_centroid_update<T>(pa, c->sm)));
+      // member sums read and written, z and the proxy rows' input written (the
+      // selected rows' direction changes it reads are data-dependent: not counted)
+      RUN(POLESTAR_KC_CLUSTER, (double)n_fire * c->K * d * (12.0 + c->esz), 0.0,
+          (launch_centroid_update<T>(pa, c->sm)));
     }
     // the projections' input rows were normalised by their producers: active
     // rows by the previous layer's final residual (or the input gather), window
@@ -993,23 +1024,29 @@ polestar_status within_step(polestar_ctx* c, const void* x0, const int32_t* n_un
     sa.o_src = c->o_src;
     sa.m_o = c->m_o;
     sa.n_active = n_active;
-    RUN(POLESTAR_KC_SELECT, 0.0, 0.0, (launch_select(sa, c->sm)));
+    RUN(POLESTAR_KC_SELECT,
+        (double)n_fire * c->K * c->H * 4.0 + (double)b * c->Wmax * 3.0 + (double)(n_active + n_fire * c->nw) * 4.0, 0.0,
+        (launch_select(sa, c->sm)));
     if (l == L - 1) {
-      RUN(POLESTAR_KC_SELECT, 0.0, 0.0, (launch_delta_finalize(c->kl_rows, b, B, c->H, c->delta, c->sm)));
+      RUN(POLESTAR_KC_SELECT, (double)b * B * c->H * 4.0, 0.0,
+          (launch_delta_finalize(c->kl_rows, b, B, c->H, c->delta, c->sm)));
     }
     // gathered O/FFN over active rows + selected window rows
     const int Rc = n_active + n_fire * c->nw;
-    launch_gather_T<T>(c->attn_out, c->o_src, c->m_o, Rc, c->qdim, c->a_in, c->sm);
-    LAUNCHED(c);
+    RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)c->qdim * 2 * c->esz, Rc, c->m_o,
+             (launch_gather_T<T>(c->attn_out, c->o_src, c->m_o, Rc, c->qdim, c->a_in, c->sm)));
     TRY(gemm<T>(c, c->a_in, c->qdim, w.wo, c->qdim, c->gout, c->ldg, Rc, c->m_o, d, c->qdim));
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_residual_rmsnorm<T>(c->h_rows, c->o_src, c->m_o, Rc, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
-                               c->a_in, c->sm)));
+    RUN_ROWS(POLESTAR_KC_ROWS, 0.0, (double)d * (12 + c->esz), Rc, c->m_o,
+             (launch_residual_rmsnorm<T>(c->h_rows, c->o_src, c->m_o, Rc, c->gout, c->ldg, w.ffn_norm, d, eps, c->h1,
+                                         c->a_in, c->sm)));
     const void* act = nullptr;
     TRY(gate_up_swiglu<T>(c, w, Rc, c->m_o, &act));
     TRY(gemm<T>(c, act, c->F, w.w_down, c->F, c->gout, c->ldg, Rc, c->m_o, d, c->F));
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
-        (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows,
-                                    c->U, c->sm, l + 1 < L ? c->W[l + 1].attn_norm : nullptr, eps, c->a_in)));
+    // every row: two fp32 rows read, one written; the active rows also write
+    // the next layer's projection input
+    RUN_ROWS(POLESTAR_KC_ROWS, l + 1 < L ? (double)n_active * d * c->esz : 0.0, (double)d * 12.0, Rc, c->m_o,
+             (launch_residual_scatter<T>(c->h1, c->gout, c->ldg, c->o_src, c->m_o, Rc, rows, d, c->Wmax, c->h_rows,
+                                         c->U, c->sm, l + 1 < L ? c->W[l + 1].attn_norm : nullptr, eps, c->a_in)));
     std::swap(sel_prev, sel_cur);
   }
   c->sel_last = sel_prev;  // selection of the last layer
@@ -1297,7 +1334,7 @@ polestar_status decode_logits_impl(polestar_ctx* c, const void* lm_head, const v
   a.gain = final_norm;
   a.eps = c->cfg.rms_eps;
   a.out = c->dec_rows;
-  RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_decode_rows<T>(a, c->sm)));
+  RUN(POLESTAR_KC_ROWS, (double)b * 2 * B * d * (4 + c->esz), 0.0, (launch_decode_rows<T>(a, c->sm)));
   TRY(gemm<T>(c, c->dec_rows, d, lm_head, d, logits, vocab, b * 2 * B, nullptr, vocab, d));
   return POLESTAR_OK;
 }
@@ -1324,7 +1361,8 @@ extern "C" polestar_status polestar_decode_tokens(polestar_ctx* c, const float* 
   if (vocab < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "vocab must be >= 1");
   if (!c->committed) return fail(c, POLESTAR_ERR_STATE, "polestar_decode_tokens needs a preceding polestar_commit");
   const int b = c->b, B = c->B;
-  RUN(POLESTAR_KC_COMMIT, 0.0, 0.0, (launch_argmax(logits, vocab, b * 2 * B, c->dec_ids, c->sm)));
+  RUN(POLESTAR_KC_COMMIT, (double)b * 2 * B * vocab * 4.0, 0.0,
+      (launch_argmax(logits, vocab, b * 2 * B, c->dec_ids, c->sm)));
   ApplyArgs a{};
   a.commit = commit_mask;
   a.conf = c->conf;
@@ -1354,11 +1392,12 @@ extern "C" polestar_status polestar_embed(polestar_ctx* c, const void* embed, in
   if (!embed || !mask_emb || !tokens || !masked || !x0) return fail(c, POLESTAR_ERR_INVALID_ARG, "NULL buffer");
   if (vocab < 1) return fail(c, POLESTAR_ERR_INVALID_ARG, "vocab must be >= 1");
   const int rows = c->b * c->N;
+  const double eb = (double)rows * c->d * 2.0 * c->esz;  // one table row read, one input row written
   if (c->bf16)
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0,
+    RUN(POLESTAR_KC_ROWS, eb, 0.0,
         (launch_embed<__nv_bfloat16>(embed, mask_emb, tokens, masked, vocab, rows, c->d, x0, c->sm)));
   else
-    RUN(POLESTAR_KC_ROWS, 0.0, 0.0, (launch_embed<float>(embed, mask_emb, tokens, masked, vocab, rows, c->d, x0, c->sm)));
+    RUN(POLESTAR_KC_ROWS, eb, 0.0, (launch_embed<float>(embed, mask_emb, tokens, masked, vocab, rows, c->d, x0, c->sm)));
   return POLESTAR_OK;
 }
 
