@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(256) window_patch_kernel(PatchArgs a) {
 constexpr int CU_THREADS = 256;
 
 template <typename T>
-__global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a, int nc, int cw) {
+__global__ void __launch_bounds__(CU_THREADS, 2) centroid_update_kernel(PatchArgs a, int nc, int cw) {
   __shared__ float4 part[CU_THREADS][KM_MAXK];  // [row lane * groups + group][cluster]
   __shared__ float nrm_part[1][KM_MAXK], nrm_full[1][KM_MAXK];
   __shared__ float wsum[CU_THREADS / 32][KM_MAXK];
@@ -545,7 +545,9 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
   __syncthreads();
   float* cs_base = a.csum + (size_t)s * K * d;
   float ssl[KM_MAXK];
-  float4 ckeep[KM_MAXK];  // one-pass layout: this thread's updated member sums, reused for z
+  // this thread's group sums; after the last pass (the only one when one_pass)
+  // the updated member sums, reused for z
+  float4 acc[KM_MAXK];
 #pragma unroll
   for (int c = 0; c < KM_MAXK; ++c) ssl[c] = 0.f;
   // RL > 1: one pass, thread t = lane rl * G + group cg.  RL == 1: group
@@ -555,26 +557,20 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
     const int cg = RL > 1 ? t % G : cgb + t;
     const int rl = RL > 1 ? t / G : 0;
     const bool act = RL > 1 ? t < RL * G : cg < G;
-    float4 acc[KM_MAXK];
 #pragma unroll
     for (int c = 0; c < KM_MAXK; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // the member sums this thread will update, requested alongside the rows
-    float4 csv[KM_MAXK];
-#pragma unroll
-    for (int c = 0; c < KM_MAXK; ++c)
-      csv[c] = (act && rl == 0 && c < K) ? *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
     if (act) {
       const float* dn = a.dn + (size_t)s * a.Wmax * d + c0 + cg * 4;
-      for (int j0 = rl; j0 < nw; j0 += 16 * RL) {
-        float4 v[16];
+      constexpr int DEPTH = 8;  // row loads in flight per thread
+      for (int j0 = rl; j0 < nw; j0 += DEPTH * RL) {
+        float4 v[DEPTH];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < DEPTH; ++u) {
           const int j = j0 + u * RL;
           v[u] = (j < nw && sl[j]) ? *(const float4*)(dn + (size_t)j * d) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < DEPTH; ++u) {
           const int j = j0 + u * RL;
           if (j >= nw || !sl[j]) continue;
           const int lab = lb[j];
@@ -617,13 +613,13 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
       for (int c = 0; c < KM_MAXK; ++c) {
         if (c >= K) continue;
         float* cs = cs_base + (size_t)c * d + c0 + cg * 4;
-        float4 v = csv[c];
+        float4 v = *(const float4*)cs;
         v.x += acc[c].x;
         v.y += acc[c].y;
         v.z += acc[c].z;
         v.w += acc[c].w;
         *(float4*)cs = v;
-        ckeep[c] = v;
+        acc[c] = v;
         ssl[c] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
       }
     }
@@ -653,7 +649,7 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
     for (int c = 0; c < KM_MAXK; ++c) {
       if (c >= K) continue;
       const float nrm = sqrtf(nrm_full[0][c]);
-      const float4 v = one_pass ? ckeep[c] : *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4);
+      const float4 v = one_pass ? acc[c] : *(const float4*)(cs_base + (size_t)c * d + c0 + cg * 4);
       const float4 zv = make_float4(v.x / nrm, v.y / nrm, v.z / nrm, v.w / nrm);
       *(float4*)(a.z + ((size_t)s * K + c) * d + c0 + cg * 4) = zv;
       T* ao = (T*)a.a_out + (size_t)(a.proxy_row[s] + c) * d + c0 + cg * 4;
@@ -662,13 +658,15 @@ __global__ void __launch_bounds__(CU_THREADS) centroid_update_kernel(PatchArgs a
   }
 }
 
-// Cluster size of the centroid update: the fewest CTAs (at most 16) that give
-// each CTA at most 256 channels in whole 4-channel groups, else the fewest with
-// whole groups.
+// Cluster size of the centroid update: the fewest CTAs (at most 8, a portable
+// cluster) that give each CTA at most 512 channels in whole 4-channel groups,
+// else the most CTAs up to 8 with whole groups.  At two CTAs per SM every
+// sequence of a batch of 32 then has its cluster resident at once on GB300
+// (16-CTA clusters at one CTA per SM ran the batch in four waves).
 int centroid_cluster_size(int d) {
-  for (int nc = 1; nc <= 16; ++nc)
-    if (d % (4 * nc) == 0 && d / nc <= 256) return nc;
-  for (int nc = 16; nc >= 1; --nc)
+  for (int nc = 1; nc <= 8; ++nc)
+    if (d % (4 * nc) == 0 && d / nc <= 512) return nc;
+  for (int nc = 8; nc >= 1; --nc)
     if (d % (4 * nc) == 0) return nc;
   return 1;
 }
@@ -681,10 +679,6 @@ template <typename T>
 void launch_centroid_update(const PatchArgs& a, cudaStream_t st) {
   const int nc = centroid_cluster_size(a.d);
   const int cw = a.d / nc;
-  static PerDeviceOnce nonportable;  // a driver call per launch costs host time
-  if (nc > 8)
-    func_attr_once(nonportable, (const void*)centroid_update_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                   1);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(nc, a.n_fire);
   cfg.blockDim = dim3(CU_THREADS);
