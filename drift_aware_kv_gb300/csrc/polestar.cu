@@ -125,6 +125,10 @@ struct polestar_ctx {
   float* st_logits = nullptr;
   size_t st_logits_cap = 0;
   uint8_t *st_masked = nullptr, *st_commit = nullptr;
+  // polestar_step_host: the commit's inputs (logits, mask) come in on a copy
+  // stream of the context's own while the calibration step computes
+  cudaStream_t st_copy = nullptr;
+  cudaEvent_t st_copy_ev = nullptr;
 
   std::vector<void*> dev_allocs;
   std::vector<void*> host_allocs;
@@ -295,6 +299,13 @@ void free_all(polestar_ctx* c) {
     c->ring_in[i] = c->ring_used[i] = c->ring_out[i] = nullptr;
   }
   c->meta_ev = c->side_ev = c->main_ev = nullptr;
+  if (c->st_copy) {
+    cudaStreamSynchronize(c->st_copy);
+    cudaStreamDestroy(c->st_copy);
+  }
+  if (c->st_copy_ev) cudaEventDestroy(c->st_copy_ev);
+  c->st_copy = nullptr;
+  c->st_copy_ev = nullptr;
   tc_gemm_cache_clear(&c->tc);
   prof_release(c);
 }
@@ -1420,10 +1431,25 @@ extern "C" polestar_status polestar_step_host(polestar_ctx* c, const void* x0_ho
     TRY(dalloc(c, &c->st_logits, lg_bytes));
     c->st_logits_cap = lg_bytes;
   }
+  if (!c->st_copy) {
+    CUDA_OR_FAIL(c, cudaStreamCreateWithFlags(&c->st_copy, cudaStreamNonBlocking));
+    CUDA_OR_FAIL(c, cudaEventCreateWithFlags(&c->st_copy_ev, cudaEventDisableTiming));
+  }
+  // the calibration step needs x0 first; the logits and mask only feed the
+  // commit, so they are copied on the copy stream while the step computes
+  // (the previous call's commit finished reading the staging buffers before
+  // that call returned)
   CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_x0, x0_host, x0_bytes, cudaMemcpyHostToDevice, c->sm));
-  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_logits, logits_host, lg_bytes, cudaMemcpyHostToDevice, c->sm));
-  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_masked, masked_host, (size_t)c->b * c->N, cudaMemcpyHostToDevice, c->sm));
-  TRY(polestar_calibrate_step(c, c->st_x0, n_unmasked, block_index, block_entry, nullptr));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_logits, logits_host, lg_bytes, cudaMemcpyHostToDevice, c->st_copy));
+  CUDA_OR_FAIL(c, cudaMemcpyAsync(c->st_masked, masked_host, (size_t)c->b * c->N, cudaMemcpyHostToDevice,
+                                  c->st_copy));
+  CUDA_OR_FAIL(c, cudaEventRecord(c->st_copy_ev, c->st_copy));
+  const polestar_status cs = polestar_calibrate_step(c, c->st_x0, n_unmasked, block_index, block_entry, nullptr);
+  CUDA_OR_FAIL(c, cudaStreamWaitEvent(c->sm, c->st_copy_ev, 0));
+  if (cs != POLESTAR_OK) {
+    cudaStreamSynchronize(c->st_copy);
+    return cs;
+  }
   TRY(polestar_commit(c, c->st_logits, vocab, c->st_masked, c->st_commit, nullptr));
   CUDA_OR_FAIL(c, cudaMemcpyAsync(commit_mask_host, c->st_commit, (size_t)c->b * 2 * c->B, cudaMemcpyDeviceToHost,
                                   c->sm));

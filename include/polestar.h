@@ -191,12 +191,14 @@ polestar_status polestar_decode_tokens(polestar_ctx *ctx, const float *logits, i
 polestar_status polestar_embed(polestar_ctx *ctx, const void *embed, int32_t vocab, const void *mask_emb,
                                const int32_t *tokens, const uint8_t *masked, void *x0);
 
-/* End-to-end step on HOST buffers: copies x0 (host [batch, N, d], config dtype),
- * logits (host [batch, 2B, vocab] fp32) and masked (host [batch, N] uint8) to the
- * device on the main stream, runs polestar_calibrate_step + polestar_commit,
+/* End-to-end step on HOST buffers: copies x0 (host [batch, N, d], config dtype)
+ * to the device on the main stream and logits (host [batch, 2B, vocab] fp32) and
+ * masked (host [batch, N] uint8) on a copy stream of the context's own, so that
+ * they arrive while polestar_calibrate_step computes; then runs polestar_commit,
  * copies the commit mask back to commit_mask_host ([batch, 2B] uint8) and
- * synchronises the main stream.  Host buffers should be pinned for full
- * bandwidth.  Staging buffers are allocated on first use. */
+ * synchronises the main stream.  The host buffers may be reused as soon as the
+ * call returns.  Host buffers should be pinned for full bandwidth.  Staging
+ * buffers and the copy stream are created on first use. */
 polestar_status polestar_step_host(polestar_ctx *ctx, const void *x0_host, const int32_t *n_unmasked,
                                    int32_t block_index, int32_t block_entry,
                                    const float *logits_host, int32_t vocab,

@@ -75,3 +75,46 @@ def test_host_offload_is_bit_identical(name, steps, side):
     ref.close()
     off.close()
     assert fired >= 1
+
+
+@pytest.mark.parametrize("name,steps", [("tiny_l1_d256_fp32", 16), ("mini_l2_d512_bf16", 14)])
+def test_step_host_is_bit_identical(name, steps):
+    """polestar_step_host (host inputs, the commit's inputs copied on the
+    context's copy stream while the calibration computes) against the same
+    steps on device buffers: identical state and commit masks at every step.
+    One set of pinned host buffers is rewritten for every step, as a caller
+    reusing its staging buffers does once the call has returned."""
+    from drift_aware_kv_gb300 import polestar as P
+    from drift_aware_kv_gb300 import synth
+    w = synth.WORKLOADS[name]
+    W = synth.make_weights(w, "cuda")
+    ref = P.Polestar(w, W)
+    hst = P.Polestar(w, W)
+    tr = synth.Trajectory(w)
+    dt = synth.torch_dtype(w)
+    cm_r = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8, device="cuda")
+    cm_h = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8).pin_memory()
+    x0_h = logits_h = masked_h = None
+    for _ in range(steps):
+        st = tr.next_step()
+        if st is None:
+            break
+        x0 = st["x0"].to(dt)
+        logits, masked = st["logits"].float(), st["masked"].to(torch.uint8)
+        if x0_h is None:
+            x0_h = torch.empty_like(x0).pin_memory()
+            logits_h = torch.empty_like(logits).pin_memory()
+            masked_h = torch.empty_like(masked).pin_memory()
+        x0_h.copy_(x0)
+        logits_h.copy_(logits)
+        masked_h.copy_(masked)
+        out_r = ref.calibrate_step(x0.cuda(), st["n_unmasked"], st["block_index"], st["block_entry"])
+        ref.commit(logits.cuda(), masked.cuda(), cm_r)
+        hst.step_host(x0_h, st["n_unmasked"], st["block_index"], st["block_entry"], logits_h, masked_h, cm_h)
+        torch.cuda.synchronize()
+        a, b = _state(ref, w, out_r), _state(hst, w, out_r)
+        for k in a:
+            assert np.array_equal(a[k], b[k]), (st["t"], k)
+        assert torch.equal(cm_r.cpu(), cm_h), st["t"]
+    ref.close()
+    hst.close()
