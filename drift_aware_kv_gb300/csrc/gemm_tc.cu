@@ -88,6 +88,15 @@ struct Params {
   __nv_bfloat16* kv_layer;
   long long kv_seq_stride;
   int kvdim, dh;
+  // two-SM pair kernel, one plain segment: when the tiles leave the last wave
+  // partly empty, each of those `rem` tiles is split along K over S clusters
+  // (S = clusters / rem, capped).  Every split writes its partial tile to
+  // tail_ws and counts it in tail_cnt; once all S are in, split s sums column
+  // slice s of the tile over the splits in split order and writes it to C
+  // (deterministic); the last split to finish clears the counters.  Null: no
+  // split.
+  float* tail_ws;  // [rem * S <= clusters][2 CTAs][BM][256] fp32
+  int* tail_cnt;   // [rem][2 CTAs][4 lane quarters] x 32 ints (count, done at +16), zero between launches
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -818,6 +827,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 // even), so each stage's uses are issued in order by one warp and its parity
 // waits never run more than one phase ahead of the barrier.
 constexpr int P2_LOADERS = 2;
+constexpr int P2_TAIL_MAX_SPLIT = 8;    // K splits of a tail tile at most
+constexpr int P2_TAIL_MIN_SPLIT = 4;    // fewer possible splits: no split
+constexpr int P2_TAIL_MIN_STAGES = 64;  // stages per tile below which tails are not split
 // Tile t of the pair kernel's walk -> (row pair, column block): groups of g
 // row pairs (the last one shorter), row pairs fastest inside a group.
 __device__ __forceinline__ void p2_tile(long long t, int mpairs, int ntn, int g, int* mp, int* nb) {
@@ -895,6 +907,40 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
   const int mpairs = (M_eff + 2 * BM - 1) / (2 * BM);
   const long long ntiles = *abort_flag ? 0 : (long long)mpairs * p.ntn;
   const int nk = (p.ktiles + KP - 1) / KP;  // stages per tile
+  // Work of this cluster: its whole tiles t = cid + i ncl below full_tiles,
+  // then (with a split tail) one K range of a tail tile.  Every cluster derives
+  // the same schedule from the live row count.
+  long long full_tiles = ntiles;
+  int tail_S = 1, tail_rem = 0;
+  if (p.tail_ws && ntiles > 0) {
+    const long long full = ntiles / ncl;
+    const int rem = (int)(ntiles - full * ncl);
+    // measured on GB300: two-way splits and short K (one 4096-deep tile)
+    // lost more to the partial tiles' round trip than the shorter tail gained
+    const int S = rem > 0 ? min(ncl / rem, P2_TAIL_MAX_SPLIT) : 1;
+    if (S >= P2_TAIL_MIN_SPLIT && nk >= P2_TAIL_MIN_STAGES) {
+      full_tiles = full * ncl;
+      tail_S = S;
+      tail_rem = rem;
+    }
+  }
+  const bool has_tail = tail_S >= 2 && cid < tail_rem * tail_S;
+  const int tail_tile = has_tail ? cid / tail_S : 0;  // 0 .. rem-1
+  const int tail_s = has_tail ? cid % tail_S : 0;     // split of that tile
+  const long long n_dp = full_tiles > cid ? (full_tiles - cid + ncl - 1) / ncl : 0;
+  const long long n_units = n_dp + (has_tail ? 1 : 0);
+  // unit i -> tile and stage range
+  auto unit = [&](long long i, long long* t, int* k0, int* k1) {
+    if (i < n_dp) {
+      *t = cid + i * ncl;
+      *k0 = 0;
+      *k1 = nk;
+    } else {
+      *t = full_tiles + tail_tile;
+      *k0 = (int)((long long)tail_s * nk / tail_S);
+      *k1 = (int)((long long)(tail_s + 1) * nk / tail_S);
+    }
+  };
 
   if (warp == 0 || warp >= 6) {
     // ---------------- TMA producers, completing on the leader's stage barrier.
@@ -908,7 +954,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
     if (lane == 0 && (split_ab ? (warp == 0 || warp == 6) : lj < p.nload)) {
       long long it = 0;
       bool live = true;
-      for (long long t = cid; t < ntiles && live; t += ncl) {
+      for (long long ui = 0; ui < n_units && live; ++ui) {
+        long long t;
+        int k0, k1;
+        unit(ui, &t, &k0, &k1);
         int mp, nb;
         p2_tile(t, mpairs, p.ntn, p.group, &mp, &nb);
         const int sg = (nb >= p.seg_start[1]) + (nb >= p.seg_start[2]);
@@ -917,7 +966,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         const CUtensorMap* tmB = p.act ? (rank == 0 ? &tmB0 : &tmB1) : (sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2));
         const int wrow = p.act ? nb * (bn / 2) : (nb - p.seg_start[sg]) * bn + rank * (bn / 2);
         const int m0 = mp * 2 * BM + rank * BM;
-        for (int k = 0; k < nk; ++k, ++it) {
+        for (int k = k0; k < k1; ++k, ++it) {
           const int s = (int)(it % STAGES);
           if (!split_ab && s % p.nload != lj) continue;
           if (it >= STAGES && !mbar_wait_cluster(smem_u32(&empty[s]), (uint32_t)((it / STAGES) - 1) & 1u, p.err, 1,
@@ -953,14 +1002,17 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
       long long it = 0;
       int tl = 0;
       bool live = true;
-      for (long long t = cid; t < ntiles && live; t += ncl, ++tl) {
+      for (long long ui = 0; ui < n_units && live; ++ui, ++tl) {
+        long long t;
+        int k0, k1;
+        unit(ui, &t, &k0, &k1);
         const int b = tl & 1;
         if (tl >= 2 &&
             !mbar_wait_cluster(smem_u32(&acc_empty[b]), (uint32_t)((tl >> 1) - 1) & 1u, p.err, 5, abort_flag))
           break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t d = tmem + (uint32_t)(b * bn);
-        for (int k = 0; k < nk; ++k, ++it) {
+        for (int k = k0; k < k1; ++k, ++it) {
           const int s = (int)(it % STAGES);
           if (!mbar_wait_cluster(smem_u32(&full[s]), (uint32_t)(it / STAGES) & 1u, p.err, 2, abort_flag)) {
             live = false;
@@ -973,7 +1025,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               umma_pair(d, smem_desc(st + kb * A_BLK + kk * 32), smem_desc(st + A_BYTES + kb * B_BLK + kk * 32), idesc,
-                        (k > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+                        (k > k0 || kb > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&empty[s]), PAIR);  // stage s free in both CTAs once read
         }
@@ -986,7 +1038,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
     const bool vec = ((p.ldc & 3) == 0);
     const uint32_t lead_acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
     int tl = 0;
-    for (long long t = cid; t < ntiles; t += ncl, ++tl) {
+    for (long long ui = 0; ui < n_units; ++ui, ++tl) {
+      long long t;
+      int k0, k1;
+      unit(ui, &t, &k0, &k1);
+      const bool tail = ui >= n_dp;
       const int b = tl & 1;
       const bool ok =
           mbar_wait_cluster(smem_u32(&acc_full[b]), (uint32_t)(tl >> 1) & 1u, p.err, 3, abort_flag, 256);
@@ -1094,6 +1150,99 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(lead_acc_empty0 + (uint32_t)(b * 8));
+        continue;
+      }
+      if (tail) {
+        // split tail tile: every split writes its partial rows, waits for the
+        // other splits' (bounded), then sums one column slice of the tile over
+        // all splits in split order and writes it to C (deterministic)
+        int* const cnt = p.tail_cnt + (((size_t)tail_tile * 2 + rank) * 4 + q) * 32;  // own 128-byte line
+        int* const done = cnt + 16;
+        const size_t wsplit = (size_t)2 * BM * 256;  // floats between consecutive splits' partials
+        float* const w0 = p.tail_ws + (((size_t)tail_tile * tail_S * 2 + rank) * BM + q * 32 + lane) * 256;
+#pragma unroll 1
+        for (int c = 0; c < bn; c += 16) {
+          float v[16];
+          tmem_ld16(tq + c, v);
+          float* w = w0 + tail_s * wsplit + c;
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) *(float4*)(w + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+        // accumulator drained: the MMA warp may go on
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_cluster(lead_acc_empty0 + (uint32_t)(b * 8));
+          __threadfence();
+          atomicAdd(cnt, 1);
+          const long long t0 = clock64();
+          while (true) {
+            int got;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(got) : "l"(cnt) : "memory");
+            if (got >= tail_S) break;
+            if (*abort_flag) break;
+            if (clock64() - t0 > g_wait_limit_cycles) {
+              atomicExch(p.err, 7);
+              *abort_flag = 1;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        __syncwarp();
+        int got;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(got) : "l"(cnt) : "memory");
+        if (got >= tail_S && row < M_eff) {
+          const int n4 = bn / 4;
+          const int c4a = (int)((long long)tail_s * n4 / tail_S), c4b = (int)((long long)(tail_s + 1) * n4 / tail_S);
+          float* dst = Cseg + (size_t)row * p.ldc + n0;
+#pragma unroll 1
+          for (int c4 = c4a; c4 < c4b; c4 += 4) {
+            float4 acc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+            for (int sp = 0; sp < tail_S; ++sp) {
+              const float* w = w0 + sp * wsplit;
+              float4 x[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) x[u] = c4 + u < c4b ? *(const float4*)(w + (c4 + u) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (sp == 0) {
+                  acc[u] = x[u];
+                } else {
+                  acc[u].x += x[u].x;
+                  acc[u].y += x[u].y;
+                  acc[u].z += x[u].z;
+                  acc[u].w += x[u].w;
+                }
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int col = (c4 + u) * 4;
+              if (c4 + u >= c4b) continue;
+              if (n0 + col + 4 <= segN && vseg) {
+                *(float4*)(dst + col) = acc[u];
+              } else {
+                const float e[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+                for (int j = 0; j < 4; ++j)
+                  if (n0 + col + j < segN) dst[col + j] = e[j];
+              }
+            }
+          }
+        }
+        // the last split to finish reading clears both counters for the next launch
+        __syncwarp();
+        if (lane == 0) {
+          const int d = atomicAdd(done, 1);
+          if (d == tail_S - 1) {
+            *cnt = 0;
+            *done = 0;
+          }
+        }
         continue;
       }
 #pragma unroll 1
@@ -1660,6 +1809,21 @@ cudaError_t tc_gemm_bf16_multi(TcGemmCache* cache, const void* A, int lda, int n
     p.group = p2_group(M, K);
     const CUtensorMap* ma = p.kpack == 1 ? get_map(cache, A, M, K, lda, BM) : get_map3(cache, A, M, K, lda, BM, p.kpack);
     if (!ma) return cudaErrorInvalidValue;
+    if (nseg == 1) {
+      // split tail: rem tail tiles split S >= 2 ways with rem * S <= ncl, so at
+      // most ncl partial tiles and ncl / 2 counted tiles
+      if (!cache->tail_ws) {
+        const size_t slots = (size_t)std::max(1, nsm / 2);
+        cudaError_t e = cudaMalloc(&cache->tail_ws, slots * 2 * BM * 256 * sizeof(float));
+        if (e == cudaSuccess) e = cudaMalloc(&cache->tail_cnt, slots * 8 * 32 * sizeof(int));
+        if (e == cudaSuccess) e = cudaMemsetAsync(cache->tail_cnt, 0, slots * 8 * 32 * sizeof(int), st);
+        if (e != cudaSuccess) return e;
+      }
+      if (ncl <= std::max(1, nsm / 2)) {
+        p.tail_ws = cache->tail_ws;
+        p.tail_cnt = cache->tail_cnt;
+      }
+    }
     return launch_p2(ma, mb, p, ncl, st);
   }
   if (kind != 1 && kind != 2) return cudaErrorInvalidValue;
@@ -1921,6 +2085,10 @@ void tc_gemm_cache_clear(TcGemmCache* c) {
   c->maps.clear();
   if (c->err) cudaFree(c->err);
   c->err = nullptr;
+  if (c->tail_ws) cudaFree(c->tail_ws);
+  if (c->tail_cnt) cudaFree(c->tail_cnt);
+  c->tail_ws = nullptr;
+  c->tail_cnt = nullptr;
 }
 
 }  // namespace polestar

@@ -37,6 +37,11 @@ struct TcGemmCache {
   // automatic launch choices by shape {M, K, segments, N0, N1, N2, SMs} ->
   // {kernel, bn, splits, stages}: the search runs once per shape
   std::map<std::array<int, 7>, std::array<int, 4>> picks;
+  // pair kernel's split tail (single plain segment): partial tiles and their
+  // counters, allocated on first use; launches through one cache run one at a
+  // time (stream order)
+  float* tail_ws = nullptr;
+  int* tail_cnt = nullptr;
 };
 
 // Kernel choice for tuning sweeps and tests; zero fields are chosen

@@ -205,6 +205,41 @@ def test_two_sm_pair_grouped_walk(M, N, K):
     _check_gemm(P.gemm_path(7, 0, 1, 192), M, N, K)
 
 
+# the pair kernel's split tail: with a device row count, the tiles of the last,
+# partly filled wave are split along K over the idle clusters (each split sums
+# one column slice over all splits' partial tiles, in split order) when at
+# least four splits fit and a tile is at least 64 stages deep (K = 12288 at two
+# k-blocks per stage).  With 76 clusters: 2560 rows leave 8 tail tiles (eight
+# splits each), 256 rows 16 tiles in all (four splits each), 300 and 4096 rows
+# too many for a split.  Live rows must match the definition, rows past the
+# count stay untouched, and repeated launches (the split counters cleared by
+# each launch for the next) give identical bits.
+@pytest.mark.parametrize("m_live", [2560, 256, 300, 4096, 0])
+def test_two_sm_pair_split_tail(m_live):
+    from drift_aware_kv_gb300 import polestar as P
+    g = torch.Generator(device="cpu").manual_seed(11)
+    M, N, K = 4096, 4096, 12288
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W = (0.02 * torch.randn(N, K, generator=g)).to(torch.bfloat16).cuda()
+    m = torch.tensor([m_live], dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(3):
+        C = torch.full((M, N), -7.0, device="cuda")
+        P.debug_gemm(A, W, C, P.gemm_path(7, 0, 2, 256), m_dev=m)
+        torch.cuda.synchronize()
+        outs.append(C)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    C = outs[0]
+    assert torch.all(C[m_live:] == -7.0)
+    if m_live:
+        rows = np.unique(np.linspace(0, m_live - 1, 48).astype(int))
+        ref = _ref(A, W, rows)
+        got = C[rows].double().cpu().numpy()
+        scale = np.sqrt((A[rows].double().cpu().numpy() ** 2).sum(1))[:, None] * \
+            np.sqrt((W.double().cpu().numpy() ** 2).sum(1))[None, :]
+        assert (np.abs(got - ref) / scale).max() < 2e-6
+
+
 def test_gate_up_swiglu_matches_unfused():
     """The fused epilogue computes silu(g) * u from the same fp32 accumulators as
     the unfused projections (same kernel, same tile width), so the results agree
