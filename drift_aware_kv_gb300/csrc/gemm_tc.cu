@@ -2081,6 +2081,12 @@ cudaError_t tc_gemm_choice(TcGemmCache* cache, int M, int nseg, const int* N, in
   return cudaSuccess;
 }
 
+cudaError_t tc_gemm_reset_after_timeout(TcGemmCache* c, cudaStream_t st) {
+  if (!c->tail_cnt) return cudaSuccess;
+  const size_t slots = (size_t)std::max(1, c->num_sms / 2);
+  return cudaMemsetAsync(c->tail_cnt, 0, slots * 8 * 32 * sizeof(int), st);
+}
+
 void tc_gemm_cache_clear(TcGemmCache* c) {
   c->maps.clear();
   if (c->err) cudaFree(c->err);

@@ -126,5 +126,8 @@ int* tc_error_word(TcGemmCache* cache);
 cudaError_t tc_debug_stalled_wait(int* err, int code, long long limit_cycles, cudaStream_t st);
 
 void tc_gemm_cache_clear(TcGemmCache* cache);
+// After a reported wait timeout: clear the split-tail counters, which a launch
+// that gave up may have left counted (stream-ordered on st).
+cudaError_t tc_gemm_reset_after_timeout(TcGemmCache* cache, cudaStream_t st);
 
 }  // namespace polestar

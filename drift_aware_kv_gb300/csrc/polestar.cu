@@ -535,6 +535,7 @@ polestar_status check_timeouts(polestar_ctx* c) {
   if (code == 0) return POLESTAR_OK;
   *c->err_host = 0;
   cudaMemsetAsync(c->tc.err, 0, sizeof(int), c->sm);
+  tc_gemm_reset_after_timeout(&c->tc, c->sm);
   return fail(c, POLESTAR_ERR_TIMEOUT, "a device wait timed out (code " + std::to_string(code) +
                                            "); the step's results are not valid");
 }
