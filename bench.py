@@ -324,36 +324,41 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
         # the same warm-up (the last three warm-up steps also through the host path)
         n_e = min(args.e2e_steps, len(timed))
         ew = min(n_warmup, 3)
-        log(f"{w.name}: pinned host copies of {ew + n_e} steps' inputs")
+        log(f"{w.name}: host copies of {ew + n_e} steps' inputs")
         host = []
         for st in steps[n_warmup - ew: n_warmup + n_e]:
-            host.append(dict(x0=st["x0"].cpu().pin_memory(), logits=st["logits"].cpu().pin_memory(),
-                             masked=st["masked"].cpu().pin_memory(), n_unmasked=st["n_unmasked"],
-                             block_index=st["block_index"], block_entry=st["block_entry"]))
-        # each pinned buffer is read once by a DMA before timing: the first
-        # copies out of freshly pinned host memory run several times slower
-        # (measured on GB300: 150-220 ms for the first 1.57 GB steps against
-        # 8 ms once warm), a one-time cost that staging buffers reused from
-        # step to step do not pay
-        for hb in host:
-            for k in ("x0", "logits", "masked"):
-                torch.empty_like(hb[k], device=dev).copy_(hb[k], non_blocking=True)
-            torch.cuda.synchronize(dev)
+            host.append(dict(x0=st["x0"].cpu(), logits=st["logits"].cpu(), masked=st["masked"].cpu(),
+                             n_unmasked=st["n_unmasked"], block_index=st["block_index"],
+                             block_entry=st["block_entry"]))
+        # two pinned staging sets, reused alternately as a serving loop reuses
+        # its staging buffers: each step's inputs are written into one before
+        # the step (untimed: that is the inputs' arrival in pinned memory), and
+        # each call of polestar_step_host is timed from the host (it returns
+        # with the result copied back and the stream synchronised).  Fresh
+        # pinned buffers per step (17 GB here) made the copies 2-25x slower on
+        # some GB300 machines, varying from box to box.
+        stage = [{k: torch.empty_like(host[0][k]).pin_memory() for k in ("x0", "logits", "masked")}
+                 for _ in range(2)]
         ps2 = P.Polestar(w, W, stream=stream, side_stream=side, host_offload=offload)
         cmh = torch.zeros(w.batch, 2 * w.block, dtype=torch.uint8).pin_memory()
         for st in steps[:n_warmup - ew]:
             ps2.calibrate_step(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"])
             ps2.commit(st["logits"], st["masked"], cm)
-        for st in host[:ew]:
-            ps2.step_host(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"], st["logits"],
-                          st["masked"], cmh)
+
+        def host_step(i, st):
+            sb = stage[i % 2]
+            for k in ("x0", "logits", "masked"):
+                sb[k].copy_(st[k])
+            t = time.perf_counter()
+            ps2.step_host(sb["x0"], st["n_unmasked"], st["block_index"], st["block_entry"], sb["logits"],
+                          sb["masked"], cmh)
+            return time.perf_counter() - t
+
+        for i, st in enumerate(host[:ew]):
+            host_step(i, st)
         log(f"{w.name}: end-to-end region")
         barrier(ws)
-        t0 = time.perf_counter()
-        for st in host[ew:]:
-            ps2.step_host(st["x0"], st["n_unmasked"], st["block_index"], st["block_entry"], st["logits"],
-                          st["masked"], cmh)
-        e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
+        e2e_s = max_over_ranks(sum(host_step(ew + i, st) for i, st in enumerate(host[ew:])), ws, dev)
         ps2.close()
         h2d = host[0]["x0"].numel() * host[0]["x0"].element_size() + \
             host[0]["logits"].numel() * 4 + host[0]["masked"].numel()
@@ -363,10 +368,11 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(cmh.numel()),
                "steps": n_e, "block_entries": n_e_entry,
                "device_value_same_steps": 1e3 * n_e / dev_ms if dev_ms > 0 else None,
-               "what": f"the first {n_e} timed steps through polestar_step_host from pinned host buffers "
-                       "(x0, logits and mask in, commit mask out, copies inside the timed region; each "
-                       "buffer read once by an untimed DMA beforehand, as reused staging buffers would be)"}
-        del host
+               "what": f"the first {n_e} timed steps, each one call of polestar_step_host timed from the host "
+                       "(x0, logits and mask copied in from pinned staging buffers, commit mask copied out, "
+                       "stream synchronised); two staging sets reused alternately, each filled with its "
+                       "step's inputs before the call"}
+        del host, stage
 
     closed = None
     if full and not args.no_closed_loop:
