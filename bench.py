@@ -335,8 +335,8 @@ def run_workload(args, w, peaks, ws, rank, local, n_warmup, n_timed, full):
         # the step (untimed: that is the inputs' arrival in pinned memory), and
         # each call of polestar_step_host is timed from the host (it returns
         # with the result copied back and the stream synchronised).  Fresh
-        # pinned buffers per step (17 GB here) made the copies 2-25x slower on
-        # some GB300 machines, varying from box to box.
+        # pinned buffers per step (17 GB at batch 32) made the copies 2-25x
+        # slower on some GB300 machines, differently from machine to machine.
         stage = [{k: torch.empty_like(host[0][k]).pin_memory() for k in ("x0", "logits", "masked")}
                  for _ in range(2)]
         ps2 = P.Polestar(w, W, stream=stream, side_stream=side, host_offload=offload)
