@@ -829,7 +829,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 constexpr int P2_LOADERS = 2;
 constexpr int P2_TAIL_MAX_SPLIT = 8;    // K splits of a tail tile at most
 constexpr int P2_TAIL_MIN_SPLIT = 4;    // fewer possible splits: no split
-constexpr int P2_TAIL_MIN_STAGES = 64;  // stages per tile below which tails are not split
+constexpr int P2_TAIL_MIN_STAGES = 32;  // stages per tile below which tails are not split
 // Tile t of the pair kernel's walk -> (row pair, column block): groups of g
 // row pairs (the last one shorter), row pairs fastest inside a group.
 __device__ __forceinline__ void p2_tile(long long t, int mpairs, int ntn, int g, int* mp, int* nb) {
@@ -915,8 +915,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
   if (p.tail_ws && ntiles > 0) {
     const long long full = ntiles / ncl;
     const int rem = (int)(ntiles - full * ncl);
-    // measured on GB300: two-way splits and short K (one 4096-deep tile)
-    // lost more to the partial tiles' round trip than the shorter tail gained
+    // measured on GB300: two- and three-way splits lost more to the partial
+    // tiles' round trip than the shorter tail gained
     const int S = rem > 0 ? min(ncl / rem, P2_TAIL_MAX_SPLIT) : 1;
     if (S >= P2_TAIL_MIN_SPLIT && nk >= P2_TAIL_MIN_STAGES) {
       full_tiles = full * ncl;
@@ -1197,37 +1197,43 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
           const int n4 = bn / 4;
           const int c4a = (int)((long long)tail_s * n4 / tail_S), c4b = (int)((long long)(tail_s + 1) * n4 / tail_S);
           float* dst = Cseg + (size_t)row * p.ldc + n0;
+          // two float4 columns per pass with every split's loads in flight
+          // together (up to P2_TAIL_MAX_SPLIT x 2 independent 16-byte loads)
 #pragma unroll 1
-          for (int c4 = c4a; c4 < c4b; c4 += 4) {
-            float4 acc[4];
+          for (int c4 = c4a; c4 < c4b; c4 += 2) {
+            const bool two = c4 + 1 < c4b;
+            float4 x0[P2_TAIL_MAX_SPLIT], x1[P2_TAIL_MAX_SPLIT];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-            for (int sp = 0; sp < tail_S; ++sp) {
-              const float* w = w0 + sp * wsplit;
-              float4 x[4];
+            for (int sp = 0; sp < P2_TAIL_MAX_SPLIT; ++sp) {
+              if (sp < tail_S) {
+                const float* w = w0 + sp * wsplit + c4 * 4;
+                x0[sp] = *(const float4*)w;
+                x1[sp] = two ? *(const float4*)(w + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+            float4 a0 = x0[0], a1 = x1[0];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) x[u] = c4 + u < c4b ? *(const float4*)(w + (c4 + u) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (sp == 0) {
-                  acc[u] = x[u];
-                } else {
-                  acc[u].x += x[u].x;
-                  acc[u].y += x[u].y;
-                  acc[u].z += x[u].z;
-                  acc[u].w += x[u].w;
-                }
+            for (int sp = 1; sp < P2_TAIL_MAX_SPLIT; ++sp) {
+              if (sp < tail_S) {
+                a0.x += x0[sp].x;
+                a0.y += x0[sp].y;
+                a0.z += x0[sp].z;
+                a0.w += x0[sp].w;
+                a1.x += x1[sp].x;
+                a1.y += x1[sp].y;
+                a1.z += x1[sp].z;
+                a1.w += x1[sp].w;
               }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 2; ++u) {
+              if (u == 1 && !two) continue;
+              const float4 av = u ? a1 : a0;
               const int col = (c4 + u) * 4;
-              if (c4 + u >= c4b) continue;
               if (n0 + col + 4 <= segN && vseg) {
-                *(float4*)(dst + col) = acc[u];
+                *(float4*)(dst + col) = av;
               } else {
-                const float e[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+                const float e[4] = {av.x, av.y, av.z, av.w};
                 for (int j = 0; j < 4; ++j)
                   if (n0 + col + j < segN) dst[col + j] = e[j];
               }

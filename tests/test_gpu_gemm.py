@@ -208,8 +208,8 @@ def test_two_sm_pair_grouped_walk(M, N, K):
 # the pair kernel's split tail: with a device row count, the tiles of the last,
 # partly filled wave are split along K over the idle clusters (each split sums
 # one column slice over all splits' partial tiles, in split order) when at
-# least four splits fit and a tile is at least 64 stages deep (K = 12288 at two
-# k-blocks per stage).  With 76 clusters: 2560 rows leave 8 tail tiles (eight
+# least four splits fit and a tile is at least 32 stages deep (K = 12288 at two
+# k-blocks per stage: 96).  With 76 clusters: 2560 rows leave 8 tail tiles (eight
 # splits each), 256 rows 16 tiles in all (four splits each), 300 and 4096 rows
 # too many for a split.  Live rows must match the definition, rows past the
 # count stay untouched, and repeated launches (the split counters cleared by
